@@ -1,0 +1,12 @@
+"""Gated DeltaNet state recurrence on GB300 (sm_103a).
+
+The compute runs in libgdn.so (hand-written CUDA: a tcgen05/TMA chunked prefill, a
+token-serial CUDA-core prefill and a one-pass decode step) behind the C ABI of
+``include/gdn.h``.  This package is the thin PyTorch binding of that ABI.
+"""
+from ._lib import GdnError, GDN_BF16, GDN_F32, GDN_NORMALIZE_QK  # noqa: F401
+from .api import (check_device_status, gdn_chunk_fwd, gdn_recurrent_step, version,  # noqa: F401
+                  workspace_size)
+
+__all__ = ["gdn_chunk_fwd", "gdn_recurrent_step", "workspace_size", "check_device_status", "version",
+           "GdnError"]

@@ -1,0 +1,166 @@
+"""PyTorch-facing binding of libgdn: argument marshalling only.
+
+Each function checks shapes and dtypes, allocates the outputs (and the scratch
+workspace) with PyTorch, and calls the C ABI entry point of the same name on the
+current (or given) CUDA stream.  Every step of the recurrence runs in libgdn's
+CUDA kernels; there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib as L
+
+_DTYPES = {torch.float32: L.GDN_F32, torch.bfloat16: L.GDN_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(name, t, dtype, device, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def _opts(lib, dtype, scale, chunk, normalize_qk, stream, device, events):
+    o = L.default_opts(lib)
+    o.dtype = _DTYPES[dtype]
+    o.chunk = int(chunk)
+    o.scale = float(scale)
+    o.flags = L.GDN_NORMALIZE_QK if normalize_qk else 0
+    o.stream = _stream_handle(stream, device)
+    keep = None
+    if events:
+        keep = (ctypes.c_void_p * len(events))(*[int(e) for e in events])
+        o.events = ctypes.cast(keep, ctypes.POINTER(ctypes.c_void_p))
+        o.num_events = len(events)
+    return o, keep
+
+
+def workspace_size(B: int, T: int, Hqk: int, Hv: int, dk: int, dv: int, *, dtype=torch.bfloat16,
+                   chunk: int = 64, num_seqs: Optional[int] = None) -> int:
+    """Bytes of device scratch gdn_chunk_fwd needs (0 when the selected kernel needs none)."""
+    lib = L.load()
+    o = L.default_opts(lib)
+    o.dtype = _DTYPES[dtype]
+    o.chunk = int(chunk)
+    if num_seqs is not None:
+        o.cu_seqlens = 16  # any non-null value marks the call as packed for the size query
+        o.num_seqs = int(num_seqs)
+    return int(lib.gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, ctypes.byref(o)))
+
+
+def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                  S0: Optional[torch.Tensor] = None, *, scale: float = 1.0, chunk: int = 64,
+                  normalize_qk: bool = False, cu_seqlens: Optional[torch.Tensor] = None,
+                  out: Optional[torch.Tensor] = None, S_final: Optional[torch.Tensor] = None,
+                  output_final_state: bool = True, workspace: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None, events: Optional[Sequence[int]] = None):
+    """Chunked prefill.  q, k [B, T, Hqk, dk]; v [B, T, Hv, dv]; g, beta [B, T, Hv] (all bf16 or all
+    fp32, on one CUDA device); S0 [nseq, Hv, dk, dv] fp32 or None.  With ``cu_seqlens`` (int32 device
+    tensor of nseq+1 offsets) B must be 1.  Returns (out [B, T, Hv, dv], S_final or None)."""
+    lib = L.load()
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, T, H, d]")
+    B, T, Hqk, dk = q.shape
+    Hv, dv = int(v.shape[2]), int(v.shape[3])
+    dev, dt = q.device, q.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    _need("q", q, dt, dev, (B, T, Hqk, dk))
+    _need("k", k, dt, dev, (B, T, Hqk, dk))
+    _need("v", v, dt, dev, (B, T, Hv, dv))
+    _need("g", g, dt, dev, (B, T, Hv))
+    _need("beta", beta, dt, dev, (B, T, Hv))
+    nseq = B
+    if cu_seqlens is not None:
+        if cu_seqlens.dim() != 1:
+            raise ValueError("cu_seqlens must be 1-D")
+        nseq = int(cu_seqlens.numel()) - 1
+        _need("cu_seqlens", cu_seqlens, torch.int32, dev, (nseq + 1,))
+    if S0 is not None:
+        _need("S0", S0, torch.float32, dev, (nseq, Hv, dk, dv))
+    if out is None:
+        out = torch.empty_like(v)
+    _need("out", out, dt, dev, (B, T, Hv, dv))
+    if S_final is None and output_final_state:
+        S_final = torch.empty((nseq, Hv, dk, dv), dtype=torch.float32, device=dev)
+    if S_final is not None:
+        _need("S_final", S_final, torch.float32, dev, (nseq, Hv, dk, dv))
+    with torch.cuda.device(dev):
+        o, keep = _opts(lib, dt, scale, chunk, normalize_qk, stream, dev, events)
+        if cu_seqlens is not None:
+            o.cu_seqlens = cu_seqlens.data_ptr()
+            o.num_seqs = nseq
+        need = int(lib.gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, ctypes.byref(o)))
+        if need:
+            if workspace is None or workspace.numel() * workspace.element_size() < need:
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+            o.workspace = workspace.data_ptr()
+            o.workspace_bytes = workspace.numel() * workspace.element_size()
+        st = lib.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(out),
+                               _ptr(S_final), B, T, Hqk, Hv, dk, dv, ctypes.byref(o))
+        del keep
+        L.check(lib, st)
+    return out, S_final
+
+
+def gdn_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                       S: torch.Tensor, *, scale: float = 1.0, normalize_qk: bool = False,
+                       out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                       events: Optional[Sequence[int]] = None) -> torch.Tensor:
+    """One decode step.  q, k [N, Hqk, dk]; v [N, Hv, dv]; g, beta [N, Hv]; S [N, Hv, dk, dv] fp32 is
+    updated in place.  Returns out [N, Hv, dv]."""
+    lib = L.load()
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be 3-D [N, H, d]")
+    N, Hqk, dk = q.shape
+    Hv, dv = int(v.shape[1]), int(v.shape[2])
+    dev, dt = q.device, q.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    _need("q", q, dt, dev, (N, Hqk, dk))
+    _need("k", k, dt, dev, (N, Hqk, dk))
+    _need("v", v, dt, dev, (N, Hv, dv))
+    _need("g", g, dt, dev, (N, Hv))
+    _need("beta", beta, dt, dev, (N, Hv))
+    _need("S", S, torch.float32, dev, (N, Hv, dk, dv))
+    if out is None:
+        out = torch.empty_like(v)
+    _need("out", out, dt, dev, (N, Hv, dv))
+    with torch.cuda.device(dev):
+        o, keep = _opts(lib, dt, scale, 64, normalize_qk, stream, dev, events)
+        st = lib.gdn_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), _ptr(out),
+                                    N, Hqk, Hv, dk, dv, ctypes.byref(o))
+        del keep
+        L.check(lib, st)
+    return out
+
+
+def check_device_status(stream: Optional[torch.cuda.Stream] = None, device=None) -> None:
+    """Synchronise and raise GdnError if a kernel reported a bounded wait that ran out."""
+    lib = L.load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        L.check(lib, lib.gdn_check_device_status(_stream_handle(stream, dev)))
+
+
+def version() -> int:
+    return int(L.load().gdn_version())

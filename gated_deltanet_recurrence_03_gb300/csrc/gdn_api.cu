@@ -1,0 +1,244 @@
+// C ABI of libgdn (declared in include/gdn.h): argument validation, kernel selection, device
+// status word, error reporting.  Every check that can fail does so on the host before anything is
+// enqueued.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "gdn_internal.cuh"
+
+#define GDN_VERSION_MAJOR 0
+#define GDN_VERSION_MINOR 3
+#define GDN_VERSION_PATCH 0
+
+namespace gdn {
+namespace {
+
+// Device status word: kernels OR kStatusTimeout into it when a bounded wait runs out.
+__device__ unsigned g_status_word;
+
+thread_local char t_last_error[256] = "";
+
+gdn_status_t fail(gdn_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+gdn_status_t fail(gdn_status_t s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+gdn_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int g_dev_checked[kMaxDevices];    // 0 unknown, 1 sm_103, -1 other
+unsigned* g_dev_status[kMaxDevices];
+
+// Current device must be sm_103; fetch its status word address (per device, once).
+gdn_status_t device_ready(unsigned** status) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_dev_checked[dev] == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major == 10 && minor == 3) {
+            void* p = nullptr;  // the symbol's device address (the host-side name is only a stand-in)
+            e = cudaGetSymbolAddress(&p, g_status_word);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+            g_dev_status[dev] = static_cast<unsigned*>(p);
+            g_dev_checked[dev] = 1;
+        } else {
+            g_dev_checked[dev] = -1;
+        }
+    }
+    if (g_dev_checked[dev] != 1)
+        return fail(GDN_ERR_UNSUPPORTED, "libgdn is built for sm_103a; device %d is not sm_103", dev);
+    *status = g_dev_status[dev];
+    return GDN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+gdn_opts_t resolve(const gdn_opts_t* o) {
+    gdn_opts_t r;
+    gdn_opts_init(&r);
+    if (o) r = *o;
+    if (r.chunk == 0) r.chunk = 64;
+    return r;
+}
+
+gdn_status_t check_common(int Hqk, int Hv, int dk, int dv, const gdn_opts_t& o) {
+    if (Hqk <= 0 || Hv <= 0) return fail(GDN_ERR_INVALID_ARG, "head counts must be positive (Hqk=%d Hv=%d)", Hqk, Hv);
+    if (Hv % Hqk != 0) return fail(GDN_ERR_INVALID_ARG, "Hv (%d) must be a multiple of Hqk (%d)", Hv, Hqk);
+    if (dk <= 0 || dv <= 0) return fail(GDN_ERR_INVALID_ARG, "head dims must be positive");
+    if (o.dtype != GDN_F32 && o.dtype != GDN_BF16) return fail(GDN_ERR_INVALID_ARG, "unknown dtype %d", o.dtype);
+    if (o.flags & ~GDN_NORMALIZE_QK) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", o.flags);
+    if (o.num_events < 0 || (o.num_events > 0 && !o.events)) return fail(GDN_ERR_INVALID_ARG, "bad event list");
+    if (!dim_ok(dk) || !dim_ok(dv)) return fail(GDN_ERR_UNSUPPORTED, "head dims dk=%d dv=%d not in {32,64,128}", dk, dv);
+    return GDN_OK;
+}
+
+void record(const gdn_opts_t& o, int i, cudaStream_t s) {
+    if (o.events && i < o.num_events && o.events[i]) cudaEventRecord(static_cast<cudaEvent_t>(o.events[i]), s);
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+void gdn_opts_init(gdn_opts_t* o) {
+    if (!o) return;
+    std::memset(o, 0, sizeof(*o));
+    o->dtype = GDN_BF16;
+    o->chunk = 64;
+    o->scale = 1.0f;
+}
+
+int gdn_version(void) { return GDN_VERSION_MAJOR * 10000 + GDN_VERSION_MINOR * 100 + GDN_VERSION_PATCH; }
+
+const char* gdn_last_error(void) { return t_last_error; }
+
+const char* gdn_status_string(gdn_status_t s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_INVALID_ARG: return "invalid argument";
+        case GDN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GDN_ERR_CUDA: return "CUDA error";
+        case GDN_ERR_TIMEOUT: return "device-side wait timed out";
+        case GDN_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts) {
+    const gdn_opts_t o = resolve(opts);
+    if (B < 0 || T < 0 || Hqk <= 0 || Hv <= 0 || Hv % Hqk) return 0;
+    if (!tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk)) return 0;
+    const bool packed = o.cu_seqlens != nullptr;
+    const int nseq = packed ? o.num_seqs : B;
+    if (nseq <= 0 || T == 0) return 0;
+    return tc_prefill_workspace_bytes(B, T, Hv, nseq, packed);
+}
+
+gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                           const float* S0, void* out, float* S_final, int B, int T, int Hqk, int Hv, int dk,
+                           int dv, const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_opts_t o = resolve(opts);
+    if (B < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "B=%d T=%d must be >= 0", B, T);
+    gdn_status_t st = check_common(Hqk, Hv, dk, dv, o);
+    if (st != GDN_OK) return st;
+    if (o.chunk != 16 && o.chunk != 32 && o.chunk != 64)
+        return fail(GDN_ERR_UNSUPPORTED, "chunk %d not in {16,32,64}", o.chunk);
+    const bool packed = o.cu_seqlens != nullptr;
+    if (packed && (B != 1 || o.num_seqs < 1))
+        return fail(GDN_ERR_INVALID_ARG, "cu_seqlens needs B == 1 and num_seqs >= 1 (B=%d num_seqs=%d)", B, o.num_seqs);
+    const int nseq = packed ? o.num_seqs : B;
+    const bool have_tokens = (long long)B * T > 0;
+    if (have_tokens && (!q || !k || !v || !g || !beta || !out))
+        return fail(GDN_ERR_INVALID_ARG, "null input/output pointer");
+    const void* ptrs[] = {q, k, v, g, beta, S0, out, S_final, o.cu_seqlens, o.workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+    if (nseq == 0) return GDN_OK;
+
+    unsigned* status = nullptr;
+    st = device_ready(&status);
+    if (st != GDN_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(o.stream);
+    const size_t state_bytes = (size_t)nseq * Hv * dk * dv * sizeof(float);
+
+    if (!have_tokens) {  // no tokens: the final state is the initial state
+        record(o, 0, stream);
+        if (S_final && S_final != S0) {
+            cudaError_t e = S0 ? cudaMemcpyAsync(S_final, S0, state_bytes, cudaMemcpyDeviceToDevice, stream)
+                               : cudaMemsetAsync(S_final, 0, state_bytes, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "state copy");
+        }
+        record(o, 1, stream);
+        return GDN_OK;
+    }
+
+    PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0; a.out = out; a.S_final = S_final;
+    a.B = B; a.T = T; a.Hqk = Hqk; a.Hv = Hv; a.dk = dk; a.dv = dv;
+    a.dtype = o.dtype; a.chunk = o.chunk; a.scale = o.scale; a.flags = o.flags;
+    a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq;
+    a.workspace = o.workspace; a.workspace_bytes = o.workspace_bytes;
+    a.stream = stream; a.status = status;
+
+    cudaError_t e;
+    if (tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk)) {
+        const size_t need = tc_prefill_workspace_bytes(B, T, Hv, nseq, packed);
+        if (!o.workspace || o.workspace_bytes < need)
+            return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                        o.workspace ? o.workspace_bytes : (size_t)0);
+        if ((reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0)
+            return fail(GDN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+        e = launch_tc_prefill(a, o.events, o.num_events);
+    } else {
+        record(o, 0, stream);
+        e = launch_recurrent_prefill(a);
+        record(o, 1, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return GDN_OK;
+}
+
+gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                                float* S, void* out, int N, int Hqk, int Hv, int dk, int dv,
+                                const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_opts_t o = resolve(opts);
+    if (N < 0) return fail(GDN_ERR_INVALID_ARG, "N=%d must be >= 0", N);
+    gdn_status_t st = check_common(Hqk, Hv, dk, dv, o);
+    if (st != GDN_OK) return st;
+    if (N == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !S || !out) return fail(GDN_ERR_INVALID_ARG, "null pointer");
+    const void* ptrs[] = {q, k, v, g, beta, S, out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+    unsigned* status = nullptr;
+    st = device_ready(&status);
+    if (st != GDN_OK) return st;
+    DecodeArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S = S; a.out = out;
+    a.N = N; a.Hqk = Hqk; a.Hv = Hv; a.dk = dk; a.dv = dv;
+    a.dtype = o.dtype; a.scale = o.scale; a.flags = o.flags;
+    a.stream = static_cast<cudaStream_t>(o.stream);
+    record(o, 0, a.stream);
+    cudaError_t e = launch_decode(a);
+    record(o, 1, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return GDN_OK;
+}
+
+gdn_status_t gdn_check_device_status(void* stream) {
+    t_last_error[0] = 0;
+    unsigned* status = nullptr;
+    gdn_status_t st = device_ready(&status);
+    if (st != GDN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned host = 0;
+    cudaError_t e = cudaMemcpyAsync(&host, status, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (host & kStatusTimeout) return fail(GDN_ERR_TIMEOUT, "a device-side wait ran out of time");
+    return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Internal interfaces of libgdn: argument bundles handed from the C ABI layer (gdn_api.cu) to the
+// kernel launchers of the other translation units, and small device helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Device status word bits (set by kernels whose bounded waits ran out).
+enum : unsigned { kStatusTimeout = 1u };
+
+// Bounded spin: every device-side wait gives up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* g;
+    const void* beta;
+    const float* S0;
+    void* out;
+    float* S_final;
+    int B, T, Hqk, Hv, dk, dv;
+    int dtype;
+    int chunk;
+    float scale;
+    unsigned flags;
+    const int32_t* cu_seqlens;  // device, or nullptr
+    int num_seqs;               // sequences (B, or num_seqs when packed)
+    void* workspace;
+    size_t workspace_bytes;
+    cudaStream_t stream;
+    unsigned* status;           // device status word
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* g;
+    const void* beta;
+    float* S;
+    void* out;
+    int N, Hqk, Hv, dk, dv;
+    int dtype;
+    float scale;
+    unsigned flags;
+    cudaStream_t stream;
+};
+
+// Launchers (return the launch error, cudaSuccess if enqueued).
+cudaError_t launch_decode(const DecodeArgs& a);
+cudaError_t launch_recurrent_prefill(const PrefillArgs& a);
+
+// Tensor-core chunked prefill: whether it takes these arguments, its workspace, and its launch.
+bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk);
+size_t tc_prefill_workspace_bytes(int B, int T, int Hv, int num_seqs, bool packed);
+cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_events);
+
+// ---------------------------------------------------------------- device helpers
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Sequence i's token range [t0, t1) in the flattened token index.
+__device__ __forceinline__ void seq_range(const int32_t* cu, int i, int T, long long& t0, long long& t1) {
+    if (cu) {
+        int a = cu[i], b = cu[i + 1];
+        a = a < 0 ? 0 : (a > T ? T : a);
+        b = b < a ? a : (b > T ? T : b);
+        t0 = a;
+        t1 = b;
+    } else {
+        t0 = (long long)i * T;
+        t1 = t0 + T;
+    }
+}
+
+}  // namespace gdn

@@ -1,0 +1,149 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet recurrence library (libgdn.so).
+ *
+ * The operation (per sequence, per value head h, state S: dk x dv, fp32):
+ *
+ *     S_t = a_t S_{t-1} + beta_t k_t (v_t - a_t S_{t-1}^T k_t)^T,   a_t = exp(g_t)
+ *     o_t = scale * S_t^T q_t
+ *
+ * as stated in "Transformer by Hand, ch. 7 -- Gated DeltaNet: the token-by-token
+ * recurrence", section "The formula", and computed step by step (decay, look up
+ * with k, write the difference times beta, read with q) by the delta_rule
+ * listing of section "qwen/deltanet.py" of the same chapter.  Value head h uses
+ * query/key head floor(h / (Hv / Hqk)), the repeat_interleave of the
+ * GatedDeltaNet shell in the same listing.  The chunk-parallel prefill computes
+ * the same result up to rounding ("mathematically equivalent to the token loop",
+ * learn-llm page "linear attention", remark on flash-linear-attention).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is CALLER-OWNED DEVICE memory, contiguous, row-major,
+ *   16-byte aligned.  The library never allocates, frees or retains device
+ *   memory; scratch space is passed in as opts->workspace.
+ * - Calls are asynchronous on opts->stream: a return of GDN_OK means the work was
+ *   validated and enqueued.  Device-side failures (a bounded wait that ran out)
+ *   are read with gdn_check_device_status().
+ * - Argument errors are detected on the host before anything is enqueued; nothing
+ *   is written in that case.
+ * - The values of g (finite, <= 0) and beta (in [0, 1]) are the caller's
+ *   contract; they are not checked.  Kernels never read or write outside the
+ *   buffers described by the sizes, whatever the values (cu_seqlens entries are
+ *   clamped to [0, T]).
+ * - Thread safety: calls on different streams may run concurrently; a workspace
+ *   must not be shared by calls that overlap on the device.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, Hv % Hqk != 0 ... */
+    GDN_ERR_UNSUPPORTED = 2, /* head dims or chunk outside the supported set, wrong GPU */
+    GDN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed (see gdn_last_error) */
+    GDN_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (gdn_check_device_status) */
+    GDN_ERR_WORKSPACE = 5    /* workspace missing or smaller than the size query asked for */
+} gdn_status_t;
+
+typedef enum gdn_dtype {
+    GDN_F32 = 0,  /* q, k, v, g, beta and out are float */
+    GDN_BF16 = 1  /* q, k, v, g, beta and out are bfloat16; the state is always float */
+} gdn_dtype_t;
+
+/* opts->flags */
+#define GDN_NORMALIZE_QK 0x1u /* divide q and k by sqrt(sum x^2 + 1e-6) inside the kernel
+                                 (the l2norm step of delta_rule); off: inputs are used as given */
+
+typedef struct gdn_opts {
+    int dtype;                  /* gdn_dtype_t of q, k, v, g, beta, out.  Default GDN_BF16. */
+    int chunk;                  /* prefill chunk length: 16, 32 or 64.  0 -> 64. */
+    float scale;                /* multiplies every output o_t.  Default 1.0f. */
+    unsigned flags;             /* GDN_NORMALIZE_QK */
+    const int32_t* cu_seqlens;  /* prefill only: DEVICE pointer to num_seqs+1 int32 token offsets
+                                   (0 = cu[0] <= cu[1] <= ... <= cu[num_seqs] = T) of packed
+                                   sequences; requires B == 1.  NULL: B sequences of T tokens. */
+    int num_seqs;               /* number of packed sequences when cu_seqlens != NULL */
+    void* workspace;            /* DEVICE scratch of >= gdn_chunk_fwd_workspace_size() bytes,
+                                   256-byte aligned; may be NULL when that size is 0 */
+    size_t workspace_bytes;
+    void* stream;               /* cudaStream_t to enqueue on; NULL = legacy default stream */
+    void** events;              /* optional cudaEvent_t[num_events]: events[0] is recorded before
+                                   the first kernel of the call and events[i] after kernel i
+                                   (kernel-level timing); NULL = none */
+    int num_events;
+} gdn_opts_t;
+
+/* Fill *opts with the defaults listed above. */
+void gdn_opts_init(gdn_opts_t* opts);
+
+/*
+ * gdn_chunk_fwd -- chunked prefill over whole sequences.
+ *
+ *   q, k     [B, T, Hqk, dk]  dtype          query / key (unit length unless GDN_NORMALIZE_QK)
+ *   v        [B, T, Hv, dv]   dtype
+ *   g        [B, T, Hv]       dtype          log decay, a_t = exp(g_t)
+ *   beta     [B, T, Hv]       dtype          write strength
+ *   S0       [nseq, Hv, dk, dv] float or NULL (zero state); nseq = B, or num_seqs when packed
+ *   out      [B, T, Hv, dv]   dtype          written for every token (rounded to nearest even)
+ *   S_final  [nseq, Hv, dk, dv] float or NULL (not written); may equal S0 (in-place update)
+ *
+ * Supported: dk, dv in {32, 64, 128}; Hv a multiple of Hqk; B, T >= 0.  T = 0 copies S0 to
+ * S_final (zeros when S0 is NULL).  bf16 inputs with dk = dv = 128 and an even Hv/Hqk run on the
+ * tcgen05 tensor-core path (chunk 64) and need the workspace; everything else runs the token-serial
+ * CUDA-core kernel and needs none.  out must not overlap any input.
+ *
+ * Errors: GDN_ERR_INVALID_ARG for null required pointers, negative sizes, Hv % Hqk != 0,
+ * pointers not 16-byte aligned, cu_seqlens with B != 1 or num_seqs < 1; GDN_ERR_UNSUPPORTED for
+ * head dims or a chunk outside the sets above or a device that is not sm_103; GDN_ERR_WORKSPACE
+ * when the tensor-core path is selected and the workspace is missing or too small;
+ * GDN_ERR_CUDA when a launch fails.
+ */
+gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta, const float* S0, void* out, float* S_final, int B,
+                           int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts);
+
+/* Bytes of device workspace gdn_chunk_fwd needs for these sizes and options (0 if none). */
+size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv,
+                                    const gdn_opts_t* opts);
+
+/*
+ * gdn_recurrent_step -- one decode step: one new token for each of N sequences.
+ *
+ *   q, k   [N, Hqk, dk] dtype;  v [N, Hv, dv] dtype;  g, beta [N, Hv] dtype
+ *   S      [N, Hv, dk, dv] float, read and UPDATED IN PLACE (the state carried between calls,
+ *          as delta_rule takes S in and returns the final S)
+ *   out    [N, Hv, dv] dtype
+ *
+ * One pass over the state: each (sequence, head) table is read once and written once.
+ * Supported: dk, dv in {32, 64, 128}; Hv a multiple of Hqk; N >= 0 (N = 0 is a no-op).
+ * opts->chunk, cu_seqlens and workspace are ignored.  Errors as for gdn_chunk_fwd.
+ */
+gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, const void* g,
+                                const void* beta, float* S, void* out, int N, int Hqk, int Hv,
+                                int dk, int dv, const gdn_opts_t* opts);
+
+/* Synchronise `stream` (cudaStream_t, NULL = legacy), then read and clear the device status word
+ * that kernels set when a bounded wait runs out.  GDN_OK if clear, GDN_ERR_TIMEOUT if set,
+ * GDN_ERR_CUDA if the synchronisation itself failed. */
+gdn_status_t gdn_check_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* gdn_status_string(gdn_status_t status);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char* gdn_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,109 @@
+"""The C ABI library on the host, without a GPU: it loads, exports every entry point that
+include/gdn.h declares, and rejects bad arguments before any CUDA call.
+
+Only argument errors that the library detects before touching the device are exercised
+here; no call in this file reaches a kernel launch.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+pkg_lib = pytest.importorskip("gated_deltanet_recurrence_03_gb300._lib")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_recurrence_03_gb300 import build
+    build.build()
+    return pkg_lib.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "gdn_chunk_fwd" in names and "gdn_recurrent_step" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in gdn.h but not exported"
+    assert set(names) == set(pkg_lib.EXPORTED)
+
+
+def test_opts_defaults_and_strings(lib):
+    o = pkg_lib.default_opts(lib)
+    assert (o.dtype, o.chunk, o.scale, o.flags) == (pkg_lib.GDN_BF16, 64, 1.0, 0)
+    assert not o.cu_seqlens and not o.workspace and not o.stream
+    assert lib.gdn_status_string(0) == b"ok"
+    assert lib.gdn_status_string(pkg_lib.GDN_ERR_TIMEOUT) == b"device-side wait timed out"
+    assert lib.gdn_version() >= 300
+
+
+def opts(lib, **kw):
+    o = pkg_lib.default_opts(lib)
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return ctypes.byref(o)
+
+
+FAKE = 0x10000  # an aligned address that is never dereferenced: every call below fails validation first
+
+
+def prefill(lib, B=1, T=8, Hqk=1, Hv=1, dk=32, dv=32, ptrs=None, **kw):
+    p = [FAKE] * 8 if ptrs is None else ptrs
+    return lib.gdn_chunk_fwd(*p, B, T, Hqk, Hv, dk, dv, opts(lib, **kw))
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(B=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(T=-5), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(Hqk=2, Hv=3), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(Hqk=0), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(dk=48), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(dv=256), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(chunk=128), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(dtype=7), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(flags=0x80), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(ptrs=[FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(ptrs=[FAKE + 8] + [FAKE] * 7), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(B=2, cu_seqlens=FAKE, num_seqs=2), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(cu_seqlens=FAKE, num_seqs=0), pkg_lib.GDN_ERR_INVALID_ARG),
+])
+def test_prefill_argument_errors(lib, case, expect):
+    assert prefill(lib, **case) == expect
+    assert lib.gdn_last_error() != b""
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(N=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(Hqk=3, Hv=4), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(dk=16), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(null=True), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(misaligned=True), pkg_lib.GDN_ERR_INVALID_ARG),
+])
+def test_decode_argument_errors(lib, case, expect):
+    N, Hqk, Hv, dk, dv = case.get("N", 2), case.get("Hqk", 1), case.get("Hv", 2), case.get("dk", 32), 32
+    p = [FAKE] * 7
+    if case.get("null"):
+        p[5] = 0
+    if case.get("misaligned"):
+        p[6] = FAKE + 4
+    assert lib.gdn_recurrent_step(*p, N, Hqk, Hv, dk, dv, opts(lib)) == expect
+
+
+def test_empty_calls_do_nothing(lib):
+    # no sequences and no tokens: nothing to do, nothing touched
+    assert prefill(lib, B=0, T=0, ptrs=[0] * 8) == pkg_lib.GDN_OK
+    assert lib.gdn_recurrent_step(*([0] * 7), 0, 1, 1, 32, 32, opts(lib)) == pkg_lib.GDN_OK
+
+
+def test_workspace_query_is_pure_host(lib):
+    # fp32 and small heads run the token-serial kernel: no workspace
+    assert lib.gdn_chunk_fwd_workspace_size(2, 512, 4, 4, 32, 32, opts(lib, dtype=pkg_lib.GDN_F32)) == 0
+    assert lib.gdn_chunk_fwd_workspace_size(-1, 512, 4, 4, 32, 32, opts(lib)) == 0
