@@ -67,6 +67,8 @@ gdn_status_t device_ready(unsigned** status) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_to(const void* p, unsigned bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; }
+unsigned elem_bytes(int dtype) { return dtype == GDN_BF16 ? 2u : 4u; }
 bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
 gdn_opts_t resolve(const gdn_opts_t* o) {
@@ -150,9 +152,11 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const vo
     const bool have_tokens = (long long)B * T > 0;
     if (have_tokens && (!q || !k || !v || !g || !beta || !out))
         return fail(GDN_ERR_INVALID_ARG, "null input/output pointer");
-    const void* ptrs[] = {q, k, v, g, beta, S0, out, S_final, o.cu_seqlens, o.workspace};
+    const void* ptrs[] = {q, k, v, S0, out, S_final, o.cu_seqlens, o.workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+    if ((g && !aligned_to(g, elem_bytes(o.dtype))) || (beta && !aligned_to(beta, elem_bytes(o.dtype))))
+        return fail(GDN_ERR_INVALID_ARG, "g/beta not aligned to their element size");
     if (nseq == 0) return GDN_OK;
 
     unsigned* status = nullptr;
@@ -208,9 +212,11 @@ gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, con
     if (st != GDN_OK) return st;
     if (N == 0) return GDN_OK;
     if (!q || !k || !v || !g || !beta || !S || !out) return fail(GDN_ERR_INVALID_ARG, "null pointer");
-    const void* ptrs[] = {q, k, v, g, beta, S, out};
+    const void* ptrs[] = {q, k, v, S, out};
     for (const void* p : ptrs)
         if (!aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+    if (!aligned_to(g, elem_bytes(o.dtype)) || !aligned_to(beta, elem_bytes(o.dtype)))
+        return fail(GDN_ERR_INVALID_ARG, "g/beta not aligned to their element size");
     unsigned* status = nullptr;
     st = device_ready(&status);
     if (st != GDN_OK) return st;

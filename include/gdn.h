@@ -17,8 +17,9 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- * - Every tensor pointer is CALLER-OWNED DEVICE memory, contiguous, row-major,
- *   16-byte aligned.  The library never allocates, frees or retains device
+ * - Every tensor pointer is CALLER-OWNED DEVICE memory, contiguous, row-major.
+ *   q, k, v, out and the states are 16-byte aligned; g and beta are aligned to
+ *   their element size.  The library never allocates, frees or retains device
  *   memory; scratch space is passed in as opts->workspace.
  * - Calls are asynchronous on opts->stream: a return of GDN_OK means the work was
  *   validated and enqueued.  Device-side failures (a bounded wait that ran out)

@@ -72,6 +72,7 @@ def prefill(lib, B=1, T=8, Hqk=1, Hv=1, dk=32, dv=32, ptrs=None, **kw):
     (dict(flags=0x80), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(ptrs=[FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(ptrs=[FAKE + 8] + [FAKE] * 7), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(ptrs=[FAKE] * 3 + [FAKE + 1] + [FAKE] * 4), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(B=2, cu_seqlens=FAKE, num_seqs=2), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(cu_seqlens=FAKE, num_seqs=0), pkg_lib.GDN_ERR_INVALID_ARG),
 ])
