@@ -128,7 +128,7 @@ const char* gdn_status_string(gdn_status_t s) {
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts) {
     const gdn_opts_t o = resolve(opts);
     if (B < 0 || T < 0 || Hqk <= 0 || Hv <= 0 || Hv % Hqk) return 0;
-    if (!tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk)) return 0;
+    if (!tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk, o.flags)) return 0;
     const bool packed = o.cu_seqlens != nullptr;
     const int nseq = packed ? o.num_seqs : B;
     if (nseq <= 0 || T == 0) return 0;
@@ -185,7 +185,7 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const vo
     a.stream = stream; a.status = status;
 
     cudaError_t e;
-    if (tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk)) {
+    if (tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk, o.flags)) {
         const size_t need = tc_prefill_workspace_bytes(B, T, Hv, nseq, packed);
         if (!o.workspace || o.workspace_bytes < need)
             return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,

@@ -58,7 +58,7 @@ cudaError_t launch_decode(const DecodeArgs& a);
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a);
 
 // Tensor-core chunked prefill: whether it takes these arguments, its workspace, and its launch.
-bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk);
+bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk, unsigned flags);
 size_t tc_prefill_workspace_bytes(int B, int T, int Hv, int num_seqs, bool packed);
 cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_events);
 

@@ -1,11 +1,653 @@
-// Tensor-core chunked prefill (tcgen05 + TMA + TMEM).  Not enabled yet: every call takes the
-// token-serial kernel.
+// Chunk-parallel prefill on the sm_103a tensor cores (tcgen05.mma kind::f16, bf16 operands, fp32
+// accumulators in TMEM, operands staged in shared memory by TMA / bulk copies).
+//
+// The chunk algebra follows from the update of "Transformer by Hand, ch. 7", section "The formula"
+// (the learn-llm "linear attention" page notes that the chunked implementations are mathematically
+// equivalent to the token loop).  Inside a chunk of C = 64 tokens of one (sequence, value head), with
+// G_r = g_1 + ... + g_r, gamma_r = exp(G_r) and S the state at the chunk start:
+//
+//   A_rs = exp(G_r - G_s) k_r.k_s (s < r),  T = (I + diag(beta) A)^-1          (UT transform)
+//   W    = T diag(beta gamma) K,  Tb = T diag(beta)                              (WY factors)
+//   P_rs = scale exp(G_r - G_s) q_r.k_s (s <= r),  Q' = scale diag(gamma) Q - P W
+//   U    = Tb V - W S                       (the deltas written by the chunk's tokens)
+//   O    = Q' S + (P Tb) V                  (= scale (diag(gamma) Q S + P U))
+//   S   <- gamma_C S + K^T diag(exp(G_C - G)) U
+//
+// Everything that does not depend on S is computed by the parallel kernel gdn_tc_prep over all
+// (chunk, value-head pair) units and packed, per (chunk, head), into one 128 x 192 bf16 operand
+//     A1 = [ -W  | Tb   ]    (rows 0-63:   tokens; the state-update deltas U)
+//          [ Q'  | P Tb ]    (rows 64-127: tokens; the outputs O)
+// so that the sequential kernel gdn_tc_chain needs two MMAs per chunk:
+//     D1 = A1 [S; V]              (M 128, K 128 + 64, N = dv slice)   -> U (rows 0-63), O (rows 64-127)
+//     S  = gamma_C S + K^T (b U)  (M = dk 128, K 64, N = dv slice),  b_r = exp(G_C - G_r)
+// The fp32 state lives in TMEM for the whole sequence; its bf16 copy in shared memory is the B
+// operand of the next D1.  Decay ratios are always exp(G_r - G_s) with s <= r (never 1/gamma).
+// Tokens past the end of a sequence inside its last chunk get beta = g = 0, which makes their rows
+// of U exactly zero, so partial chunks are exact; their outputs are not stored.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "gdn_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
+namespace {
 
-bool tc_prefill_eligible(int, int, int, int, int, int) { return false; }
-size_t tc_prefill_workspace_bytes(int, int, int, int, bool) { return 0; }
-cudaError_t launch_tc_prefill(const PrefillArgs&, void**, int) { return cudaErrorNotSupported; }
+using namespace tc;
+using bf16 = __nv_bfloat16;
+
+constexpr int kC = 64;                      // chunk length
+constexpr int kD = 128;                     // dk = dv
+constexpr uint32_t kA1Bytes = 3u * 128u * 128u;  // 3 panels x 128 rows x 128 B
+constexpr int kVecFloats = 128;             // per (chunk, head): b_r (64), gamma_C at [64]
+constexpr int kThreads = 128;
+constexpr int kSlices = 2;                  // dv slices of 64 columns per head in the chain kernel
+
+// Sequences are laid out in "slots": chunk c of sequence i lives in slot floor(start_i / C) + i + c.
+// This needs no prefix sum over the sequence lengths and stays below ceil(T_total / C) + nseq.
+__device__ bool slot_lookup(const int32_t* cu, int nseq, int T_len, int slot, int& seq, long long& t0, int& n) {
+    int lo = 0, hi = nseq - 1, best = -1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        long long a, b;
+        seq_range(cu, mid, T_len, a, b);
+        if (a / kC + mid <= slot) {
+            best = mid;
+            lo = mid + 1;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    if (best < 0) return false;
+    long long a, b;
+    seq_range(cu, best, T_len, a, b);
+    const long long c = slot - (a / kC + best);
+    if (c >= (b - a + kC - 1) / kC) return false;
+    seq = best;
+    t0 = a + c * kC;
+    n = (int)min((long long)kC, b - t0);
+    return true;
+}
+
+// ------------------------------------------------------------------ parallel intra-chunk kernel
+// Shared memory (byte offsets from a 1024-aligned base)
+constexpr uint32_t P_KQ = 0;            // 2 panels (dk 0-63, 64-127) x [K rows 0-63 | Q rows 64-127]
+constexpr uint32_t P_AP = 32768;        // blockdiag(P_0, P_1): 2 panels x 128 rows (K-major A)
+constexpr uint32_t P_TOP = 65536;       // [-W_h | Tb_h] for both heads: 3 panels x 128 rows
+constexpr uint32_t P_L = 114688;        // L_h = diag(beta) A, fp32 [2][64][68]
+constexpr uint32_t P_LSTRIDE = 68;
+constexpr uint32_t P_TD = 148480;       // [T_0 diag(beta gamma); T_1 diag(beta gamma)] 1 panel x 128 rows
+constexpr uint32_t P_BOT = P_L;         // [Q'_h | P_h Tb_h]: 2 heads x 3 panels x 64 rows (after L, TD die)
+constexpr uint32_t P_SMALL = 164864;    // G[2][64], beta[2][64], beta*gamma[2][64]
+constexpr uint32_t P_BAR = P_SMALL + 3 * 2 * 64 * 4;
+constexpr uint32_t P_SMEM = P_BAR + 64 + 1024;  // + alignment slack
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const bf16* __restrict__ g, const bf16* __restrict__ beta, const int32_t* __restrict__ cu,
+               int nseq, int T_len, int Hqk, int Hv, float scale, uint8_t* __restrict__ ws_a1,
+               float* __restrict__ ws_vec, unsigned* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    float* sG = reinterpret_cast<float*>(sm + P_SMALL);   // [2][64]
+    float* sBeta = sG + 128;                              // [2][64]
+    float* sBG = sG + 256;                                // [2][64] beta_r * gamma_r
+    float* sL = reinterpret_cast<float*>(sm + P_L);
+    const uint32_t bar_tma = sb + P_BAR, bar_mma = sb + P_BAR + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P_BAR + 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + P_BAR + 20);
+
+    const int slot = blockIdx.x, pair = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    int seq;
+    long long t0;
+    int n;
+    if (!slot_lookup(cu, nseq, T_len, slot, seq, t0, n)) return;  // unused slot (uniform per CTA)
+    const int h0 = 2 * pair;
+    const int hk = h0 / (Hv / Hqk);
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's TMEM lane quarter
+
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_tma, 4 * 8192);
+        for (int p = 0; p < 2; ++p) {
+            tma_load_3d(sb + P_KQ + p * 16384, &tm_k, 64 * p, hk, (int)t0, bar_tma);
+            tma_load_3d(sb + P_KQ + p * 16384 + 8192, &tm_q, 64 * p, hk, (int)t0, bar_tma);
+        }
+    }
+    {   // gates of the two value heads; padded tokens get g = beta = 0
+        const int hh = tid >> 6, r = tid & 63;
+        float gv = 0.f, bv = 0.f;
+        if (r < n) {
+            gv = __bfloat162float(g[(size_t)(t0 + r) * Hv + h0 + hh]);
+            bv = __bfloat162float(beta[(size_t)(t0 + r) * Hv + h0 + hh]);
+        }
+        sG[hh * 64 + r] = gv;
+        sBeta[hh * 64 + r] = bv;
+    }
+    __syncthreads();
+    if ((tid & 63) == 0) {   // inclusive cumulative sum of g, one thread per head
+        float acc = 0.f;
+        float* Gh = sG + (tid >> 6) * 64;
+        for (int r = 0; r < 64; ++r) {
+            acc += Gh[r];
+            Gh[r] = acc;
+        }
+    }
+    __syncthreads();
+    {
+        const int hh = tid >> 6, r = tid & 63;
+        const float Gr = sG[hh * 64 + r], Gl = sG[hh * 64 + 63];
+        sBG[hh * 64 + r] = sBeta[hh * 64 + r] * __expf(Gr);
+        float* vec = ws_vec + ((size_t)slot * Hv + h0 + hh) * kVecFloats;
+        vec[r] = __expf(Gl - Gr);
+        if (r == 0) vec[64] = __expf(Gl);
+    }
+
+    // ---- [K; Q] K^T : rows 0-63 K K^T, rows 64-127 Q K^T  (TMEM columns 0-63)
+    mbar_wait_bounded(bar_tma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+    if (tid == 0) {
+        tc_fence_after();
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = P_KQ + (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_bf16(tmem, smem_desc(sb + off, 16, 1024), smem_desc(sb + off, 16, 1024), idesc_bf16(128, 64, 0, 0),
+                     ks > 0);
+        }
+        mma_commit(bar_mma);
+    }
+    __syncthreads();
+    mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+    tc_fence_after();
+    {
+        uint32_t a[32], b[32];
+        tmem_ld32(tl, a);
+        tmem_ld32(tl + 32, b);
+        tmem_wait_ld();
+        if (warp < 2) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s, s < r
+            const int r = tid;
+            for (int hh = 0; hh < 2; ++hh) {
+                const float* Gh = sG + hh * 64;
+                const float br = (r < n) ? sBeta[hh * 64 + r] : 0.f, Gr = Gh[r];
+                float* Lrow = sL + (hh * 64 + r) * P_LSTRIDE;
+#pragma unroll
+                for (int s4 = 0; s4 < 16; ++s4) {
+                    float4 o;
+                    float* op = &o.x;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s = 4 * s4 + e;
+                        const float kk = __uint_as_float(s < 32 ? a[s] : b[s - 32]);
+                        op[e] = (s < r) ? br * __expf(Gr - Gh[s]) * kk : 0.f;
+                    }
+                    reinterpret_cast<float4*>(Lrow)[s4] = o;
+                }
+            }
+        } else {          // row r of Q K^T -> P_h[r][s] = scale exp(G_r - G_s) q_r.k_s, s <= r (bf16, A operand)
+            const int r = tid - 64;
+            for (int hh = 0; hh < 2; ++hh) {
+                const float* Gh = sG + hh * 64;
+                const float Gr = Gh[r];
+                const uint32_t row = 64 * hh + r;
+                uint8_t* pan = sm + P_AP + hh * 16384;
+                uint8_t* zpan = sm + P_AP + (1 - hh) * 16384;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float pv[2];
+#pragma unroll
+                        for (int f = 0; f < 2; ++f) {
+                            const int s = 8 * c + 2 * e + f;
+                            const float qk = __uint_as_float(s < 32 ? a[s] : b[s - 32]);
+                            pv[f] = (s <= r) ? scale * __expf(Gr - Gh[s]) * qk : 0.f;
+                        }
+                        w[e] = pack_bf16(pv[0], pv[1]);
+                    }
+                    *reinterpret_cast<uint4*>(pan + swz(row, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(zpan + swz(row, c)) = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- T = (I + L)^-1 by forward substitution, one column per thread (thread = head, column j)
+    {
+        const int hh = tid >> 6, j = tid & 63;
+        const float* L = sL + hh * 64 * P_LSTRIDE;
+        float t[64];
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+            const float4* Lr = reinterpret_cast<const float4*>(L + r * P_LSTRIDE);
+#pragma unroll
+            for (int s4 = 0; s4 < r / 4; ++s4) {
+                const float4 l = Lr[s4];
+                acc0 = fmaf(l.x, t[4 * s4 + 0], acc0);
+                acc1 = fmaf(l.y, t[4 * s4 + 1], acc1);
+                acc2 = fmaf(l.z, t[4 * s4 + 2], acc2);
+                acc3 = fmaf(l.w, t[4 * s4 + 3], acc3);
+            }
+#pragma unroll
+            for (int s = (r / 4) * 4; s < r; ++s) acc0 = fmaf(L[r * P_LSTRIDE + s], t[s], acc0);
+            const float sum = (acc0 + acc1) + (acc2 + acc3);
+            t[r] = (r < j) ? 0.f : (r == j ? 1.f : -sum);
+        }
+        // column j of T_h diag(beta gamma) -> TD (rows 64 hh + r), of T_h diag(beta) -> TOP panel 2
+        const float dj = sBG[hh * 64 + j], bj = sBeta[hh * 64 + j];
+        uint8_t* td = sm + P_TD;
+        uint8_t* tb = sm + P_TOP + 2 * 16384;
+        const uint32_t cj = (uint32_t)j >> 3, ej = ((uint32_t)j & 7u) * 2u;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+            const uint32_t row = 64 * hh + r;
+            *reinterpret_cast<bf16*>(td + swz(row, cj) + ej) = __float2bfloat16_rn(t[r] * dj);
+            *reinterpret_cast<bf16*>(tb + swz(row, cj) + ej) = __float2bfloat16_rn(t[r] * bj);
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- [W_0; W_1] = [T_0 D_0; T_1 D_1] K   (TMEM columns 64-191)
+    if (tid == 0) {
+        tc_fence_after();
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + 64, smem_desc(sb + P_TD + ks * 32, 16, 1024),
+                     smem_desc(sb + P_KQ + ks * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1), ks > 0);
+        mma_commit(bar_mma);
+    }
+    mbar_wait_bounded(bar_mma, 1, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+    tc_fence_after();
+    for (int cb = 0; cb < 4; ++cb) {   // row R = tid of [W_0; W_1] -> -W in TOP panels 0-1
+        uint32_t a[32];
+        tmem_ld32(tl + 64 + 32 * cb, a);
+        tmem_wait_ld();
+        uint8_t* pan = sm + P_TOP + (cb >> 1) * 16384;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16(-__uint_as_float(a[8 * c + 2 * e]), -__uint_as_float(a[8 * c + 2 * e + 1]));
+            *reinterpret_cast<uint4*>(pan + swz(tid, (cb & 1) * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- blockdiag(P_0, P_1) [-W | Tb]  (TMEM columns 0-191): -P W and P Tb for both heads
+    if (tid == 0) {
+        tc_fence_after();
+        for (int ks = 0; ks < 8; ++ks)
+            mma_bf16(tmem, smem_desc(sb + P_AP + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                     smem_desc(sb + P_TOP + ks * 2048, 16384, 1024), idesc_bf16(128, 192, 0, 1), ks > 0);
+        mma_commit(bar_mma);
+    }
+    mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+    tc_fence_after();
+    {
+        const int hh = tid >> 6, r = tid & 63;
+        const float qs = scale * __expf(sG[hh * 64 + r]);   // scale * gamma_r
+        uint8_t* bot = sm + P_BOT + hh * 24576;
+        for (int cb = 0; cb < 6; ++cb) {
+            uint32_t a[32];
+            tmem_ld32(tl + 32 * cb, a);
+            tmem_wait_ld();
+            uint8_t* pan = bot + (cb >> 1) * 8192;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t chunk = (cb & 1) * 4 + c;
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(a[8 * c + e]);
+                if (cb < 4) {   // Q' = scale gamma_r q_r - P W   (q from the Q rows of the KQ panels)
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + P_KQ + (cb >> 1) * 16384 + swz(64 + r, chunk));
+                    const bf16* qe = reinterpret_cast<const bf16*>(&qv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = fmaf(qs, __bfloat162float(qe[e]), x[e]);
+                }
+                *reinterpret_cast<uint4*>(pan + swz(r, chunk)) =
+                    make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {   // A1 of each head: panel p = [TOP rows of the head | BOT rows of the head]
+        for (int hh = 0; hh < 2; ++hh) {
+            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + h0 + hh) * kA1Bytes;
+            for (int p = 0; p < 3; ++p) {
+                bulk_s2g(dst + p * 16384, sb + P_TOP + p * 16384 + hh * 8192, 8192);
+                bulk_s2g(dst + p * 16384 + 8192, sb + P_BOT + hh * 24576 + p * 8192, 8192);
+            }
+        }
+        bulk_commit();
+        bulk_wait_all();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ------------------------------------------------------------------ sequential chain kernel
+constexpr uint32_t C_A1 = 0;            // 2 stages x 48 KB
+constexpr uint32_t C_KT = 98304;        // 2 stages x 16 KB (K tile: 2 panels x 64 token rows)
+constexpr uint32_t C_VT = 131072;       // 2 stages x 8 KB  (V slice: 1 panel x 64 token rows)
+constexpr uint32_t C_SB = 147456;       // bf16 state slice: 1 panel x 128 dk rows
+constexpr uint32_t C_UB = 163840;       // bf16 b*U: 1 panel x 64 token rows
+constexpr uint32_t C_VEC = 172032;      // 2 stages x 512 B
+constexpr uint32_t C_BAR = 173056;
+constexpr uint32_t C_SMEM = C_BAR + 64 + 1024;
+constexpr uint32_t kStageBytes = kA1Bytes + 16384 + 8192 + kVecFloats * 4;
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const uint8_t* __restrict__ ws_a1, const float* __restrict__ ws_vec, const float* __restrict__ S0,
+                bf16* __restrict__ out, float* __restrict__ S_final, const int32_t* __restrict__ cu, int nseq,
+                int T_len, int Hqk, int Hv, int num_slots, unsigned* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    const uint32_t bar_load0 = sb + C_BAR, bar_mma1 = sb + C_BAR + 16, bar_mma2 = sb + C_BAR + 24;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_BAR + 32);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C_BAR + 36);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int z = blockIdx.x % kSlices;
+    const int h = (blockIdx.x / kSlices) % Hv;
+    const int i = blockIdx.x / (kSlices * Hv);
+    const int hk = h / (Hv / Hqk);
+    long long s0, s1;
+    seq_range(cu, i, T_len, s0, s1);
+    const long long base = s0 / kC + i;
+    long long nch = (s1 - s0 + kC - 1) / kC;
+    if (base + nch > num_slots) nch = max(0LL, num_slots - base);   // only for malformed offsets
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 128);
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(bar_load0, 1);
+        mbar_init(bar_load0 + 8, 1);
+        mbar_init(bar_mma1, 1);
+        mbar_init(bar_mma2, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;            // state S: columns 0-63; D1: columns 64-127
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    const size_t srow = (((size_t)i * Hv + h) * kD + tid) * kD + 64 * z;   // this thread's state row slice
+    const int R = tid;
+
+    auto issue_loads = [&](long long c, int st) {
+        const long long slot = base + c;
+        const int tc0 = (int)(s0 + c * kC);
+        const uint32_t bar = bar_load0 + 8 * st;
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        bulk_g2s(sb + C_A1 + st * kA1Bytes, ws_a1 + ((size_t)slot * Hv + h) * kA1Bytes, kA1Bytes, bar);
+        tma_load_3d(sb + C_KT + st * 16384, &tm_k, 0, hk, tc0, bar);
+        tma_load_3d(sb + C_KT + st * 16384 + 8192, &tm_k, 64, hk, tc0, bar);
+        tma_load_3d(sb + C_VT + st * 8192, &tm_v, 64 * z, h, tc0, bar);
+        bulk_g2s(sb + C_VEC + st * 512, ws_vec + ((size_t)slot * Hv + h) * kVecFloats, kVecFloats * 4, bar);
+    };
+
+    if (nch == 0) {   // empty sequence: the final state is the initial state
+        if (S_final) {
+            for (int e = 0; e < 64; e += 4) {
+                const float4 v = S0 ? *reinterpret_cast<const float4*>(S0 + srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(S_final + srow + e) = v;
+            }
+        }
+    } else {
+        if (tid == 0) {
+            issue_loads(0, 0);
+            if (nch > 1) issue_loads(1, 1);
+        }
+        // prologue: bf16 copy of S0 into SB, gamma_C(0) * S0 into TMEM
+        mbar_wait_bounded(bar_load0, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+        const float g0 = reinterpret_cast<const float*>(sm + C_VEC)[64];
+        for (int hb = 0; hb < 2; ++hb) {
+            uint32_t v[32];
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 x = S0 ? *reinterpret_cast<const float4*>(S0 + srow + 32 * hb + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[e] = __float_as_uint(x.x); v[e + 1] = __float_as_uint(x.y);
+                v[e + 2] = __float_as_uint(x.z); v[e + 3] = __float_as_uint(x.w);
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float* f = reinterpret_cast<const float*>(v + 8 * c);
+                *reinterpret_cast<uint4*>(sm + C_SB + swz(R, 4 * hb + c)) =
+                    make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(g0 * __uint_as_float(v[e]));
+            tmem_st32(tl + 32 * hb, v);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        for (long long c = 0; c < nch; ++c) {
+            const int st = (int)(c & 1);
+            const uint32_t lpar = (uint32_t)((c >> 1) & 1), par = (uint32_t)(c & 1);
+            const long long tc0 = s0 + c * kC;
+            const int n = (int)min((long long)kC, s1 - tc0);
+            const uint32_t a1 = sb + C_A1 + st * kA1Bytes;
+            if (tid == 0) {   // D1 = A1 [S; V]
+                mbar_wait_bounded(bar_load0 + 8 * st, lpar, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+                tc_fence_after();
+                for (int ks = 0; ks < 12; ++ks) {
+                    const uint64_t ad = smem_desc(a1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+                    // single-panel MN-major B: the panel-to-panel offset is never used, so LBO = SBO
+                    const uint64_t bd = ks < 8 ? smem_desc(sb + C_SB + ks * 2048, 1024, 1024)
+                                               : smem_desc(sb + C_VT + st * 8192 + (ks - 8) * 2048, 1024, 1024);
+                    mma_bf16(tmem + 64, ad, bd, idesc_bf16(128, 64, 0, 1), ks > 0);
+                }
+                mma_commit(bar_mma1);
+            }
+            mbar_wait_bounded(bar_load0 + 8 * st, lpar, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+            mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+            tc_fence_after();
+            {
+                uint32_t a[32], b[32];
+                tmem_ld32(tl + 64, a);
+                tmem_ld32(tl + 96, b);
+                tmem_wait_ld();
+                if (warp < 2) {   // U row r = R scaled by b_r = exp(G_C - G_r) -> B operand of the state update
+                    const float br = reinterpret_cast<const float*>(sm + C_VEC + st * 512)[R];
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        const uint32_t* src = c8 < 4 ? a + 8 * c8 : b + 8 * (c8 - 4);
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = br * __uint_as_float(src[e]);
+                        *reinterpret_cast<uint4*>(sm + C_UB + swz(R, c8)) =
+                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    }
+                } else {          // output row of token R - 64
+                    const int r = R - 64;
+                    if (r < n) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z);
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) {
+                            const uint32_t* src = c8 < 4 ? a + 8 * c8 : b + 8 * (c8 - 4);
+                            dst[c8] = make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                                 pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                                 pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                                                 pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {   // S (gamma_C-scaled, in TMEM) += K^T (b U)
+                tc_fence_after();
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem, smem_desc(sb + C_KT + st * 16384 + ks * 2048, 8192, 1024),
+                             smem_desc(sb + C_UB + ks * 2048, 1024, 1024), idesc_bf16(128, 64, 1, 1), 1);
+                mma_commit(bar_mma2);
+            }
+            mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+            tc_fence_after();
+            if (tid == 0 && c + 2 < nch) issue_loads(c + 2, st);   // this stage's operands are consumed
+            const bool last = (c + 1 == nch);
+            float gnext = 1.f;
+            if (!last) {
+                mbar_wait_bounded(bar_load0 + 8 * (st ^ 1), (uint32_t)(((c + 1) >> 1) & 1), abort_flag, status,
+                                  kStatusTimeout, kWaitLimitNs);
+                gnext = reinterpret_cast<const float*>(sm + C_VEC + (st ^ 1) * 512)[64];
+            }
+            for (int hb = 0; hb < 2; ++hb) {   // new state row R: bf16 copy for the next D1, gamma-scaled in TMEM
+                uint32_t v[32];
+                tmem_ld32(tl + 32 * hb, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const float* f = reinterpret_cast<const float*>(v + 8 * c4);
+                    *reinterpret_cast<uint4*>(sm + C_SB + swz(R, 4 * hb + c4)) =
+                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                }
+                if (last) {
+                    if (S_final) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(S_final + srow + 32 * hb + e) =
+                                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                            __uint_as_float(v[e + 3]));
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(gnext * __uint_as_float(v[e]));
+                    tmem_st32(tl + 32 * hb, v);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// [tokens, heads, 128] bf16 tensor, box of 64 tokens x 1 head x 64 features, 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* m, const void* base, long long tokens, int heads) {
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
+    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+long long total_tokens(int B, int T, bool packed) { return packed ? (long long)T : (long long)B * T; }
+long long num_slots(long long ttot, int nseq) { return (ttot + kC - 1) / kC + nseq; }
+
+void record_event(void** events, int num_events, int idx, cudaStream_t s) {
+    if (events && idx < num_events && events[idx]) cudaEventRecord(static_cast<cudaEvent_t>(events[idx]), s);
+}
+
+}  // namespace
+
+bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk, unsigned flags) {
+    return dtype == GDN_BF16 && dk == kD && dv == kD && chunk == kC && (Hv / Hqk) % 2 == 0 &&
+           !(flags & GDN_NORMALIZE_QK);
+}
+
+size_t tc_prefill_workspace_bytes(int B, int T, int Hv, int num_seqs, bool packed) {
+    const long long slots = num_slots(total_tokens(B, T, packed), num_seqs);
+    const size_t a1 = (size_t)slots * Hv * kA1Bytes;
+    const size_t vec = (size_t)slots * Hv * kVecFloats * sizeof(float);
+    return a1 + vec;
+}
+
+cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_events) {
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    const bool packed = a.cu_seqlens != nullptr;
+    const long long ttot = total_tokens(a.B, a.T, packed);
+    const long long slots = num_slots(ttot, a.num_seqs);
+    if (ttot > INT32_MAX || slots > INT32_MAX) return cudaErrorInvalidValue;
+    CUtensorMap tq, tk, tv;
+    if ((e = make_map(&tq, a.q, ttot, a.Hqk)) != cudaSuccess) return e;
+    if ((e = make_map(&tk, a.k, ttot, a.Hqk)) != cudaSuccess) return e;
+    if ((e = make_map(&tv, a.v, ttot, a.Hv)) != cudaSuccess) return e;
+    uint8_t* ws_a1 = static_cast<uint8_t*>(a.workspace);
+    float* ws_vec = reinterpret_cast<float*>(ws_a1 + (size_t)slots * a.Hv * kA1Bytes);
+    const int T_len = a.T;
+
+    record_event(events, num_events, 0, a.stream);
+    tc_prep_kernel<<<dim3((unsigned)slots, (unsigned)(a.Hv / 2)), kThreads, P_SMEM, a.stream>>>(
+        tq, tk, static_cast<const bf16*>(a.g), static_cast<const bf16*>(a.beta), a.cu_seqlens, a.num_seqs, T_len,
+        a.Hqk, a.Hv, a.scale, ws_a1, ws_vec, a.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    record_event(events, num_events, 1, a.stream);
+    tc_chain_kernel<<<(unsigned)((long long)a.num_seqs * a.Hv * kSlices), kThreads, C_SMEM, a.stream>>>(
+        tk, tv, ws_a1, ws_vec, a.S0, static_cast<bf16*>(a.out), a.S_final, a.cu_seqlens, a.num_seqs, T_len, a.Hqk,
+        a.Hv, (int)slots, a.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    record_event(events, num_events, 2, a.stream);
+    return cudaSuccess;
+}
 
 }  // namespace gdn
