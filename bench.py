@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of the Gated DeltaNet recurrence on GB300: prefill tokens/s and decode steps/s at
+32 value heads of dimension 128, with the roofline fraction of the dominant kernel.
+
+One timed step = one chunked prefill (gdn_chunk_fwd) of the 8k GQA workload: B=2 sequences of
+T=8192 tokens, 16 query/key heads shared by 32 value heads, dk=dv=128, chunk 64, bf16 inputs,
+fp32 state (random initial state).  The same line carries two more measurements:
+  long_prefill: 4 packed sequences (65536/32768/24576/8192 tokens) with state reset, same heads;
+  decode:       512 consecutive single-token steps for 256 sequences x 32 value heads, with the
+                512 MiB fp32 state resident on the device (captured in one CUDA graph).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+
+N > 1 (launched by torch.distributed.run) runs one independent replica per GPU (the recurrence
+does not shard across GPUs: there is no exchange step); value is the sum over ranks divided by
+the slowest rank's time.  --impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdn_inputs as gi  # noqa: E402
+
+METRIC = "GDN prefill tokens/s & decode steps/s at H=32,d=128; % tensor/HBM roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch from ncu captures (profiles/*.md), valid only for the kernel source they
+# were taken on (sha256 prefix of the file); None once the source has changed.
+NCU_TRAFFIC = {
+    # kernel: (source file, sha256 prefix of that file at capture, bytes per launch of the bench workload)
+}
+
+PREFILL = gi.WORKLOADS["prefill_gqa_8k"]
+LONG = gi.WORKLOADS["prefill_varlen_128k"]
+DECODE = gi.WORKLOADS["decode_256x512"]
+
+
+def rank_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(path):
+    with open(os.path.join(ROOT, path), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel):
+    if kernel not in NCU_TRAFFIC:
+        return None
+    path, sha, nbytes = NCU_TRAFFIC[kernel]
+    return nbytes if source_sha(path) == sha else None
+
+
+# ---------------------------------------------------------------- algorithmic work per launch
+def prefill_flops(tokens, w):
+    """Canonical MMA flops of one chunked prefill, split by kernel (chunk C):
+    prep  : Hqk (K K^T, Q K^T) 4 C dk + Hv (T diag(beta gamma) K) 2 C dk        per token
+    chain : Hv ((T diag(beta)) V + (masked Q K^T) U) 4 C dv + Hv (W S, Q S, K^T U) 6 dk dv   per token
+    (163,840 flop per token and value head at C = 64, d = 128)."""
+    C = w.chunk
+    prep = tokens * (w.Hqk * 4 * C * w.dk + w.Hv * 2 * C * w.dk)
+    chain = tokens * w.Hv * (4 * C * w.dv + 6 * w.dk * w.dv)
+    return prep, chain
+
+
+def prefill_bytes(tokens, nseq, w, e=2):
+    """Algorithmic HBM bytes: q, k, v, g, beta read, out written, S0 read and S_final written."""
+    io = tokens * (2 * w.Hqk * w.dk + 2 * w.Hv * w.dv + 2 * w.Hv) * e
+    state = 2 * nseq * w.Hv * w.dk * w.dv * 4
+    return io + state
+
+
+def decode_bytes(w, e=2):
+    """One decode step: the fp32 state read and written once, plus q, k, v, g, beta, out."""
+    state = 2 * w.B * w.Hv * w.dk * w.dv * 4
+    io = w.B * (2 * w.Hqk * w.dk + 2 * w.Hv * w.dv + 2 * w.Hv) * e
+    return state + io
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed regions run."""
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.active = False
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            if self.active:
+                self.samples.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm = [float(s[0]) for s in self.samples if s and s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if len(s) > 1 and s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if len(s) > 3 + i and s[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def device_inputs_from_generator(torch, dev, w, copies):
+    x = gi.make_prefill_inputs(w)
+    sets = []
+    for _ in range(copies):
+        sets.append({n: torch.from_numpy(np.ascontiguousarray(x[n])).to(dev).to(torch.bfloat16)
+                     for n in ("q", "k", "v", "g", "beta")})
+    S0 = None if x["S0"] is None else torch.from_numpy(x["S0"]).to(dev)
+    return x, sets, S0
+
+
+def device_inputs_random(torch, dev, w, steps=None, seed=1):
+    """Same distributions as the shared generator, drawn on the device (for the large workloads)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    lead = (steps, w.B) if steps else (w.B, w.T)
+    unit = lambda s: torch.nn.functional.normalize(torch.randn(*s, generator=gen, device=dev), dim=-1).bfloat16()
+    q, k = unit((*lead, w.Hqk, w.dk)), unit((*lead, w.Hqk, w.dk))
+    v = torch.randn(*lead, w.Hv, w.dv, generator=gen, device=dev).bfloat16()
+    g = torch.nn.functional.logsigmoid(torch.randn(*lead, w.Hv, generator=gen, device=dev) + 3.0).bfloat16()
+    beta = torch.sigmoid(torch.randn(*lead, w.Hv, generator=gen, device=dev)).bfloat16()
+    return dict(q=q, k=k, v=v, g=g, beta=beta)
+
+
+def run_gpu(args):
+    import torch
+    import gated_deltanet_recurrence_03_gb300 as gdn
+
+    rank, world, local = rank_info()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- headline: chunked prefill of the 8k GQA workload, inputs rotated across 3 copies (> L2 each)
+    w = PREFILL
+    x, sets, S0 = device_inputs_from_generator(torch, dev, w, copies=3)
+    tokens = w.B * w.T
+    out = torch.empty_like(sets[0]["v"])
+    S_final = torch.empty((w.B, w.Hv, w.dk, w.dv), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, gdn.workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv)), dtype=torch.uint8, device=dev)
+    n_ev = 3
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+
+    def prefill_step(i, events=None):
+        s = sets[i % len(sets)]
+        gdn.gdn_chunk_fwd(s["q"], s["k"], s["v"], s["g"], s["beta"], S0, out=out, S_final=S_final, workspace=ws,
+                          chunk=w.chunk, events=None if events is None else [e.cuda_event for e in events])
+
+    for i in range(args.warmup):
+        prefill_step(i)
+    barrier()
+    clocks.active = True
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        prefill_step(i, evs[i])
+    t1.record(stream)
+    barrier()
+    clocks.active = False
+    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    ms_step = ms_total / args.steps
+    k_prep = statistics.mean(r[0].elapsed_time(r[1]) for r in evs)
+    k_chain = statistics.mean(r[1].elapsed_time(r[2]) for r in evs)
+    gdn.check_device_status()
+    f_prep, f_chain = prefill_flops(tokens, w)
+    kernels = {"gdn_tc_prep": {"ms": k_prep, "tflops": f_prep / (k_prep * 1e9), "flop": f_prep},
+               "gdn_tc_chain": {"ms": k_chain, "tflops": f_chain / (k_chain * 1e9), "flop": f_chain}}
+    dominant = max(kernels, key=lambda kname: kernels[kname]["ms"])
+    peak_tf = peaks["bf16_tflops"]
+    dom = kernels[dominant]
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(dom["tflops"], 2), "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": round(dom["tflops"] / peak_tf, 4), "traffic": traffic_for(dominant),
+                "peak_source": f"{peak_src} burst bf16"}
+    whole = (f_prep + f_chain) / (ms_step * 1e9)
+
+    # ---- e2e through the public API with host buffers (pinned), copies inside the timed region
+    host = {n: torch.from_numpy(np.ascontiguousarray(x[n])).to(torch.bfloat16).pin_memory()
+            for n in ("q", "k", "v", "g", "beta")}
+    host_S0 = torch.from_numpy(x["S0"]).pin_memory()
+    host_out = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    host_Sf = torch.empty(S_final.shape, dtype=torch.float32).pin_memory()
+    dbuf = {n: torch.empty_like(sets[0][n]) for n in host}
+    dS0 = torch.empty_like(S0)
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_S0.numel() * 4
+    d2h = host_out.numel() * 2 + host_Sf.numel() * 4
+
+    def e2e_step():
+        for n in host:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        dS0.copy_(host_S0, non_blocking=True)
+        gdn.gdn_chunk_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], dS0, out=out,
+                          S_final=S_final, workspace=ws, chunk=w.chunk)
+        host_out.copy_(out, non_blocking=True)
+        host_Sf.copy_(S_final, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    t0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    t1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1)) / e2e_steps
+
+    # ---- long-context packed prefill (state reset at each boundary)
+    wl = LONG
+    xl = device_inputs_random(torch, dev, wl)
+    cu = torch.tensor(wl.cu_seqlens, dtype=torch.int32, device=dev)
+    out_l = torch.empty_like(xl["v"])
+    Sf_l = torch.empty((wl.num_seqs, wl.Hv, wl.dk, wl.dv), dtype=torch.float32, device=dev)
+    ws_l = torch.empty(max(1, gdn.workspace_size(1, wl.T, wl.Hqk, wl.Hv, wl.dk, wl.dv, num_seqs=wl.num_seqs)),
+                       dtype=torch.uint8, device=dev)
+    long_steps = max(3, min(10, args.steps))
+    ev_l = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(long_steps)]
+    for row in ev_l:
+        for e in row:
+            e.record(stream)
+
+    def long_step(events=None):
+        gdn.gdn_chunk_fwd(xl["q"], xl["k"], xl["v"], xl["g"], xl["beta"], None, cu_seqlens=cu, out=out_l,
+                          S_final=Sf_l, workspace=ws_l, chunk=wl.chunk,
+                          events=None if events is None else [e.cuda_event for e in events])
+
+    for _ in range(3):
+        long_step()
+    barrier()
+    clocks.active = True
+    t0.record(stream)
+    for i in range(long_steps):
+        long_step(ev_l[i])
+    t1.record(stream)
+    barrier()
+    clocks.active = False
+    long_ms = max_over_ranks(t0.elapsed_time(t1)) / long_steps
+    lp = statistics.mean(r[0].elapsed_time(r[1]) for r in ev_l)
+    lc = statistics.mean(r[1].elapsed_time(r[2]) for r in ev_l)
+    lf_prep, lf_chain = prefill_flops(wl.T, wl)
+    del xl, out_l, ws_l
+
+    # ---- decode: 512 consecutive steps, state resident, one CUDA graph per pass
+    wd = DECODE
+    xd = device_inputs_random(torch, dev, wd, steps=wd.T, seed=2)
+    S = (0.1 * torch.randn(wd.B, wd.Hv, wd.dk, wd.dv, device=dev))
+    outs = torch.empty_like(xd["v"])
+
+    def decode_pass():
+        for t in range(wd.T):
+            gdn.gdn_recurrent_step(xd["q"][t], xd["k"][t], xd["v"][t], xd["g"][t], xd["beta"][t], S, out=outs[t])
+
+    for t in range(3):   # warm-up steps outside the graph
+        gdn.gdn_recurrent_step(xd["q"][t], xd["k"][t], xd["v"][t], xd["g"][t], xd["beta"][t], S, out=outs[t])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            decode_pass()
+    stream.wait_stream(cap)
+    passes = 3
+    graph.replay()   # warm-up pass
+    barrier()
+    clocks.active = True
+    t0.record(stream)
+    for _ in range(passes):
+        graph.replay()
+    t1.record(stream)
+    barrier()
+    clocks.active = False
+    dec_ms = max_over_ranks(t0.elapsed_time(t1)) / (passes * wd.T)
+    gdn.check_device_status()
+    dec_bytes = decode_bytes(wd)
+    dec_gbs = dec_bytes / (dec_ms * 1e6)
+    clocks.stop()
+
+    if rank != 0:
+        return
+    value = world * tokens / (ms_step / 1e3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill_gqa_8k: chunked prefill, B=2 x T=8192 tokens, Hqk=16 shared by Hv=32, "
+                               "dk=dv=128, chunk 64, bf16 operands, fp32 accumulate and state, random S0",
+                   "global_batch": w.B * world, "seq_len": w.T,
+                   "parallelism": f"replicas x{world} (no cross-GPU exchange)",
+                   "l2": "inputs larger than L2 (3 rotating input sets of 275 MB; L2 129 MB), no flush",
+                   "inputs": "shared seeded generator (SplitMix64 + Box-Muller), resident in HBM"},
+        "roofline": roofline,
+        "kernels": {k: {"ms": round(v["ms"], 4), "tflops": round(v["tflops"], 2)} for k, v in kernels.items()},
+        "step_tflops": round(whole, 2),
+        "e2e": {"value": round(world * tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 2 * args.steps,
+        "long_prefill": {"workload": "prefill_varlen_128k: 4 packed sequences 65536/32768/24576/8192, state reset",
+                         "value": round(world * wl.T / (long_ms / 1e3), 1), "unit": "tokens/s",
+                         "ms_per_step": round(long_ms, 4), "steps": long_steps,
+                         "kernels": {"gdn_tc_prep": round(lp, 4), "gdn_tc_chain": round(lc, 4)},
+                         "step_tflops": round((lf_prep + lf_chain) / (long_ms * 1e9), 2),
+                         "roofline": {"bound": "tensor", "achieved": round((lf_prep + lf_chain) / (long_ms * 1e9), 2),
+                                      "peak": peak_tf, "unit": "TFLOP/s",
+                                      "frac": round((lf_prep + lf_chain) / (long_ms * 1e9) / peak_tf, 4)}},
+        "decode": {"workload": "decode_256x512: 256 sequences x 32 V heads (16 QK heads), d=128, 512 steps, "
+                               "fp32 state 512 MiB resident, one CUDA graph per 512-step pass",
+                   "value": round(world / (dec_ms / 1e3), 1), "unit": "steps/s",
+                   "tokens_per_s": round(world * wd.B / (dec_ms / 1e3), 1), "us_per_step": round(dec_ms * 1e3, 2),
+                   "gpu_launches": passes * wd.T,
+                   "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": round(dec_gbs, 1),
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
+                                "traffic": traffic_for("decode_step_kernel"),
+                                "algorithmic_bytes": dec_bytes, "peak_source": f"{peak_src} copy bandwidth"}},
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+_ORACLE_INPUTS = {}
+
+
+def oracle_rate(tokens_per_seq, threads=0):
+    """Time the fp64 oracle on the first `tokens_per_seq` tokens of both sequences of the 8k GQA
+    workload, all 32 value heads.  Returns (workload tokens per second, seconds, cores)."""
+    from oracle import recurrence as orc
+    if tokens_per_seq not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS.clear()
+        _ORACLE_INPUTS[tokens_per_seq] = gi.make_prefill_inputs(gi.scaled(PREFILL, T=tokens_per_seq))
+    w = gi.scaled(PREFILL, T=tokens_per_seq)
+    x = _ORACLE_INPUTS[tokens_per_seq]
+    t = time.perf_counter()
+    orc.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], S0=x["S0"], threads=threads)
+    dt = time.perf_counter() - t
+    return w.B * tokens_per_seq / dt, dt, orc.max_threads() if threads <= 0 else threads
+
+
+def cpu_baseline(budget_s=15.0):
+    rate, dt, cores = oracle_rate(128)                      # calibration
+    n = int(max(128, min(PREFILL.T, rate * budget_s / PREFILL.B)))
+    rate, dt, cores = oracle_rate(n)
+    return {"value": round(rate, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} tokens of both sequences of prefill_gqa_8k, all 32 value heads, fp64 "
+                      f"token loop, {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    rate, dt, cores = oracle_rate(128)
+    per_step_s = max(0.2, 90.0 / max(1, args.steps + args.warmup))
+    n = int(max(64, min(PREFILL.T, rate * per_step_s / PREFILL.B)))
+    for _ in range(args.warmup):
+        oracle_rate(n)
+    times = []
+    for _ in range(args.steps):
+        r, dt, cores = oracle_rate(n)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = PREFILL.B * n / (ms / 1e3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill_gqa_8k: chunked prefill, B=2 x T=8192 tokens, Hqk=16 shared by Hv=32, "
+                               "dk=dv=128, chunk 64, bf16 operands, fp32 accumulate and state, random S0",
+                   "global_batch": PREFILL.B, "seq_len": PREFILL.T, "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: first {n} tokens of both sequences, all 32 value heads, fp64 token loop"},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_profile_case(case):
+    """One warm-up and one measured call of a single kernel family, for ncu captures."""
+    import torch
+    import gated_deltanet_recurrence_03_gb300 as gdn
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if case == "prefill":
+        w = PREFILL
+        x = device_inputs_random(torch, dev, w)
+        S0 = 0.1 * torch.randn(w.B, w.Hv, w.dk, w.dv, device=dev)
+        ws = torch.empty(gdn.workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, workspace=ws)
+    else:
+        w = DECODE
+        x = device_inputs_random(torch, dev, w, steps=2, seed=2)
+        S = 0.1 * torch.randn(w.B, w.Hv, w.dk, w.dv, device=dev)
+        for t in range(2):
+            gdn.gdn_recurrent_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], S)
+    torch.cuda.synchronize()
+    gdn.check_device_status()
+    print(f"profile case {case} done")
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None,
+                    help="run one warm-up and one measured call of one kernel family (for ncu) and exit")
+    args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
