@@ -15,7 +15,8 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_NORMALIZE_QK = 0x1
 
 EXPORTED = ("gdn_opts_init", "gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step",
-            "gdn_check_device_status", "gdn_status_string", "gdn_last_error", "gdn_version")
+            "gdn_check_device_status", "gdn_status_string", "gdn_last_error", "gdn_version",
+            "gdn_chunk_fwd_noalloc")
 
 
 class GdnOpts(ctypes.Structure):
@@ -58,6 +59,8 @@ def load(path: str = LIB_PATH):
     lib.gdn_opts_init.restype = None
     lib.gdn_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, opts_p]
     lib.gdn_chunk_fwd.restype = i
+    lib.gdn_chunk_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, opts_p]
+    lib.gdn_chunk_fwd_noalloc.restype = i
     lib.gdn_chunk_fwd_workspace_size.argtypes = [i, i, i, i, i, i, opts_p]
     lib.gdn_chunk_fwd_workspace_size.restype = ctypes.c_size_t
     lib.gdn_recurrent_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, opts_p]

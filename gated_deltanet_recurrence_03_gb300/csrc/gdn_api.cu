@@ -95,6 +95,9 @@ void record(const gdn_opts_t& o, int i, cudaStream_t s) {
 }
 
 }  // namespace
+
+void set_error_message(const char* msg) { snprintf(t_last_error, sizeof(t_last_error), "%s", msg); }
+
 }  // namespace gdn
 
 using namespace gdn;

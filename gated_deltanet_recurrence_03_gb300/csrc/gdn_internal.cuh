@@ -62,6 +62,9 @@ bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk, 
 size_t tc_prefill_workspace_bytes(int B, int T, int Hv, int num_seqs, bool packed);
 cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_events);
 
+// Set the calling thread's gdn_last_error() message.
+void set_error_message(const char* msg);
+
 // ---------------------------------------------------------------- device helpers
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);

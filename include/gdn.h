@@ -129,6 +129,30 @@ gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, con
                                 const void* beta, float* S, void* out, int N, int Hqk, int Hv,
                                 int dk, int dv, const gdn_opts_t* opts);
 
+/*
+ * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate device memory.
+ * (No counterpart in the pages: it is a service of this library.)
+ *
+ * Same arguments, layouts and results as gdn_chunk_fwd; opts->workspace and workspace_bytes are
+ * ignored.  The scratch the tensor-core path needs comes from a 64 MiB array built into the
+ * library, which every GPU that loads the library holds until the process exits.  Meant for
+ * callers that must not call cudaMalloc/cudaFree at this point (a host framework that owns all
+ * device memory, a fixed memory budget, code that must not synchronise the device).  The call
+ * allocates nothing.
+ *
+ * Limit: problems whose gdn_chunk_fwd_workspace_size() exceeds 64 MiB are rejected with
+ * GDN_ERR_WORKSPACE before anything is launched (for 32 value heads of dim 128 that is about 40
+ * chunks of 64 tokens, ~2.5k tokens, per call).  The first call on each device looks up the
+ * array's device address (a host-side query, no allocation); make that first call before any
+ * stream capture.  All calls on a device share the array, which keeps the previous call's
+ * contents (no part of it needs to start at zero); calls that overlap on the GPU race on it, so
+ * order them.
+ */
+gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                                   const void* beta, const float* S0, void* out, float* S_final,
+                                   int B, int T, int Hqk, int Hv, int dk, int dv,
+                                   const gdn_opts_t* opts);
+
 /* Synchronise `stream` (cudaStream_t, NULL = legacy), then read and clear the device status word
  * that kernels set when a bounded wait runs out.  GDN_OK if clear, GDN_ERR_TIMEOUT if set,
  * GDN_ERR_CUDA if the synchronisation itself failed. */
