@@ -76,15 +76,83 @@ __device__ bool slot_lookup(const int32_t* cu, int nseq, int T_len, int slot, in
 constexpr uint32_t P_KQ = 0;            // 2 panels (dk 0-63, 64-127) x [K rows 0-63 | Q rows 64-127]
 constexpr uint32_t P_AP = 32768;        // blockdiag(P_0, P_1): 2 panels x 128 rows (K-major A)
 constexpr uint32_t P_TOP = 65536;       // [-W_h | Tb_h] for both heads: 3 panels x 128 rows
-constexpr uint32_t P_L = 114688;        // L_h = diag(beta) A, fp32 [2][64][68]
+constexpr uint32_t P_L = 114688;        // L_h = diag(beta) A, fp32 [2][64][68]; overwritten by T_h
 constexpr uint32_t P_LSTRIDE = 68;
-constexpr uint32_t P_TD = 148480;       // [T_0 diag(beta gamma); T_1 diag(beta gamma)] 1 panel x 128 rows
+constexpr uint32_t P_LBYTES = 2 * 64 * P_LSTRIDE * 4;
+constexpr uint32_t P_TD = (P_L + P_LBYTES + 1023) & ~1023u;  // [T_0 diag(beta gamma); T_1 diag(beta gamma)] 1 panel x 128 rows
+constexpr uint32_t P_X = P_TD;          // blocked-solve scratch X [2][16][48] fp32 (before TD is written)
 constexpr uint32_t P_BOT = P_L;         // [Q'_h | P_h Tb_h]: 2 heads x 3 panels x 64 rows (after L, TD die)
-constexpr uint32_t P_SMALL = 164864;    // G[2][64], beta[2][64], beta*gamma[2][64]
+constexpr uint32_t P_SMALL = P_TD + 16384;  // G[2][64], beta[2][64], beta*gamma[2][64]
+static_assert(P_L + P_LBYTES <= P_TD, "L must not overlap TD / X");
+static_assert(P_BOT + 2 * 24576 <= P_SMALL, "BOT must end before the small buffers");
 constexpr uint32_t P_BAR = P_SMALL + 3 * 2 * 64 * 4;
 constexpr uint32_t P_SMEM = P_BAR + 64 + 1024;  // + alignment slack
+constexpr int kPrepThreads = 256;       // 8 warps: warps w and w+4 share TMEM lane quarter w % 4
 
-__global__ void __launch_bounds__(kThreads, 1)
+// In-place inverse of the unit lower-triangular I + L_h (L_h strictly lower, fp32, row stride
+// P_LSTRIDE) for both heads, by 16 x 16 blocks: the diagonal blocks by forward substitution (one
+// column per thread), then block row i from T_ij = -T_ii sum_{j<=k<i} L_ik T_kj.  128 threads per head.
+__device__ __forceinline__ void blocked_unit_lower_inverse(float* sL, float* sX, int tid) {
+    const int h = tid >> 7, t = tid & 127;
+    float* L = sL + h * 64 * P_LSTRIDE;
+    float* X = sX + h * 16 * 48;
+    float tc[16];
+    const int I = t >> 4, j = t & 15;
+    if (t < 64) {   // column j of (I + L_II)^-1
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float* Lr = L + (16 * I + r) * P_LSTRIDE + 16 * I;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int s = 0; s + 1 < r; s += 2) {
+                a0 = fmaf(Lr[s], tc[s], a0);
+                a1 = fmaf(Lr[s + 1], tc[s + 1], a1);
+            }
+            if (r & 1) a0 = fmaf(Lr[r - 1], tc[r - 1], a0);
+            tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -(a0 + a1));
+        }
+    }
+    __syncthreads();
+    if (t < 64) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) L[(16 * I + r) * P_LSTRIDE + 16 * I + j] = tc[r];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+        // X_ij = sum_{k=j}^{i-1} L_ik T_kj  (L_ik still original, T_kj final)
+        for (int e = t; e < 256 * i; e += 128) {
+            const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const float* Lr = L + (16 * i + r) * P_LSTRIDE;
+            float a0 = 0.f, a1 = 0.f;
+            for (int k = jb; k < i; ++k) {
+                const float* Tk = L + (16 * k) * P_LSTRIDE + 16 * jb + c;
+#pragma unroll
+                for (int s = 0; s < 16; s += 2) {
+                    a0 = fmaf(Lr[16 * k + s], Tk[s * P_LSTRIDE], a0);
+                    a1 = fmaf(Lr[16 * k + s + 1], Tk[(s + 1) * P_LSTRIDE], a1);
+                }
+            }
+            X[r * 48 + 16 * jb + c] = a0 + a1;
+        }
+        __syncthreads();
+        // T_ij = -T_ii X_ij, written over L_ij
+        for (int e = t; e < 256 * i; e += 128) {
+            const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const float* Ti = L + (16 * i + r) * P_LSTRIDE + 16 * i;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int s = 0; s < 16; s += 2) {
+                a0 = fmaf(Ti[s], X[s * 48 + 16 * jb + c], a0);
+                a1 = fmaf(Ti[s + 1], X[(s + 1) * 48 + 16 * jb + c], a1);
+            }
+            L[(16 * i + r) * P_LSTRIDE + 16 * jb + c] = -(a0 + a1);
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 1)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const bf16* __restrict__ g, const bf16* __restrict__ beta, const int32_t* __restrict__ cu,
                int nseq, int T_len, int Hqk, int Hv, float scale, uint8_t* __restrict__ ws_a1,
@@ -101,7 +169,9 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + P_BAR + 20);
 
     const int slot = blockIdx.x, pair = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;     // TMEM lane quarter, column half
+    const int R = 32 * quarter + lane;                   // TMEM lane = accumulator row of this thread
     int seq;
     long long t0;
     int n;
@@ -122,7 +192,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's TMEM lane quarter
+    const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);   // this warp's TMEM lane quarter
 
     if (tid == 0) {
         mbar_arrive_expect_tx(bar_tma, 4 * 8192);
@@ -131,27 +201,31 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tma_load_3d(sb + P_KQ + p * 16384 + 8192, &tm_q, 64 * p, hk, (int)t0, bar_tma);
         }
     }
-    {   // gates of the two value heads; padded tokens get g = beta = 0
-        const int hh = tid >> 6, r = tid & 63;
-        float gv = 0.f, bv = 0.f;
-        if (r < n) {
-            gv = __bfloat162float(g[(size_t)(t0 + r) * Hv + h0 + hh]);
-            bv = __bfloat162float(beta[(size_t)(t0 + r) * Hv + h0 + hh]);
+    if (warp < 2) {   // gates of value head h0 + warp; padded tokens get g = beta = 0; G = inclusive scan of g
+        const int hh = warp;
+        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+        const int r0 = 2 * lane, r1 = 2 * lane + 1;
+        if (r0 < n) {
+            g0 = __bfloat162float(g[(size_t)(t0 + r0) * Hv + h0 + hh]);
+            b0 = __bfloat162float(beta[(size_t)(t0 + r0) * Hv + h0 + hh]);
         }
-        sG[hh * 64 + r] = gv;
-        sBeta[hh * 64 + r] = bv;
+        if (r1 < n) {
+            g1 = __bfloat162float(g[(size_t)(t0 + r1) * Hv + h0 + hh]);
+            b1 = __bfloat162float(beta[(size_t)(t0 + r1) * Hv + h0 + hh]);
+        }
+        float p = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, p, o);
+            if (lane >= o) p += y;
+        }
+        sG[hh * 64 + r1] = p;
+        sG[hh * 64 + r0] = p - g1;
+        sBeta[hh * 64 + r0] = b0;
+        sBeta[hh * 64 + r1] = b1;
     }
     __syncthreads();
-    if ((tid & 63) == 0) {   // inclusive cumulative sum of g, one thread per head
-        float acc = 0.f;
-        float* Gh = sG + (tid >> 6) * 64;
-        for (int r = 0; r < 64; ++r) {
-            acc += Gh[r];
-            Gh[r] = acc;
-        }
-    }
-    __syncthreads();
-    {
+    if (tid < 128) {
         const int hh = tid >> 6, r = tid & 63;
         const float Gr = sG[hh * 64 + r], Gl = sG[hh * 64 + 63];
         sBG[hh * 64 + r] = sBeta[hh * 64 + r] * __expf(Gr);
@@ -171,35 +245,34 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         mma_commit(bar_mma);
     }
-    __syncthreads();
+    __syncthreads();   // sBG, sG, sBeta visible to all
     mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    {
-        uint32_t a[32], b[32];
-        tmem_ld32(tl, a);
-        tmem_ld32(tl + 32, b);
+    {   // this thread: row R, columns s = 32 half .. 32 half + 31
+        uint32_t a[32];
+        tmem_ld32(tl + 32 * half, a);
         tmem_wait_ld();
-        if (warp < 2) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s, s < r
-            const int r = tid;
+        const int s0 = 32 * half;
+        if (quarter < 2) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s, s < r
+            const int r = R;
             for (int hh = 0; hh < 2; ++hh) {
                 const float* Gh = sG + hh * 64;
-                const float br = (r < n) ? sBeta[hh * 64 + r] : 0.f, Gr = Gh[r];
-                float* Lrow = sL + (hh * 64 + r) * P_LSTRIDE;
+                const float br = sBeta[hh * 64 + r], Gr = Gh[r];
+                float* Lrow = sL + (hh * 64 + r) * P_LSTRIDE + s0;
 #pragma unroll
-                for (int s4 = 0; s4 < 16; ++s4) {
+                for (int s4 = 0; s4 < 8; ++s4) {
                     float4 o;
                     float* op = &o.x;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int s = 4 * s4 + e;
-                        const float kk = __uint_as_float(s < 32 ? a[s] : b[s - 32]);
-                        op[e] = (s < r) ? br * __expf(Gr - Gh[s]) * kk : 0.f;
+                        const int s = s0 + 4 * s4 + e;
+                        op[e] = (s < r) ? br * __expf(Gr - Gh[s]) * __uint_as_float(a[4 * s4 + e]) : 0.f;
                     }
                     reinterpret_cast<float4*>(Lrow)[s4] = o;
                 }
             }
-        } else {          // row r of Q K^T -> P_h[r][s] = scale exp(G_r - G_s) q_r.k_s, s <= r (bf16, A operand)
-            const int r = tid - 64;
+        } else {             // row r of Q K^T -> P_h[r][s] = scale exp(G_r - G_s) q_r.k_s, s <= r
+            const int r = R - 64;
             for (int hh = 0; hh < 2; ++hh) {
                 const float* Gh = sG + hh * 64;
                 const float Gr = Gh[r];
@@ -207,21 +280,20 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 uint8_t* pan = sm + P_AP + hh * 16384;
                 uint8_t* zpan = sm + P_AP + (1 - hh) * 16384;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float pv[2];
 #pragma unroll
                         for (int f = 0; f < 2; ++f) {
-                            const int s = 8 * c + 2 * e + f;
-                            const float qk = __uint_as_float(s < 32 ? a[s] : b[s - 32]);
-                            pv[f] = (s <= r) ? scale * __expf(Gr - Gh[s]) * qk : 0.f;
+                            const int s = s0 + 8 * c + 2 * e + f;
+                            pv[f] = (s <= r) ? scale * __expf(Gr - Gh[s]) * __uint_as_float(a[8 * c + 2 * e + f]) : 0.f;
                         }
                         w[e] = pack_bf16(pv[0], pv[1]);
                     }
-                    *reinterpret_cast<uint4*>(pan + swz(row, c)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(zpan + swz(row, c)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(pan + swz(row, 4 * half + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(zpan + swz(row, 4 * half + c)) = make_uint4(0, 0, 0, 0);
                 }
             }
         }
@@ -229,38 +301,29 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_before();
     __syncthreads();
 
-    // ---- T = (I + L)^-1 by forward substitution, one column per thread (thread = head, column j)
+    // ---- T_h = (I + L_h)^-1 in place, then T_h diag(beta gamma) -> TD, T_h diag(beta) -> TOP panel 2
+    blocked_unit_lower_inverse(sL, reinterpret_cast<float*>(sm + P_X), tid);
     {
-        const int hh = tid >> 6, j = tid & 63;
-        const float* L = sL + hh * 64 * P_LSTRIDE;
-        float t[64];
+        const int hh = tid >> 7, r = (tid & 127) >> 1, hc = tid & 1;   // row r, columns 32 hc .. 32 hc + 31
+        const float* Trow = sL + (hh * 64 + r) * P_LSTRIDE + 32 * hc;
+        const float* dg = sBG + hh * 64 + 32 * hc;
+        const float* bt = sBeta + hh * 64 + 32 * hc;
+        const uint32_t row = 64 * hh + r;
 #pragma unroll
-        for (int r = 0; r < 64; ++r) {
-            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-            const float4* Lr = reinterpret_cast<const float4*>(L + r * P_LSTRIDE);
+        for (int c = 0; c < 4; ++c) {
+            const float4 x0 = reinterpret_cast<const float4*>(Trow)[2 * c];
+            const float4 x1 = reinterpret_cast<const float4*>(Trow)[2 * c + 1];
+            const float tv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            uint32_t wd[4], wb[4];
 #pragma unroll
-            for (int s4 = 0; s4 < r / 4; ++s4) {
-                const float4 l = Lr[s4];
-                acc0 = fmaf(l.x, t[4 * s4 + 0], acc0);
-                acc1 = fmaf(l.y, t[4 * s4 + 1], acc1);
-                acc2 = fmaf(l.z, t[4 * s4 + 2], acc2);
-                acc3 = fmaf(l.w, t[4 * s4 + 3], acc3);
+            for (int e = 0; e < 4; ++e) {
+                const int s = 8 * c + 2 * e;
+                wd[e] = pack_bf16(tv[2 * e] * dg[s], tv[2 * e + 1] * dg[s + 1]);
+                wb[e] = pack_bf16(tv[2 * e] * bt[s], tv[2 * e + 1] * bt[s + 1]);
             }
-#pragma unroll
-            for (int s = (r / 4) * 4; s < r; ++s) acc0 = fmaf(L[r * P_LSTRIDE + s], t[s], acc0);
-            const float sum = (acc0 + acc1) + (acc2 + acc3);
-            t[r] = (r < j) ? 0.f : (r == j ? 1.f : -sum);
-        }
-        // column j of T_h diag(beta gamma) -> TD (rows 64 hh + r), of T_h diag(beta) -> TOP panel 2
-        const float dj = sBG[hh * 64 + j], bj = sBeta[hh * 64 + j];
-        uint8_t* td = sm + P_TD;
-        uint8_t* tb = sm + P_TOP + 2 * 16384;
-        const uint32_t cj = (uint32_t)j >> 3, ej = ((uint32_t)j & 7u) * 2u;
-#pragma unroll
-        for (int r = 0; r < 64; ++r) {
-            const uint32_t row = 64 * hh + r;
-            *reinterpret_cast<bf16*>(td + swz(row, cj) + ej) = __float2bfloat16_rn(t[r] * dj);
-            *reinterpret_cast<bf16*>(tb + swz(row, cj) + ej) = __float2bfloat16_rn(t[r] * bj);
+            *reinterpret_cast<uint4*>(sm + P_TD + swz(row, 4 * hc + c)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            *reinterpret_cast<uint4*>(sm + P_TOP + 2 * 16384 + swz(row, 4 * hc + c)) =
+                make_uint4(wb[0], wb[1], wb[2], wb[3]);
         }
     }
     fence_proxy_async_smem();
@@ -276,18 +339,18 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     mbar_wait_bounded(bar_mma, 1, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    for (int cb = 0; cb < 4; ++cb) {   // row R = tid of [W_0; W_1] -> -W in TOP panels 0-1
+    for (int cb = 0; cb < 2; ++cb) {   // row R of [W_0; W_1], dk columns 64 half + 32 cb .. -> -W in TOP panel `half`
         uint32_t a[32];
-        tmem_ld32(tl + 64 + 32 * cb, a);
+        tmem_ld32(tl + 64 + 64 * half + 32 * cb, a);
         tmem_wait_ld();
-        uint8_t* pan = sm + P_TOP + (cb >> 1) * 16384;
+        uint8_t* pan = sm + P_TOP + half * 16384;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 w[e] = pack_bf16(-__uint_as_float(a[8 * c + 2 * e]), -__uint_as_float(a[8 * c + 2 * e + 1]));
-            *reinterpret_cast<uint4*>(pan + swz(tid, (cb & 1) * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(pan + swz(R, 4 * cb + c)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
     fence_proxy_async_smem();
@@ -304,23 +367,24 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    {
-        const int hh = tid >> 6, r = tid & 63;
+    {   // row R: head hh, token r; columns 96 half .. 96 half + 95
+        const int hh = R >> 6, r = R & 63;
         const float qs = scale * __expf(sG[hh * 64 + r]);   // scale * gamma_r
         uint8_t* bot = sm + P_BOT + hh * 24576;
-        for (int cb = 0; cb < 6; ++cb) {
+        for (int cb = 0; cb < 3; ++cb) {
+            const int col0 = 96 * half + 32 * cb;
             uint32_t a[32];
-            tmem_ld32(tl + 32 * cb, a);
+            tmem_ld32(tl + col0, a);
             tmem_wait_ld();
-            uint8_t* pan = bot + (cb >> 1) * 8192;
+            uint8_t* pan = bot + (col0 >> 6) * 8192;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const uint32_t chunk = (cb & 1) * 4 + c;
+                const uint32_t chunk = ((col0 & 63) >> 3) + c;
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(a[8 * c + e]);
-                if (cb < 4) {   // Q' = scale gamma_r q_r - P W   (q from the Q rows of the KQ panels)
-                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + P_KQ + (cb >> 1) * 16384 + swz(64 + r, chunk));
+                if (col0 < 128) {   // Q' = scale gamma_r q_r - P W   (q from the Q rows of the KQ panels)
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + P_KQ + (col0 >> 6) * 16384 + swz(64 + r, chunk));
                     const bf16* qe = reinterpret_cast<const bf16*>(&qv);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = fmaf(qs, __bfloat162float(qe[e]), x[e]);
@@ -342,7 +406,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         }
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read();   // shared memory may be released; the global writes finish on their own
     }
     __syncthreads();
     if (warp == 0) {
@@ -637,7 +701,7 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
     const int T_len = a.T;
 
     record_event(events, num_events, 0, a.stream);
-    tc_prep_kernel<<<dim3((unsigned)slots, (unsigned)(a.Hv / 2)), kThreads, P_SMEM, a.stream>>>(
+    tc_prep_kernel<<<dim3((unsigned)slots, (unsigned)(a.Hv / 2)), kPrepThreads, P_SMEM, a.stream>>>(
         tq, tk, static_cast<const bf16*>(a.g), static_cast<const bf16*>(a.beta), a.cu_seqlens, a.num_seqs, T_len,
         a.Hqk, a.Hv, a.scale, ws_a1, ws_vec, a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

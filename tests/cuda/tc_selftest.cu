@@ -83,6 +83,81 @@ mma_case_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int K,
 
 }  // namespace
 
+// A (128 x K, bf16) written into TMEM columns 128.. with tcgen05.st (lane m = row m, k pairs packed
+// per 32-bit column, lower half = even k), B from shared memory (MN-major), D into columns 0..N-1.
+__global__ void __launch_bounds__(128, 1)
+mma_tmem_a_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int K, int N, unsigned* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    const uint32_t B_OFF = 0, BAR = 73728;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + BAR + 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + BAR + 12);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(sb + BAR, 1);
+        mbar_fence_init();
+    }
+    for (int e = tid; e < K * N; e += 128) {
+        const int k = e / N, n = e % N;
+        const uint32_t off = (n / 64) * (K * 128) + swz(k, (n % 64) / 8) + (n % 8) * 2;
+        *reinterpret_cast<__nv_bfloat16*>(sm + B_OFF + off) = B[e];
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int cb = 0; cb < K / 64; ++cb) {   // row tid of A, k = 64 cb .. 64 cb + 63 -> 32 columns
+        uint32_t v[32];
+        for (int e = 0; e < 32; ++e) {
+            const float lo = __bfloat162float(A[(size_t)tid * K + 64 * cb + 2 * e]);
+            const float hi = __bfloat162float(A[(size_t)tid * K + 64 * cb + 2 * e + 1]);
+            v[e] = pack_bf16(lo, hi);
+        }
+        tmem_st32(tl + 128 + 32 * cb, v);
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after();
+        for (int ks = 0; ks < K / 16; ++ks)
+            mma_bf16_ta(tmem, tmem + 128 + 8 * ks, smem_desc(sb + B_OFF + ks * 2048, N > 64 ? K * 128 : 1024, 1024),
+                        idesc_bf16(128, N, 0, 1), ks > 0);
+        mma_commit(sb + BAR);
+    }
+    mbar_wait_bounded(sb + BAR, 0, abort_flag, status, 1u, 1000000000ull);
+    tc_fence_after();
+    for (int cb = 0; cb < N / 32; ++cb) {
+        uint32_t r[32];
+        tmem_ld32(tl + 32 * cb, r);
+        tmem_wait_ld();
+        for (int e = 0; e < 32; ++e) D[(size_t)tid * N + 32 * cb + e] = __uint_as_float(r[e]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+extern "C" int tc_selftest_mma_tmem_a(const void* A, const void* B, float* D, int K, int N, unsigned* status) {
+    if (K % 64 || K < 64 || K > 128 || N % 64 || N < 64 || N > 128) return 1;
+    const int smem = 73728 + 64 + 1024;
+    if (cudaFuncSetAttribute(mma_tmem_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 2;
+    mma_tmem_a_kernel<<<1, 128, smem>>>(static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B),
+                                        D, K, N, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
 extern "C" int tc_selftest_mma(const void* A, const void* B, float* D, int K, int N, int a_mn, int b_mn,
                                unsigned* status) {
     if (K % 64 || K < 64 || K > 192 || N % 64 || N < 64 || N > 192) return 1;

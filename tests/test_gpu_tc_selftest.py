@@ -29,6 +29,7 @@ def lib():
         subprocess.check_call([b._nvcc(), *b.NVCC_FLAGS, "-shared", "-o", LIB, SRC])
     L = ctypes.CDLL(LIB)
     L.tc_selftest_mma.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    L.tc_selftest_mma_tmem_a.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p]
     return L
 
 
@@ -53,4 +54,21 @@ def test_mma_layout(lib, a_mn, b_mn, K, N):
     ref = A.double().numpy() @ B.double().numpy()
     got = D.cpu().numpy()
     err = np.abs(got - ref).max() / np.abs(ref).max()
+    assert err < 1e-5, f"max rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("K,N", [(64, 128), (128, 128), (128, 64)])
+def test_mma_a_from_tmem(lib, K, N):
+    """A operand held in TMEM (as the prefill's P and T diag(beta gamma) operands are)."""
+    rng = np.random.default_rng(K + 3 * N)
+    A = torch.from_numpy(rng.normal(size=(128, K)).astype(np.float32)).bfloat16()
+    B = torch.from_numpy(rng.normal(size=(K, N)).astype(np.float32)).bfloat16()
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.zeros(128, N, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert lib.tc_selftest_mma_tmem_a(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), K, N, status.data_ptr()) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "bounded wait ran out"
+    ref = A.double().numpy() @ B.double().numpy()
+    err = np.abs(D.cpu().numpy() - ref).max() / np.abs(ref).max()
     assert err < 1e-5, f"max rel err {err:.3e}"
