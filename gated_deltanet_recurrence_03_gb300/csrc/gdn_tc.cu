@@ -72,87 +72,105 @@ __device__ bool slot_lookup(const int32_t* cu, int nseq, int T_len, int slot, in
 }
 
 // ------------------------------------------------------------------ parallel intra-chunk kernel
+// Two CTAs fit on one SM (shared memory <= 110 KB, 256 TMEM columns each), so one CTA's MMAs and
+// memory traffic overlap the other's CUDA-core phases.
+//
 // Shared memory (byte offsets from a 1024-aligned base)
 constexpr uint32_t P_KQ = 0;            // 2 panels (dk 0-63, 64-127) x [K rows 0-63 | Q rows 64-127]
-constexpr uint32_t P_AP = 32768;        // blockdiag(P_0, P_1): 2 panels x 128 rows (K-major A)
-constexpr uint32_t P_TOP = 65536;       // [-W_h | Tb_h] for both heads: 3 panels x 128 rows
-constexpr uint32_t P_L = 114688;        // L_h = diag(beta) A, fp32 [2][64][68]; overwritten by T_h
-constexpr uint32_t P_LSTRIDE = 68;
-constexpr uint32_t P_LBYTES = 2 * 64 * P_LSTRIDE * 4;
-constexpr uint32_t P_TD = (P_L + P_LBYTES + 1023) & ~1023u;  // [T_0 diag(beta gamma); T_1 diag(beta gamma)] 1 panel x 128 rows
-constexpr uint32_t P_X = P_TD;          // blocked-solve scratch X [2][16][48] fp32 (before TD is written)
-constexpr uint32_t P_BOT = P_L;         // [Q'_h | P_h Tb_h]: 2 heads x 3 panels x 64 rows (after L, TD die)
-constexpr uint32_t P_SMALL = P_TD + 16384;  // G[2][64], beta[2][64], beta*gamma[2][64]
-static_assert(P_L + P_LBYTES <= P_TD, "L must not overlap TD / X");
-static_assert(P_BOT + 2 * 24576 <= P_SMALL, "BOT must end before the small buffers");
-constexpr uint32_t P_BAR = P_SMALL + 3 * 2 * 64 * 4;
+constexpr uint32_t P_TOP = 32768;       // [-W_h | Tb_h] for both heads: 3 panels x 128 rows (B operand)
+constexpr uint32_t P_X = P_TOP;         // blocked-solve scratch X [2][16][48] fp32 (panel 0, before -W)
+constexpr uint32_t P_HANDOFF = P_TOP + 16384;   // P_0 rows, bf16 [64][64] (panel 1, before -W)
+constexpr uint32_t P_LC = 81920;        // L_h then T_h: 10 lower blocks of 16 x 16 fp32 per head, row stride 20
+constexpr uint32_t P_LBLK = 16 * 20;    // floats per block
+constexpr uint32_t P_SMALL = P_LC + 2 * 10 * P_LBLK * 4;   // G, beta, beta*gamma, a, c: [2][64] each
+constexpr uint32_t P_BAR = P_SMALL + 5 * 2 * 64 * 4;
 constexpr uint32_t P_SMEM = P_BAR + 64 + 1024;  // + alignment slack
-constexpr int kPrepThreads = 256;       // 8 warps: warps w and w+4 share TMEM lane quarter w % 4
+constexpr int kPrepThreads = 128;
+// TMEM columns: Gram D 0-63; T diag(beta gamma) (A operand) 0-31 after the Gram is read;
+// [W_0; W_1] D 64-191; blockdiag(P_0, P_1) (A operand) 192-255; [-P W | P Tb] D 0-191.
+constexpr uint32_t T_GRAM = 0, T_TD = 0, T_W = 64, T_AP = 192, T_PW = 0;
+// Output panel i = 3 h + p of [Q'_h | P_h Tb_h] (8 KB each, after their inputs are consumed)
+__device__ __forceinline__ uint32_t bot_panel(int i) { return i < 4 ? P_KQ + 8192u * i : P_LC + 8192u * (i - 4); }
+static_assert(P_LC + 2 * 8192 <= P_SMALL, "two output panels must fit in the L/T region");
+static_assert(P_SMEM <= 113 * 1024, "two CTAs per SM");
 
-// In-place inverse of the unit lower-triangular I + L_h (L_h strictly lower, fp32, row stride
-// P_LSTRIDE) for both heads, by 16 x 16 blocks: the diagonal blocks by forward substitution (one
-// column per thread), then block row i from T_ij = -T_ii sum_{j<=k<i} L_ik T_kj.  128 threads per head.
-__device__ __forceinline__ void blocked_unit_lower_inverse(float* sL, float* sX, int tid) {
-    const int h = tid >> 7, t = tid & 127;
-    float* L = sL + h * 64 * P_LSTRIDE;
+__device__ __forceinline__ int lblk(int I, int J) { return I * (I + 1) / 2 + J; }   // J <= I
+
+// In-place inverse of I + L_h for both heads (64 threads per head): 16 x 16 diagonal blocks by
+// forward substitution (one column per thread), then block row i from T_ij = -T_ii sum_k L_ik T_kj,
+// with 2 x 4 register tiles.
+__device__ __forceinline__ void blocked_unit_lower_inverse(float* sLC, float* sX, int tid) {
+    const int h = tid >> 6, t = tid & 63;
+    float* L = sLC + h * 10 * P_LBLK;
     float* X = sX + h * 16 * 48;
-    float tc[16];
-    const int I = t >> 4, j = t & 15;
-    if (t < 64) {   // column j of (I + L_II)^-1
+    {
+        const int I = t >> 4, j = t & 15;
+        float* D = L + lblk(I, I) * P_LBLK;
+        float tc[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            const float* Lr = L + (16 * I + r) * P_LSTRIDE + 16 * I;
+            const float* Dr = D + r * 20;
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int s = 0; s + 1 < r; s += 2) {
-                a0 = fmaf(Lr[s], tc[s], a0);
-                a1 = fmaf(Lr[s + 1], tc[s + 1], a1);
+                a0 = fmaf(Dr[s], tc[s], a0);
+                a1 = fmaf(Dr[s + 1], tc[s + 1], a1);
             }
-            if (r & 1) a0 = fmaf(Lr[r - 1], tc[r - 1], a0);
+            if (r & 1) a0 = fmaf(Dr[r - 1], tc[r - 1], a0);
             tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -(a0 + a1));
         }
-    }
-    __syncthreads();
-    if (t < 64) {
+        __syncthreads();
 #pragma unroll
-        for (int r = 0; r < 16; ++r) L[(16 * I + r) * P_LSTRIDE + 16 * I + j] = tc[r];
+        for (int r = 0; r < 16; ++r) D[r * 20 + j] = tc[r];
+        __syncthreads();
     }
-    __syncthreads();
 #pragma unroll
     for (int i = 1; i < 4; ++i) {
-        // X_ij = sum_{k=j}^{i-1} L_ik T_kj  (L_ik still original, T_kj final)
-        for (int e = t; e < 256 * i; e += 128) {
-            const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const float* Lr = L + (16 * i + r) * P_LSTRIDE;
-            float a0 = 0.f, a1 = 0.f;
+        const int ncq = 4 * i;                       // column quads of block row i
+        for (int tile = t; tile < 8 * ncq; tile += 64) {
+            const int cq = tile % ncq, rp = tile / ncq;
+            const int jb = cq >> 2, c4 = (cq & 3) * 4;
+            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
             for (int k = jb; k < i; ++k) {
-                const float* Tk = L + (16 * k) * P_LSTRIDE + 16 * jb + c;
+                const float* Lik = L + lblk(i, k) * P_LBLK;
+                const float* Tkj = L + lblk(k, jb) * P_LBLK + c4;
 #pragma unroll
-                for (int s = 0; s < 16; s += 2) {
-                    a0 = fmaf(Lr[16 * k + s], Tk[s * P_LSTRIDE], a0);
-                    a1 = fmaf(Lr[16 * k + s + 1], Tk[(s + 1) * P_LSTRIDE], a1);
+                for (int s = 0; s < 16; ++s) {
+                    const float l0 = Lik[rp * 20 + s], l1 = Lik[(rp + 8) * 20 + s];
+                    const float4 tv = *reinterpret_cast<const float4*>(Tkj + s * 20);
+                    acc0.x = fmaf(l0, tv.x, acc0.x); acc0.y = fmaf(l0, tv.y, acc0.y);
+                    acc0.z = fmaf(l0, tv.z, acc0.z); acc0.w = fmaf(l0, tv.w, acc0.w);
+                    acc1.x = fmaf(l1, tv.x, acc1.x); acc1.y = fmaf(l1, tv.y, acc1.y);
+                    acc1.z = fmaf(l1, tv.z, acc1.z); acc1.w = fmaf(l1, tv.w, acc1.w);
                 }
             }
-            X[r * 48 + 16 * jb + c] = a0 + a1;
+            *reinterpret_cast<float4*>(X + rp * 48 + 16 * jb + c4) = acc0;
+            *reinterpret_cast<float4*>(X + (rp + 8) * 48 + 16 * jb + c4) = acc1;
         }
         __syncthreads();
-        // T_ij = -T_ii X_ij, written over L_ij
-        for (int e = t; e < 256 * i; e += 128) {
-            const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15;
-            const float* Ti = L + (16 * i + r) * P_LSTRIDE + 16 * i;
-            float a0 = 0.f, a1 = 0.f;
+        const float* Tii = L + lblk(i, i) * P_LBLK;
+        for (int tile = t; tile < 8 * ncq; tile += 64) {
+            const int cq = tile % ncq, rp = tile / ncq;
+            const int jb = cq >> 2, c4 = (cq & 3) * 4;
+            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
 #pragma unroll
-            for (int s = 0; s < 16; s += 2) {
-                a0 = fmaf(Ti[s], X[s * 48 + 16 * jb + c], a0);
-                a1 = fmaf(Ti[s + 1], X[(s + 1) * 48 + 16 * jb + c], a1);
+            for (int s = 0; s < 16; ++s) {
+                const float l0 = Tii[rp * 20 + s], l1 = Tii[(rp + 8) * 20 + s];
+                const float4 xv = *reinterpret_cast<const float4*>(X + s * 48 + 16 * jb + c4);
+                acc0.x = fmaf(l0, xv.x, acc0.x); acc0.y = fmaf(l0, xv.y, acc0.y);
+                acc0.z = fmaf(l0, xv.z, acc0.z); acc0.w = fmaf(l0, xv.w, acc0.w);
+                acc1.x = fmaf(l1, xv.x, acc1.x); acc1.y = fmaf(l1, xv.y, acc1.y);
+                acc1.z = fmaf(l1, xv.z, acc1.z); acc1.w = fmaf(l1, xv.w, acc1.w);
             }
-            L[(16 * i + r) * P_LSTRIDE + 16 * jb + c] = -(a0 + a1);
+            float* Tij = L + lblk(i, jb) * P_LBLK + c4;
+            *reinterpret_cast<float4*>(Tij + rp * 20) = make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w);
+            *reinterpret_cast<float4*>(Tij + (rp + 8) * 20) = make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w);
         }
         __syncthreads();
     }
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__global__ void __launch_bounds__(kPrepThreads, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const bf16* __restrict__ g, const bf16* __restrict__ beta, const int32_t* __restrict__ cu,
                int nseq, int T_len, int Hqk, int Hv, float scale, uint8_t* __restrict__ ws_a1,
@@ -160,18 +178,20 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    float* sG = reinterpret_cast<float*>(sm + P_SMALL);   // [2][64]
+    float* sG = reinterpret_cast<float*>(sm + P_SMALL);   // [2][64] cumulative log decay G_r
     float* sBeta = sG + 128;                              // [2][64]
     float* sBG = sG + 256;                                // [2][64] beta_r * gamma_r
-    float* sL = reinterpret_cast<float*>(sm + P_L);
+    float* sA = sG + 384;                                 // [2][64] exp(G_r - G_0)
+    float* sC = sG + 512;                                 // [2][64] exp(G_0 - G_s)
+    float* sLC = reinterpret_cast<float*>(sm + P_LC);
     const uint32_t bar_tma = sb + P_BAR, bar_mma = sb + P_BAR + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P_BAR + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + P_BAR + 20);
+    int* sFactor = reinterpret_cast<int*>(sm + P_BAR + 24);   // [2]: decay ratios factorise safely
 
     const int slot = blockIdx.x, pair = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;     // TMEM lane quarter, column half
-    const int R = 32 * quarter + lane;                   // TMEM lane = accumulator row of this thread
+    const int R = tid;                                   // TMEM lane = accumulator row of this thread
     int seq;
     long long t0;
     int n;
@@ -192,7 +212,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);   // this warp's TMEM lane quarter
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's TMEM lane quarter
 
     if (tid == 0) {
         mbar_arrive_expect_tx(bar_tma, 4 * 8192);
@@ -223,169 +243,214 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         sG[hh * 64 + r0] = p - g1;
         sBeta[hh * 64 + r0] = b0;
         sBeta[hh * 64 + r1] = b1;
+        const float G0 = __shfl_sync(0xffffffffu, p - g1, 0), Gl = __shfl_sync(0xffffffffu, p, 31);
+        if (lane == 0) sFactor[hh] = (G0 - Gl) < 80.f;
     }
     __syncthreads();
-    if (tid < 128) {
+    {
         const int hh = tid >> 6, r = tid & 63;
-        const float Gr = sG[hh * 64 + r], Gl = sG[hh * 64 + 63];
+        const float Gr = sG[hh * 64 + r], Gl = sG[hh * 64 + 63], G0 = sG[hh * 64];
         sBG[hh * 64 + r] = sBeta[hh * 64 + r] * __expf(Gr);
+        sA[hh * 64 + r] = __expf(Gr - G0);
+        sC[hh * 64 + r] = __expf(G0 - Gr);
         float* vec = ws_vec + ((size_t)slot * Hv + h0 + hh) * kVecFloats;
         vec[r] = __expf(Gl - Gr);
         if (r == 0) vec[64] = __expf(Gl);
     }
 
-    // ---- [K; Q] K^T : rows 0-63 K K^T, rows 64-127 Q K^T  (TMEM columns 0-63)
+    // ---- [K; Q] K^T : rows 0-63 K K^T, rows 64-127 Q K^T
     mbar_wait_bounded(bar_tma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     if (tid == 0) {
         tc_fence_after();
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = P_KQ + (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_bf16(tmem, smem_desc(sb + off, 16, 1024), smem_desc(sb + off, 16, 1024), idesc_bf16(128, 64, 0, 0),
-                     ks > 0);
+            mma_bf16(tmem + T_GRAM, smem_desc(sb + off, 16, 1024), smem_desc(sb + off, 16, 1024),
+                     idesc_bf16(128, 64, 0, 0), ks > 0);
         }
         mma_commit(bar_mma);
     }
-    __syncthreads();   // sBG, sG, sBeta visible to all
+    __syncthreads();   // gate scalars visible to all
     mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    {   // this thread: row R, columns s = 32 half .. 32 half + 31
-        uint32_t a[32];
-        tmem_ld32(tl + 32 * half, a);
+    {
+        uint32_t a[64];
+        tmem_ld32(tl + T_GRAM, *reinterpret_cast<uint32_t(*)[32]>(a));
+        tmem_ld32(tl + T_GRAM + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
         tmem_wait_ld();
-        const int s0 = 32 * half;
-        if (quarter < 2) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s, s < r
-            const int r = R;
+        if (warp < 2) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s (s < r), lower blocks
+            const int r = R, I = r >> 4, rr = r & 15;
             for (int hh = 0; hh < 2; ++hh) {
                 const float* Gh = sG + hh * 64;
-                const float br = sBeta[hh * 64 + r], Gr = Gh[r];
-                float* Lrow = sL + (hh * 64 + r) * P_LSTRIDE + s0;
+                const float br = sBeta[hh * 64 + r], ar = sA[hh * 64 + r], Gr = Gh[r];
+                const float* ch = sC + hh * 64;
+                const bool fac = sFactor[hh] != 0;
+                float* Lh = sLC + hh * 10 * P_LBLK;
+                for (int J = 0; J <= I; ++J) {
+                    float* dst = Lh + lblk(I, J) * P_LBLK + rr * 20;
 #pragma unroll
-                for (int s4 = 0; s4 < 8; ++s4) {
-                    float4 o;
-                    float* op = &o.x;
+                    for (int s4 = 0; s4 < 4; ++s4) {
+                        float o[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = s0 + 4 * s4 + e;
-                        op[e] = (s < r) ? br * __expf(Gr - Gh[s]) * __uint_as_float(a[4 * s4 + e]) : 0.f;
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 16 * J + 4 * s4 + e;
+                            const float kk = __uint_as_float(a[s]);
+                            const float dec = fac ? ar * ch[s] : __expf(Gr - Gh[s]);
+                            o[e] = (s < r) ? br * dec * kk : 0.f;
+                        }
+                        *reinterpret_cast<float4*>(dst + 4 * s4) = make_float4(o[0], o[1], o[2], o[3]);
                     }
-                    reinterpret_cast<float4*>(Lrow)[s4] = o;
                 }
             }
-        } else {             // row r of Q K^T -> P_h[r][s] = scale exp(G_r - G_s) q_r.k_s, s <= r
+        } else {          // row r of Q K^T -> P_h[r][s] = scale exp(G_r - G_s) q_r.k_s (s <= r)
             const int r = R - 64;
             for (int hh = 0; hh < 2; ++hh) {
                 const float* Gh = sG + hh * 64;
-                const float Gr = Gh[r];
-                const uint32_t row = 64 * hh + r;
-                uint8_t* pan = sm + P_AP + hh * 16384;
-                uint8_t* zpan = sm + P_AP + (1 - hh) * 16384;
+                const float ar = sA[hh * 64 + r], Gr = Gh[r];
+                const float* ch = sC + hh * 64;
+                const bool fac = sFactor[hh] != 0;
+                uint32_t w[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t w[4];
+                for (int e = 0; e < 32; ++e) {
+                    float pv[2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float pv[2];
-#pragma unroll
-                        for (int f = 0; f < 2; ++f) {
-                            const int s = s0 + 8 * c + 2 * e + f;
-                            pv[f] = (s <= r) ? scale * __expf(Gr - Gh[s]) * __uint_as_float(a[8 * c + 2 * e + f]) : 0.f;
-                        }
-                        w[e] = pack_bf16(pv[0], pv[1]);
+                    for (int f = 0; f < 2; ++f) {
+                        const int s = 2 * e + f;
+                        const float dec = fac ? ar * ch[s] : __expf(Gr - Gh[s]);
+                        pv[f] = (s <= r) ? scale * dec * __uint_as_float(a[s]) : 0.f;
                     }
-                    *reinterpret_cast<uint4*>(pan + swz(row, 4 * half + c)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(zpan + swz(row, 4 * half + c)) = make_uint4(0, 0, 0, 0);
+                    w[e] = pack_bf16(pv[0], pv[1]);
+                }
+                if (hh == 1) {   // own lane: [0 | P_1 row]
+                    uint32_t z[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) z[e] = 0u;
+                    tmem_st32(tl + T_AP, z);
+                    tmem_st32(tl + T_AP + 32, w);
+                } else {         // P_0 row r belongs to lane r: hand it over through shared memory
+                    uint4* dst = reinterpret_cast<uint4*>(sm + P_HANDOFF + r * 128);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
                 }
             }
         }
     }
+    __syncthreads();
+    if (warp < 2) {   // lanes 0-63: [P_0 row | 0]
+        uint32_t w[32], z[32];
+        const uint4* src = reinterpret_cast<const uint4*>(sm + P_HANDOFF + R * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 x = src[c];
+            w[4 * c] = x.x; w[4 * c + 1] = x.y; w[4 * c + 2] = x.z; w[4 * c + 3] = x.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = 0u;
+        tmem_st32(tl + T_AP, w);
+        tmem_st32(tl + T_AP + 32, z);
+    }
+    tmem_wait_st();
     tc_fence_before();
     __syncthreads();
 
-    // ---- T_h = (I + L_h)^-1 in place, then T_h diag(beta gamma) -> TD, T_h diag(beta) -> TOP panel 2
-    blocked_unit_lower_inverse(sL, reinterpret_cast<float*>(sm + P_X), tid);
+    // ---- T_h = (I + L_h)^-1 in place; T_h diag(beta gamma) -> TMEM (A operand), T_h diag(beta) -> TOP panel 2
+    blocked_unit_lower_inverse(sLC, reinterpret_cast<float*>(sm + P_X), tid);
     {
-        const int hh = tid >> 7, r = (tid & 127) >> 1, hc = tid & 1;   // row r, columns 32 hc .. 32 hc + 31
-        const float* Trow = sL + (hh * 64 + r) * P_LSTRIDE + 32 * hc;
-        const float* dg = sBG + hh * 64 + 32 * hc;
-        const float* bt = sBeta + hh * 64 + 32 * hc;
-        const uint32_t row = 64 * hh + r;
+        const int hh = R >> 6, r = R & 63, I = r >> 4, rr = r & 15;
+        const float* Th = sLC + hh * 10 * P_LBLK;
+        const float* dg = sBG + hh * 64;
+        const float* bt = sBeta + hh * 64;
+        uint32_t wd[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float4 x0 = reinterpret_cast<const float4*>(Trow)[2 * c];
-            const float4 x1 = reinterpret_cast<const float4*>(Trow)[2 * c + 1];
-            const float tv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            uint32_t wd[4], wb[4];
+        for (int J = 0; J < 4; ++J) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int s = 8 * c + 2 * e;
-                wd[e] = pack_bf16(tv[2 * e] * dg[s], tv[2 * e + 1] * dg[s + 1]);
-                wb[e] = pack_bf16(tv[2 * e] * bt[s], tv[2 * e + 1] * bt[s + 1]);
+            for (int c = 0; c < 2; ++c) {   // 8 columns s = 16 J + 8 c ..
+                float tv[8];
+                if (J <= I) {
+                    const float* src = Th + lblk(I, J) * P_LBLK + rr * 20 + 8 * c;
+                    const float4 x0 = *reinterpret_cast<const float4*>(src), x1 = *reinterpret_cast<const float4*>(src + 4);
+                    tv[0] = x0.x; tv[1] = x0.y; tv[2] = x0.z; tv[3] = x0.w;
+                    tv[4] = x1.x; tv[5] = x1.y; tv[6] = x1.z; tv[7] = x1.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) tv[e] = 0.f;
+                }
+                const int s0 = 16 * J + 8 * c;
+                uint32_t wb[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    wd[(s0 >> 1) + e] = pack_bf16(tv[2 * e] * dg[s0 + 2 * e], tv[2 * e + 1] * dg[s0 + 2 * e + 1]);
+                    wb[e] = pack_bf16(tv[2 * e] * bt[s0 + 2 * e], tv[2 * e + 1] * bt[s0 + 2 * e + 1]);
+                }
+                *reinterpret_cast<uint4*>(sm + P_TOP + 2 * 16384 + swz(R, s0 >> 3)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
             }
-            *reinterpret_cast<uint4*>(sm + P_TD + swz(row, 4 * hc + c)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-            *reinterpret_cast<uint4*>(sm + P_TOP + 2 * 16384 + swz(row, 4 * hc + c)) =
-                make_uint4(wb[0], wb[1], wb[2], wb[3]);
         }
+        tmem_st32(tl + T_TD, wd);
     }
+    tmem_wait_st();
     fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
 
-    // ---- [W_0; W_1] = [T_0 D_0; T_1 D_1] K   (TMEM columns 64-191)
+    // ---- [W_0; W_1] = [T_0 D_0; T_1 D_1] K
     if (tid == 0) {
         tc_fence_after();
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + 64, smem_desc(sb + P_TD + ks * 32, 16, 1024),
-                     smem_desc(sb + P_KQ + ks * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1), ks > 0);
+            mma_bf16_ta(tmem + T_W, tmem + T_TD + 8 * ks, smem_desc(sb + P_KQ + ks * 2048, 16384, 1024),
+                        idesc_bf16(128, 128, 0, 1), ks > 0);
         mma_commit(bar_mma);
     }
     mbar_wait_bounded(bar_mma, 1, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    for (int cb = 0; cb < 2; ++cb) {   // row R of [W_0; W_1], dk columns 64 half + 32 cb .. -> -W in TOP panel `half`
+    for (int cb = 0; cb < 4; ++cb) {   // row R of [W_0; W_1] -> -W in TOP panels 0-1
         uint32_t a[32];
-        tmem_ld32(tl + 64 + 64 * half + 32 * cb, a);
+        tmem_ld32(tl + T_W + 32 * cb, a);
         tmem_wait_ld();
-        uint8_t* pan = sm + P_TOP + half * 16384;
+        uint8_t* pan = sm + P_TOP + (cb >> 1) * 16384;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 w[e] = pack_bf16(-__uint_as_float(a[8 * c + 2 * e]), -__uint_as_float(a[8 * c + 2 * e + 1]));
-            *reinterpret_cast<uint4*>(pan + swz(R, 4 * cb + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(pan + swz(R, (cb & 1) * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    // ---- blockdiag(P_0, P_1) [-W | Tb]  (TMEM columns 0-191): -P W and P Tb for both heads
+    // ---- blockdiag(P_0, P_1) [-W | Tb]: -P W and P Tb for both heads
     if (tid == 0) {
         tc_fence_after();
         for (int ks = 0; ks < 8; ++ks)
-            mma_bf16(tmem, smem_desc(sb + P_AP + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                     smem_desc(sb + P_TOP + ks * 2048, 16384, 1024), idesc_bf16(128, 192, 0, 1), ks > 0);
+            mma_bf16_ta(tmem + T_PW, tmem + T_AP + 8 * ks, smem_desc(sb + P_TOP + ks * 2048, 16384, 1024),
+                        idesc_bf16(128, 192, 0, 1), ks > 0);
         mma_commit(bar_mma);
     }
+    // this thread's query row, read before the K/Q panels are reused for the outputs
+    const int hh = R >> 6, r = R & 63;
+    uint4 qrow[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+        qrow[c] = *reinterpret_cast<const uint4*>(sm + P_KQ + (c >> 3) * 16384 + 8192 + swz(r, c & 7));
     mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    {   // row R: head hh, token r; columns 96 half .. 96 half + 95
-        const int hh = R >> 6, r = R & 63;
+    __syncthreads();   // every thread holds its q row: the K/Q panels are free
+    {
         const float qs = scale * __expf(sG[hh * 64 + r]);   // scale * gamma_r
-        uint8_t* bot = sm + P_BOT + hh * 24576;
-        for (int cb = 0; cb < 3; ++cb) {
-            const int col0 = 96 * half + 32 * cb;
+        for (int cb = 0; cb < 6; ++cb) {
             uint32_t a[32];
-            tmem_ld32(tl + col0, a);
+            tmem_ld32(tl + T_PW + 32 * cb, a);
             tmem_wait_ld();
-            uint8_t* pan = bot + (col0 >> 6) * 8192;
+            uint8_t* pan = sm + bot_panel(3 * hh + (cb >> 1));
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const uint32_t chunk = ((col0 & 63) >> 3) + c;
+                const uint32_t chunk = (cb & 1) * 4 + c;
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(a[8 * c + e]);
-                if (col0 < 128) {   // Q' = scale gamma_r q_r - P W   (q from the Q rows of the KQ panels)
-                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + P_KQ + (col0 >> 6) * 16384 + swz(64 + r, chunk));
-                    const bf16* qe = reinterpret_cast<const bf16*>(&qv);
+                if (cb < 4) {   // Q' = scale gamma_r q_r - P W
+                    const bf16* qe = reinterpret_cast<const bf16*>(&qrow[(cb >> 1) * 8 + chunk]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = fmaf(qs, __bfloat162float(qe[e]), x[e]);
                 }
@@ -397,12 +462,12 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {   // A1 of each head: panel p = [TOP rows of the head | BOT rows of the head]
-        for (int hh = 0; hh < 2; ++hh) {
-            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + h0 + hh) * kA1Bytes;
+    if (tid == 0) {   // A1 of each head: panel p = [TOP rows of the head | output rows of the head]
+        for (int h = 0; h < 2; ++h) {
+            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + h0 + h) * kA1Bytes;
             for (int p = 0; p < 3; ++p) {
-                bulk_s2g(dst + p * 16384, sb + P_TOP + p * 16384 + hh * 8192, 8192);
-                bulk_s2g(dst + p * 16384 + 8192, sb + P_BOT + hh * 24576 + p * 8192, 8192);
+                bulk_s2g(dst + p * 16384, sb + P_TOP + p * 16384 + h * 8192, 8192);
+                bulk_s2g(dst + p * 16384 + 8192, sb + bot_panel(3 * h + p), 8192);
             }
         }
         bulk_commit();
@@ -683,6 +748,8 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+        if (attr_err == cudaSuccess)   // two prep CTAs per SM need the largest shared-memory carveout
+            attr_err = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (attr_err == cudaSuccess)
             attr_err = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
     });
