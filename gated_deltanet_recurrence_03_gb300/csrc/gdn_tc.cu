@@ -42,7 +42,6 @@ constexpr int kC = 64;                      // chunk length
 constexpr int kD = 128;                     // dk = dv
 constexpr uint32_t kA1Bytes = 3u * 128u * 128u;  // 3 panels x 128 rows x 128 B
 constexpr int kVecFloats = 128;             // per (chunk, head): b_r (64), gamma_C at [64]
-constexpr int kThreads = 128;
 constexpr int kSlices = 2;                  // dv slices of 64 columns per head in the chain kernel
 
 // Sequences are laid out in "slots": chunk c of sequence i lives in slot floor(start_i / C) + i + c.
@@ -482,16 +481,28 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
 // ------------------------------------------------------------------ sequential chain kernel
 constexpr uint32_t C_A1 = 0;            // 2 stages x 48 KB
-constexpr uint32_t C_KT = 98304;        // 2 stages x 16 KB (K tile: 2 panels x 64 token rows)
-constexpr uint32_t C_VT = 131072;       // 2 stages x 8 KB  (V slice: 1 panel x 64 token rows)
-constexpr uint32_t C_SB = 147456;       // bf16 state slice: 1 panel x 128 dk rows
-constexpr uint32_t C_UB = 163840;       // bf16 b*U: 1 panel x 64 token rows
-constexpr uint32_t C_VEC = 172032;      // 2 stages x 512 B
-constexpr uint32_t C_BAR = 173056;
-constexpr uint32_t C_SMEM = C_BAR + 64 + 1024;
-constexpr uint32_t kStageBytes = kA1Bytes + 16384 + 8192 + kVecFloats * 4;
+constexpr uint32_t C_VT = 98304;        // 2 stages x 8 KB  (V slice: 1 panel x 64 token rows)
+constexpr uint32_t C_KT = 114688;       // 3 stages x 16 KB (K tile: 2 panels x 64 token rows)
+constexpr uint32_t C_SB = 163840;       // bf16 state slice: 1 panel x 128 dk rows
+constexpr uint32_t C_UB = 180224;       // bf16 b*U: 1 panel x 64 token rows
+constexpr uint32_t C_VEC = 188416;      // 3 stages x 512 B
+constexpr uint32_t C_BAR = 189952;
+constexpr uint32_t C_SMEM = C_BAR + 128 + 1024;
+constexpr int kKStages = 3;
+// Operands arrive in two rings freed at different times: A1 and the V slice (2 stages, consumed by
+// D1) and the K tile with the b / gamma_C vector (3 stages, consumed by the state update and the
+// epilogues).  One lane of an output warp issues the loads, off the critical path.
+constexpr uint32_t kStageBytesA = kA1Bytes + 8192;
+constexpr uint32_t kStageBytesK = 16384 + kVecFloats * 4;
+// 8 warps: warps w and w + 4 read TMEM lane quarter w % 4 and split the slice's 64 columns.
+constexpr int kChainThreads = 256;
+// TMEM columns: state S 0-63; D1 of even chunks 64-127, of odd chunks 128-191.
 
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const uint8_t* __restrict__ ws_a1, const float* __restrict__ ws_vec, const float* __restrict__ S0,
                 bf16* __restrict__ out, float* __restrict__ S_final, const int32_t* __restrict__ cu, int nseq,
@@ -499,11 +510,17 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    const uint32_t bar_load0 = sb + C_BAR, bar_mma1 = sb + C_BAR + 16, bar_mma2 = sb + C_BAR + 24;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_BAR + 32);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C_BAR + 36);
+    // bar_a[2] (A1 + V), bar_k[3] (K + vector), mma1, mma2
+    const uint32_t bar_a0 = sb + C_BAR, bar_k0 = sb + C_BAR + 16, bar_mma1 = sb + C_BAR + 40,
+                   bar_mma2 = sb + C_BAR + 48;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_BAR + 56);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C_BAR + 60);
+    constexpr int kProducer = 192;          // lane 0 of warp 6 (an output warp) issues the loads
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int R = 32 * quarter + lane;      // TMEM lane = accumulator row
+    const int cb = 32 * half;               // this thread's 32 of the slice's 64 columns
     const int z = blockIdx.x % kSlices;
     const int h = (blockIdx.x / kSlices) % Hv;
     const int i = blockIdx.x / (kSlices * Hv);
@@ -515,68 +532,97 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     if (base + nch > num_slots) nch = max(0LL, num_slots - base);   // only for malformed offsets
 
     if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), 128);
+        tmem_alloc(smem_u32(tmem_slot), 256);
         tc_fence_before();
     }
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(bar_load0, 1);
-        mbar_init(bar_load0 + 8, 1);
+        mbar_init(bar_a0, 1);
+        mbar_init(bar_a0 + 8, 1);
+        for (int q = 0; q < kKStages; ++q) mbar_init(bar_k0 + 8 * q, 1);
         mbar_init(bar_mma1, 1);
         mbar_init(bar_mma2, 1);
         mbar_fence_init();
     }
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;            // state S: columns 0-63; D1: columns 64-127
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-    const size_t srow = (((size_t)i * Hv + h) * kD + tid) * kD + 64 * z;   // this thread's state row slice
-    const int R = tid;
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
+    const size_t srow = (((size_t)i * Hv + h) * kD + R) * kD + 64 * z + cb;   // 32 floats of state row R
 
-    auto issue_loads = [&](long long c, int st) {
+    auto wait_a = [&](long long c) {
+        return mbar_wait_bounded(bar_a0 + 8 * (uint32_t)(c & 1), (uint32_t)((c >> 1) & 1), abort_flag, status,
+                                 kStatusTimeout, kWaitLimitNs);
+    };
+    auto wait_k = [&](long long c) {
+        return mbar_wait_bounded(bar_k0 + 8 * (uint32_t)(c % kKStages), (uint32_t)((c / kKStages) & 1), abort_flag,
+                                 status, kStatusTimeout, kWaitLimitNs);
+    };
+    auto issue_loads_a = [&](long long c) {   // A1 and the V slice of chunk c
+        const int st = (int)(c & 1);
+        const long long slot = base + c;
+        const uint32_t bar = bar_a0 + 8 * st;
+        mbar_arrive_expect_tx(bar, kStageBytesA);
+        bulk_g2s(sb + C_A1 + st * kA1Bytes, ws_a1 + ((size_t)slot * Hv + h) * kA1Bytes, kA1Bytes, bar);
+        tma_load_3d(sb + C_VT + st * 8192, &tm_v, 64 * z, h, (int)(s0 + c * kC), bar);
+    };
+    auto issue_loads_k = [&](long long c) {   // K tile and the b / gamma_C vector of chunk c
+        const int st = (int)(c % kKStages);
         const long long slot = base + c;
         const int tc0 = (int)(s0 + c * kC);
-        const uint32_t bar = bar_load0 + 8 * st;
-        mbar_arrive_expect_tx(bar, kStageBytes);
-        bulk_g2s(sb + C_A1 + st * kA1Bytes, ws_a1 + ((size_t)slot * Hv + h) * kA1Bytes, kA1Bytes, bar);
+        const uint32_t bar = bar_k0 + 8 * st;
+        mbar_arrive_expect_tx(bar, kStageBytesK);
         tma_load_3d(sb + C_KT + st * 16384, &tm_k, 0, hk, tc0, bar);
         tma_load_3d(sb + C_KT + st * 16384 + 8192, &tm_k, 64, hk, tc0, bar);
-        tma_load_3d(sb + C_VT + st * 8192, &tm_v, 64 * z, h, tc0, bar);
         bulk_g2s(sb + C_VEC + st * 512, ws_vec + ((size_t)slot * Hv + h) * kVecFloats, kVecFloats * 4, bar);
+    };
+    // D1(c) = [Tb; P Tb] V_c: the part of A1 [S; V] that does not depend on the state, issued one chunk
+    // ahead so it runs while the previous chunk's state update is on the critical path.
+    auto issue_v_part = [&](long long c) {
+        const int st = (int)(c & 1);
+        const uint32_t a1 = sb + C_A1 + st * kA1Bytes + 2 * 16384;
+        const uint32_t d1 = tmem + 64 + 64 * (uint32_t)st;
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(d1, smem_desc(a1 + ks * 32, 16, 1024), smem_desc(sb + C_VT + st * 8192 + ks * 2048, 1024, 1024),
+                     idesc_bf16(128, 64, 0, 1), ks > 0);
     };
 
     if (nch == 0) {   // empty sequence: the final state is the initial state
         if (S_final) {
-            for (int e = 0; e < 64; e += 4) {
+            for (int e = 0; e < 32; e += 4) {
                 const float4 v = S0 ? *reinterpret_cast<const float4*>(S0 + srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
                 *reinterpret_cast<float4*>(S_final + srow + e) = v;
             }
         }
     } else {
-        if (tid == 0) {
-            issue_loads(0, 0);
-            if (nch > 1) issue_loads(1, 1);
+        if (tid == kProducer) {
+            for (long long c = 0; c < 2 && c < nch; ++c) issue_loads_a(c);
+            for (long long c = 0; c < kKStages && c < nch; ++c) issue_loads_k(c);
         }
-        // prologue: bf16 copy of S0 into SB, gamma_C(0) * S0 into TMEM
-        mbar_wait_bounded(bar_load0, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
-        const float g0 = reinterpret_cast<const float*>(sm + C_VEC)[64];
-        for (int hb = 0; hb < 2; ++hb) {
+        // prologue: bf16 copy of S0 into SB, gamma_C(0) * S0 into TMEM, V part of chunk 0
+        wait_k(0);
+        {
+            const float g0 = reinterpret_cast<const float*>(sm + C_VEC)[64];   // vector of chunk 0 (K stage 0)
             uint32_t v[32];
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
-                const float4 x = S0 ? *reinterpret_cast<const float4*>(S0 + srow + 32 * hb + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 x = S0 ? *reinterpret_cast<const float4*>(S0 + srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
                 v[e] = __float_as_uint(x.x); v[e + 1] = __float_as_uint(x.y);
                 v[e + 2] = __float_as_uint(x.z); v[e + 3] = __float_as_uint(x.w);
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const float* f = reinterpret_cast<const float*>(v + 8 * c);
-                *reinterpret_cast<uint4*>(sm + C_SB + swz(R, 4 * hb + c)) =
+                *reinterpret_cast<uint4*>(sm + C_SB + swz(R, (cb >> 3) + c)) =
                     make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
             }
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(g0 * __uint_as_float(v[e]));
-            tmem_st32(tl + 32 * hb, v);
+            tmem_st32(tl + cb, v);
+        }
+        if (tid == 0 && wait_a(0)) {
+            tc_fence_after();
+            issue_v_part(0);
         }
         tmem_wait_st();
         fence_proxy_async_smem();
@@ -585,98 +631,93 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
         for (long long c = 0; c < nch; ++c) {
             const int st = (int)(c & 1);
-            const uint32_t lpar = (uint32_t)((c >> 1) & 1), par = (uint32_t)(c & 1);
+            const uint32_t par = (uint32_t)(c & 1);
             const long long tc0 = s0 + c * kC;
             const int n = (int)min((long long)kC, s1 - tc0);
-            const uint32_t a1 = sb + C_A1 + st * kA1Bytes;
-            if (tid == 0) {   // D1 = A1 [S; V]
-                mbar_wait_bounded(bar_load0 + 8 * st, lpar, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+            const uint32_t d1 = tmem + 64 + 64 * (uint32_t)st;
+            if (tid == 0) {   // D1 += A1[:, S part] S   (the V part is already in D1)
+                wait_a(c);
                 tc_fence_after();
-                for (int ks = 0; ks < 12; ++ks) {
-                    const uint64_t ad = smem_desc(a1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                    // single-panel MN-major B: the panel-to-panel offset is never used, so LBO = SBO
-                    const uint64_t bd = ks < 8 ? smem_desc(sb + C_SB + ks * 2048, 1024, 1024)
-                                               : smem_desc(sb + C_VT + st * 8192 + (ks - 8) * 2048, 1024, 1024);
-                    mma_bf16(tmem + 64, ad, bd, idesc_bf16(128, 64, 0, 1), ks > 0);
-                }
+                const uint32_t a1 = sb + C_A1 + st * kA1Bytes;
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(d1, smem_desc(a1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                             smem_desc(sb + C_SB + ks * 2048, 1024, 1024), idesc_bf16(128, 64, 0, 1), 1);
                 mma_commit(bar_mma1);
             }
-            mbar_wait_bounded(bar_load0 + 8 * st, lpar, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+            wait_k(c);
             mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
             tc_fence_after();
-            {
-                uint32_t a[32], b[32];
-                tmem_ld32(tl + 64, a);
-                tmem_ld32(tl + 96, b);
-                tmem_wait_ld();
-                if (warp < 2) {   // U row r = R scaled by b_r = exp(G_C - G_r) -> B operand of the state update
-                    const float br = reinterpret_cast<const float*>(sm + C_VEC + st * 512)[R];
+            const int kst = (int)(c % kKStages);
+            if (tid == kProducer && c + 2 < nch) issue_loads_a(c + 2);   // A1 and V of this stage are consumed
+            uint32_t a[32];
+            tmem_ld32(tl + 64 + 64 * st + cb, a);
+            tmem_wait_ld();
+            if (quarter < 2) {   // U row R scaled by b_r = exp(G_C - G_r) -> B operand of the state update
+                const float br = reinterpret_cast<const float*>(sm + C_VEC + kst * 512)[R];
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        const uint32_t* src = c8 < 4 ? a + 8 * c8 : b + 8 * (c8 - 4);
-                        float f[8];
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float f[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = br * __uint_as_float(src[e]);
-                        *reinterpret_cast<uint4*>(sm + C_UB + swz(R, c8)) =
-                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
-                    }
-                } else {          // output row of token R - 64
-                    const int r = R - 64;
-                    if (r < n) {
-                        uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z);
+                    for (int e = 0; e < 8; ++e) f[e] = br * __uint_as_float(a[8 * c8 + e]);
+                    *reinterpret_cast<uint4*>(sm + C_UB + swz(R, (cb >> 3) + c8)) =
+                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_barrier_sync(1, 128);   // the four U warps only: the output warps do not gate the update
+                if (tid == 0) {   // S (gamma_C-scaled, in TMEM) += K^T (b U); then the next chunk's V part
+                    tc_fence_after();
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmem, smem_desc(sb + C_KT + kst * 16384 + ks * 2048, 8192, 1024),
+                                 smem_desc(sb + C_UB + ks * 2048, 1024, 1024), idesc_bf16(128, 64, 1, 1), 1);
+                    mma_commit(bar_mma2);
+                    if (c + 1 < nch && wait_a(c + 1)) issue_v_part(c + 1);
+                }
+            } else {             // output row of token R - 64
+                const int r = R - 64;
+                if (r < n) {
+                    uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z + cb);
 #pragma unroll
-                        for (int c8 = 0; c8 < 8; ++c8) {
-                            const uint32_t* src = c8 < 4 ? a + 8 * c8 : b + 8 * (c8 - 4);
-                            dst[c8] = make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
-                                                 pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
-                                                 pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
-                                                 pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
-                        }
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const uint32_t* src = a + 8 * c8;
+                        dst[c8] = make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                             pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                             pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                                             pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
                     }
                 }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (tid == 0) {   // S (gamma_C-scaled, in TMEM) += K^T (b U)
-                tc_fence_after();
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem, smem_desc(sb + C_KT + st * 16384 + ks * 2048, 8192, 1024),
-                             smem_desc(sb + C_UB + ks * 2048, 1024, 1024), idesc_bf16(128, 64, 1, 1), 1);
-                mma_commit(bar_mma2);
             }
             mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
             tc_fence_after();
-            if (tid == 0 && c + 2 < nch) issue_loads(c + 2, st);   // this stage's operands are consumed
+            if (tid == kProducer && c + kKStages < nch) issue_loads_k(c + kKStages);   // K, vector consumed
             const bool last = (c + 1 == nch);
             float gnext = 1.f;
             if (!last) {
-                mbar_wait_bounded(bar_load0 + 8 * (st ^ 1), (uint32_t)(((c + 1) >> 1) & 1), abort_flag, status,
-                                  kStatusTimeout, kWaitLimitNs);
-                gnext = reinterpret_cast<const float*>(sm + C_VEC + (st ^ 1) * 512)[64];
+                wait_k(c + 1);
+                gnext = reinterpret_cast<const float*>(sm + C_VEC + (int)((c + 1) % kKStages) * 512)[64];
             }
-            for (int hb = 0; hb < 2; ++hb) {   // new state row R: bf16 copy for the next D1, gamma-scaled in TMEM
+            {   // new state row R: bf16 copy for the next D1, gamma-scaled copy in TMEM
                 uint32_t v[32];
-                tmem_ld32(tl + 32 * hb, v);
+                tmem_ld32(tl + cb, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
                     const float* f = reinterpret_cast<const float*>(v + 8 * c4);
-                    *reinterpret_cast<uint4*>(sm + C_SB + swz(R, 4 * hb + c4)) =
+                    *reinterpret_cast<uint4*>(sm + C_SB + swz(R, (cb >> 3) + c4)) =
                         make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
                 }
                 if (last) {
                     if (S_final) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4*>(S_final + srow + 32 * hb + e) =
+                            *reinterpret_cast<float4*>(S_final + srow + e) =
                                 make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
                                             __uint_as_float(v[e + 3]));
                     }
                 } else {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(gnext * __uint_as_float(v[e]));
-                    tmem_st32(tl + 32 * hb, v);
+                    tmem_st32(tl + cb, v);
                 }
             }
             tmem_wait_st();
@@ -688,7 +729,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 256);
     }
 }
 
@@ -773,7 +814,7 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
         a.Hqk, a.Hv, a.scale, ws_a1, ws_vec, a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     record_event(events, num_events, 1, a.stream);
-    tc_chain_kernel<<<(unsigned)((long long)a.num_seqs * a.Hv * kSlices), kThreads, C_SMEM, a.stream>>>(
+    tc_chain_kernel<<<(unsigned)((long long)a.num_seqs * a.Hv * kSlices), kChainThreads, C_SMEM, a.stream>>>(
         tk, tv, ws_a1, ws_vec, a.S0, static_cast<bf16*>(a.out), a.S_final, a.cu_seqlens, a.num_seqs, T_len, a.Hqk,
         a.Hv, (int)slots, a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
