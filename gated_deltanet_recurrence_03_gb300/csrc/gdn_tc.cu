@@ -95,11 +95,25 @@ static_assert(P_SMEM <= 113 * 1024, "two CTAs per SM");
 
 __device__ __forceinline__ int lblk(int I, int J) { return I * (I + 1) / 2 + J; }   // J <= I
 
-// In-place inverse of I + L_h for both heads (64 threads per head): 16 x 16 diagonal blocks by
-// forward substitution (one column per thread), then block row i from T_ij = -T_ii sum_k L_ik T_kj,
-// with 2 x 4 register tiles.
+// In-place inverse of I + L_h for both heads (two warps per head): 16 x 16 diagonal blocks by forward
+// substitution (one column per thread), then block row i from X_ij = sum_k L_ik T_kj and
+// T_ij = -T_ii X_ij.  Each warp computes whole 16 x 16 blocks (uniform control flow); lane = 2 x 4 tile
+// (rows rp, rp + 8; columns c4 .. c4 + 3), which keeps the shared-memory reads conflict-free.
+__device__ __forceinline__ void block_tile_product(const float* A, int a_stride, const float* B, int b_stride,
+                                                   int rp, int c4, float4& acc0, float4& acc1) {
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        const float l0 = A[rp * a_stride + s], l1 = A[(rp + 8) * a_stride + s];
+        const float4 tv = *reinterpret_cast<const float4*>(B + s * b_stride + c4);
+        acc0.x = fmaf(l0, tv.x, acc0.x); acc0.y = fmaf(l0, tv.y, acc0.y);
+        acc0.z = fmaf(l0, tv.z, acc0.z); acc0.w = fmaf(l0, tv.w, acc0.w);
+        acc1.x = fmaf(l1, tv.x, acc1.x); acc1.y = fmaf(l1, tv.y, acc1.y);
+        acc1.z = fmaf(l1, tv.z, acc1.z); acc1.w = fmaf(l1, tv.w, acc1.w);
+    }
+}
+
 __device__ __forceinline__ void blocked_unit_lower_inverse(float* sLC, float* sX, int tid) {
-    const int h = tid >> 6, t = tid & 63;
+    const int h = tid >> 6, t = tid & 63, hw = t >> 5, lane = t & 31;
     float* L = sLC + h * 10 * P_LBLK;
     float* X = sX + h * 16 * 48;
     {
@@ -123,44 +137,24 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(float* sLC, float* sX
         for (int r = 0; r < 16; ++r) D[r * 20 + j] = tc[r];
         __syncthreads();
     }
+    const int rp = lane >> 2, c4 = (lane & 3) * 4;
 #pragma unroll
     for (int i = 1; i < 4; ++i) {
-        const int ncq = 4 * i;                       // column quads of block row i
-        for (int tile = t; tile < 8 * ncq; tile += 64) {
-            const int cq = tile % ncq, rp = tile / ncq;
-            const int jb = cq >> 2, c4 = (cq & 3) * 4;
+        // blocks of block row i handled by this warp: warp 0 takes jb = 0, warp 1 the rest
+        // (balances the products: i = 3 gives 3 + (2 + 1))
+        const int jb_lo = hw == 0 ? 0 : 1, jb_hi = hw == 0 ? 1 : i;
+        for (int jb = jb_lo; jb < jb_hi && jb < i; ++jb) {
             float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-            for (int k = jb; k < i; ++k) {
-                const float* Lik = L + lblk(i, k) * P_LBLK;
-                const float* Tkj = L + lblk(k, jb) * P_LBLK + c4;
-#pragma unroll
-                for (int s = 0; s < 16; ++s) {
-                    const float l0 = Lik[rp * 20 + s], l1 = Lik[(rp + 8) * 20 + s];
-                    const float4 tv = *reinterpret_cast<const float4*>(Tkj + s * 20);
-                    acc0.x = fmaf(l0, tv.x, acc0.x); acc0.y = fmaf(l0, tv.y, acc0.y);
-                    acc0.z = fmaf(l0, tv.z, acc0.z); acc0.w = fmaf(l0, tv.w, acc0.w);
-                    acc1.x = fmaf(l1, tv.x, acc1.x); acc1.y = fmaf(l1, tv.y, acc1.y);
-                    acc1.z = fmaf(l1, tv.z, acc1.z); acc1.w = fmaf(l1, tv.w, acc1.w);
-                }
-            }
+            for (int k = jb; k < i; ++k)
+                block_tile_product(L + lblk(i, k) * P_LBLK, 20, L + lblk(k, jb) * P_LBLK, 20, rp, c4, acc0, acc1);
             *reinterpret_cast<float4*>(X + rp * 48 + 16 * jb + c4) = acc0;
             *reinterpret_cast<float4*>(X + (rp + 8) * 48 + 16 * jb + c4) = acc1;
         }
         __syncthreads();
         const float* Tii = L + lblk(i, i) * P_LBLK;
-        for (int tile = t; tile < 8 * ncq; tile += 64) {
-            const int cq = tile % ncq, rp = tile / ncq;
-            const int jb = cq >> 2, c4 = (cq & 3) * 4;
+        for (int jb = jb_lo; jb < jb_hi && jb < i; ++jb) {
             float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-#pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const float l0 = Tii[rp * 20 + s], l1 = Tii[(rp + 8) * 20 + s];
-                const float4 xv = *reinterpret_cast<const float4*>(X + s * 48 + 16 * jb + c4);
-                acc0.x = fmaf(l0, xv.x, acc0.x); acc0.y = fmaf(l0, xv.y, acc0.y);
-                acc0.z = fmaf(l0, xv.z, acc0.z); acc0.w = fmaf(l0, xv.w, acc0.w);
-                acc1.x = fmaf(l1, xv.x, acc1.x); acc1.y = fmaf(l1, xv.y, acc1.y);
-                acc1.z = fmaf(l1, xv.z, acc1.z); acc1.w = fmaf(l1, xv.w, acc1.w);
-            }
+            block_tile_product(Tii, 20, X + 16 * jb, 48, rp, c4, acc0, acc1);
             float* Tij = L + lblk(i, jb) * P_LBLK + c4;
             *reinterpret_cast<float4*>(Tij + rp * 20) = make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w);
             *reinterpret_cast<float4*>(Tij + (rp + 8) * 20) = make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w);
@@ -197,6 +191,19 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (!slot_lookup(cu, nseq, T_len, slot, seq, t0, n)) return;  // unused slot (uniform per CTA)
     const int h0 = 2 * pair;
     const int hk = h0 / (Hv / Hqk);
+    // gates of value head h0 + warp (warps 0-1), two tokens per lane; padded tokens get g = beta = 0
+    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+    if (warp < 2) {
+        const int r0 = 2 * lane, r1 = 2 * lane + 1;
+        if (r0 < n) {
+            g0 = __bfloat162float(g[(size_t)(t0 + r0) * Hv + h0 + warp]);
+            b0 = __bfloat162float(beta[(size_t)(t0 + r0) * Hv + h0 + warp]);
+        }
+        if (r1 < n) {
+            g1 = __bfloat162float(g[(size_t)(t0 + r1) * Hv + h0 + warp]);
+            b1 = __bfloat162float(beta[(size_t)(t0 + r1) * Hv + h0 + warp]);
+        }
+    }
 
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), 256);
@@ -220,18 +227,9 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tma_load_3d(sb + P_KQ + p * 16384 + 8192, &tm_q, 64 * p, hk, (int)t0, bar_tma);
         }
     }
-    if (warp < 2) {   // gates of value head h0 + warp; padded tokens get g = beta = 0; G = inclusive scan of g
+    if (warp < 2) {   // G = inclusive scan of g over the chunk
         const int hh = warp;
-        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
         const int r0 = 2 * lane, r1 = 2 * lane + 1;
-        if (r0 < n) {
-            g0 = __bfloat162float(g[(size_t)(t0 + r0) * Hv + h0 + hh]);
-            b0 = __bfloat162float(beta[(size_t)(t0 + r0) * Hv + h0 + hh]);
-        }
-        if (r1 < n) {
-            g1 = __bfloat162float(g[(size_t)(t0 + r1) * Hv + h0 + hh]);
-            b1 = __bfloat162float(beta[(size_t)(t0 + r1) * Hv + h0 + hh]);
-        }
         float p = g0 + g1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -434,6 +432,13 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         qrow[c] = *reinterpret_cast<const uint4*>(sm + P_KQ + (c >> 3) * 16384 + 8192 + swz(r, c & 7));
     mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
+    if (tid == 0) {   // the [-W | Tb] rows of A1 are final: start their stores now
+        for (int h = 0; h < 2; ++h) {
+            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + h0 + h) * kA1Bytes;
+            for (int p = 0; p < 3; ++p) bulk_s2g(dst + p * 16384, sb + P_TOP + p * 16384 + h * 8192, 8192);
+        }
+        bulk_commit();
+    }
     __syncthreads();   // every thread holds its q row: the K/Q panels are free
     {
         const float qs = scale * __expf(sG[hh * 64 + r]);   // scale * gamma_r
@@ -464,10 +469,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (tid == 0) {   // A1 of each head: panel p = [TOP rows of the head | output rows of the head]
         for (int h = 0; h < 2; ++h) {
             uint8_t* dst = ws_a1 + ((size_t)slot * Hv + h0 + h) * kA1Bytes;
-            for (int p = 0; p < 3; ++p) {
-                bulk_s2g(dst + p * 16384, sb + P_TOP + p * 16384 + h * 8192, 8192);
-                bulk_s2g(dst + p * 16384 + 8192, sb + bot_panel(3 * h + p), 8192);
-            }
+            for (int p = 0; p < 3; ++p) bulk_s2g(dst + p * 16384 + 8192, sb + bot_panel(3 * h + p), 8192);
         }
         bulk_commit();
         bulk_wait_read();   // shared memory may be released; the global writes finish on their own
