@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(_HERE, "libgdn.so")
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT, GDN_ERR_WORKSPACE = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_NORMALIZE_QK = 0x1
+GDN_RAW_GATES = 0x2
 
 EXPORTED = ("gdn_opts_init", "gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step",
             "gdn_check_device_status", "gdn_status_string", "gdn_last_error", "gdn_version",
@@ -32,6 +33,8 @@ class GdnOpts(ctypes.Structure):
         ("stream", ctypes.c_void_p),
         ("events", ctypes.POINTER(ctypes.c_void_p)),
         ("num_events", ctypes.c_int),
+        ("A_log", ctypes.c_void_p),
+        ("dt_bias", ctypes.c_void_p),
     ]
 
 

@@ -39,12 +39,19 @@ def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
     return int(s.cuda_stream)
 
 
-def _opts(lib, dtype, scale, chunk, normalize_qk, stream, device, events):
+def _opts(lib, dtype, scale, chunk, normalize_qk, stream, device, events, raw_gates=None, Hv=None):
     o = L.default_opts(lib)
     o.dtype = _DTYPES[dtype]
     o.chunk = int(chunk)
     o.scale = float(scale)
     o.flags = L.GDN_NORMALIZE_QK if normalize_qk else 0
+    if raw_gates is not None:
+        A_log, dt_bias = raw_gates
+        _need("A_log", A_log, torch.float32, device, (Hv,))
+        _need("dt_bias", dt_bias, torch.float32, device, (Hv,))
+        o.flags |= L.GDN_RAW_GATES
+        o.A_log = A_log.data_ptr()
+        o.dt_bias = dt_bias.data_ptr()
     o.stream = _stream_handle(stream, device)
     keep = None
     if events:
@@ -72,10 +79,13 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   normalize_qk: bool = False, cu_seqlens: Optional[torch.Tensor] = None,
                   out: Optional[torch.Tensor] = None, S_final: Optional[torch.Tensor] = None,
                   output_final_state: bool = True, workspace: Optional[torch.Tensor] = None,
-                  stream: Optional[torch.cuda.Stream] = None, events: Optional[Sequence[int]] = None):
+                  stream: Optional[torch.cuda.Stream] = None, events: Optional[Sequence[int]] = None,
+                  raw_gates=None):
     """Chunked prefill.  q, k [B, T, Hqk, dk]; v [B, T, Hv, dv]; g, beta [B, T, Hv] (all bf16 or all
     fp32, on one CUDA device); S0 [nseq, Hv, dk, dv] fp32 or None.  With ``cu_seqlens`` (int32 device
-    tensor of nseq+1 offsets) B must be 1.  Returns (out [B, T, Hv, dv], S_final or None)."""
+    tensor of nseq+1 offsets) B must be 1.  With ``raw_gates=(A_log, dt_bias)`` (fp32 [Hv] each), g and
+    beta are the raw projections a and b and the kernels form the gates.
+    Returns (out [B, T, Hv, dv], S_final or None)."""
     lib = L.load()
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D [B, T, H, d]")
@@ -105,7 +115,7 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     if S_final is not None:
         _need("S_final", S_final, torch.float32, dev, (nseq, Hv, dk, dv))
     with torch.cuda.device(dev):
-        o, keep = _opts(lib, dt, scale, chunk, normalize_qk, stream, dev, events)
+        o, keep = _opts(lib, dt, scale, chunk, normalize_qk, stream, dev, events, raw_gates, Hv)
         if cu_seqlens is not None:
             o.cu_seqlens = cu_seqlens.data_ptr()
             o.num_seqs = nseq
@@ -125,9 +135,9 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
 def gdn_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
                        S: torch.Tensor, *, scale: float = 1.0, normalize_qk: bool = False,
                        out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
-                       events: Optional[Sequence[int]] = None) -> torch.Tensor:
+                       events: Optional[Sequence[int]] = None, raw_gates=None) -> torch.Tensor:
     """One decode step.  q, k [N, Hqk, dk]; v [N, Hv, dv]; g, beta [N, Hv]; S [N, Hv, dk, dv] fp32 is
-    updated in place.  Returns out [N, Hv, dv]."""
+    updated in place.  ``raw_gates`` as for gdn_chunk_fwd.  Returns out [N, Hv, dv]."""
     lib = L.load()
     if q.dim() != 3 or v.dim() != 3:
         raise ValueError("q, k, v must be 3-D [N, H, d]")
@@ -146,7 +156,7 @@ def gdn_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: tor
         out = torch.empty_like(v)
     _need("out", out, dt, dev, (N, Hv, dv))
     with torch.cuda.device(dev):
-        o, keep = _opts(lib, dt, scale, 64, normalize_qk, stream, dev, events)
+        o, keep = _opts(lib, dt, scale, 64, normalize_qk, stream, dev, events, raw_gates, Hv)
         st = lib.gdn_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), _ptr(out),
                                     N, Hqk, Hv, dk, dv, ctypes.byref(o))
         del keep

@@ -84,7 +84,9 @@ gdn_status_t check_common(int Hqk, int Hv, int dk, int dv, const gdn_opts_t& o) 
     if (Hv % Hqk != 0) return fail(GDN_ERR_INVALID_ARG, "Hv (%d) must be a multiple of Hqk (%d)", Hv, Hqk);
     if (dk <= 0 || dv <= 0) return fail(GDN_ERR_INVALID_ARG, "head dims must be positive");
     if (o.dtype != GDN_F32 && o.dtype != GDN_BF16) return fail(GDN_ERR_INVALID_ARG, "unknown dtype %d", o.dtype);
-    if (o.flags & ~GDN_NORMALIZE_QK) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", o.flags);
+    if (o.flags & ~(GDN_NORMALIZE_QK | GDN_RAW_GATES)) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", o.flags);
+    if ((o.flags & GDN_RAW_GATES) && (!o.A_log || !o.dt_bias || !aligned_to(o.A_log, 4) || !aligned_to(o.dt_bias, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "GDN_RAW_GATES needs aligned A_log and dt_bias");
     if (o.num_events < 0 || (o.num_events > 0 && !o.events)) return fail(GDN_ERR_INVALID_ARG, "bad event list");
     if (!dim_ok(dk) || !dim_ok(dv)) return fail(GDN_ERR_UNSUPPORTED, "head dims dk=%d dv=%d not in {32,64,128}", dk, dv);
     return GDN_OK;
@@ -186,6 +188,7 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const vo
     a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq;
     a.workspace = o.workspace; a.workspace_bytes = o.workspace_bytes;
     a.stream = stream; a.status = status;
+    a.A_log = o.A_log; a.dt_bias = o.dt_bias;
 
     cudaError_t e;
     if (tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk, o.flags)) {
@@ -228,6 +231,7 @@ gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, con
     a.N = N; a.Hqk = Hqk; a.Hv = Hv; a.dk = dk; a.dv = dv;
     a.dtype = o.dtype; a.scale = o.scale; a.flags = o.flags;
     a.stream = static_cast<cudaStream_t>(o.stream);
+    a.A_log = o.A_log; a.dt_bias = o.dt_bias;
     record(o, 0, a.stream);
     cudaError_t e = launch_decode(a);
     record(o, 1, a.stream);

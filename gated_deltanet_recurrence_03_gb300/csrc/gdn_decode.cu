@@ -6,6 +6,7 @@
 //     u = beta (v - a p)               (the delta written for this token)
 //     S <- a S + k u^T                 (one write)
 //     o = scale (a r + (k . q) u)      (= scale S_new^T q, expanded so the state is read once)
+// With GDN_RAW_GATES, g and beta hold the raw projections and the gates are formed here.
 //
 // One CTA of 256 threads owns one (n, h) table.  Thread (row group rg, column lane lx) holds
 // rows rg*RPT .. rg*RPT+RPT-1 and four adjacent columns 4*lx .. 4*lx+3 in registers; the loads
@@ -22,7 +23,8 @@ template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kDecThreads, 2)
 decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const T* __restrict__ g, const T* __restrict__ beta, float* __restrict__ S,
-                   T* __restrict__ out, int Hqk, int Hv, float scale, int normalize) {
+                   T* __restrict__ out, int Hqk, int Hv, float scale, int normalize,
+                   const float* __restrict__ A_log, const float* __restrict__ dt_bias) {
     constexpr int LX = DV / 4;                 // column lanes (float4 each)
     constexpr int RG = kDecThreads / LX;       // row groups
     constexpr int RPT = DK / RG;               // rows per thread
@@ -54,8 +56,9 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
         sk[i] = to_f32(kp[i]);
     }
     for (int j = tid; j < DV; j += kDecThreads) sv[j] = to_f32(v[(size_t)nh * DV + j]);
-    const float alpha = __expf(to_f32(g[nh]));
-    const float bt = to_f32(beta[nh]);
+    float gt = to_f32(g[nh]), bt = to_f32(beta[nh]);
+    if (A_log) gates_from_raw(gt, bt, A_log[h], dt_bias[h], gt, bt);   // raw projections a, b
+    const float alpha = __expf(gt);
     __syncthreads();
 
     if (tid < 32) {                            // k.q and, if asked, the norms of k and q
@@ -129,7 +132,8 @@ cudaError_t launch_typed(const DecodeArgs& a) {
     decode_step_kernel<DK, DV, T><<<blocks, kDecThreads, 0, a.stream>>>(
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
         static_cast<const T*>(a.g), static_cast<const T*>(a.beta), a.S, static_cast<T*>(a.out), a.Hqk,
-        a.Hv, a.scale, (a.flags & GDN_NORMALIZE_QK) ? 1 : 0);
+        a.Hv, a.scale, (a.flags & GDN_NORMALIZE_QK) ? 1 : 0, (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr,
+        a.dt_bias);
     return cudaGetLastError();
 }
 

@@ -36,6 +36,8 @@ struct PrefillArgs {
     size_t workspace_bytes;
     cudaStream_t stream;
     unsigned* status;           // device status word
+    const float* A_log;         // GDN_RAW_GATES
+    const float* dt_bias;
 };
 
 struct DecodeArgs {
@@ -51,6 +53,8 @@ struct DecodeArgs {
     float scale;
     unsigned flags;
     cudaStream_t stream;
+    const float* A_log;         // GDN_RAW_GATES
+    const float* dt_bias;
 };
 
 // Launchers (return the launch error, cudaSuccess if enqueued).
@@ -79,6 +83,16 @@ template <>
 __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Gates of the GatedDeltaNet shell ("Transformer by Hand, ch. 7", listing "qwen/deltanet.py",
+// GatedDeltaNet.forward): beta = sigmoid(b), g = -exp(A_log) * softplus(a + dt_bias), with
+// softplus(x) = max(x, 0) + log(1 + exp(-|x|)).
+__device__ __forceinline__ void gates_from_raw(float a, float b, float A_log, float dt_bias, float& g, float& beta) {
+    const float x = a + dt_bias;
+    const float sp = fmaxf(x, 0.f) + log1pf(__expf(-fabsf(x)));
+    g = -__expf(A_log) * sp;
+    beta = 1.f / (1.f + __expf(-b));
+}
 
 // Sequence i's token range [t0, t1) in the flattened token index.
 __device__ __forceinline__ void seq_range(const int32_t* cu, int i, int T, long long& t0, long long& t1) {

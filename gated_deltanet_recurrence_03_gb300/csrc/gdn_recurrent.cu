@@ -24,7 +24,7 @@ recurrent_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k, const
                          const T* __restrict__ g, const T* __restrict__ beta,
                          const float* __restrict__ S0, T* __restrict__ out, float* __restrict__ S_final,
                          const int32_t* __restrict__ cu, int T_len, int Hqk, int Hv, float scale,
-                         int normalize) {
+                         int normalize, const float* __restrict__ A_log, const float* __restrict__ dt_bias) {
     constexpr int SPLIT = DK / 32;           // adjacent lanes sharing one column, 32 rows each
     constexpr int NT = DV * SPLIT;           // threads
     constexpr int NW = NT / 32;
@@ -63,8 +63,10 @@ recurrent_prefill_kernel(const T* __restrict__ q, const T* __restrict__ k, const
             sv[tt][c] = to_f32(v[((size_t)(tb + tt) * Hv + h) * DV + c]);
         }
         if (tid < nt) {
-            sa[tid] = __expf(to_f32(g[(size_t)(tb + tid) * Hv + h]));
-            sb[tid] = to_f32(beta[(size_t)(tb + tid) * Hv + h]);
+            float gt = to_f32(g[(size_t)(tb + tid) * Hv + h]), bt = to_f32(beta[(size_t)(tb + tid) * Hv + h]);
+            if (A_log) gates_from_raw(gt, bt, A_log[h], dt_bias[h], gt, bt);   // raw projections a, b
+            sa[tid] = __expf(gt);
+            sb[tid] = bt;
         }
         __syncthreads();
         for (int tt = warp; tt < nt; tt += NW) {   // one warp per token: norms and k.q
@@ -137,7 +139,8 @@ cudaError_t launch_typed(const PrefillArgs& a) {
     recurrent_prefill_kernel<DK, DV, T><<<blocks, DV * (DK / 32), 0, a.stream>>>(
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
         static_cast<const T*>(a.g), static_cast<const T*>(a.beta), a.S0, static_cast<T*>(a.out),
-        a.S_final, a.cu_seqlens, T_len, a.Hqk, a.Hv, a.scale, (a.flags & GDN_NORMALIZE_QK) ? 1 : 0);
+        a.S_final, a.cu_seqlens, T_len, a.Hqk, a.Hv, a.scale, (a.flags & GDN_NORMALIZE_QK) ? 1 : 0,
+        (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr, a.dt_bias);
     return cudaGetLastError();
 }
 

@@ -81,8 +81,8 @@ constexpr uint32_t P_X = P_TOP;         // blocked-solve scratch X [2][16][48] f
 constexpr uint32_t P_HANDOFF = P_TOP + 16384;   // P_0 rows, bf16 [64][64] (panel 1, before -W)
 constexpr uint32_t P_LC = 81920;        // L_h then T_h: 10 lower blocks of 16 x 16 fp32 per head, row stride 20
 constexpr uint32_t P_LBLK = 16 * 20;    // floats per block
-constexpr uint32_t P_SMALL = P_LC + 2 * 10 * P_LBLK * 4;   // G, beta, beta*gamma, a, c: [2][64] each
-constexpr uint32_t P_BAR = P_SMALL + 5 * 2 * 64 * 4;
+constexpr uint32_t P_SMALL = P_LC + 2 * 10 * P_LBLK * 4;   // G, beta, beta*gamma, a, c: [2][64] each; 1/|k|, 1/|q|: [64]
+constexpr uint32_t P_BAR = P_SMALL + 5 * 2 * 64 * 4 + 2 * 64 * 4;
 constexpr uint32_t P_SMEM = P_BAR + 64 + 1024;  // + alignment slack
 constexpr int kPrepThreads = 128;
 // TMEM columns: Gram D 0-63; T diag(beta gamma) (A operand) 0-31 after the Gram is read;
@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const bf16* __restrict__ g, const bf16* __restrict__ beta, const int32_t* __restrict__ cu,
                int nseq, int T_len, int Hqk, int Hv, float scale, uint8_t* __restrict__ ws_a1,
-               float* __restrict__ ws_vec, unsigned* status) {
+               float* __restrict__ ws_vec, unsigned* status, const float* __restrict__ A_log,
+               const float* __restrict__ dt_bias, int normalize) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
@@ -176,6 +177,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float* sBG = sG + 256;                                // [2][64] beta_r * gamma_r
     float* sA = sG + 384;                                 // [2][64] exp(G_r - G_0)
     float* sC = sG + 512;                                 // [2][64] exp(G_0 - G_s)
+    float* sRK = sG + 640;                                // [64] 1/|k_r| (1 unless normalising)
+    float* sRQ = sG + 704;                                // [64] 1/|q_r|
     float* sLC = reinterpret_cast<float*>(sm + P_LC);
     const uint32_t bar_tma = sb + P_BAR, bar_mma = sb + P_BAR + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P_BAR + 16);
@@ -202,6 +205,11 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (r1 < n) {
             g1 = __bfloat162float(g[(size_t)(t0 + r1) * Hv + h0 + warp]);
             b1 = __bfloat162float(beta[(size_t)(t0 + r1) * Hv + h0 + warp]);
+        }
+        if (A_log) {   // raw projections a, b: form the gates (padded tokens keep g = beta = 0)
+            const float al = A_log[h0 + warp], db = dt_bias[h0 + warp];
+            if (r0 < n) gates_from_raw(g0, b0, al, db, g0, b0);
+            if (r1 < n) gates_from_raw(g1, b1, al, db, g1, b1);
         }
     }
 
@@ -251,7 +259,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         sA[hh * 64 + r] = __expf(Gr - G0);
         sC[hh * 64 + r] = __expf(G0 - Gr);
         float* vec = ws_vec + ((size_t)slot * Hv + h0 + hh) * kVecFloats;
-        vec[r] = __expf(Gl - Gr);
+        if (!normalize) vec[r] = __expf(Gl - Gr);   // with normalisation: written once 1/|k_r| is known
         if (r == 0) vec[64] = __expf(Gl);
     }
 
@@ -274,11 +282,39 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_ld32(tl + T_GRAM, *reinterpret_cast<uint32_t(*)[32]>(a));
         tmem_ld32(tl + T_GRAM + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
         tmem_wait_ld();
+        if (normalize) {   // l2 normalisation of q and k folded into per-row scalars (eps 1e-6)
+            if (warp < 2) {
+                float kk = 0.f;   // k_r . k_r is the diagonal of K K^T
+#pragma unroll
+                for (int s = 0; s < 64; ++s) kk = (s == R) ? __uint_as_float(a[s]) : kk;
+                const float rk = rsqrtf(kk + 1e-6f);
+                sRK[R] = rk;
+                for (int hh = 0; hh < 2; ++hh) {
+                    ws_vec[((size_t)slot * Hv + h0 + hh) * kVecFloats + R] = __expf(sG[hh * 64 + 63] - sG[hh * 64 + R]) * rk;
+                    sBG[hh * 64 + R] *= rk;
+                }
+            } else {
+                const int r = R - 64;
+                float qq = 0.f;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + P_KQ + (c >> 3) * 16384 + 8192 + swz(r, c & 7));
+                    const bf16* qe = reinterpret_cast<const bf16*>(&qv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qq = fmaf(__bfloat162float(qe[e]), __bfloat162float(qe[e]), qq);
+                }
+                sRQ[r] = rsqrtf(qq + 1e-6f);
+            }
+        } else if (tid < 64) {
+            sRK[tid] = 1.f;
+            sRQ[tid] = 1.f;
+        }
+        __syncthreads();
         if (warp < 2) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s (s < r), lower blocks
             const int r = R, I = r >> 4, rr = r & 15;
             for (int hh = 0; hh < 2; ++hh) {
                 const float* Gh = sG + hh * 64;
-                const float br = sBeta[hh * 64 + r], ar = sA[hh * 64 + r], Gr = Gh[r];
+                const float br = sBeta[hh * 64 + r] * sRK[r], ar = sA[hh * 64 + r], Gr = Gh[r];
                 const float* ch = sC + hh * 64;
                 const bool fac = sFactor[hh] != 0;
                 float* Lh = sLC + hh * 10 * P_LBLK;
@@ -290,7 +326,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int s = 16 * J + 4 * s4 + e;
-                            const float kk = __uint_as_float(a[s]);
+                            const float kk = __uint_as_float(a[s]) * sRK[s];
                             const float dec = fac ? ar * ch[s] : __expf(Gr - Gh[s]);
                             o[e] = (s < r) ? br * dec * kk : 0.f;
                         }
@@ -300,6 +336,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         } else {          // row r of Q K^T -> P_h[r][s] = scale exp(G_r - G_s) q_r.k_s (s <= r)
             const int r = R - 64;
+            const float sq = scale * sRQ[r];
             for (int hh = 0; hh < 2; ++hh) {
                 const float* Gh = sG + hh * 64;
                 const float ar = sA[hh * 64 + r], Gr = Gh[r];
@@ -313,7 +350,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int f = 0; f < 2; ++f) {
                         const int s = 2 * e + f;
                         const float dec = fac ? ar * ch[s] : __expf(Gr - Gh[s]);
-                        pv[f] = (s <= r) ? scale * dec * __uint_as_float(a[s]) : 0.f;
+                        pv[f] = (s <= r) ? sq * dec * __uint_as_float(a[s]) * sRK[s] : 0.f;
                     }
                     w[e] = pack_bf16(pv[0], pv[1]);
                 }
@@ -441,7 +478,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     __syncthreads();   // every thread holds its q row: the K/Q panels are free
     {
-        const float qs = scale * __expf(sG[hh * 64 + r]);   // scale * gamma_r
+        const float qs = scale * __expf(sG[hh * 64 + r]) * sRQ[r];   // scale * gamma_r / |q_r|
         for (int cb = 0; cb < 6; ++cb) {
             uint32_t a[32];
             tmem_ld32(tl + T_PW + 32 * cb, a);
@@ -773,8 +810,8 @@ void record_event(void** events, int num_events, int idx, cudaStream_t s) {
 }  // namespace
 
 bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk, unsigned flags) {
-    return dtype == GDN_BF16 && dk == kD && dv == kD && chunk == kC && (Hv / Hqk) % 2 == 0 &&
-           !(flags & GDN_NORMALIZE_QK);
+    (void)flags;   // normalisation and raw gates are handled inside the kernels
+    return dtype == GDN_BF16 && dk == kD && dv == kD && chunk == kC && (Hv / Hqk) % 2 == 0;
 }
 
 size_t tc_prefill_workspace_bytes(int B, int T, int Hv, int num_seqs, bool packed) {
@@ -813,7 +850,8 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
     record_event(events, num_events, 0, a.stream);
     tc_prep_kernel<<<dim3((unsigned)slots, (unsigned)(a.Hv / 2)), kPrepThreads, P_SMEM, a.stream>>>(
         tq, tk, static_cast<const bf16*>(a.g), static_cast<const bf16*>(a.beta), a.cu_seqlens, a.num_seqs, T_len,
-        a.Hqk, a.Hv, a.scale, ws_a1, ws_vec, a.status);
+        a.Hqk, a.Hv, a.scale, ws_a1, ws_vec, a.status, (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr, a.dt_bias,
+        (a.flags & GDN_NORMALIZE_QK) ? 1 : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     record_event(events, num_events, 1, a.stream);
     tc_chain_kernel<<<(unsigned)((long long)a.num_seqs * a.Hv * kSlices), kChainThreads, C_SMEM, a.stream>>>(

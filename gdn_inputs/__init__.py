@@ -32,6 +32,11 @@ Distributions (the workloads' recipe)
 
 Draw order (stream index): q 0, k 1, v 2, a 3, b 4, S0 5.
 
+Raw gate projections (for kernels that form the gates themselves): a_raw, b_raw ~ N(0, 1) in the
+storage dtype (streams 6, 7); per value head A_log ~ N(-0.5, 0.5) and dt_bias ~ N(0, 0.5) in fp32
+(streams 8, 9), which puts exp(A_log) and the decay in the ranges the handbook reports on real
+input.
+
 Rounding to the storage dtype: fp64 -> fp32 round-to-nearest-even; for bf16 the
 fp32 value is rounded again to bf16 (round-to-nearest-even on the fp32 bits).
 Arrays are returned as float32 holding exactly the stored values, so a caller can
@@ -68,6 +73,7 @@ _STREAM_STRIDE = 1 << 40
 _CHUNK = 1 << 22  # values generated per numpy batch (bounds temporary memory)
 
 STREAM_Q, STREAM_K, STREAM_V, STREAM_A, STREAM_B, STREAM_S0 = range(6)
+STREAM_RAW_A, STREAM_RAW_B, STREAM_A_LOG, STREAM_DT_BIAS = range(6, 10)
 
 
 def splitmix64(seed: int, idx: np.ndarray) -> np.ndarray:
@@ -267,3 +273,14 @@ def make_decode_inputs(w: Workload, steps: Optional[int] = None):
 def scaled(w: Workload, **changes) -> Workload:
     """A copy of ``w`` with some fields changed (smaller shapes for quick checks)."""
     return dataclasses.replace(w, **changes)
+
+
+def make_raw_gates(w: Workload, lead_shape=None):
+    """Raw gate projections a, b [*lead_shape, Hv] (rounded to the workload dtype) and per-head
+    A_log, dt_bias [Hv] fp32.  lead_shape defaults to (B, T)."""
+    lead = (w.B, w.T) if lead_shape is None else tuple(lead_shape)
+    a = _rounded_normal(w.seed, STREAM_RAW_A, (*lead, w.Hv), w.dtype)
+    b = _rounded_normal(w.seed, STREAM_RAW_B, (*lead, w.Hv), w.dtype)
+    A_log = round_to_dtype(_normal_tensor(w.seed, STREAM_A_LOG, (w.Hv,), mean=-0.5, std=0.5), "f32")
+    dt_bias = round_to_dtype(_normal_tensor(w.seed, STREAM_DT_BIAS, (w.Hv,), std=0.5), "f32")
+    return dict(a=a, b=b, A_log=A_log, dt_bias=dt_bias)

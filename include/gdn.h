@@ -60,6 +60,10 @@ typedef enum gdn_dtype {
 /* opts->flags */
 #define GDN_NORMALIZE_QK 0x1u /* divide q and k by sqrt(sum x^2 + 1e-6) inside the kernel
                                  (the l2norm step of delta_rule); off: inputs are used as given */
+#define GDN_RAW_GATES 0x2u    /* the g and beta arguments hold the raw per-token projections a and b of
+                                 the GatedDeltaNet shell ("qwen/deltanet.py", forward): the kernels form
+                                 beta = sigmoid(b) and g = -exp(A_log[h]) * softplus(a + dt_bias[h]) in
+                                 fp32; opts->A_log and opts->dt_bias ([Hv] float) are then required */
 
 typedef struct gdn_opts {
     int dtype;                  /* gdn_dtype_t of q, k, v, g, beta, out.  Default GDN_BF16. */
@@ -78,6 +82,8 @@ typedef struct gdn_opts {
                                    the first kernel of the call and events[i] after kernel i
                                    (kernel-level timing); NULL = none */
     int num_events;
+    const float* A_log;         /* [Hv] per-head log forgetting speed (GDN_RAW_GATES), DEVICE */
+    const float* dt_bias;       /* [Hv] per-head bias added to a (GDN_RAW_GATES), DEVICE */
 } gdn_opts_t;
 
 /* Fill *opts with the defaults listed above. */

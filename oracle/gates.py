@@ -1,0 +1,32 @@
+"""Gates of the GatedDeltaNet shell in fp64.  TEST INFRASTRUCTURE.
+
+Only the tests use this module.  "Transformer by Hand, ch. 7", listing "qwen/deltanet.py",
+GatedDeltaNet.forward, and the parts table below it:
+    beta = sigmoid(in_proj_b(x))                                   write strength in (0, 1)
+    g    = -exp(A_log) * softplus(in_proj_a(x) + dt_bias)          log decay, always <= 0
+Here a = in_proj_a(x) and b = in_proj_b(x) are given directly (the projections need trained
+weights and are out of scope).  softplus and sigmoid are numpy's logaddexp and an overflow-safe
+logistic.
+"""
+import numpy as np
+
+
+def softplus(x):
+    """log(1 + e^x)."""
+    return np.logaddexp(0.0, np.asarray(x, dtype=np.float64))
+
+
+def sigmoid(x):
+    x = np.asarray(x, dtype=np.float64)
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def gates_from_raw(a, b, A_log, dt_bias):
+    """a, b [..., Hv]; A_log, dt_bias [Hv].  Returns (g, beta) in fp64."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    A_log = np.asarray(A_log, dtype=np.float64)
+    dt_bias = np.asarray(dt_bias, dtype=np.float64)
+    g = -np.exp(A_log) * softplus(a + dt_bias)
+    return g, sigmoid(b)

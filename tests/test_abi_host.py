@@ -70,6 +70,7 @@ def prefill(lib, B=1, T=8, Hqk=1, Hv=1, dk=32, dv=32, ptrs=None, **kw):
     (dict(chunk=128), pkg_lib.GDN_ERR_UNSUPPORTED),
     (dict(dtype=7), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(flags=0x80), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(flags=pkg_lib.GDN_RAW_GATES), pkg_lib.GDN_ERR_INVALID_ARG),   # A_log / dt_bias missing
     (dict(ptrs=[FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(ptrs=[FAKE + 8] + [FAKE] * 7), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(ptrs=[FAKE] * 3 + [FAKE + 1] + [FAKE] * 4), pkg_lib.GDN_ERR_INVALID_ARG),
