@@ -14,6 +14,7 @@ GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT,
 GDN_F32, GDN_BF16 = 0, 1
 GDN_NORMALIZE_QK = 0x1
 GDN_RAW_GATES = 0x2
+GDN_OUTPUT_GATE = 0x4
 
 EXPORTED = ("gdn_opts_init", "gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step",
             "gdn_check_device_status", "gdn_status_string", "gdn_last_error", "gdn_version",
@@ -35,6 +36,9 @@ class GdnOpts(ctypes.Structure):
         ("num_events", ctypes.c_int),
         ("A_log", ctypes.c_void_p),
         ("dt_bias", ctypes.c_void_p),
+        ("z", ctypes.c_void_p),
+        ("norm_weight", ctypes.c_void_p),
+        ("norm_eps", ctypes.c_float),
     ]
 
 

@@ -39,7 +39,8 @@ def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
     return int(s.cuda_stream)
 
 
-def _opts(lib, dtype, scale, chunk, normalize_qk, stream, device, events, raw_gates=None, Hv=None):
+def _opts(lib, dtype, scale, chunk, normalize_qk, stream, device, events, raw_gates=None, Hv=None,
+          output_gate=None, out_shape=None):
     o = L.default_opts(lib)
     o.dtype = _DTYPES[dtype]
     o.chunk = int(chunk)
@@ -52,6 +53,14 @@ def _opts(lib, dtype, scale, chunk, normalize_qk, stream, device, events, raw_ga
         o.flags |= L.GDN_RAW_GATES
         o.A_log = A_log.data_ptr()
         o.dt_bias = dt_bias.data_ptr()
+    if output_gate is not None:
+        z, weight, eps = output_gate
+        _need("z", z, dtype, device, out_shape)
+        _need("norm_weight", weight, torch.float32, device, (out_shape[-1],))
+        o.flags |= L.GDN_OUTPUT_GATE
+        o.z = z.data_ptr()
+        o.norm_weight = weight.data_ptr()
+        o.norm_eps = float(eps)
     o.stream = _stream_handle(stream, device)
     keep = None
     if events:
@@ -80,12 +89,13 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   out: Optional[torch.Tensor] = None, S_final: Optional[torch.Tensor] = None,
                   output_final_state: bool = True, workspace: Optional[torch.Tensor] = None,
                   stream: Optional[torch.cuda.Stream] = None, events: Optional[Sequence[int]] = None,
-                  raw_gates=None):
+                  raw_gates=None, output_gate=None):
     """Chunked prefill.  q, k [B, T, Hqk, dk]; v [B, T, Hv, dv]; g, beta [B, T, Hv] (all bf16 or all
     fp32, on one CUDA device); S0 [nseq, Hv, dk, dv] fp32 or None.  With ``cu_seqlens`` (int32 device
     tensor of nseq+1 offsets) B must be 1.  With ``raw_gates=(A_log, dt_bias)`` (fp32 [Hv] each), g and
-    beta are the raw projections a and b and the kernels form the gates.
-    Returns (out [B, T, Hv, dv], S_final or None)."""
+    beta are the raw projections a and b and the kernels form the gates.  With
+    ``output_gate=(z, norm_weight, eps)`` (z like out, norm_weight fp32 [dv]) the outputs pass through
+    RMSNorm * norm_weight * silu(z).  Returns (out [B, T, Hv, dv], S_final or None)."""
     lib = L.load()
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D [B, T, H, d]")
@@ -115,7 +125,8 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     if S_final is not None:
         _need("S_final", S_final, torch.float32, dev, (nseq, Hv, dk, dv))
     with torch.cuda.device(dev):
-        o, keep = _opts(lib, dt, scale, chunk, normalize_qk, stream, dev, events, raw_gates, Hv)
+        o, keep = _opts(lib, dt, scale, chunk, normalize_qk, stream, dev, events, raw_gates, Hv,
+                        output_gate, (B, T, Hv, dv))
         if cu_seqlens is not None:
             o.cu_seqlens = cu_seqlens.data_ptr()
             o.num_seqs = nseq
@@ -135,9 +146,10 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
 def gdn_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
                        S: torch.Tensor, *, scale: float = 1.0, normalize_qk: bool = False,
                        out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
-                       events: Optional[Sequence[int]] = None, raw_gates=None) -> torch.Tensor:
+                       events: Optional[Sequence[int]] = None, raw_gates=None,
+                       output_gate=None) -> torch.Tensor:
     """One decode step.  q, k [N, Hqk, dk]; v [N, Hv, dv]; g, beta [N, Hv]; S [N, Hv, dk, dv] fp32 is
-    updated in place.  ``raw_gates`` as for gdn_chunk_fwd.  Returns out [N, Hv, dv]."""
+    updated in place.  ``raw_gates`` and ``output_gate`` as for gdn_chunk_fwd.  Returns out [N, Hv, dv]."""
     lib = L.load()
     if q.dim() != 3 or v.dim() != 3:
         raise ValueError("q, k, v must be 3-D [N, H, d]")
@@ -156,7 +168,8 @@ def gdn_recurrent_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: tor
         out = torch.empty_like(v)
     _need("out", out, dt, dev, (N, Hv, dv))
     with torch.cuda.device(dev):
-        o, keep = _opts(lib, dt, scale, 64, normalize_qk, stream, dev, events, raw_gates, Hv)
+        o, keep = _opts(lib, dt, scale, 64, normalize_qk, stream, dev, events, raw_gates, Hv,
+                        output_gate, (N, Hv, dv))
         st = lib.gdn_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S), _ptr(out),
                                     N, Hqk, Hv, dk, dv, ctypes.byref(o))
         del keep

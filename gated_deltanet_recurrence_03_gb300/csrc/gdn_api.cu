@@ -84,7 +84,11 @@ gdn_status_t check_common(int Hqk, int Hv, int dk, int dv, const gdn_opts_t& o) 
     if (Hv % Hqk != 0) return fail(GDN_ERR_INVALID_ARG, "Hv (%d) must be a multiple of Hqk (%d)", Hv, Hqk);
     if (dk <= 0 || dv <= 0) return fail(GDN_ERR_INVALID_ARG, "head dims must be positive");
     if (o.dtype != GDN_F32 && o.dtype != GDN_BF16) return fail(GDN_ERR_INVALID_ARG, "unknown dtype %d", o.dtype);
-    if (o.flags & ~(GDN_NORMALIZE_QK | GDN_RAW_GATES)) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", o.flags);
+    if (o.flags & ~(GDN_NORMALIZE_QK | GDN_RAW_GATES | GDN_OUTPUT_GATE))
+        return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", o.flags);
+    if ((o.flags & GDN_OUTPUT_GATE) && (!o.z || !o.norm_weight || !aligned16(o.z) || !aligned_to(o.norm_weight, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "GDN_OUTPUT_GATE needs a 16-byte aligned z and an aligned norm_weight");
+    if ((o.flags & GDN_OUTPUT_GATE) && !(o.norm_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARG, "norm_eps must be >= 0");
     if ((o.flags & GDN_RAW_GATES) && (!o.A_log || !o.dt_bias || !aligned_to(o.A_log, 4) || !aligned_to(o.dt_bias, 4)))
         return fail(GDN_ERR_INVALID_ARG, "GDN_RAW_GATES needs aligned A_log and dt_bias");
     if (o.num_events < 0 || (o.num_events > 0 && !o.events)) return fail(GDN_ERR_INVALID_ARG, "bad event list");
@@ -112,6 +116,7 @@ void gdn_opts_init(gdn_opts_t* o) {
     o->dtype = GDN_BF16;
     o->chunk = 64;
     o->scale = 1.0f;
+    o->norm_eps = 1e-6f;
 }
 
 int gdn_version(void) { return GDN_VERSION_MAJOR * 10000 + GDN_VERSION_MINOR * 100 + GDN_VERSION_PATCH; }
@@ -189,6 +194,7 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const vo
     a.workspace = o.workspace; a.workspace_bytes = o.workspace_bytes;
     a.stream = stream; a.status = status;
     a.A_log = o.A_log; a.dt_bias = o.dt_bias;
+    a.z = o.z; a.norm_weight = o.norm_weight; a.norm_eps = o.norm_eps;
 
     cudaError_t e;
     if (tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk, o.flags)) {
@@ -199,10 +205,18 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const vo
         if ((reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0)
             return fail(GDN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
         e = launch_tc_prefill(a, o.events, o.num_events);
+        if (e == cudaSuccess && (o.flags & GDN_OUTPUT_GATE)) {
+            e = launch_output_gate(out, o.z, o.norm_weight, o.norm_eps, (long long)B * T * Hv, dv, o.dtype, stream);
+            record(o, 3, stream);
+        }
     } else {
         record(o, 0, stream);
         e = launch_recurrent_prefill(a);
         record(o, 1, stream);
+        if (e == cudaSuccess && (o.flags & GDN_OUTPUT_GATE)) {
+            e = launch_output_gate(out, o.z, o.norm_weight, o.norm_eps, (long long)B * T * Hv, dv, o.dtype, stream);
+            record(o, 2, stream);
+        }
     }
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return GDN_OK;
@@ -232,6 +246,7 @@ gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, con
     a.dtype = o.dtype; a.scale = o.scale; a.flags = o.flags;
     a.stream = static_cast<cudaStream_t>(o.stream);
     a.A_log = o.A_log; a.dt_bias = o.dt_bias;
+    a.z = o.z; a.norm_weight = o.norm_weight; a.norm_eps = o.norm_eps;
     record(o, 0, a.stream);
     cudaError_t e = launch_decode(a);
     record(o, 1, a.stream);

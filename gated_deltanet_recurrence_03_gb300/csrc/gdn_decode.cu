@@ -6,7 +6,8 @@
 //     u = beta (v - a p)               (the delta written for this token)
 //     S <- a S + k u^T                 (one write)
 //     o = scale (a r + (k . q) u)      (= scale S_new^T q, expanded so the state is read once)
-// With GDN_RAW_GATES, g and beta hold the raw projections and the gates are formed here.
+// With GDN_RAW_GATES, g and beta hold the raw projections and the gates are formed here; with
+// GDN_OUTPUT_GATE the outputs pass through the shell's gated RMS normalisation before they are stored.
 //
 // One CTA of 256 threads owns one (n, h) table.  Thread (row group rg, column lane lx) holds
 // rows rg*RPT .. rg*RPT+RPT-1 and four adjacent columns 4*lx .. 4*lx+3 in registers; the loads
@@ -24,7 +25,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const T* __restrict__ g, const T* __restrict__ beta, float* __restrict__ S,
                    T* __restrict__ out, int Hqk, int Hv, float scale, int normalize,
-                   const float* __restrict__ A_log, const float* __restrict__ dt_bias) {
+                   const float* __restrict__ A_log, const float* __restrict__ dt_bias,
+                   const T* __restrict__ zg, const float* __restrict__ norm_w, float norm_eps) {
     constexpr int LX = DV / 4;                 // column lanes (float4 each)
     constexpr int RG = kDecThreads / LX;       // row groups
     constexpr int RPT = DK / RG;               // rows per thread
@@ -36,7 +38,8 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     __shared__ __align__(16) float su[DV];
     __shared__ __align__(16) float red_p[RG][DV + 4];   // rows of DV+4 floats stay 16-byte aligned
     __shared__ __align__(16) float red_r[RG][DV + 4];
-    __shared__ float s_kq, s_rk, s_rq;
+    __shared__ __align__(16) float so[DV];   // outputs kept for the output gate
+    __shared__ float s_kq, s_rk, s_rq, s_inv;
 
     const int nh = blockIdx.x;                 // n * Hv + h
     const int n = nh / Hv, h = nh % Hv;
@@ -109,7 +112,9 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
         rj *= rq;                                // S^T q_hat
         const float u = bt * (sv[tid] - alpha * pj);
         su[tid] = u;
-        out[(size_t)nh * DV + tid] = from_f32<T>(scale * fmaf(alpha, rj, s_kq * u));
+        const float o = scale * fmaf(alpha, rj, s_kq * u);
+        if (zg) so[tid] = o;
+        else out[(size_t)nh * DV + tid] = from_f32<T>(o);
     }
     __syncthreads();
 
@@ -124,6 +129,20 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
         o.w = fmaf(kr, uu.w, alpha * st[r].w);
         Sv[(size_t)(rg * RPT + r) * LX + lx] = o;
     }
+    if (zg) {   // output gate: o / sqrt(mean(o^2) + eps) * w * silu(z), after the state is written
+        __syncthreads();
+        if (tid < 32) {
+            float ss = 0.f;
+            for (int j = tid; j < DV; j += 32) ss = fmaf(so[j], so[j], ss);
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+            if (tid == 0) s_inv = rsqrtf(ss / (float)DV + norm_eps);
+        }
+        __syncthreads();
+        if (tid < DV)
+            out[(size_t)nh * DV + tid] =
+                from_f32<T>(so[tid] * s_inv * norm_w[tid] * silu_f(to_f32(zg[(size_t)nh * DV + tid])));
+    }
 }
 
 template <int DK, int DV, typename T>
@@ -133,7 +152,7 @@ cudaError_t launch_typed(const DecodeArgs& a) {
         static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
         static_cast<const T*>(a.g), static_cast<const T*>(a.beta), a.S, static_cast<T*>(a.out), a.Hqk,
         a.Hv, a.scale, (a.flags & GDN_NORMALIZE_QK) ? 1 : 0, (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr,
-        a.dt_bias);
+        a.dt_bias, (a.flags & GDN_OUTPUT_GATE) ? static_cast<const T*>(a.z) : nullptr, a.norm_weight, a.norm_eps);
     return cudaGetLastError();
 }
 

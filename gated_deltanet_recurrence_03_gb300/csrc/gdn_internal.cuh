@@ -38,6 +38,9 @@ struct PrefillArgs {
     unsigned* status;           // device status word
     const float* A_log;         // GDN_RAW_GATES
     const float* dt_bias;
+    const void* z;              // GDN_OUTPUT_GATE
+    const float* norm_weight;
+    float norm_eps;
 };
 
 struct DecodeArgs {
@@ -55,11 +58,17 @@ struct DecodeArgs {
     cudaStream_t stream;
     const float* A_log;         // GDN_RAW_GATES
     const float* dt_bias;
+    const void* z;              // GDN_OUTPUT_GATE
+    const float* norm_weight;
+    float norm_eps;
 };
 
 // Launchers (return the launch error, cudaSuccess if enqueued).
 cudaError_t launch_decode(const DecodeArgs& a);
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a);
+// out <- RMSNorm(out) * norm_weight * silu(z) over each of `rows` rows of dv values, in place.
+cudaError_t launch_output_gate(void* out, const void* z, const float* w, float eps, long long rows, int dv,
+                               int dtype, cudaStream_t stream);
 
 // Tensor-core chunked prefill: whether it takes these arguments, its workspace, and its launch.
 bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk, unsigned flags);
@@ -93,6 +102,8 @@ __device__ __forceinline__ void gates_from_raw(float a, float b, float A_log, fl
     g = -__expf(A_log) * sp;
     beta = 1.f / (1.f + __expf(-b));
 }
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
 
 // Sequence i's token range [t0, t1) in the flattened token index.
 __device__ __forceinline__ void seq_range(const int32_t* cu, int i, int T, long long& t0, long long& t1) {

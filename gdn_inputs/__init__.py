@@ -35,7 +35,8 @@ Draw order (stream index): q 0, k 1, v 2, a 3, b 4, S0 5.
 Raw gate projections (for kernels that form the gates themselves): a_raw, b_raw ~ N(0, 1) in the
 storage dtype (streams 6, 7); per value head A_log ~ N(-0.5, 0.5) and dt_bias ~ N(0, 0.5) in fp32
 (streams 8, 9), which puts exp(A_log) and the decay in the ranges the handbook reports on real
-input.
+input.  Output gate: z ~ N(0, 1) like the outputs (stream 10), norm weight ~ N(1, 0.1) fp32 per
+value feature (stream 11).
 
 Rounding to the storage dtype: fp64 -> fp32 round-to-nearest-even; for bf16 the
 fp32 value is rounded again to bf16 (round-to-nearest-even on the fp32 bits).
@@ -74,6 +75,7 @@ _CHUNK = 1 << 22  # values generated per numpy batch (bounds temporary memory)
 
 STREAM_Q, STREAM_K, STREAM_V, STREAM_A, STREAM_B, STREAM_S0 = range(6)
 STREAM_RAW_A, STREAM_RAW_B, STREAM_A_LOG, STREAM_DT_BIAS = range(6, 10)
+STREAM_Z, STREAM_NORM_W = range(10, 12)
 
 
 def splitmix64(seed: int, idx: np.ndarray) -> np.ndarray:
@@ -284,3 +286,10 @@ def make_raw_gates(w: Workload, lead_shape=None):
     A_log = round_to_dtype(_normal_tensor(w.seed, STREAM_A_LOG, (w.Hv,), mean=-0.5, std=0.5), "f32")
     dt_bias = round_to_dtype(_normal_tensor(w.seed, STREAM_DT_BIAS, (w.Hv,), std=0.5), "f32")
     return dict(a=a, b=b, A_log=A_log, dt_bias=dt_bias)
+
+
+def make_output_gate(w: Workload, out_shape):
+    """Output-gate inputs: z shaped like the outputs (workload dtype) and norm_weight [dv] fp32."""
+    z = _rounded_normal(w.seed, STREAM_Z, tuple(out_shape), w.dtype)
+    norm_w = round_to_dtype(_normal_tensor(w.seed, STREAM_NORM_W, (w.dv,), mean=1.0, std=0.1), "f32")
+    return dict(z=z, norm_weight=norm_w)

@@ -64,6 +64,10 @@ typedef enum gdn_dtype {
                                  the GatedDeltaNet shell ("qwen/deltanet.py", forward): the kernels form
                                  beta = sigmoid(b) and g = -exp(A_log[h]) * softplus(a + dt_bias[h]) in
                                  fp32; opts->A_log and opts->dt_bias ([Hv] float) are then required */
+#define GDN_OUTPUT_GATE 0x4u  /* out = RMSNorm(o) * norm_weight * silu(z) per (token, value head), the
+                                 gated normalisation of the shell (GatedRMSNorm(out, z)): o is divided by
+                                 sqrt(mean over dv of o^2 + norm_eps); opts->z ([..., Hv, dv] like out,
+                                 dtype) and opts->norm_weight ([dv] float) are then required */
 
 typedef struct gdn_opts {
     int dtype;                  /* gdn_dtype_t of q, k, v, g, beta, out.  Default GDN_BF16. */
@@ -84,6 +88,9 @@ typedef struct gdn_opts {
     int num_events;
     const float* A_log;         /* [Hv] per-head log forgetting speed (GDN_RAW_GATES), DEVICE */
     const float* dt_bias;       /* [Hv] per-head bias added to a (GDN_RAW_GATES), DEVICE */
+    const void* z;              /* output gate input, same shape and dtype as out (GDN_OUTPUT_GATE), DEVICE */
+    const float* norm_weight;   /* [dv] (GDN_OUTPUT_GATE), DEVICE */
+    float norm_eps;             /* GDN_OUTPUT_GATE epsilon; default 1e-6 */
 } gdn_opts_t;
 
 /* Fill *opts with the defaults listed above. */

@@ -30,3 +30,18 @@ def gates_from_raw(a, b, A_log, dt_bias):
     dt_bias = np.asarray(dt_bias, dtype=np.float64)
     g = -np.exp(A_log) * softplus(a + dt_bias)
     return g, sigmoid(b)
+
+
+def silu(z):
+    z = np.asarray(z, dtype=np.float64)
+    return z * sigmoid(z)
+
+
+def gated_rmsnorm(o, z, weight, eps):
+    """Output gate of the shell (GatedRMSNorm(out, z), "the output is normalised per head and then
+    multiplied by the gate silu(z)"): o / sqrt(mean(o^2) + eps) * weight * silu(z) over the last axis
+    (the dv values of one token and value head).  The GatedRMSNorm body is not printed on the pages;
+    this is the reading taken (RMS over the head's values, weight after the normalisation)."""
+    o = np.asarray(o, dtype=np.float64)
+    ms = np.mean(o * o, axis=-1, keepdims=True)
+    return o / np.sqrt(ms + eps) * np.asarray(weight, dtype=np.float64) * silu(z)

@@ -39,6 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_opts_defaults_and_strings(lib):
     o = pkg_lib.default_opts(lib)
     assert (o.dtype, o.chunk, o.scale, o.flags) == (pkg_lib.GDN_BF16, 64, 1.0, 0)
+    assert abs(o.norm_eps - 1e-6) < 1e-12
     assert not o.cu_seqlens and not o.workspace and not o.stream
     assert lib.gdn_status_string(0) == b"ok"
     assert lib.gdn_status_string(pkg_lib.GDN_ERR_TIMEOUT) == b"device-side wait timed out"
@@ -71,6 +72,7 @@ def prefill(lib, B=1, T=8, Hqk=1, Hv=1, dk=32, dv=32, ptrs=None, **kw):
     (dict(dtype=7), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(flags=0x80), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(flags=pkg_lib.GDN_RAW_GATES), pkg_lib.GDN_ERR_INVALID_ARG),   # A_log / dt_bias missing
+    (dict(flags=pkg_lib.GDN_OUTPUT_GATE), pkg_lib.GDN_ERR_INVALID_ARG),  # z / norm_weight missing
     (dict(ptrs=[FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(ptrs=[FAKE + 8] + [FAKE] * 7), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(ptrs=[FAKE] * 3 + [FAKE + 1] + [FAKE] * 4), pkg_lib.GDN_ERR_INVALID_ARG),

@@ -93,3 +93,40 @@ def test_decode_raw_gates(dtype):
     ref_o, ref_s = orc.forward(tr(d["q"]), tr(d["k"]), tr(d["v"]), tr(g), tr(beta), S0=d["S0"])
     eo, es = rel_err(ref_o, tr(got_o)), rel_err(ref_s, S.cpu().numpy())
     assert eo <= TOL[dtype] and es <= TOL[dtype], (eo, es)
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_prefill_output_gate(name):
+    w = CASES[name]
+    x = gi.make_prefill_inputs(w)
+    og = gi.make_output_gate(w, x["v"].shape)
+    dt = w.dtype
+    out, sf = gdn.gdn_chunk_fwd(up(x["q"], dt), up(x["k"], dt), up(x["v"], dt), up(x["g"], dt), up(x["beta"], dt),
+                                up(x["S0"], torch.float32), chunk=w.chunk,
+                                output_gate=(up(og["z"], dt), up(og["norm_weight"], torch.float32), 1e-6))
+    torch.cuda.synchronize()
+    ref_o, ref_s = orc.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], S0=x["S0"])
+    ref_y = ogates.gated_rmsnorm(ref_o, og["z"], og["norm_weight"], 1e-6)
+    ey, es = rel_err(ref_y, out.float().cpu().numpy()), rel_err(ref_s, sf.cpu().numpy())
+    assert ey <= TOL[dt] and es <= TOL[dt], (ey, es)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_output_gate(dtype):
+    w = gi.Workload("fe", "decode", dtype, B=4, T=3, Hqk=2, Hv=4, dk=128, dv=128, s0_std=0.1, seed=35)
+    d = gi.make_decode_inputs(w)
+    og = gi.make_output_gate(w, d["v"].shape)
+    S = up(d["S0"], torch.float32)
+    wn = up(og["norm_weight"], torch.float32)
+    outs = []
+    for t in range(w.T):
+        outs.append(gdn.gdn_recurrent_step(up(d["q"][t], dtype), up(d["k"][t], dtype), up(d["v"][t], dtype),
+                                           up(d["g"][t], dtype), up(d["beta"][t], dtype), S,
+                                           output_gate=(up(og["z"][t], dtype), wn, 1e-6)))
+    torch.cuda.synchronize()
+    tr = lambda a: np.swapaxes(a, 0, 1)
+    ref_o, ref_s = orc.forward(tr(d["q"]), tr(d["k"]), tr(d["v"]), tr(d["g"]), tr(d["beta"]), S0=d["S0"])
+    ref_y = ogates.gated_rmsnorm(ref_o, tr(og["z"]), og["norm_weight"], 1e-6)
+    ey = rel_err(ref_y, tr(torch.stack(outs).float().cpu().numpy()))
+    es = rel_err(ref_s, S.cpu().numpy())
+    assert ey <= TOL[dtype] and es <= TOL[dtype], (ey, es)

@@ -34,3 +34,20 @@ def test_gates_ranges():
     g, beta = gates.gates_from_raw(a, b, A_log, dt_bias)
     assert np.all(g < 0) and np.all((beta > 0) & (beta < 1))   # decay exp(g) in (0, 1)
     assert np.all(np.diff(gates.gates_from_raw(np.sort(a[:, 0]), b[:, 0], A_log[0], dt_bias[0])[0]) <= 0)
+
+
+def test_gated_rmsnorm_closed_forms():
+    dv = 16
+    alt = np.tile([1.0, -1.0], dv // 2)
+    w = np.linspace(0.5, 1.5, dv)
+    z = np.linspace(-3, 3, dv)
+    for c in (0.01, 2.5, 300.0):   # the RMS of c * alt is |c|: the result does not depend on c (eps = 0)
+        np.testing.assert_allclose(gates.gated_rmsnorm(c * alt, z, w, 0.0), alt * w * gates.silu(z), rtol=1e-14)
+    # silu(0) = 0 closes the gate; silu(z) -> z for large z, -> 0 for very negative z
+    assert np.all(gates.gated_rmsnorm(alt, np.zeros(dv), w, 1e-6) == 0)
+    np.testing.assert_allclose(gates.silu(np.array([40.0])), [40.0], rtol=1e-15)
+    assert abs(gates.silu(-40.0)) < 1e-15
+    # eps shrinks the normalised vector: RMS(o / sqrt(ms + eps)) = sqrt(ms / (ms + eps))
+    o = 0.01 * alt
+    y = gates.gated_rmsnorm(o, np.full(dv, 50.0), np.ones(dv), 1e-4)
+    np.testing.assert_allclose(np.sqrt(np.mean((y / gates.silu(50.0)) ** 2)), np.sqrt(1e-4 / (1e-4 + 1e-4)), rtol=1e-12)
