@@ -313,6 +313,63 @@ def run_gpu(args):
     lf_prep, lf_chain = prefill_flops(wl.T, wl)
     del xl, out_l, ws_l
 
+    # ---- the recurrent core of one layer on the same workload: short causal conv of the packed q/k/v
+    #      projection (three channel slices), gates from the raw a/b projections, l2 norm of q and k,
+    #      chunked recurrence, gated RMS norm with silu(z); prefill inputs larger than L2
+    Cq, Cv = w.Hqk * w.dk, w.Hv * w.dv
+    Cc = 2 * Cq + Cv
+    bf = torch.bfloat16
+    gen = torch.Generator(device=dev).manual_seed(5)
+    proj = torch.randn(w.B, w.T, Cc, device=dev, generator=gen).to(bf)
+    conv_w = 0.5 * torch.randn(Cc, 4, device=dev, generator=gen)
+    conv_ws = [conv_w[:Cq].contiguous(), conv_w[Cq:2 * Cq].contiguous(), conv_w[2 * Cq:].contiguous()]
+    qc = torch.empty(w.B, w.T, w.Hqk, w.dk, dtype=bf, device=dev)
+    kc, vc = torch.empty_like(qc), torch.empty(w.B, w.T, w.Hv, w.dv, dtype=bf, device=dev)
+    caches = [torch.empty(w.B, 3, c, dtype=bf, device=dev) for c in (Cq, Cq, Cv)]
+    a_raw = torch.randn(w.B, w.T, w.Hv, device=dev, generator=gen).to(bf)
+    b_raw = torch.randn(w.B, w.T, w.Hv, device=dev, generator=gen).to(bf)
+    A_log = -0.5 + 0.5 * torch.randn(w.Hv, device=dev, generator=gen)
+    dt_bias = 0.5 * torch.randn(w.Hv, device=dev, generator=gen)
+    z = torch.randn(w.B, w.T, w.Hv, w.dv, device=dev, generator=gen).to(bf)
+    norm_w = 1.0 + 0.1 * torch.randn(w.dv, device=dev, generator=gen)
+    layer_steps = max(3, min(10, args.steps))
+    ev_c = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(layer_steps)]
+    ev_p = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(layer_steps)]
+    for row in ev_c + ev_p:
+        for e in row:
+            e.record(stream)
+
+    def layer_step(i=None):
+        if i is not None:
+            ev_c[i][0].record(stream)
+        for (c0, c1), dst, cw, cache in zip(((0, Cq), (Cq, 2 * Cq), (2 * Cq, Cc)), (qc, kc, vc), conv_ws, caches):
+            gdn.gdn_causal_conv1d_fwd(proj[:, :, c0:c1], cw, None, out=dst.view(w.B, w.T, c1 - c0),
+                                      cache_out=cache)
+        if i is not None:
+            ev_c[i][1].record(stream)
+        gdn.gdn_chunk_fwd(qc, kc, vc, a_raw, b_raw, S0, out=out, S_final=S_final, workspace=ws, chunk=w.chunk,
+                          scale=w.dk ** -0.5, normalize_qk=True, raw_gates=(A_log, dt_bias),
+                          output_gate=(z, norm_w, 1e-6),
+                          events=None if i is None else [e.cuda_event for e in ev_p[i]])
+
+    for _ in range(3):
+        layer_step()
+    barrier()
+    clocks.active = True
+    t0.record(stream)
+    for i in range(layer_steps):
+        layer_step(i)
+    t1.record(stream)
+    barrier()
+    clocks.active = False
+    layer_ms = max_over_ranks(t0.elapsed_time(t1)) / layer_steps
+    gdn.check_device_status()
+    conv_ms = statistics.mean(r[0].elapsed_time(r[1]) for r in ev_c)
+    gate_ms = statistics.mean(r[2].elapsed_time(r[3]) for r in ev_p)
+    conv_bytes = 2 * (w.B * w.T * Cc * 2) + Cc * 4 * 4 + w.B * 3 * Cc * 2
+    gate_bytes = 3 * (w.B * w.T * Cv * 2) + w.dv * 4
+    del proj, qc, kc, vc, a_raw, b_raw, z
+
     # ---- decode: 512 consecutive steps, state resident, one CUDA graph per pass
     wd = DECODE
     xd = device_inputs_random(torch, dev, wd, steps=wd.T, seed=2)
@@ -376,6 +433,20 @@ def run_gpu(args):
                          "roofline": {"bound": "tensor", "achieved": round((lf_prep + lf_chain) / (long_ms * 1e9), 2),
                                       "peak": peak_tf, "unit": "TFLOP/s",
                                       "frac": round((lf_prep + lf_chain) / (long_ms * 1e9) / peak_tf, 4)}},
+        "layer": {"workload": "prefill_gqa_8k through the whole recurrent core: causal conv K=4 of the packed "
+                              "q/k/v projection (3 channel slices, 8192 channels), gates from raw a/b, l2 norm, "
+                              "chunked recurrence, gated RMS norm x silu(z)",
+                  "value": round(world * tokens / (layer_ms / 1e3), 1), "unit": "tokens/s",
+                  "ms_per_step": round(layer_ms, 4), "steps": layer_steps, "gpu_launches": 6 * layer_steps,
+                  "kernels_ms": {"conv_fwd_kernel x3": round(conv_ms, 4), "output_gate_kernel": round(gate_ms, 4)},
+                  "conv_roofline": {"bound": "hbm", "achieved": round(conv_bytes / (conv_ms * 1e6), 1),
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": round(conv_bytes / (conv_ms * 1e6) / peaks["hbm_gbs"], 4),
+                                    "algorithmic_bytes": conv_bytes},
+                  "gate_roofline": {"bound": "hbm", "achieved": round(gate_bytes / (gate_ms * 1e6), 1),
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": round(gate_bytes / (gate_ms * 1e6) / peaks["hbm_gbs"], 4),
+                                    "algorithmic_bytes": gate_bytes}},
         "decode": {"workload": "decode_256x512: 256 sequences x 32 V heads (16 QK heads), d=128, 512 steps, "
                                "fp32 state 512 MiB resident, one CUDA graph per 512-step pass",
                    "value": round(world / (dec_ms / 1e3), 1), "unit": "steps/s",

@@ -187,3 +187,70 @@ def check_device_status(stream: Optional[torch.cuda.Stream] = None, device=None)
 
 def version() -> int:
     return int(L.load().gdn_version())
+
+
+def gdn_causal_conv1d_fwd(x: torch.Tensor, w: torch.Tensor, cache_in: Optional[torch.Tensor] = None, *,
+                          cu_seqlens: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                          cache_out: Optional[torch.Tensor] = None, return_cache: bool = True, stream: Optional[torch.cuda.Stream] = None,
+                          events: Optional[Sequence[int]] = None):
+    """Depthwise causal convolution + SiLU.  x [B, T, C] (bf16 or fp32; may be a channel slice of a
+    wider tensor: rows must be evenly strided with the channels contiguous); w [C, K] fp32;
+    cache_in [nseq, K-1, C] or None.  ``cache_out`` (or a new tensor when ``return_cache``) receives each
+    sequence's last K-1 inputs.  Returns (y [B, T, C], cache_out [nseq, K-1, C] or None)."""
+    lib = L.load()
+    if x.dim() != 3 or x.stride(2) != 1 or x.stride(0) != x.shape[1] * x.stride(1):
+        raise ValueError("x must be [B, T, C] with contiguous channels and evenly strided token rows")
+    B, T, C = x.shape
+    dev, dt = x.device, x.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    K = int(w.shape[1])
+    _need("w", w, torch.float32, dev, (C, K))
+    nseq = B
+    if cu_seqlens is not None:
+        nseq = int(cu_seqlens.numel()) - 1
+        _need("cu_seqlens", cu_seqlens, torch.int32, dev, (nseq + 1,))
+    if cache_in is not None:
+        _need("cache_in", cache_in, dt, dev, (nseq, K - 1, C))
+    if out is None:
+        out = torch.empty((B, T, C), dtype=dt, device=dev)
+    _need("out", out, dt, dev, (B, T, C))
+    if cache_out is None and return_cache:
+        cache_out = torch.empty((nseq, K - 1, C), dtype=dt, device=dev)
+    if cache_out is not None:
+        _need("cache_out", cache_out, dt, dev, (nseq, K - 1, C))
+    with torch.cuda.device(dev):
+        o, keep = _opts(lib, dt, 1.0, 64, False, stream, dev, events)
+        if cu_seqlens is not None:
+            o.cu_seqlens = cu_seqlens.data_ptr()
+            o.num_seqs = nseq
+        st = lib.gdn_causal_conv1d_fwd(_ptr(x), x.stride(1), _ptr(w), _ptr(cache_in), _ptr(out), _ptr(cache_out),
+                                       B, T, C, K, ctypes.byref(o))
+        del keep
+        L.check(lib, st)
+    return out, cache_out
+
+
+def gdn_causal_conv1d_step(x: torch.Tensor, w: torch.Tensor, cache: torch.Tensor, *,
+                           out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                           events: Optional[Sequence[int]] = None) -> torch.Tensor:
+    """One decode token per sequence: x [N, C] (channels contiguous, rows evenly strided), w [C, K] fp32,
+    cache [N, K-1, C] updated in place.  Returns y [N, C]."""
+    lib = L.load()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be [N, C] with contiguous channels")
+    N, C = x.shape
+    dev, dt = x.device, x.dtype
+    K = int(w.shape[1])
+    _need("w", w, torch.float32, dev, (C, K))
+    _need("cache", cache, dt, dev, (N, K - 1, C))
+    if out is None:
+        out = torch.empty((N, C), dtype=dt, device=dev)
+    _need("out", out, dt, dev, (N, C))
+    with torch.cuda.device(dev):
+        o, keep = _opts(lib, dt, 1.0, 64, False, stream, dev, events)
+        st = lib.gdn_causal_conv1d_step(_ptr(x), x.stride(0), _ptr(w), _ptr(cache), _ptr(out), N, C, K,
+                                        ctypes.byref(o))
+        del keep
+        L.check(lib, st)
+    return out

@@ -254,6 +254,74 @@ gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, con
     return GDN_OK;
 }
 
+static gdn_status_t conv_common(const void* x, long long* x_stride, const float* w, int C, int K,
+                                const gdn_opts_t& o) {
+    if (C <= 0 || C % 8 != 0) return fail(GDN_ERR_INVALID_ARG, "C=%d must be a positive multiple of 8", C);
+    if (K < 1 || K > 4) return fail(GDN_ERR_UNSUPPORTED, "kernel width K=%d not in 1..4", K);
+    if (o.dtype != GDN_F32 && o.dtype != GDN_BF16) return fail(GDN_ERR_INVALID_ARG, "unknown dtype %d", o.dtype);
+    if (*x_stride == 0) *x_stride = C;
+    const int per16 = o.dtype == GDN_BF16 ? 8 : 4;   // elements in 16 bytes: rows must stay 16-byte aligned
+    if (*x_stride < C || *x_stride % per16 != 0)
+        return fail(GDN_ERR_INVALID_ARG, "x_stride=%lld must be >= C and a multiple of %d", *x_stride, per16);
+    if (!x || !w) return fail(GDN_ERR_INVALID_ARG, "null x or w");
+    if (!aligned16(x) || !aligned_to(w, 4)) return fail(GDN_ERR_INVALID_ARG, "x must be 16-byte aligned, w 4-byte aligned");
+    return GDN_OK;
+}
+
+gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const float* w, const void* cache_in, void* y,
+                                   void* cache_out, int B, int T, int C, int K, const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_opts_t o = resolve(opts);
+    if (B < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "B=%d T=%d must be >= 0", B, T);
+    const bool packed = o.cu_seqlens != nullptr;
+    if (packed && (B != 1 || o.num_seqs < 1))
+        return fail(GDN_ERR_INVALID_ARG, "cu_seqlens needs B == 1 and num_seqs >= 1");
+    const int nseq = packed ? o.num_seqs : B;
+    if (nseq == 0) return GDN_OK;
+    gdn_status_t st = conv_common(x, &x_stride, w, C, K, o);
+    if (st != GDN_OK) return st;
+    if ((long long)B * T > 0 && !y) return fail(GDN_ERR_INVALID_ARG, "null y");
+    const void* ptrs[] = {y, cache_in, cache_out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+    if (packed && !aligned_to(o.cu_seqlens, 4)) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+    unsigned* status = nullptr;
+    st = device_ready(&status);
+    if (st != GDN_OK) return st;
+    ConvArgs a{};
+    a.x = x; a.x_stride = x_stride; a.w = w; a.cache_in = cache_in; a.y = y; a.cache_out = cache_out;
+    a.B = B; a.T = T; a.C = C; a.K = K; a.dtype = o.dtype; a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq;
+    a.packed = packed; a.stream = static_cast<cudaStream_t>(o.stream);
+    record(o, 0, a.stream);
+    const cudaError_t e = launch_conv_fwd(a);
+    record(o, 1, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "conv launch");
+    return GDN_OK;
+}
+
+gdn_status_t gdn_causal_conv1d_step(const void* x, long long x_stride, const float* w, void* cache, void* y, int N,
+                                    int C, int K, const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_opts_t o = resolve(opts);
+    if (N < 0) return fail(GDN_ERR_INVALID_ARG, "N=%d must be >= 0", N);
+    if (N == 0) return GDN_OK;
+    gdn_status_t st = conv_common(x, &x_stride, w, C, K, o);
+    if (st != GDN_OK) return st;
+    if (!y || (K > 1 && !cache)) return fail(GDN_ERR_INVALID_ARG, "null y or cache");
+    if (!aligned16(y) || (cache && !aligned16(cache))) return fail(GDN_ERR_INVALID_ARG, "y and cache must be 16-byte aligned");
+    unsigned* status = nullptr;
+    st = device_ready(&status);
+    if (st != GDN_OK) return st;
+    ConvArgs a{};
+    a.x = x; a.x_stride = x_stride; a.w = w; a.y = y; a.cache_out = cache;
+    a.B = N; a.C = C; a.K = K; a.dtype = o.dtype; a.stream = static_cast<cudaStream_t>(o.stream);
+    record(o, 0, a.stream);
+    const cudaError_t e = launch_conv_step(a);
+    record(o, 1, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "conv step launch");
+    return GDN_OK;
+}
+
 gdn_status_t gdn_check_device_status(void* stream) {
     t_last_error[0] = 0;
     unsigned* status = nullptr;

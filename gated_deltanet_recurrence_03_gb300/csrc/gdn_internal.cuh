@@ -63,7 +63,24 @@ struct DecodeArgs {
     float norm_eps;
 };
 
+struct ConvArgs {
+    const void* x;
+    long long x_stride;         // elements between consecutive token rows of x
+    const float* w;             // [C, K]
+    const void* cache_in;       // fwd: [nseq, K-1, C] or nullptr
+    void* y;
+    void* cache_out;            // fwd: [nseq, K-1, C] or nullptr; step: the cache, updated in place
+    int B, T, C, K;             // step: B = number of sequences, T unused
+    int dtype;
+    const int32_t* cu_seqlens;
+    int num_seqs;
+    bool packed;
+    cudaStream_t stream;
+};
+
 // Launchers (return the launch error, cudaSuccess if enqueued).
+cudaError_t launch_conv_fwd(const ConvArgs& a);
+cudaError_t launch_conv_step(const ConvArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a);
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a);
 // out <- RMSNorm(out) * norm_weight * silu(z) over each of `rows` rows of dv values, in place.

@@ -166,6 +166,36 @@ gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, 
                                    int B, int T, int Hqk, int Hv, int dk, int dv,
                                    const gdn_opts_t* opts);
 
+/*
+ * gdn_causal_conv1d_fwd -- the short causal convolution that feeds q, k and v: depthwise (each
+ * channel on its own), window K, then SiLU, as in the GatedDeltaNet shell of "Transformer by Hand,
+ * ch. 7" (conv1d with groups = channels and padding K - 1, cut to the first T outputs, SiLU):
+ *     y[t, c] = silu( sum_{i<K} w[c, i] * x[t - (K - 1) + i, c] )
+ * Inputs before a sequence's first token come from cache_in (zeros when NULL).
+ *
+ *   x          [B, T, C] dtype, token rows x_stride elements apart (0 = C; a channel slice of a wider
+ *              packed projection can be passed directly), 16-byte aligned
+ *   w          [C, K] float; w[c, K-1] weighs the current token
+ *   cache_in   [nseq, K-1, C] dtype or NULL: the K-1 inputs preceding each sequence, oldest first
+ *   y          [B, T, C] dtype
+ *   cache_out  [nseq, K-1, C] dtype or NULL: the last K-1 inputs of each sequence (what a decode step
+ *              needs next; for sequences shorter than K-1 the older entries come from cache_in)
+ * nseq = B, or num_seqs with opts->cu_seqlens (B == 1, packed sequences, state reset at each start).
+ * Supported: C a multiple of 8, 1 <= K <= 4.  opts->dtype, cu_seqlens, num_seqs, stream are used.
+ */
+gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const float* w, const void* cache_in,
+                                   void* y, void* cache_out, int B, int T, int C, int K,
+                                   const gdn_opts_t* opts);
+
+/*
+ * gdn_causal_conv1d_step -- one decode token per sequence through the same convolution, with the
+ * 3-token (K-1) cache the learn-llm page describes ("at inference the most recent 3 tokens' inputs
+ * are cached"):  x [N, C] (rows x_stride apart), cache [N, K-1, C] read and updated in place (shifted
+ * by one token), y [N, C].
+ */
+gdn_status_t gdn_causal_conv1d_step(const void* x, long long x_stride, const float* w, void* cache, void* y,
+                                    int N, int C, int K, const gdn_opts_t* opts);
+
 /* Synchronise `stream` (cudaStream_t, NULL = legacy), then read and clear the device status word
  * that kernels set when a bounded wait runs out.  GDN_OK if clear, GDN_ERR_TIMEOUT if set,
  * GDN_ERR_CUDA if the synchronisation itself failed. */

@@ -25,7 +25,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "gdn.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -111,3 +111,52 @@ def test_workspace_query_is_pure_host(lib):
     # fp32 and small heads run the token-serial kernel: no workspace
     assert lib.gdn_chunk_fwd_workspace_size(2, 512, 4, 4, 32, 32, opts(lib, dtype=pkg_lib.GDN_F32)) == 0
     assert lib.gdn_chunk_fwd_workspace_size(-1, 512, 4, 4, 32, 32, opts(lib)) == 0
+
+
+def conv_fwd(lib, B=1, T=8, C=64, K=4, x_stride=0, ptrs=None, **kw):
+    p = [FAKE] * 5 if ptrs is None else ptrs   # x, w, cache_in, y, cache_out
+    return lib.gdn_causal_conv1d_fwd(p[0], x_stride, p[1], p[2], p[3], p[4], B, T, C, K, opts(lib, **kw))
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(C=0), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(C=12), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(K=0), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(K=5), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(B=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(T=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(x_stride=32), pkg_lib.GDN_ERR_INVALID_ARG),                       # narrower than C
+    (dict(x_stride=68), pkg_lib.GDN_ERR_INVALID_ARG),                       # bf16 rows lose 16-B alignment
+    (dict(dtype=7), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(ptrs=[0] + [FAKE] * 4), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(ptrs=[FAKE + 8] + [FAKE] * 4), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(ptrs=[FAKE, FAKE, FAKE, FAKE + 4, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(B=2, cu_seqlens=FAKE, num_seqs=2), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(cu_seqlens=FAKE + 2, num_seqs=2), pkg_lib.GDN_ERR_INVALID_ARG),
+])
+def test_conv_fwd_argument_errors(lib, case, expect):
+    assert conv_fwd(lib, **case) == expect
+    assert lib.gdn_last_error() != b""
+
+
+def test_conv_fwd_f32_stride_rule(lib):
+    # fp32 rows need a stride that is a multiple of 4 elements; C must still be a multiple of 8
+    assert conv_fwd(lib, x_stride=66, dtype=pkg_lib.GDN_F32) == pkg_lib.GDN_ERR_INVALID_ARG
+    assert conv_fwd(lib, C=20, dtype=pkg_lib.GDN_F32) == pkg_lib.GDN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(N=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(K=5), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(cache=0), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(y=FAKE + 4), pkg_lib.GDN_ERR_INVALID_ARG),
+])
+def test_conv_step_argument_errors(lib, case, expect):
+    st = lib.gdn_causal_conv1d_step(FAKE, 0, FAKE, case.get("cache", FAKE), case.get("y", FAKE), case.get("N", 4),
+                                    64, case.get("K", 4), opts(lib))
+    assert st == expect
+
+
+def test_conv_empty_calls_do_nothing(lib):
+    assert conv_fwd(lib, B=0, T=0, ptrs=[0] * 5) == pkg_lib.GDN_OK
+    assert lib.gdn_causal_conv1d_step(0, 0, 0, 0, 0, 0, 64, 4, opts(lib)) == pkg_lib.GDN_OK

@@ -1,0 +1,105 @@
+"""GPU causal short convolution (gdn_causal_conv1d_fwd / _step through the C ABI) against the oracle."""
+import numpy as np
+import pytest
+
+import gdn_inputs as gi
+from oracle import conv as oconv
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from gpu_util import TOL, rel_err, up  # noqa: E402
+import gated_deltanet_recurrence_03_gb300 as gdn  # noqa: E402
+
+
+def _inputs(seed, lead, C, K, dtype, nseq):
+    x = gi.round_to_dtype(gi.normals(seed, 0, int(np.prod(lead)) * C).reshape(*lead, C), dtype)
+    w = gi.round_to_dtype(0.5 * gi.normals(seed, 1, C * K).reshape(C, K), "f32")
+    cache = gi.round_to_dtype(gi.normals(seed, 2, nseq * (K - 1) * C).reshape(nseq, K - 1, C), dtype)
+    return x, w, cache
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [4, 2])
+@pytest.mark.parametrize("with_cache", [False, True])
+def test_conv_fwd_batched(dtype, K, with_cache):
+    B, T, C = 3, 150, 96
+    x, w, cache = _inputs(40 + K, (B, T), C, K, dtype, B)
+    y, co = gdn.gdn_causal_conv1d_fwd(up(x, dtype), up(w, torch.float32), up(cache, dtype) if with_cache else None)
+    torch.cuda.synchronize()
+    ry, rc = oconv.causal_conv1d(x, w, cache if with_cache else None)
+    assert rel_err(ry, y.float().cpu().numpy()) <= TOL[dtype]
+    np.testing.assert_array_equal(co.float().cpu().numpy(), rc)   # the cache holds inputs: bit-exact
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_conv_fwd_packed_with_empty_and_short(dtype):
+    lens = (0, 1, 2, 65, 0, 130, 3)
+    K, C = 4, 64
+    x, w, cache = _inputs(50, (1, sum(lens)), C, K, dtype, len(lens))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    y, co = gdn.gdn_causal_conv1d_fwd(up(x, dtype), up(w, torch.float32), up(cache, dtype),
+                                      cu_seqlens=torch.from_numpy(cu).cuda())
+    torch.cuda.synchronize()
+    ry, rc = oconv.causal_conv1d(x, w, cache, cu_seqlens=cu)
+    assert rel_err(ry, y.float().cpu().numpy()) <= TOL[dtype]
+    np.testing.assert_array_equal(co.float().cpu().numpy(), rc)
+
+
+def test_conv_on_a_channel_slice_of_the_packed_projection():
+    """q, k and v come from one packed projection: convolving each channel slice in place gives the
+    slices of the full convolution (the convolution is per channel)."""
+    B, T, Cq, Cv, K = 2, 80, 64, 128, 4
+    C = 2 * Cq + Cv
+    x, w, _ = _inputs(60, (B, T), C, K, "bf16", B)
+    xd, wd = up(x, "bf16"), up(w, torch.float32)
+    full, _ = gdn.gdn_causal_conv1d_fwd(xd, wd)
+    parts = []
+    for c0, c1 in ((0, Cq), (Cq, 2 * Cq), (2 * Cq, C)):
+        yp, _ = gdn.gdn_causal_conv1d_fwd(xd[:, :, c0:c1], wd[c0:c1].contiguous())
+        parts.append(yp)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(torch.cat(parts, -1).float().cpu().numpy(), full.float().cpu().numpy())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_conv_step_equals_fwd(dtype):
+    N, T, C, K = 5, 9, 128, 4
+    x, w, cache = _inputs(70, (N, T), C, K, dtype, N)
+    wd = up(w, torch.float32)
+    cd = up(cache, dtype)
+    ys = [gdn.gdn_causal_conv1d_step(up(np.ascontiguousarray(x[:, t]), dtype), wd, cd) for t in range(T)]
+    torch.cuda.synchronize()
+    ry, rc = oconv.causal_conv1d(x, w, cache)
+    assert rel_err(ry, torch.stack(ys, 1).float().cpu().numpy()) <= TOL[dtype]
+    np.testing.assert_array_equal(cd.float().cpu().numpy(), rc)
+
+
+def test_conv_fwd_more_token_blocks_than_grid_rows():
+    """More than 65535 blocks of 64 tokens: the token-block loop strides over the grid.  The oracle
+    checks the last tokens, starting from the inputs that precede them (cache continuity is pinned)."""
+    T, C, K = 65535 * 64 + 200, 8, 4
+    x = gi.round_to_dtype(gi.normals(80, 0, T * C).reshape(1, T, C), "bf16")
+    w = gi.round_to_dtype(0.5 * gi.normals(80, 1, C * K).reshape(C, K), "f32")
+    y, co = gdn.gdn_causal_conv1d_fwd(up(x, "bf16"), up(w, torch.float32))
+    torch.cuda.synchronize()
+    tail = 300
+    ry, rc = oconv.causal_conv1d(x[:, -tail:], w, x[:, -tail - (K - 1):-tail])
+    assert rel_err(ry, y[:, -tail:].float().cpu().numpy()) <= TOL["bf16"]
+    np.testing.assert_array_equal(co.float().cpu().numpy(), rc)
+    hy, _ = oconv.causal_conv1d(x[:, :tail], w)
+    assert rel_err(hy, y[:, :tail].float().cpu().numpy()) <= TOL["bf16"]
+
+
+def test_conv_step_more_rows_than_grid_rows():
+    N, C, K = 70000, 8, 4
+    x, w, cache = _inputs(81, (N,), C, K, "bf16", N)
+    cd = up(cache, "bf16")
+    y = gdn.gdn_causal_conv1d_step(up(x, "bf16"), up(w, torch.float32), cd)
+    torch.cuda.synchronize()
+    sel = np.r_[0:50, N - 50:N]
+    ry, rc = oconv.causal_conv1d(x[sel][:, None], w, cache[sel])
+    assert rel_err(ry[:, 0], y[sel].float().cpu().numpy()) <= TOL["bf16"]
+    np.testing.assert_array_equal(cd[sel].float().cpu().numpy(), rc)
