@@ -291,7 +291,7 @@ gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const floa
     ConvArgs a{};
     a.x = x; a.x_stride = x_stride; a.w = w; a.cache_in = cache_in; a.y = y; a.cache_out = cache_out;
     a.B = B; a.T = T; a.C = C; a.K = K; a.dtype = o.dtype; a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq;
-    a.packed = packed; a.stream = static_cast<cudaStream_t>(o.stream);
+    a.packed = packed; a.stream = static_cast<cudaStream_t>(o.stream); a.status = status;
     record(o, 0, a.stream);
     const cudaError_t e = launch_conv_fwd(a);
     record(o, 1, a.stream);

@@ -2,7 +2,7 @@
 // out = self.norm(out, z) with GatedRMSNorm, and the parts table: "the output is normalised per head
 // and then multiplied by the gate silu(z)"):
 //     y_j = o_j / sqrt(mean_j(o_j^2) + eps) * w_j * silu(z_j)      over the dv values of one (token, head)
-// A memory-bound pass over `out` in place (one warp per row), used after the prefill kernels, whose
+// A memory-bound pass over `out` in place (16-byte vectors, a lane group per row), used after the prefill kernels, whose
 // outputs are split across CTAs by value columns.  The decode kernel applies the same gate in its
 // own epilogue.
 #include "gdn_internal.cuh"
@@ -10,46 +10,85 @@
 namespace gdn {
 namespace {
 
-constexpr int kRowsPerBlock = 8;
+constexpr int kWarps = 8;
+constexpr int kRowsPerThread = 2;   // independent rows per thread, for loads in flight
+
+// 16-byte vectors: a group of DV / VEC lanes holds one row; a warp holds 32 / (DV / VEC) rows per pass.
+template <typename T>
+struct Vec16 {
+    static constexpr int N = 16 / sizeof(T);
+    __device__ static void load(const T* p, float* f) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+        for (int e = 0; e < N; ++e) f[e] = to_f32(h[e]);
+    }
+    __device__ static void store(T* p, const float* f) {
+        uint4 u;
+        T* h = reinterpret_cast<T*>(&u);
+#pragma unroll
+        for (int e = 0; e < N; ++e) h[e] = from_f32<T>(f[e]);
+        *reinterpret_cast<uint4*>(p) = u;
+    }
+};
 
 template <int DV, typename T>
-__global__ void __launch_bounds__(32 * kRowsPerBlock)
+__global__ void __launch_bounds__(32 * kWarps)
 output_gate_kernel(T* __restrict__ out, const T* __restrict__ z, const float* __restrict__ w, float eps,
                    long long rows) {
-    constexpr int PER = DV / 32;
-    const long long row = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (row >= rows) return;
-    const int lane = threadIdx.x & 31;
-    T* orow = out + row * DV + lane * PER;
-    const T* zrow = z + row * DV + lane * PER;
-    float o[PER], zz[PER];
-    float ss = 0.f;
+    constexpr int VEC = Vec16<T>::N;
+    constexpr int LPR = DV / VEC;          // lanes per row
+    constexpr int RPW = 32 / LPR;          // rows per warp and pass
+    static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must split evenly over a warp");
+    const int lane = threadIdx.x & 31, sub = lane % LPR;
+    const long long warp = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    float wv[VEC];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-        o[e] = to_f32(orow[e]);
-        zz[e] = to_f32(zrow[e]);
-        ss = fmaf(o[e], o[e], ss);
+    for (int e = 0; e < VEC; ++e) wv[e] = w[sub * VEC + e];
+    long long row[kRowsPerThread];
+    float o[kRowsPerThread][VEC], zz[kRowsPerThread][VEC], ss[kRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+        row[r] = (warp * kRowsPerThread + r) * RPW + lane / LPR;
+        ss[r] = 0.f;
+        if (row[r] < rows) {
+            Vec16<T>::load(out + row[r] * DV + sub * VEC, o[r]);
+            Vec16<T>::load(z + row[r] * DV + sub * VEC, zz[r]);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) ss[r] = fmaf(o[r][e], o[r][e], ss[r]);
+        }
     }
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    const float inv = rsqrtf(ss / (float)DV + eps);
+    for (int r = 0; r < kRowsPerThread; ++r) {
 #pragma unroll
-    for (int e = 0; e < PER; ++e) orow[e] = from_f32<T>(o[e] * inv * w[lane * PER + e] * silu_f(zz[e]));
+        for (int m = LPR / 2; m > 0; m >>= 1) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], m);
+        if (row[r] >= rows) continue;
+        const float inv = rsqrtf(ss[r] / (float)DV + eps);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o[r][e] = o[r][e] * inv * wv[e] * silu_f(zz[r][e]);
+        Vec16<T>::store(out + row[r] * DV + sub * VEC, o[r]);
+    }
+}
+
+template <int DV, typename T>
+cudaError_t launch_dv(void* out, const void* z, const float* w, float eps, long long rows, cudaStream_t stream) {
+    constexpr int RPW = 32 / (DV / Vec16<T>::N);
+    const long long per_block = (long long)kWarps * kRowsPerThread * RPW;
+    const unsigned blocks = (unsigned)((rows + per_block - 1) / per_block);
+    output_gate_kernel<DV, T><<<blocks, 32 * kWarps, 0, stream>>>(static_cast<T*>(out), static_cast<const T*>(z), w,
+                                                                  eps, rows);
+    return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_typed(void* out, const void* z, const float* w, float eps, long long rows, int dv,
                          cudaStream_t stream) {
-    const unsigned blocks = (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock);
-    if (dv == 32)
-        output_gate_kernel<32, T><<<blocks, 32 * kRowsPerBlock, 0, stream>>>(static_cast<T*>(out), static_cast<const T*>(z), w, eps, rows);
-    else if (dv == 64)
-        output_gate_kernel<64, T><<<blocks, 32 * kRowsPerBlock, 0, stream>>>(static_cast<T*>(out), static_cast<const T*>(z), w, eps, rows);
-    else if (dv == 128)
-        output_gate_kernel<128, T><<<blocks, 32 * kRowsPerBlock, 0, stream>>>(static_cast<T*>(out), static_cast<const T*>(z), w, eps, rows);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    switch (dv) {
+        case 32: return launch_dv<32, T>(out, z, w, eps, rows, stream);
+        case 64: return launch_dv<64, T>(out, z, w, eps, rows, stream);
+        case 128: return launch_dv<128, T>(out, z, w, eps, rows, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace

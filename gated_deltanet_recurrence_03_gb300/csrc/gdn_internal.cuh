@@ -76,6 +76,7 @@ struct ConvArgs {
     int num_seqs;
     bool packed;
     cudaStream_t stream;
+    unsigned* status;           // device status word (bounded waits)
 };
 
 // Launchers (return the launch error, cudaSuccess if enqueued).

@@ -51,6 +51,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Wait for phase `parity` of `bar` for at most limit_ns, ignoring any abort flag: used before a CTA
+// exits, so that no copy it issued is still writing its shared memory.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > limit_ns) return false;
+    return true;
+}
+
 // Wait for phase `parity` of `bar`, giving up after limit_ns.  On give-up the status word gets
 // `flag`, *abort is set, and false is returned; once *abort is set every later wait returns at
 // once, so a failed kernel drains quickly instead of waiting once per step.

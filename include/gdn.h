@@ -177,7 +177,7 @@ gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, 
  *              packed projection can be passed directly), 16-byte aligned
  *   w          [C, K] float; w[c, K-1] weighs the current token
  *   cache_in   [nseq, K-1, C] dtype or NULL: the K-1 inputs preceding each sequence, oldest first
- *   y          [B, T, C] dtype
+ *   y          [B, T, C] dtype; must not overlap x or either cache
  *   cache_out  [nseq, K-1, C] dtype or NULL: the last K-1 inputs of each sequence (what a decode step
  *              needs next; for sequences shorter than K-1 the older entries come from cache_in)
  * nseq = B, or num_seqs with opts->cu_seqlens (B == 1, packed sequences, state reset at each start).
