@@ -535,6 +535,25 @@ def run_profile_case(case):
         ws = torch.empty(gdn.workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv), dtype=torch.uint8, device=dev)
         for _ in range(2):
             gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, workspace=ws)
+    elif case == "layer":
+        # the conv of the packed q/k/v projection (three channel slices) and the prefill with the
+        # fused front end and the output gate, twice
+        w = PREFILL
+        x = device_inputs_random(torch, dev, w)
+        Cq, Cv = w.Hqk * w.dk, w.Hv * w.dv
+        proj = torch.randn(w.B, w.T, 2 * Cq + Cv, device=dev).to(torch.bfloat16)
+        cw = 0.5 * torch.randn(2 * Cq + Cv, 4, device=dev)
+        S0 = 0.1 * torch.randn(w.B, w.Hv, w.dk, w.dv, device=dev)
+        ws = torch.empty(gdn.workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv), dtype=torch.uint8, device=dev)
+        z = torch.randn_like(x["v"])
+        A_log, dt_bias = -0.5 + 0.5 * torch.randn(w.Hv, device=dev), 0.5 * torch.randn(w.Hv, device=dev)
+        nw = 1.0 + 0.1 * torch.randn(w.dv, device=dev)
+        for _ in range(2):
+            for (c0, c1), dst in zip(((0, Cq), (Cq, 2 * Cq), (2 * Cq, 2 * Cq + Cv)), ("q", "k", "v")):
+                gdn.gdn_causal_conv1d_fwd(proj[:, :, c0:c1], cw[c0:c1].contiguous(), None,
+                                          out=x[dst].view(w.B, w.T, c1 - c0), return_cache=False)
+            gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, workspace=ws, normalize_qk=True,
+                              raw_gates=(A_log, dt_bias), output_gate=(z, nw, 1e-6))
     else:
         w = DECODE
         x = device_inputs_random(torch, dev, w, steps=2, seed=2)
@@ -554,7 +573,7 @@ def main():
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile-case", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "layer"], default=None,
                     help="run one warm-up and one measured call of one kernel family (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_case:
