@@ -18,7 +18,8 @@ GDN_OUTPUT_GATE = 0x4
 
 EXPORTED = ("gdn_opts_init", "gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step",
             "gdn_check_device_status", "gdn_status_string", "gdn_last_error", "gdn_version",
-            "gdn_chunk_fwd_noalloc", "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_step")
+            "gdn_chunk_fwd_noalloc", "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_step",
+            "gdn_recurrent_bwd", "gdn_recurrent_bwd_workspace_size")
 
 
 class GdnOpts(ctypes.Structure):
@@ -73,6 +74,10 @@ def load(path: str = LIB_PATH):
     lib.gdn_causal_conv1d_fwd.restype = i
     lib.gdn_causal_conv1d_step.argtypes = [vp, ll, vp, vp, vp, i, i, i, opts_p]
     lib.gdn_causal_conv1d_step.restype = i
+    lib.gdn_recurrent_bwd.argtypes = [vp] * 14 + [i, i, i, i, i, i, opts_p]
+    lib.gdn_recurrent_bwd.restype = i
+    lib.gdn_recurrent_bwd_workspace_size.argtypes = [i, i, i, i, i, i, opts_p]
+    lib.gdn_recurrent_bwd_workspace_size.restype = ctypes.c_size_t
     lib.gdn_chunk_fwd_workspace_size.argtypes = [i, i, i, i, i, i, opts_p]
     lib.gdn_chunk_fwd_workspace_size.restype = ctypes.c_size_t
     lib.gdn_recurrent_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, opts_p]

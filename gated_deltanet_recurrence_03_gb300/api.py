@@ -254,3 +254,67 @@ def gdn_causal_conv1d_step(x: torch.Tensor, w: torch.Tensor, cache: torch.Tensor
         del keep
         L.check(lib, st)
     return out
+
+
+def backward_workspace_size(B: int, T: int, Hqk: int, Hv: int, dk: int, dv: int, *,
+                            num_seqs: Optional[int] = None) -> int:
+    """Bytes of device scratch gdn_recurrent_bwd needs."""
+    lib = L.load()
+    o = L.default_opts(lib)
+    if num_seqs is not None:
+        o.cu_seqlens = 1   # only tested for NULL
+        o.num_seqs = int(num_seqs)
+    return int(lib.gdn_recurrent_bwd_workspace_size(B, T, Hqk, Hv, dk, dv, ctypes.byref(o)))
+
+
+def gdn_recurrent_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                      S0: Optional[torch.Tensor], grad_out: torch.Tensor, grad_S_final: Optional[torch.Tensor] = None,
+                      *, scale: float = 1.0, cu_seqlens: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, want_grad_S0: bool = True,
+                      stream: Optional[torch.cuda.Stream] = None, events: Optional[Sequence[int]] = None):
+    """Gradients of a loss on (out, S_final) of gdn_chunk_fwd with respect to q, k, v, g, beta, S0.
+    Inputs as for gdn_chunk_fwd; grad_out like v; grad_S_final fp32 like S_final or None.  Returns fp32
+    (grad_q, grad_k, grad_v, grad_g, grad_beta, grad_S0 or None)."""
+    lib = L.load()
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, T, H, d]")
+    B, T, Hqk, dk = q.shape
+    Hv, dv = int(v.shape[2]), int(v.shape[3])
+    dev, dt = q.device, q.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    _need("q", q, dt, dev, (B, T, Hqk, dk))
+    _need("k", k, dt, dev, (B, T, Hqk, dk))
+    _need("v", v, dt, dev, (B, T, Hv, dv))
+    _need("g", g, dt, dev, (B, T, Hv))
+    _need("beta", beta, dt, dev, (B, T, Hv))
+    _need("grad_out", grad_out, dt, dev, (B, T, Hv, dv))
+    nseq = B
+    if cu_seqlens is not None:
+        nseq = int(cu_seqlens.numel()) - 1
+        _need("cu_seqlens", cu_seqlens, torch.int32, dev, (nseq + 1,))
+    if S0 is not None:
+        _need("S0", S0, torch.float32, dev, (nseq, Hv, dk, dv))
+    if grad_S_final is not None:
+        _need("grad_S_final", grad_S_final, torch.float32, dev, (nseq, Hv, dk, dv))
+    f32 = dict(dtype=torch.float32, device=dev)
+    gq, gk = torch.empty((B, T, Hqk, dk), **f32), torch.empty((B, T, Hqk, dk), **f32)
+    gv = torch.empty((B, T, Hv, dv), **f32)
+    gg, gb = torch.empty((B, T, Hv), **f32), torch.empty((B, T, Hv), **f32)
+    gS0 = torch.empty((nseq, Hv, dk, dv), **f32) if want_grad_S0 else None
+    with torch.cuda.device(dev):
+        o, keep = _opts(lib, dt, scale, 64, False, stream, dev, events)
+        if cu_seqlens is not None:
+            o.cu_seqlens = cu_seqlens.data_ptr()
+            o.num_seqs = nseq
+        need = int(lib.gdn_recurrent_bwd_workspace_size(B, T, Hqk, Hv, dk, dv, ctypes.byref(o)))
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel()
+        st = lib.gdn_recurrent_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0), _ptr(grad_out),
+                                   _ptr(grad_S_final), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gg), _ptr(gb), _ptr(gS0),
+                                   B, T, Hqk, Hv, dk, dv, ctypes.byref(o))
+        del keep
+        L.check(lib, st)
+    return gq, gk, gv, gg, gb, gS0

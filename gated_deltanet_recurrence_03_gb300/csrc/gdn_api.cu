@@ -322,6 +322,64 @@ gdn_status_t gdn_causal_conv1d_step(const void* x, long long x_stride, const flo
     return GDN_OK;
 }
 
+size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts) {
+    const gdn_opts_t o = resolve(opts);
+    if (B < 0 || T < 0 || Hqk <= 0 || Hv <= 0 || Hv % Hqk || !dim_ok(dk) || !dim_ok(dv)) return 0;
+    const bool packed = o.cu_seqlens != nullptr;
+    const int nseq = packed ? o.num_seqs : B;
+    if (nseq <= 0) return 0;
+    return backward_layout(B, T, Hv, dk, dv, nseq, packed).total;
+}
+
+gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                               const float* S0, const void* grad_out, const float* grad_S_final, float* grad_q,
+                               float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_S0, int B,
+                               int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_opts_t o = resolve(opts);
+    if (B < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "B=%d T=%d must be >= 0", B, T);
+    gdn_status_t st = check_common(Hqk, Hv, dk, dv, o);
+    if (st != GDN_OK) return st;
+    if (o.flags) return fail(GDN_ERR_UNSUPPORTED, "the backward pass takes no option flags (0x%x given)", o.flags);
+    const bool packed = o.cu_seqlens != nullptr;
+    if (packed && (B != 1 || o.num_seqs < 1))
+        return fail(GDN_ERR_INVALID_ARG, "cu_seqlens needs B == 1 and num_seqs >= 1 (B=%d num_seqs=%d)", B, o.num_seqs);
+    const int nseq = packed ? o.num_seqs : B;
+    const bool have_tokens = (long long)B * T > 0;
+    if (have_tokens && (!q || !k || !v || !g || !beta || !grad_out || !grad_q || !grad_k || !grad_v || !grad_g ||
+                        !grad_beta))
+        return fail(GDN_ERR_INVALID_ARG, "null input or gradient pointer");
+    const unsigned e = elem_bytes(o.dtype);
+    const void* in_ptrs[] = {q, k, v, g, beta, grad_out};
+    for (const void* p : in_ptrs)
+        if (p && !aligned_to(p, e)) return fail(GDN_ERR_INVALID_ARG, "input %p not aligned to its element size", p);
+    const void* f_ptrs[] = {S0, grad_S_final, grad_q, grad_k, grad_v, grad_g, grad_beta, grad_S0, o.cu_seqlens};
+    for (const void* p : f_ptrs)
+        if (p && !aligned_to(p, 4)) return fail(GDN_ERR_INVALID_ARG, "pointer %p not 4-byte aligned", p);
+    if (nseq == 0) return GDN_OK;
+    const size_t need = backward_layout(B, T, Hv, dk, dv, nseq, packed).total;
+    if (!o.workspace || o.workspace_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    o.workspace ? o.workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0)
+        return fail(GDN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    unsigned* status = nullptr;
+    st = device_ready(&status);
+    if (st != GDN_OK) return st;
+    BackwardArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.S0 = S0; a.dout = grad_out; a.dS_final = grad_S_final;
+    a.grad_q = grad_q; a.grad_k = grad_k; a.grad_v = grad_v; a.grad_g = grad_g; a.grad_beta = grad_beta;
+    a.grad_S0 = grad_S0;
+    a.B = B; a.T = T; a.Hqk = Hqk; a.Hv = Hv; a.dk = dk; a.dv = dv; a.dtype = o.dtype; a.scale = o.scale;
+    a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq; a.workspace = o.workspace;
+    a.stream = static_cast<cudaStream_t>(o.stream);
+    record(o, 0, a.stream);
+    const cudaError_t err = launch_backward(a);
+    record(o, 1, a.stream);
+    if (err != cudaSuccess) return cuda_fail(err, "backward launch");
+    return GDN_OK;
+}
+
 gdn_status_t gdn_check_device_status(void* stream) {
     t_last_error[0] = 0;
     unsigned* status = nullptr;

@@ -5,12 +5,17 @@
 //     y[t, c] = silu( sum_{i=0}^{K-1} w[c, i] * x[t - (K - 1) + i, c] )
 // with x before a sequence's first token taken from that sequence's cache (or zero).
 //
-// Memory bound (2 bytes read and written per element, ~10 instructions).  Forward pass: a persistent
-// grid of two CTAs per SM walks tiles of 64 tokens x 512 bytes of channels.  A producer warp streams
-// each tile plus its K - 1 halo rows into a 3-stage shared-memory ring with one bulk copy per token
-// row (mbarrier completion); eight consumer warps each take a run of 8 tokens across the tile's 32
-// channel vectors of 16 bytes, slide the K-row window in registers, and store 512-byte rows of y.
+// Memory bound (2 bytes read and written per element, ~6 instructions).  Forward pass: a persistent
+// grid of one CTA per SM walks tiles of 128 tokens x 512 bytes of channels, in token-major order.
+// Each tile plus its K - 1 halo rows arrives in a 3-stage shared-memory ring by one 2-D TMA copy
+// (rows before the first token or past the last come back as zeros; mbarrier completion), issued by
+// one thread once all eight warps have released the stage.  Each warp takes a run of 16 tokens
+// across the tile's 32 channel vectors of 16 bytes, slides the K-row window in registers (packed
+// fp32x2 arithmetic) and streams 512-byte rows of y out.
 // Decode step: one thread per 16-byte channel vector of one sequence, cache shifted in place.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "gdn_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -20,53 +25,57 @@ namespace {
 using namespace tc;
 
 constexpr int kRowBytes = 512;                    // channel slice of one tile row
-constexpr int kTileTokens = 64;
+constexpr int kTileTokens = 128;
 constexpr int kHalo = 3;                          // rows kept before the tile (K - 1 <= 3)
 constexpr int kStageRows = kTileTokens + kHalo;
 constexpr int kStageBytes = kStageRows * kRowBytes;
 constexpr int kStages = 3;
 constexpr int kConsumerWarps = 8;                 // one run of kTileTokens / 8 tokens each
 constexpr int kRunTokens = kTileTokens / kConsumerWarps;
-constexpr int kFwdThreads = 32 * (kConsumerWarps + 1);
+constexpr int kFwdThreads = 32 * kConsumerWarps;   // lane 0 of warp 0 also issues the tile copies
 constexpr int kBarOffset = kStages * kStageBytes;
 constexpr int kFwdSmem = kBarOffset + 2 * kStages * 8 + 16;
 constexpr int kStepThreads = 128;
 static_assert(kRowBytes / 16 == 32, "a warp covers one tile row with 16-byte vectors");
-static_assert(2 * kFwdSmem + 2048 <= 228 * 1024, "two CTAs per SM");
+static_assert(kFwdSmem <= 227 * 1024, "one CTA per SM");
 
 template <typename T>
 struct Vec;
 template <>
 struct Vec<__nv_bfloat16> {
     static constexpr int N = 8;
-    __device__ static void unpack(const uint4& u, float* f) {
-        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
+    // channel pairs: a bf16 widens to fp32 by a 16-bit shift
+    __device__ static void unpack2(const uint4& u, float2* f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(h[e]);
+        for (int p = 0; p < 4; ++p) f[p] = make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
     }
-    __device__ static uint4 pack(const float* f) {
-        uint4 u;
-        __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&u);
+    __device__ static uint4 pack2(const float2* f) {
+        uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) h[e] = __float2bfloat16_rn(f[e]);
-        return u;
+        for (int p = 0; p < 4; ++p) {
+            const __nv_bfloat162 h = __float22bfloat162_rn(f[p]);
+            w[p] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
 template <>
 struct Vec<float> {
     static constexpr int N = 4;
-    __device__ static void unpack(const uint4& u, float* f) {
-        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    __device__ static void unpack2(const uint4& u, float2* f) {
+        f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
     }
-    __device__ static uint4 pack(const float* f) {
-        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+    __device__ static uint4 pack2(const float2* f) {
+        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x), __float_as_uint(f[1].y));
     }
 };
 
 template <typename T>
-__device__ __forceinline__ void load_vec(const T* p, float* f) { Vec<T>::unpack(*reinterpret_cast<const uint4*>(p), f); }
+__device__ __forceinline__ void load_vec(const T* p, float2* f) { Vec<T>::unpack2(*reinterpret_cast<const uint4*>(p), f); }
 template <typename T>
-__device__ __forceinline__ void store_vec(T* p, const float* f) { *reinterpret_cast<uint4*>(p) = Vec<T>::pack(f); }
+__device__ __forceinline__ void store_vec(T* p, const float2* f) { __stcs(reinterpret_cast<uint4*>(p), Vec<T>::pack2(f)); }
 
 // Sequence containing token t (largest i with start_i <= t, sequences sorted by start).
 __device__ __forceinline__ int seq_of(const int32_t* cu, int nseq, int T_len, long long t) {
@@ -82,46 +91,49 @@ __device__ __forceinline__ int seq_of(const int32_t* cu, int nseq, int T_len, lo
 
 // Cached input j (0 = oldest of the K - 1) of sequence s, zeros without a cache.
 template <typename T, int K>
-__device__ __forceinline__ void load_cached(const T* cache_in, int s, int j, int C, int c0, float (&f)[Vec<T>::N]) {
+__device__ __forceinline__ void load_cached(const T* cache_in, int s, int j, int C, int c0, float2 (&f)[Vec<T>::N / 2]) {
     if (cache_in) {
         load_vec(cache_in + ((size_t)s * (K - 1) + j) * C + c0, f);
     } else {
 #pragma unroll
-        for (int e = 0; e < Vec<T>::N; ++e) f[e] = 0.f;
+        for (int p = 0; p < Vec<T>::N / 2; ++p) f[p] = make_float2(0.f, 0.f);
     }
 }
 
-// SiLU for the output type: exact (ex2 + reciprocal) for fp32 outputs; for bf16 outputs one MUFU op,
-// silu(z) = z/2 * (1 + tanh(z/2)) with the hardware tanh (relative error ~2^-11, below the 2^-9
-// rounding of a bf16 result), which halves the special-function work that otherwise caps the kernel.
+// SiLU of a channel pair for the output type: exact (ex2 + reciprocal) for fp32 outputs; for bf16
+// outputs one MUFU op per value, silu(z) = z/2 * (1 + tanh(z/2)) with the hardware tanh (relative
+// error ~2^-11, below the 2^-9 rounding of a bf16 result), which halves the special-function work
+// that otherwise caps the kernel.
 template <typename T>
-__device__ __forceinline__ float silu_out(float z) { return silu_f(z); }
+__device__ __forceinline__ float2 silu_out2(float2 z) { return make_float2(silu_f(z.x), silu_f(z.y)); }
 template <>
-__device__ __forceinline__ float silu_out<__nv_bfloat16>(float z) {
-    const float h = 0.5f * z;
-    float th;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(h));
-    return fmaf(h, th, h);
+__device__ __forceinline__ float2 silu_out2<__nv_bfloat16>(float2 z) {
+    const float2 h = __fmul2_rn(z, make_float2(0.5f, 0.5f));
+    float2 th;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(th.x) : "f"(h.x));
+    asm("tanh.approx.f32 %0, %1;" : "=f"(th.y) : "f"(h.y));
+    return __ffma2_rn(h, th, h);
 }
 
+// Channel pairs of one 16-byte vector; the K taps as packed fp32x2 multiply-adds, oldest first.
 template <typename T, int K>
-__device__ __forceinline__ void conv_out(const float (&wr)[K][Vec<T>::N], const float (&hist)[K][Vec<T>::N],
-                                         float (&out)[Vec<T>::N]) {
+__device__ __forceinline__ void conv_out(const float2 (&wr)[K][Vec<T>::N / 2], const float2 (&hist)[K][Vec<T>::N / 2],
+                                         float2 (&out)[Vec<T>::N / 2]) {
 #pragma unroll
-    for (int e = 0; e < Vec<T>::N; ++e) {
-        float acc = 0.f;
+    for (int p = 0; p < Vec<T>::N / 2; ++p) {
+        float2 acc = __fmul2_rn(wr[0][p], hist[0][p]);
 #pragma unroll
-        for (int i = 0; i < K; ++i) acc = fmaf(wr[i][e], hist[i][e], acc);
-        out[e] = silu_out<T>(acc);
+        for (int i = 1; i < K; ++i) acc = __ffma2_rn(wr[i][p], hist[i][p], acc);
+        out[p] = silu_out2<T>(acc);
     }
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kFwdThreads, 2)
-conv_fwd_kernel(const T* __restrict__ x, long long x_stride, const float* __restrict__ w,
+__global__ void __launch_bounds__(kFwdThreads, 1)
+conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restrict__ w,
                 const T* __restrict__ cache_in, T* __restrict__ y, T* __restrict__ cache_out,
                 const int32_t* __restrict__ cu, int nseq, int T_len, long long Ttot, int C, unsigned* status) {
-    constexpr int V = Vec<T>::N;
+    constexpr int V = Vec<T>::N, P = V / 2;
     constexpr int CW = kRowBytes / (int)sizeof(T);      // channels per tile
     extern __shared__ __align__(1024) uint8_t sm[];
     const uint32_t sbase = smem_u32(sm);
@@ -132,8 +144,11 @@ conv_fwd_kernel(const T* __restrict__ x, long long x_stride, const float* __rest
     const int n_cg = (C + CW - 1) / CW;
     const long long n_tt = (Ttot + kTileTokens - 1) / kTileTokens;
     const long long tiles = (long long)n_cg * n_tt;
-    // contiguous tile range of this CTA (channel group major, so weights change rarely)
-    const long long first = tiles * blockIdx.x / gridDim.x, last = tiles * (blockIdx.x + 1) / gridDim.x;
+    // tiles in token-major order (tile i = token tile i / n_cg, channel group i % n_cg), CTA b taking
+    // b, b + G, b + 2G, ...: the CTAs in flight together read whole token rows, and when G is a
+    // multiple of n_cg each CTA keeps one channel group (and its weights) throughout
+    const long long G = gridDim.x;
+    const long long my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / G + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -145,30 +160,17 @@ conv_fwd_kernel(const T* __restrict__ x, long long x_stride, const float* __rest
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
-        // ---------------- producer: one bulk copy per token row of each tile
-        for (long long i = first; i < last; ++i) {
-            const int st = (int)((i - first) % kStages);
-            const uint32_t ph = (uint32_t)(((i - first) / kStages) & 1);
-            mbar_wait_bounded(bar_empty + 8 * st, ph ^ 1u, abort_flag, status, kStatusTimeout, kWaitLimitNs);
-            const int cg = (int)(i / n_tt);
-            const long long t0 = (i % n_tt) * kTileTokens;
-            const long long r_lo = max(0LL, t0 - kHalo), r_hi = min(Ttot, t0 + kTileTokens);
-            const uint32_t rb = (uint32_t)(min(CW, C - cg * CW) * (int)sizeof(T));
-            if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, (uint32_t)(r_hi - r_lo) * rb);
-            __syncwarp();
-            for (long long r = r_lo + lane; r < r_hi; r += 32)
-                bulk_g2s(sbase + st * kStageBytes + (uint32_t)(r - (t0 - kHalo)) * kRowBytes,
-                         x + r * x_stride + (size_t)cg * CW, rb, bar_full + 8 * st);
-        }
-        // no copy of this CTA may still be writing shared memory when it exits
-        if (lane == 0) {
-            const long long n = last - first;
-            for (long long j = max(0LL, n - kStages); j < n; ++j)
-                mbar_wait_drain(bar_full + 8 * (uint32_t)(j % kStages), (uint32_t)((j / kStages) & 1), kWaitLimitNs);
-        }
-        return;
-    }
+    // one 2-D TMA copy per tile: 67 rows x 512 bytes, row 0 = token t0 - kHalo
+    const bool producer = threadIdx.x == 0;
+    const auto issue = [&](long long n) {
+        const long long i = blockIdx.x + n * G;
+        const int st = (int)(n % kStages);
+        mbar_arrive_expect_tx(bar_full + 8 * st, kStageBytes);
+        tma_load_2d(sbase + st * kStageBytes, &xmap, (int)(i % n_cg) * CW, (int)((i / n_cg) * kTileTokens - kHalo),
+                    bar_full + 8 * st);
+    };
+    if (producer)
+        for (long long n = 0; n < min((long long)kStages, my_tiles); ++n) issue(n);
 
     // ---------------- consumers
     if (blockIdx.x == 0 && cache_out) {
@@ -177,28 +179,30 @@ conv_fwd_kernel(const T* __restrict__ x, long long x_stride, const float* __rest
             long long a, b;
             seq_range(cu, s, T_len, a, b);
             if (b > a) continue;
-            for (int idx = threadIdx.x; idx < (K - 1) * (C / V); idx += 32 * kConsumerWarps) {
+            for (int idx = threadIdx.x; idx < (K - 1) * (C / V); idx += kFwdThreads) {
                 const int j = idx / (C / V), c0 = (idx % (C / V)) * V;
-                float f[V];
+                float2 f[P];
                 load_cached<T, K>(cache_in, s, j, C, c0, f);
                 store_vec(cache_out + ((size_t)s * (K - 1) + j) * C + c0, f);
             }
         }
     }
-    float wr[K][V];
+    float2 wr[K][P];
     int cg_loaded = -1;
-    for (long long i = first; i < last; ++i) {
-        const int st = (int)((i - first) % kStages);
-        const uint32_t ph = (uint32_t)(((i - first) / kStages) & 1);
-        const int cg = (int)(i / n_tt);
-        const long long t0 = (i % n_tt) * kTileTokens;
+    for (long long n = 0; n < my_tiles; ++n) {
+        const long long i = blockIdx.x + n * G;
+        const int st = (int)(n % kStages);
+        const uint32_t ph = (uint32_t)((n / kStages) & 1);
+        const int cg = (int)(i % n_cg);
+        const long long t0 = (i / n_cg) * kTileTokens;
         const int c0 = cg * CW + lane * V;
         const bool active = c0 < C;
         if (cg != cg_loaded && active) {
 #pragma unroll
-            for (int e = 0; e < V; ++e)
+            for (int p = 0; p < P; ++p)
 #pragma unroll
-                for (int k = 0; k < K; ++k) wr[k][e] = __ldg(w + (size_t)(c0 + e) * K + k);
+                for (int k = 0; k < K; ++k)
+                    wr[k][p] = make_float2(__ldg(w + (size_t)(c0 + 2 * p) * K + k), __ldg(w + (size_t)(c0 + 2 * p + 1) * K + k));
             cg_loaded = cg;
         }
         mbar_wait_bounded(bar_full + 8 * st, ph, abort_flag, status, kStatusTimeout, kWaitLimitNs);
@@ -216,19 +220,19 @@ conv_fwd_kernel(const T* __restrict__ x, long long x_stride, const float* __rest
         if (active && t_end - t == kRunTokens && s0 <= t - (K - 1) && t + kRunTokens <= s1) {
             // common case: a whole run inside one sequence with its history in the tile; fully
             // unrolled, so the window slides by renaming registers
-            float hist[K][V];
+            float2 hist[K][P];
 #pragma unroll
-            for (int k = 0; k < K - 1; ++k) Vec<T>::unpack(row(t - (K - 1) + k), hist[k]);
+            for (int k = 0; k < K - 1; ++k) Vec<T>::unpack2(row(t - (K - 1) + k), hist[k]);
 #pragma unroll
             for (int j = 0; j < kRunTokens; ++j) {
-                Vec<T>::unpack(row(t + j), hist[K - 1]);
-                float out[V];
+                Vec<T>::unpack2(row(t + j), hist[K - 1]);
+                float2 out[P];
                 conv_out<T, K>(wr, hist, out);
                 store_vec(y + (t + j) * C + c0, out);
 #pragma unroll
                 for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-                    for (int e = 0; e < V; ++e) hist[k][e] = hist[k + 1][e];
+                    for (int p = 0; p < P; ++p) hist[k][p] = hist[k + 1][p];
             }
             if (cache_out && t + kRunTokens == s1) {
 #pragma unroll
@@ -241,26 +245,26 @@ conv_fwd_kernel(const T* __restrict__ x, long long x_stride, const float* __rest
                 s = seq_of(cu, nseq, T_len, t);
                 seq_range(cu, s, T_len, s0, s1);
             }
-            float hist[K][V];   // hist[K-1] = current token, hist[0] = oldest
+            float2 hist[K][P];   // hist[K-1] = current token, hist[0] = oldest
 #pragma unroll
             for (int k = 0; k < K - 1; ++k) {
                 const long long src = t - (K - 1) + k;
                 if (src >= s0)
-                    Vec<T>::unpack(row(src), hist[k]);
+                    Vec<T>::unpack2(row(src), hist[k]);
                 else
                     load_cached<T, K>(cache_in, s, (int)(K - 1 - (s0 - src)), C, c0, hist[k]);
             }
             const long long seg_end = min(t_end, s1);
 #pragma unroll 1
             for (; t < seg_end; ++t) {
-                Vec<T>::unpack(row(t), hist[K - 1]);
-                float out[V];
+                Vec<T>::unpack2(row(t), hist[K - 1]);
+                float2 out[P];
                 conv_out<T, K>(wr, hist, out);
                 store_vec(y + t * C + c0, out);
 #pragma unroll
                 for (int k = 0; k < K - 1; ++k)
 #pragma unroll
-                    for (int e = 0; e < V; ++e) hist[k][e] = hist[k + 1][e];
+                    for (int p = 0; p < P; ++p) hist[k][p] = hist[k + 1][p];
             }
             if (cache_out && seg_end == s1) {   // the sequence ended here: keep its last K - 1 inputs
 #pragma unroll
@@ -269,28 +273,37 @@ conv_fwd_kernel(const T* __restrict__ x, long long x_stride, const float* __rest
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+        if (producer && n + kStages < my_tiles) {   // refill the stage once every warp has left it
+            mbar_wait_bounded(bar_empty + 8 * st, ph, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+            issue(n + kStages);
+        }
     }
+    // no copy of this CTA may still be writing shared memory when it exits
+    if (producer)
+        for (long long j = max(0LL, my_tiles - kStages); j < my_tiles; ++j)
+            mbar_wait_drain(bar_full + 8 * (uint32_t)(j % kStages), (uint32_t)((j / kStages) & 1), kWaitLimitNs);
 }
 
 template <typename T, int K>
 __global__ void __launch_bounds__(kStepThreads)
 conv_step_kernel(const T* __restrict__ x, long long x_stride, const float* __restrict__ w, T* __restrict__ cache,
                  T* __restrict__ y, int N, int C) {
-    constexpr int V = Vec<T>::N;
+    constexpr int V = Vec<T>::N, P = V / 2;
     const int vec = blockIdx.x * blockDim.x + threadIdx.x;
     if (vec * V >= C) return;
     const int c0 = vec * V;
-    float wr[K][V];
+    float2 wr[K][P];
 #pragma unroll
-    for (int e = 0; e < V; ++e)
+    for (int p = 0; p < P; ++p)
 #pragma unroll
-        for (int k = 0; k < K; ++k) wr[k][e] = __ldg(w + (size_t)(c0 + e) * K + k);
+        for (int k = 0; k < K; ++k)
+            wr[k][p] = make_float2(__ldg(w + (size_t)(c0 + 2 * p) * K + k), __ldg(w + (size_t)(c0 + 2 * p + 1) * K + k));
     for (size_t n = blockIdx.y; n < (size_t)N; n += gridDim.y) {
-        float hist[K][V];
+        float2 hist[K][P];
 #pragma unroll
         for (int k = 0; k < K - 1; ++k) load_vec(cache + (n * (K - 1) + k) * C + c0, hist[k]);
         load_vec(x + (long long)n * x_stride + c0, hist[K - 1]);
-        float out[V];
+        float2 out[P];
         conv_out<T, K>(wr, hist, out);
         store_vec(y + n * C + c0, out);
 #pragma unroll
@@ -302,7 +315,8 @@ template <typename T, int K>
 cudaError_t fwd_typed(const ConvArgs& a) {
     const long long Ttot = a.packed ? (long long)a.T : (long long)a.B * a.T;
     constexpr int CW = kRowBytes / (int)sizeof(T);
-    const long long tiles = (long long)((a.C + CW - 1) / CW) * ((Ttot + kTileTokens - 1) / kTileTokens);
+    const long long n_cg = (a.C + CW - 1) / CW;
+    const long long tiles = n_cg * ((Ttot + kTileTokens - 1) / kTileTokens);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -310,10 +324,31 @@ cudaError_t fwd_typed(const ConvArgs& a) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(conv_fwd_kernel<T, K>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    // at least one CTA: it also passes the caches of sequences without tokens through
-    const unsigned grid = (unsigned)max(1LL, min(tiles, 2LL * sms));
+    // one CTA per SM, rounded down to a multiple of the channel groups when there are fewer groups
+    // than CTAs; at least one CTA, which also passes the caches of sequences without tokens through
+    long long G = sms;
+    if (n_cg <= G) G = G / n_cg * n_cg;
+    const unsigned grid = (unsigned)max(1LL, min(tiles, G));
+    // x as a 2-D tensor [Ttot rows, C channels] with a row pitch of x_stride elements; box of
+    // kStageRows rows x CW channels, zero fill outside
+    CUtensorMap xmap;
+    memset(&xmap, 0, sizeof(xmap));
+    if (tiles > 0) {
+        if (Ttot > (1LL << 31) - 2 * kTileTokens) return cudaErrorInvalidValue;   // TMA coordinates are 32-bit
+        auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+        if (!encode) return cudaErrorNotSupported;
+        const cuuint64_t dims[2] = {(cuuint64_t)a.C, (cuuint64_t)Ttot};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.x_stride * sizeof(T)};
+        const cuuint32_t box[2] = {(cuuint32_t)CW, (cuuint32_t)kStageRows};
+        const cuuint32_t elem[2] = {1, 1};
+        const CUresult r = encode(&xmap, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                  2, const_cast<void*>(a.x), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     conv_fwd_kernel<T, K><<<grid, kFwdThreads, kFwdSmem, a.stream>>>(
-        static_cast<const T*>(a.x), a.x_stride, a.w, static_cast<const T*>(a.cache_in), static_cast<T*>(a.y),
+        xmap, a.w, static_cast<const T*>(a.cache_in), static_cast<T*>(a.y),
         static_cast<T*>(a.cache_out), a.cu_seqlens, a.num_seqs, a.T, Ttot, a.C, a.status);
     return cudaGetLastError();
 }

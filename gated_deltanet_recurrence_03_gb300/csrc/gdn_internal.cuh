@@ -80,6 +80,41 @@ struct ConvArgs {
 };
 
 // Launchers (return the launch error, cudaSuccess if enqueued).
+struct BackwardArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* g;
+    const void* beta;
+    const float* S0;            // or nullptr (zero state)
+    const void* dout;           // gradient of out, v's dtype
+    const float* dS_final;      // gradient of S_final, or nullptr
+    float* grad_q;
+    float* grad_k;
+    float* grad_v;
+    float* grad_g;
+    float* grad_beta;
+    float* grad_S0;             // or nullptr
+    int B, T, Hqk, Hv, dk, dv;
+    int dtype;
+    float scale;
+    const int32_t* cu_seqlens;
+    int num_seqs;
+    void* workspace;
+    cudaStream_t stream;
+};
+
+// Workspace of the backward pass: state checkpoints every 16 tokens, the per-CTA chunk scratch and
+// the per-slice partial sums (byte offsets, 256-byte aligned).
+struct BwdLayout {
+    size_t ckpt_off, scratch_off, part_off, total;
+};
+BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed);
+cudaError_t launch_backward(const BackwardArgs& a);
+
+// The driver's cuTensorMapEncodeTiled (looked up once), or nullptr when the driver lacks it.
+void* tensor_map_encoder();
+
 cudaError_t launch_conv_fwd(const ConvArgs& a);
 cudaError_t launch_conv_step(const ConvArgs& a);
 cudaError_t launch_decode(const DecodeArgs& a);

@@ -774,17 +774,9 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
 
 cudaError_t get_encoder() {
-    std::call_once(g_encode_once, [] {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
     return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
@@ -819,6 +811,20 @@ size_t tc_prefill_workspace_bytes(int B, int T, int Hv, int num_seqs, bool packe
     const size_t a1 = (size_t)slots * Hv * kA1Bytes;
     const size_t vec = (size_t)slots * Hv * kVecFloats * sizeof(float);
     return a1 + vec;
+}
+
+void* tensor_map_encoder() {
+    static std::once_flag once;
+    static void* fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = f;
+    });
+    return fn;
 }
 
 cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_events) {

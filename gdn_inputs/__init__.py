@@ -76,6 +76,7 @@ _CHUNK = 1 << 22  # values generated per numpy batch (bounds temporary memory)
 STREAM_Q, STREAM_K, STREAM_V, STREAM_A, STREAM_B, STREAM_S0 = range(6)
 STREAM_RAW_A, STREAM_RAW_B, STREAM_A_LOG, STREAM_DT_BIAS = range(6, 10)
 STREAM_Z, STREAM_NORM_W = range(10, 12)
+STREAM_DOUT, STREAM_DSF = range(12, 14)
 
 
 def splitmix64(seed: int, idx: np.ndarray) -> np.ndarray:
@@ -293,3 +294,11 @@ def make_output_gate(w: Workload, out_shape):
     z = _rounded_normal(w.seed, STREAM_Z, tuple(out_shape), w.dtype)
     norm_w = round_to_dtype(_normal_tensor(w.seed, STREAM_NORM_W, (w.dv,), mean=1.0, std=0.1), "f32")
     return dict(z=z, norm_weight=norm_w)
+
+
+def make_backward_inputs(w: Workload):
+    """Upstream gradients for the backward pass: dout like the outputs (workload dtype), N(0,1), and
+    dS_final like the final states (fp32), N(0, 0.1^2)."""
+    dout = _rounded_normal(w.seed, STREAM_DOUT, (w.B, w.T, w.Hv, w.dv), w.dtype)
+    dSf = _rounded_normal(w.seed, STREAM_DSF, (w.num_seqs, w.Hv, w.dk, w.dv), "f32", std=0.1)
+    return dict(dout=dout, dSf=dSf)

@@ -196,6 +196,34 @@ gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const floa
 gdn_status_t gdn_causal_conv1d_step(const void* x, long long x_stride, const float* w, void* cache, void* y,
                                     int N, int C, int K, const gdn_opts_t* opts);
 
+/*
+ * gdn_recurrent_bwd -- the backward pass: gradients of a loss L(out, S_final) of gdn_chunk_fwd with
+ * respect to q, k, v, g, beta and S0, given grad_out = dL/dout and grad_S_final = dL/dS_final.  It is
+ * the adjoint of the token loop of "Transformer by Hand, ch. 7" (section "The formula"), which the
+ * learn-llm "linear attention" page trains through autograd:
+ *     lam = dL/dS_t;  lam += scale q_t do_t^T;  dq_t = scale S_t do_t;  dk_t = lam u_t + S_{t-1} dp;
+ *     dv_t = beta_t du;  dbeta_t = du.(v_t - a_t p_t);  dg_t = a_t (<lam, S_{t-1}> - beta_t du.p_t);
+ *     lam <- a_t lam + k_t dp^T;  dS0 = lam at the start,
+ * with p_t = S_{t-1}^T k_t, u_t = beta_t (v_t - a_t p_t), du = lam^T k_t, dp = -a_t beta_t du.
+ *
+ *   q, k, v, g, beta, S0, B, T, Hqk, Hv, dk, dv, cu_seqlens/num_seqs, scale, dtype: as gdn_chunk_fwd
+ *   grad_out       [B, T, Hv, dv] in the inputs' dtype
+ *   grad_S_final   [nseq, Hv, dk, dv] float, or NULL (no loss on the final state)
+ *   grad_q, grad_k [B, T, Hqk, dk] float (a query/key head sums over the value heads that read it)
+ *   grad_v         [B, T, Hv, dv] float;  grad_g, grad_beta [B, T, Hv] float
+ *   grad_S0        [nseq, Hv, dk, dv] float, or NULL (not written)
+ * Gradients are always fp32.  Pointers need only element alignment.  opts->flags must be 0 (the
+ * fused front end and output gate have no backward here).  The workspace (256-byte aligned,
+ * gdn_recurrent_bwd_workspace_size bytes) holds state checkpoints every 16 tokens, a chunk scratch
+ * per (sequence, head, 32-column slice) and per-slice partial sums; GDN_ERR_WORKSPACE if missing or
+ * too small.  Asynchronous on opts->stream; events[0] before and events[1] after the two kernels.
+ */
+size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts);
+gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
+                               const float* S0, const void* grad_out, const float* grad_S_final, float* grad_q,
+                               float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_S0,
+                               int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts);
+
 /* Synchronise `stream` (cudaStream_t, NULL = legacy), then read and clear the device status word
  * that kernels set when a bounded wait runs out.  GDN_OK if clear, GDN_ERR_TIMEOUT if set,
  * GDN_ERR_CUDA if the synchronisation itself failed. */

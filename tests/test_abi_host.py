@@ -160,3 +160,44 @@ def test_conv_step_argument_errors(lib, case, expect):
 def test_conv_empty_calls_do_nothing(lib):
     assert conv_fwd(lib, B=0, T=0, ptrs=[0] * 5) == pkg_lib.GDN_OK
     assert lib.gdn_causal_conv1d_step(0, 0, 0, 0, 0, 0, 64, 4, opts(lib)) == pkg_lib.GDN_OK
+
+
+def bwd(lib, B=1, T=8, Hqk=1, Hv=1, dk=32, dv=32, ptrs=None, **kw):
+    p = [FAKE] * 14 if ptrs is None else ptrs
+    return lib.gdn_recurrent_bwd(*p, B, T, Hqk, Hv, dk, dv, opts(lib, **kw))
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(B=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(Hqk=2, Hv=3), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(dk=48), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(flags=pkg_lib.GDN_NORMALIZE_QK), pkg_lib.GDN_ERR_UNSUPPORTED),     # no backward for the front end
+    (dict(flags=pkg_lib.GDN_OUTPUT_GATE, z=FAKE, norm_weight=FAKE), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(ptrs=[FAKE] * 8 + [0] + [FAKE] * 5), pkg_lib.GDN_ERR_INVALID_ARG),   # grad_q missing
+    (dict(ptrs=[FAKE + 1] + [FAKE] * 13), pkg_lib.GDN_ERR_INVALID_ARG),        # q not element aligned
+    (dict(ptrs=[FAKE] * 9 + [FAKE + 2] + [FAKE] * 4), pkg_lib.GDN_ERR_INVALID_ARG),   # grad_k not 4-byte aligned
+    (dict(B=2, cu_seqlens=FAKE, num_seqs=2), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(), pkg_lib.GDN_ERR_WORKSPACE),                                      # no workspace
+    (dict(workspace=FAKE, workspace_bytes=16), pkg_lib.GDN_ERR_WORKSPACE),    # too small
+])
+def test_backward_argument_errors(lib, case, expect):
+    assert bwd(lib, **case) == expect
+    assert lib.gdn_last_error() != b""
+
+
+def test_backward_optional_pointers_and_empty_calls(lib):
+    # S0, grad_S_final and grad_S0 may be NULL; no sequences is a no-op even with no buffers
+    assert bwd(lib, B=0, T=0, ptrs=[0] * 14) == pkg_lib.GDN_OK
+    p = [FAKE] * 14
+    p[5] = p[7] = p[13] = 0
+    assert bwd(lib, ptrs=p) == pkg_lib.GDN_ERR_WORKSPACE   # still validated up to the workspace
+
+
+def test_backward_workspace_size_is_pure_host(lib):
+    n = lib.gdn_recurrent_bwd_workspace_size(2, 8192, 16, 32, 128, 128, opts(lib))
+    # checkpoints every 16 tokens + per-CTA 16-state scratch + per-slice partials (2*128 + 2 floats)
+    ck = (16384 // 16 + 2) * 32 * 4 * 128 * 32 * 4
+    scr = 2 * 32 * 4 * 16 * 128 * 32 * 4
+    part = 16384 * 32 * 4 * 258 * 4
+    assert ck + scr + part <= n <= ck + scr + part + 3 * 256
+    assert lib.gdn_recurrent_bwd_workspace_size(1, 8, 1, 1, 48, 32, opts(lib)) == 0
