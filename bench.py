@@ -370,6 +370,38 @@ def run_gpu(args):
     gate_bytes = 3 * (w.B * w.T * Cv * 2) + w.dv * 4
     del proj, qc, kc, vc, a_raw, b_raw, z
 
+    # ---- backward pass of the same 8k workload (gradients w.r.t. q, k, v, g, beta, S0)
+    xb = device_inputs_random(torch, dev, w, seed=3)
+    dout = torch.randn(w.B, w.T, w.Hv, w.dv, device=dev).to(torch.bfloat16)
+    dSf = 0.1 * torch.randn(w.B, w.Hv, w.dk, w.dv, device=dev)
+    ws_b = torch.empty(gdn.backward_workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv), dtype=torch.uint8, device=dev)
+    bwd_steps = 3
+    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(bwd_steps)]
+
+    def bwd_step(events=None):
+        return gdn.gdn_recurrent_bwd(xb["q"], xb["k"], xb["v"], xb["g"], xb["beta"], S0, dout, dSf, workspace=ws_b,
+                                     events=None if events is None else [e.cuda_event for e in events])
+
+    for row in ev_b:
+        for e in row:
+            e.record(stream)
+    for _ in range(3):
+        bwd_step()
+    barrier()
+    clocks.active = True
+    t0.record(stream)
+    for i in range(bwd_steps):
+        bwd_step(ev_b[i])
+    t1.record(stream)
+    barrier()
+    clocks.active = False
+    bwd_ms = max_over_ranks(t0.elapsed_time(t1)) / bwd_steps
+    gdn.check_device_status()
+    bwd_flop = 20.0 * tokens * w.Hv * w.dk * w.dv   # one forward (4 dk dv) + the adjoint (16 dk dv) per token/head
+    bwd_tf = bwd_flop / (bwd_ms * 1e9)
+    alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12      # fp32 FMA lanes x 2 flop x max SM clock
+    del xb, dout, ws_b
+
     # ---- decode: 512 consecutive steps, state resident, one CUDA graph per pass
     wd = DECODE
     xd = device_inputs_random(torch, dev, wd, steps=wd.T, seed=2)
@@ -447,6 +479,13 @@ def run_gpu(args):
                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                     "frac": round(gate_bytes / (gate_ms * 1e6) / peaks["hbm_gbs"], 4),
                                     "algorithmic_bytes": gate_bytes}},
+        "backward": {"workload": "prefill_gqa_8k backward: gradients w.r.t. q, k, v, g, beta, S0 from dout and "
+                                 "dS_final (token-serial CUDA-core kernels, checkpoints every 16 tokens)",
+                     "value": round(world * tokens / (bwd_ms / 1e3), 1), "unit": "tokens/s",
+                     "ms_per_step": round(bwd_ms, 4), "steps": bwd_steps, "gpu_launches": 2 * bwd_steps,
+                     "roofline": {"bound": "alu", "achieved": round(bwd_tf, 2), "peak": round(alu_peak, 1),
+                                  "unit": "TFLOP/s", "frac": round(bwd_tf / alu_peak, 4),
+                                  "peak_source": "fp32 FMA lanes x 2 x 2070 MHz (unit counts)"}},
         "decode": {"workload": "decode_256x512: 256 sequences x 32 V heads (16 QK heads), d=128, 512 steps, "
                                "fp32 state 512 MiB resident, one CUDA graph per 512-step pass",
                    "value": round(world / (dec_ms / 1e3), 1), "unit": "steps/s",
@@ -535,6 +574,15 @@ def run_profile_case(case):
         ws = torch.empty(gdn.workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv), dtype=torch.uint8, device=dev)
         for _ in range(2):
             gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, workspace=ws)
+    elif case == "backward":
+        # one 1024-token sequence of the GQA workload's heads (a capture-sized backward), twice
+        w = gi.scaled(PREFILL, B=1, T=1024)
+        x = device_inputs_random(torch, dev, w)
+        S0 = 0.1 * torch.randn(w.B, w.Hv, w.dk, w.dv, device=dev)
+        dout = torch.randn_like(x["v"])
+        dSf = 0.1 * torch.randn_like(S0)
+        for _ in range(2):
+            gdn.gdn_recurrent_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, dout, dSf)
     elif case == "layer":
         # the conv of the packed q/k/v projection (three channel slices) and the prefill with the
         # fused front end and the output gate, twice
@@ -573,7 +621,7 @@ def main():
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile-case", choices=["prefill", "decode", "layer"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill", "decode", "layer", "backward"], default=None,
                     help="run one warm-up and one measured call of one kernel family (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_case:

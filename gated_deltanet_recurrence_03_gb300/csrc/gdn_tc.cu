@@ -77,7 +77,7 @@ __device__ bool slot_lookup(const int32_t* cu, int nseq, int T_len, int slot, in
 // Shared memory (byte offsets from a 1024-aligned base)
 constexpr uint32_t P_KQ = 0;            // 2 panels (dk 0-63, 64-127) x [K rows 0-63 | Q rows 64-127]
 constexpr uint32_t P_TOP = 32768;       // [-W_h | Tb_h] for both heads: 3 panels x 128 rows (B operand)
-constexpr uint32_t P_X = P_TOP;         // blocked-solve scratch X [2][16][48] fp32 (panel 0, before -W)
+constexpr uint32_t P_X = P_TOP;         // blocked-solve scratch X [2][16][56] fp32 (panel 0, before -W)
 constexpr uint32_t P_HANDOFF = P_TOP + 16384;   // P_0 rows, bf16 [64][64] (panel 1, before -W)
 constexpr uint32_t P_LC = 81920;        // L_h then T_h: 10 lower blocks of 16 x 16 fp32 per head, row stride 20
 constexpr uint32_t P_LBLK = 16 * 20;    // floats per block
@@ -96,26 +96,58 @@ static_assert(P_SMEM <= 113 * 1024, "two CTAs per SM");
 __device__ __forceinline__ int lblk(int I, int J) { return I * (I + 1) / 2 + J; }   // J <= I
 
 // In-place inverse of I + L_h for both heads (two warps per head): 16 x 16 diagonal blocks by forward
-// substitution (one column per thread), then block row i from X_ij = sum_k L_ik T_kj and
-// T_ij = -T_ii X_ij.  Each warp computes whole 16 x 16 blocks (uniform control flow); lane = 2 x 4 tile
-// (rows rp, rp + 8; columns c4 .. c4 + 3), which keeps the shared-memory reads conflict-free.
-__device__ __forceinline__ void block_tile_product(const float* A, int a_stride, const float* B, int b_stride,
-                                                   int rp, int c4, float4& acc0, float4& acc1) {
+// substitution in fp32 (one column per thread), then block row i from X_ij = sum_k L_ik T_kj and
+// T_ij = -T_ii X_ij.  The off-diagonal block products run on the warp-level tensor-core MMA
+// (m16n8k8, tf32 inputs rounded to nearest, fp32 accumulation): tcgen05 has no 16-row shape, and
+// T is rounded to bf16 right after (as the W and T diag(beta) operands), far coarser than tf32.
+constexpr int kXStride = 56;   // X scratch row stride (floats): conflict-free B-fragment loads
+
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32_m16n8k8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// acc (a 16 x 16 tile as two 16 x 8 accumulator fragments) += A B, A and B 16 x 16 fp32 in shared
+// memory with row strides as and bs.  Fragment g = lane / 4, t = lane % 4: A holds (g, t), (g + 8, t),
+// (g, t + 4), (g + 8, t + 4) of each 8-wide k slice; B holds (k = t, n = g), (k = t + 4, n = g);
+// the accumulator holds (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ void tile_mma_16(float (&acc)[2][4], const float* A, int as, const float* B, int bs,
+                                            int lane) {
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-        const float l0 = A[rp * a_stride + s], l1 = A[(rp + 8) * a_stride + s];
-        const float4 tv = *reinterpret_cast<const float4*>(B + s * b_stride + c4);
-        acc0.x = fmaf(l0, tv.x, acc0.x); acc0.y = fmaf(l0, tv.y, acc0.y);
-        acc0.z = fmaf(l0, tv.z, acc0.z); acc0.w = fmaf(l0, tv.w, acc0.w);
-        acc1.x = fmaf(l1, tv.x, acc1.x); acc1.y = fmaf(l1, tv.y, acc1.y);
-        acc1.z = fmaf(l1, tv.z, acc1.z); acc1.w = fmaf(l1, tv.w, acc1.w);
+    for (int kk = 0; kk < 16; kk += 8) {
+        const uint32_t a[4] = {tf32_rna(A[g * as + kk + t]), tf32_rna(A[(g + 8) * as + kk + t]),
+                               tf32_rna(A[g * as + kk + t + 4]), tf32_rna(A[(g + 8) * as + kk + t + 4])};
+#pragma unroll
+        for (int nh = 0; nh < 2; ++nh) {
+            const uint32_t b[2] = {tf32_rna(B[(kk + t) * bs + 8 * nh + g]), tf32_rna(B[(kk + t + 4) * bs + 8 * nh + g])};
+            mma_tf32_m16n8k8(acc[nh], a, b);
+        }
+    }
+}
+
+// Store sign * acc into a 16 x 16 fp32 tile with row stride ds.
+__device__ __forceinline__ void tile_store_16(float* D, int ds, const float (&acc)[2][4], float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nh = 0; nh < 2; ++nh) {
+        *reinterpret_cast<float2*>(D + g * ds + 8 * nh + 2 * t) = make_float2(sign * acc[nh][0], sign * acc[nh][1]);
+        *reinterpret_cast<float2*>(D + (g + 8) * ds + 8 * nh + 2 * t) = make_float2(sign * acc[nh][2], sign * acc[nh][3]);
     }
 }
 
 __device__ __forceinline__ void blocked_unit_lower_inverse(float* sLC, float* sX, int tid) {
     const int h = tid >> 6, t = tid & 63, hw = t >> 5, lane = t & 31;
     float* L = sLC + h * 10 * P_LBLK;
-    float* X = sX + h * 16 * 48;
+    float* X = sX + h * 16 * kXStride;
     {
         const int I = t >> 4, j = t & 15;
         float* D = L + lblk(I, I) * P_LBLK;
@@ -137,27 +169,22 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(float* sLC, float* sX
         for (int r = 0; r < 16; ++r) D[r * 20 + j] = tc[r];
         __syncthreads();
     }
-    const int rp = lane >> 2, c4 = (lane & 3) * 4;
 #pragma unroll
     for (int i = 1; i < 4; ++i) {
         // blocks of block row i handled by this warp: warp 0 takes jb = 0, warp 1 the rest
-        // (balances the products: i = 3 gives 3 + (2 + 1))
         const int jb_lo = hw == 0 ? 0 : 1, jb_hi = hw == 0 ? 1 : i;
         for (int jb = jb_lo; jb < jb_hi && jb < i; ++jb) {
-            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+            float acc[2][4] = {};
             for (int k = jb; k < i; ++k)
-                block_tile_product(L + lblk(i, k) * P_LBLK, 20, L + lblk(k, jb) * P_LBLK, 20, rp, c4, acc0, acc1);
-            *reinterpret_cast<float4*>(X + rp * 48 + 16 * jb + c4) = acc0;
-            *reinterpret_cast<float4*>(X + (rp + 8) * 48 + 16 * jb + c4) = acc1;
+                tile_mma_16(acc, L + lblk(i, k) * P_LBLK, 20, L + lblk(k, jb) * P_LBLK, 20, lane);
+            tile_store_16(X + 16 * jb, kXStride, acc, 1.f, lane);
         }
         __syncthreads();
         const float* Tii = L + lblk(i, i) * P_LBLK;
         for (int jb = jb_lo; jb < jb_hi && jb < i; ++jb) {
-            float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-            block_tile_product(Tii, 20, X + 16 * jb, 48, rp, c4, acc0, acc1);
-            float* Tij = L + lblk(i, jb) * P_LBLK + c4;
-            *reinterpret_cast<float4*>(Tij + rp * 20) = make_float4(-acc0.x, -acc0.y, -acc0.z, -acc0.w);
-            *reinterpret_cast<float4*>(Tij + (rp + 8) * 20) = make_float4(-acc1.x, -acc1.y, -acc1.z, -acc1.w);
+            float acc[2][4] = {};
+            tile_mma_16(acc, Tii, 20, X + 16 * jb, kXStride, lane);
+            tile_store_16(L + lblk(i, jb) * P_LBLK, 20, acc, -1.f, lane);
         }
         __syncthreads();
     }
