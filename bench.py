@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # were taken on (sha256 prefix of the file); None once the source has changed.
 NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix of that file at capture, dram read + write bytes per launch)
-    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "c587284b312b5429", 139563776 + 345314560),
-    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "c587284b312b5429", 612450560 + 120080384),
+    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "a26f1df9ddb38392", 139490304 + 344800256),
+    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "a26f1df9ddb38392", 612469248 + 120179200),
     "decode_step_kernel": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_decode.cu", "e56b2f01dcac2d93", 541133824 + 480539648),
 }
 
