@@ -221,6 +221,17 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (!slot_lookup(cu, nseq, T_len, slot, seq, t0, n)) return;  // unused slot (uniform per CTA)
     const int h0 = 2 * pair;
     const int hk = h0 / (Hv / Hqk);
+    if (tid == 0) {   // barriers first, then the K / Q tile loads, so their latency overlaps the set-up
+        *abort_flag = 0;
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+        mbar_arrive_expect_tx(bar_tma, 4 * 8192);
+        for (int p = 0; p < 2; ++p) {
+            tma_load_3d(sb + P_KQ + p * 16384, &tm_k, 64 * p, hk, (int)t0, bar_tma);
+            tma_load_3d(sb + P_KQ + p * 16384 + 8192, &tm_q, 64 * p, hk, (int)t0, bar_tma);
+        }
+    }
     // gates of value head h0 + warp (warps 0-1), two tokens per lane; padded tokens get g = beta = 0
     float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
     if (warp < 2) {
@@ -244,24 +255,11 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_alloc(smem_u32(tmem_slot), 256);
         tc_fence_before();
     }
-    if (tid == 0) {
-        *abort_flag = 0;
-        mbar_init(bar_tma, 1);
-        mbar_init(bar_mma, 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
+    __syncthreads();   // also publishes the barrier initialisation to every thread
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's TMEM lane quarter
 
-    if (tid == 0) {
-        mbar_arrive_expect_tx(bar_tma, 4 * 8192);
-        for (int p = 0; p < 2; ++p) {
-            tma_load_3d(sb + P_KQ + p * 16384, &tm_k, 64 * p, hk, (int)t0, bar_tma);
-            tma_load_3d(sb + P_KQ + p * 16384 + 8192, &tm_q, 64 * p, hk, (int)t0, bar_tma);
-        }
-    }
     if (warp < 2) {   // G = inclusive scan of g over the chunk
         const int hh = warp;
         const int r0 = 2 * lane, r1 = 2 * lane + 1;
