@@ -461,6 +461,61 @@ def run_gpu(args):
     gdn.check_device_status()
     dec_bytes = decode_bytes(wd)
     dec_gbs = dec_bytes / (dec_ms * 1e6)
+
+    # ---- the recurrent core of a layer in decode, same sequences and heads: per step three conv steps
+    #      of the packed projection with their K-1 caches, then the recurrent step with raw gates, l2 norm
+    #      and the output gate; 128 steps in one CUDA graph
+    dl_steps = 128
+    bf = torch.bfloat16
+    Cq, Cv = wd.Hqk * wd.dk, wd.Hv * wd.dv
+    Cc = 2 * Cq + Cv
+    genl = torch.Generator(device=dev).manual_seed(7)
+    projd = torch.randn(dl_steps, wd.B, Cc, device=dev, generator=genl).to(bf)
+    cwd = [0.5 * torch.randn(c, 4, device=dev, generator=genl) for c in (Cq, Cq, Cv)]
+    cachesd = [torch.zeros(wd.B, 3, c, dtype=bf, device=dev) for c in (Cq, Cq, Cv)]
+    ad = torch.randn(dl_steps, wd.B, wd.Hv, device=dev, generator=genl).to(bf)
+    bd = torch.randn(dl_steps, wd.B, wd.Hv, device=dev, generator=genl).to(bf)
+    zd = torch.randn(dl_steps, wd.B, wd.Hv, wd.dv, device=dev, generator=genl).to(bf)
+    A_logd = -0.5 + 0.5 * torch.randn(wd.Hv, device=dev, generator=genl)
+    dt_biasd = 0.5 * torch.randn(wd.Hv, device=dev, generator=genl)
+    nwd = 1.0 + 0.1 * torch.randn(wd.dv, device=dev, generator=genl)
+    yq = torch.empty(wd.B, Cq, dtype=bf, device=dev)
+    yk, yv = torch.empty_like(yq), torch.empty(wd.B, Cv, dtype=bf, device=dev)
+    outd = torch.empty(dl_steps, wd.B, wd.Hv, wd.dv, dtype=bf, device=dev)
+
+    def decode_layer_step(t):
+        for (c0, c1), cw_, cache_, y_ in zip(((0, Cq), (Cq, 2 * Cq), (2 * Cq, Cc)), cwd, cachesd, (yq, yk, yv)):
+            gdn.gdn_causal_conv1d_step(projd[t][:, c0:c1], cw_, cache_, out=y_)
+        gdn.gdn_recurrent_step(yq.view(wd.B, wd.Hqk, wd.dk), yk.view(wd.B, wd.Hqk, wd.dk),
+                               yv.view(wd.B, wd.Hv, wd.dv), ad[t], bd[t], S, out=outd[t], scale=wd.dk ** -0.5,
+                               normalize_qk=True, raw_gates=(A_logd, dt_biasd), output_gate=(zd[t], nwd, 1e-6))
+
+    for t in range(3):
+        decode_layer_step(t)
+    torch.cuda.synchronize()
+    graph_l = torch.cuda.CUDAGraph()
+    cap_l = torch.cuda.Stream(dev)
+    cap_l.wait_stream(stream)
+    with torch.cuda.stream(cap_l):
+        with torch.cuda.graph(graph_l, stream=cap_l):
+            for t in range(dl_steps):
+                decode_layer_step(t)
+    stream.wait_stream(cap_l)
+    graph_l.replay()
+    barrier()
+    clocks.active = True
+    t0.record(stream)
+    for _ in range(2):
+        graph_l.replay()
+    t1.record(stream)
+    barrier()
+    clocks.active = False
+    dl_ms = max_over_ranks(t0.elapsed_time(t1)) / (2 * dl_steps)
+    gdn.check_device_status()
+    # state read + written, projection, conv caches read + written, a, b, z, out
+    dl_bytes = (2 * wd.B * wd.Hv * wd.dk * wd.dv * 4 + wd.B * Cc * 2 + 2 * wd.B * 3 * Cc * 2
+                + 2 * wd.B * wd.Hv * 2 + 2 * wd.B * wd.Hv * wd.dv * 2)
+    del projd, zd, outd
     clocks.stop()
 
     if rank != 0:
@@ -522,6 +577,16 @@ def run_gpu(args):
                                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
                                 "traffic": traffic_for("decode_step_kernel"),
                                 "algorithmic_bytes": dec_bytes, "peak_source": f"{peak_src} copy bandwidth"}},
+        "decode_layer": {"workload": "decode_256x512 heads through the layer's recurrent core: 3 conv steps (K=4) "
+                                     "of the packed 8192-channel projection with their caches, then the recurrent step "
+                                     "with raw gates, l2 norm and the output gate; 128 steps per CUDA graph",
+                         "value": round(world / (dl_ms / 1e3), 1), "unit": "steps/s",
+                         "tokens_per_s": round(world * wd.B / (dl_ms / 1e3), 1), "us_per_step": round(dl_ms * 1e3, 2),
+                         "gpu_launches": 2 * dl_steps * 4,
+                         "roofline": {"bound": "hbm", "achieved": round(dl_bytes / (dl_ms * 1e6), 1),
+                                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": round(dl_bytes / (dl_ms * 1e6) / peaks["hbm_gbs"], 4),
+                                      "algorithmic_bytes": dl_bytes}},
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:
