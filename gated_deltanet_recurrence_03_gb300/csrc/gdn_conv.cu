@@ -128,6 +128,38 @@ __device__ __forceinline__ void conv_out(const float2 (&wr)[K][Vec<T>::N / 2], c
     }
 }
 
+// The K taps of channels c0 .. c0 + V - 1 as channel pairs: one vector load per channel when K is 2 or 4
+// and the rows are aligned (uniform over the grid), scalar loads otherwise.
+template <typename T, int K>
+__device__ __forceinline__ void load_taps(const float* __restrict__ w, int c0, bool vec_ok,
+                                          float2 (&wr)[K][Vec<T>::N / 2]) {
+    constexpr int P = Vec<T>::N / 2;
+    float t[2 * P][K];
+#pragma unroll
+    for (int e = 0; e < 2 * P; ++e) {
+        const float* src = w + (size_t)(c0 + e) * K;
+        if constexpr (K == 4) {
+            if (vec_ok) {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(src));
+                t[e][0] = f.x; t[e][1] = f.y; t[e][2] = f.z; t[e][3] = f.w;
+                continue;
+            }
+        } else if constexpr (K == 2) {
+            if (vec_ok) {
+                const float2 f = __ldg(reinterpret_cast<const float2*>(src));
+                t[e][0] = f.x; t[e][1] = f.y;
+                continue;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < K; ++k) t[e][k] = __ldg(src + k);
+    }
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+#pragma unroll
+        for (int k = 0; k < K; ++k) wr[k][p] = make_float2(t[2 * p][k], t[2 * p + 1][k]);
+}
+
 template <typename T, int K>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restrict__ w,
@@ -198,11 +230,7 @@ conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restric
         const int c0 = cg * CW + lane * V;
         const bool active = c0 < C;
         if (cg != cg_loaded && active) {
-#pragma unroll
-            for (int p = 0; p < P; ++p)
-#pragma unroll
-                for (int k = 0; k < K; ++k)
-                    wr[k][p] = make_float2(__ldg(w + (size_t)(c0 + 2 * p) * K + k), __ldg(w + (size_t)(c0 + 2 * p + 1) * K + k));
+            load_taps<T, K>(w, c0, (reinterpret_cast<uintptr_t>(w) % (K * sizeof(float))) == 0, wr);
             cg_loaded = cg;
         }
         mbar_wait_bounded(bar_full + 8 * st, ph, abort_flag, status, kStatusTimeout, kWaitLimitNs);
@@ -284,6 +312,10 @@ conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restric
             mbar_wait_drain(bar_full + 8 * (uint32_t)(j % kStages), (uint32_t)((j / kStages) & 1), kWaitLimitNs);
 }
 
+// One thread per 16-byte channel vector and block of kStepRows sequences: the weights are loaded
+// once and reused, and the rows' loads are independent (in flight together).
+constexpr int kStepRows = 4;
+
 template <typename T, int K>
 __global__ void __launch_bounds__(kStepThreads)
 conv_step_kernel(const T* __restrict__ x, long long x_stride, const float* __restrict__ w, T* __restrict__ cache,
@@ -293,21 +325,22 @@ conv_step_kernel(const T* __restrict__ x, long long x_stride, const float* __res
     if (vec * V >= C) return;
     const int c0 = vec * V;
     float2 wr[K][P];
+    load_taps<T, K>(w, c0, (reinterpret_cast<uintptr_t>(w) % (K * sizeof(float))) == 0, wr);
+    for (size_t n0 = (size_t)blockIdx.y * kStepRows; n0 < (size_t)N; n0 += (size_t)gridDim.y * kStepRows) {
 #pragma unroll
-    for (int p = 0; p < P; ++p)
+        for (int r = 0; r < kStepRows; ++r) {
+            const size_t n = n0 + r;
+            if (n >= (size_t)N) break;
+            float2 hist[K][P];
 #pragma unroll
-        for (int k = 0; k < K; ++k)
-            wr[k][p] = make_float2(__ldg(w + (size_t)(c0 + 2 * p) * K + k), __ldg(w + (size_t)(c0 + 2 * p + 1) * K + k));
-    for (size_t n = blockIdx.y; n < (size_t)N; n += gridDim.y) {
-        float2 hist[K][P];
+            for (int k = 0; k < K - 1; ++k) load_vec(cache + (n * (K - 1) + k) * C + c0, hist[k]);
+            load_vec(x + (long long)n * x_stride + c0, hist[K - 1]);
+            float2 out[P];
+            conv_out<T, K>(wr, hist, out);
+            store_vec(y + n * C + c0, out);
 #pragma unroll
-        for (int k = 0; k < K - 1; ++k) load_vec(cache + (n * (K - 1) + k) * C + c0, hist[k]);
-        load_vec(x + (long long)n * x_stride + c0, hist[K - 1]);
-        float2 out[P];
-        conv_out<T, K>(wr, hist, out);
-        store_vec(y + n * C + c0, out);
-#pragma unroll
-        for (int k = 1; k < K; ++k) store_vec(cache + (n * (K - 1) + (k - 1)) * C + c0, hist[k]);
+            for (int k = 1; k < K; ++k) store_vec(cache + (n * (K - 1) + (k - 1)) * C + c0, hist[k]);
+        }
     }
 }
 
@@ -357,7 +390,7 @@ template <typename T, int K>
 cudaError_t step_typed(const ConvArgs& a) {
     const int vecs = a.C / Vec<T>::N;
     const int threads = min(kStepThreads, (vecs + 31) / 32 * 32);
-    const dim3 grid((unsigned)((vecs + threads - 1) / threads), (unsigned)min(65535, a.B));
+    const dim3 grid((unsigned)((vecs + threads - 1) / threads), (unsigned)min(65535, (a.B + kStepRows - 1) / kStepRows));
     conv_step_kernel<T, K><<<grid, threads, 0, a.stream>>>(static_cast<const T*>(a.x), a.x_stride, a.w,
                                                          static_cast<T*>(a.cache_out), static_cast<T*>(a.y),
                                                          a.B, a.C);
