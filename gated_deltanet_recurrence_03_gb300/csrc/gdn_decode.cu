@@ -141,7 +141,7 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
         __syncthreads();
         if (tid < DV)
             out[(size_t)nh * DV + tid] =
-                from_f32<T>(so[tid] * s_inv * norm_w[tid] * silu_f(to_f32(zg[(size_t)nh * DV + tid])));
+                from_f32<T>(so[tid] * s_inv * norm_w[tid] * silu_for<T>(to_f32(zg[(size_t)nh * DV + tid])));
     }
 }
 

@@ -65,7 +65,7 @@ output_gate_kernel(T* __restrict__ out, const T* __restrict__ z, const float* __
         if (row[r] >= rows) continue;
         const float inv = rsqrtf(ss[r] / (float)DV + eps);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) o[r][e] = o[r][e] * inv * wv[e] * silu_f(zz[r][e]);
+        for (int e = 0; e < VEC; ++e) o[r][e] = o[r][e] * inv * wv[e] * silu_for<T>(zz[r][e]);
         Vec16<T>::store(out + row[r] * DV + sub * VEC, o[r]);
     }
 }

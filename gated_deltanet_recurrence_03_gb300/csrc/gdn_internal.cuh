@@ -158,6 +158,19 @@ __device__ __forceinline__ void gates_from_raw(float a, float b, float A_log, fl
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
 
+// SiLU for a result stored as bf16: z/2 (1 + tanh(z/2)) with the hardware tanh, one special-function
+// op instead of two plus a division; its relative error (~2^-11 on tanh) is below bf16's 2^-9.
+__device__ __forceinline__ float silu_bf16out(float z) {
+    const float h = 0.5f * z;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
+template <typename T>
+__device__ __forceinline__ float silu_for(float z) { return silu_f(z); }
+template <>
+__device__ __forceinline__ float silu_for<__nv_bfloat16>(float z) { return silu_bf16out(z); }
+
 // Sequence i's token range [t0, t1) in the flattened token index.
 __device__ __forceinline__ void seq_range(const int32_t* cu, int i, int T, long long& t0, long long& t1) {
     if (cu) {
