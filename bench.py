@@ -44,7 +44,7 @@ NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix of that file at capture, dram read + write bytes per launch)
     "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "a26f1df9ddb38392", 139490304 + 344800256),
     "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "a26f1df9ddb38392", 612469248 + 120179200),
-    "decode_step_kernel": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_decode.cu", "e56b2f01dcac2d93", 541133824 + 480539648),
+    "decode_step_kernel": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_decode.cu", "0a3ae9abf76d8679", 541133568 + 480455680),
 }
 
 PREFILL = gi.WORKLOADS["prefill_gqa_8k"]
