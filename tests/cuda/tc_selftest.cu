@@ -167,3 +167,29 @@ extern "C" int tc_selftest_mma(const void* A, const void* B, float* D, int K, in
                                       K, N, a_mn, b_mn, status);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
+
+// Failure detection without a fault: a wait on an mbarrier that nothing completes must give up after
+// its limit, set the status flag and let the kernel return (the context stays usable).  One CTA;
+// thread 0 waits, the others wait on the abort flag through the same bounded wait.
+namespace {
+__global__ void __launch_bounds__(64, 1) wait_runs_out_kernel(unsigned* status, unsigned long long limit_ns,
+                                                              int* returned) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(b, 1);   // expects one arrival that never comes
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(b, 0, &abort_flag, status, 1u, limit_ns);
+    __syncthreads();
+    if (threadIdx.x == 0) *returned = ok ? 2 : 1;
+}
+}  // namespace
+
+extern "C" int tc_selftest_wait_runs_out(unsigned* status, unsigned long long limit_ns, int* returned) {
+    wait_runs_out_kernel<<<1, 64>>>(status, limit_ns, returned);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}

@@ -30,6 +30,7 @@ def lib():
     L = ctypes.CDLL(LIB)
     L.tc_selftest_mma.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
     L.tc_selftest_mma_tmem_a.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p]
+    L.tc_selftest_wait_runs_out.argtypes = [ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]
     return L
 
 
@@ -72,3 +73,21 @@ def test_mma_a_from_tmem(lib, K, N):
     ref = A.double().numpy() @ B.double().numpy()
     err = np.abs(D.cpu().numpy() - ref).max() / np.abs(ref).max()
     assert err < 1e-5, f"max rel err {err:.3e}"
+
+
+def test_bounded_wait_runs_out_sets_status_and_returns(lib):
+    """Failure detection without a GPU fault: an mbarrier wait that nothing completes gives up after
+    its limit (50 ms here), sets the status flag, every thread returns, and the context still runs
+    work afterwards."""
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    returned = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    assert lib.tc_selftest_wait_runs_out(status.data_ptr(), 50_000_000, returned.data_ptr()) == 0
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert int(status.item()) == 1, "the status flag was not set"
+    assert int(returned.item()) == 1, "the wait did not report failure"
+    assert elapsed < 5.0
+    x = torch.arange(1024, device="cuda", dtype=torch.float32)
+    assert float((x * 2).sum().item()) == 1023 * 1024   # the context is still usable
