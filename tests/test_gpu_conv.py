@@ -103,3 +103,47 @@ def test_conv_step_more_rows_than_grid_rows():
     ry, rc = oconv.causal_conv1d(x[sel][:, None], w, cache[sel])
     assert rel_err(ry[:, 0], y[sel].float().cpu().numpy()) <= TOL["bf16"]
     np.testing.assert_array_equal(cd[sel].float().cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [1, 3])
+def test_conv_fwd_short_kernels(dtype, K):
+    """Kernel widths 1 and 3 (K - 1 = 0 and 2 history rows), with and without a cache."""
+    B, T, C = 2, 70, 64
+    x, w, cache = _inputs(90 + K, (B, T), C, K, dtype, B)
+    for cache_in in (None, cache):
+        y, co = gdn.gdn_causal_conv1d_fwd(up(x, dtype), up(w, torch.float32),
+                                          None if cache_in is None else up(cache_in, dtype))
+        torch.cuda.synchronize()
+        ry, rc = oconv.causal_conv1d(x, w, cache_in)
+        assert rel_err(ry, y.float().cpu().numpy()) <= TOL[dtype]
+        np.testing.assert_array_equal(co.float().cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [2, 3, 4])
+def test_conv_step_kernel_widths(dtype, K):
+    N, T, C = 9, 5, 96
+    x, w, cache = _inputs(95 + K, (N, T), C, K, dtype, N)
+    wd, cd = up(w, torch.float32), up(cache, dtype)
+    ys = [gdn.gdn_causal_conv1d_step(up(np.ascontiguousarray(x[:, t]), dtype), wd, cd) for t in range(T)]
+    torch.cuda.synchronize()
+    ry, rc = oconv.causal_conv1d(x, w, cache)
+    assert rel_err(ry, torch.stack(ys, 1).float().cpu().numpy()) <= TOL[dtype]
+    np.testing.assert_array_equal(cd.float().cpu().numpy(), rc)
+
+
+def test_conv_fwd_misaligned_weights_use_scalar_taps():
+    """Weights [C, K=2] starting one float into an allocation (4-byte but not 8-byte aligned): the
+    kernel cannot load a channel's taps as one vector, falls back to scalar loads and gives the
+    same result."""
+    B, T, C, K = 1, 40, 64, 2
+    x, w, _ = _inputs(99, (B, T), C, K, "bf16", B)
+    big = np.zeros((C * K + 1,), dtype=np.float32)
+    big[1:] = w.reshape(-1)
+    wt = torch.from_numpy(big).cuda()[1:].view(C, K)   # 4-byte aligned, not 8-byte aligned
+    assert wt.data_ptr() % 8 != 0
+    y, _ = gdn.gdn_causal_conv1d_fwd(up(x, "bf16"), wt, None)
+    torch.cuda.synchronize()
+    ry, _ = oconv.causal_conv1d(x, w)
+    assert rel_err(ry, y.float().cpu().numpy()) <= TOL["bf16"]
