@@ -56,6 +56,23 @@ def rank_info():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+# ---------------------------------------------------------------- replicas (one process per GPU)
+def max_over_ranks(dist, x, device="cpu"):
+    """The largest of every rank's x (each rank's own time; the job takes as long as its slowest
+    replica).  dist is torch.distributed, or None for a single process."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, ms_max):
+    """Whole-job throughput: the units all ranks processed divided by the slowest rank's time."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 def load_peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -195,12 +212,8 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def max_ms(x):
+        return max_over_ranks(dist, x, dev)
 
     # ---- headline: chunked prefill of the 8k GQA workload, inputs rotated across 3 copies (> L2 each)
     w = PREFILL
@@ -231,7 +244,7 @@ def run_gpu(args):
     t1.record(stream)
     barrier()
     clocks.active = False
-    ms_total = max_over_ranks(t0.elapsed_time(t1))
+    ms_total = max_ms(t0.elapsed_time(t1))
     ms_step = ms_total / args.steps
     k_prep = statistics.mean(r[0].elapsed_time(r[1]) for r in evs)
     k_chain = statistics.mean(r[1].elapsed_time(r[2]) for r in evs)
@@ -301,7 +314,7 @@ def run_gpu(args):
     te0, te1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_run(e2e_steps, te0, te1)
     barrier()
-    e2e_ms = max_over_ranks(te0.elapsed_time(te1)) / e2e_steps
+    e2e_ms = max_ms(te0.elapsed_time(te1)) / e2e_steps
 
     # ---- long-context packed prefill (state reset at each boundary)
     wl = LONG
@@ -332,7 +345,7 @@ def run_gpu(args):
     t1.record(stream)
     barrier()
     clocks.active = False
-    long_ms = max_over_ranks(t0.elapsed_time(t1)) / long_steps
+    long_ms = max_ms(t0.elapsed_time(t1)) / long_steps
     lp = statistics.mean(r[0].elapsed_time(r[1]) for r in ev_l)
     lc = statistics.mean(r[1].elapsed_time(r[2]) for r in ev_l)
     lf_prep, lf_chain = prefill_flops(wl.T, wl)
@@ -387,7 +400,7 @@ def run_gpu(args):
     t1.record(stream)
     barrier()
     clocks.active = False
-    layer_ms = max_over_ranks(t0.elapsed_time(t1)) / layer_steps
+    layer_ms = max_ms(t0.elapsed_time(t1)) / layer_steps
     gdn.check_device_status()
     conv_ms = statistics.mean(r[0].elapsed_time(r[1]) for r in ev_c)
     gate_ms = statistics.mean(r[2].elapsed_time(r[3]) for r in ev_p)
@@ -420,7 +433,7 @@ def run_gpu(args):
     t1.record(stream)
     barrier()
     clocks.active = False
-    bwd_ms = max_over_ranks(t0.elapsed_time(t1)) / bwd_steps
+    bwd_ms = max_ms(t0.elapsed_time(t1)) / bwd_steps
     gdn.check_device_status()
     bwd_flop = 20.0 * tokens * w.Hv * w.dk * w.dv   # one forward (4 dk dv) + the adjoint (16 dk dv) per token/head
     bwd_tf = bwd_flop / (bwd_ms * 1e9)
@@ -457,7 +470,7 @@ def run_gpu(args):
     t1.record(stream)
     barrier()
     clocks.active = False
-    dec_ms = max_over_ranks(t0.elapsed_time(t1)) / (passes * wd.T)
+    dec_ms = max_ms(t0.elapsed_time(t1)) / (passes * wd.T)
     gdn.check_device_status()
     dec_bytes = decode_bytes(wd)
     dec_gbs = dec_bytes / (dec_ms * 1e6)
@@ -510,7 +523,7 @@ def run_gpu(args):
     t1.record(stream)
     barrier()
     clocks.active = False
-    dl_ms = max_over_ranks(t0.elapsed_time(t1)) / (2 * dl_steps)
+    dl_ms = max_ms(t0.elapsed_time(t1)) / (2 * dl_steps)
     gdn.check_device_status()
     # state read + written, projection, conv caches read + written, a, b, z, out
     dl_bytes = (2 * wd.B * wd.Hv * wd.dk * wd.dv * 4 + wd.B * Cc * 2 + 2 * wd.B * 3 * Cc * 2
@@ -520,7 +533,7 @@ def run_gpu(args):
 
     if rank != 0:
         return
-    value = world * tokens / (ms_step / 1e3)
+    value = job_rate(world, tokens, ms_step)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -705,7 +718,7 @@ def run_profile_case(case):
     print(f"profile case {case} done")
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -715,12 +728,17 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile-case", choices=["prefill", "decode", "layer", "backward"], default=None,
                     help="run one warm-up and one measured call of one kernel family (for ncu) and exit")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
+    if not args.profile_case and args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    return args
+
+
+def main():
+    args = parse_args()
     if args.profile_case:
         run_profile_case(args.profile_case)
         return
-    if args.warmup < 3:
-        ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
     else:
