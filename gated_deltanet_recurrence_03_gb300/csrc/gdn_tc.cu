@@ -335,6 +335,10 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             sRQ[tid] = 1.f;
         }
         __syncthreads();
+        if (normalize) {   // fold 1/|k_s| into the column factor exp(G_0 - G_s) once
+            sC[tid] *= sRK[tid & 63];
+            __syncthreads();
+        }
         if (warp < 2) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s (s < r), lower blocks
             const int r = R, I = r >> 4, rr = r & 15;
             for (int hh = 0; hh < 2; ++hh) {
@@ -343,17 +347,24 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const float* ch = sC + hh * 64;
                 const bool fac = sFactor[hh] != 0;
                 float* Lh = sLC + hh * 10 * P_LBLK;
+                const float rowc = br * ar;   // factorised decay: beta_r exp(G_r - G_0) / |k_r|
                 for (int J = 0; J <= I; ++J) {
                     float* dst = Lh + lblk(I, J) * P_LBLK + rr * 20;
 #pragma unroll
                     for (int s4 = 0; s4 < 4; ++s4) {
                         float o[4];
+                        if (fac) {   // uniform per head: exp(G_0 - G_s) / |k_s| is the column factor ch[s]
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int s = 16 * J + 4 * s4 + e;
-                            const float kk = __uint_as_float(a[s]) * sRK[s];
-                            const float dec = fac ? ar * ch[s] : __expf(Gr - Gh[s]);
-                            o[e] = (s < r) ? br * dec * kk : 0.f;
+                            for (int e = 0; e < 4; ++e) {
+                                const int s = 16 * J + 4 * s4 + e;
+                                o[e] = (s < r) ? rowc * __uint_as_float(a[s]) * ch[s] : 0.f;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int s = 16 * J + 4 * s4 + e;
+                                o[e] = (s < r) ? br * __expf(Gr - Gh[s]) * __uint_as_float(a[s]) * sRK[s] : 0.f;
+                            }
                         }
                         *reinterpret_cast<float4*>(dst + 4 * s4) = make_float4(o[0], o[1], o[2], o[3]);
                     }
@@ -368,16 +379,29 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const float* ch = sC + hh * 64;
                 const bool fac = sFactor[hh] != 0;
                 uint32_t w[32];
+                if (fac) {   // uniform per head
+                    const float rowc = sq * ar;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float pv[2];
+                    for (int e = 0; e < 32; ++e) {
+                        float pv[2];
 #pragma unroll
-                    for (int f = 0; f < 2; ++f) {
-                        const int s = 2 * e + f;
-                        const float dec = fac ? ar * ch[s] : __expf(Gr - Gh[s]);
-                        pv[f] = (s <= r) ? sq * dec * __uint_as_float(a[s]) * sRK[s] : 0.f;
+                        for (int f = 0; f < 2; ++f) {
+                            const int s = 2 * e + f;
+                            pv[f] = (s <= r) ? rowc * __uint_as_float(a[s]) * ch[s] : 0.f;
+                        }
+                        w[e] = pack_bf16(pv[0], pv[1]);
                     }
-                    w[e] = pack_bf16(pv[0], pv[1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float pv[2];
+#pragma unroll
+                        for (int f = 0; f < 2; ++f) {
+                            const int s = 2 * e + f;
+                            pv[f] = (s <= r) ? sq * __expf(Gr - Gh[s]) * __uint_as_float(a[s]) * sRK[s] : 0.f;
+                        }
+                        w[e] = pack_bf16(pv[0], pv[1]);
+                    }
                 }
                 if (hh == 1) {   // own lane: [0 | P_1 row]
                     uint32_t z[32];
