@@ -458,11 +458,17 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int e = 0; e < 8; ++e) tv[e] = 0.f;
                 }
                 const int s0 = 16 * J + 8 * c;
+                // eight consecutive column factors in two 16-byte loads (the vectors are 256-byte aligned)
+                float dgv[8], btv[8];
+                *reinterpret_cast<float4*>(dgv) = *reinterpret_cast<const float4*>(dg + s0);
+                *reinterpret_cast<float4*>(dgv + 4) = *reinterpret_cast<const float4*>(dg + s0 + 4);
+                *reinterpret_cast<float4*>(btv) = *reinterpret_cast<const float4*>(bt + s0);
+                *reinterpret_cast<float4*>(btv + 4) = *reinterpret_cast<const float4*>(bt + s0 + 4);
                 uint32_t wb[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    wd[(s0 >> 1) + e] = pack_bf16(tv[2 * e] * dg[s0 + 2 * e], tv[2 * e + 1] * dg[s0 + 2 * e + 1]);
-                    wb[e] = pack_bf16(tv[2 * e] * bt[s0 + 2 * e], tv[2 * e + 1] * bt[s0 + 2 * e + 1]);
+                    wd[(s0 >> 1) + e] = pack_bf16(tv[2 * e] * dgv[2 * e], tv[2 * e + 1] * dgv[2 * e + 1]);
+                    wb[e] = pack_bf16(tv[2 * e] * btv[2 * e], tv[2 * e + 1] * btv[2 * e + 1]);
                 }
                 *reinterpret_cast<uint4*>(sm + P_TOP + 2 * 16384 + swz(R, s0 >> 3)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
             }
