@@ -139,3 +139,19 @@ def test_prefill_gqa_8k_full_sampled():
 @pytest.mark.slow
 def test_prefill_varlen_128k_full_sampled():
     _sampled(gi.WORKLOADS["prefill_varlen_128k"], heads=[0, 21])
+
+
+@pytest.mark.parametrize("normalize", [False, True])
+def test_strong_decay_takes_the_exact_decay_path(normalize):
+    """Heads 0 and 3 decay by about e^-3 per token (the log-decay span of a chunk, ~190, is too wide
+    to factorise exp(G_r - G_s) = exp(G_r - G_0) exp(G_0 - G_s) in fp32), heads 1 and 2 decay weakly:
+    both branches of the decay/Gram epilogue run in one launch, on the tensor-core path."""
+    w = gi.scaled(gi.WORKLOADS["prefill_gqa_8k"], B=2, T=150, Hqk=2, Hv=4)
+    x = gi.make_prefill_inputs(w)
+    g = np.array(x["g"], dtype=np.float64)
+    g[:, :, [0, 3]] = g[:, :, [0, 3]] * 60.0 - 0.5          # ~ -3.5 per token
+    x["g"] = gi.round_to_dtype(g, "bf16")
+    if normalize:
+        x["q"] = gi.round_to_dtype(x["q"] * 2.0, "bf16")
+        x["k"] = gi.round_to_dtype(x["k"] * 0.7, "bf16")
+    check(w, x, normalize_qk=normalize)
