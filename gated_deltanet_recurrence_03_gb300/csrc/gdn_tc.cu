@@ -219,8 +219,11 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     long long t0;
     int n;
     if (!slot_lookup(cu, nseq, T_len, slot, seq, t0, n)) return;  // unused slot (uniform per CTA)
-    const int h0 = 2 * pair;
-    const int hk = h0 / (Hv / Hqk);
+    // value-head pair of this CTA: the heads of one query/key head, two at a time; with an odd number
+    // per query/key head the last one pairs with itself (both halves compute it and store the same bytes)
+    const int G = Hv / Hqk, ppq = (G + 1) / 2;
+    const int hk = pair / ppq, jp = pair % ppq;
+    const int hA = hk * G + 2 * jp, hB = min(hA + 1, hk * G + G - 1);
     if (tid == 0) {   // barriers first, then the K / Q tile loads, so their latency overlaps the set-up
         *abort_flag = 0;
         mbar_init(bar_tma, 1);
@@ -232,20 +235,20 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tma_load_3d(sb + P_KQ + p * 16384 + 8192, &tm_q, 64 * p, hk, (int)t0, bar_tma);
         }
     }
-    // gates of value head h0 + warp (warps 0-1), two tokens per lane; padded tokens get g = beta = 0
+    // gates of value head hA (warp 0) / hB (warp 1), two tokens per lane; padded tokens get g = beta = 0
     float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
     if (warp < 2) {
         const int r0 = 2 * lane, r1 = 2 * lane + 1;
         if (r0 < n) {
-            g0 = __bfloat162float(g[(size_t)(t0 + r0) * Hv + h0 + warp]);
-            b0 = __bfloat162float(beta[(size_t)(t0 + r0) * Hv + h0 + warp]);
+            g0 = __bfloat162float(g[(size_t)(t0 + r0) * Hv + (warp == 0 ? hA : hB)]);
+            b0 = __bfloat162float(beta[(size_t)(t0 + r0) * Hv + (warp == 0 ? hA : hB)]);
         }
         if (r1 < n) {
-            g1 = __bfloat162float(g[(size_t)(t0 + r1) * Hv + h0 + warp]);
-            b1 = __bfloat162float(beta[(size_t)(t0 + r1) * Hv + h0 + warp]);
+            g1 = __bfloat162float(g[(size_t)(t0 + r1) * Hv + (warp == 0 ? hA : hB)]);
+            b1 = __bfloat162float(beta[(size_t)(t0 + r1) * Hv + (warp == 0 ? hA : hB)]);
         }
         if (A_log) {   // raw projections a, b: form the gates (padded tokens keep g = beta = 0)
-            const float al = A_log[h0 + warp], db = dt_bias[h0 + warp];
+            const float al = A_log[warp == 0 ? hA : hB], db = dt_bias[warp == 0 ? hA : hB];
             if (r0 < n) gates_from_raw(g0, b0, al, db, g0, b0);
             if (r1 < n) gates_from_raw(g1, b1, al, db, g1, b1);
         }
@@ -283,7 +286,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         sBG[hh * 64 + r] = sBeta[hh * 64 + r] * __expf(Gr);
         sA[hh * 64 + r] = __expf(Gr - G0);
         sC[hh * 64 + r] = __expf(G0 - Gr);
-        float* vec = ws_vec + ((size_t)slot * Hv + h0 + hh) * kVecFloats;
+        float* vec = ws_vec + ((size_t)slot * Hv + (hh == 0 ? hA : hB)) * kVecFloats;
         if (!normalize) vec[r] = __expf(Gl - Gr);   // with normalisation: written once 1/|k_r| is known
         if (r == 0) vec[64] = __expf(Gl);
     }
@@ -315,7 +318,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const float rk = rsqrtf(kk + 1e-6f);
                 sRK[R] = rk;
                 for (int hh = 0; hh < 2; ++hh) {
-                    ws_vec[((size_t)slot * Hv + h0 + hh) * kVecFloats + R] = __expf(sG[hh * 64 + 63] - sG[hh * 64 + R]) * rk;
+                    ws_vec[((size_t)slot * Hv + (hh == 0 ? hA : hB)) * kVecFloats + R] = __expf(sG[hh * 64 + 63] - sG[hh * 64 + R]) * rk;
                     sBG[hh * 64 + R] *= rk;
                 }
             } else {
@@ -526,7 +529,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     if (tid == 0) {   // the [-W | Tb] rows of A1 are final: start their stores now
         for (int h = 0; h < 2; ++h) {
-            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + h0 + h) * kA1Bytes;
+            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + (h == 0 ? hA : hB)) * kA1Bytes;
             for (int p = 0; p < 3; ++p) bulk_s2g(dst + p * 16384, sb + P_TOP + p * 16384 + h * 8192, 8192);
         }
         bulk_commit();
@@ -560,7 +563,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     if (tid == 0) {   // A1 of each head: panel p = [TOP rows of the head | output rows of the head]
         for (int h = 0; h < 2; ++h) {
-            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + h0 + h) * kA1Bytes;
+            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + (h == 0 ? hA : hB)) * kA1Bytes;
             for (int p = 0; p < 3; ++p) bulk_s2g(dst + p * 16384 + 8192, sb + bot_panel(3 * h + p), 8192);
         }
         bulk_commit();
@@ -858,7 +861,7 @@ void record_event(void** events, int num_events, int idx, cudaStream_t s) {
 
 bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk, unsigned flags) {
     (void)flags;   // normalisation and raw gates are handled inside the kernels
-    return dtype == GDN_BF16 && dk == kD && dv == kD && chunk == kC && (Hv / Hqk) % 2 == 0;
+    return dtype == GDN_BF16 && dk == kD && dv == kD && chunk == kC;
 }
 
 size_t tc_prefill_workspace_bytes(int B, int T, int Hv, int num_seqs, bool packed) {
@@ -909,7 +912,8 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
     const int T_len = a.T;
 
     record_event(events, num_events, 0, a.stream);
-    tc_prep_kernel<<<dim3((unsigned)slots, (unsigned)(a.Hv / 2)), kPrepThreads, P_SMEM, a.stream>>>(
+    const int G = a.Hv / a.Hqk;   // value heads per query/key head, processed two at a time
+    tc_prep_kernel<<<dim3((unsigned)slots, (unsigned)(a.Hqk * ((G + 1) / 2))), kPrepThreads, P_SMEM, a.stream>>>(
         tq, tk, static_cast<const bf16*>(a.g), static_cast<const bf16*>(a.beta), a.cu_seqlens, a.num_seqs, T_len,
         a.Hqk, a.Hv, a.scale, ws_a1, ws_vec, a.status, (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr, a.dt_bias,
         (a.flags & GDN_NORMALIZE_QK) ? 1 : 0);

@@ -108,7 +108,7 @@ void gdn_opts_init(gdn_opts_t* opts);
  *   S_final  [nseq, Hv, dk, dv] float or NULL (not written); may equal S0 (in-place update)
  *
  * Supported: dk, dv in {32, 64, 128}; Hv a multiple of Hqk; B, T >= 0.  T = 0 copies S0 to
- * S_final (zeros when S0 is NULL).  bf16 inputs with dk = dv = 128 and an even Hv/Hqk run on the
+ * S_final (zeros when S0 is NULL).  bf16 inputs with dk = dv = 128 run on the
  * tcgen05 tensor-core path (chunk 64) and need the workspace; everything else runs the token-serial
  * CUDA-core kernel and needs none.  out must not overlap any input.
  *

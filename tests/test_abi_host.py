@@ -201,3 +201,8 @@ def test_backward_workspace_size_is_pure_host(lib):
     part = 16384 * 32 * 4 * 258 * 4
     assert ck + scr + part <= n <= ck + scr + part + 3 * 256
     assert lib.gdn_recurrent_bwd_workspace_size(1, 8, 1, 1, 48, 32, opts(lib)) == 0
+
+
+def test_tensor_core_path_accepts_any_head_grouping(lib):
+    for Hqk, Hv in ((2, 2), (1, 3), (16, 32)):
+        assert lib.gdn_chunk_fwd_workspace_size(1, 512, Hqk, Hv, 128, 128, opts(lib)) > 0

@@ -155,3 +155,20 @@ def test_strong_decay_takes_the_exact_decay_path(normalize):
         x["q"] = gi.round_to_dtype(x["q"] * 2.0, "bf16")
         x["k"] = gi.round_to_dtype(x["k"] * 0.7, "bf16")
     check(w, x, normalize_qk=normalize)
+
+
+@pytest.mark.parametrize("Hqk,Hv", [(2, 2), (1, 3), (2, 6)])
+def test_tensor_core_path_any_head_grouping(Hqk, Hv):
+    """One value head per query/key head (no GQA) and odd groupings run on the tensor-core path too:
+    the last value head of an odd group pairs with itself in the prep kernel."""
+    w = gi.Workload("groups", "prefill", "bf16", B=2, T=150, Hqk=Hqk, Hv=Hv, dk=128, dv=128, chunk=64,
+                    s0_std=0.1, seed=7 + Hv)
+    assert gdn.workspace_size(w.B, w.T, Hqk, Hv, 128, 128) > 0   # the tensor-core path is selected
+    check(w, gi.make_prefill_inputs(w))
+
+
+def test_tensor_core_path_odd_grouping_packed():
+    lens = (70, 0, 129)
+    w = gi.Workload("groups_packed", "prefill", "bf16", B=1, T=sum(lens), Hqk=1, Hv=3, dk=128, dv=128, chunk=64,
+                    s0_std=0.1, seqlens=lens, seed=12)
+    check(w, gi.make_prefill_inputs(w))
