@@ -84,9 +84,11 @@ mma_case_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int K,
 }  // namespace
 
 // A (128 x K, bf16) written into TMEM columns 128.. with tcgen05.st (lane m = row m, k pairs packed
-// per 32-bit column, lower half = even k), B from shared memory (MN-major), D into columns 0..N-1.
+// per 32-bit column, lower half = even k), B from shared memory (MN-major, or K-major when b_mn = 0),
+// D into columns 0..N-1.
 __global__ void __launch_bounds__(128, 1)
-mma_tmem_a_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int K, int N, unsigned* status) {
+mma_tmem_a_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int K, int N, int b_mn,
+                  unsigned* status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
@@ -105,7 +107,8 @@ mma_tmem_a_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int 
     }
     for (int e = tid; e < K * N; e += 128) {
         const int k = e / N, n = e % N;
-        const uint32_t off = (n / 64) * (K * 128) + swz(k, (n % 64) / 8) + (n % 8) * 2;
+        const uint32_t off = b_mn ? (n / 64) * (K * 128) + swz(k, (n % 64) / 8) + (n % 8) * 2
+                                  : (k / 64) * (N * 128) + swz(n, (k % 64) / 8) + (k % 8) * 2;
         *reinterpret_cast<__nv_bfloat16*>(sm + B_OFF + off) = B[e];
     }
     __syncthreads();
@@ -127,9 +130,11 @@ mma_tmem_a_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int 
     __syncthreads();
     if (tid == 0) {
         tc_fence_after();
-        for (int ks = 0; ks < K / 16; ++ks)
-            mma_bf16_ta(tmem, tmem + 128 + 8 * ks, smem_desc(sb + B_OFF + ks * 2048, N > 64 ? K * 128 : 1024, 1024),
-                        idesc_bf16(128, N, 0, 1), ks > 0);
+        for (int ks = 0; ks < K / 16; ++ks) {
+            const uint64_t bd = b_mn ? smem_desc(sb + B_OFF + ks * 2048, N > 64 ? K * 128 : 1024, 1024)
+                                     : smem_desc(sb + B_OFF + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+            mma_bf16_ta(tmem, tmem + 128 + 8 * ks, bd, idesc_bf16(128, N, 0, b_mn), ks > 0);
+        }
         mma_commit(sb + BAR);
     }
     mbar_wait_bounded(sb + BAR, 0, abort_flag, status, 1u, 1000000000ull);
@@ -148,13 +153,14 @@ mma_tmem_a_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int 
     }
 }
 
-extern "C" int tc_selftest_mma_tmem_a(const void* A, const void* B, float* D, int K, int N, unsigned* status) {
+extern "C" int tc_selftest_mma_tmem_a(const void* A, const void* B, float* D, int K, int N, int b_mn,
+                                      unsigned* status) {
     if (K % 64 || K < 64 || K > 128 || N % 64 || N < 64 || N > 128) return 1;
     const int smem = 73728 + 64 + 1024;
     if (cudaFuncSetAttribute(mma_tmem_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 2;
     mma_tmem_a_kernel<<<1, 128, smem>>>(static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B),
-                                        D, K, N, status);
+                                        D, K, N, b_mn, status);
     return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

@@ -29,7 +29,7 @@ def lib():
         subprocess.check_call([b._nvcc(), *b.NVCC_FLAGS, "-shared", "-o", LIB, SRC])
     L = ctypes.CDLL(LIB)
     L.tc_selftest_mma.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
-    L.tc_selftest_mma_tmem_a.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 2 + [ctypes.c_void_p]
+    L.tc_selftest_mma_tmem_a.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     L.tc_selftest_wait_runs_out.argtypes = [ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]
     return L
 
@@ -58,16 +58,17 @@ def test_mma_layout(lib, a_mn, b_mn, K, N):
     assert err < 1e-5, f"max rel err {err:.3e}"
 
 
-@pytest.mark.parametrize("K,N", [(64, 128), (128, 128), (128, 64)])
-def test_mma_a_from_tmem(lib, K, N):
-    """A operand held in TMEM (as the prefill's P and T diag(beta gamma) operands are)."""
+@pytest.mark.parametrize("K,N,b_mn", [(64, 128, 1), (128, 128, 1), (128, 64, 1), (128, 128, 0), (64, 128, 0)])
+def test_mma_a_from_tmem(lib, K, N, b_mn):
+    """A operand held in TMEM (as the prefill's P and T diag(beta gamma) operands and the chain's
+    transposed state are), B from shared memory MN-major or K-major."""
     rng = np.random.default_rng(K + 3 * N)
     A = torch.from_numpy(rng.normal(size=(128, K)).astype(np.float32)).bfloat16()
     B = torch.from_numpy(rng.normal(size=(K, N)).astype(np.float32)).bfloat16()
     Ad, Bd = A.cuda(), B.cuda()
     D = torch.zeros(128, N, dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    assert lib.tc_selftest_mma_tmem_a(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), K, N, status.data_ptr()) == 0
+    assert lib.tc_selftest_mma_tmem_a(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), K, N, b_mn, status.data_ptr()) == 0
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "bounded wait ran out"
     ref = A.double().numpy() @ B.double().numpy()
