@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # were taken on (sha256 prefix of the file); None once the source has changed.
 NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix of that file at capture, dram read + write bytes per launch)
-    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "c4cfed590072d332", 139530496 + 345115136),
-    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "c4cfed590072d332", 612460032 + 120580352),
+    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "565b2e8189a6d2b7", 139437568 + 344683264),
+    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "565b2e8189a6d2b7", 612447744 + 120327168),
     "decode_step_kernel": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_decode.cu", "0a3ae9abf76d8679", 541133568 + 480455680),
 }
 
