@@ -2,333 +2,918 @@
 // v, g, beta and S0.  The forward is the token loop of "Transformer by Hand, ch. 7" (section "The
 // formula", `delta_rule`), per sequence and value head with a_t = exp(g_t):
 //     p = S^T k,   u = beta (v - a p),   S <- a S + k u^T,   o = scale S^T q.
-// Walking it backwards with lam = dL/dS_t (from dL/dS_final):
-//     lam += scale q do^T;   dq = scale (a S_{t-1} do + k (u.do));   du = lam^T k;   dk = lam u + S_{t-1} dp;
-//     dv = beta du;   dbeta = du.(v - a p);   dp = -a beta du;   dg = a (<lam, S_{t-1}> - beta du.p);
-//     lam <- a lam + k dp^T;   dS0 = lam at the sequence start.
-// The value columns of S evolve independently, so one CTA owns one (sequence, value head, 32-column
-// slice): warp w holds key rows R*w .. R*w+R-1 and lane j one column, state and adjoint in registers.
-// The backward needs S_{t-1} in reverse order: a forward pass stores a checkpoint every kCk tokens;
-// then, chunk by chunk from the end, the chunk's states are recomputed into a per-CTA scratch (about
-// 64 MB over the whole grid, L2-resident) and walked backwards.  Sums over the value columns (dq, dk,
-// dg, dbeta) are per-slice partials, added by a second kernel that also folds the GQA head groups.
-// Token-serial on CUDA cores: a first path, not a tensor-core kernel.
+// The gradient is taken through the chunked form of that loop (chunk length C = 64, zero-padded at a
+// sequence end, which leaves the state unchanged).  Inside a chunk, with G_r = sum_{s<=r} g_s,
+// D_rs = exp(G_r - G_s) for s <= r, gamma = exp(G), S the state at the chunk start:
+//     A = strict lower part of D o (K K^T),    T = (I + diag(beta) A)^{-1},
+//     W = T diag(beta gamma) K,   U~ = T diag(beta) V,   U = U~ - W S,
+//     P = scale D o (Q K^T) (s <= r),   O = scale diag(gamma) Q S + P U,
+//     S' = gamma_C S + K~^T U,   K~ = diag(gamma_C / gamma) K.
+// Its adjoint, for dO and lam = dL/dS' given:
+//     dU = K~ lam + P^T dO,   dL/dS = gamma_C lam + scale Q^T diag(gamma) dO - W^T dU,
+// and the chunk-local gradients follow by the chain rule through T (dT -> -T^T dT T^T), the decay
+// ratios (d exp(G_r - G_s) adds to G_r and subtracts from G_s) and dg = reverse cumulative sum of dG.
+//
+// Four kernels, fp32 on the CUDA cores:
+//   bwd_wy_kernel         per (chunk, query/key head): T, W, U~, P and G of each of its value heads
+//   bwd_state_fwd_kernel  per (sequence, value head, column slice): chunk-start states S, and U
+//   bwd_state_adj_kernel  per (sequence, value head, column slice), chunks in reverse: lam, dU, dS0
+//   bwd_local_kernel      per (chunk, query/key head): dq, dk (summed over its value heads), dv, dg, dbeta
+// Chunks of sequence i occupy workspace slots floor(t0_i / C) + i + c, so no prefix sum is needed.
 #include "gdn_internal.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kW = 32;         // value columns per CTA
-constexpr int kCk = 16;        // tokens between checkpoints
-constexpr int kWarps = 8;
-constexpr int kThreads = 32 * kWarps;
+constexpr int kC = 64;      // chunk length
+constexpr int kLC = kC + 1; // padded row length of C x C matrices in shared memory
 
-template <int DK>
-struct BwdSmem {
-    float q[2][DK], k[2][DK];       // staged token (double buffered)
-    float v[2][kW], dout[2][kW];
-    float a[2], beta[2];
-    float red_p[kWarps][kW], red_d[kWarps][kW];
-    float wsum[kWarps];
-    float csum[3];
-};
-
-// Stage token `tok` of value head h (query/key head hk) into buffer `buf`.  Needs q and dout only for
-// backward steps.
-template <typename T, int DK>
-__device__ __forceinline__ void stage(BwdSmem<DK>& s, int buf, const T* q, const T* k, const T* v, const T* g,
-                                      const T* beta, const T* dout, long long tok, int h, int hk, int Hqk, int Hv,
-                                      int dv, int col0, bool with_q) {
-    const int tid = threadIdx.x;
-    if (tid < DK) {
-        s.k[buf][tid] = to_f32(k[(tok * Hqk + hk) * DK + tid]);
-        if (with_q) s.q[buf][tid] = to_f32(q[(tok * Hqk + hk) * DK + tid]);
-    } else if (tid < DK + kW) {
-        const int j = tid - DK;
-        s.v[buf][j] = to_f32(v[(tok * Hv + h) * dv + col0 + j]);
-        if (with_q) s.dout[buf][j] = to_f32(dout[(tok * Hv + h) * dv + col0 + j]);
-    } else if (tid == DK + kW) {
-        s.a[buf] = __expf(to_f32(g[tok * Hv + h]));
-        s.beta[buf] = to_f32(beta[tok * Hv + h]);
-    }
-}
-
-// One forward step on the thread's rows: p_j = sum_i S[i] k_i over the whole column, then the write.
-template <int DK>
-__device__ __forceinline__ void forward_step(float (&S)[DK / kWarps], BwdSmem<DK>& s, int buf, int w, int j) {
-    constexpr int R = DK / kWarps;
-    float pp = 0.f;
+// ---------------------------------------------------------------- register-tile products
+// acc[i][m] += sum_{k<K} opA(row0 + i, k) * ks[k] * opB(k, tx + 16 m)   (ks[k] = 1 unless KS), where
+//   opA(r, k) = AT ? A[k * lda + r] : A[r * lda + k],   opB(k, n) = BT ? B[n * ldb + k] : B[k * ldb + n].
+// Threads (ty, tx = tid % 16) tile the output: rows row0 = ty * RM .. + RM - 1, columns tx + 16 m.  All
+// shared-memory leading dimensions are 1 mod 32, so both operand forms are free of bank conflicts.
+template <int RM, int CN, bool AT, bool BT, int K, bool KS = false>
+__device__ __forceinline__ void tile_mm(float (&acc)[RM][CN], const float* __restrict__ A, int lda,
+                                        const float* __restrict__ B, int ldb, int row0, int tx,
+                                        const float* __restrict__ ks = nullptr) {
+#pragma unroll 8
+    for (int k = 0; k < K; ++k) {
+        float a[RM], b[CN];
+        const float s = KS ? ks[k] : 1.f;
 #pragma unroll
-    for (int i = 0; i < R; ++i) pp = fmaf(S[i], s.k[buf][R * w + i], pp);
-    s.red_p[w][j] = pp;
-    __syncthreads();
-    float p = 0.f;
-#pragma unroll
-    for (int x = 0; x < kWarps; ++x) p += s.red_p[x][j];
-    const float a = s.a[buf];
-    const float u = s.beta[buf] * (s.v[buf][j] - a * p);
-#pragma unroll
-    for (int i = 0; i < R; ++i) S[i] = fmaf(a, S[i], s.k[buf][R * w + i] * u);
-}
-
-// Sum of v[i] over the 32 lanes for every row i < R, by halving: after the call lane `lane` holds the
-// total of row row_of_lane<R>(lane) (all lanes hold one; several hold the same row).
-template <int R>
-__device__ __forceinline__ float row_reduce(float (&v)[R], int lane) {
-    int m = 16;
-#pragma unroll
-    for (int n = R; n > 1; n >>= 1, m >>= 1) {
-        const bool up = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; ++i) {
-            const float keep = up ? v[i + n / 2] : v[i];
-            const float send = up ? v[i] : v[i + n / 2];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        for (int i = 0; i < RM; ++i) {
+            a[i] = AT ? A[k * lda + row0 + i] : A[(row0 + i) * lda + k];
+            if (KS) a[i] *= s;
         }
+#pragma unroll
+        for (int m = 0; m < CN; ++m) b[m] = BT ? B[(tx + 16 * m) * ldb + k] : B[k * ldb + tx + 16 * m];
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
+#pragma unroll
+            for (int m = 0; m < CN; ++m) acc[i][m] = fmaf(a[i], b[m], acc[i][m]);
     }
-    float r = v[0];
-    for (; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
-    return r;
-}
-template <int R>
-__device__ __forceinline__ int row_of_lane(int lane) {
-    int row = 0, m = 16;
-#pragma unroll
-    for (int n = R; n > 1; n >>= 1, m >>= 1)
-        if (lane & m) row += n / 2;
-    return row;
-}
-// The one lane per row that writes it: the lane bits below the halving masks are zero.
-template <int R>
-__device__ __forceinline__ bool row_writer(int lane) {
-    int m = 16;
-#pragma unroll
-    for (int n = R; n > 1; n >>= 1) m >>= 1;
-    return (lane & (2 * m - 1)) == 0;
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
+template <int RM, int CN>
+__device__ __forceinline__ void tile_zero(float (&acc)[RM][CN]) {
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int m = 0; m < CN; ++m) acc[i][m] = 0.f;
+}
+
+// Sum over the 16 lanes that share a row group (tx = lane % 16).
+__device__ __forceinline__ float sum16(float x) {
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
     return x;
 }
 
-template <typename T, int DK>
-__global__ void __launch_bounds__(kThreads)
-bwd_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, const T* __restrict__ g,
-           const T* __restrict__ beta, const float* __restrict__ S0, const T* __restrict__ dout,
-           const float* __restrict__ dS_final, float* __restrict__ part, float* __restrict__ grad_v,
-           float* __restrict__ grad_S0, float* __restrict__ ckpt, float* __restrict__ scratch, int T_len, int Hqk,
-           int Hv, int dv, const int32_t* __restrict__ cu, int nseq, float scale) {
-    constexpr int R = DK / kWarps;
-    __shared__ BwdSmem<DK> s;
-    const int nsl = dv / kW;
-    const int sl = blockIdx.x % nsl, h = (blockIdx.x / nsl) % Hv, seq = blockIdx.x / (nsl * Hv);
-    if (seq >= nseq) return;
-    const int hk = h / (Hv / Hqk), col0 = sl * kW;
-    const int w = threadIdx.x >> 5, j = threadIdx.x & 31;
-    long long t0, t1;
-    seq_range(cu, seq, T_len, t0, t1);
-    const long long len = t1 - t0;
-    const long long nch = (len + kCk - 1) / kCk;
-    // checkpoint slots of this sequence: slot(seq, c) = floor(t0 / kCk) + seq + c (no prefix sum needed)
-    const long long slot0 = t0 / kCk + seq;
-    const size_t slice = (size_t)DK * kW;
-    const auto ck = [&](long long c) { return ckpt + (((slot0 + c) * Hv + h) * nsl + sl) * slice; };
-    float* scr = scratch + (size_t)blockIdx.x * kCk * slice;
-    const size_t state_base = ((size_t)seq * Hv + h) * DK * dv + col0 + j;   // element (row 0, column j)
-
-    float S[R];
+// 16 bytes of fp32 or bf16 values as fp32 (bf16 -> fp32 is a 16-bit shift).
+__device__ __forceinline__ void unpack16(const uint4& u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int i = 0; i < R; ++i) S[i] = S0 ? S0[state_base + (size_t)(R * w + i) * dv] : 0.f;
-
-    // ---- forward pass: checkpoint every kCk tokens
-    int buf = 0;
-    for (long long t = t0; t < t1; ++t, buf ^= 1) {
-        if ((t - t0) % kCk == 0) {
-            float* c = ck((t - t0) / kCk);
-#pragma unroll
-            for (int i = 0; i < R; ++i) c[(R * w + i) * kW + j] = S[i];
-        }
-        stage<T, DK>(s, buf, q, k, v, g, beta, dout, t, h, hk, Hqk, Hv, dv, col0, false);
-        __syncthreads();
-        forward_step<DK>(S, s, buf, w, j);
-    }
-
-    // ---- backward pass, chunk by chunk from the end
-    float lam[R];
-#pragma unroll
-    for (int i = 0; i < R; ++i) lam[i] = dS_final ? dS_final[state_base + (size_t)(R * w + i) * dv] : 0.f;
-    const int my_row = row_of_lane<R>(j);
-    const bool writer = row_writer<R>(j);
-    for (long long c = nch - 1; c >= 0; --c) {
-        const long long tc0 = t0 + c * kCk, tc1 = min(t1, tc0 + kCk);
-        const float* cs = ck(c);
-#pragma unroll
-        for (int i = 0; i < R; ++i) S[i] = cs[(R * w + i) * kW + j];
-        for (long long t = tc0; t < tc1; ++t, buf ^= 1) {   // recompute the chunk's states S_{t-1}
-            float* d = scr + (t - tc0) * slice;
-#pragma unroll
-            for (int i = 0; i < R; ++i) d[(R * w + i) * kW + j] = S[i];
-            stage<T, DK>(s, buf, q, k, v, g, beta, dout, t, h, hk, Hqk, Hv, dv, col0, false);
-            __syncthreads();
-            forward_step<DK>(S, s, buf, w, j);
-        }
-        for (long long t = tc1 - 1; t >= tc0; --t, buf ^= 1) {
-            const float* d = scr + (t - tc0) * slice;
-            float Sp[R];
-#pragma unroll
-            for (int i = 0; i < R; ++i) Sp[i] = d[(R * w + i) * kW + j];
-            stage<T, DK>(s, buf, q, k, v, g, beta, dout, t, h, hk, Hqk, Hv, dv, col0, true);
-            __syncthreads();
-            const float a = s.a[buf], bt = s.beta[buf], doj = s.dout[buf][j], vj = s.v[buf][j];
-            const float* kk = s.k[buf];
-            const float* qq = s.q[buf];
-            float pp = 0.f, dd = 0.f;
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                lam[i] = fmaf(scale * qq[R * w + i], doj, lam[i]);
-                pp = fmaf(Sp[i], kk[R * w + i], pp);
-                dd = fmaf(lam[i], kk[R * w + i], dd);
-            }
-            s.red_p[w][j] = pp;
-            s.red_d[w][j] = dd;
-            __syncthreads();
-            float p = 0.f, du = 0.f;
-#pragma unroll
-            for (int x = 0; x < kWarps; ++x) {
-                p += s.red_p[x][j];
-                du += s.red_d[x][j];
-            }
-            const float r = vj - a * p;
-            const float u = bt * r;
-            const float dp = -a * bt * du;
-            float rq[R], rk[R], ls = 0.f;
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-                rq[i] = a * Sp[i] * doj;
-                rk[i] = fmaf(lam[i], u, Sp[i] * dp);
-                ls = fmaf(lam[i], Sp[i], ls);
-            }
-            ls = warp_sum(ls);
-            if (w == 0) {
-                const float cb = warp_sum(du * r), ca = warp_sum(-bt * du * p), cu_ = warp_sum(u * doj);
-                if (j == 0) {
-                    s.csum[0] = cb;
-                    s.csum[1] = ca;
-                    s.csum[2] = cu_;
-                }
-            }
-            if (j == 0) s.wsum[w] = ls;
-            const float q_row = row_reduce<R>(rq, j);
-            const float k_row = row_reduce<R>(rk, j);
-            __syncthreads();
-            float da = s.csum[1];
-#pragma unroll
-            for (int x = 0; x < kWarps; ++x) da += s.wsum[x];
-            float* pr = part + (((size_t)t * Hv + h) * nsl + sl) * (2 * DK + 2);
-            if (writer) {
-                const int row = R * w + my_row;
-                pr[row] = scale * fmaf(kk[row], s.csum[2], q_row);
-                pr[DK + row] = k_row;
-            }
-            if (threadIdx.x == 0) {
-                pr[2 * DK] = a * da;
-                pr[2 * DK + 1] = s.csum[0];
-            }
-            if (w == 0) grad_v[((size_t)t * Hv + h) * dv + col0 + j] = bt * du;
-#pragma unroll
-            for (int i = 0; i < R; ++i) lam[i] = fmaf(a, lam[i], kk[R * w + i] * dp);
-        }
-    }
-    if (grad_S0) {
-#pragma unroll
-        for (int i = 0; i < R; ++i) grad_S0[state_base + (size_t)(R * w + i) * dv] = lam[i];
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
 }
 
-// Sum the per-slice partials: dq, dk of query/key head hk over its value heads and slices; dg, dbeta
-// of value head h over its slices.  One block per token.
-template <int DK>
-__global__ void __launch_bounds__(256)
-bwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ grad_q, float* __restrict__ grad_k,
-                  float* __restrict__ grad_g, float* __restrict__ grad_beta, int Hqk, int Hv, int nsl) {
-    const long long tok = blockIdx.x;
-    const int G = Hv / Hqk;
-    const size_t stride = 2 * DK + 2;
-    for (int idx = threadIdx.x; idx < Hqk * DK; idx += blockDim.x) {
-        const int hk = idx / DK, i = idx % DK;
-        float sq = 0.f, sk = 0.f;
-        for (int h = hk * G; h < (hk + 1) * G; ++h)
-            for (int sl = 0; sl < nsl; ++sl) {
-                const float* pr = part + ((tok * Hv + h) * nsl + sl) * stride;
-                sq += pr[i];
-                sk += pr[DK + i];
-            }
-        grad_q[(tok * Hqk + hk) * DK + i] = sq;
-        grad_k[(tok * Hqk + hk) * DK + i] = sk;
-    }
-    for (int h = threadIdx.x; h < Hv; h += blockDim.x) {
-        float sg = 0.f, sb = 0.f;
-        for (int sl = 0; sl < nsl; ++sl) {
-            const float* pr = part + ((tok * Hv + h) * nsl + sl) * stride;
-            sg += pr[2 * DK];
-            sb += pr[2 * DK + 1];
+// Rows [0, ROWS) x columns [0, WIDTH) of an element-type block (global row stride `stride` elements;
+// rows >= n read as zero) into shared memory as fp32 with leading dimension `ld`.  With `vec` (the
+// source 16-byte aligned; strides and widths are multiples of 16 bytes) every thread issues all of
+// its 16-byte loads before its stores.
+template <typename TT, int ROWS, int WIDTH, int NT>
+__device__ __forceinline__ void ld_in(float* __restrict__ dst, int ld, const TT* __restrict__ src, size_t stride,
+                                      int n, int tid, bool vec) {
+    constexpr int EPV = 16 / (int)sizeof(TT), V = WIDTH / EPV, TOTAL = ROWS * V, PER = (TOTAL + NT - 1) / NT;
+    if (vec) {
+        uint4 b[PER];
+#pragma unroll
+        for (int p = 0; p < PER; ++p) {
+            const int idx = tid + p * NT, r = idx / V;
+            b[p] = make_uint4(0u, 0u, 0u, 0u);
+            if ((TOTAL % NT == 0 || idx < TOTAL) && r < n)
+                b[p] = *reinterpret_cast<const uint4*>(src + (size_t)r * stride + (idx % V) * EPV);
         }
-        grad_g[tok * Hv + h] = sg;
-        grad_beta[tok * Hv + h] = sb;
+#pragma unroll
+        for (int p = 0; p < PER; ++p) {
+            const int idx = tid + p * NT;
+            if (TOTAL % NT == 0 || idx < TOTAL) {
+                float f[EPV];
+                unpack16(b[p], f);
+                float* d = dst + (idx / V) * ld + (idx % V) * EPV;
+#pragma unroll
+                for (int x = 0; x < EPV; ++x) d[x] = f[x];
+            }
+        }
+    } else {
+        for (int idx = tid; idx < ROWS * WIDTH; idx += NT) {
+            const int r = idx / WIDTH, j = idx % WIDTH;
+            dst[r * ld + j] = r < n ? to_f32(src[(size_t)r * stride + j]) : 0.f;
+        }
+    }
+}
+
+// Same for fp32 workspace blocks (always 16-byte aligned, all rows valid).
+template <int ROWS, int WIDTH, int NT>
+__device__ __forceinline__ void ld_ws(float* __restrict__ dst, int ld, const float* __restrict__ src, size_t stride,
+                                      int tid) {
+    ld_in<float, ROWS, WIDTH, NT>(dst, ld, src, stride, ROWS, tid, true);
+}
+
+// Workspace slot of chunk 0 of sequence i.
+__device__ __forceinline__ long long slot_base(const int32_t* cu, int i, int T) {
+    long long t0, t1;
+    seq_range(cu, i, T, t0, t1);
+    return t0 / kC + i;
+}
+
+// The (sequence, first token, valid rows) of a workspace slot, or false for a slot that holds no chunk.
+__device__ __forceinline__ bool slot_chunk(const int32_t* cu, int nseq, int T, long long slot, int& seq,
+                                           long long& tok0, int& n) {
+    int lo = 0, hi = nseq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (slot_base(cu, mid, T) <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    long long t0, t1;
+    seq_range(cu, lo, T, t0, t1);
+    const long long c = slot - (t0 / kC + lo);
+    if (c < 0 || t0 + c * kC >= t1) return false;
+    seq = lo;
+    tok0 = t0 + c * kC;
+    n = (int)min((long long)kC, t1 - tok0);
+    return true;
+}
+
+// Per-(slot, value head) workspace arrays.
+struct Ws {
+    float *T, *P, *W, *U, *G, *S, *dS, *dU;
+};
+
+template <int DK, int DV>
+struct WsDims {
+    static constexpr size_t T = (size_t)kC * kC, P = (size_t)kC * kC, W = (size_t)kC * DK, U = (size_t)kC * DV,
+                            G = kC, S = (size_t)DK * DV, dS = (size_t)DK * DV, dU = (size_t)kC * DV;
+};
+
+// ---------------------------------------------------------------- kernel 1: WY factors per chunk
+constexpr int kWyThreads = 256;   // = 4 threads per column of T in the solve
+
+template <int DK, int DV>
+struct WySmem {
+    static constexpr int LK = DK + 1, LQV = (DK > DV ? DK : DV) + 1;
+    static constexpr int K_ = 0, QV_ = K_ + kC * LK, KK_ = QV_ + kC * LQV, QK_ = KK_ + kC * kLC,
+                         L_ = QK_ + kC * kLC, T_ = L_ + kC * kLC, VEC_ = T_ + kC * kLC;
+    static constexpr int FLOATS = VEC_ + 4 * kC;
+    static constexpr size_t BYTES = (size_t)FLOATS * 4;
+};
+
+template <typename TT, int DK, int DV>
+__global__ void __launch_bounds__(kWyThreads)
+bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __restrict__ v, const TT* __restrict__ g,
+              const TT* __restrict__ beta, Ws ws, int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu,
+              int nseq, float scale, bool vec) {
+    using L = WySmem<DK, DV>;
+    using D = WsDims<DK, DV>;
+    static_assert(kWyThreads == 4 * kC, "the solve takes four threads per column");
+    extern __shared__ float sm[];
+    float* sK = sm + L::K_;
+    float* sQV = sm + L::QV_;
+    float* sKK = sm + L::KK_;
+    float* sQK = sm + L::QK_;
+    float* sL = sm + L::L_;
+    float* sT = sm + L::T_;
+    float* sG = sm + L::VEC_;
+    float* sBeta = sG + kC;
+    float* sBG = sBeta + kC;
+    float* sGraw = sBG + kC;
+
+    const long long slot = blockIdx.x;
+    const int hk = blockIdx.y, G = Hv / Hqk;
+    int seq, n;
+    long long tok0;
+    if (!slot_chunk(cu, nseq, T_len, slot, seq, tok0, n)) return;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+
+    ld_in<TT, kC, DK, kWyThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+    ld_in<TT, kC, DK, kWyThreads>(sQV, L::LQV, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+    __syncthreads();
+    {   // Gram matrices K K^T and Q K^T (C x C: 4 rows x 4 columns per thread)
+        float kk[4][4], qk[4][4];
+        tile_zero(kk);
+        tile_zero(qk);
+        tile_mm<4, 4, false, true, DK>(kk, sK, L::LK, sK, L::LK, ty * 4, tx);
+        tile_mm<4, 4, false, true, DK>(qk, sQV, L::LQV, sK, L::LK, ty * 4, tx);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                sKK[(ty * 4 + i) * kLC + tx + 16 * m] = kk[i][m];
+                sQK[(ty * 4 + i) * kLC + tx + 16 * m] = qk[i][m];
+            }
+    }
+    __syncthreads();
+
+    for (int j = 0; j < G; ++j) {
+        const int h = hk * G + j;
+        const size_t wi = (size_t)slot * Hv + h;
+        if (tid < kC) {
+            const bool ok = tid < n;
+            sGraw[tid] = ok ? to_f32(g[(tok0 + tid) * Hv + h]) : 0.f;
+            sBeta[tid] = ok ? to_f32(beta[(tok0 + tid) * Hv + h]) : 0.f;
+        }
+        // V of this value head (Q is no longer needed: its Gram is in sQK)
+        ld_in<TT, kC, DV, kWyThreads>(sQV, L::LQV, v + (tok0 * Hv + h) * DV, (size_t)Hv * DV, n, tid, vec);
+        __syncthreads();
+        if (tid == 0) {
+            float acc = 0.f;
+            for (int r = 0; r < kC; ++r) {
+                acc += sGraw[r];
+                sG[r] = acc;
+            }
+        }
+        __syncthreads();
+        if (tid < kC) {
+            sBG[tid] = sBeta[tid] * __expf(sG[tid]);
+            ws.G[wi * D::G + tid] = sG[tid];
+        }
+        // P = scale D o QK^T (s <= r) to the workspace; L = diag(beta) (D o KK^T) strictly below the diagonal
+        for (int idx = tid; idx < kC * kC; idx += kWyThreads) {
+            const int r = idx / kC, s = idx % kC;
+            const float d = s <= r ? __expf(sG[r] - sG[s]) : 0.f;
+            ws.P[wi * D::P + idx] = scale * d * sQK[r * kLC + s];
+            sL[r * kLC + s] = s < r ? sBeta[r] * d * sKK[r * kLC + s] : 0.f;
+        }
+        __syncthreads();
+        {   // T = (I + L)^{-1} by forward substitution, four threads per column:
+            // T[r][col] = [r == col] - sum_{s<r} L[r][s] T[s][col]   (T[s][col] = 0 for s < col)
+            const int col = tid / 4, part = tid % 4;
+            for (int r = 0; r < kC; ++r) {
+                float x = 0.f;
+                for (int s = part; s < r; s += 4) x = fmaf(sL[r * kLC + s], sT[s * kLC + col], x);
+                x += __shfl_xor_sync(0xffffffffu, x, 1);
+                x += __shfl_xor_sync(0xffffffffu, x, 2);
+                if (part == 0) sT[r * kLC + col] = r < col ? 0.f : (r == col ? 1.f : -x);
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < kC * kC; idx += kWyThreads) ws.T[wi * D::T + idx] = sT[(idx / kC) * kLC + idx % kC];
+        {   // W = T diag(beta gamma) K
+            constexpr int CN = DK / 16;
+            float acc[4][CN];
+            tile_zero(acc);
+            tile_mm<4, CN, false, false, kC, true>(acc, sT, kLC, sK, L::LK, ty * 4, tx, sBG);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int m = 0; m < CN; ++m) ws.W[wi * D::W + (size_t)(ty * 4 + i) * DK + tx + 16 * m] = acc[i][m];
+        }
+        {   // U~ = T diag(beta) V
+            constexpr int CN = DV / 16;
+            float acc[4][CN];
+            tile_zero(acc);
+            tile_mm<4, CN, false, false, kC, true>(acc, sT, kLC, sQV, L::LQV, ty * 4, tx, sBeta);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int m = 0; m < CN; ++m) ws.U[wi * D::U + (size_t)(ty * 4 + i) * DV + tx + 16 * m] = acc[i][m];
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- kernels 2 and 3: the chunk chains
+constexpr int kStThreads = 256;
+
+template <int DV>
+constexpr int slice_width() { return DV < 64 ? DV : 64; }
+
+template <int DK, int DV>
+struct StSmem {
+    static constexpr int SW = slice_width<DV>(), LK = DK + 1, LS = SW + 1;
+    // forward: W, K, U slice, S slice.  adjoint: W, K, Q, P, dO slice, dU slice, lam slice
+    static constexpr int W_ = 0, K_ = W_ + kC * LK, Q_ = K_ + kC * LK, P_ = Q_ + kC * LK, X_ = P_ + kC * kLC,
+                         Y_ = X_ + kC * LS, S_ = Y_ + kC * LS, G_ = S_ + DK * LS, R_ = G_ + kC;
+    static constexpr int FLOATS = R_ + kC;
+    static constexpr size_t BYTES = (size_t)FLOATS * 4;
+};
+
+// Chunk-start states S (to the workspace) and U = U~ - W S (over U~ in the workspace).
+template <typename TT, int DK, int DV>
+__global__ void __launch_bounds__(kStThreads)
+bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws ws, int T_len, int Hqk, int Hv,
+                     const int32_t* __restrict__ cu, int nseq, bool vec) {
+    using L = StSmem<DK, DV>;
+    using D = WsDims<DK, DV>;
+    constexpr int SW = L::SW, NSL = DV / SW;
+    extern __shared__ float sm[];
+    float* sW = sm + L::W_;
+    float* sK = sm + L::K_;
+    float* sU = sm + L::X_;
+    float* sS = sm + L::S_;
+    float* sG = sm + L::G_;
+    const int sl = blockIdx.x % NSL, h = (blockIdx.x / NSL) % Hv, seq = blockIdx.x / (NSL * Hv);
+    if (seq >= nseq) return;
+    const int hk = h / (Hv / Hqk), col0 = sl * SW;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    long long t0, t1;
+    seq_range(cu, seq, T_len, t0, t1);
+    const long long nch = (t1 - t0 + kC - 1) / kC, slot0 = t0 / kC + seq;
+    const size_t sbase = ((size_t)seq * Hv + h) * DK * DV + col0;
+    for (int idx = tid; idx < DK * SW; idx += kStThreads) {
+        const int i = idx / SW, j = idx % SW;
+        sS[i * L::LS + j] = S0 ? S0[sbase + (size_t)i * DV + j] : 0.f;
+    }
+    constexpr int RU = kC / 16, CU = SW / 16;   // U tile: C x SW
+    constexpr int RS = DK / 16;                 // S tile: DK x SW
+    for (long long c = 0; c < nch; ++c) {
+        const size_t wi = (size_t)(slot0 + c) * Hv + h;
+        const long long tok0 = t0 + c * kC;
+        const int n = (int)min((long long)kC, t1 - tok0);
+        if (tid < kC) sG[tid] = ws.G[wi * D::G + tid];
+        ld_ws<kC, DK, kStThreads>(sW, L::LK, ws.W + wi * D::W, DK, tid);
+        ld_ws<kC, SW, kStThreads>(sU, L::LS, ws.U + wi * D::U + col0, DV, tid);
+        ld_in<TT, kC, DK, kStThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+        __syncthreads();
+        for (int idx = tid; idx < DK * SW; idx += kStThreads) {
+            const int i = idx / SW, j = idx % SW;
+            ws.S[wi * D::S + (size_t)i * DV + col0 + j] = sS[i * L::LS + j];
+        }
+        {   // U = U~ - W S to the workspace; sU holds diag(gamma_C / gamma) U (each thread its own elements)
+            float acc[RU][CU];
+            tile_zero(acc);
+            tile_mm<RU, CU, false, false, DK>(acc, sW, L::LK, sS, L::LS, ty * RU, tx);
+#pragma unroll
+            for (int i = 0; i < RU; ++i) {
+                const int r = ty * RU + i;
+                const float kc = __expf(sG[kC - 1] - sG[r]);
+#pragma unroll
+                for (int m = 0; m < CU; ++m) {
+                    const int j = tx + 16 * m;
+                    const float u = sU[r * L::LS + j] - acc[i][m];
+                    sU[r * L::LS + j] = kc * u;
+                    ws.U[wi * D::U + (size_t)r * DV + col0 + j] = u;
+                }
+            }
+        }
+        __syncthreads();
+        {   // S <- gamma_C S + K^T diag(gamma_C / gamma) U
+            float acc[RS][CU];
+            tile_zero(acc);
+            tile_mm<RS, CU, true, false, kC>(acc, sK, L::LK, sU, L::LS, ty * RS, tx);
+            const float gC = __expf(sG[kC - 1]);
+#pragma unroll
+            for (int i = 0; i < RS; ++i)
+#pragma unroll
+                for (int m = 0; m < CU; ++m) {
+                    float& s = sS[(ty * RS + i) * L::LS + tx + 16 * m];
+                    s = fmaf(gC, s, acc[i][m]);
+                }
+        }
+        __syncthreads();
+    }
+}
+
+// Adjoint chain, chunks in reverse: lam (= dL/dS at the chunk end) and dU to the workspace; dS0 at the end.
+template <typename TT, int DK, int DV>
+__global__ void __launch_bounds__(kStThreads)
+bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __restrict__ dout,
+                     const float* __restrict__ dS_final, float* __restrict__ grad_S0, Ws ws, int T_len, int Hqk,
+                     int Hv, const int32_t* __restrict__ cu, int nseq, float scale, bool vec) {
+    using L = StSmem<DK, DV>;
+    using D = WsDims<DK, DV>;
+    constexpr int SW = L::SW, NSL = DV / SW;
+    extern __shared__ float sm[];
+    float* sW = sm + L::W_;
+    float* sK = sm + L::K_;
+    float* sQ = sm + L::Q_;
+    float* sP = sm + L::P_;
+    float* sdO = sm + L::X_;
+    float* sdU = sm + L::Y_;
+    float* sLam = sm + L::S_;
+    float* sG = sm + L::G_;
+    float* sQs = sm + L::R_;   // scale gamma_r
+    const int sl = blockIdx.x % NSL, h = (blockIdx.x / NSL) % Hv, seq = blockIdx.x / (NSL * Hv);
+    if (seq >= nseq) return;
+    const int hk = h / (Hv / Hqk), col0 = sl * SW;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    long long t0, t1;
+    seq_range(cu, seq, T_len, t0, t1);
+    const long long nch = (t1 - t0 + kC - 1) / kC, slot0 = t0 / kC + seq;
+    const size_t sbase = ((size_t)seq * Hv + h) * DK * DV + col0;
+    for (int idx = tid; idx < DK * SW; idx += kStThreads) {
+        const int i = idx / SW, j = idx % SW;
+        sLam[i * L::LS + j] = dS_final ? dS_final[sbase + (size_t)i * DV + j] : 0.f;
+    }
+    constexpr int RU = kC / 16, CU = SW / 16;
+    constexpr int RS = DK / 16;
+    for (long long c = nch - 1; c >= 0; --c) {
+        const size_t wi = (size_t)(slot0 + c) * Hv + h;
+        const long long tok0 = t0 + c * kC;
+        const int n = (int)min((long long)kC, t1 - tok0);
+        if (tid < kC) {
+            const float gr = ws.G[wi * D::G + tid];
+            sG[tid] = gr;
+            sQs[tid] = scale * __expf(gr);
+        }
+        ld_ws<kC, DK, kStThreads>(sW, L::LK, ws.W + wi * D::W, DK, tid);
+        ld_ws<kC, kC, kStThreads>(sP, kLC, ws.P + wi * D::P, kC, tid);
+        ld_in<TT, kC, DK, kStThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+        ld_in<TT, kC, DK, kStThreads>(sQ, L::LK, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+        ld_in<TT, kC, SW, kStThreads>(sdO, L::LS, dout + (tok0 * Hv + h) * DV + col0, (size_t)Hv * DV, n, tid, vec);
+        __syncthreads();
+        for (int idx = tid; idx < DK * SW; idx += kStThreads) {
+            const int i = idx / SW, j = idx % SW;
+            ws.dS[wi * D::dS + (size_t)i * DV + col0 + j] = sLam[i * L::LS + j];
+        }
+        {   // dU = diag(gamma_C / gamma) K lam + P^T dO
+            float kl[RU][CU], acc[RU][CU];
+            tile_zero(kl);
+            tile_zero(acc);
+            tile_mm<RU, CU, false, false, DK>(kl, sK, L::LK, sLam, L::LS, ty * RU, tx);
+            tile_mm<RU, CU, true, false, kC>(acc, sP, kLC, sdO, L::LS, ty * RU, tx);
+#pragma unroll
+            for (int i = 0; i < RU; ++i) {
+                const int r = ty * RU + i;
+                const float kc = __expf(sG[kC - 1] - sG[r]);
+#pragma unroll
+                for (int m = 0; m < CU; ++m) {
+                    const int j = tx + 16 * m;
+                    const float du = fmaf(kc, kl[i][m], acc[i][m]);
+                    sdU[r * L::LS + j] = du;
+                    ws.dU[wi * D::dU + (size_t)r * DV + col0 + j] = du;
+                }
+            }
+        }
+        __syncthreads();
+        {   // lam <- gamma_C lam + Q^T diag(scale gamma) dO - W^T dU  (each thread rewrites its own elements)
+            float acc[RS][CU], neg[RS][CU];
+            tile_zero(acc);
+            tile_zero(neg);
+            tile_mm<RS, CU, true, false, kC, true>(acc, sQ, L::LK, sdO, L::LS, ty * RS, tx, sQs);
+            tile_mm<RS, CU, true, false, kC>(neg, sW, L::LK, sdU, L::LS, ty * RS, tx);
+            const float gC = __expf(sG[kC - 1]);
+#pragma unroll
+            for (int i = 0; i < RS; ++i)
+#pragma unroll
+                for (int m = 0; m < CU; ++m) {
+                    float& l = sLam[(ty * RS + i) * L::LS + tx + 16 * m];
+                    l = fmaf(gC, l, acc[i][m] - neg[i][m]);
+                }
+        }
+        __syncthreads();
+    }
+    if (grad_S0) {
+        for (int idx = tid; idx < DK * SW; idx += kStThreads) {
+            const int i = idx / SW, j = idx % SW;
+            grad_S0[sbase + (size_t)i * DV + j] = sLam[i * L::LS + j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel 4: chunk-local gradients
+constexpr int kLoThreads = 512;
+constexpr int kLoRowGroups = kLoThreads / 16;   // 32 row groups of 2 rows
+constexpr int kDvc = 32;                        // value columns per pass over dv
+
+template <int DK, int DV>
+struct LoSmem {
+    static constexpr int LK = DK + 1, LD = kDvc + 1;
+    static constexpr int K_ = 0, Q_ = K_ + kC * LK, KK_ = Q_ + kC * LK, QK_ = KK_ + kC * kLC, T_ = QK_ + kC * kLC,
+                         X_ = T_ + kC * kLC, DVB_ = X_ + kC * kLC;
+    // dv pass buffers (dU, U, dO, V: C x 32; S, lam: DK x 32); afterwards dW (C x DK) over them
+    static constexpr int dU_ = DVB_, U_ = dU_ + kC * LD, dO_ = U_ + kC * LD, V_ = dO_ + kC * LD, S_ = V_ + kC * LD,
+                         Lam_ = S_ + DK * LD, DVB_END = Lam_ + DK * LD, DW_END = DVB_ + kC * LK;
+    static constexpr int VEC_ = DVB_END > DW_END ? DVB_END : DW_END;
+    // G, beta, dG, dbeta, row scratch, h, column scratch [row groups][C], warp sums
+    static constexpr int G_ = VEC_, Beta_ = G_ + kC, dG_ = Beta_ + kC, dB_ = dG_ + kC, Row_ = dB_ + kC,
+                         H_ = Row_ + kC, Col_ = H_ + kC, Red_ = Col_ + kLoRowGroups * kC;
+    static constexpr int FLOATS = Red_ + kLoThreads / 32;
+    static constexpr size_t BYTES = (size_t)FLOATS * 4;
+};
+
+// dst[r] += rowsum_s F[r][s] - colsum_r F[r][s] for a C x C register tile F (2 x 4 per thread): the
+// derivative of sum F with respect to G through the ratios exp(G_r - G_s).
+__device__ __forceinline__ void add_rows_minus_cols(const float (&F)[2][4], float* sRow, float* sCol, float* dst,
+                                                    int tid, int tx, int ty) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float x = sum16(F[i][0] + F[i][1] + F[i][2] + F[i][3]);
+        if (tx == 0) sRow[ty * 2 + i] = x;
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) sCol[ty * kC + tx + 16 * m] = F[0][m] + F[1][m];
+    __syncthreads();
+    if (tid < kC) {
+        float c = 0.f;
+        for (int t = 0; t < kLoRowGroups; ++t) c += sCol[t * kC + tid];
+        dst[tid] += sRow[tid] - c;
+    }
+    __syncthreads();
+}
+
+// dst[r] += sum over the 16 lanes of a row group of x[i] (row ty * 2 + i).
+__device__ __forceinline__ void add_rows(const float (&x)[2], float* sRow, float* dst, int tid, int tx, int ty) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float s = sum16(x[i]);
+        if (tx == 0) sRow[ty * 2 + i] = s;
+    }
+    __syncthreads();
+    if (tid < kC) dst[tid] += sRow[tid];
+    __syncthreads();
+}
+
+template <typename TT, int DK, int DV>
+__global__ void __launch_bounds__(kLoThreads, 1)
+bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __restrict__ v,
+                 const TT* __restrict__ beta, const TT* __restrict__ dout, Ws ws, float* __restrict__ grad_q,
+                 float* __restrict__ grad_k, float* __restrict__ grad_v, float* __restrict__ grad_g,
+                 float* __restrict__ grad_beta, int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu, int nseq,
+                 float scale, bool vec) {
+    using L = LoSmem<DK, DV>;
+    using D = WsDims<DK, DV>;
+    constexpr int CK = DK / 16;   // columns per thread of a C x DK tile (2 rows each)
+    extern __shared__ float sm[];
+    float* sK = sm + L::K_;
+    float* sQ = sm + L::Q_;
+    float* sKK = sm + L::KK_;
+    float* sQK = sm + L::QK_;
+    float* sT = sm + L::T_;
+    float* sX = sm + L::X_;
+    float* sdU = sm + L::dU_;
+    float* sU = sm + L::U_;
+    float* sdO = sm + L::dO_;
+    float* sV = sm + L::V_;
+    float* sS = sm + L::S_;
+    float* sLam = sm + L::Lam_;
+    float* sDW = sm + L::DVB_;
+    float* sG = sm + L::G_;
+    float* sBeta = sm + L::Beta_;
+    float* sdG = sm + L::dG_;
+    float* sdB = sm + L::dB_;
+    float* sRow = sm + L::Row_;
+    float* sH = sm + L::H_;
+    float* sCol = sm + L::Col_;
+    float* sRed = sm + L::Red_;
+
+    const long long slot = blockIdx.x;
+    const int hk = blockIdx.y, G = Hv / Hqk;
+    int seq, n;
+    long long tok0;
+    if (!slot_chunk(cu, nseq, T_len, slot, seq, tok0, n)) return;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16, r0 = ty * 2;
+
+    ld_in<TT, kC, DK, kLoThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+    ld_in<TT, kC, DK, kLoThreads>(sQ, L::LK, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+    __syncthreads();
+    {
+        float kk[2][4], qk[2][4];
+        tile_zero(kk);
+        tile_zero(qk);
+        tile_mm<2, 4, false, true, DK>(kk, sK, L::LK, sK, L::LK, r0, tx);
+        tile_mm<2, 4, false, true, DK>(qk, sQ, L::LK, sK, L::LK, r0, tx);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                sKK[(r0 + i) * kLC + tx + 16 * m] = kk[i][m];
+                sQK[(r0 + i) * kLC + tx + 16 * m] = qk[i][m];
+            }
+    }
+
+    for (int jh = 0; jh < G; ++jh) {
+        const int h = hk * G + jh;
+        const size_t wi = (size_t)slot * Hv + h;
+        ld_ws<kC, kC, kLoThreads>(sT, kLC, ws.T + wi * D::T, kC, tid);
+        if (tid < kC) {
+            sG[tid] = ws.G[wi * D::G + tid];
+            sBeta[tid] = tid < n ? to_f32(beta[(tok0 + tid) * Hv + h]) : 0.f;
+            sdG[tid] = 0.f;
+            sdB[tid] = 0.f;
+        }
+        float aW[2][CK], aX[2][CK], aY[2][CK], aP[2][4], aTv[2][4];
+        tile_zero(aW);
+        tile_zero(aX);
+        tile_zero(aY);
+        tile_zero(aP);
+        tile_zero(aTv);
+        float zv[2] = {0.f, 0.f}, ss = 0.f;
+        for (int jc = 0; jc < DV; jc += kDvc) {
+            __syncthreads();
+            ld_ws<kC, kDvc, kLoThreads>(sdU, L::LD, ws.dU + wi * D::dU + jc, DV, tid);
+            ld_ws<kC, kDvc, kLoThreads>(sU, L::LD, ws.U + wi * D::U + jc, DV, tid);
+            ld_in<TT, kC, kDvc, kLoThreads>(sdO, L::LD, dout + (tok0 * Hv + h) * DV + jc, (size_t)Hv * DV, n, tid, vec);
+            ld_in<TT, kC, kDvc, kLoThreads>(sV, L::LD, v + (tok0 * Hv + h) * DV + jc, (size_t)Hv * DV, n, tid, vec);
+            ld_ws<DK, kDvc, kLoThreads>(sS, L::LD, ws.S + wi * D::S + jc, DV, tid);
+            ld_ws<DK, kDvc, kLoThreads>(sLam, L::LD, ws.dS + wi * D::dS + jc, DV, tid);
+            __syncthreads();
+            for (int idx = tid; idx < DK * kDvc; idx += kLoThreads) {
+                const int i = idx / kDvc, j = idx % kDvc;
+                ss = fmaf(sS[i * L::LD + j], sLam[i * L::LD + j], ss);
+            }
+            tile_mm<2, CK, false, true, kDvc>(aW, sdU, L::LD, sS, L::LD, r0, tx);     // dU S^T
+            tile_mm<2, CK, false, true, kDvc>(aX, sdO, L::LD, sS, L::LD, r0, tx);     // dO S^T
+            tile_mm<2, CK, false, true, kDvc>(aY, sU, L::LD, sLam, L::LD, r0, tx);    // U lam^T
+            tile_mm<2, 4, false, true, kDvc>(aP, sdO, L::LD, sU, L::LD, r0, tx);      // dO U^T
+            tile_mm<2, 4, false, true, kDvc>(aTv, sdU, L::LD, sV, L::LD, r0, tx);     // dU V^T
+            {   // dV = diag(beta) T^T dU;  dbeta += rowsum(T^T dU o V)
+                float z[2][2];
+                tile_zero(z);
+                tile_mm<2, 2, true, false, kC>(z, sT, kLC, sdU, L::LD, r0, tx);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = r0 + i;
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const int j = tx + 16 * m;
+                        zv[i] = fmaf(z[i][m], sV[r * L::LD + j], zv[i]);
+                        if (r < n) grad_v[((tok0 + r) * Hv + h) * DV + jc + j] = sBeta[r] * z[i][m];
+                    }
+                }
+            }
+        }
+        {   // gamma_C <lam, S>: warp sums of ss (added below)
+            float x = ss;
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+            if ((tid & 31) == 0) sRed[tid / 32] = x;
+        }
+        add_rows(zv, sRow, sdB, tid, tx, ty);   // its barriers also end the dv passes
+        // dW = -dU S^T to shared memory (over the dv pass buffers)
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int m = 0; m < CK; ++m) sDW[(r0 + i) * L::LK + tx + 16 * m] = -aW[i][m];
+        // dQ = scale diag(gamma) (dO S^T);  dG_r += scale gamma_r (dO S^T)_r . q_r
+        // dK = diag(gamma_C / gamma) (U lam^T);  with h_r = (gamma_C / gamma_r) (U lam^T)_r . k_r:
+        // dG_r -= h_r and dG_{C-1} += sum_r h_r + gamma_C <lam, S>
+        float dQ[2][CK], dK[2][CK];
+        {
+            float xr[2], hr[2];
+            const float GC = sG[kC - 1];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int r = r0 + i;
+                const float gr = scale * __expf(sG[r]), kc = __expf(GC - sG[r]);
+                float a = 0.f, b = 0.f;
+#pragma unroll
+                for (int m = 0; m < CK; ++m) {
+                    const int c = tx + 16 * m;
+                    a = fmaf(aX[i][m], sQ[r * L::LK + c], a);
+                    b = fmaf(aY[i][m], sK[r * L::LK + c], b);
+                    dQ[i][m] = gr * aX[i][m];
+                    dK[i][m] = kc * aY[i][m];
+                }
+                xr[i] = gr * a;
+                hr[i] = -kc * b;
+            }
+            add_rows(xr, sRow, sdG, tid, tx, ty);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float s = sum16(hr[i]);
+                if (tx == 0) sH[r0 + i] = s;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                float tot = 0.f, lam_s = 0.f;
+                for (int r = 0; r < kC; ++r) tot += sH[r];
+                for (int w = 0; w < kLoThreads / 32; ++w) lam_s += sRed[w];
+                sdG[kC - 1] += __expf(GC) * lam_s - tot;
+            }
+            __syncthreads();
+            if (tid < kC) sdG[tid] += sH[tid];
+        }
+        {   // E = scale D o dP (s <= r) -> sX;  dG from E o QK^T
+            float F[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int r = r0 + i, s = tx + 16 * m;
+                    const float e = s <= r ? scale * __expf(sG[r] - sG[s]) * aP[i][m] : 0.f;
+                    sX[r * kLC + s] = e;
+                    F[i][m] = e * sQK[r * kLC + s];
+                }
+            add_rows_minus_cols(F, sRow, sCol, sdG, tid, tx, ty);   // its barriers publish sX
+        }
+        tile_mm<2, CK, false, false, kC>(dQ, sX, kLC, sK, L::LK, r0, tx);   // dQ += E K
+        tile_mm<2, CK, true, false, kC>(dK, sX, kLC, sQ, L::LK, r0, tx);    // dK += E^T Q
+        {   // R = T^T dW;  dK += diag(beta gamma) R;  dbeta_s += gamma_s R_s.k_s;  dG_s += beta_s gamma_s R_s.k_s
+            float R[2][CK];
+            tile_zero(R);
+            tile_mm<2, CK, true, false, kC>(R, sT, kLC, sDW, L::LK, r0, tx);
+            float rb[2], rg[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int s = r0 + i;
+                const float gm = __expf(sG[s]), bg = sBeta[s] * gm;
+                float a = 0.f;
+#pragma unroll
+                for (int m = 0; m < CK; ++m) {
+                    a = fmaf(R[i][m], sK[s * L::LK + tx + 16 * m], a);
+                    dK[i][m] = fmaf(bg, R[i][m], dK[i][m]);
+                }
+                rb[i] = gm * a;
+                rg[i] = bg * a;
+            }
+            add_rows(rb, sRow, sdB, tid, tx, ty);   // its barriers also end every read of E in sX
+            add_rows(rg, sRow, sdG, tid, tx, ty);
+        }
+        {   // dT = (dU V^T + dW K^T diag(gamma)) diag(beta), lower part -> sX
+            float Tk[2][4];
+            tile_zero(Tk);
+            tile_mm<2, 4, false, true, DK>(Tk, sDW, L::LK, sK, L::LK, r0, tx);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int r = r0 + i, s = tx + 16 * m;
+                    sX[r * kLC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]), Tk[i][m], aTv[i][m]) : 0.f;
+                }
+        }
+        __syncthreads();
+        {   // M1 = T^T dT -> sX
+            float M1[2][4];
+            tile_zero(M1);
+            tile_mm<2, 4, true, false, kC>(M1, sT, kLC, sX, kLC, r0, tx);
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) sX[(r0 + i) * kLC + tx + 16 * m] = M1[i][m];
+        }
+        __syncthreads();
+        {   // dM = -(M1 T^T) strictly lower;  dbeta_r += sum_s dM_rs A_rs;  H = diag(beta) D o dM -> sX
+            float Mm[2][4];
+            tile_zero(Mm);
+            tile_mm<2, 4, false, true, kC>(Mm, sX, kLC, sT, kLC, r0, tx);
+            float F[2][4], rb[2] = {0.f, 0.f};
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int r = r0 + i, s = tx + 16 * m;
+                    float hv = 0.f, f = 0.f;
+                    if (s < r) {
+                        const float d = __expf(sG[r] - sG[s]), kk = sKK[r * kLC + s], dm = -Mm[i][m];
+                        rb[i] = fmaf(dm, d * kk, rb[i]);
+                        hv = sBeta[r] * d * dm;
+                        f = hv * kk;
+                    }
+                    sX[r * kLC + s] = hv;
+                    F[i][m] = f;
+                }
+            add_rows(rb, sRow, sdB, tid, tx, ty);
+            add_rows_minus_cols(F, sRow, sCol, sdG, tid, tx, ty);
+        }
+        tile_mm<2, CK, false, false, kC>(dK, sX, kLC, sK, L::LK, r0, tx);   // dK += H K
+        tile_mm<2, CK, true, false, kC>(dK, sX, kLC, sK, L::LK, r0, tx);    // dK += H^T K
+        // dg = reverse cumulative sum of dG;  dbeta
+        if (tid == 0) {
+            float acc = 0.f;
+            for (int r = kC - 1; r >= 0; --r) {
+                acc += sdG[r];
+                sRow[r] = acc;
+            }
+        }
+        __syncthreads();
+        if (tid < n) {
+            grad_g[(tok0 + tid) * Hv + h] = sRow[tid];
+            grad_beta[(tok0 + tid) * Hv + h] = sdB[tid];
+        }
+        // dq, dk of the query/key head: its first value head writes, the others add (same thread, same element)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = r0 + i;
+            if (r < n) {
+#pragma unroll
+                for (int m = 0; m < CK; ++m) {
+                    const size_t o = ((tok0 + r) * Hqk + hk) * DK + tx + 16 * m;
+                    grad_q[o] = jh == 0 ? dQ[i][m] : grad_q[o] + dQ[i][m];
+                    grad_k[o] = jh == 0 ? dK[i][m] : grad_k[o] + dK[i][m];
+                }
+            }
+        }
+        __syncthreads();
     }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-template <typename T, int DK>
-cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& L) {
-    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-    float* ckpt = reinterpret_cast<float*>(ws + L.ckpt_off);
-    float* scratch = reinterpret_cast<float*>(ws + L.scratch_off);
-    float* part = reinterpret_cast<float*>(ws + L.part_off);
-    const int nsl = a.dv / kW;
-    bwd_kernel<T, DK><<<(unsigned)(a.num_seqs * a.Hv * nsl), kThreads, 0, a.stream>>>(
-        static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
-        static_cast<const T*>(a.g), static_cast<const T*>(a.beta), a.S0, static_cast<const T*>(a.dout),
-        a.dS_final, part, a.grad_v, a.grad_S0, ckpt, scratch, a.T, a.Hqk, a.Hv, a.dv, a.cu_seqlens, a.num_seqs,
-        a.scale);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const long long ttot = a.cu_seqlens ? (long long)a.T : (long long)a.B * a.T;
-    if (ttot > 0) {
-        bwd_reduce_kernel<DK><<<(unsigned)ttot, 256, 0, a.stream>>>(part, a.grad_q, a.grad_k, a.grad_g, a.grad_beta,
-                                                                     a.Hqk, a.Hv, nsl);
-        e = cudaGetLastError();
+template <typename F>
+cudaError_t set_smem(F* kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <typename TT, int DK, int DV>
+cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
+    uint8_t* base = static_cast<uint8_t*>(a.workspace);
+    Ws ws;
+    ws.T = reinterpret_cast<float*>(base + Lw.T_off);
+    ws.P = reinterpret_cast<float*>(base + Lw.P_off);
+    ws.W = reinterpret_cast<float*>(base + Lw.W_off);
+    ws.U = reinterpret_cast<float*>(base + Lw.U_off);
+    ws.G = reinterpret_cast<float*>(base + Lw.G_off);
+    ws.S = reinterpret_cast<float*>(base + Lw.S_off);
+    ws.dS = reinterpret_cast<float*>(base + Lw.dS_off);
+    ws.dU = reinterpret_cast<float*>(base + Lw.dU_off);
+    const TT* q = static_cast<const TT*>(a.q);
+    const TT* k = static_cast<const TT*>(a.k);
+    const TT* v = static_cast<const TT*>(a.v);
+    const TT* g = static_cast<const TT*>(a.g);
+    const TT* beta = static_cast<const TT*>(a.beta);
+    const TT* dout = static_cast<const TT*>(a.dout);
+    constexpr int NSL = DV / slice_width<DV>();
+    cudaError_t e;
+    // 16-byte vector loads of the inputs need 16-byte aligned bases (row strides are multiples of 16 bytes)
+    const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool vec = al16(a.q) && al16(a.k) && al16(a.v) && al16(a.dout);
+
+    using S1 = WySmem<DK, DV>;
+    using S2 = StSmem<DK, DV>;
+    using S4 = LoSmem<DK, DV>;
+    const dim3 chunk_grid((unsigned)Lw.slots, (unsigned)a.Hqk);
+    const unsigned nst = (unsigned)((long long)a.num_seqs * a.Hv * NSL);
+    if ((e = set_smem(bwd_wy_kernel<TT, DK, DV>, S1::BYTES)) != cudaSuccess) return e;
+    if ((e = set_smem(bwd_state_fwd_kernel<TT, DK, DV>, S2::BYTES)) != cudaSuccess) return e;
+    if ((e = set_smem(bwd_state_adj_kernel<TT, DK, DV>, S2::BYTES)) != cudaSuccess) return e;
+    if ((e = set_smem(bwd_local_kernel<TT, DK, DV>, S4::BYTES)) != cudaSuccess) return e;
+
+    bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
+        q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(k, a.S0, ws, a.T, a.Hqk, a.Hv,
+                                                                              a.cu_seqlens, a.num_seqs, vec);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_state_adj_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
+        q, k, dout, a.dS_final, a.grad_S0, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_local_kernel<TT, DK, DV><<<chunk_grid, kLoThreads, S4::BYTES, a.stream>>>(
+        q, k, v, beta, dout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk, a.Hv,
+        a.cu_seqlens, a.num_seqs, a.scale, vec);
+    return cudaGetLastError();
+}
+
+template <typename TT, int DK>
+cudaError_t launch_dk(const BackwardArgs& a, const BwdLayout& L) {
+    switch (a.dv) {
+        case 32: return launch_typed<TT, DK, 32>(a, L);
+        case 64: return launch_typed<TT, DK, 64>(a, L);
+        case 128: return launch_typed<TT, DK, 128>(a, L);
     }
-    return e;
+    return cudaErrorInvalidValue;
+}
+
+template <typename TT>
+cudaError_t launch_dtype(const BackwardArgs& a, const BwdLayout& L) {
+    switch (a.dk) {
+        case 32: return launch_dk<TT, 32>(a, L);
+        case 64: return launch_dk<TT, 64>(a, L);
+        case 128: return launch_dk<TT, 128>(a, L);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed) {
     const long long ttot = packed ? (long long)T : (long long)B * T;
-    const int nsl = dv / kW;
-    const size_t slice = (size_t)dk * kW * sizeof(float);
-    const long long slots = (ttot + kCk - 1) / kCk + nseq;
     BwdLayout L{};
-    L.ckpt_off = 0;
-    L.scratch_off = align256(L.ckpt_off + (size_t)slots * Hv * nsl * slice);
-    L.part_off = align256(L.scratch_off + (size_t)nseq * Hv * nsl * kCk * slice);
-    L.total = align256(L.part_off + (size_t)ttot * Hv * nsl * (2 * dk + 2) * sizeof(float));
+    L.slots = (ttot + kC - 1) / kC + nseq;
+    const size_t per = (size_t)L.slots * Hv * sizeof(float);
+    size_t off = 0;
+    const auto take = [&](size_t& field, size_t floats) {
+        field = off;
+        off = align256(off + per * floats);
+    };
+    take(L.T_off, (size_t)kC * kC);
+    take(L.P_off, (size_t)kC * kC);
+    take(L.W_off, (size_t)kC * dk);
+    take(L.U_off, (size_t)kC * dv);
+    take(L.G_off, (size_t)kC);
+    take(L.S_off, (size_t)dk * dv);
+    take(L.dS_off, (size_t)dk * dv);
+    take(L.dU_off, (size_t)kC * dv);
+    L.total = off;
     return L;
 }
 
 cudaError_t launch_backward(const BackwardArgs& a) {
     const BwdLayout L = backward_layout(a.B, a.T, a.Hv, a.dk, a.dv, a.num_seqs, a.cu_seqlens != nullptr);
-    const bool bf = a.dtype == GDN_BF16;
-    switch (a.dk) {
-        case 32: return bf ? launch_typed<__nv_bfloat16, 32>(a, L) : launch_typed<float, 32>(a, L);
-        case 64: return bf ? launch_typed<__nv_bfloat16, 64>(a, L) : launch_typed<float, 64>(a, L);
-        case 128: return bf ? launch_typed<__nv_bfloat16, 128>(a, L) : launch_typed<float, 128>(a, L);
-    }
-    return cudaErrorInvalidValue;
+    return a.dtype == GDN_BF16 ? launch_dtype<__nv_bfloat16>(a, L) : launch_dtype<float>(a, L);
 }
 
 }  // namespace gdn

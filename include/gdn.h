@@ -213,10 +213,12 @@ gdn_status_t gdn_causal_conv1d_step(const void* x, long long x_stride, const flo
  *   grad_v         [B, T, Hv, dv] float;  grad_g, grad_beta [B, T, Hv] float
  *   grad_S0        [nseq, Hv, dk, dv] float, or NULL (not written)
  * Gradients are always fp32.  Pointers need only element alignment.  opts->flags must be 0 (the
- * fused front end and output gate have no backward here).  The workspace (256-byte aligned,
- * gdn_recurrent_bwd_workspace_size bytes) holds state checkpoints every 16 tokens, a chunk scratch
- * per (sequence, head, 32-column slice) and per-slice partial sums; GDN_ERR_WORKSPACE if missing or
- * too small.  Asynchronous on opts->stream; events[0] before and events[1] after the two kernels.
+ * fused front end and output gate have no backward here).  It is computed through the chunked form
+ * of the loop (64-token chunks): the workspace (256-byte aligned, gdn_recurrent_bwd_workspace_size
+ * bytes) holds per (chunk, value head) the chunk's UT inverse, decay-masked Q K^T, W, U, decay
+ * prefix sums, the state at the chunk start and its adjoint, and dU, all fp32; GDN_ERR_WORKSPACE if
+ * missing or too small.  Asynchronous on opts->stream; events[0] before and events[1] after the
+ * four kernels.
  */
 size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts);
 gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
