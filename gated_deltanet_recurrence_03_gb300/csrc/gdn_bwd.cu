@@ -70,6 +70,61 @@ __device__ __forceinline__ float sum16(float x) {
     return x;
 }
 
+// ---------------------------------------------------------------- tensor-core products in fp32 accuracy
+// mma.sync m16n8k8 with tf32 operands; each fp32 operand is split as x = hi + lo (hi = x rounded to
+// tf32, lo = the remainder rounded to tf32) and a b ~ hi_a hi_b + hi_a lo_b + lo_a hi_b, whose
+// dropped lo_a lo_b term is about 2^-22 of the product.  Fragment coordinates (g = lane / 4,
+// t = lane % 4): A (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4); B (k = t, n = g), (k = t + 4, n = g);
+// accumulator (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                           const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+    mma_tf32(d, al, bh);
+    mma_tf32(d, ah, bl);
+    mma_tf32(d, ah, bh);
+}
+// A fragment: rows row0 + g (+ 8), columns k0 + t (+ 4) of a row-major fp32 matrix.
+__device__ __forceinline__ void frag_a(const float* A, int ld, int row0, int k0, int g, int t, uint32_t (&hi)[4],
+                                       uint32_t (&lo)[4]) {
+    split_tf32(A[(row0 + g) * ld + k0 + t], hi[0], lo[0]);
+    split_tf32(A[(row0 + g + 8) * ld + k0 + t], hi[1], lo[1]);
+    split_tf32(A[(row0 + g) * ld + k0 + t + 4], hi[2], lo[2]);
+    split_tf32(A[(row0 + g + 8) * ld + k0 + t + 4], hi[3], lo[3]);
+}
+// B fragment of B = X^T (B[k][n] = X[n][k], X row-major): n = n0 + g, k = k0 + t (+ 4).
+__device__ __forceinline__ void frag_bt(const float* X, int ld, int n0, int k0, int g, int t, uint32_t (&hi)[2],
+                                        uint32_t (&lo)[2]) {
+    split_tf32(X[(n0 + g) * ld + k0 + t], hi[0], lo[0]);
+    split_tf32(X[(n0 + g) * ld + k0 + t + 4], hi[1], lo[1]);
+}
+// sign * (N accumulator fragments of rows row0 .. row0 + 15, n-tiles nb0 .. nb0 + N - 1) to D.
+template <int N>
+__device__ __forceinline__ void store_frag(float* D, int ld, const float (&f)[N][4], int row0, int nb0, int g, int t,
+                                           float sign) {
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+        const int c = 8 * (nb0 + q) + 2 * t;
+        D[(row0 + g) * ld + c] = sign * f[q][0];
+        D[(row0 + g) * ld + c + 1] = sign * f[q][1];
+        D[(row0 + g + 8) * ld + c] = sign * f[q][2];
+        D[(row0 + g + 8) * ld + c + 1] = sign * f[q][3];
+    }
+}
+
 // 16 bytes of fp32 or bf16 values as fp32 (bf16 -> fp32 is a 16-bit shift).
 __device__ __forceinline__ void unpack16(const uint4& u, float (&f)[4]) {
     f[0] = __uint_as_float(u.x);
@@ -157,7 +212,7 @@ __device__ __forceinline__ bool slot_chunk(const int32_t* cu, int nseq, int T, l
 
 // Per-(slot, value head) workspace arrays.
 struct Ws {
-    float *T, *P, *W, *U, *G, *S, *dS, *dU;
+    float *T, *P, *W, *Wt, *U, *G, *S, *dS, *dU;   // Wt = W^T [dk][C]
 };
 
 template <int DK, int DV>
@@ -167,13 +222,13 @@ struct WsDims {
 };
 
 // ---------------------------------------------------------------- kernel 1: WY factors per chunk
-constexpr int kWyThreads = 256;   // = 4 threads per column of T in the solve
+constexpr int kWyThreads = 256;
 
 template <int DK, int DV>
 struct WySmem {
     static constexpr int LK = DK + 1, LQV = (DK > DV ? DK : DV) + 1;
     static constexpr int K_ = 0, QV_ = K_ + kC * LK, KK_ = QV_ + kC * LQV, QK_ = KK_ + kC * kLC,
-                         L_ = QK_ + kC * kLC, T_ = L_ + kC * kLC, VEC_ = T_ + kC * kLC;
+                         L_ = QK_ + kC * kLC, T_ = L_ + kC * kLC, Y_ = T_ + kC * kLC, VEC_ = Y_ + 3 * 256;
     static constexpr int FLOATS = VEC_ + 4 * kC;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
 };
@@ -185,14 +240,14 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
               int nseq, float scale, bool vec) {
     using L = WySmem<DK, DV>;
     using D = WsDims<DK, DV>;
-    static_assert(kWyThreads == 4 * kC, "the solve takes four threads per column");
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     float* sK = sm + L::K_;
     float* sQV = sm + L::QV_;
     float* sKK = sm + L::KK_;
     float* sQK = sm + L::QK_;
     float* sL = sm + L::L_;
     float* sT = sm + L::T_;
+    float* sY = sm + L::Y_;   // off-diagonal block sums of the solve: up to 3 blocks of 16 x 16
     float* sG = sm + L::VEC_;
     float* sBeta = sG + kC;
     float* sBG = sBeta + kC;
@@ -235,12 +290,16 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
         // V of this value head (Q is no longer needed: its Gram is in sQK)
         ld_in<TT, kC, DV, kWyThreads>(sQV, L::LQV, v + (tok0 * Hv + h) * DV, (size_t)Hv * DV, n, tid, vec);
         __syncthreads();
-        if (tid == 0) {
-            float acc = 0.f;
-            for (int r = 0; r < kC; ++r) {
-                acc += sGraw[r];
-                sG[r] = acc;
+        if (tid < 32) {   // G = inclusive prefix sum of g: lane l holds tokens 2l, 2l + 1
+            const float a = sGraw[2 * tid], b = sGraw[2 * tid + 1];
+            float x = a + b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (tid >= o) x += y;
             }
+            sG[2 * tid] = x - b;
+            sG[2 * tid + 1] = x;
         }
         __syncthreads();
         if (tid < kC) {
@@ -255,19 +314,51 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
             sL[r * kLC + s] = s < r ? sBeta[r] * d * sKK[r * kLC + s] : 0.f;
         }
         __syncthreads();
-        {   // T = (I + L)^{-1} by forward substitution, four threads per column:
-            // T[r][col] = [r == col] - sum_{s<r} L[r][s] T[s][col]   (T[s][col] = 0 for s < col)
-            const int col = tid / 4, part = tid % 4;
-            for (int r = 0; r < kC; ++r) {
-                float x = 0.f;
-                for (int s = part; s < r; s += 4) x = fmaf(sL[r * kLC + s], sT[s * kLC + col], x);
-                x += __shfl_xor_sync(0xffffffffu, x, 1);
-                x += __shfl_xor_sync(0xffffffffu, x, 2);
-                if (part == 0) sT[r * kLC + col] = r < col ? 0.f : (r == col ? 1.f : -x);
-                __syncwarp();
+        {   // T = (I + L)^{-1} in 16 x 16 blocks: each diagonal block by forward substitution (one thread
+            // per column), then block row i below the diagonal from (I + L) T = I:
+            //     T_ij = -T_ii sum_{l=j}^{i-1} L_il T_lj,   for i - j = 1, 2, 3 in turn.
+            if (tid < kC) {
+                const int o = 16 * (tid / 16), c = tid % 16;
+                float x[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float acc = r == c ? 1.f : 0.f;
+#pragma unroll
+                    for (int q = 0; q < r; ++q) acc = fmaf(-sL[(o + r) * kLC + o + q], x[q], acc);
+                    x[r] = acc;
+                    sT[(o + r) * kLC + o + c] = acc;
+                }
+            } else {   // blocks above the diagonal are zero
+                for (int idx = tid - kC; idx < 6 * 256; idx += kWyThreads - kC) {
+                    const int blk = idx / 256, e = idx % 256;
+                    const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2), bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    sT[(16 * bi + e / 16) * kLC + 16 * bj + e % 16] = 0.f;
+                }
+            }
+            __syncthreads();
+            for (int d = 1; d < 4; ++d) {
+                const int nb = 4 - d;
+                for (int idx = tid; idx < nb * 256; idx += kWyThreads) {
+                    const int bj = idx / 256, e = idx % 256, r = e / 16, c = e % 16, bi = bj + d;
+                    float acc = 0.f;
+                    for (int bl = bj; bl < bi; ++bl)
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            acc = fmaf(sL[(16 * bi + r) * kLC + 16 * bl + q], sT[(16 * bl + q) * kLC + 16 * bj + c], acc);
+                    sY[idx] = acc;
+                }
+                __syncthreads();
+                for (int idx = tid; idx < nb * 256; idx += kWyThreads) {
+                    const int bj = idx / 256, e = idx % 256, r = e / 16, c = e % 16, bi = bj + d;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        acc = fmaf(sT[(16 * bi + r) * kLC + 16 * bi + q], sY[bj * 256 + q * 16 + c], acc);
+                    sT[(16 * bi + r) * kLC + 16 * bj + c] = -acc;
+                }
+                __syncthreads();
             }
         }
-        __syncthreads();
         for (int idx = tid; idx < kC * kC; idx += kWyThreads) ws.T[wi * D::T + idx] = sT[(idx / kC) * kLC + idx % kC];
         {   // W = T diag(beta gamma) K
             constexpr int CN = DK / 16;
@@ -277,7 +368,10 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int m = 0; m < CN; ++m) ws.W[wi * D::W + (size_t)(ty * 4 + i) * DK + tx + 16 * m] = acc[i][m];
+                for (int m = 0; m < CN; ++m) {
+                    ws.W[wi * D::W + (size_t)(ty * 4 + i) * DK + tx + 16 * m] = acc[i][m];
+                    ws.Wt[wi * D::W + (size_t)(tx + 16 * m) * kC + ty * 4 + i] = acc[i][m];
+                }
         }
         {   // U~ = T diag(beta) V
             constexpr int CN = DV / 16;
@@ -299,14 +393,99 @@ constexpr int kStThreads = 256;
 template <int DV>
 constexpr int slice_width() { return DV < 64 ? DV : 64; }
 
+// N contiguous fp32 from shared memory (16-byte aligned for N >= 4, 8-byte for N = 2).
+template <int N>
+__device__ __forceinline__ void lds_vec(float* dst, const float* p) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int v = 0; v < N / 4; ++v) {
+            const float4 x = *reinterpret_cast<const float4*>(p + 4 * v);
+            dst[4 * v] = x.x;
+            dst[4 * v + 1] = x.y;
+            dst[4 * v + 2] = x.z;
+            dst[4 * v + 3] = x.w;
+        }
+    } else if constexpr (N == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(p);
+        dst[0] = x.x;
+        dst[1] = x.y;
+    } else {
+#pragma unroll
+        for (int v = 0; v < N; ++v) dst[v] = p[v];
+    }
+}
+
+// Outer-product tile: acc[i][e] += sum_{k<K} At[k][row0 + i] (* ks[k]) * B[k][col0 + e], both operands
+// stored k-major (rows 16-byte aligned), so each k costs one vector load of RM values (shared by the
+// 16 threads of a row group) and one of CN values.
+template <int RM, int CN, int K, bool KS = false>
+__device__ __forceinline__ void tile_tn(float (&acc)[RM][CN], const float* __restrict__ At, int lda,
+                                        const float* __restrict__ B, int ldb, int row0, int col0,
+                                        const float* __restrict__ ks = nullptr) {
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float a[RM], b[CN];
+        lds_vec<RM>(a, At + k * lda + row0);
+        lds_vec<CN>(b, B + k * ldb + col0);
+        if (KS) {
+            const float s = ks[k];
+#pragma unroll
+            for (int i = 0; i < RM; ++i) a[i] *= s;
+        }
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
+#pragma unroll
+            for (int e = 0; e < CN; ++e) acc[i][e] = fmaf(a[i], b[e], acc[i][e]);
+    }
+}
+
+// Rows [0, ROWS) x columns [0, WIDTH) of an element-type block (rows >= n zero) into shared memory
+// TRANSPOSED: dst[c * ld + r].  Consecutive threads take consecutive rows, so the stores are
+// conflict-free.
+template <typename TT, int ROWS, int WIDTH, int NT>
+__device__ __forceinline__ void ld_in_t(float* __restrict__ dst, int ld, const TT* __restrict__ src, size_t stride,
+                                        int n, int tid, bool vec) {
+    constexpr int EPV = 16 / (int)sizeof(TT), V = WIDTH / EPV, TOTAL = ROWS * V, PER = (TOTAL + NT - 1) / NT;
+    if (vec) {
+        uint4 b[PER];
+#pragma unroll
+        for (int p = 0; p < PER; ++p) {
+            const int idx = tid + p * NT, r = idx % ROWS;
+            b[p] = make_uint4(0u, 0u, 0u, 0u);
+            if ((TOTAL % NT == 0 || idx < TOTAL) && r < n)
+                b[p] = *reinterpret_cast<const uint4*>(src + (size_t)r * stride + (idx / ROWS) * EPV);
+        }
+#pragma unroll
+        for (int p = 0; p < PER; ++p) {
+            const int idx = tid + p * NT;
+            if (TOTAL % NT == 0 || idx < TOTAL) {
+                float f[EPV];
+                unpack16(b[p], f);
+                const int r = idx % ROWS, c0 = (idx / ROWS) * EPV;
+#pragma unroll
+                for (int x = 0; x < EPV; ++x) dst[(c0 + x) * ld + r] = f[x];
+            }
+        }
+    } else {
+        for (int idx = tid; idx < ROWS * WIDTH; idx += NT) {
+            const int r = idx % ROWS, c = idx / ROWS;
+            dst[c * ld + r] = r < n ? to_f32(src[(size_t)r * stride + c]) : 0.f;
+        }
+    }
+}
+
 template <int DK, int DV>
 struct StSmem {
-    static constexpr int SW = slice_width<DV>(), LK = DK + 1, LS = SW + 1;
-    // forward: W, K, U slice, S slice.  adjoint: W, K, Q, P, dO slice, dU slice, lam slice
-    static constexpr int W_ = 0, K_ = W_ + kC * LK, Q_ = K_ + kC * LK, P_ = Q_ + kC * LK, X_ = P_ + kC * kLC,
+    // leading dimensions: width + 4 (rows 16-byte aligned, and rows 4 banks apart)
+    static constexpr int SW = slice_width<DV>(), LK = DK + 4, LCC = kC + 4, LS = SW + 4;
+    // forward: W^T [DK][C], K [C][DK], U slice [C][SW], S slice [DK][SW]
+    // adjoint: K^T [DK][C], W [C][DK], Q [C][DK], P [C][C], dO and dU slices [C][SW], lam slice [DK][SW]
+    static constexpr int At_ = 0, B_ = At_ + DK * LCC, Q_ = B_ + kC * LK, P_ = Q_ + kC * LK, X_ = P_ + kC * LCC,
                          Y_ = X_ + kC * LS, S_ = Y_ + kC * LS, G_ = S_ + DK * LS, R_ = G_ + kC;
     static constexpr int FLOATS = R_ + kC;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
+    static_assert(B_ % 4 == 0 && Q_ % 4 == 0 && P_ % 4 == 0 && X_ % 4 == 0 && Y_ % 4 == 0 && S_ % 4 == 0,
+                  "16-byte aligned regions");
 };
 
 // Chunk-start states S (to the workspace) and U = U~ - W S (over U~ in the workspace).
@@ -317,16 +496,17 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws 
     using L = StSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int SW = L::SW, NSL = DV / SW;
-    extern __shared__ float sm[];
-    float* sW = sm + L::W_;
-    float* sK = sm + L::K_;
+    constexpr int RU = kC / 16, RS = DK / 16, CV = SW / 16;   // tiles: U C x SW, S DK x SW (CV columns)
+    extern __shared__ __align__(16) float sm[];
+    float* sWt = sm + L::At_;
+    float* sK = sm + L::B_;
     float* sU = sm + L::X_;
     float* sS = sm + L::S_;
     float* sG = sm + L::G_;
     const int sl = blockIdx.x % NSL, h = (blockIdx.x / NSL) % Hv, seq = blockIdx.x / (NSL * Hv);
     if (seq >= nseq) return;
     const int hk = h / (Hv / Hqk), col0 = sl * SW;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16, cc = CV * tx;
     long long t0, t1;
     seq_range(cu, seq, T_len, t0, t1);
     const long long nch = (t1 - t0 + kC - 1) / kC, slot0 = t0 / kC + seq;
@@ -335,14 +515,12 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws 
         const int i = idx / SW, j = idx % SW;
         sS[i * L::LS + j] = S0 ? S0[sbase + (size_t)i * DV + j] : 0.f;
     }
-    constexpr int RU = kC / 16, CU = SW / 16;   // U tile: C x SW
-    constexpr int RS = DK / 16;                 // S tile: DK x SW
     for (long long c = 0; c < nch; ++c) {
         const size_t wi = (size_t)(slot0 + c) * Hv + h;
         const long long tok0 = t0 + c * kC;
         const int n = (int)min((long long)kC, t1 - tok0);
         if (tid < kC) sG[tid] = ws.G[wi * D::G + tid];
-        ld_ws<kC, DK, kStThreads>(sW, L::LK, ws.W + wi * D::W, DK, tid);
+        ld_ws<DK, kC, kStThreads>(sWt, L::LCC, ws.Wt + wi * D::W, kC, tid);
         ld_ws<kC, SW, kStThreads>(sU, L::LS, ws.U + wi * D::U + col0, DV, tid);
         ld_in<TT, kC, DK, kStThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
         __syncthreads();
@@ -351,34 +529,33 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws 
             ws.S[wi * D::S + (size_t)i * DV + col0 + j] = sS[i * L::LS + j];
         }
         {   // U = U~ - W S to the workspace; sU holds diag(gamma_C / gamma) U (each thread its own elements)
-            float acc[RU][CU];
+            float acc[RU][CV];
             tile_zero(acc);
-            tile_mm<RU, CU, false, false, DK>(acc, sW, L::LK, sS, L::LS, ty * RU, tx);
+            tile_tn<RU, CV, DK>(acc, sWt, L::LCC, sS, L::LS, ty * RU, cc);
 #pragma unroll
             for (int i = 0; i < RU; ++i) {
                 const int r = ty * RU + i;
                 const float kc = __expf(sG[kC - 1] - sG[r]);
 #pragma unroll
-                for (int m = 0; m < CU; ++m) {
-                    const int j = tx + 16 * m;
-                    const float u = sU[r * L::LS + j] - acc[i][m];
-                    sU[r * L::LS + j] = kc * u;
-                    ws.U[wi * D::U + (size_t)r * DV + col0 + j] = u;
+                for (int e = 0; e < CV; ++e) {
+                    const float u = sU[r * L::LS + cc + e] - acc[i][e];
+                    sU[r * L::LS + cc + e] = kc * u;
+                    ws.U[wi * D::U + (size_t)r * DV + col0 + cc + e] = u;
                 }
             }
         }
         __syncthreads();
         {   // S <- gamma_C S + K^T diag(gamma_C / gamma) U
-            float acc[RS][CU];
+            float acc[RS][CV];
             tile_zero(acc);
-            tile_mm<RS, CU, true, false, kC>(acc, sK, L::LK, sU, L::LS, ty * RS, tx);
+            tile_tn<RS, CV, kC>(acc, sK, L::LK, sU, L::LS, ty * RS, cc);
             const float gC = __expf(sG[kC - 1]);
 #pragma unroll
             for (int i = 0; i < RS; ++i)
 #pragma unroll
-                for (int m = 0; m < CU; ++m) {
-                    float& s = sS[(ty * RS + i) * L::LS + tx + 16 * m];
-                    s = fmaf(gC, s, acc[i][m]);
+                for (int e = 0; e < CV; ++e) {
+                    float& s = sS[(ty * RS + i) * L::LS + cc + e];
+                    s = fmaf(gC, s, acc[i][e]);
                 }
         }
         __syncthreads();
@@ -394,9 +571,10 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
     using L = StSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int SW = L::SW, NSL = DV / SW;
-    extern __shared__ float sm[];
-    float* sW = sm + L::W_;
-    float* sK = sm + L::K_;
+    constexpr int RU = kC / 16, RS = DK / 16, CV = SW / 16;
+    extern __shared__ __align__(16) float sm[];
+    float* sKt = sm + L::At_;
+    float* sW = sm + L::B_;
     float* sQ = sm + L::Q_;
     float* sP = sm + L::P_;
     float* sdO = sm + L::X_;
@@ -407,7 +585,7 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
     const int sl = blockIdx.x % NSL, h = (blockIdx.x / NSL) % Hv, seq = blockIdx.x / (NSL * Hv);
     if (seq >= nseq) return;
     const int hk = h / (Hv / Hqk), col0 = sl * SW;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16, cc = CV * tx;
     long long t0, t1;
     seq_range(cu, seq, T_len, t0, t1);
     const long long nch = (t1 - t0 + kC - 1) / kC, slot0 = t0 / kC + seq;
@@ -416,8 +594,6 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
         const int i = idx / SW, j = idx % SW;
         sLam[i * L::LS + j] = dS_final ? dS_final[sbase + (size_t)i * DV + j] : 0.f;
     }
-    constexpr int RU = kC / 16, CU = SW / 16;
-    constexpr int RS = DK / 16;
     for (long long c = nch - 1; c >= 0; --c) {
         const size_t wi = (size_t)(slot0 + c) * Hv + h;
         const long long tok0 = t0 + c * kC;
@@ -428,8 +604,8 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
             sQs[tid] = scale * __expf(gr);
         }
         ld_ws<kC, DK, kStThreads>(sW, L::LK, ws.W + wi * D::W, DK, tid);
-        ld_ws<kC, kC, kStThreads>(sP, kLC, ws.P + wi * D::P, kC, tid);
-        ld_in<TT, kC, DK, kStThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+        ld_ws<kC, kC, kStThreads>(sP, L::LCC, ws.P + wi * D::P, kC, tid);
+        ld_in_t<TT, kC, DK, kStThreads>(sKt, L::LCC, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
         ld_in<TT, kC, DK, kStThreads>(sQ, L::LK, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
         ld_in<TT, kC, SW, kStThreads>(sdO, L::LS, dout + (tok0 * Hv + h) * DV + col0, (size_t)Hv * DV, n, tid, vec);
         __syncthreads();
@@ -438,38 +614,37 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
             ws.dS[wi * D::dS + (size_t)i * DV + col0 + j] = sLam[i * L::LS + j];
         }
         {   // dU = diag(gamma_C / gamma) K lam + P^T dO
-            float kl[RU][CU], acc[RU][CU];
+            float kl[RU][CV], acc[RU][CV];
             tile_zero(kl);
             tile_zero(acc);
-            tile_mm<RU, CU, false, false, DK>(kl, sK, L::LK, sLam, L::LS, ty * RU, tx);
-            tile_mm<RU, CU, true, false, kC>(acc, sP, kLC, sdO, L::LS, ty * RU, tx);
+            tile_tn<RU, CV, DK>(kl, sKt, L::LCC, sLam, L::LS, ty * RU, cc);
+            tile_tn<RU, CV, kC>(acc, sP, L::LCC, sdO, L::LS, ty * RU, cc);
 #pragma unroll
             for (int i = 0; i < RU; ++i) {
                 const int r = ty * RU + i;
                 const float kc = __expf(sG[kC - 1] - sG[r]);
 #pragma unroll
-                for (int m = 0; m < CU; ++m) {
-                    const int j = tx + 16 * m;
-                    const float du = fmaf(kc, kl[i][m], acc[i][m]);
-                    sdU[r * L::LS + j] = du;
-                    ws.dU[wi * D::dU + (size_t)r * DV + col0 + j] = du;
+                for (int e = 0; e < CV; ++e) {
+                    const float du = fmaf(kc, kl[i][e], acc[i][e]);
+                    sdU[r * L::LS + cc + e] = du;
+                    ws.dU[wi * D::dU + (size_t)r * DV + col0 + cc + e] = du;
                 }
             }
         }
         __syncthreads();
         {   // lam <- gamma_C lam + Q^T diag(scale gamma) dO - W^T dU  (each thread rewrites its own elements)
-            float acc[RS][CU], neg[RS][CU];
+            float acc[RS][CV], neg[RS][CV];
             tile_zero(acc);
             tile_zero(neg);
-            tile_mm<RS, CU, true, false, kC, true>(acc, sQ, L::LK, sdO, L::LS, ty * RS, tx, sQs);
-            tile_mm<RS, CU, true, false, kC>(neg, sW, L::LK, sdU, L::LS, ty * RS, tx);
+            tile_tn<RS, CV, kC, true>(acc, sQ, L::LK, sdO, L::LS, ty * RS, cc, sQs);
+            tile_tn<RS, CV, kC>(neg, sW, L::LK, sdU, L::LS, ty * RS, cc);
             const float gC = __expf(sG[kC - 1]);
 #pragma unroll
             for (int i = 0; i < RS; ++i)
 #pragma unroll
-                for (int m = 0; m < CU; ++m) {
-                    float& l = sLam[(ty * RS + i) * L::LS + tx + 16 * m];
-                    l = fmaf(gC, l, acc[i][m] - neg[i][m]);
+                for (int e = 0; e < CV; ++e) {
+                    float& l = sLam[(ty * RS + i) * L::LS + cc + e];
+                    l = fmaf(gC, l, acc[i][e] - neg[i][e]);
                 }
         }
         __syncthreads();
@@ -489,12 +664,15 @@ constexpr int kDvc = 32;                        // value columns per pass over d
 
 template <int DK, int DV>
 struct LoSmem {
-    static constexpr int LK = DK + 1, LD = kDvc + 1;
+    // LD = 36: rows of the pass buffers are 4 banks apart, so fragment loads (g, t) hit 32 banks
+    static constexpr int LK = DK + 1, LD = kDvc + 4;
     static constexpr int K_ = 0, Q_ = K_ + kC * LK, KK_ = Q_ + kC * LK, QK_ = KK_ + kC * kLC, T_ = QK_ + kC * kLC,
                          X_ = T_ + kC * kLC, DVB_ = X_ + kC * kLC;
-    // dv pass buffers (dU, U, dO, V: C x 32; S, lam: DK x 32); afterwards dW (C x DK) over them
+    // dv pass buffers (dU, U, dO, V: C x 32; S, lam: DK x 32); afterwards dW (C x DK) and one more C x DK
+    // (or C x C) exchange buffer over them
     static constexpr int dU_ = DVB_, U_ = dU_ + kC * LD, dO_ = U_ + kC * LD, V_ = dO_ + kC * LD, S_ = V_ + kC * LD,
-                         Lam_ = S_ + DK * LD, DVB_END = Lam_ + DK * LD, DW_END = DVB_ + kC * LK;
+                         Lam_ = S_ + DK * LD, DVB_END = Lam_ + DK * LD, XY_ = DVB_ + kC * LK,
+                         DW_END = XY_ + (LK > kLC ? kC * LK : kC * kLC);
     static constexpr int VEC_ = DVB_END > DW_END ? DVB_END : DW_END;
     // G, beta, dG, dbeta, row scratch, h, column scratch [row groups][C], warp sums
     static constexpr int G_ = VEC_, Beta_ = G_ + kC, dG_ = Beta_ + kC, dB_ = dG_ + kC, Row_ = dB_ + kC,
@@ -545,7 +723,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     using L = LoSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int CK = DK / 16;   // columns per thread of a C x DK tile (2 rows each)
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float sm[];
     float* sK = sm + L::K_;
     float* sQ = sm + L::Q_;
     float* sKK = sm + L::KK_;
@@ -559,6 +737,8 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     float* sS = sm + L::S_;
     float* sLam = sm + L::Lam_;
     float* sDW = sm + L::DVB_;
+    float* sXY = sm + L::XY_;
+    float* sTv = sm + L::XY_;
     float* sG = sm + L::G_;
     float* sBeta = sm + L::Beta_;
     float* sdG = sm + L::dG_;
@@ -574,6 +754,9 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     long long tok0;
     if (!slot_chunk(cu, nseq, T_len, slot, seq, tok0, n)) return;
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16, r0 = ty * 2;
+    constexpr int NTW = DK / 32;   // value-side n-tiles of 8 per warp (16 warps: 4 row tiles x 4 column groups)
+    const int warp = tid / 32, lane = tid % 32, g = lane / 4, t = lane % 4;
+    const int mt = warp % 4, nb0 = (warp / 4) * NTW, pb0 = (warp / 4) * 2;
 
     ld_in<TT, kC, DK, kLoThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
     ld_in<TT, kC, DK, kLoThreads>(sQ, L::LK, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
@@ -603,12 +786,13 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             sdG[tid] = 0.f;
             sdB[tid] = 0.f;
         }
-        float aW[2][CK], aX[2][CK], aY[2][CK], aP[2][4], aTv[2][4];
-        tile_zero(aW);
-        tile_zero(aX);
-        tile_zero(aY);
-        tile_zero(aP);
-        tile_zero(aTv);
+        // fragment accumulators (warp w: rows 16 mt .. +15; value-side n-tiles of 8 from nb0, C-side from pb0)
+        float fW[NTW][4], fX[NTW][4], fY[NTW][4], fP[2][4], fTv[2][4];
+        tile_zero(fW);
+        tile_zero(fX);
+        tile_zero(fY);
+        tile_zero(fP);
+        tile_zero(fTv);
         float zv[2] = {0.f, 0.f}, ss = 0.f;
         for (int jc = 0; jc < DV; jc += kDvc) {
             __syncthreads();
@@ -623,11 +807,33 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                 const int i = idx / kDvc, j = idx % kDvc;
                 ss = fmaf(sS[i * L::LD + j], sLam[i * L::LD + j], ss);
             }
-            tile_mm<2, CK, false, true, kDvc>(aW, sdU, L::LD, sS, L::LD, r0, tx);     // dU S^T
-            tile_mm<2, CK, false, true, kDvc>(aX, sdO, L::LD, sS, L::LD, r0, tx);     // dO S^T
-            tile_mm<2, CK, false, true, kDvc>(aY, sU, L::LD, sLam, L::LD, r0, tx);    // U lam^T
-            tile_mm<2, 4, false, true, kDvc>(aP, sdO, L::LD, sU, L::LD, r0, tx);      // dO U^T
-            tile_mm<2, 4, false, true, kDvc>(aTv, sdU, L::LD, sV, L::LD, r0, tx);     // dU V^T
+#pragma unroll
+            for (int k0 = 0; k0 < kDvc; k0 += 8) {   // tensor cores: dU S^T, dU V^T, dO S^T, dO U^T, U lam^T
+                uint32_t ah[4], al[4], bh[2], bl[2], sh[NTW][2], sl[NTW][2];
+#pragma unroll
+                for (int q = 0; q < NTW; ++q) frag_bt(sS, L::LD, 8 * (nb0 + q), k0, g, t, sh[q], sl[q]);
+                frag_a(sdU, L::LD, 16 * mt, k0, g, t, ah, al);
+#pragma unroll
+                for (int q = 0; q < NTW; ++q) mma_3xtf32(fW[q], ah, al, sh[q], sl[q]);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    frag_bt(sV, L::LD, 8 * (pb0 + q), k0, g, t, bh, bl);
+                    mma_3xtf32(fTv[q], ah, al, bh, bl);
+                }
+                frag_a(sdO, L::LD, 16 * mt, k0, g, t, ah, al);
+#pragma unroll
+                for (int q = 0; q < NTW; ++q) mma_3xtf32(fX[q], ah, al, sh[q], sl[q]);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    frag_bt(sU, L::LD, 8 * (pb0 + q), k0, g, t, bh, bl);
+                    mma_3xtf32(fP[q], ah, al, bh, bl);
+                }
+#pragma unroll
+                for (int q = 0; q < NTW; ++q) frag_bt(sLam, L::LD, 8 * (nb0 + q), k0, g, t, sh[q], sl[q]);
+                frag_a(sU, L::LD, 16 * mt, k0, g, t, ah, al);
+#pragma unroll
+                for (int q = 0; q < NTW; ++q) mma_3xtf32(fY[q], ah, al, sh[q], sl[q]);
+            }
             {   // dV = diag(beta) T^T dU;  dbeta += rowsum(T^T dU o V)
                 float z[2][2];
                 tile_zero(z);
@@ -651,11 +857,11 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             if ((tid & 31) == 0) sRed[tid / 32] = x;
         }
         add_rows(zv, sRow, sdB, tid, tx, ty);   // its barriers also end the dv passes
-        // dW = -dU S^T to shared memory (over the dv pass buffers)
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int m = 0; m < CK; ++m) sDW[(r0 + i) * L::LK + tx + 16 * m] = -aW[i][m];
+        // The fragment accumulators go through shared memory to the (row group, tx) tiles:
+        // dW = -dU S^T stays there (sDW); dO S^T, then U lam^T, then dU V^T and dO U^T pass through.
+        store_frag<NTW>(sDW, L::LK, fW, 16 * mt, nb0, g, t, -1.f);
+        store_frag<NTW>(sXY, L::LK, fX, 16 * mt, nb0, g, t, 1.f);
+        __syncthreads();
         // dQ = scale diag(gamma) (dO S^T);  dG_r += scale gamma_r (dO S^T)_r . q_r
         // dK = diag(gamma_C / gamma) (U lam^T);  with h_r = (gamma_C / gamma_r) (U lam^T)_r . k_r:
         // dG_r -= h_r and dG_{C-1} += sum_r h_r + gamma_C <lam, S>
@@ -666,31 +872,52 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int r = r0 + i;
-                const float gr = scale * __expf(sG[r]), kc = __expf(GC - sG[r]);
-                float a = 0.f, b = 0.f;
+                const float gr = scale * __expf(sG[r]);
+                float a = 0.f;
 #pragma unroll
                 for (int m = 0; m < CK; ++m) {
                     const int c = tx + 16 * m;
-                    a = fmaf(aX[i][m], sQ[r * L::LK + c], a);
-                    b = fmaf(aY[i][m], sK[r * L::LK + c], b);
-                    dQ[i][m] = gr * aX[i][m];
-                    dK[i][m] = kc * aY[i][m];
+                    const float x = sXY[r * L::LK + c];
+                    a = fmaf(x, sQ[r * L::LK + c], a);
+                    dQ[i][m] = gr * x;
                 }
                 xr[i] = gr * a;
+            }
+            __syncthreads();
+            store_frag<NTW>(sXY, L::LK, fY, 16 * mt, nb0, g, t, 1.f);
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int r = r0 + i;
+                const float kc = __expf(GC - sG[r]);
+                float b = 0.f;
+#pragma unroll
+                for (int m = 0; m < CK; ++m) {
+                    const int c = tx + 16 * m;
+                    const float y = sXY[r * L::LK + c];
+                    b = fmaf(y, sK[r * L::LK + c], b);
+                    dK[i][m] = kc * y;
+                }
                 hr[i] = -kc * b;
             }
-            add_rows(xr, sRow, sdG, tid, tx, ty);
+            __syncthreads();
+            store_frag<2>(sTv, kLC, fTv, 16 * mt, pb0, g, t, 1.f);
+            store_frag<2>(sX, kLC, fP, 16 * mt, pb0, g, t, 1.f);
+            add_rows(xr, sRow, sdG, tid, tx, ty);   // its barriers publish sTv and sX
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const float s = sum16(hr[i]);
                 if (tx == 0) sH[r0 + i] = s;
             }
             __syncthreads();
-            if (tid == 0) {
-                float tot = 0.f, lam_s = 0.f;
-                for (int r = 0; r < kC; ++r) tot += sH[r];
-                for (int w = 0; w < kLoThreads / 32; ++w) lam_s += sRed[w];
-                sdG[kC - 1] += __expf(GC) * lam_s - tot;
+            if (tid < 32) {
+                float th = sH[tid] + sH[tid + 32], tl = tid < kLoThreads / 32 ? sRed[tid] : 0.f;
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) {
+                    th += __shfl_xor_sync(0xffffffffu, th, m);
+                    tl += __shfl_xor_sync(0xffffffffu, tl, m);
+                }
+                if (tid == 0) sdG[kC - 1] += __expf(GC) * tl - th;
             }
             __syncthreads();
             if (tid < kC) sdG[tid] += sH[tid];
@@ -702,7 +929,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int r = r0 + i, s = tx + 16 * m;
-                    const float e = s <= r ? scale * __expf(sG[r] - sG[s]) * aP[i][m] : 0.f;
+                    const float e = s <= r ? scale * __expf(sG[r] - sG[s]) * sX[r * kLC + s] : 0.f;
                     sX[r * kLC + s] = e;
                     F[i][m] = e * sQK[r * kLC + s];
                 }
@@ -740,7 +967,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int r = r0 + i, s = tx + 16 * m;
-                    sX[r * kLC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]), Tk[i][m], aTv[i][m]) : 0.f;
+                    sX[r * kLC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]), Tk[i][m], sTv[r * kLC + s]) : 0.f;
                 }
         }
         __syncthreads();
@@ -782,12 +1009,16 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
         tile_mm<2, CK, false, false, kC>(dK, sX, kLC, sK, L::LK, r0, tx);   // dK += H K
         tile_mm<2, CK, true, false, kC>(dK, sX, kLC, sK, L::LK, r0, tx);    // dK += H^T K
         // dg = reverse cumulative sum of dG;  dbeta
-        if (tid == 0) {
-            float acc = 0.f;
-            for (int r = kC - 1; r >= 0; --r) {
-                acc += sdG[r];
-                sRow[r] = acc;
+        if (tid < 32) {   // dg = suffix sums of dG: lane l holds tokens 2l, 2l + 1
+            const float a = sdG[2 * tid], b = sdG[2 * tid + 1];
+            float x = a + b;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, x, o);
+                if (tid + o < 32) x += y;
             }
+            sRow[2 * tid] = x;
+            sRow[2 * tid + 1] = x - a;
         }
         __syncthreads();
         if (tid < n) {
@@ -825,6 +1056,7 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     ws.T = reinterpret_cast<float*>(base + Lw.T_off);
     ws.P = reinterpret_cast<float*>(base + Lw.P_off);
     ws.W = reinterpret_cast<float*>(base + Lw.W_off);
+    ws.Wt = reinterpret_cast<float*>(base + Lw.Wt_off);
     ws.U = reinterpret_cast<float*>(base + Lw.U_off);
     ws.G = reinterpret_cast<float*>(base + Lw.G_off);
     ws.S = reinterpret_cast<float*>(base + Lw.S_off);
@@ -902,6 +1134,7 @@ BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool p
     take(L.T_off, (size_t)kC * kC);
     take(L.P_off, (size_t)kC * kC);
     take(L.W_off, (size_t)kC * dk);
+    take(L.Wt_off, (size_t)kC * dk);
     take(L.U_off, (size_t)kC * dv);
     take(L.G_off, (size_t)kC);
     take(L.S_off, (size_t)dk * dv);
