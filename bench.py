@@ -575,9 +575,11 @@ def run_gpu(args):
                                     "frac": round(gate_bytes / (gate_ms * 1e6) / peaks["hbm_gbs"], 4),
                                     "algorithmic_bytes": gate_bytes}},
         "backward": {"workload": "prefill_gqa_8k backward: gradients w.r.t. q, k, v, g, beta, S0 from dout and "
-                                 "dS_final (token-serial CUDA-core kernels, checkpoints every 16 tokens)",
+                                 "dS_final through the chunked form (64-token chunks: WY factors, forward and "
+                                 "adjoint chunk chains, chunk-local gradients; fp32, dv contractions on tf32 "
+                                 "tensor cores with a three-product split)",
                      "value": round(world * tokens / (bwd_ms / 1e3), 1), "unit": "tokens/s",
-                     "ms_per_step": round(bwd_ms, 4), "steps": bwd_steps, "gpu_launches": 2 * bwd_steps,
+                     "ms_per_step": round(bwd_ms, 4), "steps": bwd_steps, "gpu_launches": 4 * bwd_steps,
                      "roofline": {"bound": "alu", "achieved": round(bwd_tf, 2), "peak": round(alu_peak, 1),
                                   "unit": "TFLOP/s", "frac": round(bwd_tf / alu_peak, 4),
                                   "peak_source": "fp32 FMA lanes x 2 x 2070 MHz (unit counts)"}},
@@ -680,14 +682,15 @@ def run_profile_case(case):
         for _ in range(2):
             gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, workspace=ws)
     elif case == "backward":
-        # one 1024-token sequence of the GQA workload's heads (a capture-sized backward), twice
-        w = gi.scaled(PREFILL, B=1, T=1024)
+        # the backward pass of the 8k GQA workload (about 2.6 GB of device memory with its workspace), twice
+        w = PREFILL
         x = device_inputs_random(torch, dev, w)
         S0 = 0.1 * torch.randn(w.B, w.Hv, w.dk, w.dv, device=dev)
         dout = torch.randn_like(x["v"])
         dSf = 0.1 * torch.randn_like(S0)
+        ws = torch.empty(gdn.backward_workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv), dtype=torch.uint8, device=dev)
         for _ in range(2):
-            gdn.gdn_recurrent_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, dout, dSf)
+            gdn.gdn_recurrent_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, dout, dSf, workspace=ws)
     elif case == "layer":
         # the conv of the packed q/k/v projection (three channel slices) and the prefill with the
         # fused front end and the output gate, twice

@@ -661,28 +661,64 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
 constexpr int kLoThreads = 512;
 constexpr int kLoRowGroups = kLoThreads / 16;   // 32 row groups of 2 rows
 constexpr int kDvc = 32;                        // value columns per pass over dv
+constexpr int kLCC = kC + 4;                    // C x C matrices: rows 16-byte aligned
 
 template <int DK, int DV>
 struct LoSmem {
     // LD = 36: rows of the pass buffers are 4 banks apart, so fragment loads (g, t) hit 32 banks
-    static constexpr int LK = DK + 1, LD = kDvc + 4;
-    static constexpr int K_ = 0, Q_ = K_ + kC * LK, KK_ = Q_ + kC * LK, QK_ = KK_ + kC * kLC, T_ = QK_ + kC * kLC,
-                         X_ = T_ + kC * kLC, DVB_ = X_ + kC * kLC;
+    static constexpr int LK = DK + 4, LD = kDvc + 4;
+    static constexpr int K_ = 0, Q_ = K_ + kC * LK, KK_ = Q_ + kC * LK, QK_ = KK_ + kC * kLCC,
+                         T_ = QK_ + kC * kLCC, X_ = T_ + kC * kLCC, DVB_ = X_ + kC * kLCC;
     // dv pass buffers (dU, U, dO, V: C x 32; S, lam: DK x 32); afterwards dW (C x DK) and one more C x DK
     // (or C x C) exchange buffer over them
     static constexpr int dU_ = DVB_, U_ = dU_ + kC * LD, dO_ = U_ + kC * LD, V_ = dO_ + kC * LD, S_ = V_ + kC * LD,
                          Lam_ = S_ + DK * LD, DVB_END = Lam_ + DK * LD, XY_ = DVB_ + kC * LK,
-                         DW_END = XY_ + (LK > kLC ? kC * LK : kC * kLC);
+                         DW_END = XY_ + (LK > kLCC ? kC * LK : kC * kLCC);
     static constexpr int VEC_ = DVB_END > DW_END ? DVB_END : DW_END;
     // G, beta, dG, dbeta, row scratch, h, column scratch [row groups][C], warp sums
     static constexpr int G_ = VEC_, Beta_ = G_ + kC, dG_ = Beta_ + kC, dB_ = dG_ + kC, Row_ = dB_ + kC,
                          H_ = Row_ + kC, Col_ = H_ + kC, Red_ = Col_ + kLoRowGroups * kC;
     static constexpr int FLOATS = Red_ + kLoThreads / 32;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
+    static_assert(Q_ % 4 == 0 && KK_ % 4 == 0 && T_ % 4 == 0 && X_ % 4 == 0 && DVB_ % 4 == 0 && XY_ % 4 == 0,
+                  "16-byte aligned regions");
 };
 
-// dst[r] += rowsum_s F[r][s] - colsum_r F[r][s] for a C x C register tile F (2 x 4 per thread): the
-// derivative of sum F with respect to G through the ratios exp(G_r - G_s).
+// Column c of a thread's tile in the contiguous layout: groups of VW = min(CN, 4) columns, the 16
+// threads of a row group covering 16 VW adjacent columns per group.
+template <int CN>
+__device__ __forceinline__ int tcol(int c, int tx) {
+    constexpr int VW = CN < 4 ? CN : 4;
+    return (c / VW) * 16 * VW + VW * tx + c % VW;
+}
+
+// acc[i][c] += sum_{k<K} opA(row0 + i, k) * B[k][tcol(c)], opA(r, k) = AT ? A[k][r] : A[r][k]; B is
+// k-major, so each thread loads its columns with CN / VW vector loads (a row group reads 16 VW
+// adjacent floats per load).
+template <int RM, int CN, bool AT, int K>
+__device__ __forceinline__ void tile_nn(float (&acc)[RM][CN], const float* __restrict__ A, int lda,
+                                        const float* __restrict__ B, int ldb, int row0, int tx) {
+    constexpr int VW = CN < 4 ? CN : 4, NV = CN / VW;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float a[RM], b[CN];
+        if (AT) {
+            lds_vec<RM>(a, A + k * lda + row0);
+        } else {
+#pragma unroll
+            for (int i = 0; i < RM; ++i) a[i] = A[(row0 + i) * lda + k];
+        }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) lds_vec<VW>(b + v * VW, B + k * ldb + v * 16 * VW + VW * tx);
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
+#pragma unroll
+            for (int c = 0; c < CN; ++c) acc[i][c] = fmaf(a[i], b[c], acc[i][c]);
+    }
+}
+
+// dst[r] += rowsum_s F[r][s] - colsum_r F[r][s] for a C x C register tile F (rows ty * 2 + i, columns
+// tx + 16 m): the derivative of sum F with respect to G through the ratios exp(G_r - G_s).
 __device__ __forceinline__ void add_rows_minus_cols(const float (&F)[2][4], float* sRow, float* sCol, float* dst,
                                                     int tid, int tx, int ty) {
 #pragma unroll
@@ -722,7 +758,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                  float scale, bool vec) {
     using L = LoSmem<DK, DV>;
     using D = WsDims<DK, DV>;
-    constexpr int CK = DK / 16;   // columns per thread of a C x DK tile (2 rows each)
+    constexpr int CK = DK / 16;   // columns per thread of a C x DK tile (2 rows each), at tcol<CK>
     extern __shared__ __align__(16) float sm[];
     float* sK = sm + L::K_;
     float* sQ = sm + L::Q_;
@@ -771,15 +807,15 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                sKK[(r0 + i) * kLC + tx + 16 * m] = kk[i][m];
-                sQK[(r0 + i) * kLC + tx + 16 * m] = qk[i][m];
+                sKK[(r0 + i) * kLCC + tx + 16 * m] = kk[i][m];
+                sQK[(r0 + i) * kLCC + tx + 16 * m] = qk[i][m];
             }
     }
 
     for (int jh = 0; jh < G; ++jh) {
         const int h = hk * G + jh;
         const size_t wi = (size_t)slot * Hv + h;
-        ld_ws<kC, kC, kLoThreads>(sT, kLC, ws.T + wi * D::T, kC, tid);
+        ld_ws<kC, kC, kLoThreads>(sT, kLCC, ws.T + wi * D::T, kC, tid);
         if (tid < kC) {
             sG[tid] = ws.G[wi * D::G + tid];
             sBeta[tid] = tid < n ? to_f32(beta[(tok0 + tid) * Hv + h]) : 0.f;
@@ -837,15 +873,15 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             {   // dV = diag(beta) T^T dU;  dbeta += rowsum(T^T dU o V)
                 float z[2][2];
                 tile_zero(z);
-                tile_mm<2, 2, true, false, kC>(z, sT, kLC, sdU, L::LD, r0, tx);
+                tile_nn<2, 2, true, kC>(z, sT, kLCC, sdU, L::LD, r0, tx);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     const int r = r0 + i;
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const int j = tx + 16 * m;
-                        zv[i] = fmaf(z[i][m], sV[r * L::LD + j], zv[i]);
-                        if (r < n) grad_v[((tok0 + r) * Hv + h) * DV + jc + j] = sBeta[r] * z[i][m];
+                    for (int c = 0; c < 2; ++c) {
+                        const int j = tcol<2>(c, tx);
+                        zv[i] = fmaf(z[i][c], sV[r * L::LD + j], zv[i]);
+                        if (r < n) grad_v[((tok0 + r) * Hv + h) * DV + jc + j] = sBeta[r] * z[i][c];
                     }
                 }
             }
@@ -875,11 +911,11 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                 const float gr = scale * __expf(sG[r]);
                 float a = 0.f;
 #pragma unroll
-                for (int m = 0; m < CK; ++m) {
-                    const int c = tx + 16 * m;
-                    const float x = sXY[r * L::LK + c];
-                    a = fmaf(x, sQ[r * L::LK + c], a);
-                    dQ[i][m] = gr * x;
+                for (int c = 0; c < CK; ++c) {
+                    const int col = tcol<CK>(c, tx);
+                    const float x = sXY[r * L::LK + col];
+                    a = fmaf(x, sQ[r * L::LK + col], a);
+                    dQ[i][c] = gr * x;
                 }
                 xr[i] = gr * a;
             }
@@ -892,17 +928,17 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                 const float kc = __expf(GC - sG[r]);
                 float b = 0.f;
 #pragma unroll
-                for (int m = 0; m < CK; ++m) {
-                    const int c = tx + 16 * m;
-                    const float y = sXY[r * L::LK + c];
-                    b = fmaf(y, sK[r * L::LK + c], b);
-                    dK[i][m] = kc * y;
+                for (int c = 0; c < CK; ++c) {
+                    const int col = tcol<CK>(c, tx);
+                    const float y = sXY[r * L::LK + col];
+                    b = fmaf(y, sK[r * L::LK + col], b);
+                    dK[i][c] = kc * y;
                 }
                 hr[i] = -kc * b;
             }
             __syncthreads();
-            store_frag<2>(sTv, kLC, fTv, 16 * mt, pb0, g, t, 1.f);
-            store_frag<2>(sX, kLC, fP, 16 * mt, pb0, g, t, 1.f);
+            store_frag<2>(sTv, kLCC, fTv, 16 * mt, pb0, g, t, 1.f);
+            store_frag<2>(sX, kLCC, fP, 16 * mt, pb0, g, t, 1.f);
             add_rows(xr, sRow, sdG, tid, tx, ty);   // its barriers publish sTv and sX
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
@@ -929,18 +965,18 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int r = r0 + i, s = tx + 16 * m;
-                    const float e = s <= r ? scale * __expf(sG[r] - sG[s]) * sX[r * kLC + s] : 0.f;
-                    sX[r * kLC + s] = e;
-                    F[i][m] = e * sQK[r * kLC + s];
+                    const float e = s <= r ? scale * __expf(sG[r] - sG[s]) * sX[r * kLCC + s] : 0.f;
+                    sX[r * kLCC + s] = e;
+                    F[i][m] = e * sQK[r * kLCC + s];
                 }
             add_rows_minus_cols(F, sRow, sCol, sdG, tid, tx, ty);   // its barriers publish sX
         }
-        tile_mm<2, CK, false, false, kC>(dQ, sX, kLC, sK, L::LK, r0, tx);   // dQ += E K
-        tile_mm<2, CK, true, false, kC>(dK, sX, kLC, sQ, L::LK, r0, tx);    // dK += E^T Q
+        tile_nn<2, CK, false, kC>(dQ, sX, kLCC, sK, L::LK, r0, tx);   // dQ += E K
+        tile_nn<2, CK, true, kC>(dK, sX, kLCC, sQ, L::LK, r0, tx);    // dK += E^T Q
         {   // R = T^T dW;  dK += diag(beta gamma) R;  dbeta_s += gamma_s R_s.k_s;  dG_s += beta_s gamma_s R_s.k_s
             float R[2][CK];
             tile_zero(R);
-            tile_mm<2, CK, true, false, kC>(R, sT, kLC, sDW, L::LK, r0, tx);
+            tile_nn<2, CK, true, kC>(R, sT, kLCC, sDW, L::LK, r0, tx);
             float rb[2], rg[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
@@ -948,9 +984,9 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                 const float gm = __expf(sG[s]), bg = sBeta[s] * gm;
                 float a = 0.f;
 #pragma unroll
-                for (int m = 0; m < CK; ++m) {
-                    a = fmaf(R[i][m], sK[s * L::LK + tx + 16 * m], a);
-                    dK[i][m] = fmaf(bg, R[i][m], dK[i][m]);
+                for (int c = 0; c < CK; ++c) {
+                    a = fmaf(R[i][c], sK[s * L::LK + tcol<CK>(c, tx)], a);
+                    dK[i][c] = fmaf(bg, R[i][c], dK[i][c]);
                 }
                 rb[i] = gm * a;
                 rg[i] = bg * a;
@@ -967,25 +1003,26 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int r = r0 + i, s = tx + 16 * m;
-                    sX[r * kLC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]), Tk[i][m], sTv[r * kLC + s]) : 0.f;
+                    sX[r * kLCC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]), Tk[i][m], sTv[r * kLCC + s]) : 0.f;
                 }
         }
         __syncthreads();
         {   // M1 = T^T dT -> sX
             float M1[2][4];
             tile_zero(M1);
-            tile_mm<2, 4, true, false, kC>(M1, sT, kLC, sX, kLC, r0, tx);
+            tile_nn<2, 4, true, kC>(M1, sT, kLCC, sX, kLCC, r0, tx);
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int m = 0; m < 4; ++m) sX[(r0 + i) * kLC + tx + 16 * m] = M1[i][m];
+                for (int c = 0; c < 4; ++c) sX[(r0 + i) * kLCC + tcol<4>(c, tx)] = M1[i][c];
         }
         __syncthreads();
-        {   // dM = -(M1 T^T) strictly lower;  dbeta_r += sum_s dM_rs A_rs;  H = diag(beta) D o dM -> sX
+        {   // dM = -(M1 T^T) strictly lower;  dbeta_r += sum_s dM_rs A_rs;  H = diag(beta) D o dM, and
+            // sX <- H + H^T (symmetric, so one product gives H K + H^T K)
             float Mm[2][4];
             tile_zero(Mm);
-            tile_mm<2, 4, false, true, kC>(Mm, sX, kLC, sT, kLC, r0, tx);
+            tile_mm<2, 4, false, true, kC>(Mm, sX, kLCC, sT, kLCC, r0, tx);
             float F[2][4], rb[2] = {0.f, 0.f};
             __syncthreads();
 #pragma unroll
@@ -993,22 +1030,23 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int r = r0 + i, s = tx + 16 * m;
-                    float hv = 0.f, f = 0.f;
+                    float f = 0.f;
                     if (s < r) {
-                        const float d = __expf(sG[r] - sG[s]), kk = sKK[r * kLC + s], dm = -Mm[i][m];
+                        const float d = __expf(sG[r] - sG[s]), kk = sKK[r * kLCC + s], dm = -Mm[i][m];
+                        const float hv = sBeta[r] * d * dm;
                         rb[i] = fmaf(dm, d * kk, rb[i]);
-                        hv = sBeta[r] * d * dm;
                         f = hv * kk;
+                        sX[r * kLCC + s] = hv;
+                        sX[s * kLCC + r] = hv;
+                    } else if (s == r) {
+                        sX[r * kLCC + s] = 0.f;
                     }
-                    sX[r * kLC + s] = hv;
                     F[i][m] = f;
                 }
             add_rows(rb, sRow, sdB, tid, tx, ty);
             add_rows_minus_cols(F, sRow, sCol, sdG, tid, tx, ty);
         }
-        tile_mm<2, CK, false, false, kC>(dK, sX, kLC, sK, L::LK, r0, tx);   // dK += H K
-        tile_mm<2, CK, true, false, kC>(dK, sX, kLC, sK, L::LK, r0, tx);    // dK += H^T K
-        // dg = reverse cumulative sum of dG;  dbeta
+        tile_nn<2, CK, true, kC>(dK, sX, kLCC, sK, L::LK, r0, tx);   // dK += (H + H^T) K
         if (tid < 32) {   // dg = suffix sums of dG: lane l holds tokens 2l, 2l + 1
             const float a = sdG[2 * tid], b = sdG[2 * tid + 1];
             float x = a + b;
@@ -1031,10 +1069,10 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             const int r = r0 + i;
             if (r < n) {
 #pragma unroll
-                for (int m = 0; m < CK; ++m) {
-                    const size_t o = ((tok0 + r) * Hqk + hk) * DK + tx + 16 * m;
-                    grad_q[o] = jh == 0 ? dQ[i][m] : grad_q[o] + dQ[i][m];
-                    grad_k[o] = jh == 0 ? dK[i][m] : grad_k[o] + dK[i][m];
+                for (int c = 0; c < CK; ++c) {
+                    const size_t o = ((tok0 + r) * Hqk + hk) * DK + tcol<CK>(c, tx);
+                    grad_q[o] = jh == 0 ? dQ[i][c] : grad_q[o] + dQ[i][c];
+                    grad_k[o] = jh == 0 ? dK[i][c] : grad_k[o] + dK[i][c];
                 }
             }
         }
