@@ -56,6 +56,21 @@ def test_backward_packed_with_empty_and_short(dtype):
     run(w, x, y, with_s0=False, with_dsf=False)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_packed_multichunk_odd_grouping_strong_decay(dtype):
+    """Packed sequences spanning several 64-token chunks (full, partial and a 1-token tail), three value
+    heads per query/key head, and one head with strong decay (~e^-3.5 per token, whose decay ratios
+    underflow within a chunk)."""
+    lens = (130, 0, 64, 1, 200)
+    w = gi.Workload("bwd_packed_mc", "prefill", dtype, B=1, T=sum(lens), Hqk=1, Hv=3, dk=64, dv=32, s0_std=0.1,
+                    seqlens=lens, seed=14)
+    x, y = gi.make_prefill_inputs(w), gi.make_backward_inputs(w)
+    g = np.array(x["g"], dtype=np.float64)
+    g[:, :, 1] = g[:, :, 1] * 60.0 - 0.5
+    x["g"] = gi.round_to_dtype(g, dtype)
+    run(w, x, y, scale=0.7)
+
+
 def test_backward_longer_gqa_d128():
     w = gi.scaled(gi.WORKLOADS["prefill_gqa_8k"], B=1, T=300, Hqk=2, Hv=4)
     run(w, gi.make_prefill_inputs(w), gi.make_backward_inputs(w))
@@ -105,3 +120,16 @@ def test_backward_prefill_gqa_8k_full_sampled():
     mine = [got[0][:1, :, 8:9], got[1][:1, :, 8:9], sub(got[2], 2), sub(got[3], 2), sub(got[4], 2), sub(got[5], 1)]
     errs = {n: rel_err(r, m) for n, r, m in zip(NAMES, ref, mine)}
     assert all(e <= TOL for e in errs.values()), errs
+
+
+def test_backward_no_tokens_passes_the_final_state_gradient_through():
+    """T = 0: the state is never touched, so dL/dS0 = dL/dS_final."""
+    dSf = torch.randn(2, 2, 32, 32, device="cuda")
+    e = torch.empty(2, 0, 1, 32, dtype=torch.bfloat16, device="cuda")
+    ev = torch.empty(2, 0, 2, 32, dtype=torch.bfloat16, device="cuda")
+    eg = torch.empty(2, 0, 2, dtype=torch.bfloat16, device="cuda")
+    S0 = torch.randn(2, 2, 32, 32, device="cuda")
+    got = gdn.gdn_recurrent_bwd(e, e, ev, eg, eg, S0, ev, dSf)
+    torch.cuda.synchronize()
+    assert torch.equal(got[5], dSf)
+    assert all(t.numel() == 0 for t in got[:5])
