@@ -598,6 +598,9 @@ constexpr int kChainThreads = 256;
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+__device__ __forceinline__ void named_barrier_arrive(int id, int threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -726,6 +729,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         tc_fence_before();
         __syncthreads();
 
+        uint32_t spend[32];   // gamma-scaled state row of the previous step, stored to TMEM after the next D1 issue
         for (long long c = 0; c < nch; ++c) {
             const int st = (int)(c & 1);
             const uint32_t par = (uint32_t)(c & 1);
@@ -740,6 +744,11 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     mma_bf16(d1, smem_desc(a1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                              smem_desc(sb + C_SB + ks * 2048, 1024, 1024), idesc_bf16(128, 64, 0, 1), 1);
                 mma_commit(bar_mma1);
+            }
+            if (c > 0) {   // TMEM columns 0-63 (the state) are not touched by the D1 MMA
+                tmem_st32(tl + cb, spend);
+                tmem_wait_st();
+                tc_fence_before();
             }
             wait_k(c);
             mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
@@ -761,7 +770,8 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_barrier_sync(1, 128);   // the four U warps only: the output warps do not gate the update
+                // all 256 threads arrive (their gamma-scaled state rows are in TMEM); only the U warps wait
+                named_barrier_sync(1, 256);
                 if (tid == 0) {   // S (gamma_C-scaled, in TMEM) += K^T (b U); then the next chunk's V part
                     tc_fence_after();
                     for (int ks = 0; ks < 4; ++ks)
@@ -771,6 +781,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     if (c + 1 < nch && wait_a(c + 1)) issue_v_part(c + 1);
                 }
             } else {             // output row of token R - 64
+                named_barrier_arrive(1, 256);
                 const int r = R - 64;
                 if (r < n) {
                     uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z + cb);
@@ -784,16 +795,16 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     }
                 }
             }
-            mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
-            tc_fence_after();
-            if (tid == kProducer && c + kKStages < nch) issue_loads_k(c + kKStages);   // K, vector consumed
             const bool last = (c + 1 == nch);
             float gnext = 1.f;
-            if (!last) {
+            if (!last) {   // the next chunk's gamma_C, read while the state update runs
                 wait_k(c + 1);
                 gnext = reinterpret_cast<const float*>(sm + C_VEC + (int)((c + 1) % kKStages) * 512)[64];
             }
-            {   // new state row R: bf16 copy for the next D1, gamma-scaled copy in TMEM
+            mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+            tc_fence_after();
+            if (tid == kProducer && c + kKStages < nch) issue_loads_k(c + kKStages);   // K, vector consumed
+            {   // new state row R: bf16 copy for the next D1 now, gamma-scaled copy to TMEM next step
                 uint32_t v[32];
                 tmem_ld32(tl + cb, v);
                 tmem_wait_ld();
@@ -813,11 +824,9 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(gnext * __uint_as_float(v[e]));
-                    tmem_st32(tl + cb, v);
+                    for (int e = 0; e < 32; ++e) spend[e] = __float_as_uint(gnext * __uint_as_float(v[e]));
                 }
             }
-            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
