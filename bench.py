@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # were taken on (sha256 prefix of the file); None once the source has changed.
 NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix of that file at capture, dram read + write bytes per launch)
-    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "565b2e8189a6d2b7", 139437568 + 344683264),
-    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "565b2e8189a6d2b7", 612447744 + 120327168),
+    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "0bcae087cc59422e", 139425536 + 344787456),
+    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "0bcae087cc59422e", 612621568 + 119872000),
     "decode_step_kernel": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_decode.cu", "0a3ae9abf76d8679", 541133568 + 480455680),
 }
 
@@ -276,7 +276,7 @@ def run_gpu(args):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = host_out[0].numel() * 2 + host_Sf[0].numel() * 4
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(3, min(args.steps, 50))
     n_e = e2e_steps + 2
     ev_in = [torch.cuda.Event() for _ in range(n_e)]
     ev_cmp = [torch.cuda.Event() for _ in range(n_e)]
