@@ -630,13 +630,34 @@ def oracle_rate(tokens_per_seq, threads=0):
     return w.B * tokens_per_seq / dt, dt, orc.max_threads() if threads <= 0 else threads
 
 
+def small_config_rates():
+    """The oracle on the two small workloads (tiny_f32, charlm_bf16), on one core and on all cores:
+    tokens/s of the whole workload, best of three runs."""
+    from oracle import recurrence as orc
+    res = {}
+    for name in ("tiny_f32", "charlm_bf16"):
+        w = gi.WORKLOADS[name]
+        x = gi.make_prefill_inputs(w)
+        for threads in (1, 0):
+            best = None
+            for _ in range(3):
+                t = time.perf_counter()
+                orc.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], S0=x["S0"], threads=threads)
+                dt = time.perf_counter() - t
+                best = dt if best is None else min(best, dt)
+            key = "1_core" if threads == 1 else f"{orc.max_threads()}_cores"
+            res.setdefault(name, {})[key] = round(w.B * w.T / best, 1)
+    return res
+
+
 def cpu_baseline(budget_s=15.0):
     rate, dt, cores = oracle_rate(128)                      # calibration
     n = int(max(128, min(PREFILL.T, rate * budget_s / PREFILL.B)))
     rate, dt, cores = oracle_rate(n)
     return {"value": round(rate, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"first {n} tokens of both sequences of prefill_gqa_8k, all 32 value heads, fp64 "
-                      f"token loop, {dt:.1f} s"}
+                      f"token loop, {dt:.1f} s",
+            "small_workloads_tokens_per_s": small_config_rates()}
 
 
 def run_reference(args):
