@@ -14,8 +14,9 @@
 // and the chunk-local gradients follow by the chain rule through T (dT -> -T^T dT T^T), the decay
 // ratios (d exp(G_r - G_s) adds to G_r and subtracts from G_s) and dg = reverse cumulative sum of dG.
 //
-// Four kernels, fp32 on the CUDA cores:
-//   bwd_wy_kernel         per (chunk, query/key head): T, W, U~, P and G of each of its value heads
+// Four kernels, all in fp32 accuracy (CUDA cores; the chunk-local contractions over dv on tf32 tensor
+// cores with each operand split into two tf32 parts):
+//   bwd_wy_kernel         per (chunk, query/key head): T, W, W^T, U~, P and G of each of its value heads
 //   bwd_state_fwd_kernel  per (sequence, value head, column slice): chunk-start states S, and U
 //   bwd_state_adj_kernel  per (sequence, value head, column slice), chunks in reverse: lam, dU, dS0
 //   bwd_local_kernel      per (chunk, query/key head): dq, dk (summed over its value heads), dv, dg, dbeta
