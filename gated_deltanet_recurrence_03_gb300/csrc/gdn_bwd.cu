@@ -64,13 +64,6 @@ __device__ __forceinline__ void tile_zero(float (&acc)[RM][CN]) {
         for (int m = 0; m < CN; ++m) acc[i][m] = 0.f;
 }
 
-// Sum over the 16 lanes that share a row group (tx = lane % 16).
-__device__ __forceinline__ float sum16(float x) {
-#pragma unroll
-    for (int m = 1; m < 16; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-    return x;
-}
-
 // ---------------------------------------------------------------- tensor-core products in fp32 accuracy
 // mma.sync m16n8k8 with tf32 operands; each fp32 operand is split as x = hi + lo (hi = x rounded to
 // tf32, lo = the remainder rounded to tf32) and a b ~ hi_a hi_b + hi_a lo_b + lo_a hi_b, whose
@@ -111,6 +104,39 @@ __device__ __forceinline__ void frag_bt(const float* X, int ld, int n0, int k0, 
                                         uint32_t (&lo)[2]) {
     split_tf32(X[(n0 + g) * ld + k0 + t], hi[0], lo[0]);
     split_tf32(X[(n0 + g) * ld + k0 + t + 4], hi[1], lo[1]);
+}
+// A fragment of A stored k-major (A[m][k] = X[k][m]): rows row0 + g (+ 8), k = k0 + t (+ 4).
+__device__ __forceinline__ void frag_at(const float* X, int ld, int row0, int k0, int g, int t, uint32_t (&hi)[4],
+                                        uint32_t (&lo)[4]) {
+    split_tf32(X[(k0 + t) * ld + row0 + g], hi[0], lo[0]);
+    split_tf32(X[(k0 + t) * ld + row0 + g + 8], hi[1], lo[1]);
+    split_tf32(X[(k0 + t + 4) * ld + row0 + g], hi[2], lo[2]);
+    split_tf32(X[(k0 + t + 4) * ld + row0 + g + 8], hi[3], lo[3]);
+}
+// B fragment of B stored k-major (B[k][n] = X[k][n]): n = n0 + g, k = k0 + t (+ 4).
+__device__ __forceinline__ void frag_b(const float* X, int ld, int n0, int k0, int g, int t, uint32_t (&hi)[2],
+                                       uint32_t (&lo)[2]) {
+    split_tf32(X[(k0 + t) * ld + n0 + g], hi[0], lo[0]);
+    split_tf32(X[(k0 + t + 4) * ld + n0 + g], hi[1], lo[1]);
+}
+// acc[q] += A B over k < K for the 16 rows from row0 and the NT n-tiles of 8 from nb0, in fp32 accuracy
+// (three-product tf32 split).  AT: A stored k-major; BT: B stored n-major (X[n][k]).
+template <int NT, int K, bool AT, bool BT>
+__device__ __forceinline__ void mma_prod(float (&acc)[NT][4], const float* A, int lda, const float* B, int ldb,
+                                         int row0, int nb0, int g, int t) {
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t ah[4], al[4];
+        if (AT) frag_at(A, lda, row0, k0, g, t, ah, al);
+        else frag_a(A, lda, row0, k0, g, t, ah, al);
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            uint32_t bh[2], bl[2];
+            if (BT) frag_bt(B, ldb, 8 * (nb0 + q), k0, g, t, bh, bl);
+            else frag_b(B, ldb, 8 * (nb0 + q), k0, g, t, bh, bl);
+            mma_3xtf32(acc[q], ah, al, bh, bl);
+        }
+    }
 }
 // sign * (N accumulator fragments of rows row0 .. row0 + 15, n-tiles nb0 .. nb0 + N - 1) to D.
 template <int N>
@@ -659,94 +685,91 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
 }
 
 // ---------------------------------------------------------------- kernel 4: chunk-local gradients
-constexpr int kLoThreads = 512;
-constexpr int kLoRowGroups = kLoThreads / 16;   // 32 row groups of 2 rows
-constexpr int kDvc = 32;                        // value columns per pass over dv
-constexpr int kLCC = kC + 4;                    // C x C matrices: rows 16-byte aligned
+// Every product runs on tf32 tensor cores with the three-product split (fp32 accuracy), in the
+// accumulator fragment layout: warp w owns rows 16 (w % 4) .. +15 and, of a C x dk product, the
+// n-tiles of 8 from (w / 4) dk / 32; of a C x C product, n-tiles 2 (w / 4) and 2 (w / 4) + 1.  dq and
+// dk stay in those fragments across the value heads of the query/key head.
+constexpr int kLoThreads = 512;   // 16 warps
+constexpr int kDvc = 32;          // value columns per pass over dv
+constexpr int kLCC = kC + 4;      // C x C matrices: rows 4 banks apart (conflict-free row-major fragments)
 
 template <int DK, int DV>
 struct LoSmem {
-    // LD = 36: rows of the pass buffers are 4 banks apart, so fragment loads (g, t) hit 32 banks
+    // LK, LD = 4 mod 32 as well
     static constexpr int LK = DK + 4, LD = kDvc + 4;
     static constexpr int K_ = 0, Q_ = K_ + kC * LK, KK_ = Q_ + kC * LK, QK_ = KK_ + kC * kLCC,
                          T_ = QK_ + kC * kLCC, X_ = T_ + kC * kLCC, DVB_ = X_ + kC * kLCC;
-    // dv pass buffers (dU, U, dO, V: C x 32; S, lam: DK x 32); afterwards dW (C x DK) and one more C x DK
-    // (or C x C) exchange buffer over them
+    // dv pass buffers (dU, U, dO, V: C x 32; S, lam: DK x 32); afterwards dW (C x DK) over them
     static constexpr int dU_ = DVB_, U_ = dU_ + kC * LD, dO_ = U_ + kC * LD, V_ = dO_ + kC * LD, S_ = V_ + kC * LD,
-                         Lam_ = S_ + DK * LD, DVB_END = Lam_ + DK * LD, XY_ = DVB_ + kC * LK,
-                         DW_END = XY_ + (LK > kLCC ? kC * LK : kC * kLCC);
+                         Lam_ = S_ + DK * LD, DVB_END = Lam_ + DK * LD, DW_END = DVB_ + kC * LK;
     static constexpr int VEC_ = DVB_END > DW_END ? DVB_END : DW_END;
-    // G, beta, dG, dbeta, row scratch, h, column scratch [row groups][C], warp sums
+    // G, beta, dG, dbeta, row scratch, h, reduction scratch [8][C], warp sums
     static constexpr int G_ = VEC_, Beta_ = G_ + kC, dG_ = Beta_ + kC, dB_ = dG_ + kC, Row_ = dB_ + kC,
-                         H_ = Row_ + kC, Col_ = H_ + kC, Red_ = Col_ + kLoRowGroups * kC;
+                         H_ = Row_ + kC, Scr_ = H_ + kC, Red_ = Scr_ + 8 * kC;
     static constexpr int FLOATS = Red_ + kLoThreads / 32;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
-    static_assert(Q_ % 4 == 0 && KK_ % 4 == 0 && T_ % 4 == 0 && X_ % 4 == 0 && DVB_ % 4 == 0 && XY_ % 4 == 0,
-                  "16-byte aligned regions");
+    static_assert(Q_ % 4 == 0 && KK_ % 4 == 0 && T_ % 4 == 0 && X_ % 4 == 0 && DVB_ % 4 == 0, "aligned regions");
 };
 
-// Column c of a thread's tile in the contiguous layout: groups of VW = min(CN, 4) columns, the 16
-// threads of a row group covering 16 VW adjacent columns per group.
-template <int CN>
-__device__ __forceinline__ int tcol(int c, int tx) {
-    constexpr int VW = CN < 4 ? CN : 4;
-    return (c / VW) * 16 * VW + VW * tx + c % VW;
+// Fragment coordinates of accumulator element e of n-tile nb: row row0 + g (+ 8 for e >= 2),
+// column 8 nb + 2 t + (e & 1).
+__device__ __forceinline__ int frow(int row0, int g, int e) { return row0 + g + (e >= 2 ? 8 : 0); }
+__device__ __forceinline__ int fcol(int nb, int t, int e) { return 8 * nb + 2 * t + (e & 1); }
+
+// dst[r] += full sum of row r, given this thread's partial sums p0 (row row0 + g) and p1 (row row0 + g + 8):
+// a quad sum over t, then the four column-group warps of the row tile in a fixed order.
+__device__ __forceinline__ void frag_rows_add(float p0, float p1, float* scr, float* dst, int tid, int row0, int wg,
+                                              int g, int t) {
+    p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+    p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+    p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+    p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+    if (t == 0) {
+        scr[wg * kC + row0 + g] = p0;
+        scr[wg * kC + row0 + g + 8] = p1;
+    }
+    __syncthreads();
+    if (tid < kC) dst[tid] += ((scr[tid] + scr[kC + tid]) + scr[2 * kC + tid]) + scr[3 * kC + tid];
+    __syncthreads();
 }
 
-// acc[i][c] += sum_{k<K} opA(row0 + i, k) * B[k][tcol(c)], opA(r, k) = AT ? A[k][r] : A[r][k]; B is
-// k-major, so each thread loads its columns with CN / VW vector loads (a row group reads 16 VW
-// adjacent floats per load).
-template <int RM, int CN, bool AT, int K>
-__device__ __forceinline__ void tile_nn(float (&acc)[RM][CN], const float* __restrict__ A, int lda,
-                                        const float* __restrict__ B, int ldb, int row0, int tx) {
-    constexpr int VW = CN < 4 ? CN : 4, NV = CN / VW;
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float a[RM], b[CN];
-        if (AT) {
-            lds_vec<RM>(a, A + k * lda + row0);
-        } else {
+// dst[r] += rowsum_s F[r][s] - colsum_r F[r][s] for a C x C product in fragments (n-tiles 2 wg, 2 wg + 1):
+// the derivative of sum F with respect to G through the ratios exp(G_r - G_s).
+__device__ __forceinline__ void frag_rows_minus_cols(const float (&F)[2][4], float* scr, float* dst, int tid,
+                                                     int row0, int wg, int mt, int g, int t) {
+    float r0 = (F[0][0] + F[0][1]) + (F[1][0] + F[1][1]);
+    float r1 = (F[0][2] + F[0][3]) + (F[1][2] + F[1][3]);
+    r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
+    r0 += __shfl_xor_sync(0xffffffffu, r0, 2);
+    r1 += __shfl_xor_sync(0xffffffffu, r1, 1);
+    r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
+    float c[2][2];
 #pragma unroll
-            for (int i = 0; i < RM; ++i) a[i] = A[(row0 + i) * lda + k];
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float x = F[q][j] + F[q][2 + j];
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            x += __shfl_xor_sync(0xffffffffu, x, 8);
+            x += __shfl_xor_sync(0xffffffffu, x, 16);
+            c[q][j] = x;
         }
-#pragma unroll
-        for (int v = 0; v < NV; ++v) lds_vec<VW>(b + v * VW, B + k * ldb + v * 16 * VW + VW * tx);
-#pragma unroll
-        for (int i = 0; i < RM; ++i)
-#pragma unroll
-            for (int c = 0; c < CN; ++c) acc[i][c] = fmaf(a[i], b[c], acc[i][c]);
+    if (t == 0) {
+        scr[wg * kC + row0 + g] = r0;
+        scr[wg * kC + row0 + g + 8] = r1;
     }
-}
-
-// dst[r] += rowsum_s F[r][s] - colsum_r F[r][s] for a C x C register tile F (rows ty * 2 + i, columns
-// tx + 16 m): the derivative of sum F with respect to G through the ratios exp(G_r - G_s).
-__device__ __forceinline__ void add_rows_minus_cols(const float (&F)[2][4], float* sRow, float* sCol, float* dst,
-                                                    int tid, int tx, int ty) {
+    if (g == 0) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float x = sum16(F[i][0] + F[i][1] + F[i][2] + F[i][3]);
-        if (tx == 0) sRow[ty * 2 + i] = x;
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) scr[(4 + mt) * kC + fcol(2 * wg + q, t, j)] = c[q][j];
     }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) sCol[ty * kC + tx + 16 * m] = F[0][m] + F[1][m];
     __syncthreads();
     if (tid < kC) {
-        float c = 0.f;
-        for (int t = 0; t < kLoRowGroups; ++t) c += sCol[t * kC + tid];
-        dst[tid] += sRow[tid] - c;
+        const float rs = ((scr[tid] + scr[kC + tid]) + scr[2 * kC + tid]) + scr[3 * kC + tid];
+        const float cs = ((scr[4 * kC + tid] + scr[5 * kC + tid]) + scr[6 * kC + tid]) + scr[7 * kC + tid];
+        dst[tid] += rs - cs;
     }
-    __syncthreads();
-}
-
-// dst[r] += sum over the 16 lanes of a row group of x[i] (row ty * 2 + i).
-__device__ __forceinline__ void add_rows(const float (&x)[2], float* sRow, float* dst, int tid, int tx, int ty) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float s = sum16(x[i]);
-        if (tx == 0) sRow[ty * 2 + i] = s;
-    }
-    __syncthreads();
-    if (tid < kC) dst[tid] += sRow[tid];
     __syncthreads();
 }
 
@@ -759,7 +782,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                  float scale, bool vec) {
     using L = LoSmem<DK, DV>;
     using D = WsDims<DK, DV>;
-    constexpr int CK = DK / 16;   // columns per thread of a C x DK tile (2 rows each), at tcol<CK>
+    constexpr int NTW = DK / 32;   // n-tiles of 8 per warp of a C x dk product
     extern __shared__ __align__(16) float sm[];
     float* sK = sm + L::K_;
     float* sQ = sm + L::Q_;
@@ -774,15 +797,13 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     float* sS = sm + L::S_;
     float* sLam = sm + L::Lam_;
     float* sDW = sm + L::DVB_;
-    float* sXY = sm + L::XY_;
-    float* sTv = sm + L::XY_;
     float* sG = sm + L::G_;
     float* sBeta = sm + L::Beta_;
     float* sdG = sm + L::dG_;
     float* sdB = sm + L::dB_;
     float* sRow = sm + L::Row_;
     float* sH = sm + L::H_;
-    float* sCol = sm + L::Col_;
+    float* sScr = sm + L::Scr_;
     float* sRed = sm + L::Red_;
 
     const long long slot = blockIdx.x;
@@ -790,27 +811,21 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     int seq, n;
     long long tok0;
     if (!slot_chunk(cu, nseq, T_len, slot, seq, tok0, n)) return;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16, r0 = ty * 2;
-    constexpr int NTW = DK / 32;   // value-side n-tiles of 8 per warp (16 warps: 4 row tiles x 4 column groups)
-    const int warp = tid / 32, lane = tid % 32, g = lane / 4, t = lane % 4;
-    const int mt = warp % 4, nb0 = (warp / 4) * NTW, pb0 = (warp / 4) * 2;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, g = lane / 4, t = lane % 4;
+    const int mt = warp % 4, wg = warp / 4, row0 = 16 * mt, nb0 = wg * NTW, pb0 = 2 * wg;
+    const int ra = row0 + g, rb = ra + 8;   // this thread's two accumulator rows
 
     ld_in<TT, kC, DK, kLoThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
     ld_in<TT, kC, DK, kLoThreads>(sQ, L::LK, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
     __syncthreads();
-    {
+    {   // Gram matrices K K^T and Q K^T (shared by the value heads)
         float kk[2][4], qk[2][4];
         tile_zero(kk);
         tile_zero(qk);
-        tile_mm<2, 4, false, true, DK>(kk, sK, L::LK, sK, L::LK, r0, tx);
-        tile_mm<2, 4, false, true, DK>(qk, sQ, L::LK, sK, L::LK, r0, tx);
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                sKK[(r0 + i) * kLCC + tx + 16 * m] = kk[i][m];
-                sQK[(r0 + i) * kLCC + tx + 16 * m] = qk[i][m];
-            }
+        mma_prod<2, DK, false, true>(kk, sK, L::LK, sK, L::LK, row0, pb0, g, t);
+        mma_prod<2, DK, false, true>(qk, sQ, L::LK, sK, L::LK, row0, pb0, g, t);
+        store_frag<2>(sKK, kLCC, kk, row0, pb0, g, t, 1.f);
+        store_frag<2>(sQK, kLCC, qk, row0, pb0, g, t, 1.f);
     }
 
     for (int jh = 0; jh < G; ++jh) {
@@ -822,15 +837,16 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             sBeta[tid] = tid < n ? to_f32(beta[(tok0 + tid) * Hv + h]) : 0.f;
             sdG[tid] = 0.f;
             sdB[tid] = 0.f;
+            sH[tid] = 0.f;
         }
-        // fragment accumulators (warp w: rows 16 mt .. +15; value-side n-tiles of 8 from nb0, C-side from pb0)
+        // fW: dU S^T, fX: dO S^T, fY: U lam^T (n-tiles from nb0); fP: dO U^T, fTv: dU V^T (n-tiles from pb0)
         float fW[NTW][4], fX[NTW][4], fY[NTW][4], fP[2][4], fTv[2][4];
         tile_zero(fW);
         tile_zero(fX);
         tile_zero(fY);
         tile_zero(fP);
         tile_zero(fTv);
-        float zv[2] = {0.f, 0.f}, ss = 0.f;
+        float zv0 = 0.f, zv1 = 0.f, ss = 0.f;
         for (int jc = 0; jc < DV; jc += kDvc) {
             __syncthreads();
             ld_ws<kC, kDvc, kLoThreads>(sdU, L::LD, ws.dU + wi * D::dU + jc, DV, tid);
@@ -845,45 +861,48 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                 ss = fmaf(sS[i * L::LD + j], sLam[i * L::LD + j], ss);
             }
 #pragma unroll
-            for (int k0 = 0; k0 < kDvc; k0 += 8) {   // tensor cores: dU S^T, dU V^T, dO S^T, dO U^T, U lam^T
+            for (int k0 = 0; k0 < kDvc; k0 += 8) {   // dU S^T, dU V^T, dO S^T, dO U^T, U lam^T
                 uint32_t ah[4], al[4], bh[2], bl[2], sh[NTW][2], sl[NTW][2];
 #pragma unroll
-                for (int q = 0; q < NTW; ++q) frag_bt(sS, L::LD, 8 * (nb0 + q), k0, g, t, sh[q], sl[q]);
-                frag_a(sdU, L::LD, 16 * mt, k0, g, t, ah, al);
+                for (int qq = 0; qq < NTW; ++qq) frag_bt(sS, L::LD, 8 * (nb0 + qq), k0, g, t, sh[qq], sl[qq]);
+                frag_a(sdU, L::LD, row0, k0, g, t, ah, al);
 #pragma unroll
-                for (int q = 0; q < NTW; ++q) mma_3xtf32(fW[q], ah, al, sh[q], sl[q]);
+                for (int qq = 0; qq < NTW; ++qq) mma_3xtf32(fW[qq], ah, al, sh[qq], sl[qq]);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    frag_bt(sV, L::LD, 8 * (pb0 + q), k0, g, t, bh, bl);
-                    mma_3xtf32(fTv[q], ah, al, bh, bl);
+                for (int qq = 0; qq < 2; ++qq) {
+                    frag_bt(sV, L::LD, 8 * (pb0 + qq), k0, g, t, bh, bl);
+                    mma_3xtf32(fTv[qq], ah, al, bh, bl);
                 }
-                frag_a(sdO, L::LD, 16 * mt, k0, g, t, ah, al);
+                frag_a(sdO, L::LD, row0, k0, g, t, ah, al);
 #pragma unroll
-                for (int q = 0; q < NTW; ++q) mma_3xtf32(fX[q], ah, al, sh[q], sl[q]);
+                for (int qq = 0; qq < NTW; ++qq) mma_3xtf32(fX[qq], ah, al, sh[qq], sl[qq]);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    frag_bt(sU, L::LD, 8 * (pb0 + q), k0, g, t, bh, bl);
-                    mma_3xtf32(fP[q], ah, al, bh, bl);
+                for (int qq = 0; qq < 2; ++qq) {
+                    frag_bt(sU, L::LD, 8 * (pb0 + qq), k0, g, t, bh, bl);
+                    mma_3xtf32(fP[qq], ah, al, bh, bl);
                 }
 #pragma unroll
-                for (int q = 0; q < NTW; ++q) frag_bt(sLam, L::LD, 8 * (nb0 + q), k0, g, t, sh[q], sl[q]);
-                frag_a(sU, L::LD, 16 * mt, k0, g, t, ah, al);
+                for (int qq = 0; qq < NTW; ++qq) frag_bt(sLam, L::LD, 8 * (nb0 + qq), k0, g, t, sh[qq], sl[qq]);
+                frag_a(sU, L::LD, row0, k0, g, t, ah, al);
 #pragma unroll
-                for (int q = 0; q < NTW; ++q) mma_3xtf32(fY[q], ah, al, sh[q], sl[q]);
+                for (int qq = 0; qq < NTW; ++qq) mma_3xtf32(fY[qq], ah, al, sh[qq], sl[qq]);
             }
-            {   // dV = diag(beta) T^T dU;  dbeta += rowsum(T^T dU o V)
-                float z[2][2];
+            {   // dV = diag(beta) T^T dU (this pass's columns 8 wg .. 8 wg + 7);  dbeta += rowsum(T^T dU o V)
+                float z[1][4];
                 tile_zero(z);
-                tile_nn<2, 2, true, kC>(z, sT, kLCC, sdU, L::LD, r0, tx);
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int r = r0 + i;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int j = tcol<2>(c, tx);
-                        zv[i] = fmaf(z[i][c], sV[r * L::LD + j], zv[i]);
-                        if (r < n) grad_v[((tok0 + r) * Hv + h) * DV + jc + j] = sBeta[r] * z[i][c];
-                    }
+                mma_prod<1, kC, true, false>(z, sT, kLCC, sdU, L::LD, row0, wg, g, t);
+                const int j = fcol(wg, t, 0);
+                zv0 = fmaf(z[0][0], sV[ra * L::LD + j], fmaf(z[0][1], sV[ra * L::LD + j + 1], zv0));
+                zv1 = fmaf(z[0][2], sV[rb * L::LD + j], fmaf(z[0][3], sV[rb * L::LD + j + 1], zv1));
+                if (ra < n) {   // (grad_v needs only 4-byte alignment: scalar stores)
+                    float* o = grad_v + ((tok0 + ra) * Hv + h) * DV + jc + j;
+                    o[0] = sBeta[ra] * z[0][0];
+                    o[1] = sBeta[ra] * z[0][1];
+                }
+                if (rb < n) {
+                    float* o = grad_v + ((tok0 + rb) * Hv + h) * DV + jc + j;
+                    o[0] = sBeta[rb] * z[0][2];
+                    o[1] = sBeta[rb] * z[0][3];
                 }
             }
         }
@@ -891,163 +910,128 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             float x = ss;
 #pragma unroll
             for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-            if ((tid & 31) == 0) sRed[tid / 32] = x;
+            if (lane == 0) sRed[warp] = x;
         }
-        add_rows(zv, sRow, sdB, tid, tx, ty);   // its barriers also end the dv passes
-        // The fragment accumulators go through shared memory to the (row group, tx) tiles:
-        // dW = -dU S^T stays there (sDW); dO S^T, then U lam^T, then dU V^T and dO U^T pass through.
-        store_frag<NTW>(sDW, L::LK, fW, 16 * mt, nb0, g, t, -1.f);
-        store_frag<NTW>(sXY, L::LK, fX, 16 * mt, nb0, g, t, 1.f);
-        __syncthreads();
-        // dQ = scale diag(gamma) (dO S^T);  dG_r += scale gamma_r (dO S^T)_r . q_r
-        // dK = diag(gamma_C / gamma) (U lam^T);  with h_r = (gamma_C / gamma_r) (U lam^T)_r . k_r:
+        frag_rows_add(zv0, zv1, sScr, sdB, tid, row0, wg, g, t);   // its barriers also end the dv passes
+        store_frag<NTW>(sDW, L::LK, fW, row0, nb0, g, t, -1.f);      // dW = -dU S^T (over the pass buffers)
+        // dQ = scale diag(gamma) (dO S^T) in fX;  dG_r += scale gamma_r (dO S^T)_r . q_r
+        // dK = diag(gamma_C / gamma) (U lam^T) in fY;  with h_r = (gamma_C / gamma_r) (U lam^T)_r . k_r:
         // dG_r -= h_r and dG_{C-1} += sum_r h_r + gamma_C <lam, S>
-        float dQ[2][CK], dK[2][CK];
+        float (&dQ)[NTW][4] = fX;
+        float (&dK)[NTW][4] = fY;
+        const float GC = sG[kC - 1];
         {
-            float xr[2], hr[2];
-            const float GC = sG[kC - 1];
+            const float gra = scale * __expf(sG[ra]), grb = scale * __expf(sG[rb]);
+            const float kca = __expf(GC - sG[ra]), kcb = __expf(GC - sG[rb]);
+            float xa = 0.f, xb = 0.f, ya = 0.f, yb = 0.f;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int r = r0 + i;
-                const float gr = scale * __expf(sG[r]);
-                float a = 0.f;
+            for (int qq = 0; qq < NTW; ++qq)
 #pragma unroll
-                for (int c = 0; c < CK; ++c) {
-                    const int col = tcol<CK>(c, tx);
-                    const float x = sXY[r * L::LK + col];
-                    a = fmaf(x, sQ[r * L::LK + col], a);
-                    dQ[i][c] = gr * x;
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(row0, g, e), c = fcol(nb0 + qq, t, e);
+                    const float xq = fX[qq][e] * sQ[r * L::LK + c], yk = fY[qq][e] * sK[r * L::LK + c];
+                    if (e < 2) { xa += xq; ya += yk; } else { xb += xq; yb += yk; }
+                    dQ[qq][e] = (e < 2 ? gra : grb) * fX[qq][e];
+                    dK[qq][e] = (e < 2 ? kca : kcb) * fY[qq][e];
                 }
-                xr[i] = gr * a;
-            }
-            __syncthreads();
-            store_frag<NTW>(sXY, L::LK, fY, 16 * mt, nb0, g, t, 1.f);
-            __syncthreads();
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int r = r0 + i;
-                const float kc = __expf(GC - sG[r]);
-                float b = 0.f;
-#pragma unroll
-                for (int c = 0; c < CK; ++c) {
-                    const int col = tcol<CK>(c, tx);
-                    const float y = sXY[r * L::LK + col];
-                    b = fmaf(y, sK[r * L::LK + col], b);
-                    dK[i][c] = kc * y;
-                }
-                hr[i] = -kc * b;
-            }
-            __syncthreads();
-            store_frag<2>(sTv, kLCC, fTv, 16 * mt, pb0, g, t, 1.f);
-            store_frag<2>(sX, kLCC, fP, 16 * mt, pb0, g, t, 1.f);
-            add_rows(xr, sRow, sdG, tid, tx, ty);   // its barriers publish sTv and sX
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float s = sum16(hr[i]);
-                if (tx == 0) sH[r0 + i] = s;
-            }
-            __syncthreads();
-            if (tid < 32) {
-                float th = sH[tid] + sH[tid + 32], tl = tid < kLoThreads / 32 ? sRed[tid] : 0.f;
-#pragma unroll
-                for (int m = 16; m >= 1; m >>= 1) {
-                    th += __shfl_xor_sync(0xffffffffu, th, m);
-                    tl += __shfl_xor_sync(0xffffffffu, tl, m);
-                }
-                if (tid == 0) sdG[kC - 1] += __expf(GC) * tl - th;
-            }
-            __syncthreads();
-            if (tid < kC) sdG[tid] += sH[tid];
+            frag_rows_add(gra * xa, grb * xb, sScr, sdG, tid, row0, wg, g, t);
+            frag_rows_add(-kca * ya, -kcb * yb, sScr, sH, tid, row0, wg, g, t);   // sH = -h
         }
-        {   // E = scale D o dP (s <= r) -> sX;  dG from E o QK^T
+        if (tid < 32) {
+            float th = sH[tid] + sH[tid + 32], tl = tid < kLoThreads / 32 ? sRed[tid] : 0.f;
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) {
+                th += __shfl_xor_sync(0xffffffffu, th, m);
+                tl += __shfl_xor_sync(0xffffffffu, tl, m);
+            }
+            if (tid == 0) sdG[kC - 1] += __expf(GC) * tl - th;
+        }
+        __syncthreads();
+        if (tid < kC) sdG[tid] += sH[tid];
+        {   // E = scale D o dP (s <= r) -> sX (row-major);  dG from E o QK^T
             float F[2][4];
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = r0 + i, s = tx + 16 * m;
-                    const float e = s <= r ? scale * __expf(sG[r] - sG[s]) * sX[r * kLCC + s] : 0.f;
-                    sX[r * kLCC + s] = e;
-                    F[i][m] = e * sQK[r * kLCC + s];
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(row0, g, e), s = fcol(pb0 + qq, t, e);
+                    const float ev = s <= r ? scale * __expf(sG[r] - sG[s]) * fP[qq][e] : 0.f;
+                    sX[r * kLCC + s] = ev;
+                    F[qq][e] = ev * sQK[r * kLCC + s];
                 }
-            add_rows_minus_cols(F, sRow, sCol, sdG, tid, tx, ty);   // its barriers publish sX
+            frag_rows_minus_cols(F, sScr, sdG, tid, row0, wg, mt, g, t);   // its barriers publish sX and sDW
         }
-        tile_nn<2, CK, false, kC>(dQ, sX, kLCC, sK, L::LK, r0, tx);   // dQ += E K
-        tile_nn<2, CK, true, kC>(dK, sX, kLCC, sQ, L::LK, r0, tx);    // dK += E^T Q
+        mma_prod<NTW, kC, false, false>(dQ, sX, kLCC, sK, L::LK, row0, nb0, g, t);   // dQ += E K
+        mma_prod<NTW, kC, true, false>(dK, sX, kLCC, sQ, L::LK, row0, nb0, g, t);    // dK += E^T Q
         {   // R = T^T dW;  dK += diag(beta gamma) R;  dbeta_s += gamma_s R_s.k_s;  dG_s += beta_s gamma_s R_s.k_s
-            float R[2][CK];
+            float R[NTW][4];
             tile_zero(R);
-            tile_nn<2, CK, true, kC>(R, sT, kLCC, sDW, L::LK, r0, tx);
-            float rb[2], rg[2];
+            mma_prod<NTW, kC, true, false>(R, sT, kLCC, sDW, L::LK, row0, nb0, g, t);
+            const float gma = __expf(sG[ra]), gmb = __expf(sG[rb]);
+            const float bga = sBeta[ra] * gma, bgb = sBeta[rb] * gmb;
+            float rka = 0.f, rkb = 0.f;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int s = r0 + i;
-                const float gm = __expf(sG[s]), bg = sBeta[s] * gm;
-                float a = 0.f;
+            for (int qq = 0; qq < NTW; ++qq)
 #pragma unroll
-                for (int c = 0; c < CK; ++c) {
-                    a = fmaf(R[i][c], sK[s * L::LK + tcol<CK>(c, tx)], a);
-                    dK[i][c] = fmaf(bg, R[i][c], dK[i][c]);
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(row0, g, e), c = fcol(nb0 + qq, t, e);
+                    const float x = R[qq][e] * sK[r * L::LK + c];
+                    if (e < 2) rka += x; else rkb += x;
+                    dK[qq][e] = fmaf(e < 2 ? bga : bgb, R[qq][e], dK[qq][e]);
                 }
-                rb[i] = gm * a;
-                rg[i] = bg * a;
-            }
-            add_rows(rb, sRow, sdB, tid, tx, ty);   // its barriers also end every read of E in sX
-            add_rows(rg, sRow, sdG, tid, tx, ty);
+            frag_rows_add(gma * rka, gmb * rkb, sScr, sdB, tid, row0, wg, g, t);   // also ends the reads of E
+            frag_rows_add(bga * rka, bgb * rkb, sScr, sdG, tid, row0, wg, g, t);
         }
         {   // dT = (dU V^T + dW K^T diag(gamma)) diag(beta), lower part -> sX
             float Tk[2][4];
             tile_zero(Tk);
-            tile_mm<2, 4, false, true, DK>(Tk, sDW, L::LK, sK, L::LK, r0, tx);
+            mma_prod<2, DK, false, true>(Tk, sDW, L::LK, sK, L::LK, row0, pb0, g, t);
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = r0 + i, s = tx + 16 * m;
-                    sX[r * kLCC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]), Tk[i][m], sTv[r * kLCC + s]) : 0.f;
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(row0, g, e), s = fcol(pb0 + qq, t, e);
+                    sX[r * kLCC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]), Tk[qq][e], fTv[qq][e]) : 0.f;
                 }
         }
         __syncthreads();
         {   // M1 = T^T dT -> sX
             float M1[2][4];
             tile_zero(M1);
-            tile_nn<2, 4, true, kC>(M1, sT, kLCC, sX, kLCC, r0, tx);
+            mma_prod<2, kC, true, false>(M1, sT, kLCC, sX, kLCC, row0, pb0, g, t);
             __syncthreads();
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) sX[(r0 + i) * kLCC + tcol<4>(c, tx)] = M1[i][c];
+            store_frag<2>(sX, kLCC, M1, row0, pb0, g, t, 1.f);
         }
         __syncthreads();
         {   // dM = -(M1 T^T) strictly lower;  dbeta_r += sum_s dM_rs A_rs;  H = diag(beta) D o dM, and
             // sX <- H + H^T (symmetric, so one product gives H K + H^T K)
             float Mm[2][4];
             tile_zero(Mm);
-            tile_mm<2, 4, false, true, kC>(Mm, sX, kLCC, sT, kLCC, r0, tx);
-            float F[2][4], rb[2] = {0.f, 0.f};
+            mma_prod<2, kC, false, true>(Mm, sX, kLCC, sT, kLCC, row0, pb0, g, t);
+            float F[2][4], ba = 0.f, bb = 0.f;
             __syncthreads();
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = r0 + i, s = tx + 16 * m;
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(row0, g, e), s = fcol(pb0 + qq, t, e);
                     float f = 0.f;
                     if (s < r) {
-                        const float d = __expf(sG[r] - sG[s]), kk = sKK[r * kLCC + s], dm = -Mm[i][m];
+                        const float d = __expf(sG[r] - sG[s]), kk = sKK[r * kLCC + s], dm = -Mm[qq][e];
                         const float hv = sBeta[r] * d * dm;
-                        rb[i] = fmaf(dm, d * kk, rb[i]);
+                        if (e < 2) ba = fmaf(dm, d * kk, ba); else bb = fmaf(dm, d * kk, bb);
                         f = hv * kk;
                         sX[r * kLCC + s] = hv;
                         sX[s * kLCC + r] = hv;
                     } else if (s == r) {
                         sX[r * kLCC + s] = 0.f;
                     }
-                    F[i][m] = f;
+                    F[qq][e] = f;
                 }
-            add_rows(rb, sRow, sdB, tid, tx, ty);
-            add_rows_minus_cols(F, sRow, sCol, sdG, tid, tx, ty);
+            frag_rows_add(ba, bb, sScr, sdB, tid, row0, wg, g, t);
+            frag_rows_minus_cols(F, sScr, sdG, tid, row0, wg, mt, g, t);
         }
-        tile_nn<2, CK, true, kC>(dK, sX, kLCC, sK, L::LK, r0, tx);   // dK += (H + H^T) K
+        mma_prod<NTW, kC, false, false>(dK, sX, kLCC, sK, L::LK, row0, nb0, g, t);   // dK += (H + H^T) K
         if (tid < 32) {   // dg = suffix sums of dG: lane l holds tokens 2l, 2l + 1
             const float a = sdG[2 * tid], b = sdG[2 * tid + 1];
             float x = a + b;
@@ -1066,17 +1050,16 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
         }
         // dq, dk of the query/key head: its first value head writes, the others add (same thread, same element)
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int r = r0 + i;
-            if (r < n) {
+        for (int qq = 0; qq < NTW; ++qq)
 #pragma unroll
-                for (int c = 0; c < CK; ++c) {
-                    const size_t o = ((tok0 + r) * Hqk + hk) * DK + tcol<CK>(c, tx);
-                    grad_q[o] = jh == 0 ? dQ[i][c] : grad_q[o] + dQ[i][c];
-                    grad_k[o] = jh == 0 ? dK[i][c] : grad_k[o] + dK[i][c];
+            for (int e = 0; e < 4; ++e) {
+                const int r = frow(row0, g, e);
+                if (r < n) {
+                    const size_t o = ((tok0 + r) * Hqk + hk) * DK + fcol(nb0 + qq, t, e);
+                    grad_q[o] = jh == 0 ? dQ[qq][e] : grad_q[o] + dQ[qq][e];
+                    grad_k[o] = jh == 0 ? dK[qq][e] : grad_k[o] + dK[qq][e];
                 }
             }
-        }
         __syncthreads();
     }
 }
