@@ -91,19 +91,36 @@ __device__ __forceinline__ void mma_3xtf32(float (&d)[4], const uint32_t (&ah)[4
     mma_tf32(d, ah, bl);
     mma_tf32(d, ah, bh);
 }
+// Operands whose values tf32 represents exactly (bf16 inputs widened to fp32: K, Q, dO, V) have a zero
+// lo part, so their lo products are skipped: EA / EB mark A / B exact (three, two or one MMA).
+template <bool EA, bool EB>
+__device__ __forceinline__ void mma_split(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                          const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+    if (!EA) mma_tf32(d, al, bh);
+    if (!EB) mma_tf32(d, ah, bl);
+    mma_tf32(d, ah, bh);
+}
+// Split x into tf32 hi / lo, or, for an exact operand, take its bits as they are (lo unused).
+template <bool EXACT>
+__device__ __forceinline__ void split_x(float x, uint32_t& hi, uint32_t& lo) {
+    if (EXACT) hi = __float_as_uint(x);
+    else split_tf32(x, hi, lo);
+}
 // A fragment: rows row0 + g (+ 8), columns k0 + t (+ 4) of a row-major fp32 matrix.
+template <bool EXACT = false>
 __device__ __forceinline__ void frag_a(const float* A, int ld, int row0, int k0, int g, int t, uint32_t (&hi)[4],
                                        uint32_t (&lo)[4]) {
-    split_tf32(A[(row0 + g) * ld + k0 + t], hi[0], lo[0]);
-    split_tf32(A[(row0 + g + 8) * ld + k0 + t], hi[1], lo[1]);
-    split_tf32(A[(row0 + g) * ld + k0 + t + 4], hi[2], lo[2]);
-    split_tf32(A[(row0 + g + 8) * ld + k0 + t + 4], hi[3], lo[3]);
+    split_x<EXACT>(A[(row0 + g) * ld + k0 + t], hi[0], lo[0]);
+    split_x<EXACT>(A[(row0 + g + 8) * ld + k0 + t], hi[1], lo[1]);
+    split_x<EXACT>(A[(row0 + g) * ld + k0 + t + 4], hi[2], lo[2]);
+    split_x<EXACT>(A[(row0 + g + 8) * ld + k0 + t + 4], hi[3], lo[3]);
 }
 // B fragment of B = X^T (B[k][n] = X[n][k], X row-major): n = n0 + g, k = k0 + t (+ 4).
+template <bool EXACT = false>
 __device__ __forceinline__ void frag_bt(const float* X, int ld, int n0, int k0, int g, int t, uint32_t (&hi)[2],
                                         uint32_t (&lo)[2]) {
-    split_tf32(X[(n0 + g) * ld + k0 + t], hi[0], lo[0]);
-    split_tf32(X[(n0 + g) * ld + k0 + t + 4], hi[1], lo[1]);
+    split_x<EXACT>(X[(n0 + g) * ld + k0 + t], hi[0], lo[0]);
+    split_x<EXACT>(X[(n0 + g) * ld + k0 + t + 4], hi[1], lo[1]);
 }
 // A fragment of A stored k-major (A[m][k] = X[k][m]): rows row0 + g (+ 8), k = k0 + t (+ 4).
 __device__ __forceinline__ void frag_at(const float* X, int ld, int row0, int k0, int g, int t, uint32_t (&hi)[4],
@@ -114,27 +131,28 @@ __device__ __forceinline__ void frag_at(const float* X, int ld, int row0, int k0
     split_tf32(X[(k0 + t + 4) * ld + row0 + g + 8], hi[3], lo[3]);
 }
 // B fragment of B stored k-major (B[k][n] = X[k][n]): n = n0 + g, k = k0 + t (+ 4).
+template <bool EXACT = false>
 __device__ __forceinline__ void frag_b(const float* X, int ld, int n0, int k0, int g, int t, uint32_t (&hi)[2],
                                        uint32_t (&lo)[2]) {
-    split_tf32(X[(k0 + t) * ld + n0 + g], hi[0], lo[0]);
-    split_tf32(X[(k0 + t + 4) * ld + n0 + g], hi[1], lo[1]);
+    split_x<EXACT>(X[(k0 + t) * ld + n0 + g], hi[0], lo[0]);
+    split_x<EXACT>(X[(k0 + t + 4) * ld + n0 + g], hi[1], lo[1]);
 }
 // acc[q] += A B over k < K for the 16 rows from row0 and the NT n-tiles of 8 from nb0, in fp32 accuracy
 // (three-product tf32 split).  AT: A stored k-major; BT: B stored n-major (X[n][k]).
-template <int NT, int K, bool AT, bool BT>
+template <int NT, int K, bool AT, bool BT, bool EA = false, bool EB = false>
 __device__ __forceinline__ void mma_prod(float (&acc)[NT][4], const float* A, int lda, const float* B, int ldb,
                                          int row0, int nb0, int g, int t) {
 #pragma unroll 2
     for (int k0 = 0; k0 < K; k0 += 8) {
         uint32_t ah[4], al[4];
         if (AT) frag_at(A, lda, row0, k0, g, t, ah, al);
-        else frag_a(A, lda, row0, k0, g, t, ah, al);
+        else frag_a<EA>(A, lda, row0, k0, g, t, ah, al);
 #pragma unroll
         for (int q = 0; q < NT; ++q) {
             uint32_t bh[2], bl[2];
-            if (BT) frag_bt(B, ldb, 8 * (nb0 + q), k0, g, t, bh, bl);
-            else frag_b(B, ldb, 8 * (nb0 + q), k0, g, t, bh, bl);
-            mma_3xtf32(acc[q], ah, al, bh, bl);
+            if (BT) frag_bt<EB>(B, ldb, 8 * (nb0 + q), k0, g, t, bh, bl);
+            else frag_b<EB>(B, ldb, 8 * (nb0 + q), k0, g, t, bh, bl);
+            mma_split<EA, EB>(acc[q], ah, al, bh, bl);
         }
     }
 }
@@ -783,6 +801,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     using L = LoSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int NTW = DK / 32;   // n-tiles of 8 per warp of a C x dk product
+    constexpr bool kEx = sizeof(TT) == 2;   // bf16 inputs: K, Q, dO, V are exact in tf32
     extern __shared__ __align__(16) float sm[];
     float* sK = sm + L::K_;
     float* sQ = sm + L::Q_;
@@ -822,8 +841,8 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
         float kk[2][4], qk[2][4];
         tile_zero(kk);
         tile_zero(qk);
-        mma_prod<2, DK, false, true>(kk, sK, L::LK, sK, L::LK, row0, pb0, g, t);
-        mma_prod<2, DK, false, true>(qk, sQ, L::LK, sK, L::LK, row0, pb0, g, t);
+        mma_prod<2, DK, false, true, kEx, kEx>(kk, sK, L::LK, sK, L::LK, row0, pb0, g, t);
+        mma_prod<2, DK, false, true, kEx, kEx>(qk, sQ, L::LK, sK, L::LK, row0, pb0, g, t);
         store_frag<2>(sKK, kLCC, kk, row0, pb0, g, t, 1.f);
         store_frag<2>(sQK, kLCC, qk, row0, pb0, g, t, 1.f);
     }
@@ -870,16 +889,16 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                 for (int qq = 0; qq < NTW; ++qq) mma_3xtf32(fW[qq], ah, al, sh[qq], sl[qq]);
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq) {
-                    frag_bt(sV, L::LD, 8 * (pb0 + qq), k0, g, t, bh, bl);
-                    mma_3xtf32(fTv[qq], ah, al, bh, bl);
+                    frag_bt<kEx>(sV, L::LD, 8 * (pb0 + qq), k0, g, t, bh, bl);
+                    mma_split<false, kEx>(fTv[qq], ah, al, bh, bl);
                 }
-                frag_a(sdO, L::LD, row0, k0, g, t, ah, al);
+                frag_a<kEx>(sdO, L::LD, row0, k0, g, t, ah, al);
 #pragma unroll
-                for (int qq = 0; qq < NTW; ++qq) mma_3xtf32(fX[qq], ah, al, sh[qq], sl[qq]);
+                for (int qq = 0; qq < NTW; ++qq) mma_split<kEx, false>(fX[qq], ah, al, sh[qq], sl[qq]);
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq) {
                     frag_bt(sU, L::LD, 8 * (pb0 + qq), k0, g, t, bh, bl);
-                    mma_3xtf32(fP[qq], ah, al, bh, bl);
+                    mma_split<kEx, false>(fP[qq], ah, al, bh, bl);
                 }
 #pragma unroll
                 for (int qq = 0; qq < NTW; ++qq) frag_bt(sLam, L::LD, 8 * (nb0 + qq), k0, g, t, sh[qq], sl[qq]);
@@ -961,8 +980,8 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                 }
             frag_rows_minus_cols(F, sScr, sdG, tid, row0, wg, mt, g, t);   // its barriers publish sX and sDW
         }
-        mma_prod<NTW, kC, false, false>(dQ, sX, kLCC, sK, L::LK, row0, nb0, g, t);   // dQ += E K
-        mma_prod<NTW, kC, true, false>(dK, sX, kLCC, sQ, L::LK, row0, nb0, g, t);    // dK += E^T Q
+        mma_prod<NTW, kC, false, false, false, kEx>(dQ, sX, kLCC, sK, L::LK, row0, nb0, g, t);   // dQ += E K
+        mma_prod<NTW, kC, true, false, false, kEx>(dK, sX, kLCC, sQ, L::LK, row0, nb0, g, t);    // dK += E^T Q
         {   // R = T^T dW;  dK += diag(beta gamma) R;  dbeta_s += gamma_s R_s.k_s;  dG_s += beta_s gamma_s R_s.k_s
             float R[NTW][4];
             tile_zero(R);
@@ -985,7 +1004,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
         {   // dT = (dU V^T + dW K^T diag(gamma)) diag(beta), lower part -> sX
             float Tk[2][4];
             tile_zero(Tk);
-            mma_prod<2, DK, false, true>(Tk, sDW, L::LK, sK, L::LK, row0, pb0, g, t);
+            mma_prod<2, DK, false, true, false, kEx>(Tk, sDW, L::LK, sK, L::LK, row0, pb0, g, t);
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
@@ -1031,7 +1050,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             frag_rows_add(ba, bb, sScr, sdB, tid, row0, wg, g, t);
             frag_rows_minus_cols(F, sScr, sdG, tid, row0, wg, mt, g, t);
         }
-        mma_prod<NTW, kC, false, false>(dK, sX, kLCC, sK, L::LK, row0, nb0, g, t);   // dK += (H + H^T) K
+        mma_prod<NTW, kC, false, false, false, kEx>(dK, sX, kLCC, sK, L::LK, row0, nb0, g, t);   // dK += (H + H^T) K
         if (tid < 32) {   // dg = suffix sums of dG: lane l holds tokens 2l, 2l + 1
             const float a = sdG[2 * tid], b = sdG[2 * tid + 1];
             float x = a + b;
