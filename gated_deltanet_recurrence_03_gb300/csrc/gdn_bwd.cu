@@ -14,9 +14,9 @@
 // and the chunk-local gradients follow by the chain rule through T (dT -> -T^T dT T^T), the decay
 // ratios (d exp(G_r - G_s) adds to G_r and subtracts from G_s) and dg = reverse cumulative sum of dG.
 //
-// Four kernels, all in fp32 accuracy (CUDA cores; the chunk-local contractions over dv on tf32 tensor
-// cores with each operand split into two tf32 parts):
-//   bwd_wy_kernel         per (chunk, query/key head): T, W, W^T, U~, P and G of each of its value heads
+// Four kernels, all in fp32 accuracy: the WY kernel on CUDA cores, the chains and the chunk-local
+// kernel on tf32 tensor cores with each fp32 operand split into two tf32 parts:
+//   bwd_wy_kernel         per (chunk, query/key head): T, W, U~, P and G of each of its value heads
 //   bwd_state_fwd_kernel  per (sequence, value head, column slice): chunk-start states S, and U
 //   bwd_state_adj_kernel  per (sequence, value head, column slice), chunks in reverse: lam, dU, dS0
 //   bwd_local_kernel      per (chunk, query/key head): dq, dk (summed over its value heads), dv, dg, dbeta
@@ -123,12 +123,22 @@ __device__ __forceinline__ void frag_bt(const float* X, int ld, int n0, int k0, 
     split_x<EXACT>(X[(n0 + g) * ld + k0 + t + 4], hi[1], lo[1]);
 }
 // A fragment of A stored k-major (A[m][k] = X[k][m]): rows row0 + g (+ 8), k = k0 + t (+ 4).
+template <bool EXACT = false>
 __device__ __forceinline__ void frag_at(const float* X, int ld, int row0, int k0, int g, int t, uint32_t (&hi)[4],
                                         uint32_t (&lo)[4]) {
-    split_tf32(X[(k0 + t) * ld + row0 + g], hi[0], lo[0]);
-    split_tf32(X[(k0 + t) * ld + row0 + g + 8], hi[1], lo[1]);
-    split_tf32(X[(k0 + t + 4) * ld + row0 + g], hi[2], lo[2]);
-    split_tf32(X[(k0 + t + 4) * ld + row0 + g + 8], hi[3], lo[3]);
+    split_x<EXACT>(X[(k0 + t) * ld + row0 + g], hi[0], lo[0]);
+    split_x<EXACT>(X[(k0 + t) * ld + row0 + g + 8], hi[1], lo[1]);
+    split_x<EXACT>(X[(k0 + t + 4) * ld + row0 + g], hi[2], lo[2]);
+    split_x<EXACT>(X[(k0 + t + 4) * ld + row0 + g + 8], hi[3], lo[3]);
+}
+// The same with column k of A (row k of X) scaled by ks[k] (a diagonal matrix between the factors).
+__device__ __forceinline__ void frag_at_scaled(const float* X, int ld, const float* ks, int row0, int k0, int g, int t,
+                                               uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    const float s0 = ks[k0 + t], s1 = ks[k0 + t + 4];
+    split_tf32(s0 * X[(k0 + t) * ld + row0 + g], hi[0], lo[0]);
+    split_tf32(s0 * X[(k0 + t) * ld + row0 + g + 8], hi[1], lo[1]);
+    split_tf32(s1 * X[(k0 + t + 4) * ld + row0 + g], hi[2], lo[2]);
+    split_tf32(s1 * X[(k0 + t + 4) * ld + row0 + g + 8], hi[3], lo[3]);
 }
 // B fragment of B stored k-major (B[k][n] = X[k][n]): n = n0 + g, k = k0 + t (+ 4).
 template <bool EXACT = false>
@@ -145,7 +155,7 @@ __device__ __forceinline__ void mma_prod(float (&acc)[NT][4], const float* A, in
 #pragma unroll 2
     for (int k0 = 0; k0 < K; k0 += 8) {
         uint32_t ah[4], al[4];
-        if (AT) frag_at(A, lda, row0, k0, g, t, ah, al);
+        if (AT) frag_at<EA>(A, lda, row0, k0, g, t, ah, al);
         else frag_a<EA>(A, lda, row0, k0, g, t, ah, al);
 #pragma unroll
         for (int q = 0; q < NT; ++q) {
@@ -257,7 +267,7 @@ __device__ __forceinline__ bool slot_chunk(const int32_t* cu, int nseq, int T, l
 
 // Per-(slot, value head) workspace arrays.
 struct Ws {
-    float *T, *P, *W, *Wt, *U, *G, *S, *dS, *dU;   // Wt = W^T [dk][C]
+    float *T, *P, *W, *U, *G, *S, *dS, *dU;
 };
 
 template <int DK, int DV>
@@ -413,10 +423,7 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int m = 0; m < CN; ++m) {
-                    ws.W[wi * D::W + (size_t)(ty * 4 + i) * DK + tx + 16 * m] = acc[i][m];
-                    ws.Wt[wi * D::W + (size_t)(tx + 16 * m) * kC + ty * 4 + i] = acc[i][m];
-                }
+                for (int m = 0; m < CN; ++m) ws.W[wi * D::W + (size_t)(ty * 4 + i) * DK + tx + 16 * m] = acc[i][m];
         }
         {   // U~ = T diag(beta) V
             constexpr int CN = DV / 16;
@@ -432,104 +439,38 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
     }
 }
 
+// Fragment coordinates of accumulator element e of n-tile nb: row row0 + g (+ 8 for e >= 2),
+// column 8 nb + 2 t + (e & 1).
+__device__ __forceinline__ int frow(int row0, int g, int e) { return row0 + g + (e >= 2 ? 8 : 0); }
+__device__ __forceinline__ int fcol(int nb, int t, int e) { return 8 * nb + 2 * t + (e & 1); }
+
 // ---------------------------------------------------------------- kernels 2 and 3: the chunk chains
+// Both chains run their products on tf32 tensor cores with the three-product split (fp32 accuracy),
+// 8 warps per CTA; each product's 16 x 8 output tiles are spread over the warps by ChainTiles.
 constexpr int kStThreads = 256;
 
 template <int DV>
 constexpr int slice_width() { return DV < 64 ? DV : 64; }
 
-// N contiguous fp32 from shared memory (16-byte aligned for N >= 4, 8-byte for N = 2).
-template <int N>
-__device__ __forceinline__ void lds_vec(float* dst, const float* p) {
-    if constexpr (N % 4 == 0) {
-#pragma unroll
-        for (int v = 0; v < N / 4; ++v) {
-            const float4 x = *reinterpret_cast<const float4*>(p + 4 * v);
-            dst[4 * v] = x.x;
-            dst[4 * v + 1] = x.y;
-            dst[4 * v + 2] = x.z;
-            dst[4 * v + 3] = x.w;
-        }
-    } else if constexpr (N == 2) {
-        const float2 x = *reinterpret_cast<const float2*>(p);
-        dst[0] = x.x;
-        dst[1] = x.y;
-    } else {
-#pragma unroll
-        for (int v = 0; v < N; ++v) dst[v] = p[v];
-    }
-}
-
-// Outer-product tile: acc[i][e] += sum_{k<K} At[k][row0 + i] (* ks[k]) * B[k][col0 + e], both operands
-// stored k-major (rows 16-byte aligned), so each k costs one vector load of RM values (shared by the
-// 16 threads of a row group) and one of CN values.
-template <int RM, int CN, int K, bool KS = false>
-__device__ __forceinline__ void tile_tn(float (&acc)[RM][CN], const float* __restrict__ At, int lda,
-                                        const float* __restrict__ B, int ldb, int row0, int col0,
-                                        const float* __restrict__ ks = nullptr) {
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float a[RM], b[CN];
-        lds_vec<RM>(a, At + k * lda + row0);
-        lds_vec<CN>(b, B + k * ldb + col0);
-        if (KS) {
-            const float s = ks[k];
-#pragma unroll
-            for (int i = 0; i < RM; ++i) a[i] *= s;
-        }
-#pragma unroll
-        for (int i = 0; i < RM; ++i)
-#pragma unroll
-            for (int e = 0; e < CN; ++e) acc[i][e] = fmaf(a[i], b[e], acc[i][e]);
-    }
-}
-
-// Rows [0, ROWS) x columns [0, WIDTH) of an element-type block (rows >= n zero) into shared memory
-// TRANSPOSED: dst[c * ld + r].  Consecutive threads take consecutive rows, so the stores are
-// conflict-free.
-template <typename TT, int ROWS, int WIDTH, int NT>
-__device__ __forceinline__ void ld_in_t(float* __restrict__ dst, int ld, const TT* __restrict__ src, size_t stride,
-                                        int n, int tid, bool vec) {
-    constexpr int EPV = 16 / (int)sizeof(TT), V = WIDTH / EPV, TOTAL = ROWS * V, PER = (TOTAL + NT - 1) / NT;
-    if (vec) {
-        uint4 b[PER];
-#pragma unroll
-        for (int p = 0; p < PER; ++p) {
-            const int idx = tid + p * NT, r = idx % ROWS;
-            b[p] = make_uint4(0u, 0u, 0u, 0u);
-            if ((TOTAL % NT == 0 || idx < TOTAL) && r < n)
-                b[p] = *reinterpret_cast<const uint4*>(src + (size_t)r * stride + (idx / ROWS) * EPV);
-        }
-#pragma unroll
-        for (int p = 0; p < PER; ++p) {
-            const int idx = tid + p * NT;
-            if (TOTAL % NT == 0 || idx < TOTAL) {
-                float f[EPV];
-                unpack16(b[p], f);
-                const int r = idx % ROWS, c0 = (idx / ROWS) * EPV;
-#pragma unroll
-                for (int x = 0; x < EPV; ++x) dst[(c0 + x) * ld + r] = f[x];
-            }
-        }
-    } else {
-        for (int idx = tid; idx < ROWS * WIDTH; idx += NT) {
-            const int r = idx % ROWS, c = idx / ROWS;
-            dst[c * ld + r] = r < n ? to_f32(src[(size_t)r * stride + c]) : 0.f;
-        }
-    }
-}
+// An M x N product over the 8 warps: the M / 16 row tiles first, the N / 8 column tiles split among
+// the warps that share a row tile.  Warp w: row tile w % MT, column tiles (w / MT) NT .. + NT - 1.
+template <int M, int N>
+struct ChainTiles {
+    static constexpr int MT = M / 16, WPM = 8 / MT, NT = (N / 8) / WPM;
+    static_assert(MT >= 1 && MT <= 8 && 8 % MT == 0 && (N / 8) % WPM == 0 && NT >= 1, "tile split");
+};
 
 template <int DK, int DV>
 struct StSmem {
-    // leading dimensions: width + 4 (rows 16-byte aligned, and rows 4 banks apart)
+    // leading dimensions: width + 4 (= 4 mod 32: conflict-free row-major fragments)
     static constexpr int SW = slice_width<DV>(), LK = DK + 4, LCC = kC + 4, LS = SW + 4;
-    // forward: W^T [DK][C], K [C][DK], U slice [C][SW], S slice [DK][SW]
-    // adjoint: K^T [DK][C], W [C][DK], Q [C][DK], P [C][C], dO and dU slices [C][SW], lam slice [DK][SW]
-    static constexpr int At_ = 0, B_ = At_ + DK * LCC, Q_ = B_ + kC * LK, P_ = Q_ + kC * LK, X_ = P_ + kC * LCC,
+    // forward: W [C][DK], K [C][DK], U slice [C][SW], S slice [DK][SW]
+    // adjoint: W, K, Q [C][DK], P [C][C], dO and dU slices [C][SW], lam slice [DK][SW]
+    static constexpr int W_ = 0, K_ = W_ + kC * LK, Q_ = K_ + kC * LK, P_ = Q_ + kC * LK, X_ = P_ + kC * LCC,
                          Y_ = X_ + kC * LS, S_ = Y_ + kC * LS, G_ = S_ + DK * LS, R_ = G_ + kC;
     static constexpr int FLOATS = R_ + kC;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
-    static_assert(B_ % 4 == 0 && Q_ % 4 == 0 && P_ % 4 == 0 && X_ % 4 == 0 && Y_ % 4 == 0 && S_ % 4 == 0,
+    static_assert(K_ % 4 == 0 && Q_ % 4 == 0 && P_ % 4 == 0 && X_ % 4 == 0 && Y_ % 4 == 0 && S_ % 4 == 0,
                   "16-byte aligned regions");
 };
 
@@ -541,17 +482,21 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws 
     using L = StSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int SW = L::SW, NSL = DV / SW;
-    constexpr int RU = kC / 16, RS = DK / 16, CV = SW / 16;   // tiles: U C x SW, S DK x SW (CV columns)
+    using TU = ChainTiles<kC, SW>;   // U: C x SW
+    using TS = ChainTiles<DK, SW>;   // S: DK x SW
+    constexpr bool kEx = sizeof(TT) == 2;   // bf16 K is exact in tf32
     extern __shared__ __align__(16) float sm[];
-    float* sWt = sm + L::At_;
-    float* sK = sm + L::B_;
+    float* sW = sm + L::W_;
+    float* sK = sm + L::K_;
     float* sU = sm + L::X_;
     float* sS = sm + L::S_;
     float* sG = sm + L::G_;
     const int sl = blockIdx.x % NSL, h = (blockIdx.x / NSL) % Hv, seq = blockIdx.x / (NSL * Hv);
     if (seq >= nseq) return;
     const int hk = h / (Hv / Hqk), col0 = sl * SW;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16, cc = CV * tx;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, g = lane / 4, t = lane % 4;
+    const int um = 16 * (warp % TU::MT), un = (warp / TU::MT) * TU::NT;
+    const int sm0 = 16 * (warp % TS::MT), sn = (warp / TS::MT) * TS::NT;
     long long t0, t1;
     seq_range(cu, seq, T_len, t0, t1);
     const long long nch = (t1 - t0 + kC - 1) / kC, slot0 = t0 / kC + seq;
@@ -565,7 +510,7 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws 
         const long long tok0 = t0 + c * kC;
         const int n = (int)min((long long)kC, t1 - tok0);
         if (tid < kC) sG[tid] = ws.G[wi * D::G + tid];
-        ld_ws<DK, kC, kStThreads>(sWt, L::LCC, ws.Wt + wi * D::W, kC, tid);
+        ld_ws<kC, DK, kStThreads>(sW, L::LK, ws.W + wi * D::W, DK, tid);
         ld_ws<kC, SW, kStThreads>(sU, L::LS, ws.U + wi * D::U + col0, DV, tid);
         ld_in<TT, kC, DK, kStThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
         __syncthreads();
@@ -574,33 +519,32 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws 
             ws.S[wi * D::S + (size_t)i * DV + col0 + j] = sS[i * L::LS + j];
         }
         {   // U = U~ - W S to the workspace; sU holds diag(gamma_C / gamma) U (each thread its own elements)
-            float acc[RU][CV];
+            float acc[TU::NT][4];
             tile_zero(acc);
-            tile_tn<RU, CV, DK>(acc, sWt, L::LCC, sS, L::LS, ty * RU, cc);
+            mma_prod<TU::NT, DK, false, false>(acc, sW, L::LK, sS, L::LS, um, un, g, t);
+            const float GC = sG[kC - 1];
 #pragma unroll
-            for (int i = 0; i < RU; ++i) {
-                const int r = ty * RU + i;
-                const float kc = __expf(sG[kC - 1] - sG[r]);
+            for (int q = 0; q < TU::NT; ++q)
 #pragma unroll
-                for (int e = 0; e < CV; ++e) {
-                    const float u = sU[r * L::LS + cc + e] - acc[i][e];
-                    sU[r * L::LS + cc + e] = kc * u;
-                    ws.U[wi * D::U + (size_t)r * DV + col0 + cc + e] = u;
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(um, g, e), j = fcol(un + q, t, e);
+                    const float u = sU[r * L::LS + j] - acc[q][e];
+                    sU[r * L::LS + j] = __expf(GC - sG[r]) * u;
+                    ws.U[wi * D::U + (size_t)r * DV + col0 + j] = u;
                 }
-            }
         }
         __syncthreads();
-        {   // S <- gamma_C S + K^T diag(gamma_C / gamma) U
-            float acc[RS][CV];
+        {   // S <- gamma_C S + K^T diag(gamma_C / gamma) U  (each thread updates its own elements)
+            float acc[TS::NT][4];
             tile_zero(acc);
-            tile_tn<RS, CV, kC>(acc, sK, L::LK, sU, L::LS, ty * RS, cc);
+            mma_prod<TS::NT, kC, true, false, kEx, false>(acc, sK, L::LK, sU, L::LS, sm0, sn, g, t);
             const float gC = __expf(sG[kC - 1]);
 #pragma unroll
-            for (int i = 0; i < RS; ++i)
+            for (int q = 0; q < TS::NT; ++q)
 #pragma unroll
-                for (int e = 0; e < CV; ++e) {
-                    float& s = sS[(ty * RS + i) * L::LS + cc + e];
-                    s = fmaf(gC, s, acc[i][e]);
+                for (int e = 0; e < 4; ++e) {
+                    float& s = sS[frow(sm0, g, e) * L::LS + fcol(sn + q, t, e)];
+                    s = fmaf(gC, s, acc[q][e]);
                 }
         }
         __syncthreads();
@@ -616,10 +560,12 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
     using L = StSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int SW = L::SW, NSL = DV / SW;
-    constexpr int RU = kC / 16, RS = DK / 16, CV = SW / 16;
+    using TU = ChainTiles<kC, SW>;   // dU: C x SW
+    using TS = ChainTiles<DK, SW>;   // lam: DK x SW
+    constexpr bool kEx = sizeof(TT) == 2;   // bf16 K and dO are exact in tf32
     extern __shared__ __align__(16) float sm[];
-    float* sKt = sm + L::At_;
-    float* sW = sm + L::B_;
+    float* sW = sm + L::W_;
+    float* sK = sm + L::K_;
     float* sQ = sm + L::Q_;
     float* sP = sm + L::P_;
     float* sdO = sm + L::X_;
@@ -630,7 +576,9 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
     const int sl = blockIdx.x % NSL, h = (blockIdx.x / NSL) % Hv, seq = blockIdx.x / (NSL * Hv);
     if (seq >= nseq) return;
     const int hk = h / (Hv / Hqk), col0 = sl * SW;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16, cc = CV * tx;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, g = lane / 4, t = lane % 4;
+    const int um = 16 * (warp % TU::MT), un = (warp / TU::MT) * TU::NT;
+    const int sm0 = 16 * (warp % TS::MT), sn = (warp / TS::MT) * TS::NT;
     long long t0, t1;
     seq_range(cu, seq, T_len, t0, t1);
     const long long nch = (t1 - t0 + kC - 1) / kC, slot0 = t0 / kC + seq;
@@ -650,7 +598,7 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
         }
         ld_ws<kC, DK, kStThreads>(sW, L::LK, ws.W + wi * D::W, DK, tid);
         ld_ws<kC, kC, kStThreads>(sP, L::LCC, ws.P + wi * D::P, kC, tid);
-        ld_in_t<TT, kC, DK, kStThreads>(sKt, L::LCC, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+        ld_in<TT, kC, DK, kStThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
         ld_in<TT, kC, DK, kStThreads>(sQ, L::LK, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
         ld_in<TT, kC, SW, kStThreads>(sdO, L::LS, dout + (tok0 * Hv + h) * DV + col0, (size_t)Hv * DV, n, tid, vec);
         __syncthreads();
@@ -659,37 +607,46 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
             ws.dS[wi * D::dS + (size_t)i * DV + col0 + j] = sLam[i * L::LS + j];
         }
         {   // dU = diag(gamma_C / gamma) K lam + P^T dO
-            float kl[RU][CV], acc[RU][CV];
+            float kl[TU::NT][4], acc[TU::NT][4];
             tile_zero(kl);
             tile_zero(acc);
-            tile_tn<RU, CV, DK>(kl, sKt, L::LCC, sLam, L::LS, ty * RU, cc);
-            tile_tn<RU, CV, kC>(acc, sP, L::LCC, sdO, L::LS, ty * RU, cc);
+            mma_prod<TU::NT, DK, false, false, kEx, false>(kl, sK, L::LK, sLam, L::LS, um, un, g, t);
+            mma_prod<TU::NT, kC, true, false, false, kEx>(acc, sP, L::LCC, sdO, L::LS, um, un, g, t);
+            const float GC = sG[kC - 1];
 #pragma unroll
-            for (int i = 0; i < RU; ++i) {
-                const int r = ty * RU + i;
-                const float kc = __expf(sG[kC - 1] - sG[r]);
+            for (int qq = 0; qq < TU::NT; ++qq)
 #pragma unroll
-                for (int e = 0; e < CV; ++e) {
-                    const float du = fmaf(kc, kl[i][e], acc[i][e]);
-                    sdU[r * L::LS + cc + e] = du;
-                    ws.dU[wi * D::dU + (size_t)r * DV + col0 + cc + e] = du;
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(um, g, e), j = fcol(un + qq, t, e);
+                    const float du = fmaf(__expf(GC - sG[r]), kl[qq][e], acc[qq][e]);
+                    sdU[r * L::LS + j] = du;
+                    ws.dU[wi * D::dU + (size_t)r * DV + col0 + j] = du;
                 }
-            }
         }
         __syncthreads();
-        {   // lam <- gamma_C lam + Q^T diag(scale gamma) dO - W^T dU  (each thread rewrites its own elements)
-            float acc[RS][CV], neg[RS][CV];
+        {   // lam <- gamma_C lam + Q^T diag(scale gamma) dO - W^T dU  (each thread updates its own elements)
+            float acc[TS::NT][4], neg[TS::NT][4];
             tile_zero(acc);
             tile_zero(neg);
-            tile_tn<RS, CV, kC, true>(acc, sQ, L::LK, sdO, L::LS, ty * RS, cc, sQs);
-            tile_tn<RS, CV, kC>(neg, sW, L::LK, sdU, L::LS, ty * RS, cc);
+#pragma unroll 2
+            for (int k0 = 0; k0 < kC; k0 += 8) {
+                uint32_t ah[4], al[4];
+                frag_at_scaled(sQ, L::LK, sQs, sm0, k0, g, t, ah, al);
+#pragma unroll
+                for (int qq = 0; qq < TS::NT; ++qq) {
+                    uint32_t bh[2], bl[2];
+                    frag_b<kEx>(sdO, L::LS, 8 * (sn + qq), k0, g, t, bh, bl);
+                    mma_split<false, kEx>(acc[qq], ah, al, bh, bl);
+                }
+            }
+            mma_prod<TS::NT, kC, true, false>(neg, sW, L::LK, sdU, L::LS, sm0, sn, g, t);
             const float gC = __expf(sG[kC - 1]);
 #pragma unroll
-            for (int i = 0; i < RS; ++i)
+            for (int qq = 0; qq < TS::NT; ++qq)
 #pragma unroll
-                for (int e = 0; e < CV; ++e) {
-                    float& l = sLam[(ty * RS + i) * L::LS + cc + e];
-                    l = fmaf(gC, l, acc[i][e] - neg[i][e]);
+                for (int e = 0; e < 4; ++e) {
+                    float& l = sLam[frow(sm0, g, e) * L::LS + fcol(sn + qq, t, e)];
+                    l = fmaf(gC, l, acc[qq][e] - neg[qq][e]);
                 }
         }
         __syncthreads();
@@ -728,11 +685,6 @@ struct LoSmem {
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
     static_assert(Q_ % 4 == 0 && KK_ % 4 == 0 && T_ % 4 == 0 && X_ % 4 == 0 && DVB_ % 4 == 0, "aligned regions");
 };
-
-// Fragment coordinates of accumulator element e of n-tile nb: row row0 + g (+ 8 for e >= 2),
-// column 8 nb + 2 t + (e & 1).
-__device__ __forceinline__ int frow(int row0, int g, int e) { return row0 + g + (e >= 2 ? 8 : 0); }
-__device__ __forceinline__ int fcol(int nb, int t, int e) { return 8 * nb + 2 * t + (e & 1); }
 
 // dst[r] += full sum of row r, given this thread's partial sums p0 (row row0 + g) and p1 (row row0 + g + 8):
 // a quad sum over t, then the four column-group warps of the row tile in a fixed order.
@@ -1097,7 +1049,6 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     ws.T = reinterpret_cast<float*>(base + Lw.T_off);
     ws.P = reinterpret_cast<float*>(base + Lw.P_off);
     ws.W = reinterpret_cast<float*>(base + Lw.W_off);
-    ws.Wt = reinterpret_cast<float*>(base + Lw.Wt_off);
     ws.U = reinterpret_cast<float*>(base + Lw.U_off);
     ws.G = reinterpret_cast<float*>(base + Lw.G_off);
     ws.S = reinterpret_cast<float*>(base + Lw.S_off);
@@ -1175,7 +1126,6 @@ BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool p
     take(L.T_off, (size_t)kC * kC);
     take(L.P_off, (size_t)kC * kC);
     take(L.W_off, (size_t)kC * dk);
-    take(L.Wt_off, (size_t)kC * dk);
     take(L.U_off, (size_t)kC * dv);
     take(L.G_off, (size_t)kC);
     take(L.S_off, (size_t)dk * dv);

@@ -104,12 +104,12 @@ struct BackwardArgs {
     cudaStream_t stream;
 };
 
-// Workspace of the backward pass: per (chunk slot, value head) fp32 arrays T, P (C x C), W and W^T
-// (C x dk), U (C x dv), G (C), chunk-start state S and its adjoint dS (dk x dv), dU (C x dv); byte
-// offsets, 256-byte aligned.  `slots` = ceil(tokens / C) + sequences.
+// Workspace of the backward pass: per (chunk slot, value head) fp32 arrays T, P (C x C), W (C x dk),
+// U (C x dv), G (C), chunk-start state S and its adjoint dS (dk x dv), dU (C x dv); byte offsets,
+// 256-byte aligned.  `slots` = ceil(tokens / C) + sequences.
 struct BwdLayout {
     long long slots;
-    size_t T_off, P_off, W_off, Wt_off, U_off, G_off, S_off, dS_off, dU_off, total;
+    size_t T_off, P_off, W_off, U_off, G_off, S_off, dS_off, dU_off, total;
 };
 BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed);
 cudaError_t launch_backward(const BackwardArgs& a);
