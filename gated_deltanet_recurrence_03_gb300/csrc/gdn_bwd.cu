@@ -27,35 +27,9 @@ namespace gdn {
 namespace {
 
 constexpr int kC = 64;      // chunk length
-constexpr int kLC = kC + 1; // padded row length of C x C matrices in shared memory
+constexpr int kLCC = kC + 4; // C x C matrices in shared memory: rows 4 banks apart (conflict-free fragments)
 
-// ---------------------------------------------------------------- register-tile products
-// acc[i][m] += sum_{k<K} opA(row0 + i, k) * ks[k] * opB(k, tx + 16 m)   (ks[k] = 1 unless KS), where
-//   opA(r, k) = AT ? A[k * lda + r] : A[r * lda + k],   opB(k, n) = BT ? B[n * ldb + k] : B[k * ldb + n].
-// Threads (ty, tx = tid % 16) tile the output: rows row0 = ty * RM .. + RM - 1, columns tx + 16 m.  All
-// shared-memory leading dimensions are 1 mod 32, so both operand forms are free of bank conflicts.
-template <int RM, int CN, bool AT, bool BT, int K, bool KS = false>
-__device__ __forceinline__ void tile_mm(float (&acc)[RM][CN], const float* __restrict__ A, int lda,
-                                        const float* __restrict__ B, int ldb, int row0, int tx,
-                                        const float* __restrict__ ks = nullptr) {
-#pragma unroll 8
-    for (int k = 0; k < K; ++k) {
-        float a[RM], b[CN];
-        const float s = KS ? ks[k] : 1.f;
-#pragma unroll
-        for (int i = 0; i < RM; ++i) {
-            a[i] = AT ? A[k * lda + row0 + i] : A[(row0 + i) * lda + k];
-            if (KS) a[i] *= s;
-        }
-#pragma unroll
-        for (int m = 0; m < CN; ++m) b[m] = BT ? B[(tx + 16 * m) * ldb + k] : B[k * ldb + tx + 16 * m];
-#pragma unroll
-        for (int i = 0; i < RM; ++i)
-#pragma unroll
-            for (int m = 0; m < CN; ++m) acc[i][m] = fmaf(a[i], b[m], acc[i][m]);
-    }
-}
-
+// ---------------------------------------------------------------- register tiles
 template <int RM, int CN>
 __device__ __forceinline__ void tile_zero(float (&acc)[RM][CN]) {
 #pragma unroll
@@ -130,6 +104,15 @@ __device__ __forceinline__ void frag_at(const float* X, int ld, int row0, int k0
     split_x<EXACT>(X[(k0 + t) * ld + row0 + g + 8], hi[1], lo[1]);
     split_x<EXACT>(X[(k0 + t + 4) * ld + row0 + g], hi[2], lo[2]);
     split_x<EXACT>(X[(k0 + t + 4) * ld + row0 + g + 8], hi[3], lo[3]);
+}
+// A fragment of a row-major A with column k scaled by ks[k] (A diag(ks)).
+__device__ __forceinline__ void frag_a_scaled(const float* A, int ld, const float* ks, int row0, int k0, int g, int t,
+                                              uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+    const float s0 = ks[k0 + t], s1 = ks[k0 + t + 4];
+    split_tf32(s0 * A[(row0 + g) * ld + k0 + t], hi[0], lo[0]);
+    split_tf32(s0 * A[(row0 + g + 8) * ld + k0 + t], hi[1], lo[1]);
+    split_tf32(s1 * A[(row0 + g) * ld + k0 + t + 4], hi[2], lo[2]);
+    split_tf32(s1 * A[(row0 + g + 8) * ld + k0 + t + 4], hi[3], lo[3]);
 }
 // The same with column k of A (row k of X) scaled by ks[k] (a diagonal matrix between the factors).
 __device__ __forceinline__ void frag_at_scaled(const float* X, int ld, const float* ks, int row0, int k0, int g, int t,
@@ -276,14 +259,27 @@ struct WsDims {
                             G = kC, S = (size_t)DK * DV, dS = (size_t)DK * DV, dU = (size_t)kC * DV;
 };
 
+// Fragment coordinates of accumulator element e of n-tile nb: row row0 + g (+ 8 for e >= 2),
+// column 8 nb + 2 t + (e & 1).
+__device__ __forceinline__ int frow(int row0, int g, int e) { return row0 + g + (e >= 2 ? 8 : 0); }
+__device__ __forceinline__ int fcol(int nb, int t, int e) { return 8 * nb + 2 * t + (e & 1); }
+
+// An M x N product over the 8 warps: the M / 16 row tiles first, the N / 8 column tiles split among
+// the warps that share a row tile.  Warp w: row tile w % MT, column tiles (w / MT) NT .. + NT - 1.
+template <int M, int N>
+struct ChainTiles {
+    static constexpr int MT = M / 16, WPM = 8 / MT, NT = (N / 8) / WPM;
+    static_assert(MT >= 1 && MT <= 8 && 8 % MT == 0 && (N / 8) % WPM == 0 && NT >= 1, "tile split");
+};
+
 // ---------------------------------------------------------------- kernel 1: WY factors per chunk
 constexpr int kWyThreads = 256;
 
 template <int DK, int DV>
 struct WySmem {
-    static constexpr int LK = DK + 1, LQV = (DK > DV ? DK : DV) + 1;
-    static constexpr int K_ = 0, QV_ = K_ + kC * LK, KK_ = QV_ + kC * LQV, QK_ = KK_ + kC * kLC,
-                         L_ = QK_ + kC * kLC, T_ = L_ + kC * kLC, Y_ = T_ + kC * kLC, VEC_ = Y_ + 3 * 256;
+    static constexpr int LK = DK + 4, LQV = (DK > DV ? DK : DV) + 4;   // = 4 mod 32
+    static constexpr int K_ = 0, QV_ = K_ + kC * LK, KK_ = QV_ + kC * LQV, QK_ = KK_ + kC * kLCC,
+                         L_ = QK_ + kC * kLCC, T_ = L_ + kC * kLCC, Y_ = T_ + kC * kLCC, VEC_ = Y_ + 3 * 256;
     static constexpr int FLOATS = VEC_ + 4 * kC;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
 };
@@ -313,24 +309,22 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
     int seq, n;
     long long tok0;
     if (!slot_chunk(cu, nseq, T_len, slot, seq, tok0, n)) return;
-    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, lg = lane / 4, lt = lane % 4;   // fragment (g, t)
+    constexpr bool kEx = sizeof(TT) == 2;   // bf16 K, Q, V are exact in tf32
 
     ld_in<TT, kC, DK, kWyThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
     ld_in<TT, kC, DK, kWyThreads>(sQV, L::LQV, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
     __syncthreads();
-    {   // Gram matrices K K^T and Q K^T (C x C: 4 rows x 4 columns per thread)
-        float kk[4][4], qk[4][4];
+    {   // Gram matrices K K^T and Q K^T on tensor cores (both operands exact in tf32 for bf16 inputs)
+        using TG = ChainTiles<kC, kC>;
+        float kk[TG::NT][4], qk[TG::NT][4];
         tile_zero(kk);
         tile_zero(qk);
-        tile_mm<4, 4, false, true, DK>(kk, sK, L::LK, sK, L::LK, ty * 4, tx);
-        tile_mm<4, 4, false, true, DK>(qk, sQV, L::LQV, sK, L::LK, ty * 4, tx);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                sKK[(ty * 4 + i) * kLC + tx + 16 * m] = kk[i][m];
-                sQK[(ty * 4 + i) * kLC + tx + 16 * m] = qk[i][m];
-            }
+        const int gm = 16 * (warp % TG::MT), gn = (warp / TG::MT) * TG::NT;
+        mma_prod<TG::NT, DK, false, true, kEx, kEx>(kk, sK, L::LK, sK, L::LK, gm, gn, lg, lt);
+        mma_prod<TG::NT, DK, false, true, kEx, kEx>(qk, sQV, L::LQV, sK, L::LK, gm, gn, lg, lt);
+        store_frag<TG::NT>(sKK, kLCC, kk, gm, gn, lg, lt, 1.f);
+        store_frag<TG::NT>(sQK, kLCC, qk, gm, gn, lg, lt, 1.f);
     }
     __syncthreads();
 
@@ -365,8 +359,8 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
         for (int idx = tid; idx < kC * kC; idx += kWyThreads) {
             const int r = idx / kC, s = idx % kC;
             const float d = s <= r ? __expf(sG[r] - sG[s]) : 0.f;
-            ws.P[wi * D::P + idx] = scale * d * sQK[r * kLC + s];
-            sL[r * kLC + s] = s < r ? sBeta[r] * d * sKK[r * kLC + s] : 0.f;
+            ws.P[wi * D::P + idx] = scale * d * sQK[r * kLCC + s];
+            sL[r * kLCC + s] = s < r ? sBeta[r] * d * sKK[r * kLCC + s] : 0.f;
         }
         __syncthreads();
         {   // T = (I + L)^{-1} in 16 x 16 blocks: each diagonal block by forward substitution (one thread
@@ -379,15 +373,15 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
                 for (int r = 0; r < 16; ++r) {
                     float acc = r == c ? 1.f : 0.f;
 #pragma unroll
-                    for (int q = 0; q < r; ++q) acc = fmaf(-sL[(o + r) * kLC + o + q], x[q], acc);
+                    for (int q = 0; q < r; ++q) acc = fmaf(-sL[(o + r) * kLCC + o + q], x[q], acc);
                     x[r] = acc;
-                    sT[(o + r) * kLC + o + c] = acc;
+                    sT[(o + r) * kLCC + o + c] = acc;
                 }
             } else {   // blocks above the diagonal are zero
                 for (int idx = tid - kC; idx < 6 * 256; idx += kWyThreads - kC) {
                     const int blk = idx / 256, e = idx % 256;
                     const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2), bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    sT[(16 * bi + e / 16) * kLC + 16 * bj + e % 16] = 0.f;
+                    sT[(16 * bi + e / 16) * kLCC + 16 * bj + e % 16] = 0.f;
                 }
             }
             __syncthreads();
@@ -399,7 +393,7 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
                     for (int bl = bj; bl < bi; ++bl)
 #pragma unroll
                         for (int q = 0; q < 16; ++q)
-                            acc = fmaf(sL[(16 * bi + r) * kLC + 16 * bl + q], sT[(16 * bl + q) * kLC + 16 * bj + c], acc);
+                            acc = fmaf(sL[(16 * bi + r) * kLCC + 16 * bl + q], sT[(16 * bl + q) * kLCC + 16 * bj + c], acc);
                     sY[idx] = acc;
                 }
                 __syncthreads();
@@ -408,41 +402,60 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
                     float acc = 0.f;
 #pragma unroll
                     for (int q = 0; q < 16; ++q)
-                        acc = fmaf(sT[(16 * bi + r) * kLC + 16 * bi + q], sY[bj * 256 + q * 16 + c], acc);
-                    sT[(16 * bi + r) * kLC + 16 * bj + c] = -acc;
+                        acc = fmaf(sT[(16 * bi + r) * kLCC + 16 * bi + q], sY[bj * 256 + q * 16 + c], acc);
+                    sT[(16 * bi + r) * kLCC + 16 * bj + c] = -acc;
                 }
                 __syncthreads();
             }
         }
-        for (int idx = tid; idx < kC * kC; idx += kWyThreads) ws.T[wi * D::T + idx] = sT[(idx / kC) * kLC + idx % kC];
-        {   // W = T diag(beta gamma) K
-            constexpr int CN = DK / 16;
-            float acc[4][CN];
+        for (int idx = tid; idx < kC * kC; idx += kWyThreads) ws.T[wi * D::T + idx] = sT[(idx / kC) * kLCC + idx % kC];
+        {   // W = T diag(beta gamma) K on tensor cores (K exact for bf16 inputs)
+            using TW = ChainTiles<kC, DK>;
+            float acc[TW::NT][4];
             tile_zero(acc);
-            tile_mm<4, CN, false, false, kC, true>(acc, sT, kLC, sK, L::LK, ty * 4, tx, sBG);
+            const int wm = 16 * (warp % TW::MT), wn = (warp / TW::MT) * TW::NT;
+#pragma unroll 2
+            for (int k0 = 0; k0 < kC; k0 += 8) {
+                uint32_t ah[4], al[4];
+                frag_a_scaled(sT, kLCC, sBG, wm, k0, lg, lt, ah, al);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int qq = 0; qq < TW::NT; ++qq) {
+                    uint32_t bh[2], bl[2];
+                    frag_b<kEx>(sK, L::LK, 8 * (wn + qq), k0, lg, lt, bh, bl);
+                    mma_split<false, kEx>(acc[qq], ah, al, bh, bl);
+                }
+            }
 #pragma unroll
-                for (int m = 0; m < CN; ++m) ws.W[wi * D::W + (size_t)(ty * 4 + i) * DK + tx + 16 * m] = acc[i][m];
+            for (int qq = 0; qq < TW::NT; ++qq)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    ws.W[wi * D::W + (size_t)frow(wm, lg, e) * DK + fcol(wn + qq, lt, e)] = acc[qq][e];
         }
-        {   // U~ = T diag(beta) V
-            constexpr int CN = DV / 16;
-            float acc[4][CN];
+        {   // U~ = T diag(beta) V on tensor cores (V exact for bf16 inputs)
+            using TV = ChainTiles<kC, DV>;
+            float acc[TV::NT][4];
             tile_zero(acc);
-            tile_mm<4, CN, false, false, kC, true>(acc, sT, kLC, sQV, L::LQV, ty * 4, tx, sBeta);
+            const int vm = 16 * (warp % TV::MT), vn = (warp / TV::MT) * TV::NT;
+#pragma unroll 2
+            for (int k0 = 0; k0 < kC; k0 += 8) {
+                uint32_t ah[4], al[4];
+                frag_a_scaled(sT, kLCC, sBeta, vm, k0, lg, lt, ah, al);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int qq = 0; qq < TV::NT; ++qq) {
+                    uint32_t bh[2], bl[2];
+                    frag_b<kEx>(sQV, L::LQV, 8 * (vn + qq), k0, lg, lt, bh, bl);
+                    mma_split<false, kEx>(acc[qq], ah, al, bh, bl);
+                }
+            }
 #pragma unroll
-                for (int m = 0; m < CN; ++m) ws.U[wi * D::U + (size_t)(ty * 4 + i) * DV + tx + 16 * m] = acc[i][m];
+            for (int qq = 0; qq < TV::NT; ++qq)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    ws.U[wi * D::U + (size_t)frow(vm, lg, e) * DV + fcol(vn + qq, lt, e)] = acc[qq][e];
         }
         __syncthreads();
     }
 }
-
-// Fragment coordinates of accumulator element e of n-tile nb: row row0 + g (+ 8 for e >= 2),
-// column 8 nb + 2 t + (e & 1).
-__device__ __forceinline__ int frow(int row0, int g, int e) { return row0 + g + (e >= 2 ? 8 : 0); }
-__device__ __forceinline__ int fcol(int nb, int t, int e) { return 8 * nb + 2 * t + (e & 1); }
 
 // ---------------------------------------------------------------- kernels 2 and 3: the chunk chains
 // Both chains run their products on tf32 tensor cores with the three-product split (fp32 accuracy),
@@ -451,14 +464,6 @@ constexpr int kStThreads = 256;
 
 template <int DV>
 constexpr int slice_width() { return DV < 64 ? DV : 64; }
-
-// An M x N product over the 8 warps: the M / 16 row tiles first, the N / 8 column tiles split among
-// the warps that share a row tile.  Warp w: row tile w % MT, column tiles (w / MT) NT .. + NT - 1.
-template <int M, int N>
-struct ChainTiles {
-    static constexpr int MT = M / 16, WPM = 8 / MT, NT = (N / 8) / WPM;
-    static_assert(MT >= 1 && MT <= 8 && 8 % MT == 0 && (N / 8) % WPM == 0 && NT >= 1, "tile split");
-};
 
 template <int DK, int DV>
 struct StSmem {
@@ -666,7 +671,6 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
 // dk stay in those fragments across the value heads of the query/key head.
 constexpr int kLoThreads = 512;   // 16 warps
 constexpr int kDvc = 32;          // value columns per pass over dv
-constexpr int kLCC = kC + 4;      // C x C matrices: rows 4 banks apart (conflict-free row-major fragments)
 
 template <int DK, int DV>
 struct LoSmem {
