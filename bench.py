@@ -576,13 +576,14 @@ def run_gpu(args):
                                     "algorithmic_bytes": gate_bytes}},
         "backward": {"workload": "prefill_gqa_8k backward: gradients w.r.t. q, k, v, g, beta, S0 from dout and "
                                  "dS_final through the chunked form (64-token chunks: WY factors, forward and "
-                                 "adjoint chunk chains, chunk-local gradients; fp32, dv contractions on tf32 "
-                                 "tensor cores with a three-product split)",
+                                 "adjoint chunk chains, chunk-local gradients; fp32 accuracy, the products on tf32 "
+                                 "tensor cores with split operands)",
                      "value": round(world * tokens / (bwd_ms / 1e3), 1), "unit": "tokens/s",
                      "ms_per_step": round(bwd_ms, 4), "steps": bwd_steps, "gpu_launches": 4 * bwd_steps,
                      "roofline": {"bound": "alu", "achieved": round(bwd_tf, 2), "peak": round(alu_peak, 1),
                                   "unit": "TFLOP/s", "frac": round(bwd_tf / alu_peak, 4),
-                                  "peak_source": "fp32 FMA lanes x 2 x 2070 MHz (unit counts)"}},
+                                  "peak_source": "fp32 FMA lanes x 2 x 2070 MHz (unit counts): the fp32 work's own "
+                                                 "peak; the products run as split tf32 MMAs"}},
         "decode": {"workload": "decode_256x512: 256 sequences x 32 V heads (16 QK heads), d=128, 512 steps, "
                                "fp32 state 512 MiB resident, one CUDA graph per 512-step pass",
                    "value": round(world / (dec_ms / 1e3), 1), "unit": "steps/s",
