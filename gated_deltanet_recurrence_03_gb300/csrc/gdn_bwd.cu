@@ -670,17 +670,38 @@ bwd_state_adj_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const T
 // n-tiles of 8 from (w / 4) dk / 32; of a C x C product, n-tiles 2 (w / 4) and 2 (w / 4) + 1.  dq and
 // dk stay in those fragments across the value heads of the query/key head.
 constexpr int kLoThreads = 512;   // 16 warps
-constexpr int kDvc = 32;          // value columns per pass over dv
+constexpr int kDvc = 16;          // value columns per pass over dv (two buffer sets, the next pass loading)
+
+__device__ __forceinline__ void cp_async16(float* smem, const float* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// fp32 workspace block rows [0, ROWS) x [0, WIDTH) to shared memory (leading dimension ld) by
+// asynchronous 16-byte copies (both sides 16-byte aligned).
+template <int ROWS, int WIDTH, int NT>
+__device__ __forceinline__ void cp_ws(float* dst, int ld, const float* src, size_t stride, int tid) {
+    constexpr int V = WIDTH / 4, TOTAL = ROWS * V;
+    for (int idx = tid; idx < TOTAL; idx += NT) {
+        const int r = idx / V, c = (idx % V) * 4;
+        cp_async16(dst + r * ld + c, src + (size_t)r * stride + c);
+    }
+}
 
 template <int DK, int DV>
 struct LoSmem {
-    // LK, LD = 4 mod 32 as well
+    // LK = 4 mod 32; LD = 20 (rows 20 banks apart: row-major fragment loads still hit 32 banks)
     static constexpr int LK = DK + 4, LD = kDvc + 4;
     static constexpr int K_ = 0, Q_ = K_ + kC * LK, KK_ = Q_ + kC * LK, QK_ = KK_ + kC * kLCC,
                          T_ = QK_ + kC * kLCC, X_ = T_ + kC * kLCC, DVB_ = X_ + kC * kLCC;
-    // dv pass buffers (dU, U, dO, V: C x 32; S, lam: DK x 32); afterwards dW (C x DK) over them
-    static constexpr int dU_ = DVB_, U_ = dU_ + kC * LD, dO_ = U_ + kC * LD, V_ = dO_ + kC * LD, S_ = V_ + kC * LD,
-                         Lam_ = S_ + DK * LD, DVB_END = Lam_ + DK * LD, DW_END = DVB_ + kC * LK;
+    // two sets of dv pass buffers (dU, U, dO, V: C x 16; S, lam: DK x 16), offsets within a set; afterwards
+    // dW (C x DK) over them
+    static constexpr int dU_ = 0, U_ = kC * LD, dO_ = 2 * kC * LD, V_ = 3 * kC * LD, S_ = 4 * kC * LD,
+                         Lam_ = S_ + DK * LD, PS = Lam_ + DK * LD, DVB_END = DVB_ + 2 * PS, DW_END = DVB_ + kC * LK;
     static constexpr int VEC_ = DVB_END > DW_END ? DVB_END : DW_END;
     // G, beta, dG, dbeta, row scratch, h, reduction scratch [8][C], warp sums
     static constexpr int G_ = VEC_, Beta_ = G_ + kC, dG_ = Beta_ + kC, dB_ = dG_ + kC, Row_ = dB_ + kC,
@@ -765,12 +786,6 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     float* sQK = sm + L::QK_;
     float* sT = sm + L::T_;
     float* sX = sm + L::X_;
-    float* sdU = sm + L::dU_;
-    float* sU = sm + L::U_;
-    float* sdO = sm + L::dO_;
-    float* sV = sm + L::V_;
-    float* sS = sm + L::S_;
-    float* sLam = sm + L::Lam_;
     float* sDW = sm + L::DVB_;
     float* sG = sm + L::G_;
     float* sBeta = sm + L::Beta_;
@@ -822,14 +837,55 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
         tile_zero(fP);
         tile_zero(fTv);
         float zv0 = 0.f, zv1 = 0.f, ss = 0.f;
-        for (int jc = 0; jc < DV; jc += kDvc) {
-            __syncthreads();
-            ld_ws<kC, kDvc, kLoThreads>(sdU, L::LD, ws.dU + wi * D::dU + jc, DV, tid);
-            ld_ws<kC, kDvc, kLoThreads>(sU, L::LD, ws.U + wi * D::U + jc, DV, tid);
-            ld_in<TT, kC, kDvc, kLoThreads>(sdO, L::LD, dout + (tok0 * Hv + h) * DV + jc, (size_t)Hv * DV, n, tid, vec);
-            ld_in<TT, kC, kDvc, kLoThreads>(sV, L::LD, v + (tok0 * Hv + h) * DV + jc, (size_t)Hv * DV, n, tid, vec);
-            ld_ws<DK, kDvc, kLoThreads>(sS, L::LD, ws.S + wi * D::S + jc, DV, tid);
-            ld_ws<DK, kDvc, kLoThreads>(sLam, L::LD, ws.dS + wi * D::dS + jc, DV, tid);
+        // Passes over dv, double-buffered: while pass p computes, the fp32 workspace blocks of pass p + 1
+        // arrive by cp.async in the other buffer set and its dO / V rows (16-byte pieces, one per thread)
+        // wait in registers.
+        constexpr int NP = DV / kDvc;
+        constexpr int EPV = 16 / (int)sizeof(TT), PPR = kDvc / EPV, PIECES = kC * PPR;   // per dO or V block
+        static_assert(2 * PIECES <= kLoThreads, "one input piece per thread");
+        const TT* in_base[2] = {dout + (tok0 * Hv + h) * DV, v + (tok0 * Hv + h) * DV};
+        const int pw = tid / PIECES, pr = (tid % PIECES) / PPR, pc = (tid % PIECES) % PPR * EPV;
+        uint4 piece = make_uint4(0u, 0u, 0u, 0u);
+        auto issue_pass = [&](int p) {   // fp32 blocks of pass p into set p & 1; its dO / V piece into registers
+            float* B = sm + L::DVB_ + (p & 1) * L::PS;
+            const int jc = p * kDvc;
+            cp_ws<kC, kDvc, kLoThreads>(B + L::dU_, L::LD, ws.dU + wi * D::dU + jc, DV, tid);
+            cp_ws<kC, kDvc, kLoThreads>(B + L::U_, L::LD, ws.U + wi * D::U + jc, DV, tid);
+            cp_ws<DK, kDvc, kLoThreads>(B + L::S_, L::LD, ws.S + wi * D::S + jc, DV, tid);
+            cp_ws<DK, kDvc, kLoThreads>(B + L::Lam_, L::LD, ws.dS + wi * D::dS + jc, DV, tid);
+            cp_async_commit();
+            piece = make_uint4(0u, 0u, 0u, 0u);
+            if (vec && pw < 2 && pr < n)
+                piece = *reinterpret_cast<const uint4*>(in_base[pw] + (size_t)pr * Hv * DV + jc + pc);
+        };
+        issue_pass(0);
+        for (int p = 0; p < NP; ++p) {
+            const int jc = p * kDvc;
+            float* B = sm + L::DVB_ + (p & 1) * L::PS;
+            float* sdU = B + L::dU_;
+            float* sU = B + L::U_;
+            float* sdO = B + L::dO_;
+            float* sV = B + L::V_;
+            float* sS = B + L::S_;
+            float* sLam = B + L::Lam_;
+            if (vec) {   // this pass's dO / V piece, converted to fp32
+                if (pw < 2) {
+                    float f[EPV];
+                    unpack16(piece, f);
+                    float* d = (pw == 0 ? sdO : sV) + pr * L::LD + pc;
+#pragma unroll
+                    for (int x = 0; x < EPV; ++x) d[x] = f[x];
+                }
+            } else {
+                ld_in<TT, kC, kDvc, kLoThreads>(sdO, L::LD, in_base[0] + jc, (size_t)Hv * DV, n, tid, false);
+                ld_in<TT, kC, kDvc, kLoThreads>(sV, L::LD, in_base[1] + jc, (size_t)Hv * DV, n, tid, false);
+            }
+            if (p + 1 < NP) {
+                issue_pass(p + 1);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
             __syncthreads();
             for (int idx = tid; idx < DK * kDvc; idx += kLoThreads) {
                 const int i = idx / kDvc, j = idx % kDvc;
@@ -862,7 +918,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 #pragma unroll
                 for (int qq = 0; qq < NTW; ++qq) mma_3xtf32(fY[qq], ah, al, sh[qq], sl[qq]);
             }
-            {   // dV = diag(beta) T^T dU (this pass's columns 8 wg .. 8 wg + 7);  dbeta += rowsum(T^T dU o V)
+            if (wg < kDvc / 8) {   // dV = diag(beta) T^T dU (columns 8 wg .. 8 wg + 7);  dbeta += rowsum(T^T dU o V)
                 float z[1][4];
                 tile_zero(z);
                 mma_prod<1, kC, true, false>(z, sT, kLCC, sdU, L::LD, row0, wg, g, t);
@@ -880,6 +936,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                     o[1] = sBeta[rb] * z[0][3];
                 }
             }
+            __syncthreads();   // this set is free for pass p + 2
         }
         {   // gamma_C <lam, S>: warp sums of ss (added below)
             float x = ss;
@@ -887,7 +944,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
             if (lane == 0) sRed[warp] = x;
         }
-        frag_rows_add(zv0, zv1, sScr, sdB, tid, row0, wg, g, t);   // its barriers also end the dv passes
+        frag_rows_add(zv0, zv1, sScr, sdB, tid, row0, wg, g, t);
         store_frag<NTW>(sDW, L::LK, fW, row0, nb0, g, t, -1.f);      // dW = -dU S^T (over the pass buffers)
         // dQ = scale diag(gamma) (dO S^T) in fX;  dG_r += scale gamma_r (dO S^T)_r . q_r
         // dK = diag(gamma_C / gamma) (U lam^T) in fY;  with h_r = (gamma_C / gamma_r) (U lam^T)_r . k_r:
