@@ -529,6 +529,31 @@ def run_gpu(args):
     dl_bytes = (2 * wd.B * wd.Hv * wd.dk * wd.dv * 4 + wd.B * Cc * 2 + 2 * wd.B * 3 * Cc * 2
                 + 2 * wd.B * wd.Hv * 2 + 2 * wd.B * wd.Hv * wd.dv * 2)
     del projd, zd, outd
+
+    # ---- the small character-LM workload (4 x 512 tokens, 4 / 4 heads, d = 32, bf16, S0 = 0, S_final
+    # returned): a latency-bound call, timed over many back-to-back calls
+    wc = gi.WORKLOADS["charlm_bf16"]
+    xc = device_inputs_random(torch, dev, wc, seed=5)
+    wsc = torch.empty(max(1, gdn.workspace_size(wc.B, wc.T, wc.Hqk, wc.Hv, wc.dk, wc.dv)), dtype=torch.uint8,
+                      device=dev)
+    outc = torch.empty_like(xc["v"])
+    Sfc = torch.empty(wc.B, wc.Hv, wc.dk, wc.dv, device=dev)
+
+    def charlm_call():
+        gdn.gdn_chunk_fwd(xc["q"], xc["k"], xc["v"], xc["g"], xc["beta"], None, out=outc, S_final=Sfc,
+                          workspace=wsc, chunk=wc.chunk)
+
+    for _ in range(10):
+        charlm_call()
+    charlm_reps = 200
+    barrier()
+    t0.record(stream)
+    for _ in range(charlm_reps):
+        charlm_call()
+    t1.record(stream)
+    barrier()
+    charlm_ms = max_ms(t0.elapsed_time(t1)) / charlm_reps
+    gdn.check_device_status()
     clocks.stop()
 
     if rank != 0:
@@ -593,6 +618,10 @@ def run_gpu(args):
                                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(dec_gbs / peaks["hbm_gbs"], 4),
                                 "traffic": traffic_for("decode_step_kernel"),
                                 "algorithmic_bytes": dec_bytes, "peak_source": f"{peak_src} copy bandwidth"}},
+        "charlm": {"workload": "charlm_bf16: B=4 x T=512 tokens, 4 / 4 heads, dk=dv=32, bf16, S0 = 0, final state "
+                               "returned (chunked kernels on split-tf32 MMAs: d = 32 is off the tcgen05 tile)",
+                   "value": round(world * wc.B * wc.T / (charlm_ms / 1e3), 1), "unit": "tokens/s",
+                   "us_per_call": round(charlm_ms * 1e3, 2), "calls": charlm_reps, "bound": "latency"},
         "decode_layer": {"workload": "decode_256x512 heads through the layer's recurrent core: 3 conv steps (K=4) "
                                      "of the packed 8192-channel projection with their caches, then the recurrent step "
                                      "with raw gates, l2 norm and the output gate; 128 steps per CUDA graph",

@@ -135,14 +135,29 @@ const char* gdn_status_string(gdn_status_t s) {
     return "unknown status";
 }
 
+}  // extern "C"
+
+namespace {
+// The chunked prefill takes the token loop's inputs as they are: no in-kernel normalisation or raw
+// gates (the output gate is a separate pass after either prefill).
+bool chunked_prefill_eligible(int dk, int dv, unsigned flags) {
+    return (flags & (GDN_NORMALIZE_QK | GDN_RAW_GATES)) == 0 && (dk == 32 || dk == 64 || dk == 128) &&
+           (dv == 32 || dv == 64 || dv == 128);
+}
+}  // namespace
+
+extern "C" {
+
 size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts) {
     const gdn_opts_t o = resolve(opts);
     if (B < 0 || T < 0 || Hqk <= 0 || Hv <= 0 || Hv % Hqk) return 0;
-    if (!tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk, o.flags)) return 0;
     const bool packed = o.cu_seqlens != nullptr;
     const int nseq = packed ? o.num_seqs : B;
     if (nseq <= 0 || T == 0) return 0;
-    return tc_prefill_workspace_bytes(B, T, Hv, nseq, packed);
+    if (tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk, o.flags))
+        return tc_prefill_workspace_bytes(B, T, Hv, nseq, packed);
+    if (chunked_prefill_eligible(dk, dv, o.flags)) return chunked_prefill_workspace_bytes(B, T, Hv, dk, dv, nseq, packed);
+    return 0;
 }
 
 gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
@@ -209,7 +224,18 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const vo
             e = launch_output_gate(out, o.z, o.norm_weight, o.norm_eps, (long long)B * T * Hv, dv, o.dtype, stream);
             record(o, 3, stream);
         }
-    } else {
+    } else if (chunked_prefill_eligible(dk, dv, o.flags) && o.workspace &&
+               (reinterpret_cast<uintptr_t>(o.workspace) & 255u) == 0 &&
+               o.workspace_bytes >= chunked_prefill_workspace_bytes(B, T, Hv, dk, dv, nseq, packed)) {
+        // chunked form on the split-tf32 tensor-core kernels (fp32 accuracy)
+        record(o, 0, stream);
+        e = launch_chunked_prefill(a);
+        record(o, 1, stream);
+        if (e == cudaSuccess && (o.flags & GDN_OUTPUT_GATE)) {
+            e = launch_output_gate(out, o.z, o.norm_weight, o.norm_eps, (long long)B * T * Hv, dv, o.dtype, stream);
+            record(o, 2, stream);
+        }
+    } else {   // no (or too small a) workspace, or a front-end option: the token-serial kernel
         record(o, 0, stream);
         e = launch_recurrent_prefill(a);
         record(o, 1, stream);
@@ -328,7 +354,7 @@ size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, i
     const bool packed = o.cu_seqlens != nullptr;
     const int nseq = packed ? o.num_seqs : B;
     if (nseq <= 0) return 0;
-    return backward_layout(B, T, Hv, dk, dv, nseq, packed).total;
+    return backward_layout(B, T, Hv, dk, dv, nseq, packed, true).total;
 }
 
 gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
@@ -357,7 +383,7 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
     for (const void* p : f_ptrs)
         if (p && !aligned_to(p, 4)) return fail(GDN_ERR_INVALID_ARG, "pointer %p not 4-byte aligned", p);
     if (nseq == 0) return GDN_OK;
-    const size_t need = backward_layout(B, T, Hv, dk, dv, nseq, packed).total;
+    const size_t need = backward_layout(B, T, Hv, dk, dv, nseq, packed, true).total;
     if (!o.workspace || o.workspace_bytes < need)
         return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     o.workspace ? o.workspace_bytes : (size_t)0);

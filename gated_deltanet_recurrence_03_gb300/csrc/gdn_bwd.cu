@@ -482,8 +482,8 @@ struct StSmem {
 // Chunk-start states S (to the workspace) and U = U~ - W S (over U~ in the workspace).
 template <typename TT, int DK, int DV>
 __global__ void __launch_bounds__(kStThreads)
-bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws ws, int T_len, int Hqk, int Hv,
-                     const int32_t* __restrict__ cu, int nseq, bool vec) {
+bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, float* __restrict__ S_final, Ws ws,
+                     int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu, int nseq, bool vec) {
     using L = StSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int SW = L::SW, NSL = DV / SW;
@@ -553,6 +553,12 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, Ws 
                 }
         }
         __syncthreads();
+    }
+    if (S_final) {   // the state after the last chunk (the forward's final state)
+        for (int idx = tid; idx < DK * SW; idx += kStThreads) {
+            const int i = idx / SW, j = idx % SW;
+            S_final[sbase + (size_t)i * DV + j] = sS[i * L::LS + j];
+        }
     }
 }
 
@@ -1096,6 +1102,133 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     }
 }
 
+// ---------------------------------------------------------------- chunked forward (any head dims, fp32 accuracy)
+// The prefill through the same chunk algebra: the WY kernel, the forward chain (chunk-start states,
+// U, and the final state), then per chunk O = scale diag(gamma) Q S + P U with P = scale D o (Q K^T)
+// (s <= r), which is the unrolled read o_r = scale S_r^T q_r.
+template <int DK, int DV>
+struct OutSmem {
+    static constexpr int LK = DK + 4, LV = DV + 4;
+    static constexpr int Q_ = 0, S_ = Q_ + kC * LK, P_ = S_ + DK * LV, U_ = P_ + kC * kLCC, G_ = U_ + kC * LV;
+    static constexpr int FLOATS = G_ + kC;
+    static constexpr size_t BYTES = (size_t)FLOATS * 4;
+    static_assert(S_ % 4 == 0 && P_ % 4 == 0 && U_ % 4 == 0, "16-byte aligned regions");
+};
+
+template <typename TT, int DK, int DV>
+__global__ void __launch_bounds__(kStThreads)
+fwd_out_kernel(const TT* __restrict__ q, TT* __restrict__ out, Ws ws, int T_len, int Hqk, int Hv,
+               const int32_t* __restrict__ cu, int nseq, float scale, bool vec) {
+    using L = OutSmem<DK, DV>;
+    using D = WsDims<DK, DV>;
+    using TO = ChainTiles<kC, DV>;
+    constexpr bool kEx = sizeof(TT) == 2;   // bf16 Q is exact in tf32
+    extern __shared__ __align__(16) float sm[];
+    float* sQ = sm + L::Q_;
+    float* sS = sm + L::S_;
+    float* sP = sm + L::P_;
+    float* sU = sm + L::U_;
+    float* sG = sm + L::G_;
+    const long long slot = blockIdx.x;
+    const int hk = blockIdx.y, G = Hv / Hqk;
+    int seq, n;
+    long long tok0;
+    if (!slot_chunk(cu, nseq, T_len, slot, seq, tok0, n)) return;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, g = lane / 4, t = lane % 4;
+    const int om = 16 * (warp % TO::MT), on = (warp / TO::MT) * TO::NT;
+    ld_in<TT, kC, DK, kStThreads>(sQ, L::LK, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+    for (int jh = 0; jh < G; ++jh) {
+        const int h = hk * G + jh;
+        const size_t wi = (size_t)slot * Hv + h;
+        if (tid < kC) sG[tid] = ws.G[wi * D::G + tid];
+        ld_ws<DK, DV, kStThreads>(sS, L::LV, ws.S + wi * D::S, DV, tid);
+        ld_ws<kC, kC, kStThreads>(sP, kLCC, ws.P + wi * D::P, kC, tid);
+        ld_ws<kC, DV, kStThreads>(sU, L::LV, ws.U + wi * D::U, DV, tid);
+        __syncthreads();
+        float y1[TO::NT][4], y2[TO::NT][4];
+        tile_zero(y1);
+        tile_zero(y2);
+        mma_prod<TO::NT, DK, false, false, kEx, false>(y1, sQ, L::LK, sS, L::LV, om, on, g, t);   // Q S
+        mma_prod<TO::NT, kC, false, false>(y2, sP, kLCC, sU, L::LV, om, on, g, t);              // P U
+        const int ra = om + g, rb = ra + 8;
+        const float ca = scale * __expf(sG[ra]), cb = scale * __expf(sG[rb]);
+#pragma unroll
+        for (int qq = 0; qq < TO::NT; ++qq) {
+            const int j = fcol(on + qq, t, 0);
+            if (ra < n) {
+                TT* o = out + ((tok0 + ra) * Hv + h) * DV + j;
+                o[0] = from_f32<TT>(fmaf(ca, y1[qq][0], y2[qq][0]));
+                o[1] = from_f32<TT>(fmaf(ca, y1[qq][1], y2[qq][1]));
+            }
+            if (rb < n) {
+                TT* o = out + ((tok0 + rb) * Hv + h) * DV + j;
+                o[0] = from_f32<TT>(fmaf(cb, y1[qq][2], y2[qq][2]));
+                o[1] = from_f32<TT>(fmaf(cb, y1[qq][3], y2[qq][3]));
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename TT, int DK, int DV>
+cudaError_t launch_fwd_typed(const PrefillArgs& a, const BwdLayout& Lw) {
+    uint8_t* base = static_cast<uint8_t*>(a.workspace);
+    Ws ws{};
+    ws.T = reinterpret_cast<float*>(base + Lw.T_off);
+    ws.P = reinterpret_cast<float*>(base + Lw.P_off);
+    ws.W = reinterpret_cast<float*>(base + Lw.W_off);
+    ws.U = reinterpret_cast<float*>(base + Lw.U_off);
+    ws.G = reinterpret_cast<float*>(base + Lw.G_off);
+    ws.S = reinterpret_cast<float*>(base + Lw.S_off);
+    const TT* q = static_cast<const TT*>(a.q);
+    const TT* k = static_cast<const TT*>(a.k);
+    const TT* v = static_cast<const TT*>(a.v);
+    const TT* g = static_cast<const TT*>(a.g);
+    const TT* beta = static_cast<const TT*>(a.beta);
+    TT* out = static_cast<TT*>(a.out);
+    constexpr int NSL = DV / slice_width<DV>();
+    // the prefill entry point requires 16-byte aligned q, k, v and out
+    const bool vec = true;
+    using S1 = WySmem<DK, DV>;
+    using S2 = StSmem<DK, DV>;
+    using S3 = OutSmem<DK, DV>;
+    cudaError_t e;
+    if ((e = set_smem(bwd_wy_kernel<TT, DK, DV>, S1::BYTES)) != cudaSuccess) return e;
+    if ((e = set_smem(bwd_state_fwd_kernel<TT, DK, DV>, S2::BYTES)) != cudaSuccess) return e;
+    if ((e = set_smem(fwd_out_kernel<TT, DK, DV>, S3::BYTES)) != cudaSuccess) return e;
+    const dim3 chunk_grid((unsigned)Lw.slots, (unsigned)a.Hqk);
+    const unsigned nst = (unsigned)((long long)a.num_seqs * a.Hv * NSL);
+    bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
+        q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(k, a.S0, a.S_final, ws, a.T, a.Hqk,
+                                                                              a.Hv, a.cu_seqlens, a.num_seqs, vec);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    fwd_out_kernel<TT, DK, DV><<<chunk_grid, kStThreads, S3::BYTES, a.stream>>>(
+        q, out, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+    return cudaGetLastError();
+}
+
+template <typename TT, int DK>
+cudaError_t launch_fwd_dk(const PrefillArgs& a, const BwdLayout& L) {
+    switch (a.dv) {
+        case 32: return launch_fwd_typed<TT, DK, 32>(a, L);
+        case 64: return launch_fwd_typed<TT, DK, 64>(a, L);
+        case 128: return launch_fwd_typed<TT, DK, 128>(a, L);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename TT>
+cudaError_t launch_fwd_dtype(const PrefillArgs& a, const BwdLayout& L) {
+    switch (a.dk) {
+        case 32: return launch_fwd_dk<TT, 32>(a, L);
+        case 64: return launch_fwd_dk<TT, 64>(a, L);
+        case 128: return launch_fwd_dk<TT, 128>(a, L);
+    }
+    return cudaErrorInvalidValue;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 template <typename F>
@@ -1140,8 +1273,8 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
         q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(k, a.S0, ws, a.T, a.Hqk, a.Hv,
-                                                                              a.cu_seqlens, a.num_seqs, vec);
+    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(k, a.S0, nullptr, ws, a.T, a.Hqk,
+                                                                              a.Hv, a.cu_seqlens, a.num_seqs, vec);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_state_adj_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
         q, k, dout, a.dS_final, a.grad_S0, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
@@ -1174,7 +1307,7 @@ cudaError_t launch_dtype(const BackwardArgs& a, const BwdLayout& L) {
 
 }  // namespace
 
-BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed) {
+BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed, bool adjoint) {
     const long long ttot = packed ? (long long)T : (long long)B * T;
     BwdLayout L{};
     L.slots = (ttot + kC - 1) / kC + nseq;
@@ -1190,14 +1323,25 @@ BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool p
     take(L.U_off, (size_t)kC * dv);
     take(L.G_off, (size_t)kC);
     take(L.S_off, (size_t)dk * dv);
-    take(L.dS_off, (size_t)dk * dv);
-    take(L.dU_off, (size_t)kC * dv);
+    if (adjoint) {
+        take(L.dS_off, (size_t)dk * dv);
+        take(L.dU_off, (size_t)kC * dv);
+    }
     L.total = off;
     return L;
 }
 
+size_t chunked_prefill_workspace_bytes(int B, int T, int Hv, int dk, int dv, int nseq, bool packed) {
+    return backward_layout(B, T, Hv, dk, dv, nseq, packed, false).total;
+}
+
+cudaError_t launch_chunked_prefill(const PrefillArgs& a) {
+    const BwdLayout L = backward_layout(a.B, a.T, a.Hv, a.dk, a.dv, a.num_seqs, a.cu_seqlens != nullptr, false);
+    return a.dtype == GDN_BF16 ? launch_fwd_dtype<__nv_bfloat16>(a, L) : launch_fwd_dtype<float>(a, L);
+}
+
 cudaError_t launch_backward(const BackwardArgs& a) {
-    const BwdLayout L = backward_layout(a.B, a.T, a.Hv, a.dk, a.dv, a.num_seqs, a.cu_seqlens != nullptr);
+    const BwdLayout L = backward_layout(a.B, a.T, a.Hv, a.dk, a.dv, a.num_seqs, a.cu_seqlens != nullptr, true);
     return a.dtype == GDN_BF16 ? launch_dtype<__nv_bfloat16>(a, L) : launch_dtype<float>(a, L);
 }
 

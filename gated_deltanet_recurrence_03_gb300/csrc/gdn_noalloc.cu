@@ -63,6 +63,10 @@ extern "C" gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, cons
     o.workspace_bytes = 0;
     const size_t need = gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, &o);
     if (need > gdn::kNoAllocScratchBytes) {
+        // the chunked path of shapes off the tensor-core tile falls back to the token-serial kernel,
+        // which needs no scratch; the tensor-core path has no such fallback
+        if (!gdn::tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk, o.flags))
+            return gdn_chunk_fwd(q, k, v, g, beta, S0, out, S_final, B, T, Hqk, Hv, dk, dv, &o);
         gdn::set_error_message("gdn_chunk_fwd_noalloc: this problem needs more scratch than the built-in "
                                "64 MiB array; use gdn_chunk_fwd with a caller workspace");
         return GDN_ERR_WORKSPACE;

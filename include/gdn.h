@@ -108,9 +108,14 @@ void gdn_opts_init(gdn_opts_t* opts);
  *   S_final  [nseq, Hv, dk, dv] float or NULL (not written); may equal S0 (in-place update)
  *
  * Supported: dk, dv in {32, 64, 128}; Hv a multiple of Hqk; B, T >= 0.  T = 0 copies S0 to
- * S_final (zeros when S0 is NULL).  bf16 inputs with dk = dv = 128 run on the
- * tcgen05 tensor-core path (chunk 64) and need the workspace; everything else runs the token-serial
- * CUDA-core kernel and needs none.  out must not overlap any input.
+ * S_final (zeros when S0 is NULL).  Three kernel families, chosen in this order:
+ *   - bf16 inputs with dk = dv = 128: the tcgen05 tensor-core path (chunk 64); it needs the
+ *     workspace (GDN_ERR_WORKSPACE if missing or too small);
+ *   - other inputs without GDN_NORMALIZE_QK / GDN_RAW_GATES, when the workspace is at least
+ *     gdn_chunk_fwd_workspace_size() bytes (256-byte aligned): the same chunk algebra on split-tf32
+ *     tensor-core MMAs in fp32 accuracy (64-token chunks whatever opts->chunk says);
+ *   - otherwise the token-serial CUDA-core kernel, which needs no workspace.
+ * out must not overlap any input.
  *
  * Errors: GDN_ERR_INVALID_ARG for null required pointers, negative sizes, Hv % Hqk != 0,
  * pointers not 16-byte aligned, cu_seqlens with B != 1 or num_seqs < 1; GDN_ERR_UNSUPPORTED for
@@ -153,9 +158,10 @@ gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, con
  * device memory, a fixed memory budget, code that must not synchronise the device).  The call
  * allocates nothing.
  *
- * Limit: problems whose gdn_chunk_fwd_workspace_size() exceeds 64 MiB are rejected with
- * GDN_ERR_WORKSPACE before anything is launched (for 32 value heads of dim 128 that is about 40
- * chunks of 64 tokens, ~2.5k tokens, per call).  The first call on each device looks up the
+ * Limit: on the tensor-core path, problems whose gdn_chunk_fwd_workspace_size() exceeds 64 MiB
+ * are rejected with GDN_ERR_WORKSPACE before anything is launched (for 32 value heads of dim 128
+ * that is about 40 chunks of 64 tokens, ~2.5k tokens, per call); other shapes that large run the
+ * token-serial kernel.  The first call on each device looks up the
  * array's device address (a host-side query, no allocation); make that first call before any
  * stream capture.  All calls on a device share the array, which keeps the previous call's
  * contents (no part of it needs to start at zero); calls that overlap on the GPU race on it, so

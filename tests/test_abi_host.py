@@ -108,8 +108,15 @@ def test_empty_calls_do_nothing(lib):
 
 
 def test_workspace_query_is_pure_host(lib):
-    # fp32 and small heads run the token-serial kernel: no workspace
-    assert lib.gdn_chunk_fwd_workspace_size(2, 512, 4, 4, 32, 32, opts(lib, dtype=pkg_lib.GDN_F32)) == 0
+    # fp32 and small heads take the chunked prefill: per (64-token chunk slot, value head) fp32 T, P
+    # (64 x 64), W (64 x dk), U (64 x dv), G (64) and the chunk-start state (dk x dv); slots = 2 * 8 + 2
+    per = 2 * 64 * 64 + 64 * 32 + 64 * 32 + 64 + 32 * 32
+    need = 18 * 4 * per * 4
+    n = lib.gdn_chunk_fwd_workspace_size(2, 512, 4, 4, 32, 32, opts(lib, dtype=pkg_lib.GDN_F32))
+    assert need <= n <= need + 6 * 256
+    # with in-kernel normalisation or raw gates they run the token-serial kernel: no workspace
+    assert lib.gdn_chunk_fwd_workspace_size(2, 512, 4, 4, 32, 32,
+                                            opts(lib, dtype=pkg_lib.GDN_F32, flags=pkg_lib.GDN_NORMALIZE_QK)) == 0
     assert lib.gdn_chunk_fwd_workspace_size(-1, 512, 4, 4, 32, 32, opts(lib)) == 0
 
 
