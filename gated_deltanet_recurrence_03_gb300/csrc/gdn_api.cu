@@ -138,11 +138,11 @@ const char* gdn_status_string(gdn_status_t s) {
 }  // extern "C"
 
 namespace {
-// The chunked prefill takes the token loop's inputs as they are: no in-kernel normalisation or raw
-// gates (the output gate is a separate pass after either prefill).
-bool chunked_prefill_eligible(int dk, int dv, unsigned flags) {
-    return (flags & (GDN_NORMALIZE_QK | GDN_RAW_GATES)) == 0 && (dk == 32 || dk == 64 || dk == 128) &&
-           (dv == 32 || dv == 64 || dv == 128);
+// The chunked prefill covers every head-dim pair in {32, 64, 128}^2 with the full front end (l2 norm
+// of q and k as per-row scalars, gates from raw projections); the output gate is a separate pass after
+// either prefill.
+bool chunked_prefill_eligible(int dk, int dv) {
+    return (dk == 32 || dk == 64 || dk == 128) && (dv == 32 || dv == 64 || dv == 128);
 }
 }  // namespace
 
@@ -156,7 +156,7 @@ size_t gdn_chunk_fwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int d
     if (nseq <= 0 || T == 0) return 0;
     if (tc_prefill_eligible(o.dtype, dk, dv, Hqk, Hv, o.chunk, o.flags))
         return tc_prefill_workspace_bytes(B, T, Hv, nseq, packed);
-    if (chunked_prefill_eligible(dk, dv, o.flags)) return chunked_prefill_workspace_bytes(B, T, Hv, dk, dv, nseq, packed);
+    if (chunked_prefill_eligible(dk, dv)) return chunked_prefill_workspace_bytes(B, T, Hv, dk, dv, nseq, packed);
     return 0;
 }
 
@@ -224,7 +224,7 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const vo
             e = launch_output_gate(out, o.z, o.norm_weight, o.norm_eps, (long long)B * T * Hv, dv, o.dtype, stream);
             record(o, 3, stream);
         }
-    } else if (chunked_prefill_eligible(dk, dv, o.flags) && o.workspace &&
+    } else if (chunked_prefill_eligible(dk, dv) && o.workspace &&
                (reinterpret_cast<uintptr_t>(o.workspace) & 255u) == 0 &&
                o.workspace_bytes >= chunked_prefill_workspace_bytes(B, T, Hv, dk, dv, nseq, packed)) {
         // chunked form on the split-tf32 tensor-core kernels (fp32 accuracy)
@@ -235,7 +235,7 @@ gdn_status_t gdn_chunk_fwd(const void* q, const void* k, const void* v, const vo
             e = launch_output_gate(out, o.z, o.norm_weight, o.norm_eps, (long long)B * T * Hv, dv, o.dtype, stream);
             record(o, 2, stream);
         }
-    } else {   // no (or too small a) workspace, or a front-end option: the token-serial kernel
+    } else {   // no (or too small a) workspace: the token-serial kernel
         record(o, 0, stream);
         e = launch_recurrent_prefill(a);
         record(o, 1, stream);

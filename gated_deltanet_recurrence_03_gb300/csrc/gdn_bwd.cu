@@ -222,6 +222,21 @@ __device__ __forceinline__ void ld_ws(float* __restrict__ dst, int ld, const flo
     ld_in<float, ROWS, WIDTH, NT>(dst, ld, src, stride, ROWS, tid, true);
 }
 
+// l2 normalisation of q and k kept as per-row scalars: r[i] = 1 / sqrt(|x_i|^2 + 1e-6) for the ROWS rows
+// of a [ROWS][WIDTH] tile in shared memory, one warp per row.  The tile itself stays as loaded (bf16
+// rows stay exact in tf32); each product applies the scalars to its other operand or its output.
+template <int ROWS, int WIDTH, int NWARPS>
+__device__ __forceinline__ void row_rnorm(const float* __restrict__ x, int ld, float* __restrict__ r, int warp,
+                                          int lane) {
+    for (int i = warp; i < ROWS; i += NWARPS) {
+        float s = 0.f;
+        for (int c = lane; c < WIDTH; c += 32) s = fmaf(x[i * ld + c], x[i * ld + c], s);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) r[i] = rsqrtf(s + 1e-6f);
+    }
+}
+
 // Workspace slot of chunk 0 of sequence i.
 __device__ __forceinline__ long long slot_base(const int32_t* cu, int i, int T) {
     long long t0, t1;
@@ -250,13 +265,13 @@ __device__ __forceinline__ bool slot_chunk(const int32_t* cu, int nseq, int T, l
 
 // Per-(slot, value head) workspace arrays.
 struct Ws {
-    float *T, *P, *W, *U, *G, *S, *dS, *dU;
+    float *T, *P, *W, *U, *G, *S, *dS, *dU, *R;   // R: per-row l2 scalars of K and Q (prefill front end)
 };
 
 template <int DK, int DV>
 struct WsDims {
     static constexpr size_t T = (size_t)kC * kC, P = (size_t)kC * kC, W = (size_t)kC * DK, U = (size_t)kC * DV,
-                            G = kC, S = (size_t)DK * DV, dS = (size_t)DK * DV, dU = (size_t)kC * DV;
+                            G = kC, S = (size_t)DK * DV, dS = (size_t)DK * DV, dU = (size_t)kC * DV, R = 2 * kC;
 };
 
 // Fragment coordinates of accumulator element e of n-tile nb: row row0 + g (+ 8 for e >= 2),
@@ -280,15 +295,18 @@ struct WySmem {
     static constexpr int LK = DK + 4, LQV = (DK > DV ? DK : DV) + 4;   // = 4 mod 32
     static constexpr int K_ = 0, QV_ = K_ + kC * LK, KK_ = QV_ + kC * LQV, QK_ = KK_ + kC * kLCC,
                          L_ = QK_ + kC * kLCC, T_ = L_ + kC * kLCC, Y_ = T_ + kC * kLCC, VEC_ = Y_ + 3 * 256;
-    static constexpr int FLOATS = VEC_ + 4 * kC;
+    static constexpr int FLOATS = VEC_ + 6 * kC;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
 };
 
+// With A_log non-null, g and beta hold the raw projections a, b and the gates are formed on load;
+// with normalize, q and k are l2-normalised through per-row scalars (the prefill's front end).
 template <typename TT, int DK, int DV>
 __global__ void __launch_bounds__(kWyThreads)
 bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __restrict__ v, const TT* __restrict__ g,
               const TT* __restrict__ beta, Ws ws, int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu,
-              int nseq, float scale, bool vec) {
+              int nseq, float scale, bool vec, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
+              bool normalize) {
     using L = WySmem<DK, DV>;
     using D = WsDims<DK, DV>;
     extern __shared__ __align__(16) float sm[];
@@ -303,6 +321,8 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
     float* sBeta = sG + kC;
     float* sBG = sBeta + kC;
     float* sGraw = sBG + kC;
+    float* sRK = sGraw + kC;   // per-row l2 scalars of K and Q (1 without normalisation)
+    float* sRQ = sRK + kC;
 
     const long long slot = blockIdx.x;
     const int hk = blockIdx.y, G = Hv / Hqk;
@@ -315,6 +335,13 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
     ld_in<TT, kC, DK, kWyThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
     ld_in<TT, kC, DK, kWyThreads>(sQV, L::LQV, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
     __syncthreads();
+    if (normalize) {
+        row_rnorm<kC, DK, kWyThreads / 32>(sK, L::LK, sRK, warp, lane);
+        row_rnorm<kC, DK, kWyThreads / 32>(sQV, L::LQV, sRQ, warp, lane);
+    } else if (tid < kC) {
+        sRK[tid] = 1.f;
+        sRQ[tid] = 1.f;
+    }
     {   // Gram matrices K K^T and Q K^T on tensor cores (both operands exact in tf32 for bf16 inputs)
         using TG = ChainTiles<kC, kC>;
         float kk[TG::NT][4], qk[TG::NT][4];
@@ -333,8 +360,11 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
         const size_t wi = (size_t)slot * Hv + h;
         if (tid < kC) {
             const bool ok = tid < n;
-            sGraw[tid] = ok ? to_f32(g[(tok0 + tid) * Hv + h]) : 0.f;
-            sBeta[tid] = ok ? to_f32(beta[(tok0 + tid) * Hv + h]) : 0.f;
+            float gt = ok ? to_f32(g[(tok0 + tid) * Hv + h]) : 0.f;
+            float bt = ok ? to_f32(beta[(tok0 + tid) * Hv + h]) : 0.f;
+            if (A_log && ok) gates_from_raw(gt, bt, A_log[h], dt_bias[h], gt, bt);   // rows past n stay 0
+            sGraw[tid] = gt;
+            sBeta[tid] = bt;
         }
         // V of this value head (Q is no longer needed: its Gram is in sQK)
         ld_in<TT, kC, DV, kWyThreads>(sQV, L::LQV, v + (tok0 * Hv + h) * DV, (size_t)Hv * DV, n, tid, vec);
@@ -352,15 +382,19 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
         }
         __syncthreads();
         if (tid < kC) {
-            sBG[tid] = sBeta[tid] * __expf(sG[tid]);
+            sBG[tid] = sBeta[tid] * __expf(sG[tid]) * sRK[tid];   // W = T diag(beta gamma) (diag(rk) K)
             ws.G[wi * D::G + tid] = sG[tid];
+            if (normalize) {   // for the chain and the output kernel
+                ws.R[wi * D::R + tid] = sRK[tid];
+                ws.R[wi * D::R + kC + tid] = sRQ[tid];
+            }
         }
         // P = scale D o QK^T (s <= r) to the workspace; L = diag(beta) (D o KK^T) strictly below the diagonal
         for (int idx = tid; idx < kC * kC; idx += kWyThreads) {
             const int r = idx / kC, s = idx % kC;
             const float d = s <= r ? __expf(sG[r] - sG[s]) : 0.f;
-            ws.P[wi * D::P + idx] = scale * d * sQK[r * kLCC + s];
-            sL[r * kLCC + s] = s < r ? sBeta[r] * d * sKK[r * kLCC + s] : 0.f;
+            ws.P[wi * D::P + idx] = scale * d * (sRQ[r] * sRK[s]) * sQK[r * kLCC + s];
+            sL[r * kLCC + s] = s < r ? sBeta[r] * d * (sRK[r] * sRK[s]) * sKK[r * kLCC + s] : 0.f;
         }
         __syncthreads();
         {   // T = (I + L)^{-1} in 16 x 16 blocks: each diagonal block by forward substitution (one thread
@@ -479,11 +513,12 @@ struct StSmem {
                   "16-byte aligned regions");
 };
 
-// Chunk-start states S (to the workspace) and U = U~ - W S (over U~ in the workspace).
+// Chunk-start states S (to the workspace) and U = U~ - W S (over U~ in the workspace).  With normalize,
+// the update reads K through its per-row l2 scalars (written by the WY kernel).
 template <typename TT, int DK, int DV>
 __global__ void __launch_bounds__(kStThreads)
 bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, float* __restrict__ S_final, Ws ws,
-                     int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu, int nseq, bool vec) {
+                     int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu, int nseq, bool vec, bool normalize) {
     using L = StSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int SW = L::SW, NSL = DV / SW;
@@ -496,6 +531,7 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, flo
     float* sU = sm + L::X_;
     float* sS = sm + L::S_;
     float* sG = sm + L::G_;
+    float* sRK = sm + L::R_;   // per-row l2 scalars of K
     const int sl = blockIdx.x % NSL, h = (blockIdx.x / NSL) % Hv, seq = blockIdx.x / (NSL * Hv);
     if (seq >= nseq) return;
     const int hk = h / (Hv / Hqk), col0 = sl * SW;
@@ -510,11 +546,15 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, flo
         const int i = idx / SW, j = idx % SW;
         sS[i * L::LS + j] = S0 ? S0[sbase + (size_t)i * DV + j] : 0.f;
     }
+
     for (long long c = 0; c < nch; ++c) {
         const size_t wi = (size_t)(slot0 + c) * Hv + h;
         const long long tok0 = t0 + c * kC;
         const int n = (int)min((long long)kC, t1 - tok0);
-        if (tid < kC) sG[tid] = ws.G[wi * D::G + tid];
+        if (tid < kC) {
+            sG[tid] = ws.G[wi * D::G + tid];
+            sRK[tid] = normalize ? ws.R[wi * D::R + tid] : 1.f;
+        }
         ld_ws<kC, DK, kStThreads>(sW, L::LK, ws.W + wi * D::W, DK, tid);
         ld_ws<kC, SW, kStThreads>(sU, L::LS, ws.U + wi * D::U + col0, DV, tid);
         ld_in<TT, kC, DK, kStThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
@@ -523,7 +563,7 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, flo
             const int i = idx / SW, j = idx % SW;
             ws.S[wi * D::S + (size_t)i * DV + col0 + j] = sS[i * L::LS + j];
         }
-        {   // U = U~ - W S to the workspace; sU holds diag(gamma_C / gamma) U (each thread its own elements)
+        {   // U = U~ - W S to the workspace; sU holds diag(rk gamma_C / gamma) U (each thread its own elements)
             float acc[TU::NT][4];
             tile_zero(acc);
             mma_prod<TU::NT, DK, false, false>(acc, sW, L::LK, sS, L::LS, um, un, g, t);
@@ -534,7 +574,7 @@ bwd_state_fwd_kernel(const TT* __restrict__ k, const float* __restrict__ S0, flo
                 for (int e = 0; e < 4; ++e) {
                     const int r = frow(um, g, e), j = fcol(un + q, t, e);
                     const float u = sU[r * L::LS + j] - acc[q][e];
-                    sU[r * L::LS + j] = __expf(GC - sG[r]) * u;
+                    sU[r * L::LS + j] = __expf(GC - sG[r]) * sRK[r] * u;
                     ws.U[wi * D::U + (size_t)r * DV + col0 + j] = u;
                 }
         }
@@ -1109,8 +1149,9 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 template <int DK, int DV>
 struct OutSmem {
     static constexpr int LK = DK + 4, LV = DV + 4;
-    static constexpr int Q_ = 0, S_ = Q_ + kC * LK, P_ = S_ + DK * LV, U_ = P_ + kC * kLCC, G_ = U_ + kC * LV;
-    static constexpr int FLOATS = G_ + kC;
+    static constexpr int Q_ = 0, S_ = Q_ + kC * LK, P_ = S_ + DK * LV, U_ = P_ + kC * kLCC, G_ = U_ + kC * LV,
+                         R_ = G_ + kC;
+    static constexpr int FLOATS = R_ + kC;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
     static_assert(S_ % 4 == 0 && P_ % 4 == 0 && U_ % 4 == 0, "16-byte aligned regions");
 };
@@ -1118,7 +1159,7 @@ struct OutSmem {
 template <typename TT, int DK, int DV>
 __global__ void __launch_bounds__(kStThreads)
 fwd_out_kernel(const TT* __restrict__ q, TT* __restrict__ out, Ws ws, int T_len, int Hqk, int Hv,
-               const int32_t* __restrict__ cu, int nseq, float scale, bool vec) {
+               const int32_t* __restrict__ cu, int nseq, float scale, bool vec, bool normalize) {
     using L = OutSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     using TO = ChainTiles<kC, DV>;
@@ -1129,6 +1170,7 @@ fwd_out_kernel(const TT* __restrict__ q, TT* __restrict__ out, Ws ws, int T_len,
     float* sP = sm + L::P_;
     float* sU = sm + L::U_;
     float* sG = sm + L::G_;
+    float* sRQ = sm + L::R_;   // per-row l2 scalars of Q (P already carries them)
     const long long slot = blockIdx.x;
     const int hk = blockIdx.y, G = Hv / Hqk;
     int seq, n;
@@ -1140,7 +1182,10 @@ fwd_out_kernel(const TT* __restrict__ q, TT* __restrict__ out, Ws ws, int T_len,
     for (int jh = 0; jh < G; ++jh) {
         const int h = hk * G + jh;
         const size_t wi = (size_t)slot * Hv + h;
-        if (tid < kC) sG[tid] = ws.G[wi * D::G + tid];
+        if (tid < kC) {
+            sG[tid] = ws.G[wi * D::G + tid];
+            sRQ[tid] = normalize ? ws.R[wi * D::R + kC + tid] : 1.f;
+        }
         ld_ws<DK, DV, kStThreads>(sS, L::LV, ws.S + wi * D::S, DV, tid);
         ld_ws<kC, kC, kStThreads>(sP, kLCC, ws.P + wi * D::P, kC, tid);
         ld_ws<kC, DV, kStThreads>(sU, L::LV, ws.U + wi * D::U, DV, tid);
@@ -1151,7 +1196,7 @@ fwd_out_kernel(const TT* __restrict__ q, TT* __restrict__ out, Ws ws, int T_len,
         mma_prod<TO::NT, DK, false, false, kEx, false>(y1, sQ, L::LK, sS, L::LV, om, on, g, t);   // Q S
         mma_prod<TO::NT, kC, false, false>(y2, sP, kLCC, sU, L::LV, om, on, g, t);              // P U
         const int ra = om + g, rb = ra + 8;
-        const float ca = scale * __expf(sG[ra]), cb = scale * __expf(sG[rb]);
+        const float ca = scale * __expf(sG[ra]) * sRQ[ra], cb = scale * __expf(sG[rb]) * sRQ[rb];
 #pragma unroll
         for (int qq = 0; qq < TO::NT; ++qq) {
             const int j = fcol(on + qq, t, 0);
@@ -1180,6 +1225,7 @@ cudaError_t launch_fwd_typed(const PrefillArgs& a, const BwdLayout& Lw) {
     ws.U = reinterpret_cast<float*>(base + Lw.U_off);
     ws.G = reinterpret_cast<float*>(base + Lw.G_off);
     ws.S = reinterpret_cast<float*>(base + Lw.S_off);
+    ws.R = reinterpret_cast<float*>(base + Lw.R_off);
     const TT* q = static_cast<const TT*>(a.q);
     const TT* k = static_cast<const TT*>(a.k);
     const TT* v = static_cast<const TT*>(a.v);
@@ -1198,14 +1244,16 @@ cudaError_t launch_fwd_typed(const PrefillArgs& a, const BwdLayout& Lw) {
     if ((e = set_smem(fwd_out_kernel<TT, DK, DV>, S3::BYTES)) != cudaSuccess) return e;
     const dim3 chunk_grid((unsigned)Lw.slots, (unsigned)a.Hqk);
     const unsigned nst = (unsigned)((long long)a.num_seqs * a.Hv * NSL);
+    const bool normalize = (a.flags & GDN_NORMALIZE_QK) != 0;
+    const float* A_log = (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr;
     bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
-        q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+        q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec, A_log, a.dt_bias, normalize);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(k, a.S0, a.S_final, ws, a.T, a.Hqk,
-                                                                              a.Hv, a.cu_seqlens, a.num_seqs, vec);
+    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
+        k, a.S0, a.S_final, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, vec, normalize);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     fwd_out_kernel<TT, DK, DV><<<chunk_grid, kStThreads, S3::BYTES, a.stream>>>(
-        q, out, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+        q, out, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec, normalize);
     return cudaGetLastError();
 }
 
@@ -1239,7 +1287,7 @@ cudaError_t set_smem(F* kernel, size_t bytes) {
 template <typename TT, int DK, int DV>
 cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     uint8_t* base = static_cast<uint8_t*>(a.workspace);
-    Ws ws;
+    Ws ws{};
     ws.T = reinterpret_cast<float*>(base + Lw.T_off);
     ws.P = reinterpret_cast<float*>(base + Lw.P_off);
     ws.W = reinterpret_cast<float*>(base + Lw.W_off);
@@ -1271,10 +1319,10 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     if ((e = set_smem(bwd_local_kernel<TT, DK, DV>, S4::BYTES)) != cudaSuccess) return e;
 
     bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
-        q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+        q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec, nullptr, nullptr, false);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(k, a.S0, nullptr, ws, a.T, a.Hqk,
-                                                                              a.Hv, a.cu_seqlens, a.num_seqs, vec);
+    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
+        k, a.S0, nullptr, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, vec, false);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_state_adj_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
         q, k, dout, a.dS_final, a.grad_S0, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
@@ -1326,6 +1374,8 @@ BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool p
     if (adjoint) {
         take(L.dS_off, (size_t)dk * dv);
         take(L.dU_off, (size_t)kC * dv);
+    } else {
+        take(L.R_off, (size_t)2 * kC);   // the prefill front end's per-row l2 scalars
     }
     L.total = off;
     return L;

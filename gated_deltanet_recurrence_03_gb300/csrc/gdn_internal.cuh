@@ -109,12 +109,12 @@ struct BackwardArgs {
 // 256-byte aligned.  `slots` = ceil(tokens / C) + sequences.
 struct BwdLayout {
     long long slots;
-    size_t T_off, P_off, W_off, U_off, G_off, S_off, dS_off, dU_off, total;
+    size_t T_off, P_off, W_off, U_off, G_off, S_off, dS_off, dU_off, R_off, total;
 };
 BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed, bool adjoint);
 cudaError_t launch_backward(const BackwardArgs& a);
-// Chunked prefill for shapes outside the tensor-core path (fp32 inputs, head dims 32 / 64) when no
-// front-end option is set: the backward's WY kernel and forward chain plus an output kernel.
+// Chunked prefill for shapes outside the tensor-core path (fp32 inputs, head dims 32 / 64, front end
+// included): the backward's WY kernel and forward chain plus an output kernel.
 size_t chunked_prefill_workspace_bytes(int B, int T, int Hv, int dk, int dv, int nseq, bool packed);
 cudaError_t launch_chunked_prefill(const PrefillArgs& a);
 

@@ -111,9 +111,9 @@ void gdn_opts_init(gdn_opts_t* opts);
  * S_final (zeros when S0 is NULL).  Three kernel families, chosen in this order:
  *   - bf16 inputs with dk = dv = 128: the tcgen05 tensor-core path (chunk 64); it needs the
  *     workspace (GDN_ERR_WORKSPACE if missing or too small);
- *   - other inputs without GDN_NORMALIZE_QK / GDN_RAW_GATES, when the workspace is at least
- *     gdn_chunk_fwd_workspace_size() bytes (256-byte aligned): the same chunk algebra on split-tf32
- *     tensor-core MMAs in fp32 accuracy (64-token chunks whatever opts->chunk says);
+ *   - other inputs, when the workspace is at least gdn_chunk_fwd_workspace_size() bytes (256-byte
+ *     aligned): the same chunk algebra on split-tf32 tensor-core MMAs in fp32 accuracy (64-token
+ *     chunks whatever opts->chunk says), GDN_NORMALIZE_QK and GDN_RAW_GATES included;
  *   - otherwise the token-serial CUDA-core kernel, which needs no workspace.
  * out must not overlap any input.
  *

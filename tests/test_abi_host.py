@@ -109,14 +109,16 @@ def test_empty_calls_do_nothing(lib):
 
 def test_workspace_query_is_pure_host(lib):
     # fp32 and small heads take the chunked prefill: per (64-token chunk slot, value head) fp32 T, P
-    # (64 x 64), W (64 x dk), U (64 x dv), G (64) and the chunk-start state (dk x dv); slots = 2 * 8 + 2
-    per = 2 * 64 * 64 + 64 * 32 + 64 * 32 + 64 + 32 * 32
+    # (64 x 64), W (64 x dk), U (64 x dv), G (64), the chunk-start state (dk x dv) and the front end's
+    # row scalars of k and q (2 x 64); slots = 2 * 8 + 2
+    per = 2 * 64 * 64 + 64 * 32 + 64 * 32 + 64 + 32 * 32 + 2 * 64
     need = 18 * 4 * per * 4
     n = lib.gdn_chunk_fwd_workspace_size(2, 512, 4, 4, 32, 32, opts(lib, dtype=pkg_lib.GDN_F32))
-    assert need <= n <= need + 6 * 256
-    # with in-kernel normalisation or raw gates they run the token-serial kernel: no workspace
-    assert lib.gdn_chunk_fwd_workspace_size(2, 512, 4, 4, 32, 32,
-                                            opts(lib, dtype=pkg_lib.GDN_F32, flags=pkg_lib.GDN_NORMALIZE_QK)) == 0
+    assert need <= n <= need + 7 * 256
+    # the in-kernel front end (l2 norm, raw gates) runs inside the same kernels: the same workspace
+    for flags in (pkg_lib.GDN_NORMALIZE_QK, pkg_lib.GDN_RAW_GATES, pkg_lib.GDN_NORMALIZE_QK | pkg_lib.GDN_RAW_GATES):
+        assert lib.gdn_chunk_fwd_workspace_size(2, 512, 4, 4, 32, 32,
+                                                opts(lib, dtype=pkg_lib.GDN_F32, flags=flags)) == n
     assert lib.gdn_chunk_fwd_workspace_size(-1, 512, 4, 4, 32, 32, opts(lib)) == 0
 
 

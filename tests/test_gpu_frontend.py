@@ -1,6 +1,7 @@
 """GPU front end against the oracle: gates formed in-kernel from the raw projections
-(GDN_RAW_GATES) and in-kernel l2 normalisation of q and k (GDN_NORMALIZE_QK), on every kernel
-family (tensor-core prefill, token-serial prefill, decode)."""
+(GDN_RAW_GATES) and in-kernel l2 normalisation of q and k (GDN_NORMALIZE_QK), on the tensor-core
+prefill, the chunked prefill of other shapes (the binding always passes the workspace) and decode;
+the token-serial prefill's front end is covered through the C ABI in test_gpu_prefill_paths."""
 import numpy as np
 import pytest
 
@@ -18,9 +19,9 @@ import gated_deltanet_recurrence_03_gb300 as gdn  # noqa: E402
 
 CASES = {
     "tc_bf16_d128": gi.Workload("fe", "prefill", "bf16", B=2, T=150, Hqk=2, Hv=4, dk=128, dv=128, s0_std=0.1, seed=31),
-    "serial_f32_d64": gi.Workload("fe", "prefill", "f32", B=2, T=70, Hqk=1, Hv=2, dk=64, dv=64, chunk=32,
+    "chunked_f32_d64": gi.Workload("fe", "prefill", "f32", B=2, T=70, Hqk=1, Hv=2, dk=64, dv=64, chunk=32,
                                   s0_std=0.1, seed=32),
-    "serial_bf16_d32": gi.Workload("fe", "prefill", "bf16", B=1, T=90, Hqk=2, Hv=2, dk=32, dv=32, s0_std=0.1, seed=33),
+    "chunked_bf16_d32": gi.Workload("fe", "prefill", "bf16", B=1, T=90, Hqk=2, Hv=2, dk=32, dv=32, s0_std=0.1, seed=33),
 }
 
 

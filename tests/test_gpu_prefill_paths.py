@@ -1,14 +1,16 @@
 """Both prefill paths for shapes off the tensor-core tile (fp32 inputs, head dims 32 / 64), called
 through the C ABI on the same inputs: without a workspace (the token-serial kernel) and with
-gdn_chunk_fwd_workspace_size() bytes (the chunked kernels on split-tf32 MMAs).  Each is compared
-with the fp64 oracle at the parity bound of its input dtype (1e-4 fp32, 2e-2 bf16), outputs and
-final states."""
+gdn_chunk_fwd_workspace_size() bytes (the chunked kernels on split-tf32 MMAs), each plain and with the
+in-kernel front end (gates from raw projections, l2 norm of q and k off the unit sphere).  Each is
+compared with the fp64 oracle at the parity bound of its input dtype (1e-4 fp32, 2e-2 bf16), outputs
+and final states."""
 import ctypes
 
 import numpy as np
 import pytest
 
 import gdn_inputs as gi
+from oracle import gates as ogates
 from oracle import recurrence as orc
 
 pytestmark = pytest.mark.gpu
@@ -35,9 +37,10 @@ CASES = [
 ]
 
 
-def _run(lib, w, x, scale, with_workspace):
+def _run(lib, w, x, scale, with_workspace, raw=None, normalize=False):
     dt = TORCH_DT[w.dtype]
     d = {n: torch.from_numpy(np.ascontiguousarray(x[n])).cuda().to(dt) for n in ("q", "k", "v", "g", "beta")}
+    keep = []
     S0 = None if x.get("S0") is None else torch.from_numpy(x["S0"]).cuda()
     out = torch.empty_like(d["v"])
     sf = torch.empty((w.num_seqs, w.Hv, w.dk, w.dv), dtype=torch.float32, device="cuda")
@@ -45,6 +48,14 @@ def _run(lib, w, x, scale, with_workspace):
     o.dtype = L.GDN_BF16 if w.dtype == "bf16" else L.GDN_F32
     o.scale = scale
     o.stream = torch.cuda.current_stream().cuda_stream
+    if normalize:
+        o.flags |= L.GDN_NORMALIZE_QK
+    if raw is not None:   # g and beta hold the raw projections a and b
+        d["g"] = torch.from_numpy(raw["a"]).cuda().to(dt)
+        d["beta"] = torch.from_numpy(raw["b"]).cuda().to(dt)
+        keep = [torch.from_numpy(raw[n]).cuda().float() for n in ("A_log", "dt_bias")]
+        o.flags |= L.GDN_RAW_GATES
+        o.A_log, o.dt_bias = keep[0].data_ptr(), keep[1].data_ptr()
     cu = None
     if x.get("cu_seqlens") is not None:
         cu = torch.from_numpy(np.asarray(x["cu_seqlens"], np.int32)).cuda()
@@ -68,11 +79,19 @@ def _run(lib, w, x, scale, with_workspace):
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 @pytest.mark.parametrize("with_workspace", [False, True], ids=["token_serial", "chunked"])
-def test_prefill_paths_off_the_tensor_core_tile(lib, w, with_workspace):
+@pytest.mark.parametrize("front", [False, True], ids=["plain", "front_end"])
+def test_prefill_paths_off_the_tensor_core_tile(lib, w, with_workspace, front):
     x = gi.make_prefill_inputs(w)
     scale = w.dk ** -0.5
-    got_o, got_s = _run(lib, w, x, scale, with_workspace)
-    ref_o, ref_s = orc.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], S0=x.get("S0"),
-                               cu_seqlens=x.get("cu_seqlens"), scale=scale)
+    raw = None
+    g, beta = x["g"], x["beta"]
+    if front:   # rows off the unit sphere, so the norm matters; gates formed from a, b
+        x["q"] = gi.round_to_dtype(x["q"] * 2.5, w.dtype)
+        x["k"] = gi.round_to_dtype(x["k"] * 0.45, w.dtype)
+        raw = gi.make_raw_gates(w)
+        g, beta = ogates.gates_from_raw(raw["a"], raw["b"], raw["A_log"], raw["dt_bias"])
+    got_o, got_s = _run(lib, w, x, scale, with_workspace, raw=raw, normalize=front)
+    ref_o, ref_s = orc.forward(x["q"], x["k"], x["v"], g, beta, S0=x.get("S0"),
+                               cu_seqlens=x.get("cu_seqlens"), scale=scale, normalize_qk=front)
     eo, es = rel_err(ref_o, got_o), rel_err(ref_s, got_s)
     assert eo <= TOL[w.dtype] and es <= TOL[w.dtype], (w.name, eo, es)
