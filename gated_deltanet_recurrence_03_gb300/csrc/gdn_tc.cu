@@ -293,12 +293,16 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     // ---- [K; Q] K^T : rows 0-63 K K^T, rows 64-127 Q K^T
     mbar_wait_bounded(bar_tma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+    // shared-memory descriptors built once; (address >> 4) < 2^14 in this CTA, so a byte offset o moves
+    // a descriptor by o >> 4 without a carry
+    const uint64_t dKQk = smem_desc(sb + P_KQ, 16, 1024), dKQm = smem_desc(sb + P_KQ, 16384, 1024),
+                   dTOP = smem_desc(sb + P_TOP, 16384, 1024);
     if (tid == 0) {
         tc_fence_after();
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = P_KQ + (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_bf16(tmem + T_GRAM, smem_desc(sb + off, 16, 1024), smem_desc(sb + off, 16, 1024),
-                     idesc_bf16(128, 64, 0, 0), ks > 0);
+            const uint64_t d = dKQk + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
+            mma_bf16(tmem + T_GRAM, d, d, idesc_bf16(128, 64, 0, 0), ks > 0);
         }
         mma_commit(bar_mma);
     }
@@ -486,9 +490,9 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // ---- [W_0; W_1] = [T_0 D_0; T_1 D_1] K
     if (tid == 0) {
         tc_fence_after();
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16_ta(tmem + T_W, tmem + T_TD + 8 * ks, smem_desc(sb + P_KQ + ks * 2048, 16384, 1024),
-                        idesc_bf16(128, 128, 0, 1), ks > 0);
+            mma_bf16_ta(tmem + T_W, tmem + T_TD + 8 * ks, dKQm + ((ks * 2048) >> 4), idesc_bf16(128, 128, 0, 1), ks > 0);
         mma_commit(bar_mma);
     }
     mbar_wait_bounded(bar_mma, 1, abort_flag, status, kStatusTimeout, kWaitLimitNs);
@@ -514,9 +518,9 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // ---- blockdiag(P_0, P_1) [-W | Tb]: -P W and P Tb for both heads
     if (tid == 0) {
         tc_fence_after();
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            mma_bf16_ta(tmem + T_PW, tmem + T_AP + 8 * ks, smem_desc(sb + P_TOP + ks * 2048, 16384, 1024),
-                        idesc_bf16(128, 192, 0, 1), ks > 0);
+            mma_bf16_ta(tmem + T_PW, tmem + T_AP + 8 * ks, dTOP + ((ks * 2048) >> 4), idesc_bf16(128, 192, 0, 1), ks > 0);
         mma_commit(bar_mma);
     }
     // this thread's query row, read before the K/Q panels are reused for the outputs
@@ -678,13 +682,18 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     };
     // D1(c) = [Tb; P Tb] V_c: the part of A1 [S; V] that does not depend on the state, issued one chunk
     // ahead so it runs while the previous chunk's state update is on the critical path.
+    // Shared-memory descriptors built once: the 14-bit address field holds (address >> 4) < 2^14 for
+    // every operand of this CTA, so a byte offset o moves a descriptor by o >> 4 without a carry.
+    const uint64_t dA1 = smem_desc(sb + C_A1, 16, 1024), dVT = smem_desc(sb + C_VT, 1024, 1024),
+                   dSB = smem_desc(sb + C_SB, 1024, 1024), dKT = smem_desc(sb + C_KT, 8192, 1024),
+                   dUB = smem_desc(sb + C_UB, 1024, 1024);
     auto issue_v_part = [&](long long c) {
         const int st = (int)(c & 1);
-        const uint32_t a1 = sb + C_A1 + st * kA1Bytes + 2 * 16384;
+        const uint64_t a1 = dA1 + ((st * kA1Bytes + 2 * 16384) >> 4), vt = dVT + ((st * 8192) >> 4);
         const uint32_t d1 = tmem + 64 + 64 * (uint32_t)st;
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(d1, smem_desc(a1 + ks * 32, 16, 1024), smem_desc(sb + C_VT + st * 8192 + ks * 2048, 1024, 1024),
-                     idesc_bf16(128, 64, 0, 1), ks > 0);
+            mma_bf16(d1, a1 + ((ks * 32) >> 4), vt + ((ks * 2048) >> 4), idesc_bf16(128, 64, 0, 1), ks > 0);
     };
 
     if (nch == 0) {   // empty sequence: the final state is the initial state
@@ -739,10 +748,11 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             if (tid == 0) {   // D1 += A1[:, S part] S   (the V part is already in D1)
                 wait_a(c);
                 tc_fence_after();
-                const uint32_t a1 = sb + C_A1 + st * kA1Bytes;
+                const uint64_t a1 = dA1 + ((st * kA1Bytes) >> 4);
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(d1, smem_desc(a1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                             smem_desc(sb + C_SB + ks * 2048, 1024, 1024), idesc_bf16(128, 64, 0, 1), 1);
+                    mma_bf16(d1, a1 + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), dSB + ((ks * 2048) >> 4),
+                             idesc_bf16(128, 64, 0, 1), 1);
                 mma_commit(bar_mma1);
             }
             if (c > 0) {   // TMEM columns 0-63 (the state) are not touched by the D1 MMA
@@ -774,9 +784,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 named_barrier_sync(1, 256);
                 if (tid == 0) {   // S (gamma_C-scaled, in TMEM) += K^T (b U); then the next chunk's V part
                     tc_fence_after();
+                    const uint64_t kt = dKT + ((kst * 16384) >> 4);
+#pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem, smem_desc(sb + C_KT + kst * 16384 + ks * 2048, 8192, 1024),
-                                 smem_desc(sb + C_UB + ks * 2048, 1024, 1024), idesc_bf16(128, 64, 1, 1), 1);
+                        mma_bf16(tmem, kt + ((ks * 2048) >> 4), dUB + ((ks * 2048) >> 4), idesc_bf16(128, 64, 1, 1), 1);
                     mma_commit(bar_mma2);
                     if (c + 1 < nch && wait_a(c + 1)) issue_v_part(c + 1);
                 }
