@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # were taken on (sha256 prefix of the file); None once the source has changed.
 NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix of that file at capture, dram read + write bytes per launch)
-    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "0bcae087cc59422e", 139425536 + 344787456),
-    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "0bcae087cc59422e", 612621568 + 119872000),
+    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "225e61d62044eedf", 139433728 + 344655360),
+    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "225e61d62044eedf", 612453632 + 119804928),
     "decode_step_kernel": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_decode.cu", "0a3ae9abf76d8679", 541133568 + 480455680),
 }
 
@@ -683,10 +683,17 @@ def small_config_rates():
 def cpu_baseline(budget_s=15.0):
     rate, dt, cores = oracle_rate(128)                      # calibration
     n = int(max(128, min(PREFILL.T, rate * budget_s / PREFILL.B)))
-    rate, dt, cores = oracle_rate(n)
+    # when the whole workload takes less than the budget, repeat it (at most 15 runs) and report the
+    # aggregate rate over all runs
+    runs, total = 0, 0.0
+    while runs < 15 and (runs == 0 or total < budget_s):
+        _, dt, cores = oracle_rate(n)
+        runs, total = runs + 1, total + dt
+    rate = runs * PREFILL.B * n / total
+    what = "the whole workload" if n == PREFILL.T else f"the first {n} tokens of both sequences"
     return {"value": round(rate, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {n} tokens of both sequences of prefill_gqa_8k, all 32 value heads, fp64 "
-                      f"token loop, {dt:.1f} s",
+            "sample": f"{what} of prefill_gqa_8k, all 32 value heads, fp64 token loop, {runs} run(s) in "
+                      f"{total:.1f} s",
             "small_workloads_tokens_per_s": small_config_rates()}
 
 
