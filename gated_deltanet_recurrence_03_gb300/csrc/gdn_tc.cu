@@ -541,40 +541,42 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();   // every thread holds its q row: the K/Q panels are free
     {
         const float qs = scale * __expf(sG[hh * 64 + r]) * sRQ[r];   // scale * gamma_r / |q_r|
-        for (int cb = 0; cb < 6; ++cb) {
-            uint32_t a[32];
-            tmem_ld32(tl + T_PW + 32 * cb, a);
-            tmem_wait_ld();
-            uint8_t* pan = sm + bot_panel(3 * hh + (cb >> 1));
+        // panel by panel, so that the bulk stores of the first panels drain while the later ones are built
+        for (int p = 0; p < 3; ++p) {
+            for (int cb = 2 * p; cb < 2 * p + 2; ++cb) {
+                uint32_t a[32];
+                tmem_ld32(tl + T_PW + 32 * cb, a);
+                tmem_wait_ld();
+                uint8_t* pan = sm + bot_panel(3 * hh + p);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t chunk = (cb & 1) * 4 + c;
-                float x[8];
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t chunk = (cb & 1) * 4 + c;
+                    float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(a[8 * c + e]);
-                if (cb < 4) {   // Q' = scale gamma_r q_r - P W
-                    const bf16* qe = reinterpret_cast<const bf16*>(&qrow[(cb >> 1) * 8 + chunk]);
+                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(a[8 * c + e]);
+                    if (cb < 4) {   // Q' = scale gamma_r q_r - P W
+                        const bf16* qe = reinterpret_cast<const bf16*>(&qrow[p * 8 + chunk]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = fmaf(qs, __bfloat162float(qe[e]), x[e]);
+                        for (int e = 0; e < 8; ++e) x[e] = fmaf(qs, __bfloat162float(qe[e]), x[e]);
+                    }
+                    *reinterpret_cast<uint4*>(pan + swz(r, chunk)) =
+                        make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
                 }
-                *reinterpret_cast<uint4*>(pan + swz(r, chunk)) =
-                    make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+            }
+            fence_proxy_async_smem();
+            if (p == 2) tc_fence_before();   // every TMEM read of this CTA precedes the deallocation
+            __syncthreads();
+            if (tid == 0) {   // panel p of A1 for each head: [TOP rows of the head | output rows of the head]
+                for (int h = 0; h < 2; ++h)
+                    bulk_s2g(ws_a1 + ((size_t)slot * Hv + (h == 0 ? hA : hB)) * kA1Bytes + p * 16384 + 8192,
+                             sb + bot_panel(3 * h + p), 8192);
+                bulk_commit();
             }
         }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {   // A1 of each head: panel p = [TOP rows of the head | output rows of the head]
-        for (int h = 0; h < 2; ++h) {
-            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + (h == 0 ? hA : hB)) * kA1Bytes;
-            for (int p = 0; p < 3; ++p) bulk_s2g(dst + p * 16384 + 8192, sb + bot_panel(3 * h + p), 8192);
-        }
-        bulk_commit();
-        bulk_wait_read();   // shared memory may be released; the global writes finish on their own
-    }
-    __syncthreads();
     if (warp == 0) {
+        if (tid == 0) bulk_wait_read();   // shared memory may be released; the global writes finish on their own
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 256);
     }
