@@ -43,11 +43,14 @@ def _device_inputs(seed, T):
     return w, d
 
 
-def _call(lib, fn, w, d, workspace=None):
+def _call(lib, fn, w, d, workspace=None, dtype=None, flags=0):
     out = torch.empty_like(d["v"])
     sf = torch.empty((w.B, w.Hv, w.dk, w.dv), dtype=torch.float32, device="cuda")
     o = L.default_opts(lib)
     o.stream = torch.cuda.current_stream().cuda_stream
+    if dtype is not None:
+        o.dtype = dtype
+    o.flags = flags
     if workspace is not None:
         o.workspace = workspace.data_ptr()
         o.workspace_bytes = workspace.numel()
@@ -89,3 +92,30 @@ def test_noalloc_refuses_problems_larger_than_its_scratch(lib):
     st, _, _ = _call(lib, lib.gdn_chunk_fwd_noalloc, w, d)
     assert st == L.GDN_ERR_WORKSPACE
     assert b"64 MiB" in lib.gdn_last_error()
+
+
+@pytest.mark.parametrize("T", [300, 4096], ids=["chunked_from_scratch", "token_serial_fallback"])
+def test_noalloc_off_the_tensor_core_tile(lib, T):
+    # fp32, head dim 128, in-kernel l2 norm: a short call runs the chunked kernels on the built-in
+    # scratch; at 32 value heads x 4096 tokens their workspace exceeds 64 MiB and the call falls back
+    # to the token-serial kernel, which needs none.  Either must match the workspace entry point.
+    w = gi.Workload("noalloc_f32", "prefill", "f32", B=1, T=T, Hqk=16, Hv=32, dk=128, dv=128, s0_std=0.1,
+                    seed=23)
+    x = gi.make_prefill_inputs(w)
+    d = {n: torch.from_numpy(np.ascontiguousarray(x[n])).cuda().float() for n in ("q", "k", "v", "g", "beta")}
+    d["q"], d["k"] = 2.0 * d["q"], 0.5 * d["k"]   # off the unit sphere, so the norm matters
+    d["S0"] = torch.from_numpy(x["S0"]).cuda()
+    o = L.default_opts(lib)
+    o.dtype, o.flags = L.GDN_F32, L.GDN_NORMALIZE_QK
+    need = lib.gdn_chunk_fwd_workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv, ctypes.byref(o))
+    assert (need <= 64 << 20) == (T == 300)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st_ref, out_ref, sf_ref = _call(lib, lib.gdn_chunk_fwd, w, d, workspace=ws, dtype=L.GDN_F32,
+                                    flags=L.GDN_NORMALIZE_QK)
+    assert st_ref == L.GDN_OK, lib.gdn_last_error()
+    st, out, sf = _call(lib, lib.gdn_chunk_fwd_noalloc, w, d, dtype=L.GDN_F32, flags=L.GDN_NORMALIZE_QK)
+    assert st == L.GDN_OK, lib.gdn_last_error()
+    torch.cuda.synchronize()
+    assert lib.gdn_check_device_status(None) == L.GDN_OK
+    # both paths are within 1e-4 of the fp64 oracle, so within 2e-4 of each other
+    assert _rel(out_ref, out) <= 2e-4 and _rel(sf_ref, sf) <= 2e-4
