@@ -118,7 +118,7 @@ cudaError_t launch_backward(const BackwardArgs& a);
 size_t chunked_prefill_workspace_bytes(int B, int T, int Hv, int dk, int dv, int nseq, bool packed);
 cudaError_t launch_chunked_prefill(const PrefillArgs& a);
 
-// The driver's cuTensorMapEncodeTiled (looked up once), or nullptr when the driver lacks it.
+// The CUDA driver's cuTensorMapEncodeTiled (looked up once), or nullptr when the CUDA driver lacks it.
 void* tensor_map_encoder();
 
 cudaError_t launch_conv_fwd(const ConvArgs& a);

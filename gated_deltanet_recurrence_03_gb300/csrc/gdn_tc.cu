@@ -766,7 +766,6 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
             tc_fence_after();
             const int kst = (int)(c % kKStages);
-            if (tid == kProducer && c + 2 < nch) issue_loads_a(c + 2);   // A1 and V of this stage are consumed
             uint32_t a[32];
             tmem_ld32(tl + 64 + 64 * st + cb, a);
             tmem_wait_ld();
@@ -795,6 +794,9 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 }
             } else {             // output row of token R - 64
                 named_barrier_arrive(1, 256);
+                // A1 and V of this stage are consumed (D1 is complete); issued after the arrival, off the
+                // state-update path
+                if (tid == kProducer && c + 2 < nch) issue_loads_a(c + 2);
                 const int r = R - 64;
                 if (r < n) {
                     uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z + cb);
@@ -816,7 +818,6 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
             tc_fence_after();
-            if (tid == kProducer && c + kKStages < nch) issue_loads_k(c + kKStages);   // K, vector consumed
             {   // new state row R: bf16 copy for the next D1 now, gamma-scaled copy to TMEM next step
                 uint32_t v[32];
                 tmem_ld32(tl + cb, v);
@@ -843,6 +844,8 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
+            // K and the vector of this stage are consumed (state update and epilogues done)
+            if (tid == kProducer && c + kKStages < nch) issue_loads_k(c + kKStages);
         }
     }
     __syncthreads();

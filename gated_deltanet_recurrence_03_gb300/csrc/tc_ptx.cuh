@@ -65,13 +65,15 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
 }
 
 // Wait for phase `parity` of `bar`, giving up after limit_ns.  On give-up the status word gets
-// `flag`, *abort is set, and false is returned; once *abort is set every later wait returns at
-// once, so a failed kernel drains quickly instead of waiting once per step.
+// `flag`, *abort is set, and false is returned; once *abort is set every later wait that would
+// have to wait returns at once, so a failed kernel drains quickly instead of waiting once per step.
+// A phase that has already completed is reported at once (the abort flag is read only on the
+// slow path: its shared-memory load would otherwise sit on every fast wait).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   unsigned* status, unsigned flag,
                                                   unsigned long long limit_ns) {
-    if (*abort) return false;
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
     const unsigned long long t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
