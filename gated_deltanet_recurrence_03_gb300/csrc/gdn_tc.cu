@@ -594,11 +594,16 @@ constexpr uint32_t C_SMEM = C_BAR + 128 + 1024;
 constexpr int kKStages = 3;
 // Operands arrive in two rings freed at different times: A1 and the V slice (2 stages, consumed by
 // D1) and the K tile with the b / gamma_C vector (3 stages, consumed by the state update and the
-// epilogues).  One lane of an output warp issues the loads, off the critical path.
+// epilogues).
 constexpr uint32_t kStageBytesA = kA1Bytes + 8192;
 constexpr uint32_t kStageBytesK = 16384 + kVecFloats * 4;
-// 8 warps: warps w and w + 4 read TMEM lane quarter w % 4 and split the slice's 64 columns.
-constexpr int kChainThreads = 256;
+// 9 warps.  Warps 0-7 are the epilogue warps: warps w and w + 4 read TMEM lane quarter w % 4 and split
+// the slice's 64 columns.  Lane 0 of warp 8 issues every MMA and every load and does no epilogue work:
+// an issuing thread that also ran an epilogue made its warp the last to reach each barrier (its
+// proxy fence and its late start after the MMA issue sat on the chain's critical path).
+constexpr int kEpilogueThreads = 256;
+constexpr int kChainThreads = kEpilogueThreads + 32;
+constexpr int kIssuer = kEpilogueThreads;
 // TMEM columns: state S 0-63; D1 of even chunks 64-127, of odd chunks 128-191.
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
@@ -621,10 +626,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                    bar_mma2 = sb + C_BAR + 48;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_BAR + 56);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C_BAR + 60);
-    constexpr int kProducer = 192;          // lane 0 of warp 6 (an output warp) issues the loads
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
+    const bool epi = warp < kEpilogueThreads / 32;   // an epilogue warp (warp 8 issues)
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
     const int R = 32 * quarter + lane;      // TMEM lane = accumulator row
     const int cb = 32 * half;               // this thread's 32 of the slice's 64 columns
     const int z = blockIdx.x % kSlices;
@@ -699,20 +704,20 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     };
 
     if (nch == 0) {   // empty sequence: the final state is the initial state
-        if (S_final) {
+        if (S_final && epi) {
             for (int e = 0; e < 32; e += 4) {
                 const float4 v = S0 ? *reinterpret_cast<const float4*>(S0 + srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
                 *reinterpret_cast<float4*>(S_final + srow + e) = v;
             }
         }
     } else {
-        if (tid == kProducer) {
+        if (tid == kIssuer) {
             for (long long c = 0; c < 2 && c < nch; ++c) issue_loads_a(c);
             for (long long c = 0; c < kKStages && c < nch; ++c) issue_loads_k(c);
         }
         // prologue: bf16 copy of S0 into SB, gamma_C(0) * S0 into TMEM, V part of chunk 0
-        wait_k(0);
-        {
+        if (epi) {
+            wait_k(0);
             const float g0 = reinterpret_cast<const float*>(sm + C_VEC)[64];   // vector of chunk 0 (K stage 0)
             uint32_t v[32];
 #pragma unroll
@@ -730,12 +735,11 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(g0 * __uint_as_float(v[e]));
             tmem_st32(tl + cb, v);
-        }
-        if (tid == 0 && wait_a(0)) {
+            tmem_wait_st();
+        } else if (lane == 0 && wait_a(0)) {
             tc_fence_after();
             issue_v_part(0);
         }
-        tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -747,105 +751,116 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             const long long tc0 = s0 + c * kC;
             const int n = (int)min((long long)kC, s1 - tc0);
             const uint32_t d1 = tmem + 64 + 64 * (uint32_t)st;
-            if (tid == 0) {   // D1 += A1[:, S part] S   (the V part is already in D1)
-                wait_a(c);
-                tc_fence_after();
-                const uint64_t a1 = dA1 + ((st * kA1Bytes) >> 4);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(d1, a1 + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), dSB + ((ks * 2048) >> 4),
-                             idesc_bf16(128, 64, 0, 1), 1);
-                mma_commit(bar_mma1);
-            }
-            if (c > 0) {   // TMEM columns 0-63 (the state) are not touched by the D1 MMA
-                tmem_st32(tl + cb, spend);
-                tmem_wait_st();
-                tc_fence_before();
-            }
-            wait_k(c);
-            mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
-            tc_fence_after();
             const int kst = (int)(c % kKStages);
-            uint32_t a[32];
-            tmem_ld32(tl + 64 + 64 * st + cb, a);
-            tmem_wait_ld();
-            if (quarter < 2) {   // U row R scaled by b_r = exp(G_C - G_r) -> B operand of the state update
-                const float br = reinterpret_cast<const float*>(sm + C_VEC + kst * 512)[R];
+            const bool last = (c + 1 == nch);
+            if (!epi) {   // ---- the issuing warp
+                if (lane == 0) {   // D1 += A1[:, S part] S   (the V part is already in D1)
+                    wait_a(c);
+                    tc_fence_after();
+                    const uint64_t a1 = dA1 + ((st * kA1Bytes) >> 4);
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = br * __uint_as_float(a[8 * c8 + e]);
-                    *reinterpret_cast<uint4*>(sm + C_UB + swz(R, (cb >> 3) + c8)) =
-                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16(d1, a1 + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), dSB + ((ks * 2048) >> 4),
+                                 idesc_bf16(128, 64, 0, 1), 1);
+                    mma_commit(bar_mma1);
+                    // the K stage of chunk c - 1 is free once its state update is complete
+                    if (c >= 1 && c + 2 < nch) {
+                        mbar_wait_bounded(bar_mma2, par ^ 1u, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+                        tc_fence_after();
+                        issue_loads_k(c + 2);
+                    }
+                    // A1 and V of this stage are free once D1 is complete
+                    mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+                    tc_fence_after();
+                    if (c + 2 < nch) issue_loads_a(c + 2);
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                // all 256 threads arrive (their gamma-scaled state rows are in TMEM); only the U warps wait
-                named_barrier_sync(1, 256);
-                if (tid == 0) {   // S (gamma_C-scaled, in TMEM) += K^T (b U); then the next chunk's V part
+                __syncwarp();
+                named_barrier_sync(1, kChainThreads);   // b U is in shared memory, every state row in TMEM
+                if (lane == 0) {   // S (gamma_C-scaled, in TMEM) += K^T (b U); then the next chunk's V part
                     tc_fence_after();
                     const uint64_t kt = dKT + ((kst * 16384) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_bf16(tmem, kt + ((ks * 2048) >> 4), dUB + ((ks * 2048) >> 4), idesc_bf16(128, 64, 1, 1), 1);
                     mma_commit(bar_mma2);
-                    if (c + 1 < nch && wait_a(c + 1)) issue_v_part(c + 1);
+                    if (!last && wait_a(c + 1)) issue_v_part(c + 1);
                 }
-            } else {             // output row of token R - 64
-                named_barrier_arrive(1, 256);
-                // A1 and V of this stage are consumed (D1 is complete); issued after the arrival, off the
-                // state-update path
-                if (tid == kProducer && c + 2 < nch) issue_loads_a(c + 2);
-                const int r = R - 64;
-                if (r < n) {
-                    uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z + cb);
+                __syncwarp();
+            } else {      // ---- the epilogue warps
+                if (c > 0) {   // TMEM columns 0-63 (the state) are not touched by the D1 MMA
+                    tmem_st32(tl + cb, spend);
+                    tmem_wait_st();
+                    tc_fence_before();
+                }
+                wait_k(c);
+                mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+                tc_fence_after();
+                uint32_t a[32];
+                tmem_ld32(tl + 64 + 64 * st + cb, a);
+                tmem_wait_ld();
+                if (quarter < 2) {   // U row R scaled by b_r = exp(G_C - G_r) -> B operand of the state update
+                    const float br = reinterpret_cast<const float*>(sm + C_VEC + kst * 512)[R];
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
-                        const uint32_t* src = a + 8 * c8;
-                        dst[c8] = make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
-                                             pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
-                                             pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
-                                             pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = br * __uint_as_float(a[8 * c8 + e]);
+                        *reinterpret_cast<uint4*>(sm + C_UB + swz(R, (cb >> 3) + c8)) =
+                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    named_barrier_arrive(1, kChainThreads);
+                } else {             // output row of token R - 64
+                    tc_fence_before();
+                    named_barrier_arrive(1, kChainThreads);   // its gamma-scaled state rows are in TMEM
+                    const int r = R - 64;
+                    if (r < n) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z + cb);
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const uint32_t* src = a + 8 * c8;
+                            dst[c8] = make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                                 pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                                 pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                                                 pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
+                        }
                     }
                 }
-            }
-            const bool last = (c + 1 == nch);
-            float gnext = 1.f;
-            if (!last) {   // the next chunk's gamma_C, read while the state update runs
-                wait_k(c + 1);
-                gnext = reinterpret_cast<const float*>(sm + C_VEC + (int)((c + 1) % kKStages) * 512)[64];
-            }
-            mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
-            tc_fence_after();
-            {   // new state row R: bf16 copy for the next D1 now, gamma-scaled copy to TMEM next step
-                uint32_t v[32];
-                tmem_ld32(tl + cb, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const float* f = reinterpret_cast<const float*>(v + 8 * c4);
-                    *reinterpret_cast<uint4*>(sm + C_SB + swz(R, (cb >> 3) + c4)) =
-                        make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+                float gnext = 1.f;
+                if (!last) {   // the next chunk's gamma_C, read while the state update runs
+                    wait_k(c + 1);
+                    gnext = reinterpret_cast<const float*>(sm + C_VEC + (int)((c + 1) % kKStages) * 512)[64];
                 }
-                if (last) {
-                    if (S_final) {
+                mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+                tc_fence_after();
+                {   // new state row R: bf16 copy for the next D1 now, gamma-scaled copy to TMEM next step
+                    uint32_t v[32];
+                    tmem_ld32(tl + cb, v);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4*>(S_final + srow + e) =
-                                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                                            __uint_as_float(v[e + 3]));
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const float* f = reinterpret_cast<const float*>(v + 8 * c4);
+                        *reinterpret_cast<uint4*>(sm + C_SB + swz(R, (cb >> 3) + c4)) =
+                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
                     }
-                } else {
+                    if (last) {
+                        if (S_final) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) spend[e] = __float_as_uint(gnext * __uint_as_float(v[e]));
+                            for (int e = 0; e < 32; e += 4)
+                                *reinterpret_cast<float4*>(S_final + srow + e) =
+                                    make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                                __uint_as_float(v[e + 3]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) spend[e] = __float_as_uint(gnext * __uint_as_float(v[e]));
+                    }
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
             __syncthreads();
-            // K and the vector of this stage are consumed (state update and epilogues done)
-            if (tid == kProducer && c + kKStages < nch) issue_loads_k(c + kKStages);
         }
     }
     __syncthreads();
