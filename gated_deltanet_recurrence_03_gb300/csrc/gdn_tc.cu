@@ -598,12 +598,15 @@ constexpr int kKStages = 3;
 constexpr uint32_t kStageBytesA = kA1Bytes + 8192;
 constexpr uint32_t kStageBytesK = 16384 + kVecFloats * 4;
 // 9 warps.  Warps 0-7 are the epilogue warps: warps w and w + 4 read TMEM lane quarter w % 4 and split
-// the slice's 64 columns.  Lane 0 of warp 8 issues every MMA and every load and does no epilogue work:
-// an issuing thread that also ran an epilogue made its warp the last to reach each barrier (its
-// proxy fence and its late start after the MMA issue sat on the chain's critical path).
+// the slice's 64 columns.  Lane 0 of warp 8 issues every MMA and does no epilogue work: an issuing
+// thread that also ran an epilogue made its warp the last to reach each barrier.  Lane 0 of warp 6 (an
+// output warp, with slack) issues the operand loads once the state-update barrier has passed: the
+// shared-memory proxy fences of the epilogues measured several times slower while a bulk copy was
+// landing in shared memory, so the copies land between the two epilogues.
 constexpr int kEpilogueThreads = 256;
 constexpr int kChainThreads = kEpilogueThreads + 32;
 constexpr int kIssuer = kEpilogueThreads;
+constexpr int kProducer = 192;
 // TMEM columns: state S 0-63; D1 of even chunks 64-127, of odd chunks 128-191.
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
@@ -763,16 +766,6 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                         mma_bf16(d1, a1 + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4), dSB + ((ks * 2048) >> 4),
                                  idesc_bf16(128, 64, 0, 1), 1);
                     mma_commit(bar_mma1);
-                    // the K stage of chunk c - 1 is free once its state update is complete
-                    if (c >= 1 && c + 2 < nch) {
-                        mbar_wait_bounded(bar_mma2, par ^ 1u, abort_flag, status, kStatusTimeout, kWaitLimitNs);
-                        tc_fence_after();
-                        issue_loads_k(c + 2);
-                    }
-                    // A1 and V of this stage are free once D1 is complete
-                    mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
-                    tc_fence_after();
-                    if (c + 2 < nch) issue_loads_a(c + 2);
                 }
                 __syncwarp();
                 named_barrier_sync(1, kChainThreads);   // b U is in shared memory, every state row in TMEM
@@ -813,7 +806,16 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     named_barrier_arrive(1, kChainThreads);
                 } else {             // output row of token R - 64
                     tc_fence_before();
-                    named_barrier_arrive(1, kChainThreads);   // its gamma-scaled state rows are in TMEM
+                    if (warp == kProducer / 32) {   // waits for the barrier, then issues the loads
+                        named_barrier_sync(1, kChainThreads);
+                        if (lane == 0) {
+                            if (c + 2 < nch) issue_loads_a(c + 2);   // A1 and V of this stage: D1 is complete
+                            // the K stage of chunk c - 1: its state update completed before the last step ended
+                            if (c >= 1 && c + 2 < nch) issue_loads_k(c + 2);
+                        }
+                    } else {
+                        named_barrier_arrive(1, kChainThreads);   // its gamma-scaled state rows are in TMEM
+                    }
                     const int r = R - 64;
                     if (r < n) {
                         uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z + cb);
