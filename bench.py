@@ -42,8 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # were taken on (sha256 prefix of the file); None once the source has changed.
 NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix of that file at capture, dram read + write bytes per launch)
-    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "6ada995c3b2dd37e", 139449344 + 344672256),
-    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "6ada995c3b2dd37e", 612446464 + 120006656),
+    "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "3302073e7ce961a4", 139527936 + 345190144),
+    "gdn_tc_chain": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "3302073e7ce961a4", 612445952 + 120108544),
     "decode_step_kernel": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_decode.cu", "0a3ae9abf76d8679", 541133568 + 480455680),
 }
 

@@ -522,6 +522,13 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int ks = 0; ks < 8; ++ks)
             mma_bf16_ta(tmem + T_PW, tmem + T_AP + 8 * ks, dTOP + ((ks * 2048) >> 4), idesc_bf16(128, 192, 0, 1), ks > 0);
         mma_commit(bar_mma);
+        // the [-W | Tb] rows of A1 are final (they are this MMA's B operand): their stores read the same
+        // shared memory while the MMA runs, and issuing them here keeps the issue off the barrier below
+        for (int h = 0; h < 2; ++h) {
+            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + (h == 0 ? hA : hB)) * kA1Bytes;
+            for (int p = 0; p < 3; ++p) bulk_s2g(dst + p * 16384, sb + P_TOP + p * 16384 + h * 8192, 8192);
+        }
+        bulk_commit();
     }
     // this thread's query row, read before the K/Q panels are reused for the outputs
     const int hh = R >> 6, r = R & 63;
@@ -531,13 +538,6 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         qrow[c] = *reinterpret_cast<const uint4*>(sm + P_KQ + (c >> 3) * 16384 + 8192 + swz(r, c & 7));
     mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    if (tid == 0) {   // the [-W | Tb] rows of A1 are final: start their stores now
-        for (int h = 0; h < 2; ++h) {
-            uint8_t* dst = ws_a1 + ((size_t)slot * Hv + (h == 0 ? hA : hB)) * kA1Bytes;
-            for (int p = 0; p < 3; ++p) bulk_s2g(dst + p * 16384, sb + P_TOP + p * 16384 + h * 8192, 8192);
-        }
-        bulk_commit();
-    }
     __syncthreads();   // every thread holds its q row: the K/Q panels are free
     {
         const float qs = scale * __expf(sG[hh * 64 + r]) * sRQ[r];   // scale * gamma_r / |q_r|
