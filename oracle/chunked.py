@@ -47,8 +47,35 @@ def chunk_step(Q, K, V, g, beta, S0, scale=1.0):
     return O, S_n
 
 
-def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, chunk=64, scale=1.0):
-    """Same interface and layouts as :func:`oracle.recurrence.forward` (fp64 results)."""
+def chunk_step_folded(Q, K, V, g, beta, S0, scale=1.0):
+    """The same chunk with U eliminated, so that the state moves by one affine map per chunk.
+
+    With b = exp(G_n - G) and K~ = diag(b) K, substituting U = U~ - W S0 into the update and the
+    outputs gives
+        S_n = gamma_n S0 + (-K~^T W) S0 + K~^T U~
+        O   = (scale diag(gamma) Q - P W) S0 + P U~,   P = scale (M * Q K^T)
+    (the first line is the form in which a chunk step needs a single product with the state)."""
+    n = Q.shape[0]
+    G = np.cumsum(g)
+    gamma = np.exp(G)
+    D = G[:, None] - G[None, :]
+    lower = np.tril(np.ones((n, n), dtype=bool), -1)
+    causal = np.tril(np.ones((n, n), dtype=bool), 0)
+    A = np.where(lower, np.exp(np.where(lower, D, 0.0)) * (K @ K.T), 0.0)
+    Tmat = np.linalg.solve(np.eye(n) + beta[:, None] * A, np.eye(n))
+    W = Tmat @ ((beta * gamma)[:, None] * K)
+    Ut = Tmat @ (beta[:, None] * V)
+    Kt = np.exp(G[-1] - G)[:, None] * K
+    P = scale * np.where(causal, np.exp(np.where(causal, D, 0.0)), 0.0) * (Q @ K.T)
+    S_n = gamma[-1] * S0 + (-Kt.T @ W) @ S0 + Kt.T @ Ut
+    O = (scale * gamma[:, None] * Q - P @ W) @ S0 + P @ Ut
+    return O, S_n
+
+
+def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, chunk=64, scale=1.0, folded=False):
+    """Same interface and layouts as :func:`oracle.recurrence.forward` (fp64 results).  With
+    folded=True every chunk goes through :func:`chunk_step_folded`."""
+    step = chunk_step_folded if folded else chunk_step
     q, k, v, g, beta = (np.asarray(t, dtype=np.float64) for t in (q, k, v, g, beta))
     B, T, Hqk, dk = q.shape
     Hv, dv = v.shape[2], v.shape[3]
@@ -66,8 +93,8 @@ def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, chunk=64, scale=1.0):
             S = np.zeros((dk, dv)) if S0 is None else np.array(S0[i, h], dtype=np.float64)
             for c0 in range(t0, t1, chunk):
                 c1 = min(c0 + chunk, t1)
-                O, S = chunk_step(q[b, c0:c1, hk], k[b, c0:c1, hk], v[b, c0:c1, h], g[b, c0:c1, h],
-                                  beta[b, c0:c1, h], S, scale)
+                O, S = step(q[b, c0:c1, hk], k[b, c0:c1, hk], v[b, c0:c1, h], g[b, c0:c1, h],
+                            beta[b, c0:c1, h], S, scale)
                 out[b, c0:c1, h] = O
             S_final[i, h] = S
     return out, S_final

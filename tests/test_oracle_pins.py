@@ -289,6 +289,27 @@ def test_chunk_form_equals_token_loop(chunk):
     np.testing.assert_allclose(s_chk, s_ref, rtol=0, atol=1e-12 * np.abs(s_ref).max())
 
 
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_folded_chunk_form_equals_token_loop(chunk):
+    """The chunk step with U eliminated (one affine map of the state per chunk:
+    S_n = (gamma_n I - K~^T W) S0 + K~^T U~) equals the token loop, ragged and packed, with GQA."""
+    rng = np.random.default_rng(20 + chunk)
+    lens = [150, 9, 64]
+    T = sum(lens)
+    Hqk, Hv, dk, dv = 2, 4, 16, 8
+    q = unit_rows(rng.normal(size=(1, T, Hqk, dk)))
+    k = unit_rows(rng.normal(size=(1, T, Hqk, dk)))
+    v = rng.normal(size=(1, T, Hv, dv))
+    g = np.log(1 / (1 + np.exp(-rng.normal(3, 1, size=(1, T, Hv)))))
+    beta = 1 / (1 + np.exp(-rng.normal(size=(1, T, Hv))))
+    S0 = 0.1 * rng.normal(size=(len(lens), Hv, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o_ref, s_ref = orc.forward(q, k, v, g, beta, S0=S0, cu_seqlens=cu, scale=0.5)
+    o_f, s_f = chunked.forward(q, k, v, g, beta, S0=S0, cu_seqlens=cu, chunk=chunk, scale=0.5, folded=True)
+    np.testing.assert_allclose(o_f, o_ref, rtol=0, atol=1e-12 * np.abs(o_ref).max())
+    np.testing.assert_allclose(s_f, s_ref, rtol=0, atol=1e-12 * np.abs(s_ref).max())
+
+
 def test_chunk_form_survives_strong_decay():
     """Cumulated decay far below fp64's range (sum g < -745 inside one chunk) stays finite,
     because decay ratios are exp(G_r - G_s) with s <= r."""
