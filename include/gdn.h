@@ -73,7 +73,7 @@ typedef struct gdn_opts {
     int dtype;                  /* gdn_dtype_t of q, k, v, g, beta, out.  Default GDN_BF16. */
     int chunk;                  /* prefill chunk length: 16, 32 or 64.  0 -> 64. */
     float scale;                /* multiplies every output o_t.  Default 1.0f. */
-    unsigned flags;             /* GDN_NORMALIZE_QK */
+    unsigned flags;             /* GDN_NORMALIZE_QK | GDN_RAW_GATES | GDN_OUTPUT_GATE, default 0 */
     const int32_t* cu_seqlens;  /* prefill only: DEVICE pointer to num_seqs+1 int32 token offsets
                                    (0 = cu[0] <= cu[1] <= ... <= cu[num_seqs] = T) of packed
                                    sequences; requires B == 1.  NULL: B sequences of T tokens. */
