@@ -212,6 +212,40 @@ def test_backward_workspace_size_is_pure_host(lib):
     assert lib.gdn_recurrent_bwd_workspace_size(1, 8, 1, 1, 48, 32, opts(lib)) == 0
 
 
+@pytest.mark.parametrize("B,T,Hqk,Hv,dk,dv,dtype,nseq", [
+    (2, 8192, 16, 32, 128, 128, "bf16", None),    # tensor-core path, batched
+    (1, 131072, 16, 32, 128, 128, "bf16", 4),     # tensor-core path, packed
+    (3, 97, 2, 6, 128, 128, "bf16", None),        # ragged, odd grouping
+    (2, 8192, 16, 32, 128, 128, "f32", None),     # chunked path (fp32)
+    (1, 300, 1, 2, 64, 32, "bf16", 5),            # chunked path, packed, small heads
+    (4, 512, 4, 4, 32, 32, "bf16", None),         # chunked path, character-LM heads
+])
+def test_workspace_sizes_follow_the_slot_layout(lib, B, T, Hqk, Hv, dk, dv, dtype, nseq):
+    """Both prefill workspaces and the backward workspace, against the slot layout written out here:
+    chunk c of sequence i in slot floor(start_i / 64) + i + c, so slots = ceil(tokens / 64) + nseq."""
+    packed = nseq is not None
+    kw = dict(dtype=pkg_lib.GDN_BF16 if dtype == "bf16" else pkg_lib.GDN_F32)
+    if packed:
+        kw.update(cu_seqlens=FAKE, num_seqs=nseq)   # the size query only looks at the pointer's presence
+    n_seq = nseq if packed else B
+    tokens = T if packed else B * T
+    slots = -(-tokens // 64) + n_seq
+    got = lib.gdn_chunk_fwd_workspace_size(B, T, Hqk, Hv, dk, dv, opts(lib, **kw))
+    if dtype == "bf16" and dk == dv == 128:
+        # per (slot, value head): the 128 x 192 bf16 A1 operand and 128 floats (b_r, gamma_C)
+        assert got == slots * Hv * (128 * 192 * 2 + 128 * 4)
+    else:
+        # fp32 T, P (64 x 64), W (64 x dk), U (64 x dv), G (64), S (dk x dv), row scalars (2 x 64)
+        per = 2 * 64 * 64 + 64 * dk + 64 * dv + 64 + dk * dv + 2 * 64
+        need = slots * Hv * per * 4
+        assert need <= got <= need + 7 * 256
+    bwd_kw = dict(kw, dtype=pkg_lib.GDN_BF16 if dtype == "bf16" else pkg_lib.GDN_F32)
+    got_b = lib.gdn_recurrent_bwd_workspace_size(B, T, Hqk, Hv, dk, dv, opts(lib, **bwd_kw))
+    per_b = 2 * 64 * 64 + 64 * dk + 2 * 64 * dv + 64 + 2 * dk * dv   # + dU (64 x dv) and dS (dk x dv)
+    need_b = slots * Hv * per_b * 4
+    assert need_b <= got_b <= need_b + 8 * 256
+
+
 def test_tensor_core_path_accepts_any_head_grouping(lib):
     for Hqk, Hv in ((2, 2), (1, 3), (16, 32)):
         assert lib.gdn_chunk_fwd_workspace_size(1, 512, Hqk, Hv, 128, 128, opts(lib)) > 0
