@@ -38,8 +38,8 @@ METRIC = "GDN prefill tokens/s & decode steps/s at H=32,d=128; % tensor/HBM roof
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch from ncu captures (profiles/*.md), valid only for the kernel source they
-# were taken on (sha256 prefix of the file); None once the source has changed.
+# DRAM bytes per launch from ncu captures, valid only for the kernel source they were taken on
+# (sha256 prefix of the file); None once the source has changed.
 NCU_TRAFFIC = {
     # kernel: (source file, sha256 prefix of that file at capture, dram read + write bytes per launch)
     "gdn_tc_prep": ("gated_deltanet_recurrence_03_gb300/csrc/gdn_tc.cu", "3302073e7ce961a4", 139527936 + 345190144),

@@ -104,6 +104,11 @@ void record(const gdn_opts_t& o, int i, cudaStream_t s) {
 
 void set_error_message(const char* msg) { snprintf(t_last_error, sizeof(t_last_error), "%s", msg); }
 
+gdn_status_t check_current_device() {
+    unsigned* status = nullptr;
+    return device_ready(&status);
+}
+
 }  // namespace gdn
 
 using namespace gdn;

@@ -136,6 +136,9 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
 
 // Set the calling thread's gdn_last_error() message.
 void set_error_message(const char* msg);
+// GDN_OK when the current device is an sm_103 GPU this library runs on; otherwise the status (and
+// gdn_last_error() message) every entry point returns for it.
+gdn_status_t check_current_device();
 
 // ---------------------------------------------------------------- device helpers
 template <typename T>

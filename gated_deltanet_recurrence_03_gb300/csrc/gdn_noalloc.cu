@@ -9,12 +9,18 @@
 // instead of from the caller.
 //
 // The array lives in device memory of every GPU that loads the library, for the life of the
-// process.  Its size caps the problem size; larger problems are rejected with
+// process.  It is committed when this translation unit's module is loaded on a device: with CUDA's
+// default lazy module loading that happens inside the first call of this entry point on that
+// device (the cudaGetSymbolAddress below loads it), with CUDA_MODULE_LOADING=EAGER when the
+// process creates its context.  A caller that owns nearly all device memory should make that first
+// call early (before handing the rest of the memory to its pool) and before any stream capture.
+// Its size caps the problem size; larger problems are rejected with
 // GDN_ERR_WORKSPACE before anything is launched.  Every call on a device uses the same array and
 // it keeps whatever the previous call wrote.  Nothing in it has to start at zero: each call
 // writes every scratch byte it later reads.  Two calls whose work overlaps on the GPU (for
 // example on two streams of one device) would use the array at the same time and race; order
 // them on one stream or with events.
+#include <cstdio>
 #include <mutex>
 
 #include "gdn_internal.cuh"
@@ -72,10 +78,18 @@ extern "C" gdn_status_t gdn_chunk_fwd_noalloc(const void* q, const void* k, cons
         return GDN_ERR_WORKSPACE;
     }
     if (need > 0) {
+        // the same status as gdn_chunk_fwd on a device this library does not run on, before the
+        // symbol lookup (which would fail there with a less useful CUDA error)
+        const gdn_status_t dst = gdn::check_current_device();
+        if (dst != GDN_OK) return dst;
         void* p = nullptr;
         const cudaError_t e = gdn::scratch_on_current_device(&p);
         if (e != cudaSuccess) {
-            gdn::set_error_message("gdn_chunk_fwd_noalloc: cudaGetSymbolAddress of the scratch array failed");
+            char msg[200];
+            snprintf(msg, sizeof(msg),
+                     "gdn_chunk_fwd_noalloc: cudaGetSymbolAddress of the scratch array failed "
+                     "(loading the module commits the 64 MiB array): %s", cudaGetErrorString(e));
+            gdn::set_error_message(msg);
             return GDN_ERR_CUDA;
         }
         o.workspace = p;

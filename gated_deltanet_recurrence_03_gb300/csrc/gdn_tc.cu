@@ -211,6 +211,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + P_BAR + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + P_BAR + 20);
     int* sFactor = reinterpret_cast<int*>(sm + P_BAR + 24);   // [2]: decay ratios factorise safely
+    const uint32_t bar_drain = sb + P_BAR + 32;
 
     const int slot = blockIdx.x, pair = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -228,6 +229,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         *abort_flag = 0;
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_drain, 1);
         mbar_fence_init();
         mbar_arrive_expect_tx(bar_tma, 4 * 8192);
         for (int p = 0; p < 2; ++p) {
@@ -575,7 +577,13 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     }
     if (warp == 0) {
-        if (tid == 0) bulk_wait_read();   // shared memory may be released; the global writes finish on their own
+        if (tid == 0) {
+            bulk_wait_read();   // shared memory may be released; the global writes finish on their own
+            // after a bounded wait gave up: no MMA or tile load of this CTA may still be running
+            mma_commit(bar_drain);
+            mbar_wait_drain(bar_drain, 0, kWaitLimitNs);
+            mbar_wait_drain(bar_tma, 0, kWaitLimitNs);
+        }
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 256);
@@ -626,7 +634,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const uint32_t sb = smem_u32(sm);
     // bar_a[2] (A1 + V), bar_k[3] (K + vector), mma1, mma2
     const uint32_t bar_a0 = sb + C_BAR, bar_k0 = sb + C_BAR + 16, bar_mma1 = sb + C_BAR + 40,
-                   bar_mma2 = sb + C_BAR + 48;
+                   bar_mma2 = sb + C_BAR + 48, bar_drain = sb + C_BAR + 64;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C_BAR + 56);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C_BAR + 60);
 
@@ -656,6 +664,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         for (int q = 0; q < kKStages; ++q) mbar_init(bar_k0 + 8 * q, 1);
         mbar_init(bar_mma1, 1);
         mbar_init(bar_mma2, 1);
+        mbar_init(bar_drain, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -672,7 +681,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         return mbar_wait_bounded(bar_k0 + 8 * (uint32_t)(c % kKStages), (uint32_t)((c / kKStages) & 1), abort_flag,
                                  status, kStatusTimeout, kWaitLimitNs);
     };
+    // After a bounded wait has given up no further copies are issued, so that the drain before exit
+    // covers every copy still in flight.
     auto issue_loads_a = [&](long long c) {   // A1 and the V slice of chunk c
+        if (*abort_flag) return;
         const int st = (int)(c & 1);
         const long long slot = base + c;
         const uint32_t bar = bar_a0 + 8 * st;
@@ -681,6 +693,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         tma_load_3d(sb + C_VT + st * 8192, &tm_v, 64 * z, h, (int)(s0 + c * kC), bar);
     };
     auto issue_loads_k = [&](long long c) {   // K tile and the b / gamma_C vector of chunk c
+        if (*abort_flag) return;
         const int st = (int)(c % kKStages);
         const long long slot = base + c;
         const int tc0 = (int)(s0 + c * kC);
@@ -864,6 +877,17 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             __syncthreads();
         }
+        if (tid == kIssuer) {
+            // Before the TMEM and shared memory are released: every MMA has completed and no copy is still
+            // landing (after a bounded wait gave up, consumers may have skipped chunks whose loads were
+            // issued).  Each stage's last armed phase is the latest one, so its parity test is exact.
+            mma_commit(bar_drain);
+            mbar_wait_drain(bar_drain, 0, kWaitLimitNs);
+            for (long long c = max(0LL, nch - 2); c < nch; ++c)
+                mbar_wait_drain(bar_a0 + 8 * (uint32_t)(c & 1), (uint32_t)((c >> 1) & 1), kWaitLimitNs);
+            for (long long c = max(0LL, nch - kKStages); c < nch; ++c)
+                mbar_wait_drain(bar_k0 + 8 * (uint32_t)(c % kKStages), (uint32_t)((c / kKStages) & 1), kWaitLimitNs);
+        }
     }
     __syncthreads();
     if (warp == 0) {
@@ -927,19 +951,30 @@ void* tensor_map_encoder() {
     return fn;
 }
 
+// Kernel attributes (shared-memory size and carveout) belong to a device: set them once per device.
+cudaError_t set_kernel_attributes() {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static bool done[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+    if (e == cudaSuccess)   // two prep CTAs per SM need the largest shared-memory carveout
+        e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+}
+
 cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_events) {
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
-        if (attr_err == cudaSuccess)   // two prep CTAs per SM need the largest shared-memory carveout
-            attr_err = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    if ((e = set_kernel_attributes()) != cudaSuccess) return e;
 
     const bool packed = a.cu_seqlens != nullptr;
     const long long ttot = total_tokens(a.B, a.T, packed);

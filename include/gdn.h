@@ -161,9 +161,14 @@ gdn_status_t gdn_recurrent_step(const void* q, const void* k, const void* v, con
  * Limit: on the tensor-core path, problems whose gdn_chunk_fwd_workspace_size() exceeds 64 MiB
  * are rejected with GDN_ERR_WORKSPACE before anything is launched (for 32 value heads of dim 128
  * that is about 40 chunks of 64 tokens, ~2.5k tokens, per call); other shapes that large run the
- * token-serial kernel.  The first call on each device looks up the
- * array's device address (a host-side query, no allocation); make that first call before any
- * stream capture.  All calls on a device share the array, which keeps the previous call's
+ * token-serial kernel.  The 64 MiB are committed on a device when the library's module that
+ * holds the array is loaded there: with CUDA's default lazy module loading that is the first call
+ * of this entry point on that device (which also looks up the array's device address), with
+ * CUDA_MODULE_LOADING=EAGER it is context creation.  A caller that owns nearly all device memory
+ * should therefore make its first call early, before the rest of the memory goes to its pool, and
+ * before any stream capture; if loading fails the call returns GDN_ERR_CUDA with CUDA's reason in
+ * gdn_last_error().  On a device that is not sm_103 it returns GDN_ERR_UNSUPPORTED, as
+ * gdn_chunk_fwd does.  All calls on a device share the array, which keeps the previous call's
  * contents (no part of it needs to start at zero); calls that overlap on the GPU race on it, so
  * order them.
  */
