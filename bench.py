@@ -352,18 +352,18 @@ def run_gpu(args):
     del xl, out_l, ws_l
 
     # ---- the recurrent core of one layer on the same workload: short causal conv of the packed q/k/v
-    #      projection (three channel slices), gates from the raw a/b projections, l2 norm of q and k,
-    #      chunked recurrence, gated RMS norm with silu(z); prefill inputs larger than L2
+    #      projection (one launch, q, k and v written as the dense tensors the recurrence takes), gates
+    #      from the raw a/b projections, l2 norm of q and k, chunked recurrence, gated RMS norm with
+    #      silu(z); prefill inputs larger than L2
     Cq, Cv = w.Hqk * w.dk, w.Hv * w.dv
     Cc = 2 * Cq + Cv
     bf = torch.bfloat16
     gen = torch.Generator(device=dev).manual_seed(5)
     proj = torch.randn(w.B, w.T, Cc, device=dev, generator=gen).to(bf)
     conv_w = 0.5 * torch.randn(Cc, 4, device=dev, generator=gen)
-    conv_ws = [conv_w[:Cq].contiguous(), conv_w[Cq:2 * Cq].contiguous(), conv_w[2 * Cq:].contiguous()]
     qc = torch.empty(w.B, w.T, w.Hqk, w.dk, dtype=bf, device=dev)
     kc, vc = torch.empty_like(qc), torch.empty(w.B, w.T, w.Hv, w.dv, dtype=bf, device=dev)
-    caches = [torch.empty(w.B, 3, c, dtype=bf, device=dev) for c in (Cq, Cq, Cv)]
+    conv_cache = torch.empty(w.B, 3, Cc, dtype=bf, device=dev)
     a_raw = torch.randn(w.B, w.T, w.Hv, device=dev, generator=gen).to(bf)
     b_raw = torch.randn(w.B, w.T, w.Hv, device=dev, generator=gen).to(bf)
     A_log = -0.5 + 0.5 * torch.randn(w.Hv, device=dev, generator=gen)
@@ -380,9 +380,8 @@ def run_gpu(args):
     def layer_step(i=None):
         if i is not None:
             ev_c[i][0].record(stream)
-        for (c0, c1), dst, cw, cache in zip(((0, Cq), (Cq, 2 * Cq), (2 * Cq, Cc)), (qc, kc, vc), conv_ws, caches):
-            gdn.gdn_causal_conv1d_fwd(proj[:, :, c0:c1], cw, None, out=dst.view(w.B, w.T, c1 - c0),
-                                      cache_out=cache)
+        gdn.gdn_causal_conv1d_fwd_qkv(proj, conv_w, (Cq, Cq, Cv), None, cache_out=conv_cache,
+                                      out=(qc.view(w.B, w.T, Cq), kc.view(w.B, w.T, Cq), vc.view(w.B, w.T, Cv)))
         if i is not None:
             ev_c[i][1].record(stream)
         gdn.gdn_chunk_fwd(qc, kc, vc, a_raw, b_raw, S0, out=out, S_final=S_final, workspace=ws, chunk=w.chunk,
@@ -475,17 +474,17 @@ def run_gpu(args):
     dec_bytes = decode_bytes(wd)
     dec_gbs = dec_bytes / (dec_ms * 1e6)
 
-    # ---- the recurrent core of a layer in decode, same sequences and heads: per step three conv steps
-    #      of the packed projection with their K-1 caches, then the recurrent step with raw gates, l2 norm
-    #      and the output gate; 128 steps in one CUDA graph
+    # ---- the recurrent core of a layer in decode, same sequences and heads: per step one conv step of the
+    #      packed projection with its K-1 cache (q, k, v written as dense tensors), then the recurrent step
+    #      with raw gates, l2 norm and the output gate; 128 steps in one CUDA graph
     dl_steps = 128
     bf = torch.bfloat16
     Cq, Cv = wd.Hqk * wd.dk, wd.Hv * wd.dv
     Cc = 2 * Cq + Cv
     genl = torch.Generator(device=dev).manual_seed(7)
     projd = torch.randn(dl_steps, wd.B, Cc, device=dev, generator=genl).to(bf)
-    cwd = [0.5 * torch.randn(c, 4, device=dev, generator=genl) for c in (Cq, Cq, Cv)]
-    cachesd = [torch.zeros(wd.B, 3, c, dtype=bf, device=dev) for c in (Cq, Cq, Cv)]
+    cwd = 0.5 * torch.randn(Cc, 4, device=dev, generator=genl)
+    cached = torch.zeros(wd.B, 3, Cc, dtype=bf, device=dev)
     ad = torch.randn(dl_steps, wd.B, wd.Hv, device=dev, generator=genl).to(bf)
     bd = torch.randn(dl_steps, wd.B, wd.Hv, device=dev, generator=genl).to(bf)
     zd = torch.randn(dl_steps, wd.B, wd.Hv, wd.dv, device=dev, generator=genl).to(bf)
@@ -497,8 +496,7 @@ def run_gpu(args):
     outd = torch.empty(dl_steps, wd.B, wd.Hv, wd.dv, dtype=bf, device=dev)
 
     def decode_layer_step(t):
-        for (c0, c1), cw_, cache_, y_ in zip(((0, Cq), (Cq, 2 * Cq), (2 * Cq, Cc)), cwd, cachesd, (yq, yk, yv)):
-            gdn.gdn_causal_conv1d_step(projd[t][:, c0:c1], cw_, cache_, out=y_)
+        gdn.gdn_causal_conv1d_step_qkv(projd[t], cwd, cached, (Cq, Cq, Cv), out=(yq, yk, yv))
         gdn.gdn_recurrent_step(yq.view(wd.B, wd.Hqk, wd.dk), yk.view(wd.B, wd.Hqk, wd.dk),
                                yv.view(wd.B, wd.Hv, wd.dv), ad[t], bd[t], S, out=outd[t], scale=wd.dk ** -0.5,
                                normalize_qk=True, raw_gates=(A_logd, dt_biasd), output_gate=(zd[t], nwd, 1e-6))
@@ -586,11 +584,11 @@ def run_gpu(args):
                                       "peak": peak_tf, "unit": "TFLOP/s",
                                       "frac": round((lf_prep + lf_chain) / (long_ms * 1e9) / peak_tf, 4)}},
         "layer": {"workload": "prefill_gqa_8k through the whole recurrent core: causal conv K=4 of the packed "
-                              "q/k/v projection (3 channel slices, 8192 channels), gates from raw a/b, l2 norm, "
-                              "chunked recurrence, gated RMS norm x silu(z)",
+                              "q/k/v projection (one launch over its 8192 channels, q, k, v written as dense "
+                              "tensors), gates from raw a/b, l2 norm, chunked recurrence, gated RMS norm x silu(z)",
                   "value": round(world * tokens / (layer_ms / 1e3), 1), "unit": "tokens/s",
-                  "ms_per_step": round(layer_ms, 4), "steps": layer_steps, "gpu_launches": 6 * layer_steps,
-                  "kernels_ms": {"conv_fwd_kernel x3": round(conv_ms, 4), "output_gate_kernel": round(gate_ms, 4)},
+                  "ms_per_step": round(layer_ms, 4), "steps": layer_steps, "gpu_launches": 4 * layer_steps,
+                  "kernels_ms": {"conv_fwd_kernel": round(conv_ms, 4), "output_gate_kernel": round(gate_ms, 4)},
                   "conv_roofline": {"bound": "hbm", "achieved": round(conv_bytes / (conv_ms * 1e6), 1),
                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                     "frac": round(conv_bytes / (conv_ms * 1e6) / peaks["hbm_gbs"], 4),
@@ -622,12 +620,13 @@ def run_gpu(args):
                                "returned (chunked kernels on split-tf32 MMAs: d = 32 is off the tcgen05 tile)",
                    "value": round(world * wc.B * wc.T / (charlm_ms / 1e3), 1), "unit": "tokens/s",
                    "us_per_call": round(charlm_ms * 1e3, 2), "calls": charlm_reps, "bound": "latency"},
-        "decode_layer": {"workload": "decode_256x512 heads through the layer's recurrent core: 3 conv steps (K=4) "
-                                     "of the packed 8192-channel projection with their caches, then the recurrent step "
-                                     "with raw gates, l2 norm and the output gate; 128 steps per CUDA graph",
+        "decode_layer": {"workload": "decode_256x512 heads through the layer's recurrent core: one conv step (K=4) "
+                                     "of the packed 8192-channel projection with its cache (q, k, v written as dense "
+                                     "tensors), then the recurrent step with raw gates, l2 norm and the output gate; "
+                                     "128 steps per CUDA graph",
                          "value": round(world / (dl_ms / 1e3), 1), "unit": "steps/s",
                          "tokens_per_s": round(world * wd.B / (dl_ms / 1e3), 1), "us_per_step": round(dl_ms * 1e3, 2),
-                         "gpu_launches": 2 * dl_steps * 4,
+                         "gpu_launches": 2 * dl_steps * 2,
                          "roofline": {"bound": "hbm", "achieved": round(dl_bytes / (dl_ms * 1e6), 1),
                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": round(dl_bytes / (dl_ms * 1e6) / peaks["hbm_gbs"], 4),
@@ -750,8 +749,8 @@ def run_profile_case(case):
         for _ in range(2):
             gdn.gdn_recurrent_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, dout, dSf, workspace=ws)
     elif case == "layer":
-        # the conv of the packed q/k/v projection (three channel slices) and the prefill with the
-        # fused front end and the output gate, twice
+        # the conv of the packed q/k/v projection (one launch) and the prefill with the fused front end
+        # and the output gate, twice
         w = PREFILL
         x = device_inputs_random(torch, dev, w)
         Cq, Cv = w.Hqk * w.dk, w.Hv * w.dv
@@ -763,9 +762,9 @@ def run_profile_case(case):
         A_log, dt_bias = -0.5 + 0.5 * torch.randn(w.Hv, device=dev), 0.5 * torch.randn(w.Hv, device=dev)
         nw = 1.0 + 0.1 * torch.randn(w.dv, device=dev)
         for _ in range(2):
-            for (c0, c1), dst in zip(((0, Cq), (Cq, 2 * Cq), (2 * Cq, 2 * Cq + Cv)), ("q", "k", "v")):
-                gdn.gdn_causal_conv1d_fwd(proj[:, :, c0:c1], cw[c0:c1].contiguous(), None,
-                                          out=x[dst].view(w.B, w.T, c1 - c0), return_cache=False)
+            gdn.gdn_causal_conv1d_fwd_qkv(proj, cw, (Cq, Cq, Cv), None, return_cache=False,
+                                          out=(x["q"].view(w.B, w.T, Cq), x["k"].view(w.B, w.T, Cq),
+                                               x["v"].view(w.B, w.T, Cv)))
             gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, workspace=ws, normalize_qk=True,
                               raw_gates=(A_log, dt_bias), output_gate=(z, nw, 1e-6))
     else:

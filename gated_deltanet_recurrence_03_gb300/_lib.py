@@ -19,7 +19,8 @@ GDN_OUTPUT_GATE = 0x4
 EXPORTED = ("gdn_opts_init", "gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step",
             "gdn_check_device_status", "gdn_status_string", "gdn_last_error", "gdn_version",
             "gdn_chunk_fwd_noalloc", "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_step",
-            "gdn_recurrent_bwd", "gdn_recurrent_bwd_workspace_size")
+            "gdn_recurrent_bwd", "gdn_recurrent_bwd_workspace_size", "gdn_causal_conv1d_fwd_qkv",
+            "gdn_causal_conv1d_step_qkv")
 
 
 class GdnOpts(ctypes.Structure):
@@ -74,6 +75,10 @@ def load(path: str = LIB_PATH):
     lib.gdn_causal_conv1d_fwd.restype = i
     lib.gdn_causal_conv1d_step.argtypes = [vp, ll, vp, vp, vp, i, i, i, opts_p]
     lib.gdn_causal_conv1d_step.restype = i
+    lib.gdn_causal_conv1d_fwd_qkv.argtypes = [vp, ll, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, opts_p]
+    lib.gdn_causal_conv1d_fwd_qkv.restype = i
+    lib.gdn_causal_conv1d_step_qkv.argtypes = [vp, ll, vp, vp, vp, vp, vp, i, i, i, i, i, opts_p]
+    lib.gdn_causal_conv1d_step_qkv.restype = i
     lib.gdn_recurrent_bwd.argtypes = [vp] * 14 + [i, i, i, i, i, i, opts_p]
     lib.gdn_recurrent_bwd.restype = i
     lib.gdn_recurrent_bwd_workspace_size.argtypes = [i, i, i, i, i, i, opts_p]

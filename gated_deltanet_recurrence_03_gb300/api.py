@@ -256,6 +256,83 @@ def gdn_causal_conv1d_step(x: torch.Tensor, w: torch.Tensor, cache: torch.Tensor
     return out
 
 
+def gdn_causal_conv1d_fwd_qkv(x: torch.Tensor, w: torch.Tensor, widths: Sequence[int],
+                              cache_in: Optional[torch.Tensor] = None, *, cu_seqlens: Optional[torch.Tensor] = None,
+                              out: Optional[Sequence[torch.Tensor]] = None, cache_out: Optional[torch.Tensor] = None,
+                              return_cache: bool = True, stream: Optional[torch.cuda.Stream] = None,
+                              events: Optional[Sequence[int]] = None):
+    """The convolution of gdn_causal_conv1d_fwd over the packed q | k | v projection x [B, T, Cq + Ck + Cv]
+    in one launch, the three channel ranges (``widths`` = (Cq, Ck, Cv)) written to three dense tensors.
+    Returns ((y_q, y_k, y_v), cache_out [nseq, K-1, C] or None)."""
+    lib = L.load()
+    if x.dim() != 3 or x.stride(2) != 1 or x.stride(0) != x.shape[1] * x.stride(1):
+        raise ValueError("x must be [B, T, C] with contiguous channels and evenly strided token rows")
+    B, T, C = x.shape
+    Cq, Ck, Cv = (int(c) for c in widths)
+    if Cq + Ck + Cv != C:
+        raise ValueError(f"widths {widths} do not add up to the {C} channels of x")
+    dev, dt = x.device, x.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    K = int(w.shape[1])
+    _need("w", w, torch.float32, dev, (C, K))
+    nseq = B
+    if cu_seqlens is not None:
+        nseq = int(cu_seqlens.numel()) - 1
+        _need("cu_seqlens", cu_seqlens, torch.int32, dev, (nseq + 1,))
+    if cache_in is not None:
+        _need("cache_in", cache_in, dt, dev, (nseq, K - 1, C))
+    if out is None:
+        out = tuple(torch.empty((B, T, c), dtype=dt, device=dev) for c in (Cq, Ck, Cv))
+    for name, y, c in zip(("y_q", "y_k", "y_v"), out, (Cq, Ck, Cv)):
+        _need(name, y, dt, dev, (B, T, c))
+    if cache_out is None and return_cache:
+        cache_out = torch.empty((nseq, K - 1, C), dtype=dt, device=dev)
+    if cache_out is not None:
+        _need("cache_out", cache_out, dt, dev, (nseq, K - 1, C))
+    with torch.cuda.device(dev):
+        o, keep = _opts(lib, dt, 1.0, 64, False, stream, dev, events)
+        if cu_seqlens is not None:
+            o.cu_seqlens = cu_seqlens.data_ptr()
+            o.num_seqs = nseq
+        st = lib.gdn_causal_conv1d_fwd_qkv(_ptr(x), x.stride(1), _ptr(w), _ptr(cache_in), _ptr(out[0]), _ptr(out[1]),
+                                           _ptr(out[2]), _ptr(cache_out), B, T, Cq, Ck, Cv, K, ctypes.byref(o))
+        del keep
+        L.check(lib, st)
+    return tuple(out), cache_out
+
+
+def gdn_causal_conv1d_step_qkv(x: torch.Tensor, w: torch.Tensor, cache: torch.Tensor, widths: Sequence[int], *,
+                               out: Optional[Sequence[torch.Tensor]] = None,
+                               stream: Optional[torch.cuda.Stream] = None,
+                               events: Optional[Sequence[int]] = None):
+    """One decode token per sequence through the convolution of the packed q | k | v projection
+    x [N, Cq + Ck + Cv] (``widths`` = (Cq, Ck, Cv)), cache [N, K-1, C] updated in place, in one launch.
+    Returns (y_q [N, Cq], y_k [N, Ck], y_v [N, Cv])."""
+    lib = L.load()
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be [N, C] with contiguous channels")
+    N, C = x.shape
+    Cq, Ck, Cv = (int(c) for c in widths)
+    if Cq + Ck + Cv != C:
+        raise ValueError(f"widths {widths} do not add up to the {C} channels of x")
+    dev, dt = x.device, x.dtype
+    K = int(w.shape[1])
+    _need("w", w, torch.float32, dev, (C, K))
+    _need("cache", cache, dt, dev, (N, K - 1, C))
+    if out is None:
+        out = tuple(torch.empty((N, c), dtype=dt, device=dev) for c in (Cq, Ck, Cv))
+    for name, y, c in zip(("y_q", "y_k", "y_v"), out, (Cq, Ck, Cv)):
+        _need(name, y, dt, dev, (N, c))
+    with torch.cuda.device(dev):
+        o, keep = _opts(lib, dt, 1.0, 64, False, stream, dev, events)
+        st = lib.gdn_causal_conv1d_step_qkv(_ptr(x), x.stride(0), _ptr(w), _ptr(cache), _ptr(out[0]), _ptr(out[1]),
+                                            _ptr(out[2]), N, Cq, Ck, Cv, K, ctypes.byref(o))
+        del keep
+        L.check(lib, st)
+    return tuple(out)
+
+
 def backward_workspace_size(B: int, T: int, Hqk: int, Hv: int, dk: int, dv: int, *,
                             num_seqs: Optional[int] = None) -> int:
     """Bytes of device scratch gdn_recurrent_bwd needs."""

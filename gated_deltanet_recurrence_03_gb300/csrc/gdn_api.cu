@@ -299,8 +299,14 @@ static gdn_status_t conv_common(const void* x, long long* x_stride, const float*
     return GDN_OK;
 }
 
-gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const float* w, const void* cache_in, void* y,
-                                   void* cache_out, int B, int T, int C, int K, const gdn_opts_t* opts) {
+}  // extern "C"
+
+namespace {
+
+// Shared by the single-output and the q | k | v split entry points: y_k == nullptr means one output.
+gdn_status_t conv_fwd_impl(const void* x, long long x_stride, const float* w, const void* cache_in, void* y,
+                           void* y_k, void* y_v, int c1, int c2, void* cache_out, int B, int T, int C, int K,
+                           const gdn_opts_t* opts) {
     t_last_error[0] = 0;
     const gdn_opts_t o = resolve(opts);
     if (B < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "B=%d T=%d must be >= 0", B, T);
@@ -311,8 +317,9 @@ gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const floa
     if (nseq == 0) return GDN_OK;
     gdn_status_t st = conv_common(x, &x_stride, w, C, K, o);
     if (st != GDN_OK) return st;
-    if ((long long)B * T > 0 && !y) return fail(GDN_ERR_INVALID_ARG, "null y");
-    const void* ptrs[] = {y, cache_in, cache_out};
+    const bool have_tokens = (long long)B * T > 0;
+    if (have_tokens && (!y || (y_k && !y_v))) return fail(GDN_ERR_INVALID_ARG, "null y");
+    const void* ptrs[] = {y, y_k, y_v, cache_in, cache_out};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
     if (packed && !aligned_to(o.cu_seqlens, 4)) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
@@ -321,6 +328,7 @@ gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const floa
     if (st != GDN_OK) return st;
     ConvArgs a{};
     a.x = x; a.x_stride = x_stride; a.w = w; a.cache_in = cache_in; a.y = y; a.cache_out = cache_out;
+    a.y_k = y_k; a.y_v = y_v; a.c1 = c1; a.c2 = c2;
     a.B = B; a.T = T; a.C = C; a.K = K; a.dtype = o.dtype; a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq;
     a.packed = packed; a.stream = static_cast<cudaStream_t>(o.stream); a.status = status;
     record(o, 0, a.stream);
@@ -330,27 +338,72 @@ gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const floa
     return GDN_OK;
 }
 
-gdn_status_t gdn_causal_conv1d_step(const void* x, long long x_stride, const float* w, void* cache, void* y, int N,
-                                    int C, int K, const gdn_opts_t* opts) {
+gdn_status_t conv_step_impl(const void* x, long long x_stride, const float* w, void* cache, void* y, void* y_k,
+                            void* y_v, int c1, int c2, int N, int C, int K, const gdn_opts_t* opts) {
     t_last_error[0] = 0;
     const gdn_opts_t o = resolve(opts);
     if (N < 0) return fail(GDN_ERR_INVALID_ARG, "N=%d must be >= 0", N);
     if (N == 0) return GDN_OK;
     gdn_status_t st = conv_common(x, &x_stride, w, C, K, o);
     if (st != GDN_OK) return st;
-    if (!y || (K > 1 && !cache)) return fail(GDN_ERR_INVALID_ARG, "null y or cache");
-    if (!aligned16(y) || (cache && !aligned16(cache))) return fail(GDN_ERR_INVALID_ARG, "y and cache must be 16-byte aligned");
+    if (!y || (y_k && !y_v) || (K > 1 && !cache)) return fail(GDN_ERR_INVALID_ARG, "null y or cache");
+    const void* ptrs[] = {y, y_k, y_v, cache};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "y and cache must be 16-byte aligned");
     unsigned* status = nullptr;
     st = device_ready(&status);
     if (st != GDN_OK) return st;
     ConvArgs a{};
     a.x = x; a.x_stride = x_stride; a.w = w; a.y = y; a.cache_out = cache;
+    a.y_k = y_k; a.y_v = y_v; a.c1 = c1; a.c2 = c2;
     a.B = N; a.C = C; a.K = K; a.dtype = o.dtype; a.stream = static_cast<cudaStream_t>(o.stream);
     record(o, 0, a.stream);
     const cudaError_t e = launch_conv_step(a);
     record(o, 1, a.stream);
     if (e != cudaSuccess) return cuda_fail(e, "conv step launch");
     return GDN_OK;
+}
+
+gdn_status_t qkv_widths(int Cq, int Ck, int Cv) {
+    if (Cq <= 0 || Ck <= 0 || Cv <= 0 || Cq % 8 || Ck % 8 || Cv % 8)
+        return fail(GDN_ERR_INVALID_ARG, "q/k/v widths %d/%d/%d must be positive multiples of 8", Cq, Ck, Cv);
+    if ((long long)Cq + Ck + Cv > INT32_MAX) return fail(GDN_ERR_INVALID_ARG, "too many channels");
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status_t gdn_causal_conv1d_fwd(const void* x, long long x_stride, const float* w, const void* cache_in, void* y,
+                                   void* cache_out, int B, int T, int C, int K, const gdn_opts_t* opts) {
+    return conv_fwd_impl(x, x_stride, w, cache_in, y, nullptr, nullptr, 0, 0, cache_out, B, T, C, K, opts);
+}
+
+gdn_status_t gdn_causal_conv1d_fwd_qkv(const void* x, long long x_stride, const float* w, const void* cache_in,
+                                       void* y_q, void* y_k, void* y_v, void* cache_out, int B, int T, int Cq,
+                                       int Ck, int Cv, int K, const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_status_t st = qkv_widths(Cq, Ck, Cv);
+    if (st != GDN_OK) return st;
+    if ((long long)B * T > 0 && (!y_q || !y_k || !y_v)) return fail(GDN_ERR_INVALID_ARG, "null y_q, y_k or y_v");
+    return conv_fwd_impl(x, x_stride, w, cache_in, y_q, y_k, y_v, Cq, Cq + Ck, cache_out, B, T, Cq + Ck + Cv, K,
+                         opts);
+}
+
+gdn_status_t gdn_causal_conv1d_step(const void* x, long long x_stride, const float* w, void* cache, void* y, int N,
+                                    int C, int K, const gdn_opts_t* opts) {
+    return conv_step_impl(x, x_stride, w, cache, y, nullptr, nullptr, 0, 0, N, C, K, opts);
+}
+
+gdn_status_t gdn_causal_conv1d_step_qkv(const void* x, long long x_stride, const float* w, void* cache, void* y_q,
+                                        void* y_k, void* y_v, int N, int Cq, int Ck, int Cv, int K,
+                                        const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_status_t st = qkv_widths(Cq, Ck, Cv);
+    if (st != GDN_OK) return st;
+    if (N > 0 && (!y_q || !y_k || !y_v)) return fail(GDN_ERR_INVALID_ARG, "null y_q, y_k or y_v");
+    return conv_step_impl(x, x_stride, w, cache, y_q, y_k, y_v, Cq, Cq + Ck, N, Cq + Ck + Cv, K, opts);
 }
 
 size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts) {

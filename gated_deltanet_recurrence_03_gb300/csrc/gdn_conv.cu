@@ -13,6 +13,8 @@
 // across the tile's 32 channel vectors of 16 bytes, slides the K-row window in registers (packed
 // fp32x2 arithmetic) and streams 512-byte rows of y out.
 // Decode step: one thread per 16-byte channel vector of one sequence, cache shifted in place.
+// Both can split their output by channel into up to three contiguous tensors (the q, k and v slices
+// of the packed projection the layer convolves in one pass), whatever the split, one launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -76,6 +78,21 @@ template <typename T>
 __device__ __forceinline__ void load_vec(const T* p, float2* f) { Vec<T>::unpack2(*reinterpret_cast<const uint4*>(p), f); }
 template <typename T>
 __device__ __forceinline__ void store_vec(T* p, const float2* f) { __stcs(reinterpret_cast<uint4*>(p), Vec<T>::pack2(f)); }
+
+// Where the outputs of one 16-byte channel vector go: y (channels [0, c1)), y_k ([c1, c2)) or y_v
+// ([c2, C)), each a dense [rows, width] tensor; without a split, y holds all C channels.
+template <typename T>
+struct OutSplit {
+    T* y;
+    T* y_k;
+    T* y_v;
+    int c1, c2, C;
+    __device__ __forceinline__ void route(int c0, T*& base, int& width, int& col) const {
+        if (!y_k || c0 < c1) { base = y; width = y_k ? c1 : C; col = c0; }
+        else if (c0 < c2) { base = y_k; width = c2 - c1; col = c0 - c1; }
+        else { base = y_v; width = C - c2; col = c0 - c2; }
+    }
+};
 
 // Sequence containing token t (largest i with start_i <= t, sequences sorted by start).
 __device__ __forceinline__ int seq_of(const int32_t* cu, int nseq, int T_len, long long t) {
@@ -163,7 +180,7 @@ __device__ __forceinline__ void load_taps(const float* __restrict__ w, int c0, b
 template <typename T, int K>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restrict__ w,
-                const T* __restrict__ cache_in, T* __restrict__ y, T* __restrict__ cache_out,
+                const T* __restrict__ cache_in, const OutSplit<T> ys, T* __restrict__ cache_out,
                 const int32_t* __restrict__ cu, int nseq, int T_len, long long Ttot, int C, unsigned* status) {
     constexpr int V = Vec<T>::N, P = V / 2;
     constexpr int CW = kRowBytes / (int)sizeof(T);      // channels per tile
@@ -229,6 +246,10 @@ conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restric
         const long long t0 = (i / n_cg) * kTileTokens;
         const int c0 = cg * CW + lane * V;
         const bool active = c0 < C;
+        T* yb;
+        int yw, yc;
+        ys.route(c0, yb, yw, yc);
+        T* __restrict__ y = yb + yc;   // token t of this vector at y[t * yw]
         if (cg != cg_loaded && active) {
             load_taps<T, K>(w, c0, (reinterpret_cast<uintptr_t>(w) % (K * sizeof(float))) == 0, wr);
             cg_loaded = cg;
@@ -256,7 +277,7 @@ conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restric
                 Vec<T>::unpack2(row(t + j), hist[K - 1]);
                 float2 out[P];
                 conv_out<T, K>(wr, hist, out);
-                store_vec(y + (t + j) * C + c0, out);
+                store_vec(y + (t + j) * yw, out);
 #pragma unroll
                 for (int k = 0; k < K - 1; ++k)
 #pragma unroll
@@ -288,7 +309,7 @@ conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restric
                 Vec<T>::unpack2(row(t), hist[K - 1]);
                 float2 out[P];
                 conv_out<T, K>(wr, hist, out);
-                store_vec(y + t * C + c0, out);
+                store_vec(y + t * yw, out);
 #pragma unroll
                 for (int k = 0; k < K - 1; ++k)
 #pragma unroll
@@ -319,11 +340,14 @@ constexpr int kStepRows = 4;
 template <typename T, int K>
 __global__ void __launch_bounds__(kStepThreads)
 conv_step_kernel(const T* __restrict__ x, long long x_stride, const float* __restrict__ w, T* __restrict__ cache,
-                 T* __restrict__ y, int N, int C) {
+                 const OutSplit<T> ys, int N, int C) {
     constexpr int V = Vec<T>::N, P = V / 2;
     const int vec = blockIdx.x * blockDim.x + threadIdx.x;
     if (vec * V >= C) return;
     const int c0 = vec * V;
+    T* yb;
+    int yw, yc;
+    ys.route(c0, yb, yw, yc);
     float2 wr[K][P];
     load_taps<T, K>(w, c0, (reinterpret_cast<uintptr_t>(w) % (K * sizeof(float))) == 0, wr);
     for (size_t n0 = (size_t)blockIdx.y * kStepRows; n0 < (size_t)N; n0 += (size_t)gridDim.y * kStepRows) {
@@ -337,7 +361,7 @@ conv_step_kernel(const T* __restrict__ x, long long x_stride, const float* __res
             load_vec(x + (long long)n * x_stride + c0, hist[K - 1]);
             float2 out[P];
             conv_out<T, K>(wr, hist, out);
-            store_vec(y + n * C + c0, out);
+            store_vec(yb + n * yw + yc, out);
 #pragma unroll
             for (int k = 1; k < K; ++k) store_vec(cache + (n * (K - 1) + (k - 1)) * C + c0, hist[k]);
         }
@@ -380,9 +404,10 @@ cudaError_t fwd_typed(const ConvArgs& a) {
                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
+    const OutSplit<T> ys{static_cast<T*>(a.y), static_cast<T*>(a.y_k), static_cast<T*>(a.y_v), a.c1, a.c2, a.C};
     conv_fwd_kernel<T, K><<<grid, kFwdThreads, kFwdSmem, a.stream>>>(
-        xmap, a.w, static_cast<const T*>(a.cache_in), static_cast<T*>(a.y),
-        static_cast<T*>(a.cache_out), a.cu_seqlens, a.num_seqs, a.T, Ttot, a.C, a.status);
+        xmap, a.w, static_cast<const T*>(a.cache_in), ys, static_cast<T*>(a.cache_out), a.cu_seqlens, a.num_seqs,
+        a.T, Ttot, a.C, a.status);
     return cudaGetLastError();
 }
 
@@ -391,9 +416,9 @@ cudaError_t step_typed(const ConvArgs& a) {
     const int vecs = a.C / Vec<T>::N;
     const int threads = min(kStepThreads, (vecs + 31) / 32 * 32);
     const dim3 grid((unsigned)((vecs + threads - 1) / threads), (unsigned)min(65535, (a.B + kStepRows - 1) / kStepRows));
+    const OutSplit<T> ys{static_cast<T*>(a.y), static_cast<T*>(a.y_k), static_cast<T*>(a.y_v), a.c1, a.c2, a.C};
     conv_step_kernel<T, K><<<grid, threads, 0, a.stream>>>(static_cast<const T*>(a.x), a.x_stride, a.w,
-                                                         static_cast<T*>(a.cache_out), static_cast<T*>(a.y),
-                                                         a.B, a.C);
+                                                         static_cast<T*>(a.cache_out), ys, a.B, a.C);
     return cudaGetLastError();
 }
 

@@ -77,6 +77,11 @@ struct ConvArgs {
     bool packed;
     cudaStream_t stream;
     unsigned* status;           // device status word (bounded waits)
+    // Split output (the packed q | k | v projection): channels [c1, c2) go to y_k, [c2, C) to y_v, each
+    // a contiguous [rows, width] tensor; y holds [0, c1).  y_k == nullptr: all C channels go to y.
+    void* y_k;
+    void* y_v;
+    int c1, c2;
 };
 
 // Launchers (return the launch error, cudaSuccess if enqueued).

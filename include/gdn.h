@@ -208,6 +208,26 @@ gdn_status_t gdn_causal_conv1d_step(const void* x, long long x_stride, const flo
                                     int N, int C, int K, const gdn_opts_t* opts);
 
 /*
+ * gdn_causal_conv1d_fwd_qkv / gdn_causal_conv1d_step_qkv -- the same convolutions over the packed
+ * projection of the GatedDeltaNet shell (its q, k and v channels side by side in one row: q in
+ * [0, Cq), k in [Cq, Cq + Ck), v in [Cq + Ck, C), C = Cq + Ck + Cv), in one launch, writing the three
+ * channel ranges to three dense tensors -- the layouts gdn_chunk_fwd and gdn_recurrent_step take:
+ *
+ *   x          [B, T, C] (fwd) or [N, C] (step) dtype, rows x_stride elements apart (0 = C)
+ *   w          [C, K] float, the channels in the same q | k | v order
+ *   y_q, y_k, y_v  [B, T, Cq], [B, T, Ck], [B, T, Cv] (fwd) or [N, Cq], [N, Ck], [N, Cv] (step) dtype
+ *   caches     as for the single-output calls, over all C channels
+ * Cq, Ck, Cv positive multiples of 8; the results are bit-identical to the single-output call
+ * followed by a split of y.  Errors and options as for the single-output calls.
+ */
+gdn_status_t gdn_causal_conv1d_fwd_qkv(const void* x, long long x_stride, const float* w, const void* cache_in,
+                                       void* y_q, void* y_k, void* y_v, void* cache_out, int B, int T, int Cq,
+                                       int Ck, int Cv, int K, const gdn_opts_t* opts);
+gdn_status_t gdn_causal_conv1d_step_qkv(const void* x, long long x_stride, const float* w, void* cache, void* y_q,
+                                        void* y_k, void* y_v, int N, int Cq, int Ck, int Cv, int K,
+                                        const gdn_opts_t* opts);
+
+/*
  * gdn_recurrent_bwd -- the backward pass: gradients of a loss L(out, S_final) of gdn_chunk_fwd with
  * respect to q, k, v, g, beta and S0, given grad_out = dL/dout and grad_S_final = dL/dS_final.  It is
  * the adjoint of the token loop of "Transformer by Hand, ch. 7" (section "The formula"), which the

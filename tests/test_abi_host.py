@@ -171,6 +171,34 @@ def test_conv_empty_calls_do_nothing(lib):
     assert lib.gdn_causal_conv1d_step(0, 0, 0, 0, 0, 0, 64, 4, opts(lib)) == pkg_lib.GDN_OK
 
 
+def conv_qkv(lib, step=False, B=1, T=8, widths=(64, 64, 128), K=4, ptrs=None, **kw):
+    p = [FAKE] * 7 if ptrs is None else ptrs   # x, w, cache (in), y_q, y_k, y_v, cache_out
+    Cq, Ck, Cv = widths
+    if step:
+        return lib.gdn_causal_conv1d_step_qkv(p[0], 0, p[1], p[2], p[3], p[4], p[5], B, Cq, Ck, Cv, K, opts(lib, **kw))
+    return lib.gdn_causal_conv1d_fwd_qkv(p[0], 0, p[1], p[2], p[3], p[4], p[5], p[6], B, T, Cq, Ck, Cv, K,
+                                         opts(lib, **kw))
+
+
+@pytest.mark.parametrize("step", [False, True])
+@pytest.mark.parametrize("case,expect", [
+    (dict(widths=(0, 64, 64)), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(widths=(64, 12, 64)), pkg_lib.GDN_ERR_INVALID_ARG),      # not a multiple of 8
+    (dict(widths=(64, 64, -8)), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(K=5), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(ptrs=[FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),          # y_k missing
+    (dict(ptrs=[FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),   # y_v misaligned
+])
+def test_conv_qkv_argument_errors(lib, step, case, expect):
+    assert conv_qkv(lib, step=step, **case) == expect
+    assert lib.gdn_last_error() != b""
+
+
+def test_conv_qkv_empty_calls_do_nothing(lib):
+    assert conv_qkv(lib, B=0, T=0, ptrs=[0] * 7) == pkg_lib.GDN_OK
+    assert conv_qkv(lib, step=True, B=0, ptrs=[0] * 7) == pkg_lib.GDN_OK
+
+
 def bwd(lib, B=1, T=8, Hqk=1, Hv=1, dk=32, dv=32, ptrs=None, **kw):
     p = [FAKE] * 14 if ptrs is None else ptrs
     return lib.gdn_recurrent_bwd(*p, B, T, Hqk, Hv, dk, dv, opts(lib, **kw))

@@ -147,3 +147,53 @@ def test_conv_fwd_misaligned_weights_use_scalar_taps():
     torch.cuda.synchronize()
     ry, _ = oconv.causal_conv1d(x, w)
     assert rel_err(ry, y.float().cpu().numpy()) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("packed", [False, True])
+def test_conv_fwd_qkv_is_the_split_of_one_convolution(dtype, packed):
+    """The packed q | k | v projection in one launch, written to three dense tensors: bit-identical to
+    the single-output convolution of the whole projection split by channel, and within the parity
+    tolerance of the oracle (caches over all channels, in and out)."""
+    widths = (64, 64, 128)
+    C, K = sum(widths), 4
+    if packed:
+        lens = (0, 3, 130, 1, 70)
+        B, T, nseq = 1, sum(lens), len(lens)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    else:
+        B, T, nseq, cu = 2, 150, 2, None
+    x, w, cache = _inputs(110, (B, T), C, K, dtype, nseq)
+    xd, wd, cd = up(x, dtype), up(w, torch.float32), up(cache, dtype)
+    cu_d = None if cu is None else torch.from_numpy(cu).cuda()
+    (yq, yk, yv), co = gdn.gdn_causal_conv1d_fwd_qkv(xd, wd, widths, cd, cu_seqlens=cu_d)
+    full, co_full = gdn.gdn_causal_conv1d_fwd(xd, wd, cd, cu_seqlens=cu_d)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([yq, yk, yv], -1), full)
+    assert torch.equal(co, co_full)
+    ry, rc = oconv.causal_conv1d(x, w, cache, cu_seqlens=cu)
+    assert rel_err(ry, torch.cat([yq, yk, yv], -1).float().cpu().numpy()) <= TOL[dtype]
+    np.testing.assert_array_equal(co.float().cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_conv_step_qkv_is_the_split_of_one_step(dtype):
+    """Decode steps of the packed projection in one launch each, against the single-output step on a
+    copy of the cache (bit-identical outputs and caches) and the oracle over all steps."""
+    widths = (32, 32, 64)
+    N, T, C, K = 7, 5, sum(widths), 4
+    x, w, cache = _inputs(120, (N, T), C, K, dtype, N)
+    wd = up(w, torch.float32)
+    c_split, c_one = up(cache, dtype), up(cache, dtype)
+    ys = []
+    for t in range(T):
+        xt = up(np.ascontiguousarray(x[:, t]), dtype)
+        yq, yk, yv = gdn.gdn_causal_conv1d_step_qkv(xt, wd, c_split, widths)
+        y1 = gdn.gdn_causal_conv1d_step(xt, wd, c_one)
+        torch.cuda.synchronize()
+        assert torch.equal(torch.cat([yq, yk, yv], -1), y1)
+        ys.append(y1)
+    assert torch.equal(c_split, c_one)
+    ry, rc = oconv.causal_conv1d(x, w, cache)
+    assert rel_err(ry, torch.stack(ys, 1).float().cpu().numpy()) <= TOL[dtype]
+    np.testing.assert_array_equal(c_split.float().cpu().numpy(), rc)
