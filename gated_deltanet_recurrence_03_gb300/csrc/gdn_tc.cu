@@ -229,7 +229,6 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         *abort_flag = 0;
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
-        mbar_init(bar_drain, 1);
         mbar_fence_init();
         mbar_arrive_expect_tx(bar_tma, 4 * 8192);
         for (int p = 0; p < 2; ++p) {
@@ -579,10 +578,13 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (warp == 0) {
         if (tid == 0) {
             bulk_wait_read();   // shared memory may be released; the global writes finish on their own
-            // after a bounded wait gave up: no MMA or tile load of this CTA may still be running
-            mma_commit(bar_drain);
-            mbar_wait_drain(bar_drain, 0, kWaitLimitNs);
-            mbar_wait_drain(bar_tma, 0, kWaitLimitNs);
+            if (*abort_flag) {   // a bounded wait gave up: no MMA or tile load of this CTA may still be running
+                mbar_init(bar_drain, 1);   // initialised only here: off the normal path
+                mbar_fence_init();
+                mma_commit(bar_drain);
+                mbar_wait_drain(bar_drain, 0, kWaitLimitNs);
+                mbar_wait_drain(bar_tma, 0, kWaitLimitNs);
+            }
         }
         __syncwarp();
         tc_fence_after();
@@ -664,7 +666,6 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         for (int q = 0; q < kKStages; ++q) mbar_init(bar_k0 + 8 * q, 1);
         mbar_init(bar_mma1, 1);
         mbar_init(bar_mma2, 1);
-        mbar_init(bar_drain, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -681,10 +682,12 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         return mbar_wait_bounded(bar_k0 + 8 * (uint32_t)(c % kKStages), (uint32_t)((c / kKStages) & 1), abort_flag,
                                  status, kStatusTimeout, kWaitLimitNs);
     };
-    // After a bounded wait has given up no further copies are issued, so that the drain before exit
-    // covers every copy still in flight.
+    // A stage is refilled only by a thread whose own waits showed it consumed (a register test: a
+    // shared-memory read of the abort flag here added ~8 us to the 8k prefill's chain), so after a bounded
+    // wait gives up no load overlaps another on a stage and the drain before exit covers every one.
+    bool waits_ok = true;
     auto issue_loads_a = [&](long long c) {   // A1 and the V slice of chunk c
-        if (*abort_flag) return;
+        if (!waits_ok) return;
         const int st = (int)(c & 1);
         const long long slot = base + c;
         const uint32_t bar = bar_a0 + 8 * st;
@@ -693,7 +696,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         tma_load_3d(sb + C_VT + st * 8192, &tm_v, 64 * z, h, (int)(s0 + c * kC), bar);
     };
     auto issue_loads_k = [&](long long c) {   // K tile and the b / gamma_C vector of chunk c
-        if (*abort_flag) return;
+        if (!waits_ok) return;
         const int st = (int)(c % kKStages);
         const long long slot = base + c;
         const int tc0 = (int)(s0 + c * kC);
@@ -798,8 +801,8 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     tmem_wait_st();
                     tc_fence_before();
                 }
-                wait_k(c);
-                mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+                waits_ok &= wait_k(c);
+                waits_ok &= mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
                 tc_fence_after();
                 uint32_t a[32];
                 tmem_ld32(tl + 64 + 64 * st + cb, a);
@@ -844,10 +847,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 }
                 float gnext = 1.f;
                 if (!last) {   // the next chunk's gamma_C, read while the state update runs
-                    wait_k(c + 1);
+                    waits_ok &= wait_k(c + 1);
                     gnext = reinterpret_cast<const float*>(sm + C_VEC + (int)((c + 1) % kKStages) * 512)[64];
                 }
-                mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+                waits_ok &= mbar_wait_bounded(bar_mma2, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
                 tc_fence_after();
                 {   // new state row R: bf16 copy for the next D1 now, gamma-scaled copy to TMEM next step
                     uint32_t v[32];
@@ -877,10 +880,12 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             __syncthreads();
         }
-        if (tid == kIssuer) {
-            // Before the TMEM and shared memory are released: every MMA has completed and no copy is still
-            // landing (after a bounded wait gave up, consumers may have skipped chunks whose loads were
+        if (tid == kIssuer && *abort_flag) {
+            // A bounded wait gave up: before the TMEM and shared memory are released, every MMA has
+            // completed and no copy is still landing (consumers may have skipped chunks whose loads were
             // issued).  Each stage's last armed phase is the latest one, so its parity test is exact.
+            mbar_init(bar_drain, 1);   // initialised only here: off the normal path
+            mbar_fence_init();
             mma_commit(bar_drain);
             mbar_wait_drain(bar_drain, 0, kWaitLimitNs);
             for (long long c = max(0LL, nch - 2); c < nch; ++c)
