@@ -71,7 +71,11 @@ typedef enum gdn_dtype {
 
 typedef struct gdn_opts {
     int dtype;                  /* gdn_dtype_t of q, k, v, g, beta, out.  Default GDN_BF16. */
-    int chunk;                  /* prefill chunk length: 16, 32 or 64.  0 -> 64. */
+    int chunk;                  /* prefill chunk length: 16, 32 or 64 (0 -> 64; others rejected).
+                                   Every chunk length gives the token loop's result up to rounding
+                                   (the chunked form is the loop regrouped), and both chunked kernel
+                                   families are built on 64-token tensor-core tiles: they serve all
+                                   three values with 64-token chunks, so results do not depend on it. */
     float scale;                /* multiplies every output o_t.  Default 1.0f. */
     unsigned flags;             /* GDN_NORMALIZE_QK | GDN_RAW_GATES | GDN_OUTPUT_GATE, default 0 */
     const int32_t* cu_seqlens;  /* prefill only: DEVICE pointer to num_seqs+1 int32 token offsets
@@ -108,12 +112,13 @@ void gdn_opts_init(gdn_opts_t* opts);
  *   S_final  [nseq, Hv, dk, dv] float or NULL (not written); may equal S0 (in-place update)
  *
  * Supported: dk, dv in {32, 64, 128}; Hv a multiple of Hqk; B, T >= 0.  T = 0 copies S0 to
- * S_final (zeros when S0 is NULL).  Three kernel families, chosen in this order:
- *   - bf16 inputs with dk = dv = 128: the tcgen05 tensor-core path (chunk 64); it needs the
- *     workspace (GDN_ERR_WORKSPACE if missing or too small);
+ * S_final (zeros when S0 is NULL).  Three kernel families, chosen in this order (opts->chunk does
+ * not take part in the choice: the two chunked families block in 64-token chunks for every value):
+ *   - bf16 inputs with dk = dv = 128: the tcgen05 tensor-core path; it needs the workspace
+ *     (GDN_ERR_WORKSPACE if missing or too small);
  *   - other inputs, when the workspace is at least gdn_chunk_fwd_workspace_size() bytes (256-byte
- *     aligned): the same chunk algebra on split-tf32 tensor-core MMAs in fp32 accuracy (64-token
- *     chunks whatever opts->chunk says), GDN_NORMALIZE_QK and GDN_RAW_GATES included;
+ *     aligned): the same chunk algebra on split-tf32 tensor-core MMAs in fp32 accuracy,
+ *     GDN_NORMALIZE_QK and GDN_RAW_GATES included;
  *   - otherwise the token-serial CUDA-core kernel, which needs no workspace.
  * out must not overlap any input.
  *

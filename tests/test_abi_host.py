@@ -277,3 +277,12 @@ def test_workspace_sizes_follow_the_slot_layout(lib, B, T, Hqk, Hv, dk, dv, dtyp
 def test_tensor_core_path_accepts_any_head_grouping(lib):
     for Hqk, Hv in ((2, 2), (1, 3), (16, 32)):
         assert lib.gdn_chunk_fwd_workspace_size(1, 512, Hqk, Hv, 128, 128, opts(lib)) > 0
+
+
+def test_chunk_option_does_not_change_the_path(lib):
+    # opts.chunk in {16, 32, 64} is a blocking choice both chunked families serve with 64-token chunks:
+    # the same kernels, hence the same workspace, whatever the value (bf16 d=128: the tcgen05 path)
+    for dtype, d in ((pkg_lib.GDN_BF16, 128), (pkg_lib.GDN_F32, 32), (pkg_lib.GDN_BF16, 64)):
+        sizes = {c: lib.gdn_chunk_fwd_workspace_size(2, 300, 2, 4, d, d, opts(lib, dtype=dtype, chunk=c))
+                 for c in (0, 16, 32, 64)}
+        assert len(set(sizes.values())) == 1 and sizes[64] > 0, sizes

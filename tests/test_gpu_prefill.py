@@ -109,6 +109,21 @@ def test_deterministic():
     np.testing.assert_array_equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("name,dtype,d", [("tc", "bf16", 128), ("split_tf32", "f32", 32)])
+def test_chunk_option_gives_the_same_result(name, dtype, d):
+    """opts.chunk 16, 32 and 64 run the same 64-token blocking: bit-identical results, each within
+    the tolerance of the oracle (configs asking for chunk 16 or 32 get the fast path, not a fallback)."""
+    w = gi.Workload("chunks_" + name, "prefill", dtype, B=2, T=150, Hqk=2, Hv=4, dk=d, dv=d, chunk=16,
+                    s0_std=0.1, seed=21)
+    x = gi.make_prefill_inputs(w)
+    ref_o, ref_s = orc.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], S0=x.get("S0"))
+    res = {c: prefill_on_gpu(x, dtype, chunk=c) for c in (16, 32, 64)}
+    for c in (16, 32):
+        np.testing.assert_array_equal(res[c][0], res[64][0])
+        np.testing.assert_array_equal(res[c][1], res[64][1])
+    assert rel_err(ref_o, res[16][0]) <= TOL[dtype] and rel_err(ref_s, res[16][1]) <= TOL[dtype]
+
+
 # ---------------------------------------------------------------- full sizes, sampled heads
 def _sampled(w, heads, seqs=None):
     x = gi.make_prefill_inputs(w)
