@@ -334,7 +334,9 @@ conv_fwd_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restric
 }
 
 // One thread per 16-byte channel vector and block of kStepRows sequences: the weights are loaded
-// once and reused, and the rows' loads are independent (in flight together).
+// once and reused.  Every row's cache and input vectors are loaded before any row is written (the
+// cache is updated in place, so loads placed after a row's stores could not be hoisted above them),
+// which keeps 4 K 16-byte loads of each thread in flight together.
 constexpr int kStepRows = 4;
 
 template <typename T, int K>
@@ -351,19 +353,32 @@ conv_step_kernel(const T* __restrict__ x, long long x_stride, const float* __res
     float2 wr[K][P];
     load_taps<T, K>(w, c0, (reinterpret_cast<uintptr_t>(w) % (K * sizeof(float))) == 0, wr);
     for (size_t n0 = (size_t)blockIdx.y * kStepRows; n0 < (size_t)N; n0 += (size_t)gridDim.y * kStepRows) {
+        uint4 raw[kStepRows][K];   // the K - 1 cached inputs, oldest first, then this step's input
+#pragma unroll
+        for (int r = 0; r < kStepRows; ++r) {
+            const size_t n = n0 + r;
+            if (n < (size_t)N) {
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k)
+                    raw[r][k] = *reinterpret_cast<const uint4*>(cache + (n * (K - 1) + k) * C + c0);
+                raw[r][K - 1] = *reinterpret_cast<const uint4*>(x + (long long)n * x_stride + c0);
+            } else {
+#pragma unroll
+                for (int k = 0; k < K; ++k) raw[r][k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
 #pragma unroll
         for (int r = 0; r < kStepRows; ++r) {
             const size_t n = n0 + r;
             if (n >= (size_t)N) break;
             float2 hist[K][P];
 #pragma unroll
-            for (int k = 0; k < K - 1; ++k) load_vec(cache + (n * (K - 1) + k) * C + c0, hist[k]);
-            load_vec(x + (long long)n * x_stride + c0, hist[K - 1]);
+            for (int k = 0; k < K; ++k) Vec<T>::unpack2(raw[r][k], hist[k]);
             float2 out[P];
             conv_out<T, K>(wr, hist, out);
             store_vec(yb + n * yw + yc, out);
 #pragma unroll
-            for (int k = 1; k < K; ++k) store_vec(cache + (n * (K - 1) + (k - 1)) * C + c0, hist[k]);
+            for (int k = 1; k < K; ++k) __stcs(reinterpret_cast<uint4*>(cache + (n * (K - 1) + (k - 1)) * C + c0), raw[r][k]);
         }
     }
 }
@@ -382,7 +397,9 @@ cudaError_t fwd_typed(const ConvArgs& a) {
         e = cudaFuncSetAttribute(conv_fwd_kernel<T, K>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     // one CTA per SM, rounded down to a multiple of the channel groups when there are fewer groups
-    // than CTAs; at least one CTA, which also passes the caches of sequences without tokens through
+    // than CTAs (a grid of every SM, each CTA reloading its taps when its group changes, measured the
+    // same on the 8192-channel projection: 0.101 ms); at least one CTA, which also passes the caches
+    // of sequences without tokens through
     long long G = sms;
     if (n_cg <= G) G = G / n_cg * n_cg;
     const unsigned grid = (unsigned)max(1LL, min(tiles, G));
