@@ -457,6 +457,7 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
     a.B = B; a.T = T; a.Hqk = Hqk; a.Hv = Hv; a.dk = dk; a.dv = dv; a.dtype = o.dtype; a.scale = o.scale;
     a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq; a.workspace = o.workspace;
     a.stream = static_cast<cudaStream_t>(o.stream);
+    a.status = status;
     record(o, 0, a.stream);
     const cudaError_t err = launch_backward(a);
     record(o, 1, a.stream);

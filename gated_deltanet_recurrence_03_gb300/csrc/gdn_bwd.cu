@@ -1321,8 +1321,16 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
         q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec, nullptr, nullptr, false);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
-        k, a.S0, nullptr, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, vec, false);
+    // the forward chain: on the tcgen05 tensor cores for bf16 inputs with dk = dv = 128 (16-byte aligned k)
+    e = cudaErrorNotSupported;
+    if constexpr (sizeof(TT) == 2 && DK == 128 && DV == 128)
+        e = launch_bwd_state_fwd_tc(a.k, a.S0, nullptr, ws.W, ws.U, ws.G, ws.S, nullptr, a.T, a.Hqk, a.Hv,
+                                    a.cu_seqlens, a.num_seqs, false, a.stream, a.status);
+    if (e == cudaErrorNotSupported)
+        bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
+            k, a.S0, nullptr, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, vec, false);
+    else if (e != cudaSuccess)
+        return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_state_adj_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
         q, k, dout, a.dS_final, a.grad_S0, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);

@@ -107,6 +107,7 @@ struct BackwardArgs {
     int num_seqs;
     void* workspace;
     cudaStream_t stream;
+    unsigned* status;           // device status word (bounded waits)
 };
 
 // Workspace of the backward pass: per (chunk slot, value head) fp32 arrays T, P (C x C), W (C x dk),
@@ -118,6 +119,14 @@ struct BwdLayout {
 };
 BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed, bool adjoint);
 cudaError_t launch_backward(const BackwardArgs& a);
+// The backward's forward chunk chain on the tcgen05 tensor cores, for bf16 k with dk = dv = 128: the
+// chunk-start states into ws_S, U = U~ - W S over ws_U (U~ read from there), the last state into
+// S_final (or not).  cudaErrorNotSupported when k is not 16-byte aligned (the caller then runs the
+// general chain).
+cudaError_t launch_bwd_state_fwd_tc(const void* k, const float* S0, float* S_final, const float* ws_W, float* ws_U,
+                                    const float* ws_G, float* ws_S, const float* ws_R, int T, int Hqk, int Hv,
+                                    const int32_t* cu, int nseq, bool normalize, cudaStream_t stream,
+                                    unsigned* status);
 // Chunked prefill for shapes outside the tensor-core path (fp32 inputs, head dims 32 / 64, front end
 // included): the backward's WY kernel and forward chain plus an output kernel.
 size_t chunked_prefill_workspace_bytes(int B, int T, int Hv, int dk, int dv, int nseq, bool packed);
