@@ -1332,8 +1332,16 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     else if (e != cudaSuccess)
         return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_state_adj_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
-        q, k, dout, a.dS_final, a.grad_S0, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+    // the adjoint chain: on the tcgen05 tensor cores for bf16 inputs with dk = dv = 128 (16-byte aligned q, k, dout)
+    e = cudaErrorNotSupported;
+    if constexpr (sizeof(TT) == 2 && DK == 128 && DV == 128)
+        e = launch_bwd_state_adj_tc(a.q, a.k, a.dout, a.dS_final, a.grad_S0, ws.W, ws.P, ws.G, ws.dS, ws.dU, a.T, a.Hqk,
+                                    a.Hv, a.cu_seqlens, a.num_seqs, a.scale, a.stream, a.status);
+    if (e == cudaErrorNotSupported)
+        bwd_state_adj_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
+            q, k, dout, a.dS_final, a.grad_S0, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
+    else if (e != cudaSuccess)
+        return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_local_kernel<TT, DK, DV><<<chunk_grid, kLoThreads, S4::BYTES, a.stream>>>(
         q, k, v, beta, dout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk, a.Hv,

@@ -432,6 +432,356 @@ bwd_state_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
     }
 }
 
+// ------------------------------------------------------------------ the adjoint chain
+// Chunks in reverse, per (sequence, value head, 64-column slice); lam = dL/dS at a chunk's end (fp32,
+// in TMEM), dO the output gradient, P = scale D o Q K^T (from the WY kernel):
+//     dU  = b o (K lam) + P^T dO                       (to the workspace)
+//     lam <- gamma_C lam + (s gamma o Q)^T dO - W^T dU  (the chunk-end values go to the workspace)
+// with the same three-part splits: K lam = K (lam_h + lam_m + lam_l) and P^T dO = sum_p P^T_p dO
+// (K, dO exact bf16 inputs), (s gamma o Q)^T dO = sum_p A_p dO, and W^T dU over the six part pairs
+// above 2^-22.  The 64-row products run as M = 128 MMAs whose rows 64-127 are not used.  (s gamma o
+// Q)^T, -W^T and P^T are written to TMEM by the epilogue warps as bf16 A operands (lane = the
+// product's row) while K lam runs.
+constexpr uint32_t A_LB = 0;          // lam parts: MN-major B, 128 dk rows x 64 columns (16 KB each)
+constexpr uint32_t A_UB = 49152;      // dU parts: MN-major B, 64 token rows x 64 columns (8 KB each)
+constexpr uint32_t A_KT = 73728;      // K tile (2 panels x 64 token rows); K lam reads 64 rows past it
+constexpr uint32_t A_QT = 90112;      // Q tile
+constexpr uint32_t A_OT = 106496;     // dO slice, 2 stages x 64 token rows x 64 columns
+constexpr uint32_t A_WST = 122880;    // W fp32, 4 swizzled panels of 32 columns x 64 rows
+constexpr uint32_t A_PST = 155648;    // P fp32, 2 swizzled panels of 32 columns x 64 rows
+constexpr uint32_t A_GST = 172032;    // G [64]
+constexpr uint32_t A_XU = 173056;     // dU fp32, 2 swizzled panels (the TMA store's source)
+constexpr uint32_t A_SST = 189440;    // a chunk-end lam, fp32, 4 swizzled panels (the TMA store's source)
+constexpr uint32_t A_BAR = 222208;
+constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
+static_assert(A_SMEM <= 227 * 1024 && A_XU % 1024 == 0 && A_SST % 1024 == 0 && A_PST % 1024 == 0, "adjoint layout");
+// TMEM: lam 0-63, K lam 64-127, P^T dO 128-191, (s gamma o Q)^T parts 192-287, -W^T parts 288-383,
+// P^T parts 384-479 (32 columns a part: 64 K values).
+constexpr uint32_t J_L = 0, J_D = 64, J_E = 128, J_AQ = 192, J_AW = 288, J_AP = 384;
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_w,
+                        const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_du,
+                        const __grid_constant__ CUtensorMap tm_ds, const float* __restrict__ ws_G,
+                        const float* __restrict__ dS_final, float* __restrict__ grad_S0, float* __restrict__ ws_dS,
+                        int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu, int nseq, float scale,
+                        unsigned* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    // K tile, dO stages [2], staging (Q, W, P, G), K lam + P^T dO done, lam update done, drain
+    const uint32_t bar_kt = sb + A_BAR, bar_o0 = sb + A_BAR + 8, bar_st = sb + A_BAR + 24, bar_du = sb + A_BAR + 32,
+                   bar_l = sb + A_BAR + 40, bar_drain = sb + A_BAR + 48;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + A_BAR + 56);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + A_BAR + 60);
+    int* issued = reinterpret_cast<int*>(sm + A_BAR + 64);   // K tiles, dO tiles, staging sets issued
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool epi = warp < kEpiThreads / 32;
+    const int quarter = warp & 3, half = (warp >> 2) & 1;
+    const int R = 32 * quarter + lane, cb = 32 * half;
+    const int z = blockIdx.x % kSlices, h = (blockIdx.x / kSlices) % Hv, i = blockIdx.x / (kSlices * Hv);
+    if (i >= nseq) return;
+    const int hk = h / (Hv / Hqk), col0 = kSW * z;
+    long long t0, t1;
+    seq_range(cu, i, T_len, t0, t1);
+    const long long nch = (t1 - t0 + kC - 1) / kC, slot0 = t0 / kC + i;
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tc_fence_before();
+    }
+    if (tid == 0) {
+        *abort_flag = 0;
+        issued[0] = issued[1] = issued[2] = 0;
+        mbar_init(bar_kt, 1);
+        mbar_init(bar_o0, 1);
+        mbar_init(bar_o0 + 8, 1);
+        mbar_init(bar_st, 1);
+        mbar_init(bar_du, 1);
+        mbar_init(bar_l, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
+    const size_t sbase = ((size_t)i * Hv + h) * kD * kD + col0;
+
+    // chunks run c = nch - 1 .. 0; j = nch - 1 - c counts the steps (and each resource's loads)
+    auto wi = [&](long long c) { return (size_t)(slot0 + c) * Hv + h; };
+    auto wait_par = [&](uint32_t bar, uint32_t par) {
+        return mbar_wait_bounded(bar, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
+    };
+    bool waits_ok = true;
+    auto load_kt = [&](long long c) {
+        if (!waits_ok) return;
+        const int tc0 = (int)(t0 + c * kC);
+        mbar_arrive_expect_tx(bar_kt, 16384);
+        tma_load_3d(sb + A_KT, &tm_k, 0, hk, tc0, bar_kt);
+        tma_load_3d(sb + A_KT + 8192, &tm_k, 64, hk, tc0, bar_kt);
+        issued[0] += 1;
+    };
+    auto load_do = [&](long long c) {   // into stage (nch - 1 - c) & 1
+        if (!waits_ok) return;
+        const uint32_t st = (uint32_t)((nch - 1 - c) & 1), bar = bar_o0 + 8 * st;
+        mbar_arrive_expect_tx(bar, 8192);
+        tma_load_3d(sb + A_OT + st * 8192, &tm_do, col0, h, (int)(t0 + c * kC), bar);
+        issued[1] += 1;
+    };
+    auto load_st = [&](long long c) {   // Q tile, W, P, G of chunk c
+        if (!waits_ok) return;
+        const int tc0 = (int)(t0 + c * kC);
+        mbar_arrive_expect_tx(bar_st, 16384 + 32768 + 16384 + 256);
+        tma_load_3d(sb + A_QT, &tm_q, 0, hk, tc0, bar_st);
+        tma_load_3d(sb + A_QT + 8192, &tm_q, 64, hk, tc0, bar_st);
+        for (int p = 0; p < 4; ++p) tma_load_2d(sb + A_WST + p * 8192, &tm_w, 32 * p, (int)(wi(c) * kC), bar_st);
+        for (int p = 0; p < 2; ++p) tma_load_2d(sb + A_PST + p * 8192, &tm_p, 32 * p, (int)(wi(c) * kC), bar_st);
+        bulk_g2s(sb + A_GST, ws_G + wi(c) * kC, 256, bar_st);
+        issued[2] += 1;
+    };
+    const float* sG = reinterpret_cast<const float*>(sm + A_GST);
+    const uint64_t dLB = smem_desc(sb + A_LB, 1024, 1024), dUB = smem_desc(sb + A_UB, 1024, 1024),
+                   dKT = smem_desc(sb + A_KT, 16, 1024), dOT = smem_desc(sb + A_OT, 1024, 1024);
+
+    // (s gamma o Q)^T, -W^T (rows = dk R, tokens 32 half .. + 31) and P^T (rows R < 64) of the staged chunk
+    // with n tokens: the tiles' rows past a sequence's end hold the next sequence's q, so s gamma is
+    // zero there (W and P rows are zero there by construction)
+    auto put_a = [&](int n) {
+        uint32_t ph[16], pm[16], pl[16];
+        const uint32_t jq = (uint32_t)((R & 63) >> 3), oq = (uint32_t)(R & 7) * 2;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {   // (s gamma_t q_t)[R], tokens t, t + 1
+            const uint32_t ta = (uint32_t)(32 * half + 2 * e), tb = ta + 1;
+            const uint8_t* qp = sm + A_QT + (R >> 6) * 8192;
+            const float qa = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(qp + ta * 128 + ((jq ^ (ta & 7)) << 4) + oq) << 16);
+            const float qb = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(qp + tb * 128 + ((jq ^ (tb & 7)) << 4) + oq) << 16);
+            const float fa = (int)ta < n ? scale * __expf(sG[ta]) : 0.f, fb = (int)tb < n ? scale * __expf(sG[tb]) : 0.f;
+            split3(fa * qa, fb * qb, ph[e], pm[e], pl[e]);
+        }
+        tmem_st16(tl + J_AQ + 16 * half, ph);
+        tmem_st16(tl + J_AQ + 32 + 16 * half, pm);
+        tmem_st16(tl + J_AQ + 64 + 16 * half, pl);
+        const uint32_t jw = (uint32_t)((R & 31) >> 2), ow = (uint32_t)(R & 3) * 4;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {   // -W[t][R]
+            const uint32_t ta = (uint32_t)(32 * half + 2 * e), tb = ta + 1;
+            const uint8_t* wp = sm + A_WST + (R >> 5) * 8192;
+            const float wa = *reinterpret_cast<const float*>(wp + ta * 128 + ((jw ^ (ta & 7)) << 4) + ow);
+            const float wb = *reinterpret_cast<const float*>(wp + tb * 128 + ((jw ^ (tb & 7)) << 4) + ow);
+            split3(-wa, -wb, ph[e], pm[e], pl[e]);
+        }
+        tmem_st16(tl + J_AW + 16 * half, ph);
+        tmem_st16(tl + J_AW + 32 + 16 * half, pm);
+        tmem_st16(tl + J_AW + 64 + 16 * half, pl);
+        if (R < 64) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {   // P[s][R], s = 32 half + 2 e, + 1
+                const uint32_t sa = (uint32_t)(32 * half + 2 * e), sb2 = sa + 1;
+                const uint8_t* pp = sm + A_PST + (R >> 5) * 8192;
+                const float pa = *reinterpret_cast<const float*>(pp + sa * 128 + ((jw ^ (sa & 7)) << 4) + ow);
+                const float pb = *reinterpret_cast<const float*>(pp + sb2 * 128 + ((jw ^ (sb2 & 7)) << 4) + ow);
+                split3(pa, pb, ph[e], pm[e], pl[e]);
+            }
+            tmem_st16(tl + J_AP + 16 * half, ph);
+            tmem_st16(tl + J_AP + 32 + 16 * half, pm);
+            tmem_st16(tl + J_AP + 64 + 16 * half, pl);
+        }
+    };
+
+    if (nch == 0) {   // no tokens: the gradient of S0 is that of S_final
+        if (grad_S0 && epi) {
+            for (int e = 0; e < 32; e += 4) {
+                const size_t o = sbase + (size_t)R * kD + cb + e;
+                *reinterpret_cast<float4*>(grad_S0 + o) =
+                    dS_final ? *reinterpret_cast<const float4*>(dS_final + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    } else {
+        if (tid == kIssuer) {
+            load_kt(nch - 1);
+            load_st(nch - 1);
+            load_do(nch - 1);
+            if (nch > 1) load_do(nch - 2);
+        }
+        if (epi) {   // lam of the last chunk's end: workspace, parts, gamma_C-scaled into TMEM
+            uint32_t v[32];
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 x = dS_final ? *reinterpret_cast<const float4*>(dS_final + sbase + (size_t)R * kD + cb + e)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[e] = __float_as_uint(x.x); v[e + 1] = __float_as_uint(x.y);
+                v[e + 2] = __float_as_uint(x.z); v[e + 3] = __float_as_uint(x.w);
+                *reinterpret_cast<float4*>(ws_dS + wi(nch - 1) * kD * kD + (size_t)R * kD + col0 + cb + e) = x;
+            }
+            store_parts(sm + A_LB, 16384, R, cb >> 3, v);
+            waits_ok &= wait_par(bar_st, 0);
+            const float g = __expf(sG[kC - 1]);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(g * __uint_as_float(v[e]));
+            tmem_st32(tl + J_L + cb, v);
+            tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        for (long long c = nch - 1; c >= 0; --c) {
+            const long long j = nch - 1 - c;
+            const uint32_t par = (uint32_t)(j & 1);
+            if (!epi) {   // ---- the issuing warp
+                if (j > 0) nb_sync(1, kThreads);   // lam parts in LB, gamma-scaled lam in TMEM
+                if (lane == 0) {   // K lam = K (lam_h + lam_m + lam_l)
+                    wait_par(bar_kt, par);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int p = 0; p < 3; ++p)
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_bf16(tmem + J_D, dKT + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4),
+                                     dLB + ((p * 16384 + ks * 2048) >> 4), idesc_bf16(128, 64, 0, 1), (p > 0 || ks > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+                nb_sync(2, kThreads);   // the A operands of this chunk are in TMEM; the staging was read
+                if (lane == 0) {   // P^T dO, then lam += (s gamma o Q)^T dO
+                    if (c > 0) load_st(c - 1);
+                    wait_par(bar_o0 + 8 * par, (uint32_t)((j >> 1) & 1));
+                    tc_fence_after();
+                    const uint64_t od = dOT + ((par * 8192u) >> 4);
+#pragma unroll 1
+                    for (int p = 0; p < 3; ++p)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16_ta(tmem + J_E, tmem + J_AP + 32 * p + 8 * ks, od + ((ks * 2048) >> 4),
+                                        idesc_bf16(128, 64, 0, 1), (p > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar_du);
+#pragma unroll 1
+                    for (int p = 0; p < 3; ++p)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16_ta(tmem + J_L, tmem + J_AQ + 32 * p + 8 * ks, od + ((ks * 2048) >> 4),
+                                        idesc_bf16(128, 64, 0, 1), 1u);
+                }
+                __syncwarp();
+                nb_sync(3, kThreads);   // the dU parts are in UB
+                if (lane == 0) {   // lam -= W^T dU over the part pairs (h,h) (h,m) (m,h) (h,l) (l,h) (m,m)
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int q = 0; q < 6; ++q) {
+                        const int a = (q == 2 || q == 5) ? 1 : (q == 4 ? 2 : 0);
+                        const int u = (q == 1 || q == 5) ? 1 : (q == 3 ? 2 : 0);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16_ta(tmem + J_L, tmem + J_AW + 32 * a + 8 * ks, dUB + ((u * 8192 + ks * 2048) >> 4),
+                                        idesc_bf16(128, 64, 0, 1), 1u);
+                    }
+                    mma_commit(bar_l);
+                }
+                __syncwarp();
+            } else {      // ---- the epilogue warps
+                float b = 0.f;
+                const int n = (int)min((long long)kC, t1 - (t0 + c * kC));   // tokens of this chunk
+                waits_ok &= wait_par(bar_st, par);   // this chunk's Q, W, P, G
+                put_a(n);
+                if (R < 64) b = __expf(sG[kC - 1] - sG[R]);
+                tmem_wait_st();
+                tc_fence_before();
+                nb_arrive(2, kThreads);
+                waits_ok &= wait_par(bar_du, par);
+                tc_fence_after();
+                if (warp == 7 && lane == 0 && c > 0) load_kt(c - 1);   // K lam has read the K tile
+                if (R < 64) {   // dU = b o (K lam) + P^T dO: to the workspace and as three parts into UB
+                    uint32_t d[32], e2[32];
+                    tmem_ld32(tl + J_D + cb, d);
+                    tmem_ld32(tl + J_E + cb, e2);
+                    tmem_wait_ld();
+                    uint8_t* xu = sm + A_XU + half * 8192;
+                    const float bm = R < n ? b : 0.f, em = R < n ? 1.f : 0.f;   // rows past the sequence's end: 0
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        d[e] = __float_as_uint(fmaf(bm, __uint_as_float(d[e]), em * __uint_as_float(e2[e])));
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<uint4*>(xu + swz((uint32_t)R, (uint32_t)(e >> 2))) = make_uint4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+                    store_parts(sm + A_UB, 8192, R, cb >> 3, d);
+                    fence_proxy_async_smem();
+                    nb_sync(5, 128);
+                    if (tid == 0) {
+                        tma_store_2d(&tm_du, col0, (int)(wi(c) * kC), sb + A_XU);
+                        tma_store_2d(&tm_du, col0 + 32, (int)(wi(c) * kC), sb + A_XU + 8192);
+                        bulk_commit();
+                    }
+                } else if (warp == 6 && lane == 0) {   // the previous lam store has read its staging
+                    bulk_wait_read();
+                }
+                tc_fence_before();
+                nb_arrive(3, kThreads);
+                waits_ok &= wait_par(bar_l, par);
+                tc_fence_after();
+                if (warp == 7 && lane == 0 && c >= 2) load_do(c - 2);   // this chunk's dO stage has been read
+                {
+                    uint32_t v[32];
+                    tmem_ld32(tl + J_L + cb, v);
+                    tmem_wait_ld();
+                    if (c == 0) {   // lam at the first chunk's start: the gradient of S0
+                        if (grad_S0) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                *reinterpret_cast<float4*>(grad_S0 + sbase + (size_t)R * kD + cb + e) =
+                                    make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                                __uint_as_float(v[e + 3]));
+                        }
+                    } else {   // lam at the end of chunk c - 1: workspace (TMA store), parts, gamma_C-scaled
+                        uint8_t* sst = sm + A_SST + ((R >> 6) * 2 + half) * 8192;
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<uint4*>(sst + swz((uint32_t)(R & 63), (uint32_t)(e >> 2))) =
+                                make_uint4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                        store_parts(sm + A_LB, 16384, R, cb >> 3, v);
+                        waits_ok &= wait_par(bar_st, par ^ 1u);   // chunk c - 1's G
+                        const float g = __expf(sG[kC - 1]);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(g * __uint_as_float(v[e]));
+                        tmem_st32(tl + J_L + cb, v);
+                        tmem_wait_st();
+                        fence_proxy_async_smem();
+                        tc_fence_before();
+                        nb_sync(4, kEpiThreads);
+                        if (warp == 6 && lane == 0) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                tma_store_2d(&tm_ds, col0 + 32 * (q & 1), (int)(wi(c - 1) * kD + 64 * (q >> 1)),
+                                             sb + A_SST + q * 8192);
+                            bulk_commit();
+                        }
+                        if (tid == 0) bulk_wait_read();   // the dU store has read its staging
+                        nb_arrive(1, kThreads);
+                    }
+                }
+            }
+        }
+    }
+    if (tid == 0 || (warp == 6 && lane == 0)) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == kIssuer && *abort_flag) {   // a bounded wait gave up: drain MMAs and loads before release
+        mbar_init(bar_drain, 1);
+        mbar_fence_init();
+        mma_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0, kWaitLimitNs);
+        const int nk = issued[0], no = issued[1], ns = issued[2];
+        if (nk > 0) mbar_wait_drain(bar_kt, (uint32_t)((nk - 1) & 1), kWaitLimitNs);
+        if (ns > 0) mbar_wait_drain(bar_st, (uint32_t)((ns - 1) & 1), kWaitLimitNs);
+        for (int q = max(0, no - 2); q < no; ++q)
+            mbar_wait_drain(bar_o0 + 8 * (uint32_t)(q & 1), (uint32_t)((q >> 1) & 1), kWaitLimitNs);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
 }  // namespace
 
 cudaError_t launch_bwd_state_fwd_tc(const void* k, const float* S0, float* S_final, const float* ws_W, float* ws_U,
@@ -476,6 +826,56 @@ cudaError_t launch_bwd_state_fwd_tc(const void* k, const float* S0, float* S_fin
     const unsigned grid = (unsigned)((long long)nseq * Hv * kSlices);
     bwd_state_fwd_tc_kernel<<<grid, kThreads, B_SMEM, stream>>>(tm, tw, tu, ts, S0, S_final, ws_W, ws_U, ws_G, ws_S, ws_R,
                                                                 T, Hqk, Hv, cu, nseq, normalize ? 1 : 0, status);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn
+
+namespace gdn {
+
+cudaError_t launch_bwd_state_adj_tc(const void* q, const void* k, const void* dout, const float* dS_final,
+                                    float* grad_S0, const float* ws_W, const float* ws_P, const float* ws_G,
+                                    float* ws_dS, float* ws_dU, int T, int Hqk, int Hv, const int32_t* cu, int nseq,
+                                    float scale, cudaStream_t stream, unsigned* status) {
+    const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al16(q) || !al16(k) || !al16(dout)) return cudaErrorNotSupported;
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+    if (!encode) return cudaErrorNotSupported;
+    const long long tokens = cu ? (long long)T : (long long)nseq * T;
+    const long long slots = (tokens + kC - 1) / kC + nseq;
+    if (tokens > INT32_MAX || slots * Hv * kD > INT32_MAX) return cudaErrorInvalidValue;
+    // bf16 [tokens, heads, 128], boxes of 64 features x 1 head x 64 tokens; fp32 [rows, width], boxes of
+    // 32 columns x 64 rows; 128-byte swizzle
+    auto map_bf16 = [&](CUtensorMap* m, const void* base, int heads) {
+        memset(m, 0, sizeof(*m));
+        const cuuint64_t d3[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)(tokens > 0 ? tokens : 1)};
+        const cuuint64_t s3[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
+        const cuuint32_t b3[3] = {64, 1, 64};
+        const cuuint32_t e3[3] = {1, 1, 1};
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), d3, s3, b3, e3,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    auto map_f32 = [&](CUtensorMap* m, const float* base, long long rows, int width) {
+        memset(m, 0, sizeof(*m));
+        const cuuint64_t d2[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+        const cuuint64_t s2[1] = {(cuuint64_t)width * 4};
+        const cuuint32_t b2[2] = {32, (cuuint32_t)kC};
+        const cuuint32_t e2[2] = {1, 1};
+        return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), d2, s2, b2, e2,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    CUtensorMap tk, tq, to, tw, tp, tdu, tds;
+    if (!map_bf16(&tk, k, Hqk) || !map_bf16(&tq, q, Hqk) || !map_bf16(&to, dout, Hv) ||
+        !map_f32(&tw, ws_W, slots * Hv * kC, kD) || !map_f32(&tp, ws_P, slots * Hv * kC, kC) ||
+        !map_f32(&tdu, ws_dU, slots * Hv * kC, kD) || !map_f32(&tds, ws_dS, slots * Hv * kD, kD))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(bwd_state_adj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)A_SMEM);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)((long long)nseq * Hv * kSlices);
+    bwd_state_adj_tc_kernel<<<grid, kThreads, A_SMEM, stream>>>(tk, tq, to, tw, tp, tdu, tds, ws_G, dS_final, grad_S0, ws_dS,
+                                                                T, Hqk, Hv, cu, nseq, scale, status);
     return cudaGetLastError();
 }
 

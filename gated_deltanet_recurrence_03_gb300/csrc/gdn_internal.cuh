@@ -127,6 +127,13 @@ cudaError_t launch_bwd_state_fwd_tc(const void* k, const float* S0, float* S_fin
                                     const float* ws_G, float* ws_S, const float* ws_R, int T, int Hqk, int Hv,
                                     const int32_t* cu, int nseq, bool normalize, cudaStream_t stream,
                                     unsigned* status);
+// The backward's adjoint chunk chain on the tcgen05 tensor cores (bf16 inputs, dk = dv = 128): dU and
+// the chunk-end adjoints into the workspace, the gradient of S0 (or not).  cudaErrorNotSupported when
+// q, k or dout is not 16-byte aligned.
+cudaError_t launch_bwd_state_adj_tc(const void* q, const void* k, const void* dout, const float* dS_final,
+                                    float* grad_S0, const float* ws_W, const float* ws_P, const float* ws_G,
+                                    float* ws_dS, float* ws_dU, int T, int Hqk, int Hv, const int32_t* cu, int nseq,
+                                    float scale, cudaStream_t stream, unsigned* status);
 // Chunked prefill for shapes outside the tensor-core path (fp32 inputs, head dims 32 / 64, front end
 // included): the backward's WY kernel and forward chain plus an output kernel.
 size_t chunked_prefill_workspace_bytes(int B, int T, int Hv, int dk, int dv, int nseq, bool packed);
