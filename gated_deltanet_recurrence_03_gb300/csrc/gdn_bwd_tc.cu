@@ -436,12 +436,13 @@ bwd_state_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
 // Chunks in reverse, per (sequence, value head, 64-column slice); lam = dL/dS at a chunk's end (fp32,
 // in TMEM), dO the output gradient, P = scale D o Q K^T (from the WY kernel):
 //     dU  = b o (K lam) + P^T dO                       (to the workspace)
-//     lam <- gamma_C lam + (s gamma o Q)^T dO - W^T dU  (the chunk-end values go to the workspace)
+//     lam <- gamma_C lam + Q^T (s gamma o dO) - W^T dU  (the chunk-end values go to the workspace)
 // with the same three-part splits: K lam = K (lam_h + lam_m + lam_l) and P^T dO = sum_p P^T_p dO
-// (K, dO exact bf16 inputs), (s gamma o Q)^T dO = sum_p A_p dO, and W^T dU over the six part pairs
-// above 2^-22.  The 64-row products run as M = 128 MMAs whose rows 64-127 are not used.  (s gamma o
-// Q)^T, -W^T and P^T are written to TMEM by the epilogue warps as bf16 A operands (lane = the
-// product's row) while K lam runs.
+// (K, Q, dO exact bf16 inputs), Q^T (s gamma o dO) = sum_p Q^T (s gamma o dO)_p, and W^T dU over the
+// six part pairs above 2^-22.  The 64-row products run as M = 128 MMAs whose rows 64-127 are not
+// used.  Q^T, -W^T and P^T are written to TMEM by the epilogue warps as bf16 A operands (lane = the
+// product's row) while K lam runs; the (s gamma o dO) parts are built by the warps of rows 64-127,
+// which have no dU rows, into the lam parts' shared memory once K lam has read it.
 constexpr uint32_t A_LB = 0;          // lam parts: MN-major B, 128 dk rows x 64 columns (16 KB each)
 constexpr uint32_t A_UB = 49152;      // dU parts: MN-major B, 64 token rows x 64 columns (8 KB each)
 constexpr uint32_t A_KT = 73728;      // K tile (2 panels x 64 token rows); K lam reads 64 rows past it
@@ -455,8 +456,8 @@ constexpr uint32_t A_SST = 189440;    // a chunk-end lam, fp32, 4 swizzled panel
 constexpr uint32_t A_BAR = 222208;
 constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
 static_assert(A_SMEM <= 227 * 1024 && A_XU % 1024 == 0 && A_SST % 1024 == 0 && A_PST % 1024 == 0, "adjoint layout");
-// TMEM: lam 0-63, K lam 64-127, P^T dO 128-191, (s gamma o Q)^T parts 192-287, -W^T parts 288-383,
-// P^T parts 384-479 (32 columns a part: 64 K values).
+// TMEM: lam 0-63, K lam 64-127, P^T dO 128-191, Q^T 192-223, -W^T parts 288-383, P^T parts 384-479
+// (32 columns a part: 64 K values).
 constexpr uint32_t J_L = 0, J_D = 64, J_E = 128, J_AQ = 192, J_AW = 288, J_AP = 384;
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -545,24 +546,19 @@ bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
     const uint64_t dLB = smem_desc(sb + A_LB, 1024, 1024), dUB = smem_desc(sb + A_UB, 1024, 1024),
                    dKT = smem_desc(sb + A_KT, 16, 1024), dOT = smem_desc(sb + A_OT, 1024, 1024);
 
-    // (s gamma o Q)^T, -W^T (rows = dk R, tokens 32 half .. + 31) and P^T (rows R < 64) of the staged chunk
-    // with n tokens: the tiles' rows past a sequence's end hold the next sequence's q, so s gamma is
-    // zero there (W and P rows are zero there by construction)
-    auto put_a = [&](int n) {
+    // Q^T (exact), -W^T (rows = dk R, tokens 32 half .. + 31) and P^T (rows R < 64) of the staged chunk
+    auto put_a = [&]() {
         uint32_t ph[16], pm[16], pl[16];
         const uint32_t jq = (uint32_t)((R & 63) >> 3), oq = (uint32_t)(R & 7) * 2;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {   // (s gamma_t q_t)[R], tokens t, t + 1
+        for (int e = 0; e < 16; ++e) {   // q_t[R], tokens t, t + 1
             const uint32_t ta = (uint32_t)(32 * half + 2 * e), tb = ta + 1;
             const uint8_t* qp = sm + A_QT + (R >> 6) * 8192;
-            const float qa = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(qp + ta * 128 + ((jq ^ (ta & 7)) << 4) + oq) << 16);
-            const float qb = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(qp + tb * 128 + ((jq ^ (tb & 7)) << 4) + oq) << 16);
-            const float fa = (int)ta < n ? scale * __expf(sG[ta]) : 0.f, fb = (int)tb < n ? scale * __expf(sG[tb]) : 0.f;
-            split3(fa * qa, fb * qb, ph[e], pm[e], pl[e]);
+            const uint32_t qa = *reinterpret_cast<const uint16_t*>(qp + ta * 128 + ((jq ^ (ta & 7)) << 4) + oq);
+            const uint32_t qb = *reinterpret_cast<const uint16_t*>(qp + tb * 128 + ((jq ^ (tb & 7)) << 4) + oq);
+            ph[e] = qa | (qb << 16);
         }
         tmem_st16(tl + J_AQ + 16 * half, ph);
-        tmem_st16(tl + J_AQ + 32 + 16 * half, pm);
-        tmem_st16(tl + J_AQ + 64 + 16 * half, pl);
         const uint32_t jw = (uint32_t)((R & 31) >> 2), ow = (uint32_t)(R & 3) * 4;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {   // -W[t][R]
@@ -645,7 +641,6 @@ bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
                 __syncwarp();
                 nb_sync(2, kThreads);   // the A operands of this chunk are in TMEM; the staging was read
                 if (lane == 0) {   // P^T dO, then lam += (s gamma o Q)^T dO
-                    if (c > 0) load_st(c - 1);
                     wait_par(bar_o0 + 8 * par, (uint32_t)((j >> 1) & 1));
                     tc_fence_after();
                     const uint64_t od = dOT + ((par * 8192u) >> 4);
@@ -656,11 +651,17 @@ bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
                             mma_bf16_ta(tmem + J_E, tmem + J_AP + 32 * p + 8 * ks, od + ((ks * 2048) >> 4),
                                         idesc_bf16(128, 64, 0, 1), (p > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar_du);
+                    if (c > 0) load_st(c - 1);
+                }
+                __syncwarp();
+                nb_sync(6, 160);   // the (s gamma o dO) parts are in the lam parts' shared memory
+                if (lane == 0) {   // lam += Q^T (s gamma o dO)
+                    tc_fence_after();
 #pragma unroll 1
                     for (int p = 0; p < 3; ++p)
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma_bf16_ta(tmem + J_L, tmem + J_AQ + 32 * p + 8 * ks, od + ((ks * 2048) >> 4),
+                            mma_bf16_ta(tmem + J_L, tmem + J_AQ + 8 * ks, dLB + ((p * 8192 + ks * 2048) >> 4),
                                         idesc_bf16(128, 64, 0, 1), 1u);
                 }
                 __syncwarp();
@@ -680,11 +681,12 @@ bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
                 }
                 __syncwarp();
             } else {      // ---- the epilogue warps
-                float b = 0.f;
+                float b = 0.f;   // rows R < 64: b_R; rows 64-127: s gamma of token R - 64 (0 past the sequence's end)
                 const int n = (int)min((long long)kC, t1 - (t0 + c * kC));   // tokens of this chunk
                 waits_ok &= wait_par(bar_st, par);   // this chunk's Q, W, P, G
-                put_a(n);
+                put_a();
                 if (R < 64) b = __expf(sG[kC - 1] - sG[R]);
+                else b = (R - 64) < n ? scale * __expf(sG[R - 64]) : 0.f;
                 tmem_wait_st();
                 tc_fence_before();
                 nb_arrive(2, kThreads);
@@ -712,8 +714,24 @@ bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
                         tma_store_2d(&tm_du, col0 + 32, (int)(wi(c) * kC), sb + A_XU + 8192);
                         bulk_commit();
                     }
-                } else if (warp == 6 && lane == 0) {   // the previous lam store has read its staging
-                    bulk_wait_read();
+                } else {   // rows 64-127: (s gamma o dO) of token R - 64 as three parts (K lam has read LB)
+                    const uint8_t* od = sm + A_OT + par * 8192;
+                    const int t = R - 64;
+                    uint32_t x[32];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(od + swz((uint32_t)t, (uint32_t)((cb >> 3) + q)));
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            x[8 * q + 2 * e] = __float_as_uint(b * __uint_as_float(w4[e] << 16));
+                            x[8 * q + 2 * e + 1] = __float_as_uint(b * __uint_as_float(w4[e] & 0xffff0000u));
+                        }
+                    }
+                    store_parts(sm + A_LB, 8192, t, cb >> 3, x);
+                    fence_proxy_async_smem();
+                    nb_arrive(6, 160);
+                    if (warp == 6 && lane == 0) bulk_wait_read();   // the previous lam store has read its staging
                 }
                 tc_fence_before();
                 nb_arrive(3, kThreads);
