@@ -413,7 +413,7 @@ def run_gpu(args):
     dSf = 0.1 * torch.randn(w.B, w.Hv, w.dk, w.dv, device=dev)
     ws_b = torch.empty(gdn.backward_workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv), dtype=torch.uint8, device=dev)
     bwd_steps = 3
-    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(bwd_steps)]
+    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(bwd_steps)]   # around its 4 kernels
 
     def bwd_step(events=None):
         return gdn.gdn_recurrent_bwd(xb["q"], xb["k"], xb["v"], xb["g"], xb["beta"], S0, dout, dSf, workspace=ws_b,
@@ -437,6 +437,8 @@ def run_gpu(args):
     bwd_flop = 20.0 * tokens * w.Hv * w.dk * w.dv   # one forward (4 dk dv) + the adjoint (16 dk dv) per token/head
     bwd_tf = bwd_flop / (bwd_ms * 1e9)
     alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12      # fp32 FMA lanes x 2 flop x max SM clock
+    bwd_kernels = {name: round(statistics.mean(r[i].elapsed_time(r[i + 1]) for r in ev_b), 4)
+                   for i, name in enumerate(("bwd_wy", "bwd_state_fwd", "bwd_state_adj", "bwd_local"))}
     del xb, dout, ws_b
 
     # ---- decode: 512 consecutive steps, state resident, one CUDA graph per pass
@@ -599,14 +601,21 @@ def run_gpu(args):
                                     "algorithmic_bytes": gate_bytes}},
         "backward": {"workload": "prefill_gqa_8k backward: gradients w.r.t. q, k, v, g, beta, S0 from dout and "
                                  "dS_final through the chunked form (64-token chunks: WY factors, forward and "
-                                 "adjoint chunk chains, chunk-local gradients; fp32 accuracy, the products on tf32 "
-                                 "tensor cores with split operands)",
+                                 "adjoint chunk chains, chunk-local gradients; fp32 accuracy: the chains on tcgen05 "
+                                 "bf16 MMAs with three-part operand splits, the chunk-local kernel on split-tf32 "
+                                 "mma.sync)",
                      "value": round(world * tokens / (bwd_ms / 1e3), 1), "unit": "tokens/s",
                      "ms_per_step": round(bwd_ms, 4), "steps": bwd_steps, "gpu_launches": 4 * bwd_steps,
-                     "roofline": {"bound": "alu", "achieved": round(bwd_tf, 2), "peak": round(alu_peak, 1),
-                                  "unit": "TFLOP/s", "frac": round(bwd_tf / alu_peak, 4),
-                                  "peak_source": "fp32 FMA lanes x 2 x 2070 MHz (unit counts): the fp32 work's own "
-                                                 "peak; the products run as split tf32 MMAs"}},
+                     "kernels_ms": bwd_kernels,
+                     "roofline": {"bound": "tensor", "achieved": round(bwd_tf, 2),
+                                  "peak": round(peaks["bf16_tflops"] / 3, 1), "unit": "TFLOP/s",
+                                  "frac": round(bwd_tf / (peaks["bf16_tflops"] / 3), 4),
+                                  "peak_source": "measured bf16 burst / 3: an fp32-accurate product from bf16 tensor "
+                                                 "MMAs takes three part products when one operand is an exact bf16 "
+                                                 "input (six when neither is)"},
+                     "roofline_alu": {"bound": "alu", "achieved": round(bwd_tf, 2), "peak": round(alu_peak, 1),
+                                      "unit": "TFLOP/s", "frac": round(bwd_tf / alu_peak, 4),
+                                      "peak_source": "fp32 FMA lanes x 2 x 2070 MHz (unit counts)"}},
         "decode": {"workload": "decode_256x512: 256 sequences x 32 V heads (16 QK heads), d=128, 512 steps, "
                                "fp32 state 512 MiB resident, one CUDA graph per 512-step pass",
                    "value": round(world / (dec_ms / 1e3), 1), "unit": "steps/s",

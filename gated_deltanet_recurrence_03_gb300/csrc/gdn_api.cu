@@ -458,9 +458,10 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
     a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq; a.workspace = o.workspace;
     a.stream = static_cast<cudaStream_t>(o.stream);
     a.status = status;
+    a.events = o.events;
+    a.num_events = o.num_events;
     record(o, 0, a.stream);
-    const cudaError_t err = launch_backward(a);
-    record(o, 1, a.stream);
+    const cudaError_t err = launch_backward(a);   // records events[1..4] after its kernels
     if (err != cudaSuccess) return cuda_fail(err, "backward launch");
     return GDN_OK;
 }

@@ -1304,6 +1304,9 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     const TT* dout = static_cast<const TT*>(a.dout);
     constexpr int NSL = DV / slice_width<DV>();
     cudaError_t e;
+    const auto mark = [&](int i) {
+        if (a.events && i < a.num_events && a.events[i]) cudaEventRecord(static_cast<cudaEvent_t>(a.events[i]), a.stream);
+    };
     // 16-byte vector loads of the inputs need 16-byte aligned bases (row strides are multiples of 16 bytes)
     const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     const bool vec = al16(a.q) && al16(a.k) && al16(a.v) && al16(a.dout);
@@ -1321,6 +1324,7 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
         q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec, nullptr, nullptr, false);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark(1);
     // the forward chain: on the tcgen05 tensor cores for bf16 inputs with dk = dv = 128 (16-byte aligned k)
     e = cudaErrorNotSupported;
     if constexpr (sizeof(TT) == 2 && DK == 128 && DV == 128)
@@ -1332,6 +1336,7 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     else if (e != cudaSuccess)
         return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark(2);
     // the adjoint chain: on the tcgen05 tensor cores for bf16 inputs with dk = dv = 128 (16-byte aligned q, k, dout)
     e = cudaErrorNotSupported;
     if constexpr (sizeof(TT) == 2 && DK == 128 && DV == 128)
@@ -1343,10 +1348,13 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     else if (e != cudaSuccess)
         return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark(3);
     bwd_local_kernel<TT, DK, DV><<<chunk_grid, kLoThreads, S4::BYTES, a.stream>>>(
         q, k, v, beta, dout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk, a.Hv,
         a.cu_seqlens, a.num_seqs, a.scale, vec);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark(4);
+    return cudaSuccess;
 }
 
 template <typename TT, int DK>

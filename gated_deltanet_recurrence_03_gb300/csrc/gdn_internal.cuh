@@ -108,6 +108,8 @@ struct BackwardArgs {
     void* workspace;
     cudaStream_t stream;
     unsigned* status;           // device status word (bounded waits)
+    void** events;              // optional: events[i] recorded after kernel i (1..4)
+    int num_events;
 };
 
 // Workspace of the backward pass: per (chunk slot, value head) fp32 arrays T, P (C x C), W (C x dk),

@@ -253,8 +253,10 @@ gdn_status_t gdn_causal_conv1d_step_qkv(const void* x, long long x_stride, const
  * of the loop (64-token chunks): the workspace (256-byte aligned, gdn_recurrent_bwd_workspace_size
  * bytes) holds per (chunk, value head) the chunk's UT inverse, decay-masked Q K^T, W, U, decay
  * prefix sums, the state at the chunk start and its adjoint, and dU, all fp32; GDN_ERR_WORKSPACE if
- * missing or too small.  Asynchronous on opts->stream; events[0] before and events[1] after the
- * four kernels.
+ * missing or too small.  For bf16 inputs with dk = dv = 128 and 16-byte aligned q, k and grad_out the
+ * two chunk chains run on the tcgen05 tensor cores (fp32 accuracy through three-part bf16 operand
+ * splits).  Asynchronous on opts->stream; events[0] before the four kernels and events[i] after
+ * kernel i (1: WY factors, 2: forward chain, 3: adjoint chain, 4: chunk-local gradients).
  */
 size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts);
 gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
