@@ -599,7 +599,8 @@ constexpr uint32_t C_KT = 114688;       // 3 stages x 16 KB (K tile: 2 panels x 
 constexpr uint32_t C_SB = 163840;       // bf16 state slice: 1 panel x 128 dk rows
 constexpr uint32_t C_UB = 180224;       // bf16 b*U: 1 panel x 64 token rows
 constexpr uint32_t C_VEC = 188416;      // 3 stages x 512 B
-constexpr uint32_t C_BAR = 189952;
+constexpr uint32_t C_OST = 190464;      // output rows of a full chunk, 3 buffers x 64 token rows x 64 bf16 (swizzled)
+constexpr uint32_t C_BAR = C_OST + 3 * 8192;
 constexpr uint32_t C_SMEM = C_BAR + 128 + 1024;
 constexpr int kKStages = 3;
 // Operands arrive in two rings freed at different times: A1 and the V slice (2 stages, consumed by
@@ -628,7 +629,7 @@ __device__ __forceinline__ void named_barrier_arrive(int id, int threads) {
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                const uint8_t* __restrict__ ws_a1, const float* __restrict__ ws_vec, const float* __restrict__ S0,
+                const __grid_constant__ CUtensorMap tm_out, const uint8_t* __restrict__ ws_a1, const float* __restrict__ ws_vec, const float* __restrict__ S0,
                 bf16* __restrict__ out, float* __restrict__ S_final, const int32_t* __restrict__ cu, int nseq,
                 int T_len, int Hqk, int Hv, int num_slots, unsigned* status) {
     extern __shared__ uint8_t smem_raw[];
@@ -833,7 +834,25 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                         named_barrier_arrive(1, kChainThreads);   // its gamma-scaled state rows are in TMEM
                     }
                     const int r = R - 64;
-                    if (r < n) {
+                    if (n == kC) {   // a full chunk: rows into swizzled staging, one TMA store by warp 7
+                        uint8_t* ost = sm + C_OST + (uint32_t)(c % 3) * 8192;
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const uint32_t* src = a + 8 * c8;
+                            *reinterpret_cast<uint4*>(ost + swz((uint32_t)r, (uint32_t)((cb >> 3) + c8))) =
+                                make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                           pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                           pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                                           pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
+                        }
+                        fence_proxy_async_smem();
+                        named_barrier_sync(3, 128);   // the four output warps' rows are staged
+                        if (warp == 7 && lane == 0) {
+                            tma_store_3d(&tm_out, 64 * z, h, (int)tc0, sb + C_OST + (uint32_t)(c % 3) * 8192);
+                            bulk_commit();
+                            bulk_wait_read_1();   // the store of two chunks back has read its buffer
+                        }
+                    } else if (r < n) {   // the last chunk of a sequence: only its own rows
                         uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z + cb);
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
@@ -880,6 +899,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             __syncthreads();
         }
+        if (warp == 7 && lane == 0) bulk_wait_all();   // the output stores are complete
         if (tid == kIssuer && *abort_flag) {
             // A bounded wait gave up: before the TMEM and shared memory are released, every MMA has
             // completed and no copy is still landing (consumers may have skipped chunks whose loads were
@@ -989,10 +1009,11 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
     const long long ttot = total_tokens(a.B, a.T, packed);
     const long long slots = num_slots(ttot, a.num_seqs);
     if (ttot > INT32_MAX || slots > INT32_MAX) return cudaErrorInvalidValue;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if ((e = make_map(&tq, a.q, ttot, a.Hqk)) != cudaSuccess) return e;
     if ((e = make_map(&tk, a.k, ttot, a.Hqk)) != cudaSuccess) return e;
     if ((e = make_map(&tv, a.v, ttot, a.Hv)) != cudaSuccess) return e;
+    if ((e = make_map(&to, a.out, ttot, a.Hv)) != cudaSuccess) return e;
     uint8_t* ws_a1 = static_cast<uint8_t*>(a.workspace);
     float* ws_vec = reinterpret_cast<float*>(ws_a1 + (size_t)slots * a.Hv * kA1Bytes);
     const int T_len = a.T;
@@ -1006,7 +1027,7 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     record_event(events, num_events, 1, a.stream);
     tc_chain_kernel<<<(unsigned)((long long)a.num_seqs * a.Hv * kSlices), kChainThreads, C_SMEM, a.stream>>>(
-        tk, tv, ws_a1, ws_vec, a.S0, static_cast<bf16*>(a.out), a.S_final, a.cu_seqlens, a.num_seqs, T_len, a.Hqk,
+        tk, tv, to, ws_a1, ws_vec, a.S0, static_cast<bf16*>(a.out), a.S_final, a.cu_seqlens, a.num_seqs, T_len, a.Hqk,
         a.Hv, (int)slots, a.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     record_event(events, num_events, 2, a.stream);

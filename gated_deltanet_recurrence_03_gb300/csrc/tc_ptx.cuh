@@ -114,6 +114,15 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int c0, int c1, u
                  : "memory");
 }
 
+// 3-D tiled TMA store from shared memory, tracked by the bulk-group of the issuing thread.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int c0, int c1, int c2, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+// Wait until at most one committed bulk store still reads its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // Contiguous global -> shared bulk copy (both 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
