@@ -723,6 +723,47 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             mma_bf16(d1, a1 + ((ks * 32) >> 4), vt + ((ks * 2048) >> 4), idesc_bf16(128, 64, 0, 1), ks > 0);
     };
 
+    // Output rows R - 64 of chunk cc (warps of lane quarters 2-3) from its D1 buffer: a full chunk
+    // goes through swizzled staging and one TMA store by warp 7; the last chunk of a sequence stores
+    // its own rows (the next sequence's rows follow them).
+    auto write_out = [&](long long cc) {
+        const long long tcc = s0 + cc * kC;
+        const int nn = (int)min((long long)kC, s1 - tcc), r = R - 64;
+        uint32_t a[32];
+        tmem_ld32(tl + 64 + 64 * (uint32_t)(cc & 1) + cb, a);
+        tmem_wait_ld();
+        tc_fence_before();
+        if (nn == kC) {
+            uint8_t* ost = sm + C_OST + (uint32_t)(cc % 3) * 8192;
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                const uint32_t* src = a + 8 * c8;
+                *reinterpret_cast<uint4*>(ost + swz((uint32_t)r, (uint32_t)((cb >> 3) + c8))) =
+                    make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                               pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                               pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                               pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
+            }
+            fence_proxy_async_smem();
+            named_barrier_sync(3, 128);   // the four output warps' rows are staged
+            if (warp == 7 && lane == 0) {
+                tma_store_3d(&tm_out, 64 * z, h, (int)tcc, sb + C_OST + (uint32_t)(cc % 3) * 8192);
+                bulk_commit();
+                bulk_wait_read_1();   // the store of two chunks back has read its buffer
+            }
+        } else if (r < nn) {
+            uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tcc + r) * Hv + h) * kD + 64 * z + cb);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                const uint32_t* src = a + 8 * c8;
+                dst[c8] = make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                     pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                     pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                                     pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
+            }
+        }
+    };
+
     if (nch == 0) {   // empty sequence: the final state is the initial state
         if (S_final && epi) {
             for (int e = 0; e < 32; e += 4) {
@@ -802,13 +843,16 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     tmem_wait_st();
                     tc_fence_before();
                 }
+                // the previous chunk's output rows, while this chunk's D1 runs: its D1 buffer is next
+                // overwritten by the V part issued after this step's state-update barrier
+                if (quarter >= 2 && c > 0) write_out(c - 1);
                 waits_ok &= wait_k(c);
                 waits_ok &= mbar_wait_bounded(bar_mma1, par, abort_flag, status, kStatusTimeout, kWaitLimitNs);
                 tc_fence_after();
-                uint32_t a[32];
-                tmem_ld32(tl + 64 + 64 * st + cb, a);
-                tmem_wait_ld();
                 if (quarter < 2) {   // U row R scaled by b_r = exp(G_C - G_r) -> B operand of the state update
+                    uint32_t a[32];
+                    tmem_ld32(tl + 64 + 64 * st + cb, a);
+                    tmem_wait_ld();
                     const float br = reinterpret_cast<const float*>(sm + C_VEC + kst * 512)[R];
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
@@ -821,8 +865,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     fence_proxy_async_smem();
                     tc_fence_before();
                     named_barrier_arrive(1, kChainThreads);
-                } else {             // output row of token R - 64
-                    tc_fence_before();
+                } else {             // the output warps (their rows are written a step later)
                     if (warp == kProducer / 32) {   // waits for the barrier, then issues the loads
                         named_barrier_sync(1, kChainThreads);
                         if (lane == 0) {
@@ -832,36 +875,6 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                         }
                     } else {
                         named_barrier_arrive(1, kChainThreads);   // its gamma-scaled state rows are in TMEM
-                    }
-                    const int r = R - 64;
-                    if (n == kC) {   // a full chunk: rows into swizzled staging, one TMA store by warp 7
-                        uint8_t* ost = sm + C_OST + (uint32_t)(c % 3) * 8192;
-#pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            const uint32_t* src = a + 8 * c8;
-                            *reinterpret_cast<uint4*>(ost + swz((uint32_t)r, (uint32_t)((cb >> 3) + c8))) =
-                                make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
-                                           pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
-                                           pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
-                                           pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
-                        }
-                        fence_proxy_async_smem();
-                        named_barrier_sync(3, 128);   // the four output warps' rows are staged
-                        if (warp == 7 && lane == 0) {
-                            tma_store_3d(&tm_out, 64 * z, h, (int)tc0, sb + C_OST + (uint32_t)(c % 3) * 8192);
-                            bulk_commit();
-                            bulk_wait_read_1();   // the store of two chunks back has read its buffer
-                        }
-                    } else if (r < n) {   // the last chunk of a sequence: only its own rows
-                        uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)(tc0 + r) * Hv + h) * kD + 64 * z + cb);
-#pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            const uint32_t* src = a + 8 * c8;
-                            dst[c8] = make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
-                                                 pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
-                                                 pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
-                                                 pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
-                        }
                     }
                 }
                 float gnext = 1.f;
@@ -899,6 +912,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
             __syncthreads();
         }
+        if (epi && quarter >= 2) write_out(nch - 1);   // the last chunk's output rows
         if (warp == 7 && lane == 0) bulk_wait_all();   // the output stores are complete
         if (tid == kIssuer && *abort_flag) {
             // A bounded wait gave up: before the TMEM and shared memory are released, every MMA has
