@@ -71,36 +71,36 @@ __device__ bool slot_lookup(const int32_t* cu, int nseq, int T_len, int slot, in
 }
 
 // ------------------------------------------------------------------ parallel intra-chunk kernel
-// Two CTAs fit on one SM (shared memory <= 110 KB, 256 TMEM columns each), so one CTA's MMAs and
-// memory traffic overlap the other's CUDA-core phases.
+// One CTA per (chunk, value-head pair): two 4-warp groups, group 0 for value head A and group 1 for
+// value head B, sharing the chunk's K / Q tiles and their Gram matrices.  Two CTAs fit on one SM
+// (shared memory <= 110 KB, 256 TMEM columns, <= 128 registers a thread), so sixteen warps per SM
+// hide each other's latencies in the CUDA-core phases.
 //
 // Shared memory (byte offsets from a 1024-aligned base)
 constexpr uint32_t P_KQ = 0;            // 2 panels (dk 0-63, 64-127) x [K rows 0-63 | Q rows 64-127]
 constexpr uint32_t P_TOP = 32768;       // [-W_h | Tb_h] for both heads: 3 panels x 128 rows (B operand)
-constexpr uint32_t P_X = P_TOP;         // blocked-solve scratch X [2][16][56] fp32 (panel 0, before -W)
+constexpr uint32_t P_Y = P_TOP;         // UT-solve scratch [2 heads][2 block rows][16][kYStride] fp32 (panel 0, before -W)
 constexpr uint32_t P_HANDOFF = P_TOP + 16384;   // P_0 rows, bf16 [64][64] (panel 1, before -W)
 constexpr uint32_t P_LC = 81920;        // L_h then T_h: 10 lower blocks of 16 x 16 fp32 per head, row stride 20
 constexpr uint32_t P_LBLK = 16 * 20;    // floats per block
 constexpr uint32_t P_SMALL = P_LC + 2 * 10 * P_LBLK * 4;   // G, beta, beta*gamma, a, c: [2][64] each; 1/|k|, 1/|q|: [64]
 constexpr uint32_t P_BAR = P_SMALL + 5 * 2 * 64 * 4 + 2 * 64 * 4;
 constexpr uint32_t P_SMEM = P_BAR + 64 + 1024;  // + alignment slack
-constexpr int kPrepThreads = 128;
+constexpr int kPrepThreads = 256;
 // TMEM columns: Gram D 0-63; T diag(beta gamma) (A operand) 0-31 after the Gram is read;
 // [W_0; W_1] D 64-191; blockdiag(P_0, P_1) (A operand) 192-255; [-P W | P Tb] D 0-191.
 constexpr uint32_t T_GRAM = 0, T_TD = 0, T_W = 64, T_AP = 192, T_PW = 0;
+// Scratch of the UT solve: block rows 2 and 3 of T, columns 0-31 (16 rows each), stride 40 floats
+// (conflict-free B-fragment loads, 16-byte aligned rows).
+constexpr int kYStride = 40;
+constexpr uint32_t kYHeadFloats = 2 * 16 * kYStride;
+static_assert(2 * kYHeadFloats * 4 <= 16384, "the solve scratch lives in TOP panel 0");
 // Output panel i = 3 h + p of [Q'_h | P_h Tb_h] (8 KB each, after their inputs are consumed)
 __device__ __forceinline__ uint32_t bot_panel(int i) { return i < 4 ? P_KQ + 8192u * i : P_LC + 8192u * (i - 4); }
 static_assert(P_LC + 2 * 8192 <= P_SMALL, "two output panels must fit in the L/T region");
 static_assert(P_SMEM <= 113 * 1024, "two CTAs per SM");
 
 __device__ __forceinline__ int lblk(int I, int J) { return I * (I + 1) / 2 + J; }   // J <= I
-
-// In-place inverse of I + L_h for both heads (two warps per head): 16 x 16 diagonal blocks by forward
-// substitution in fp32 (one column per thread), then block row i from X_ij = sum_k L_ik T_kj and
-// T_ij = -T_ii X_ij.  The off-diagonal block products run on the warp-level tensor-core MMA
-// (m16n8k8, tf32 inputs rounded to nearest, fp32 accumulation): tcgen05 has no 16-row shape, and
-// T is rounded to bf16 right after (as the W and T diag(beta) operands), far coarser than tf32.
-constexpr int kXStride = 56;   // X scratch row stride (floats): conflict-free B-fragment loads
 
 __device__ __forceinline__ uint32_t tf32_rna(float x) {
     uint32_t r;
@@ -115,78 +115,118 @@ __device__ __forceinline__ void mma_tf32_m16n8k8(float (&d)[4], const uint32_t (
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// acc (a 16 x 16 tile as two 16 x 8 accumulator fragments) += A B, A and B 16 x 16 fp32 in shared
-// memory with row strides as and bs.  Fragment g = lane / 4, t = lane % 4: A holds (g, t), (g + 8, t),
-// (g, t + 4), (g + 8, t + 4) of each 8-wide k slice; B holds (k = t, n = g), (k = t + 4, n = g);
-// the accumulator holds (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
-__device__ __forceinline__ void tile_mma_16(float (&acc)[2][4], const float* A, int as, const float* B, int bs,
-                                            int lane) {
+// acc (a 16 x 8 accumulator fragment) += A B, A 16 x 16 and B 16 x 8 fp32 in shared memory with row
+// strides as and bs (B points at its first column).  Fragment g = lane / 4, t = lane % 4: A holds
+// (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4) of each 8-wide k slice; B holds (k = t, n = g),
+// (k = t + 4, n = g); the accumulator holds (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
+__device__ __forceinline__ void tile_mma_16x8(float (&acc)[4], const float* A, int as, const float* B, int bs,
+                                              int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int kk = 0; kk < 16; kk += 8) {
         const uint32_t a[4] = {tf32_rna(A[g * as + kk + t]), tf32_rna(A[(g + 8) * as + kk + t]),
                                tf32_rna(A[g * as + kk + t + 4]), tf32_rna(A[(g + 8) * as + kk + t + 4])};
-#pragma unroll
-        for (int nh = 0; nh < 2; ++nh) {
-            const uint32_t b[2] = {tf32_rna(B[(kk + t) * bs + 8 * nh + g]), tf32_rna(B[(kk + t + 4) * bs + 8 * nh + g])};
-            mma_tf32_m16n8k8(acc[nh], a, b);
-        }
+        const uint32_t b[2] = {tf32_rna(B[(kk + t) * bs + g]), tf32_rna(B[(kk + t + 4) * bs + g])};
+        mma_tf32_m16n8k8(acc, a, b);
     }
 }
 
-// Store sign * acc into a 16 x 16 fp32 tile with row stride ds.
-__device__ __forceinline__ void tile_store_16(float* D, int ds, const float (&acc)[2][4], float sign, int lane) {
+// Store sign * acc (a 16 x 8 fragment) at D (its first column), row stride ds.
+__device__ __forceinline__ void tile_store_16x8(float* D, int ds, const float (&acc)[4], float sign, int lane) {
     const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int nh = 0; nh < 2; ++nh) {
-        *reinterpret_cast<float2*>(D + g * ds + 8 * nh + 2 * t) = make_float2(sign * acc[nh][0], sign * acc[nh][1]);
-        *reinterpret_cast<float2*>(D + (g + 8) * ds + 8 * nh + 2 * t) = make_float2(sign * acc[nh][2], sign * acc[nh][3]);
-    }
+    *reinterpret_cast<float2*>(D + g * ds + 2 * t) = make_float2(sign * acc[0], sign * acc[1]);
+    *reinterpret_cast<float2*>(D + (g + 8) * ds + 2 * t) = make_float2(sign * acc[2], sign * acc[3]);
 }
 
-__device__ __forceinline__ void blocked_unit_lower_inverse(float* sLC, float* sX, int tid) {
-    const int h = tid >> 6, t = tid & 63, hw = t >> 5, lane = t & 31;
-    float* L = sLC + h * 10 * P_LBLK;
-    float* X = sX + h * 16 * kXStride;
-    {
-        const int I = t >> 4, j = t & 15;
-        float* D = L + lblk(I, I) * P_LBLK;
-        float tc[16];
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+__device__ __forceinline__ void named_barrier_arrive(int id, int threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// T = (I + L)^-1 of one head in place, by one 4-warp group (gw = warp in the group, bar = the group's
+// named barrier).  With 16 x 16 blocks L_IJ (I, J = 0..3) and the 2 x 2 split into 32 x 32 halves:
+//   (a) the diagonal blocks T_II by forward substitution in fp32 (warps 0, 1: one column a thread);
+//   (b) inside each half, T_10 = -T_11 L_10 T_00 (warp 0) and T_32 = -T_33 L_32 T_22 (warp 1) -- each
+//       warp uses only the blocks it has just inverted, so only warp-level syncs are needed;
+//   (c) the off-diagonal half T[2:4, 0:2] = -T[2:4, 2:4] Y with Y = L[2:4, 0:2] T[0:2, 0:2], one warp
+//       per (block column j, 8-column half): Y_2j, Y_3j, then T_2j = -T_22 Y_2j and
+//       T_3j = -(T_32 Y_2j + T_33 Y_3j), kept in the scratch Yh (block rows 2, 3; columns 0-31).
+// The off-diagonal block products run on the warp-level tensor-core MMA (m16n8k8, tf32 inputs rounded
+// to nearest, fp32 accumulation): tcgen05 has no 16-row shape, and T is rounded to bf16 right after (as
+// the W and T diag(beta) operands), far coarser than tf32.
+__device__ __forceinline__ void unit_lower_inverse(float* L, float* Yh, int gw, int lane, int bar) {
+    if (gw < 2) {
+        {   // (a) column j of the diagonal block I: this warp holds blocks 2 gw and 2 gw + 1
+            const int I = 2 * gw + (lane >> 4), j = lane & 15;
+            float* D = L + lblk(I, I) * P_LBLK;
+            float tc[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float* Dr = D + r * 20;
-            float a0 = 0.f, a1 = 0.f;
+            for (int r = 0; r < 16; ++r) {
+                const float* Dr = D + r * 20;
+                float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int s = 0; s + 1 < r; s += 2) {
-                a0 = fmaf(Dr[s], tc[s], a0);
-                a1 = fmaf(Dr[s + 1], tc[s + 1], a1);
+                for (int s = 0; s + 1 < r; s += 2) {
+                    a0 = fmaf(Dr[s], tc[s], a0);
+                    a1 = fmaf(Dr[s + 1], tc[s + 1], a1);
+                }
+                if (r & 1) a0 = fmaf(Dr[r - 1], tc[r - 1], a0);
+                tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -(a0 + a1));
             }
-            if (r & 1) a0 = fmaf(Dr[r - 1], tc[r - 1], a0);
-            tc[r] = (r < j) ? 0.f : (r == j ? 1.f : -(a0 + a1));
-        }
-        __syncthreads();
+            __syncwarp();   // every lane of the block has read D
 #pragma unroll
-        for (int r = 0; r < 16; ++r) D[r * 20 + j] = tc[r];
-        __syncthreads();
+            for (int r = 0; r < 16; ++r) D[r * 20 + j] = tc[r];
+            __syncwarp();
+        }
+        {   // (b) X = L_{i+1,i} T_ii into the scratch, then T_{i+1,i} = -T_{i+1,i+1} X over L_{i+1,i}
+            const int i = 2 * gw;
+            float* X = Yh + (uint32_t)gw * 16 * kYStride;   // block row 2 + gw of the scratch, free until (c)
+            float* Lo = L + lblk(i + 1, i) * P_LBLK;
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                tile_mma_16x8(acc, Lo, 20, L + lblk(i, i) * P_LBLK + 8 * nh, 20, lane);
+                tile_store_16x8(X + 8 * nh, kYStride, acc, 1.f, lane);
+            }
+            __syncwarp();   // X complete; every lane has finished reading L_{i+1,i}
+            const float* Td = L + lblk(i + 1, i + 1) * P_LBLK;
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                tile_mma_16x8(acc, Td, 20, X + 8 * nh, kYStride, lane);
+                tile_store_16x8(Lo + 8 * nh, 20, acc, -1.f, lane);
+            }
+        }
     }
-#pragma unroll
-    for (int i = 1; i < 4; ++i) {
-        // blocks of block row i handled by this warp: warp 0 takes jb = 0, warp 1 the rest
-        const int jb_lo = hw == 0 ? 0 : 1, jb_hi = hw == 0 ? 1 : i;
-        for (int jb = jb_lo; jb < jb_hi && jb < i; ++jb) {
-            float acc[2][4] = {};
-            for (int k = jb; k < i; ++k)
-                tile_mma_16(acc, L + lblk(i, k) * P_LBLK, 20, L + lblk(k, jb) * P_LBLK, 20, lane);
-            tile_store_16(X + 16 * jb, kXStride, acc, 1.f, lane);
+    // T_00, T_10, T_11, T_22, T_32, T_33 are final (literal barrier ids keep the kernel at two barriers)
+    if (bar == 1)
+        named_barrier_sync(1, 128);
+    else
+        named_barrier_sync(2, 128);
+    {   // (c) block column j, columns 8 nh .. 8 nh + 7 of it
+        const int j = gw >> 1, nh = gw & 1;
+        float* Y2 = Yh + 16 * j + 8 * nh;
+        float* Y3 = Yh + 16 * kYStride + 16 * j + 8 * nh;
+        const float* T1j = L + lblk(1, j) * P_LBLK + 8 * nh;   // T_10 or T_11
+        float y2[4] = {0.f, 0.f, 0.f, 0.f}, y3[4] = {0.f, 0.f, 0.f, 0.f};
+        if (j == 0) {   // T_01 = 0
+            const float* T00 = L + lblk(0, 0) * P_LBLK + 8 * nh;
+            tile_mma_16x8(y2, L + lblk(2, 0) * P_LBLK, 20, T00, 20, lane);
+            tile_mma_16x8(y3, L + lblk(3, 0) * P_LBLK, 20, T00, 20, lane);
         }
-        __syncthreads();
-        const float* Tii = L + lblk(i, i) * P_LBLK;
-        for (int jb = jb_lo; jb < jb_hi && jb < i; ++jb) {
-            float acc[2][4] = {};
-            tile_mma_16(acc, Tii, 20, X + 16 * jb, kXStride, lane);
-            tile_store_16(L + lblk(i, jb) * P_LBLK, 20, acc, -1.f, lane);
-        }
-        __syncthreads();
+        tile_mma_16x8(y2, L + lblk(2, 1) * P_LBLK, 20, T1j, 20, lane);
+        tile_mma_16x8(y3, L + lblk(3, 1) * P_LBLK, 20, T1j, 20, lane);
+        tile_store_16x8(Y2, kYStride, y2, 1.f, lane);
+        tile_store_16x8(Y3, kYStride, y3, 1.f, lane);
+        __syncwarp();   // this warp's columns of Y_2j and Y_3j are complete
+        float t2[4] = {0.f, 0.f, 0.f, 0.f}, t3[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma_16x8(t2, L + lblk(2, 2) * P_LBLK, 20, Y2, kYStride, lane);
+        tile_mma_16x8(t3, L + lblk(3, 2) * P_LBLK, 20, Y2, kYStride, lane);
+        tile_mma_16x8(t3, L + lblk(3, 3) * P_LBLK, 20, Y3, kYStride, lane);
+        __syncwarp();   // every lane has read its Y columns
+        tile_store_16x8(Y2, kYStride, t2, -1.f, lane);
+        tile_store_16x8(Y3, kYStride, t3, -1.f, lane);
     }
 }
 
@@ -215,7 +255,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     const int slot = blockIdx.x, pair = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int R = tid;                                   // TMEM lane = accumulator row of this thread
+    const int hg = warp >> 2;                            // the group's value head: 0 = hA, 1 = hB
+    const int R = tid & 127;                             // TMEM lane = accumulator row of this thread
     int seq;
     long long t0;
     int n;
@@ -225,6 +266,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int G = Hv / Hqk, ppq = (G + 1) / 2;
     const int hk = pair / ppq, jp = pair % ppq;
     const int hA = hk * G + 2 * jp, hB = min(hA + 1, hk * G + G - 1);
+    const int hOwn = hg == 0 ? hA : hB;
     if (tid == 0) {   // barriers first, then the K / Q tile loads, so their latency overlaps the set-up
         *abort_flag = 0;
         mbar_init(bar_tma, 1);
@@ -240,16 +282,17 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
     if (warp < 2) {
         const int r0 = 2 * lane, r1 = 2 * lane + 1;
+        const int hw = warp == 0 ? hA : hB;
         if (r0 < n) {
-            g0 = __bfloat162float(g[(size_t)(t0 + r0) * Hv + (warp == 0 ? hA : hB)]);
-            b0 = __bfloat162float(beta[(size_t)(t0 + r0) * Hv + (warp == 0 ? hA : hB)]);
+            g0 = __bfloat162float(g[(size_t)(t0 + r0) * Hv + hw]);
+            b0 = __bfloat162float(beta[(size_t)(t0 + r0) * Hv + hw]);
         }
         if (r1 < n) {
-            g1 = __bfloat162float(g[(size_t)(t0 + r1) * Hv + (warp == 0 ? hA : hB)]);
-            b1 = __bfloat162float(beta[(size_t)(t0 + r1) * Hv + (warp == 0 ? hA : hB)]);
+            g1 = __bfloat162float(g[(size_t)(t0 + r1) * Hv + hw]);
+            b1 = __bfloat162float(beta[(size_t)(t0 + r1) * Hv + hw]);
         }
         if (A_log) {   // raw projections a, b: form the gates (padded tokens keep g = beta = 0)
-            const float al = A_log[warp == 0 ? hA : hB], db = dt_bias[warp == 0 ? hA : hB];
+            const float al = A_log[hw], db = dt_bias[hw];
             if (r0 < n) gates_from_raw(g0, b0, al, db, g0, b0);
             if (r1 < n) gates_from_raw(g1, b1, al, db, g1, b1);
         }
@@ -262,7 +305,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();   // also publishes the barrier initialisation to every thread
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);   // this warp's TMEM lane quarter
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);   // this warp's TMEM lane quarter
 
     if (warp < 2) {   // G = inclusive scan of g over the chunk
         const int hh = warp;
@@ -281,7 +324,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0) sFactor[hh] = (G0 - Gl) < 80.f;
     }
     __syncthreads();
-    {
+    if (tid < 128) {
         const int hh = tid >> 6, r = tid & 63;
         const float Gr = sG[hh * 64 + r], Gl = sG[hh * 64 + 63], G0 = sG[hh * 64];
         sBG[hh * 64 + r] = sBeta[hh * 64 + r] * __expf(Gr);
@@ -311,22 +354,21 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
     {
+        // row R of the Gram; group hg builds the rows of its own head
         uint32_t a[64];
         tmem_ld32(tl + T_GRAM, *reinterpret_cast<uint32_t(*)[32]>(a));
         tmem_ld32(tl + T_GRAM + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
         tmem_wait_ld();
         if (normalize) {   // l2 normalisation of q and k folded into per-row scalars (eps 1e-6)
-            if (warp < 2) {
+            if (R < 64) {
                 float kk = 0.f;   // k_r . k_r is the diagonal of K K^T
 #pragma unroll
                 for (int s = 0; s < 64; ++s) kk = (s == R) ? __uint_as_float(a[s]) : kk;
                 const float rk = rsqrtf(kk + 1e-6f);
-                sRK[R] = rk;
-                for (int hh = 0; hh < 2; ++hh) {
-                    ws_vec[((size_t)slot * Hv + (hh == 0 ? hA : hB)) * kVecFloats + R] = __expf(sG[hh * 64 + 63] - sG[hh * 64 + R]) * rk;
-                    sBG[hh * 64 + R] *= rk;
-                }
-            } else {
+                if (hg == 0) sRK[R] = rk;
+                ws_vec[((size_t)slot * Hv + hOwn) * kVecFloats + R] = __expf(sG[hg * 64 + 63] - sG[hg * 64 + R]) * rk;
+                sBG[hg * 64 + R] *= rk;
+            } else if (hg == 0) {
                 const int r = R - 64;
                 float qq = 0.f;
 #pragma unroll
@@ -344,120 +386,121 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         __syncthreads();
         if (normalize) {   // fold 1/|k_s| into the column factor exp(G_0 - G_s) once
-            sC[tid] *= sRK[tid & 63];
+            if (tid < 128) sC[tid] *= sRK[tid & 63];
             __syncthreads();
         }
-        if (warp < 2) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s (s < r), lower blocks
+        const float* Gh = sG + hg * 64;
+        const float* ch = sC + hg * 64;
+        const bool fac = sFactor[hg] != 0;
+        if (R < 64) {   // row r of K K^T -> L_h[r][s] = beta_r exp(G_r - G_s) k_r.k_s (s < r), lower blocks
             const int r = R, I = r >> 4, rr = r & 15;
-            for (int hh = 0; hh < 2; ++hh) {
-                const float* Gh = sG + hh * 64;
-                const float br = sBeta[hh * 64 + r] * sRK[r], ar = sA[hh * 64 + r], Gr = Gh[r];
-                const float* ch = sC + hh * 64;
-                const bool fac = sFactor[hh] != 0;
-                float* Lh = sLC + hh * 10 * P_LBLK;
-                const float rowc = br * ar;   // factorised decay: beta_r exp(G_r - G_0) / |k_r|
-                for (int J = 0; J <= I; ++J) {
-                    float* dst = Lh + lblk(I, J) * P_LBLK + rr * 20;
+            const float br = sBeta[hg * 64 + r] * sRK[r], ar = sA[hg * 64 + r], Gr = Gh[r];
+            float* Lh = sLC + hg * 10 * P_LBLK;
+            const float rowc = br * ar;   // factorised decay: beta_r exp(G_r - G_0) / |k_r|
+            for (int J = 0; J <= I; ++J) {
+                float* dst = Lh + lblk(I, J) * P_LBLK + rr * 20;
 #pragma unroll
-                    for (int s4 = 0; s4 < 4; ++s4) {
-                        float o[4];
-                        if (fac) {   // uniform per head: exp(G_0 - G_s) / |k_s| is the column factor ch[s]
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    float o[4];
+                    if (fac) {   // uniform per head: exp(G_0 - G_s) / |k_s| is the column factor ch[s]
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int s = 16 * J + 4 * s4 + e;
-                                o[e] = (s < r) ? rowc * __uint_as_float(a[s]) * ch[s] : 0.f;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int s = 16 * J + 4 * s4 + e;
-                                o[e] = (s < r) ? br * __expf(Gr - Gh[s]) * __uint_as_float(a[s]) * sRK[s] : 0.f;
-                            }
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 16 * J + 4 * s4 + e;
+                            o[e] = (s < r) ? rowc * __uint_as_float(a[s]) * ch[s] : 0.f;
                         }
-                        *reinterpret_cast<float4*>(dst + 4 * s4) = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 16 * J + 4 * s4 + e;
+                            o[e] = (s < r) ? br * __expf(Gr - Gh[s]) * __uint_as_float(a[s]) * sRK[s] : 0.f;
+                        }
                     }
+                    *reinterpret_cast<float4*>(dst + 4 * s4) = make_float4(o[0], o[1], o[2], o[3]);
                 }
             }
-        } else {          // row r of Q K^T -> P_h[r][s] = scale exp(G_r - G_s) q_r.k_s (s <= r)
+        } else {        // row r of Q K^T -> P_h[r][s] = scale exp(G_r - G_s) q_r.k_s (s <= r)
             const int r = R - 64;
             const float sq = scale * sRQ[r];
-            for (int hh = 0; hh < 2; ++hh) {
-                const float* Gh = sG + hh * 64;
-                const float ar = sA[hh * 64 + r], Gr = Gh[r];
-                const float* ch = sC + hh * 64;
-                const bool fac = sFactor[hh] != 0;
-                uint32_t w[32];
-                if (fac) {   // uniform per head
-                    const float rowc = sq * ar;
+            const float ar = sA[hg * 64 + r], Gr = Gh[r];
+            uint32_t w[32];
+            if (fac) {   // uniform per head
+                const float rowc = sq * ar;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float pv[2];
+                for (int e = 0; e < 32; ++e) {
+                    float pv[2];
 #pragma unroll
-                        for (int f = 0; f < 2; ++f) {
-                            const int s = 2 * e + f;
-                            pv[f] = (s <= r) ? rowc * __uint_as_float(a[s]) * ch[s] : 0.f;
-                        }
-                        w[e] = pack_bf16(pv[0], pv[1]);
+                    for (int f = 0; f < 2; ++f) {
+                        const int s = 2 * e + f;
+                        pv[f] = (s <= r) ? rowc * __uint_as_float(a[s]) * ch[s] : 0.f;
                     }
-                } else {
+                    w[e] = pack_bf16(pv[0], pv[1]);
+                }
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float pv[2];
+                for (int e = 0; e < 32; ++e) {
+                    float pv[2];
 #pragma unroll
-                        for (int f = 0; f < 2; ++f) {
-                            const int s = 2 * e + f;
-                            pv[f] = (s <= r) ? sq * __expf(Gr - Gh[s]) * __uint_as_float(a[s]) * sRK[s] : 0.f;
-                        }
-                        w[e] = pack_bf16(pv[0], pv[1]);
+                    for (int f = 0; f < 2; ++f) {
+                        const int s = 2 * e + f;
+                        pv[f] = (s <= r) ? sq * __expf(Gr - Gh[s]) * __uint_as_float(a[s]) * sRK[s] : 0.f;
                     }
+                    w[e] = pack_bf16(pv[0], pv[1]);
                 }
-                if (hh == 1) {   // own lane: [0 | P_1 row]
-                    uint32_t z[32];
+            }
+            if (hg == 1) {   // own lane: [0 | P_1 row] (the zero half is written by group 0)
+                tmem_st32(tl + T_AP + 32, w);
+            } else {         // P_0 row r belongs to lane r: hand it over through shared memory
+                uint4* dst = reinterpret_cast<uint4*>(sm + P_HANDOFF + r * 128);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) z[e] = 0u;
-                    tmem_st32(tl + T_AP, z);
-                    tmem_st32(tl + T_AP + 32, w);
-                } else {         // P_0 row r belongs to lane r: hand it over through shared memory
-                    uint4* dst = reinterpret_cast<uint4*>(sm + P_HANDOFF + r * 128);
+                for (int c = 0; c < 8; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                }
+                for (int e = 0; e < 32; ++e) w[e] = 0u;
+                tmem_st32(tl + T_AP, w);
             }
         }
     }
     __syncthreads();
-    if (warp < 2) {   // lanes 0-63: [P_0 row | 0]
-        uint32_t w[32], z[32];
-        const uint4* src = reinterpret_cast<const uint4*>(sm + P_HANDOFF + R * 128);
+    if (R < 64) {   // lanes 0-63: [P_0 row | 0], the halves written by the two groups
+        uint32_t w[32];
+        if (hg == 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(sm + P_HANDOFF + R * 128);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint4 x = src[c];
-            w[4 * c] = x.x; w[4 * c + 1] = x.y; w[4 * c + 2] = x.z; w[4 * c + 3] = x.w;
+            for (int c = 0; c < 8; ++c) {
+                const uint4 x = src[c];
+                w[4 * c] = x.x; w[4 * c + 1] = x.y; w[4 * c + 2] = x.z; w[4 * c + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) w[e] = 0u;
         }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) z[e] = 0u;
-        tmem_st32(tl + T_AP, w);
-        tmem_st32(tl + T_AP + 32, z);
+        tmem_st32(tl + T_AP + 32 * hg, w);
     }
     tmem_wait_st();
     tc_fence_before();
     __syncthreads();
 
-    // ---- T_h = (I + L_h)^-1 in place; T_h diag(beta gamma) -> TMEM (A operand), T_h diag(beta) -> TOP panel 2
-    blocked_unit_lower_inverse(sLC, reinterpret_cast<float*>(sm + P_X), tid);
+    // ---- T_h = (I + L_h)^-1 in place (group hg, head hg); then T_h diag(beta gamma) -> TMEM (A
+    // operand) and T_h diag(beta) -> TOP panel 2, the two groups taking 32 columns each
+    unit_lower_inverse(sLC + hg * 10 * P_LBLK, reinterpret_cast<float*>(sm + P_Y) + hg * kYHeadFloats, warp & 3,
+                       lane, 1 + hg);
+    __syncthreads();
     {
         const int hh = R >> 6, r = R & 63, I = r >> 4, rr = r & 15;
         const float* Th = sLC + hh * 10 * P_LBLK;
+        const float* Yh = reinterpret_cast<const float*>(sm + P_Y) + hh * kYHeadFloats;
         const float* dg = sBG + hh * 64;
         const float* bt = sBeta + hh * 64;
-        uint32_t wd[32];
+        uint32_t wd[16];
 #pragma unroll
-        for (int J = 0; J < 4; ++J) {
+        for (int jj = 0; jj < 2; ++jj) {
+            const int J = 2 * hg + jj;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {   // 8 columns s = 16 J + 8 c ..
                 float tv[8];
                 if (J <= I) {
-                    const float* src = Th + lblk(I, J) * P_LBLK + rr * 20 + 8 * c;
+                    // blocks (2|3, 0|1) of T are in the scratch, the others in place of L
+                    const float* src = (I >= 2 && J <= 1) ? Yh + ((I - 2) * 16 + rr) * kYStride + 16 * J + 8 * c
+                                                          : Th + lblk(I, J) * P_LBLK + rr * 20 + 8 * c;
                     const float4 x0 = *reinterpret_cast<const float4*>(src), x1 = *reinterpret_cast<const float4*>(src + 4);
                     tv[0] = x0.x; tv[1] = x0.y; tv[2] = x0.z; tv[3] = x0.w;
                     tv[4] = x1.x; tv[5] = x1.y; tv[6] = x1.z; tv[7] = x1.w;
@@ -475,13 +518,13 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 uint32_t wb[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    wd[(s0 >> 1) + e] = pack_bf16(tv[2 * e] * dgv[2 * e], tv[2 * e + 1] * dgv[2 * e + 1]);
+                    wd[8 * jj + 4 * c + e] = pack_bf16(tv[2 * e] * dgv[2 * e], tv[2 * e + 1] * dgv[2 * e + 1]);
                     wb[e] = pack_bf16(tv[2 * e] * btv[2 * e], tv[2 * e + 1] * btv[2 * e + 1]);
                 }
                 *reinterpret_cast<uint4*>(sm + P_TOP + 2 * 16384 + swz(R, s0 >> 3)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
             }
         }
-        tmem_st32(tl + T_TD, wd);
+        tmem_st16(tl + T_TD + 16 * hg, wd);
     }
     tmem_wait_st();
     fence_proxy_async_smem();
@@ -498,18 +541,21 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     mbar_wait_bounded(bar_mma, 1, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    for (int cb = 0; cb < 4; ++cb) {   // row R of [W_0; W_1] -> -W in TOP panels 0-1
-        uint32_t a[32];
-        tmem_ld32(tl + T_W + 32 * cb, a);
-        tmem_wait_ld();
-        uint8_t* pan = sm + P_TOP + (cb >> 1) * 16384;
+    {   // row R of [W_0; W_1] -> -W in TOP panel hg (columns 64 hg .. 64 hg + 63)
+        uint8_t* pan = sm + P_TOP + hg * 16384;
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+            uint32_t a[32];
+            tmem_ld32(tl + T_W + 64 * hg + 32 * cc, a);
+            tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t w[4];
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                w[e] = pack_bf16(-__uint_as_float(a[8 * c + 2 * e]), -__uint_as_float(a[8 * c + 2 * e + 1]));
-            *reinterpret_cast<uint4*>(pan + swz(R, (cb & 1) * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack_bf16(-__uint_as_float(a[8 * c + 2 * e]), -__uint_as_float(a[8 * c + 2 * e + 1]));
+                *reinterpret_cast<uint4*>(pan + swz(R, cc * 4 + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
     }
     fence_proxy_async_smem();
@@ -531,38 +577,39 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         bulk_commit();
     }
-    // this thread's query row, read before the K/Q panels are reused for the outputs
+    // this thread's query row, the 64 features its group needs (columns 32 cb .. of the panels 0, 1 of
+    // the output rows, cb = hg, hg + 2), read before the K/Q panels are reused for the outputs
     const int hh = R >> 6, r = R & 63;
-    uint4 qrow[16];
+    uint4 qrow[8];
 #pragma unroll
-    for (int c = 0; c < 16; ++c)
-        qrow[c] = *reinterpret_cast<const uint4*>(sm + P_KQ + (c >> 3) * 16384 + 8192 + swz(r, c & 7));
+    for (int c = 0; c < 8; ++c)
+        qrow[c] = *reinterpret_cast<const uint4*>(sm + P_KQ + (c >> 2) * 16384 + 8192 + swz(r, 4 * hg + (c & 3)));
     mbar_wait_bounded(bar_mma, 0, abort_flag, status, kStatusTimeout, kWaitLimitNs);
     tc_fence_after();
-    __syncthreads();   // every thread holds its q row: the K/Q panels are free
+    __syncthreads();   // every thread holds its q features: the K/Q panels are free
     {
         const float qs = scale * __expf(sG[hh * 64 + r]) * sRQ[r];   // scale * gamma_r / |q_r|
-        // panel by panel, so that the bulk stores of the first panels drain while the later ones are built
+        // panel by panel, so that the bulk stores of the first panels drain while the later ones are built;
+        // column block cb = 2 p + hg of the 192 columns is this group's half of panel p
         for (int p = 0; p < 3; ++p) {
-            for (int cb = 2 * p; cb < 2 * p + 2; ++cb) {
-                uint32_t a[32];
-                tmem_ld32(tl + T_PW + 32 * cb, a);
-                tmem_wait_ld();
-                uint8_t* pan = sm + bot_panel(3 * hh + p);
+            const int cb = 2 * p + hg;
+            uint32_t a[32];
+            tmem_ld32(tl + T_PW + 32 * cb, a);
+            tmem_wait_ld();
+            uint8_t* pan = sm + bot_panel(3 * hh + p);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t chunk = (cb & 1) * 4 + c;
-                    float x[8];
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t chunk = hg * 4 + c;
+                float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(a[8 * c + e]);
-                    if (cb < 4) {   // Q' = scale gamma_r q_r - P W
-                        const bf16* qe = reinterpret_cast<const bf16*>(&qrow[p * 8 + chunk]);
+                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(a[8 * c + e]);
+                if (p < 2) {   // Q' = scale gamma_r q_r - P W
+                    const bf16* qe = reinterpret_cast<const bf16*>(&qrow[p * 4 + c]);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = fmaf(qs, __bfloat162float(qe[e]), x[e]);
-                    }
-                    *reinterpret_cast<uint4*>(pan + swz(r, chunk)) =
-                        make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+                    for (int e = 0; e < 8; ++e) x[e] = fmaf(qs, __bfloat162float(qe[e]), x[e]);
                 }
+                *reinterpret_cast<uint4*>(pan + swz(r, chunk)) =
+                    make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
             }
             fence_proxy_async_smem();
             if (p == 2) tc_fence_before();   // every TMEM read of this CTA precedes the deallocation
@@ -620,12 +667,6 @@ constexpr int kIssuer = kEpilogueThreads;
 constexpr int kProducer = 192;
 // TMEM columns: state S 0-63; D1 of even chunks 64-127, of odd chunks 128-191.
 
-__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-__device__ __forceinline__ void named_barrier_arrive(int id, int threads) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 
 __global__ void __launch_bounds__(kChainThreads, 1)
 tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
