@@ -41,6 +41,8 @@ class GdnOpts(ctypes.Structure):
         ("z", ctypes.c_void_p),
         ("norm_weight", ctypes.c_void_p),
         ("norm_eps", ctypes.c_float),
+        ("grad_A_log", ctypes.c_void_p),
+        ("grad_dt_bias", ctypes.c_void_p),
     ]
 
 

@@ -348,10 +348,14 @@ def gdn_recurrent_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torc
                       S0: Optional[torch.Tensor], grad_out: torch.Tensor, grad_S_final: Optional[torch.Tensor] = None,
                       *, scale: float = 1.0, cu_seqlens: Optional[torch.Tensor] = None,
                       workspace: Optional[torch.Tensor] = None, want_grad_S0: bool = True,
-                      stream: Optional[torch.cuda.Stream] = None, events: Optional[Sequence[int]] = None):
+                      stream: Optional[torch.cuda.Stream] = None, events: Optional[Sequence[int]] = None,
+                      normalize_qk: bool = False, raw_gates=None):
     """Gradients of a loss on (out, S_final) of gdn_chunk_fwd with respect to q, k, v, g, beta, S0.
     Inputs as for gdn_chunk_fwd; grad_out like v; grad_S_final fp32 like S_final or None.  Returns fp32
-    (grad_q, grad_k, grad_v, grad_g, grad_beta, grad_S0 or None)."""
+    (grad_q, grad_k, grad_v, grad_g, grad_beta, grad_S0 or None).  With normalize_qk and / or
+    raw_gates=(A_log, dt_bias) (g and beta then hold the raw projections a and b) the gradients are
+    those of the forward with the same front end, with respect to its raw inputs, and two more tensors
+    are returned with raw_gates: grad_A_log, grad_dt_bias (fp32 [Hv])."""
     lib = L.load()
     if q.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D [B, T, H, d]")
@@ -379,11 +383,20 @@ def gdn_recurrent_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torc
     gv = torch.empty((B, T, Hv, dv), **f32)
     gg, gb = torch.empty((B, T, Hv), **f32), torch.empty((B, T, Hv), **f32)
     gS0 = torch.empty((nseq, Hv, dk, dv), **f32) if want_grad_S0 else None
+    gA = gdt = None
     with torch.cuda.device(dev):
-        o, keep = _opts(lib, dt, scale, 64, False, stream, dev, events)
+        o, keep = _opts(lib, dt, scale, 64, normalize_qk, stream, dev, events)
         if cu_seqlens is not None:
             o.cu_seqlens = cu_seqlens.data_ptr()
             o.num_seqs = nseq
+        if raw_gates is not None:
+            A_log, dt_bias = raw_gates
+            _need("A_log", A_log, torch.float32, dev, (Hv,))
+            _need("dt_bias", dt_bias, torch.float32, dev, (Hv,))
+            gA, gdt = torch.empty((Hv,), **f32), torch.empty((Hv,), **f32)
+            o.flags |= L.GDN_RAW_GATES
+            o.A_log, o.dt_bias = A_log.data_ptr(), dt_bias.data_ptr()
+            o.grad_A_log, o.grad_dt_bias = gA.data_ptr(), gdt.data_ptr()
         need = int(lib.gdn_recurrent_bwd_workspace_size(B, T, Hqk, Hv, dk, dv, ctypes.byref(o)))
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
@@ -394,4 +407,6 @@ def gdn_recurrent_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torc
                                    B, T, Hqk, Hv, dk, dv, ctypes.byref(o))
         del keep
         L.check(lib, st)
+    if raw_gates is not None:
+        return gq, gk, gv, gg, gb, gS0, gA, gdt
     return gq, gk, gv, gg, gb, gS0

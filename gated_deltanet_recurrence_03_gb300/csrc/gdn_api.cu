@@ -412,7 +412,10 @@ size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, i
     const bool packed = o.cu_seqlens != nullptr;
     const int nseq = packed ? o.num_seqs : B;
     if (nseq <= 0) return 0;
-    return backward_layout(B, T, Hv, dk, dv, nseq, packed, true).total;
+    size_t bytes = backward_layout(B, T, Hv, dk, dv, nseq, packed, true).total;
+    if (o.flags & (GDN_NORMALIZE_QK | GDN_RAW_GATES))
+        bytes = ((bytes + 255) & ~(size_t)255) + frontend_backward_bytes(B, T, Hqk, Hv, dk, dv, packed);
+    return bytes;
 }
 
 gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, const void* g, const void* beta,
@@ -424,7 +427,11 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
     if (B < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "B=%d T=%d must be >= 0", B, T);
     gdn_status_t st = check_common(Hqk, Hv, dk, dv, o);
     if (st != GDN_OK) return st;
-    if (o.flags) return fail(GDN_ERR_UNSUPPORTED, "the backward pass takes no option flags (0x%x given)", o.flags);
+    if (o.flags & ~(GDN_NORMALIZE_QK | GDN_RAW_GATES))
+        return fail(GDN_ERR_UNSUPPORTED, "the backward pass has no output gate (flags 0x%x given)", o.flags);
+    if ((o.flags & GDN_RAW_GATES) && (!o.A_log || !o.dt_bias))
+        return fail(GDN_ERR_INVALID_ARG, "GDN_RAW_GATES needs opts->A_log and opts->dt_bias");
+    const bool front_end = (o.flags & (GDN_NORMALIZE_QK | GDN_RAW_GATES)) != 0;
     const bool packed = o.cu_seqlens != nullptr;
     if (packed && (B != 1 || o.num_seqs < 1))
         return fail(GDN_ERR_INVALID_ARG, "cu_seqlens needs B == 1 and num_seqs >= 1 (B=%d num_seqs=%d)", B, o.num_seqs);
@@ -437,11 +444,14 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
     const void* in_ptrs[] = {q, k, v, g, beta, grad_out};
     for (const void* p : in_ptrs)
         if (p && !aligned_to(p, e)) return fail(GDN_ERR_INVALID_ARG, "input %p not aligned to its element size", p);
-    const void* f_ptrs[] = {S0, grad_S_final, grad_q, grad_k, grad_v, grad_g, grad_beta, grad_S0, o.cu_seqlens};
+    const void* f_ptrs[] = {S0, grad_S_final, grad_q, grad_k, grad_v, grad_g, grad_beta, grad_S0, o.cu_seqlens,
+                            o.A_log, o.dt_bias, o.grad_A_log, o.grad_dt_bias};
     for (const void* p : f_ptrs)
         if (p && !aligned_to(p, 4)) return fail(GDN_ERR_INVALID_ARG, "pointer %p not 4-byte aligned", p);
     if (nseq == 0) return GDN_OK;
-    const size_t need = backward_layout(B, T, Hv, dk, dv, nseq, packed, true).total;
+    const size_t core = backward_layout(B, T, Hv, dk, dv, nseq, packed, true).total;
+    const size_t need =
+        front_end ? ((core + 255) & ~(size_t)255) + frontend_backward_bytes(B, T, Hqk, Hv, dk, dv, packed) : core;
     if (!o.workspace || o.workspace_bytes < need)
         return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     o.workspace ? o.workspace_bytes : (size_t)0);
@@ -461,7 +471,10 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
     a.events = o.events;
     a.num_events = o.num_events;
     record(o, 0, a.stream);
-    const cudaError_t err = launch_backward(a);   // records events[1..4] after its kernels
+    // records events[1..4] after the four kernels of the recurrence's backward
+    const cudaError_t err = front_end ? launch_frontend_backward(a, o.flags, o.A_log, o.dt_bias, o.grad_A_log,
+                                                                 o.grad_dt_bias, core)
+                                      : launch_backward(a);
     if (err != cudaSuccess) return cuda_fail(err, "backward launch");
     return GDN_OK;
 }

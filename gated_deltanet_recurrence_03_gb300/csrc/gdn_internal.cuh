@@ -121,6 +121,13 @@ struct BwdLayout {
 };
 BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed, bool adjoint);
 cudaError_t launch_backward(const BackwardArgs& a);
+// The backward through the fused front end (GDN_NORMALIZE_QK, GDN_RAW_GATES): fp32 copies of the front
+// end's outputs after the first core_bytes of a.workspace (frontend_backward_bytes more), the backward
+// on them, then the gradients mapped back to the raw q, k, a, b in place; dA_log and d dt_bias into
+// grad_A_log / grad_dt_bias when not NULL.
+size_t frontend_backward_bytes(int B, int T, int Hqk, int Hv, int dk, int dv, bool packed);
+cudaError_t launch_frontend_backward(const BackwardArgs& a, unsigned flags, const float* A_log, const float* dt_bias,
+                                     float* grad_A_log, float* grad_dt_bias, size_t core_bytes);
 // The backward's forward chunk chain on the tcgen05 tensor cores, for bf16 k with dk = dv = 128: the
 // chunk-start states into ws_S, U = U~ - W S over ws_U (U~ read from there), the last state into
 // S_final (or not).  cudaErrorNotSupported when k is not 16-byte aligned (the caller then runs the

@@ -95,6 +95,8 @@ typedef struct gdn_opts {
     const void* z;              /* output gate input, same shape and dtype as out (GDN_OUTPUT_GATE), DEVICE */
     const float* norm_weight;   /* [dv] (GDN_OUTPUT_GATE), DEVICE */
     float norm_eps;             /* GDN_OUTPUT_GATE epsilon; default 1e-6 */
+    float* grad_A_log;          /* gdn_recurrent_bwd with GDN_RAW_GATES: [Hv] dL/dA_log out, DEVICE; NULL = not computed */
+    float* grad_dt_bias;        /* gdn_recurrent_bwd with GDN_RAW_GATES: [Hv] dL/ddt_bias out, DEVICE; NULL = not computed */
 } gdn_opts_t;
 
 /* Fill *opts with the defaults listed above. */
@@ -248,8 +250,15 @@ gdn_status_t gdn_causal_conv1d_step_qkv(const void* x, long long x_stride, const
  *   grad_q, grad_k [B, T, Hqk, dk] float (a query/key head sums over the value heads that read it)
  *   grad_v         [B, T, Hv, dv] float;  grad_g, grad_beta [B, T, Hv] float
  *   grad_S0        [nseq, Hv, dk, dv] float, or NULL (not written)
- * Gradients are always fp32.  Pointers need only element alignment.  opts->flags must be 0 (the
- * fused front end and output gate have no backward here).  It is computed through the chunked form
+ * Gradients are always fp32.  Pointers need only element alignment.
+ * opts->flags may hold GDN_NORMALIZE_QK and GDN_RAW_GATES (GDN_OUTPUT_GATE: GDN_ERR_UNSUPPORTED): the
+ * gradients are then those of the forward with the same flags, with respect to its raw inputs -- the
+ * unnormalised q, k (dx = r dx_n - r^3 (x . dx_n) x, r = (x . x + 1e-6)^-1/2) and the raw projections
+ * a, b passed as g, beta (da = dg (-exp(A_log)) sigmoid(a + dt_bias), db = dbeta beta (1 - beta)) --
+ * and, when opts->grad_A_log / grad_dt_bias are not NULL, [Hv] fp32 sums over all tokens of dg g and
+ * of da (overwritten, deterministic order).  With either flag the inputs' front-end outputs are formed
+ * in fp32 in the workspace (gdn_recurrent_bwd_workspace_size grows accordingly) and the recurrence's
+ * backward runs on them in fp32 (the split-tf32 kernels).  It is computed through the chunked form
  * of the loop (64-token chunks): the workspace (256-byte aligned, gdn_recurrent_bwd_workspace_size
  * bytes) holds per (chunk, value head) the chunk's UT inverse, decay-masked Q K^T, W, U, decay
  * prefix sums, the state at the chunk start and its adjoint, and dU, all fp32; GDN_ERR_WORKSPACE if

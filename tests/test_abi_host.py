@@ -208,8 +208,11 @@ def bwd(lib, B=1, T=8, Hqk=1, Hv=1, dk=32, dv=32, ptrs=None, **kw):
     (dict(B=-1), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(Hqk=2, Hv=3), pkg_lib.GDN_ERR_INVALID_ARG),
     (dict(dk=48), pkg_lib.GDN_ERR_UNSUPPORTED),
-    (dict(flags=pkg_lib.GDN_NORMALIZE_QK), pkg_lib.GDN_ERR_UNSUPPORTED),     # no backward for the front end
-    (dict(flags=pkg_lib.GDN_OUTPUT_GATE, z=FAKE, norm_weight=FAKE), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(flags=pkg_lib.GDN_NORMALIZE_QK), pkg_lib.GDN_ERR_WORKSPACE),       # front end: validated up to the workspace
+    (dict(flags=pkg_lib.GDN_RAW_GATES), pkg_lib.GDN_ERR_INVALID_ARG),        # raw gates need A_log and dt_bias
+    (dict(flags=pkg_lib.GDN_RAW_GATES, A_log=FAKE, dt_bias=FAKE, grad_A_log=FAKE + 2), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(flags=pkg_lib.GDN_RAW_GATES, A_log=FAKE, dt_bias=FAKE), pkg_lib.GDN_ERR_WORKSPACE),
+    (dict(flags=pkg_lib.GDN_OUTPUT_GATE, z=FAKE, norm_weight=FAKE), pkg_lib.GDN_ERR_UNSUPPORTED),   # no gate backward
     (dict(ptrs=[FAKE] * 8 + [0] + [FAKE] * 5), pkg_lib.GDN_ERR_INVALID_ARG),   # grad_q missing
     (dict(ptrs=[FAKE + 1] + [FAKE] * 13), pkg_lib.GDN_ERR_INVALID_ARG),        # q not element aligned
     (dict(ptrs=[FAKE] * 9 + [FAKE + 2] + [FAKE] * 4), pkg_lib.GDN_ERR_INVALID_ARG),   # grad_k not 4-byte aligned
@@ -238,6 +241,12 @@ def test_backward_workspace_size_is_pure_host(lib):
     need = 258 * 32 * per * 4
     assert need <= n <= need + 8 * 256
     assert lib.gdn_recurrent_bwd_workspace_size(1, 8, 1, 1, 48, 32, opts(lib)) == 0
+    # with the front end: fp32 copies of the normalised q, k (tokens x Hqk x dk each), v and dout
+    # (tokens x Hv x dv each) and the two gates (tokens x Hv each) follow the recurrence's workspace
+    extra = (2 * 16384 * 16 * 128 + 2 * 16384 * 32 * 128 + 2 * 16384 * 32) * 4
+    for flags in (pkg_lib.GDN_NORMALIZE_QK, pkg_lib.GDN_RAW_GATES, pkg_lib.GDN_NORMALIZE_QK | pkg_lib.GDN_RAW_GATES):
+        m = lib.gdn_recurrent_bwd_workspace_size(2, 8192, 16, 32, 128, 128, opts(lib, flags=flags))
+        assert n + extra <= m <= n + extra + 7 * 256
 
 
 @pytest.mark.parametrize("B,T,Hqk,Hv,dk,dv,dtype,nseq", [
