@@ -4,6 +4,7 @@ Only the tests use this module.  "Transformer by Hand, ch. 7", listing "qwen/del
 GatedDeltaNet.forward, and the parts table below it:
     beta = sigmoid(in_proj_b(x))                                   write strength in (0, 1)
     g    = -exp(A_log) * softplus(in_proj_a(x) + dt_bias)          log decay, always <= 0
+Their backward (silu_grad, gated_rmsnorm_backward) is the chain rule written out.
 Here a = in_proj_a(x) and b = in_proj_b(x) are given directly (the projections need trained
 weights and are out of scope).  softplus and sigmoid are numpy's logaddexp and an overflow-safe
 logistic.
@@ -45,3 +46,28 @@ def gated_rmsnorm(o, z, weight, eps):
     o = np.asarray(o, dtype=np.float64)
     ms = np.mean(o * o, axis=-1, keepdims=True)
     return o / np.sqrt(ms + eps) * np.asarray(weight, dtype=np.float64) * silu(z)
+
+
+def silu_grad(z):
+    """d silu / dz = sigmoid(z) (1 + z (1 - sigmoid(z)))."""
+    z = np.asarray(z, dtype=np.float64)
+    s = sigmoid(z)
+    return s * (1.0 + z * (1.0 - s))
+
+
+def gated_rmsnorm_backward(o, z, weight, eps, dy):
+    """Gradients of a loss through y = gated_rmsnorm(o, z, weight, eps) given dy = dL/dy: with
+    inv = (mean(o^2) + eps)^-1/2, o_hat = o inv and gy = dy weight silu(z),
+        do = inv (gy - o_hat mean(gy o_hat)),   dz = dy o_hat weight silu'(z),
+        dweight = sum over all rows of dy o_hat silu(z).
+    Returns (do, dz, dweight) in fp64."""
+    o, z, dy = (np.asarray(x, dtype=np.float64) for x in (o, z, dy))
+    weight = np.asarray(weight, dtype=np.float64)
+    inv = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    oh = o * inv
+    s = silu(z)
+    gy = dy * weight * s
+    do = inv * (gy - oh * np.mean(gy * oh, axis=-1, keepdims=True))
+    dz = dy * oh * weight * silu_grad(z)
+    dw = np.sum((dy * oh * s).reshape(-1, o.shape[-1]), axis=0)
+    return do, dz, dw

@@ -64,3 +64,66 @@ def test_packed_equals_separate():
         yi, ci = conv.causal_conv1d(x[:, cu[i]:cu[i + 1]], w, cache[i:i + 1])
         np.testing.assert_array_equal(y[:, cu[i]:cu[i + 1]], yi)
         np.testing.assert_array_equal(co[i], ci[0])
+
+
+def _fd(f, x, eps=1e-6):
+    x = np.array(x, dtype=np.float64)
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        hi, lo = x.copy(), x.copy()
+        hi[i] += eps
+        lo[i] -= eps
+        g[i] = (f(hi) - f(lo)) / (2 * eps)
+    return g
+
+
+@pytest.mark.parametrize("case", [
+    dict(B=2, T=6, C=3, K=4, cache=True, dco=True),
+    dict(B=1, T=9, C=2, K=3, cache=False, dco=False),
+    dict(lens=(4, 0, 1, 5), C=3, K=4, cache=True, dco=True),   # packed; an empty and a short sequence
+    dict(B=1, T=5, C=2, K=1, cache=False, dco=False),           # no history: a pointwise map
+])
+def test_conv_backward_matches_finite_differences(case):
+    rng = np.random.default_rng(9)
+    lens = case.get("lens")
+    B, T = (1, sum(lens)) if lens else (case["B"], case["T"])
+    C, K = case["C"], case["K"]
+    nseq = len(lens) if lens else B
+    cu = np.concatenate([[0], np.cumsum(lens)]) if lens else None
+    x = rng.normal(size=(B, T, C))
+    w = rng.normal(size=(C, K))
+    cache = rng.normal(size=(nseq, K - 1, C)) if case["cache"] else None
+    dy = rng.normal(size=(B, T, C))
+    dco = rng.normal(size=(nseq, K - 1, C)) if case["dco"] else None
+
+    def loss(xx=x, ww=w, cc=cache):
+        y, co = conv.causal_conv1d(xx, ww, cc, cu_seqlens=cu)
+        return float(np.sum(y * dy) + (np.sum(co * dco) if dco is not None else 0.0))
+
+    dx, dw, dc = conv.causal_conv1d_backward(x, w, dy, cache, cu_seqlens=cu, dcache_out=dco)
+    np.testing.assert_allclose(dx, _fd(lambda t: loss(xx=t), x), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dw, _fd(lambda t: loss(ww=t), w), rtol=1e-6, atol=1e-8)
+    if cache is not None:
+        np.testing.assert_allclose(dc, _fd(lambda t: loss(cc=t), cache), rtol=1e-6, atol=1e-8)
+
+
+def test_conv_backward_closed_form_single_tap():
+    """K = 1: y = silu(w x) per element, so dx = w silu'(w x) dy and dw_c = sum_t x silu'(w x) dy."""
+    from oracle.gates import silu_grad
+    rng = np.random.default_rng(10)
+    x, w, dy = rng.normal(size=(2, 7, 4)), rng.normal(size=(4, 1)), rng.normal(size=(2, 7, 4))
+    dx, dw, _ = conv.causal_conv1d_backward(x, w, dy)
+    u = x * w[:, 0]
+    np.testing.assert_allclose(dx, w[:, 0] * silu_grad(u) * dy, rtol=1e-13)
+    np.testing.assert_allclose(dw[:, 0], np.sum(x * silu_grad(u) * dy, axis=(0, 1)), rtol=1e-12)
+
+
+def test_conv_backward_pins_catch_a_reversed_window():
+    """Applying the taps in the wrong order (w[:, K-1-j]) is caught by the difference pin."""
+    rng = np.random.default_rng(11)
+    x, w, dy = rng.normal(size=(1, 6, 2)), rng.normal(size=(2, 4)), rng.normal(size=(1, 6, 2))
+    dx = conv.causal_conv1d_backward(x, w[:, ::-1], dy)[0]
+    fd = _fd(lambda t: float(np.sum(conv.causal_conv1d(t, w)[0] * dy)), x)
+    assert np.max(np.abs(dx - fd)) > 1e-2

@@ -51,3 +51,50 @@ def test_gated_rmsnorm_closed_forms():
     o = 0.01 * alt
     y = gates.gated_rmsnorm(o, np.full(dv, 50.0), np.ones(dv), 1e-4)
     np.testing.assert_allclose(np.sqrt(np.mean((y / gates.silu(50.0)) ** 2)), np.sqrt(1e-4 / (1e-4 + 1e-4)), rtol=1e-12)
+
+
+def _fd(f, x, eps=1e-6):
+    x = np.array(x, dtype=np.float64)
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        hi, lo = x.copy(), x.copy()
+        hi[i] += eps
+        lo[i] -= eps
+        g[i] = (f(hi) - f(lo)) / (2 * eps)
+    return g
+
+
+def test_silu_grad_matches_differences_and_closed_values():
+    z = np.linspace(-8, 8, 33)
+    # central differences of a sum of 33 terms (~30): cancellation error ~ 30 * 2^-52 / 1e-6 ~ 1e-8
+    np.testing.assert_allclose(gates.silu_grad(z), _fd(lambda t: np.sum(gates.silu(t)), z), rtol=1e-7, atol=3e-8)
+    assert gates.silu_grad(0.0) == 0.5   # sigmoid(0) (1 + 0)
+
+
+def test_gated_rmsnorm_backward_matches_finite_differences():
+    """All three gradients of a weighted sum of the gate's outputs, rows of 8 values, eps both tiny and
+    comparable to the mean square."""
+    rng = np.random.default_rng(3)
+    o, z, w = rng.normal(size=(5, 8)), rng.normal(size=(5, 8)), rng.normal(1.0, 0.2, size=8)
+    dy = rng.normal(size=(5, 8))
+    for eps in (1e-6, 0.3):
+        do, dz, dw = gates.gated_rmsnorm_backward(o, z, w, eps, dy)
+        loss = lambda oo=o, zz=z, ww=w: float(np.sum(gates.gated_rmsnorm(oo, zz, ww, eps) * dy))
+        np.testing.assert_allclose(do, _fd(lambda t: loss(oo=t), o), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(dz, _fd(lambda t: loss(zz=t), z), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(dw, _fd(lambda t: loss(ww=t), w), rtol=1e-6, atol=1e-8)
+
+
+def test_gated_rmsnorm_backward_is_scale_free_in_o():
+    """With eps = 0 the gate depends on the direction of each row only: do is orthogonal to o and
+    halves when o doubles; a planted slip (the projection term dropped) breaks both."""
+    rng = np.random.default_rng(4)
+    o, z, w, dy = rng.normal(size=(3, 16)), rng.normal(size=(3, 16)), rng.normal(size=16), rng.normal(size=(3, 16))
+    do = gates.gated_rmsnorm_backward(o, z, w, 0.0, dy)[0]
+    np.testing.assert_allclose(np.sum(do * o, axis=-1), 0.0, atol=1e-12)
+    np.testing.assert_allclose(gates.gated_rmsnorm_backward(2 * o, z, w, 0.0, dy)[0], do / 2, rtol=1e-12)
+    inv = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True))
+    slip = inv * dy * w * gates.silu(z)
+    assert np.max(np.abs(np.sum(slip * o, axis=-1))) > 1e-3
