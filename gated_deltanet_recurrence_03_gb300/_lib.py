@@ -20,7 +20,8 @@ EXPORTED = ("gdn_opts_init", "gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "g
             "gdn_check_device_status", "gdn_status_string", "gdn_last_error", "gdn_version",
             "gdn_chunk_fwd_noalloc", "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_step",
             "gdn_recurrent_bwd", "gdn_recurrent_bwd_workspace_size", "gdn_causal_conv1d_fwd_qkv",
-            "gdn_causal_conv1d_step_qkv")
+            "gdn_causal_conv1d_step_qkv", "gdn_output_gate_fwd", "gdn_output_gate_bwd",
+            "gdn_output_gate_bwd_workspace_size", "gdn_causal_conv1d_bwd", "gdn_causal_conv1d_bwd_workspace_size")
 
 
 class GdnOpts(ctypes.Structure):
@@ -83,6 +84,16 @@ def load(path: str = LIB_PATH):
     lib.gdn_causal_conv1d_step_qkv.restype = i
     lib.gdn_recurrent_bwd.argtypes = [vp] * 14 + [i, i, i, i, i, i, opts_p]
     lib.gdn_recurrent_bwd.restype = i
+    lib.gdn_output_gate_fwd.argtypes = [vp, vp, vp, vp, ll, i, opts_p]
+    lib.gdn_output_gate_fwd.restype = i
+    lib.gdn_output_gate_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ll, i, opts_p]
+    lib.gdn_output_gate_bwd.restype = i
+    lib.gdn_output_gate_bwd_workspace_size.argtypes = [ll, i, opts_p]
+    lib.gdn_output_gate_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.gdn_causal_conv1d_bwd.argtypes = [vp, ll, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, opts_p]
+    lib.gdn_causal_conv1d_bwd.restype = i
+    lib.gdn_causal_conv1d_bwd_workspace_size.argtypes = [i, i, i, i, opts_p]
+    lib.gdn_causal_conv1d_bwd_workspace_size.restype = ctypes.c_size_t
     lib.gdn_recurrent_bwd_workspace_size.argtypes = [i, i, i, i, i, i, opts_p]
     lib.gdn_recurrent_bwd_workspace_size.restype = ctypes.c_size_t
     lib.gdn_chunk_fwd_workspace_size.argtypes = [i, i, i, i, i, i, opts_p]

@@ -231,6 +231,53 @@ def gdn_causal_conv1d_fwd(x: torch.Tensor, w: torch.Tensor, cache_in: Optional[t
     return out, cache_out
 
 
+def gdn_causal_conv1d_bwd(x: torch.Tensor, w: torch.Tensor, grad_y: torch.Tensor, cache_in: Optional[torch.Tensor] = None,
+                          *, grad_cache_out: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                          want_grad_w: bool = True, want_grad_cache_in: bool = True,
+                          stream: Optional[torch.cuda.Stream] = None, events: Optional[Sequence[int]] = None):
+    """Gradients through gdn_causal_conv1d_fwd: x, w, cache_in as there; grad_y [B, T, C] like x (dense);
+    grad_cache_out [nseq, K-1, C] like x or None.  Returns fp32 (grad_x [B, T, C], grad_w [C, K] or None,
+    grad_cache_in [nseq, K-1, C] or None)."""
+    lib = L.load()
+    if x.dim() != 3 or x.stride(2) != 1 or x.stride(0) != x.shape[1] * x.stride(1):
+        raise ValueError("x must be [B, T, C] with contiguous channels and evenly strided token rows")
+    B, T, C = x.shape
+    dev, dt = x.device, x.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    K = int(w.shape[1])
+    _need("w", w, torch.float32, dev, (C, K))
+    _need("grad_y", grad_y, dt, dev, (B, T, C))
+    nseq = B
+    if cu_seqlens is not None:
+        nseq = int(cu_seqlens.numel()) - 1
+        _need("cu_seqlens", cu_seqlens, torch.int32, dev, (nseq + 1,))
+    if cache_in is not None:
+        _need("cache_in", cache_in, dt, dev, (nseq, K - 1, C))
+    if grad_cache_out is not None:
+        _need("grad_cache_out", grad_cache_out, dt, dev, (nseq, K - 1, C))
+    f32 = dict(dtype=torch.float32, device=dev)
+    gx = torch.empty((B, T, C), **f32)
+    gw = torch.empty((C, K), **f32) if want_grad_w else None
+    gc = torch.empty((nseq, K - 1, C), **f32) if want_grad_cache_in and K > 1 else None
+    with torch.cuda.device(dev):
+        o, keep = _opts(lib, dt, 1.0, 64, False, stream, dev, events)
+        if cu_seqlens is not None:
+            o.cu_seqlens = cu_seqlens.data_ptr()
+            o.num_seqs = nseq
+        ws = None
+        if want_grad_w:
+            need = int(lib.gdn_causal_conv1d_bwd_workspace_size(B, T, C, K, ctypes.byref(o)))
+            ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+            o.workspace, o.workspace_bytes = ws.data_ptr(), ws.numel()
+        st = lib.gdn_causal_conv1d_bwd(_ptr(x), x.stride(1), _ptr(w), _ptr(cache_in), _ptr(grad_y),
+                                       _ptr(grad_cache_out), _ptr(gx), _ptr(gw), _ptr(gc), B, T, C, K,
+                                       ctypes.byref(o))
+        del keep
+        L.check(lib, st)
+    return gx, gw, gc
+
+
 def gdn_causal_conv1d_step(x: torch.Tensor, w: torch.Tensor, cache: torch.Tensor, *,
                            out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
                            events: Optional[Sequence[int]] = None) -> torch.Tensor:
@@ -410,3 +457,55 @@ def gdn_recurrent_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torc
     if raw_gates is not None:
         return gq, gk, gv, gg, gb, gS0, gA, gdt
     return gq, gk, gv, gg, gb, gS0
+
+
+def gdn_output_gate_fwd(o: torch.Tensor, z: torch.Tensor, norm_weight: torch.Tensor, eps: float = 1e-6, *,
+                        out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """The shell's output gate on its own: o / sqrt(mean(o^2) + eps) * norm_weight * silu(z) over the last
+    axis (dv of 32, 64 or 128).  o, z [..., dv] (bf16 or fp32, contiguous); out like o (may be o)."""
+    lib = L.load()
+    dev, dt = o.device, o.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    dv = int(o.shape[-1])
+    _need("z", z, dt, dev, tuple(o.shape))
+    _need("norm_weight", norm_weight, torch.float32, dev, (dv,))
+    if not o.is_contiguous():
+        raise ValueError("o must be contiguous")
+    y = torch.empty_like(o) if out is None else out
+    _need("out", y, dt, dev, tuple(o.shape))
+    with torch.cuda.device(dev):
+        op, keep = _opts(lib, dt, 1.0, 64, False, stream, dev, None)
+        op.norm_eps = float(eps)
+        st = lib.gdn_output_gate_fwd(_ptr(o), _ptr(z), _ptr(norm_weight), _ptr(y), o.numel() // dv, dv,
+                                     ctypes.byref(op))
+        del keep
+        L.check(lib, st)
+    return y
+
+
+def gdn_output_gate_bwd(o: torch.Tensor, z: torch.Tensor, norm_weight: torch.Tensor, grad_y: torch.Tensor,
+                        eps: float = 1e-6, *, stream: Optional[torch.cuda.Stream] = None):
+    """Gradients through gdn_output_gate_fwd: returns fp32 (grad_o, grad_z like o, grad_norm_weight [dv])."""
+    lib = L.load()
+    dev, dt = o.device, o.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    dv = int(o.shape[-1])
+    _need("z", z, dt, dev, tuple(o.shape))
+    _need("grad_y", grad_y, dt, dev, tuple(o.shape))
+    _need("norm_weight", norm_weight, torch.float32, dev, (dv,))
+    rows = o.numel() // dv
+    f32 = dict(dtype=torch.float32, device=dev)
+    go, gz, gw = torch.empty(tuple(o.shape), **f32), torch.empty(tuple(o.shape), **f32), torch.empty((dv,), **f32)
+    with torch.cuda.device(dev):
+        op, keep = _opts(lib, dt, 1.0, 64, False, stream, dev, None)
+        op.norm_eps = float(eps)
+        need = int(lib.gdn_output_gate_bwd_workspace_size(rows, dv, ctypes.byref(op)))
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        op.workspace, op.workspace_bytes = ws.data_ptr(), ws.numel()
+        st = lib.gdn_output_gate_bwd(_ptr(o), _ptr(z), _ptr(norm_weight), _ptr(grad_y), _ptr(go), _ptr(gz),
+                                     _ptr(gw), rows, dv, ctypes.byref(op))
+        del keep
+        L.check(lib, st)
+    return go, gz, gw

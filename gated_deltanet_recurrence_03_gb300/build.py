@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
 
-SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_recurrent.cu", "gdn_tc.cu", "gdn_noalloc.cu", "gdn_gate.cu", "gdn_conv.cu", "gdn_bwd.cu", "gdn_bwd_tc.cu", "gdn_frontend_bwd.cu"]
+SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_recurrent.cu", "gdn_tc.cu", "gdn_noalloc.cu", "gdn_gate.cu", "gdn_conv.cu", "gdn_bwd.cu", "gdn_bwd_tc.cu", "gdn_frontend_bwd.cu", "gdn_conv_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                      "-I", INCLUDE, "-I", CSRC]

@@ -406,6 +406,56 @@ gdn_status_t gdn_causal_conv1d_step_qkv(const void* x, long long x_stride, const
     return conv_step_impl(x, x_stride, w, cache, y_q, y_k, y_v, Cq, Cq + Ck, N, Cq + Ck + Cv, K, opts);
 }
 
+size_t gdn_causal_conv1d_bwd_workspace_size(int B, int T, int C, int K, const gdn_opts_t* opts) {
+    const gdn_opts_t o = resolve(opts);
+    if (B < 0 || T < 0 || C <= 0 || C % 8 || K < 1 || K > 4) return 0;
+    const bool packed = o.cu_seqlens != nullptr;
+    const int nseq = packed ? o.num_seqs : B;
+    if (nseq <= 0) return 0;
+    return conv_bwd_workspace_bytes(B, T, C, K, nseq, packed);
+}
+
+gdn_status_t gdn_causal_conv1d_bwd(const void* x, long long x_stride, const float* w, const void* cache_in,
+                                   const void* grad_y, const void* grad_cache_out, float* grad_x, float* grad_w,
+                                   float* grad_cache_in, int B, int T, int C, int K, const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_opts_t o = resolve(opts);
+    if (B < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "B=%d T=%d must be >= 0", B, T);
+    const bool packed = o.cu_seqlens != nullptr;
+    if (packed && (B != 1 || o.num_seqs < 1))
+        return fail(GDN_ERR_INVALID_ARG, "cu_seqlens needs B == 1 and num_seqs >= 1");
+    const int nseq = packed ? o.num_seqs : B;
+    if (nseq == 0) return GDN_OK;
+    gdn_status_t st = conv_common(x, &x_stride, w, C, K, o);
+    if (st != GDN_OK) return st;
+    const bool have_tokens = (long long)B * T > 0;
+    if (have_tokens && (!grad_y || !grad_x)) return fail(GDN_ERR_INVALID_ARG, "null grad_y or grad_x");
+    const void* ptrs[] = {cache_in, grad_y, grad_cache_out, grad_x, grad_cache_in};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+    if (grad_w && !aligned_to(grad_w, 4)) return fail(GDN_ERR_INVALID_ARG, "grad_w must be 4-byte aligned");
+    if (packed && !aligned_to(o.cu_seqlens, 4)) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens must be 4-byte aligned");
+    const size_t need = conv_bwd_workspace_bytes(B, T, C, K, nseq, packed);
+    if (grad_w && (!o.workspace || o.workspace_bytes < need))
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    o.workspace ? o.workspace_bytes : (size_t)0);
+    if (o.workspace && (reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0)
+        return fail(GDN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    unsigned* status = nullptr;
+    st = device_ready(&status);
+    if (st != GDN_OK) return st;
+    ConvArgs a{};
+    a.x = x; a.x_stride = x_stride; a.w = w; a.cache_in = cache_in;
+    a.B = B; a.T = T; a.C = C; a.K = K; a.dtype = o.dtype; a.cu_seqlens = o.cu_seqlens; a.num_seqs = nseq;
+    a.packed = packed; a.stream = static_cast<cudaStream_t>(o.stream); a.status = status;
+    record(o, 0, a.stream);
+    const cudaError_t e = launch_conv_bwd(a, grad_y, grad_cache_out, grad_x, grad_w, grad_cache_in,
+                                          grad_w ? o.workspace : nullptr);
+    record(o, 1, a.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "conv backward launch");
+    return GDN_OK;
+}
+
 size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts) {
     const gdn_opts_t o = resolve(opts);
     if (B < 0 || T < 0 || Hqk <= 0 || Hv <= 0 || Hv % Hqk || !dim_ok(dk) || !dim_ok(dv)) return 0;
@@ -476,6 +526,78 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
                                                                  o.grad_dt_bias, core)
                                       : launch_backward(a);
     if (err != cudaSuccess) return cuda_fail(err, "backward launch");
+    return GDN_OK;
+}
+
+namespace {
+gdn_status_t gate_common(const gdn_opts_t& o, long long rows, int dv, const float* norm_weight) {
+    if (rows < 0) return fail(GDN_ERR_INVALID_ARG, "rows=%lld must be >= 0", rows);
+    if (dv != 32 && dv != 64 && dv != 128) return fail(GDN_ERR_UNSUPPORTED, "dv=%d: supported 32, 64, 128", dv);
+    if (o.dtype != GDN_F32 && o.dtype != GDN_BF16) return fail(GDN_ERR_INVALID_ARG, "unknown dtype %d", o.dtype);
+    if (!(o.norm_eps >= 0.f)) return fail(GDN_ERR_INVALID_ARG, "norm_eps must be >= 0");
+    if (rows > 0 && !norm_weight) return fail(GDN_ERR_INVALID_ARG, "null norm_weight");
+    return GDN_OK;
+}
+}  // namespace
+
+gdn_status_t gdn_output_gate_fwd(const void* o, const void* z, const float* norm_weight, void* y, long long rows, int dv,
+                                 const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_opts_t op = resolve(opts);
+    gdn_status_t st = gate_common(op, rows, dv, norm_weight);
+    if (st != GDN_OK) return st;
+    if (rows == 0) return GDN_OK;
+    if (!o || !z || !y) return fail(GDN_ERR_INVALID_ARG, "null o, z or y");
+    const void* vec16[] = {o, z, y};
+    for (const void* p : vec16)
+        if (!aligned_to(p, 16)) return fail(GDN_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
+    if (!aligned_to(norm_weight, 4)) return fail(GDN_ERR_INVALID_ARG, "norm_weight not 4-byte aligned");
+    unsigned* status = nullptr;
+    if ((st = device_ready(&status)) != GDN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(op.stream);
+    record(op, 0, s);
+    const cudaError_t e = launch_output_gate_to(o, y, z, norm_weight, op.norm_eps, rows, dv, op.dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "output gate launch");
+    record(op, 1, s);
+    return GDN_OK;
+}
+
+size_t gdn_output_gate_bwd_workspace_size(long long rows, int dv, const gdn_opts_t* opts) {
+    (void)opts;
+    if (rows < 0 || (dv != 32 && dv != 64 && dv != 128)) return 0;
+    return output_gate_bwd_workspace_bytes(rows, dv);
+}
+
+gdn_status_t gdn_output_gate_bwd(const void* o, const void* z, const float* norm_weight, const void* grad_y,
+                                 float* grad_o, float* grad_z, float* grad_norm_weight, long long rows, int dv,
+                                 const gdn_opts_t* opts) {
+    t_last_error[0] = 0;
+    const gdn_opts_t op = resolve(opts);
+    gdn_status_t st = gate_common(op, rows, dv, norm_weight);
+    if (st != GDN_OK) return st;
+    if (rows > 0 && (!o || !z || !grad_y || !grad_o || !grad_z))
+        return fail(GDN_ERR_INVALID_ARG, "null o, z, grad_y, grad_o or grad_z");
+    const void* vec16[] = {o, z, grad_y, grad_o, grad_z};
+    for (const void* p : vec16)
+        if (p && !aligned_to(p, 16)) return fail(GDN_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
+    const void* f4[] = {norm_weight, grad_norm_weight};
+    for (const void* p : f4)
+        if (p && !aligned_to(p, 4)) return fail(GDN_ERR_INVALID_ARG, "pointer %p not 4-byte aligned", p);
+    if (rows == 0 && !grad_norm_weight) return GDN_OK;
+    const size_t need = output_gate_bwd_workspace_bytes(rows, dv);
+    if (grad_norm_weight && rows > 0 && (!op.workspace || op.workspace_bytes < need))
+        return fail(GDN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    op.workspace ? op.workspace_bytes : (size_t)0);
+    if (op.workspace && (reinterpret_cast<uintptr_t>(op.workspace) & 255u) != 0)
+        return fail(GDN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    unsigned* status = nullptr;
+    if ((st = device_ready(&status)) != GDN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(op.stream);
+    record(op, 0, s);
+    const cudaError_t e = launch_output_gate_bwd(o, z, norm_weight, op.norm_eps, grad_y, grad_o, grad_z,
+                                                 grad_norm_weight, op.workspace, rows, dv, op.dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "output gate backward launch");
+    record(op, 1, s);
     return GDN_OK;
 }
 

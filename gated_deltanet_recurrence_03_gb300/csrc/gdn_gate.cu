@@ -2,9 +2,12 @@
 // out = self.norm(out, z) with GatedRMSNorm, and the parts table: "the output is normalised per head
 // and then multiplied by the gate silu(z)"):
 //     y_j = o_j / sqrt(mean_j(o_j^2) + eps) * w_j * silu(z_j)      over the dv values of one (token, head)
-// A memory-bound pass over `out` in place (16-byte vectors, a lane group per row), used after the prefill kernels, whose
-// outputs are split across CTAs by value columns.  The decode kernel applies the same gate in its
-// own epilogue.
+// A memory-bound pass (16-byte vectors, a lane group per row), in place over `out` after the prefill
+// kernels, whose outputs are split across CTAs by value columns, or from o to y for the standalone entry
+// point.  The decode kernel applies the same gate in its own epilogue.  The backward below gives the
+// gradients with respect to o, z and the weight.
+#include <algorithm>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -34,7 +37,7 @@ struct Vec16 {
 
 template <int DV, typename T>
 __global__ void __launch_bounds__(32 * kWarps)
-output_gate_kernel(T* __restrict__ out, const T* __restrict__ z, const float* __restrict__ w, float eps,
+output_gate_kernel(const T* in, T* out, const T* __restrict__ z, const float* __restrict__ w, float eps,
                    long long rows) {
     constexpr int VEC = Vec16<T>::N;
     constexpr int LPR = DV / VEC;          // lanes per row
@@ -52,7 +55,7 @@ output_gate_kernel(T* __restrict__ out, const T* __restrict__ z, const float* __
         row[r] = (warp * kRowsPerThread + r) * RPW + lane / LPR;
         ss[r] = 0.f;
         if (row[r] < rows) {
-            Vec16<T>::load(out + row[r] * DV + sub * VEC, o[r]);
+            Vec16<T>::load(in + row[r] * DV + sub * VEC, o[r]);
             Vec16<T>::load(z + row[r] * DV + sub * VEC, zz[r]);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) ss[r] = fmaf(o[r][e], o[r][e], ss[r]);
@@ -71,22 +74,140 @@ output_gate_kernel(T* __restrict__ out, const T* __restrict__ z, const float* __
 }
 
 template <int DV, typename T>
-cudaError_t launch_dv(void* out, const void* z, const float* w, float eps, long long rows, cudaStream_t stream) {
+cudaError_t launch_dv(const void* in, void* out, const void* z, const float* w, float eps, long long rows,
+                      cudaStream_t stream) {
     constexpr int RPW = 32 / (DV / Vec16<T>::N);
     const long long per_block = (long long)kWarps * kRowsPerThread * RPW;
     const unsigned blocks = (unsigned)((rows + per_block - 1) / per_block);
-    output_gate_kernel<DV, T><<<blocks, 32 * kWarps, 0, stream>>>(static_cast<T*>(out), static_cast<const T*>(z), w,
-                                                                  eps, rows);
+    output_gate_kernel<DV, T><<<blocks, 32 * kWarps, 0, stream>>>(static_cast<const T*>(in), static_cast<T*>(out),
+                                                                  static_cast<const T*>(z), w, eps, rows);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_typed(void* out, const void* z, const float* w, float eps, long long rows, int dv,
+cudaError_t launch_typed(const void* in, void* out, const void* z, const float* w, float eps, long long rows, int dv,
                          cudaStream_t stream) {
     switch (dv) {
-        case 32: return launch_dv<32, T>(out, z, w, eps, rows, stream);
-        case 64: return launch_dv<64, T>(out, z, w, eps, rows, stream);
-        case 128: return launch_dv<128, T>(out, z, w, eps, rows, stream);
+        case 32: return launch_dv<32, T>(in, out, z, w, eps, rows, stream);
+        case 64: return launch_dv<64, T>(in, out, z, w, eps, rows, stream);
+        case 128: return launch_dv<128, T>(in, out, z, w, eps, rows, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------- backward
+// With inv = (mean(o^2) + eps)^-1/2, o_hat = o inv, s = silu(z) and gy = dy w s, per row:
+//     do = inv (gy - o_hat mean(gy o_hat)),   dz = dy o_hat w silu'(z),
+// and dw = sum over the rows of dy o_hat s: each block sums its rows' terms per column (threads of a
+// column in a fixed order) into partial[block][dv]; a second kernel adds the blocks in order.
+constexpr int kBwdBlocksMax = 1024;
+
+template <int DV, typename T>
+__global__ void __launch_bounds__(32 * kWarps)
+output_gate_bwd_kernel(const T* __restrict__ o_in, const T* __restrict__ z, const float* __restrict__ w, float eps,
+                       const T* __restrict__ dy_in, float* __restrict__ d_o, float* __restrict__ d_z,
+                       float* __restrict__ partial, long long rows) {
+    constexpr int VEC = Vec16<T>::N;
+    constexpr int LPR = DV / VEC;          // lanes per row
+    constexpr int RPW = 32 / LPR;          // rows per warp and pass
+    constexpr int THREADS = 32 * kWarps;
+    __shared__ float red[THREADS][VEC + 1];
+    const int tid = threadIdx.x, lane = tid & 31, sub = lane % LPR;
+    float wv[VEC], acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        wv[e] = w[sub * VEC + e];
+        acc[e] = 0.f;
+    }
+    const long long rows_per_pass = (long long)gridDim.x * kWarps * RPW;
+    for (long long row = ((long long)blockIdx.x * kWarps + (tid >> 5)) * RPW + lane / LPR; row - lane / LPR < rows;
+         row += rows_per_pass) {
+        const bool ok = row < rows;
+        float o[VEC], zz[VEC], dy[VEC];
+        float ss = 0.f;
+        if (ok) {
+            Vec16<T>::load(o_in + row * DV + sub * VEC, o);
+            Vec16<T>::load(z + row * DV + sub * VEC, zz);
+            Vec16<T>::load(dy_in + row * DV + sub * VEC, dy);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) ss = fmaf(o[e], o[e], ss);
+        }
+#pragma unroll
+        for (int m = LPR / 2; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        const float inv = rsqrtf(ss / (float)DV + eps);
+        float gy[VEC], oh[VEC], sg[VEC], dot = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float sig = 1.f / (1.f + __expf(-zz[e]));
+                sg[e] = sig;
+                oh[e] = o[e] * inv;
+                gy[e] = dy[e] * wv[e] * zz[e] * sig;
+                dot = fmaf(gy[e], oh[e], dot);
+            }
+        }
+#pragma unroll
+        for (int m = LPR / 2; m > 0; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
+        if (!ok) continue;
+        const float mdot = dot / (float)DV;
+        float rdo[VEC], rdz[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            const float sig = sg[e], sz = zz[e] * sig;
+            rdo[e] = inv * (gy[e] - oh[e] * mdot);
+            rdz[e] = dy[e] * oh[e] * wv[e] * sig * (1.f + zz[e] * (1.f - sig));
+            acc[e] = fmaf(dy[e] * oh[e], sz, acc[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4) {
+            *reinterpret_cast<float4*>(d_o + row * DV + sub * VEC + e) = make_float4(rdo[e], rdo[e + 1], rdo[e + 2], rdo[e + 3]);
+            *reinterpret_cast<float4*>(d_z + row * DV + sub * VEC + e) = make_float4(rdz[e], rdz[e + 1], rdz[e + 2], rdz[e + 3]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) red[tid][e] = acc[e];
+    __syncthreads();
+    // column c = sub * VEC + e is held by every thread whose lane % LPR == sub: add them in thread order
+    for (int c = tid; c < DV; c += THREADS) {
+        const int sb = c / VEC, e = c % VEC;
+        float t = 0.f;
+        for (int th = sb; th < THREADS; th += LPR) t += red[th][e];
+        partial[(size_t)blockIdx.x * DV + c] = t;
+    }
+}
+
+__global__ void gate_dw_reduce_kernel(const float* __restrict__ partial, int blocks, int dv, float* __restrict__ dw) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= dv) return;
+    float t = 0.f;
+    for (int b = 0; b < blocks; ++b) t += partial[(size_t)b * dv + c];
+    dw[c] = t;
+}
+
+template <int DV, typename T>
+int bwd_blocks(long long rows) {
+    constexpr int RPW = 32 / (DV / Vec16<T>::N);
+    const long long per_block = (long long)kWarps * RPW;
+    return (int)std::min<long long>(std::max<long long>((rows + per_block - 1) / per_block, 1), kBwdBlocksMax);
+}
+
+template <int DV, typename T>
+cudaError_t launch_bwd_dv(const void* o, const void* z, const float* w, float eps, const void* dy, float* d_o,
+                          float* d_z, float* d_w, float* partial, long long rows, cudaStream_t stream) {
+    const int blocks = bwd_blocks<DV, T>(rows);
+    output_gate_bwd_kernel<DV, T><<<blocks, 32 * kWarps, 0, stream>>>(
+        static_cast<const T*>(o), static_cast<const T*>(z), w, eps, static_cast<const T*>(dy), d_o, d_z, partial, rows);
+    if (d_w) gate_dw_reduce_kernel<<<(DV + 127) / 128, 128, 0, stream>>>(partial, blocks, DV, d_w);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_bwd_typed(const void* o, const void* z, const float* w, float eps, const void* dy, float* d_o,
+                             float* d_z, float* d_w, float* partial, long long rows, int dv, cudaStream_t stream) {
+    switch (dv) {
+        case 32: return launch_bwd_dv<32, T>(o, z, w, eps, dy, d_o, d_z, d_w, partial, rows, stream);
+        case 64: return launch_bwd_dv<64, T>(o, z, w, eps, dy, d_o, d_z, d_w, partial, rows, stream);
+        case 128: return launch_bwd_dv<128, T>(o, z, w, eps, dy, d_o, d_z, d_w, partial, rows, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -95,9 +216,34 @@ cudaError_t launch_typed(void* out, const void* z, const float* w, float eps, lo
 
 cudaError_t launch_output_gate(void* out, const void* z, const float* w, float eps, long long rows, int dv,
                                int dtype, cudaStream_t stream) {
+    return launch_output_gate_to(out, out, z, w, eps, rows, dv, dtype, stream);
+}
+
+cudaError_t launch_output_gate_to(const void* in, void* out, const void* z, const float* w, float eps, long long rows,
+                                  int dv, int dtype, cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
-    return dtype == GDN_BF16 ? launch_typed<__nv_bfloat16>(out, z, w, eps, rows, dv, stream)
-                             : launch_typed<float>(out, z, w, eps, rows, dv, stream);
+    return dtype == GDN_BF16 ? launch_typed<__nv_bfloat16>(in, out, z, w, eps, rows, dv, stream)
+                             : launch_typed<float>(in, out, z, w, eps, rows, dv, stream);
+}
+
+size_t output_gate_bwd_workspace_bytes(long long rows, int dv) {
+    (void)rows;
+    return (size_t)kBwdBlocksMax * dv * sizeof(float);
+}
+
+cudaError_t launch_output_gate_bwd(const void* o, const void* z, const float* w, float eps, const void* dy, float* d_o,
+                                   float* d_z, float* d_w, void* workspace, long long rows, int dv, int dtype,
+                                   cudaStream_t stream) {
+    float* partial = static_cast<float*>(workspace);
+    if (rows <= 0) {   // no rows: the weight gradient is zero
+        if (d_w) {
+            const cudaError_t e = cudaMemsetAsync(d_w, 0, (size_t)dv * sizeof(float), stream);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    return dtype == GDN_BF16 ? launch_bwd_typed<__nv_bfloat16>(o, z, w, eps, dy, d_o, d_z, d_w, partial, rows, dv, stream)
+                             : launch_bwd_typed<float>(o, z, w, eps, dy, d_o, d_z, d_w, partial, rows, dv, stream);
 }
 
 }  // namespace gdn

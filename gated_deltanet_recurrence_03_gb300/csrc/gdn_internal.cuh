@@ -153,11 +153,27 @@ void* tensor_map_encoder();
 
 cudaError_t launch_conv_fwd(const ConvArgs& a);
 cudaError_t launch_conv_step(const ConvArgs& a);
+// Backward of the conv + SiLU: dx [B*T, C] and dcache [nseq, K-1, C] fp32 (dcache may be NULL), dw [C, K]
+// fp32 summed over 64-token slots in a fixed order through `workspace` (conv_bwd_workspace_bytes; may be
+// NULL when dw is NULL).  dy is dense [B*T, C], dco (the outgoing cache's gradient) [nseq, K-1, C] or NULL,
+// both in a.dtype.
+size_t conv_bwd_workspace_bytes(int B, int T, int C, int K, int nseq, bool packed);
+cudaError_t launch_conv_bwd(const ConvArgs& a, const void* dy, const void* dco, float* dx, float* dw, float* dcache,
+                            void* workspace);
 cudaError_t launch_decode(const DecodeArgs& a);
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a);
 // out <- RMSNorm(out) * norm_weight * silu(z) over each of `rows` rows of dv values, in place.
 cudaError_t launch_output_gate(void* out, const void* z, const float* w, float eps, long long rows, int dv,
                                int dtype, cudaStream_t stream);
+// y <- RMSNorm(o) * norm_weight * silu(z) (in may equal out), and its backward: d_o, d_z (fp32, rows x dv)
+// and, when d_w is not NULL, d_w [dv] summed over the rows in a fixed order through `workspace`
+// (output_gate_bwd_workspace_bytes, 16-byte aligned).
+cudaError_t launch_output_gate_to(const void* in, void* out, const void* z, const float* w, float eps, long long rows,
+                                  int dv, int dtype, cudaStream_t stream);
+size_t output_gate_bwd_workspace_bytes(long long rows, int dv);
+cudaError_t launch_output_gate_bwd(const void* o, const void* z, const float* w, float eps, const void* dy, float* d_o,
+                                   float* d_z, float* d_w, void* workspace, long long rows, int dv, int dtype,
+                                   cudaStream_t stream);
 
 // Tensor-core chunked prefill: whether it takes these arguments, its workspace, and its launch.
 bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk, unsigned flags);

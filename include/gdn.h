@@ -235,6 +235,30 @@ gdn_status_t gdn_causal_conv1d_step_qkv(const void* x, long long x_stride, const
                                         const gdn_opts_t* opts);
 
 /*
+ * gdn_causal_conv1d_bwd -- gradients through gdn_causal_conv1d_fwd, given grad_y = dL/dy and, for a
+ * decode that continues from the outgoing cache, grad_cache_out = dL/dcache_out.  With xp a sequence's
+ * inputs padded on the left by its K-1 cached inputs, u_t = sum_i w[c, i] xp[t + i] and
+ * du_t = grad_y[t] silu'(u_t):
+ *     grad_x (and grad_cache_in for the cached rows) = sum_i w[c, i] du_{p - i} at input position p,
+ *     plus grad_cache_out for the inputs the outgoing cache holds;
+ *     grad_w[c, i] = sum over all tokens of du_t xp[t + i].
+ *   x, x_stride, w, cache_in, B, T, C, K, cu_seqlens / num_seqs, dtype: as gdn_causal_conv1d_fwd
+ *   grad_y           [B, T, C] dtype, dense (the gradients of the q, k and v slices side by side for
+ *                    the packed projection), 16-byte aligned
+ *   grad_cache_out   [nseq, K-1, C] dtype or NULL (no loss on the outgoing cache)
+ *   grad_x           [B, T, C] float, dense, 16-byte aligned (overwritten)
+ *   grad_w           [C, K] float or NULL (not computed); summed over 64-token slots in a fixed order
+ *                    through opts->workspace (256-byte aligned, gdn_causal_conv1d_bwd_workspace_size
+ *                    bytes; GDN_ERR_WORKSPACE if missing)
+ *   grad_cache_in    [nseq, K-1, C] float or NULL (not written), 16-byte aligned
+ * Deterministic.  Asynchronous on opts->stream; events[0] / [1] around the kernels.
+ */
+size_t gdn_causal_conv1d_bwd_workspace_size(int B, int T, int C, int K, const gdn_opts_t* opts);
+gdn_status_t gdn_causal_conv1d_bwd(const void* x, long long x_stride, const float* w, const void* cache_in,
+                                   const void* grad_y, const void* grad_cache_out, float* grad_x, float* grad_w,
+                                   float* grad_cache_in, int B, int T, int C, int K, const gdn_opts_t* opts);
+
+/*
  * gdn_recurrent_bwd -- the backward pass: gradients of a loss L(out, S_final) of gdn_chunk_fwd with
  * respect to q, k, v, g, beta and S0, given grad_out = dL/dout and grad_S_final = dL/dS_final.  It is
  * the adjoint of the token loop of "Transformer by Hand, ch. 7" (section "The formula"), which the
@@ -272,6 +296,37 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
                                const float* S0, const void* grad_out, const float* grad_S_final, float* grad_q,
                                float* grad_k, float* grad_v, float* grad_g, float* grad_beta, float* grad_S0,
                                int B, int T, int Hqk, int Hv, int dk, int dv, const gdn_opts_t* opts);
+
+/*
+ * gdn_output_gate_fwd -- the output gate of the GatedDeltaNet shell on its own ("Transformer by Hand,
+ * ch. 7", listing "qwen/deltanet.py": out = GatedRMSNorm(o, z); its parts table: normalised per head,
+ * then times silu(z)), per row of dv values (one token and value head):
+ *     y_j = o_j / sqrt(mean_j(o_j^2) + eps) * norm_weight_j * silu(z_j)
+ * the same pass gdn_chunk_fwd applies with GDN_OUTPUT_GATE, for callers that keep the recurrence's
+ * output o (a training step needs it for the backward below).
+ *   o, z, y        [rows, dv] dtype (opts->dtype), 16-byte aligned; y may equal o (in place)
+ *   norm_weight    [dv] float;  eps = opts->norm_eps
+ * Supported dv: 32, 64, 128.  Asynchronous on opts->stream; events[0] / [1] around the kernel.
+ */
+gdn_status_t gdn_output_gate_fwd(const void* o, const void* z, const float* norm_weight, void* y, long long rows,
+                                 int dv, const gdn_opts_t* opts);
+
+/*
+ * gdn_output_gate_bwd -- gradients through gdn_output_gate_fwd given grad_y = dL/dy: with
+ * inv = (mean(o^2) + eps)^-1/2, o_hat = o inv and gy = grad_y norm_weight silu(z), per row
+ *     grad_o = inv (gy - o_hat mean(gy o_hat)),   grad_z = grad_y o_hat norm_weight silu'(z),
+ * and grad_norm_weight = sum over all rows of grad_y o_hat silu(z).
+ *   o, z, grad_y            [rows, dv] dtype, 16-byte aligned
+ *   grad_o, grad_z          [rows, dv] float (overwritten), 16-byte aligned
+ *   grad_norm_weight        [dv] float (overwritten), or NULL (not computed); its sum over rows is
+ *                           taken in a fixed order through opts->workspace (256-byte aligned,
+ *                           gdn_output_gate_bwd_workspace_size bytes; GDN_ERR_WORKSPACE if missing)
+ * Deterministic.  Asynchronous on opts->stream; events[0] / [1] around the kernels.
+ */
+size_t gdn_output_gate_bwd_workspace_size(long long rows, int dv, const gdn_opts_t* opts);
+gdn_status_t gdn_output_gate_bwd(const void* o, const void* z, const float* norm_weight, const void* grad_y,
+                                 float* grad_o, float* grad_z, float* grad_norm_weight, long long rows, int dv,
+                                 const gdn_opts_t* opts);
 
 /* Synchronise `stream` (cudaStream_t, NULL = legacy), then read and clear the device status word
  * that kernels set when a bounded wait runs out.  GDN_OK if clear, GDN_ERR_TIMEOUT if set,

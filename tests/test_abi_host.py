@@ -295,3 +295,72 @@ def test_chunk_option_does_not_change_the_path(lib):
         sizes = {c: lib.gdn_chunk_fwd_workspace_size(2, 300, 2, 4, d, d, opts(lib, dtype=dtype, chunk=c))
                  for c in (0, 16, 32, 64)}
         assert len(set(sizes.values())) == 1 and sizes[64] > 0, sizes
+
+
+# ---------------------------------------------------------------- output gate on its own
+@pytest.mark.parametrize("case,expect", [
+    (dict(rows=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(dv=48), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(dtype=7), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(norm_eps=-1.0), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(ptrs=[FAKE, FAKE, 0, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),         # no norm_weight
+    (dict(ptrs=[FAKE, 0, FAKE, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),         # no z
+    (dict(ptrs=[FAKE + 8, FAKE, FAKE, FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),  # o not 16-byte aligned
+])
+def test_output_gate_forward_argument_errors(lib, case, expect):
+    p = case.pop("ptrs", [FAKE] * 4)
+    rows, dv = case.pop("rows", 8), case.pop("dv", 128)
+    assert lib.gdn_output_gate_fwd(*p, rows, dv, opts(lib, **case)) == expect
+    assert lib.gdn_last_error() != b""
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(rows=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(dv=96), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(ptrs=[FAKE] * 4 + [0] + [FAKE] * 2), pkg_lib.GDN_ERR_INVALID_ARG),          # no grad_o
+    (dict(ptrs=[FAKE] * 5 + [FAKE + 4] + [FAKE]), pkg_lib.GDN_ERR_INVALID_ARG),       # grad_z misaligned
+    (dict(ptrs=[FAKE] * 6 + [FAKE + 2]), pkg_lib.GDN_ERR_INVALID_ARG),                # grad_norm_weight misaligned
+    (dict(), pkg_lib.GDN_ERR_WORKSPACE),                                             # weight sum needs scratch
+    (dict(workspace=FAKE, workspace_bytes=64), pkg_lib.GDN_ERR_WORKSPACE),
+    (dict(workspace=FAKE + 16, workspace_bytes=1 << 20), pkg_lib.GDN_ERR_INVALID_ARG),   # not 256-byte aligned
+])
+def test_output_gate_backward_argument_errors(lib, case, expect):
+    p = case.pop("ptrs", [FAKE] * 7)
+    rows, dv = case.pop("rows", 8), case.pop("dv", 128)
+    assert lib.gdn_output_gate_bwd(*p, rows, dv, opts(lib, **case)) == expect
+    assert lib.gdn_last_error() != b""
+
+
+def test_output_gate_sizes_and_empty_calls(lib):
+    for dv in (32, 64, 128):   # one partial row of dv floats per block, at most 1024 blocks
+        assert lib.gdn_output_gate_bwd_workspace_size(10 ** 6, dv, opts(lib)) == 1024 * dv * 4
+    assert lib.gdn_output_gate_bwd_workspace_size(10, 40, opts(lib)) == 0
+    assert lib.gdn_output_gate_fwd(0, 0, 0, 0, 0, 128, opts(lib)) == pkg_lib.GDN_OK
+    assert lib.gdn_output_gate_bwd(0, 0, 0, 0, 0, 0, 0, 0, 64, opts(lib)) == pkg_lib.GDN_OK   # nothing to write
+
+
+# ---------------------------------------------------------------- conv backward
+def conv_bwd(lib, B=1, T=8, C=64, K=4, ptrs=None, x_stride=0, **kw):
+    p = [FAKE] * 8 if ptrs is None else ptrs   # x, w, cache_in, grad_y, grad_cache_out, grad_x, grad_w, grad_cache_in
+    return lib.gdn_causal_conv1d_bwd(p[0], x_stride, *p[1:], B, T, C, K, opts(lib, **kw))
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(B=-1), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(C=60), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(K=5), pkg_lib.GDN_ERR_UNSUPPORTED),
+    (dict(ptrs=[FAKE] * 3 + [0] + [FAKE] * 4), pkg_lib.GDN_ERR_INVALID_ARG),       # no grad_y
+    (dict(ptrs=[FAKE] * 5 + [FAKE + 4] + [FAKE] * 2), pkg_lib.GDN_ERR_INVALID_ARG),  # grad_x misaligned
+    (dict(B=2, cu_seqlens=FAKE, num_seqs=2), pkg_lib.GDN_ERR_INVALID_ARG),
+    (dict(), pkg_lib.GDN_ERR_WORKSPACE),                                           # grad_w needs scratch
+])
+def test_conv_backward_argument_errors(lib, case, expect):
+    assert conv_bwd(lib, **case) == expect
+    assert lib.gdn_last_error() != b""
+
+
+def test_conv_backward_workspace_and_empty(lib):
+    # per 64-token slot (ceil(tokens / 64) + sequences of them) one float per channel and tap
+    assert lib.gdn_causal_conv1d_bwd_workspace_size(2, 8192, 8192, 4, opts(lib)) == (256 + 2) * 8192 * 4 * 4
+    assert lib.gdn_causal_conv1d_bwd_workspace_size(1, 8, 60, 4, opts(lib)) == 0
+    assert conv_bwd(lib, B=0, T=0, ptrs=[0] * 8) == pkg_lib.GDN_OK
