@@ -441,6 +441,51 @@ def run_gpu(args):
                    for i, name in enumerate(("bwd_wy", "bwd_state_fwd", "bwd_state_adj", "bwd_local"))}
     del xb, dout, ws_b
 
+    # ---- backward of the layer's other pieces on the same 8k workload: the recurrence's backward through
+    #      the fused front end (l2 norm of q, k; gates from raw a, b), the output gate's backward and the
+    #      conv's backward over the packed q/k/v projection
+    bf = torch.bfloat16
+    gen = torch.Generator(device=dev).manual_seed(7)
+    xb = device_inputs_random(torch, dev, w, seed=4)
+    a_raw = torch.randn(w.B, w.T, w.Hv, device=dev, generator=gen).to(bf)
+    b_raw = torch.randn(w.B, w.T, w.Hv, device=dev, generator=gen).to(bf)
+    A_log = -0.5 + 0.5 * torch.randn(w.Hv, device=dev, generator=gen)
+    dt_bias = 0.5 * torch.randn(w.Hv, device=dev, generator=gen)
+    dout = torch.randn(w.B, w.T, w.Hv, w.dv, device=dev, generator=gen).to(bf)
+    ws_f = torch.empty(int(gdn.backward_workspace_size(w.B, w.T, w.Hqk, w.Hv, w.dk, w.dv, front_end=True)),
+                       dtype=torch.uint8, device=dev)
+
+    def timed(fn, reps, warm=3):
+        for _ in range(warm):
+            fn()
+        barrier()
+        t0.record(stream)
+        for _ in range(reps):
+            fn()
+        t1.record(stream)
+        barrier()
+        return max_ms(t0.elapsed_time(t1)) / reps
+
+    clocks.active = True
+    fe_ms = timed(lambda: gdn.gdn_recurrent_bwd(xb["q"], xb["k"], xb["v"], a_raw, b_raw, S0, dout, dSf, workspace=ws_f,
+                                                normalize_qk=True, raw_gates=(A_log, dt_bias)), 2)
+    del ws_f, xb, a_raw, b_raw
+    o_g = torch.randn(w.B, w.T, w.Hv, w.dv, device=dev, generator=gen).to(bf)
+    z_g = torch.randn(w.B, w.T, w.Hv, w.dv, device=dev, generator=gen).to(bf)
+    nw = 1.0 + 0.1 * torch.randn(w.dv, device=dev, generator=gen)
+    gate_bwd_ms = timed(lambda: gdn.gdn_output_gate_bwd(o_g, z_g, nw, dout), 10)
+    gate_bwd_bytes = 3 * (w.B * w.T * Cv * 2) + 2 * (w.B * w.T * Cv * 4)   # o, z, dy in; do, dz out (fp32)
+    del o_g, z_g
+    proj = torch.randn(w.B, w.T, Cc, device=dev, generator=gen).to(bf)
+    dy_c = torch.randn(w.B, w.T, Cc, device=dev, generator=gen).to(bf)
+    conv_w = 0.5 * torch.randn(Cc, 4, device=dev, generator=gen)
+    conv_bwd_ms = timed(lambda: gdn.gdn_causal_conv1d_bwd(proj, conv_w, dy_c, want_grad_cache_in=False), 10)
+    slots_c = (w.B * w.T + 63) // 64 + w.B
+    conv_bwd_bytes = 2 * (w.B * w.T * Cc * 2) + w.B * w.T * Cc * 4 + 2 * slots_c * Cc * 4 * 4   # x, dy in; dx, dw shares
+    clocks.active = False
+    gdn.check_device_status()
+    del proj, dy_c, dout
+
     # ---- decode: 512 consecutive steps, state resident, one CUDA graph per pass
     wd = DECODE
     xd = device_inputs_random(torch, dev, wd, steps=wd.T, seed=2)
@@ -616,6 +661,23 @@ def run_gpu(args):
                      "roofline_alu": {"bound": "alu", "achieved": round(bwd_tf, 2), "peak": round(alu_peak, 1),
                                       "unit": "TFLOP/s", "frac": round(bwd_tf / alu_peak, 4),
                                       "peak_source": "fp32 FMA lanes x 2 x 2070 MHz (unit counts)"}},
+        "layer_backward": {"workload": "prefill_gqa_8k backward through the layer's other pieces: the recurrence's "
+                                       "backward with the fused front end (l2 norm of q, k and gates from raw a, b: fp32 "
+                                       "copies of the front end's outputs, the split-tf32 backward kernels, the chain rule "
+                                       "back), the output gate's backward (bf16 in, fp32 gradients) and the causal conv's "
+                                       "backward over the packed 8192-channel q/k/v projection (K=4)",
+                           "front_end_backward_ms": round(fe_ms, 4),
+                           "front_end_backward_tokens_per_s": round(world * tokens / (fe_ms / 1e3), 1),
+                           "output_gate_backward": {"ms": round(gate_bwd_ms, 4), "roofline": {
+                               "bound": "hbm", "achieved": round(gate_bwd_bytes / (gate_bwd_ms * 1e6), 1),
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": round(gate_bwd_bytes / (gate_bwd_ms * 1e6) / peaks["hbm_gbs"], 4),
+                               "algorithmic_bytes": gate_bwd_bytes}},
+                           "conv_backward": {"ms": round(conv_bwd_ms, 4), "roofline": {
+                               "bound": "hbm", "achieved": round(conv_bwd_bytes / (conv_bwd_ms * 1e6), 1),
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": round(conv_bwd_bytes / (conv_bwd_ms * 1e6) / peaks["hbm_gbs"], 4),
+                               "algorithmic_bytes": conv_bwd_bytes}}},
         "decode": {"workload": "decode_256x512: 256 sequences x 32 V heads (16 QK heads), d=128, 512 steps, "
                                "fp32 state 512 MiB resident, one CUDA graph per 512-step pass",
                    "value": round(world / (dec_ms / 1e3), 1), "unit": "steps/s",

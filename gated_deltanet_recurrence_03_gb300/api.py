@@ -381,10 +381,13 @@ def gdn_causal_conv1d_step_qkv(x: torch.Tensor, w: torch.Tensor, cache: torch.Te
 
 
 def backward_workspace_size(B: int, T: int, Hqk: int, Hv: int, dk: int, dv: int, *,
-                            num_seqs: Optional[int] = None) -> int:
-    """Bytes of device scratch gdn_recurrent_bwd needs."""
+                            num_seqs: Optional[int] = None, front_end: bool = False) -> int:
+    """Bytes of device scratch gdn_recurrent_bwd needs (with ``front_end``: through the l2 norm and / or
+    the raw gates)."""
     lib = L.load()
     o = L.default_opts(lib)
+    if front_end:
+        o.flags = L.GDN_NORMALIZE_QK
     if num_seqs is not None:
         o.cu_seqlens = 1   # only tested for NULL
         o.num_seqs = int(num_seqs)

@@ -7,10 +7,10 @@
 //     dxp[p] = sum_j w[c, j] du_{p - j}     (the input at p feeds the outputs p - j, j < K)
 //     dw[c, j] = sum_t du_t xp[t + j]
 // and the outgoing cache (the last K - 1 rows of xp) passes its gradient straight to those rows.
-// One thread per (64-token slot of a sequence, 16-byte vector of channels): it slides a K-row window of
-// x and a K-entry ring of du over its tokens plus K - 1 on each side (the du of the next slot's first
+// One thread per (64-token slot of a sequence, 4-byte vector of channels): it slides a K-row window of
+// x and a K-entry ring of du over its tokens plus K - 1 on each side, the raw rows loaded three ahead (the du of the next slot's first
 // tokens are recomputed, so slots are independent), writes dx of its own tokens (and of the cached
-// inputs in a sequence's first slot) and its share of dw; a second kernel adds the slots' shares in a
+// inputs in a sequence's first slot) and its share of dw; column_sum_kernel adds the slots' shares in a
 // fixed order.
 #include <algorithm>
 
@@ -47,30 +47,47 @@ __device__ bool conv_slot(const int32_t* cu, int nseq, int T_len, long long slot
     return true;
 }
 
+// 4-byte vectors of channels (2 bf16 or 1 fp32): a warp covers 128 contiguous bytes of a row, and the
+// per-thread state fits 64 registers, four blocks of 256 threads per SM (measured on the 8k layer's
+// projection: 16-byte vectors 926 us, 8-byte 749-769 us, 4-byte 641 us, 4-byte at four blocks per SM
+// 519-521 us; five or more blocks per SM spill and run slower).
+constexpr int kVecBytes = 4;
+constexpr int kMinBlocks = 4;
+constexpr int kPrefetch = 3;   // rows of x and dy loaded ahead of the row being used
+
 template <typename T>
-struct V16 {
-    static constexpr int N = 16 / (int)sizeof(T);
-    __device__ static void load(const T* p, float* f) {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
+struct V4 {
+    static constexpr int N = kVecBytes / (int)sizeof(T);
+    using Raw = uint32_t;
+    __device__ static Raw raw(const T* p) { return *reinterpret_cast<const Raw*>(p); }
+    __device__ static void unpack(const Raw& u, float* f) {
         const T* h = reinterpret_cast<const T*>(&u);
 #pragma unroll
         for (int e = 0; e < N; ++e) f[e] = to_f32(h[e]);
     }
+    __device__ static void load(const T* p, float* f) { unpack(raw(p), f); }
 };
 
 template <int N>
 __device__ __forceinline__ void store_f32(float* p, const float (&f)[N]) {
+    if constexpr (N % 4 == 0) {
 #pragma unroll
-    for (int e = 0; e < N; e += 4) *reinterpret_cast<float4*>(p + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+        for (int e = 0; e < N; e += 4) *reinterpret_cast<float4*>(p + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+    } else if constexpr (N == 2) {
+        *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
+    } else {
+        static_assert(N == 1, "one, two or a multiple of four channels");
+        p[0] = f[0];
+    }
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
 conv_bwd_kernel(const T* __restrict__ x, long long xs, const float* __restrict__ w, const T* __restrict__ cache_in,
                 const T* __restrict__ dy, const T* __restrict__ dco, float* __restrict__ dx, float* __restrict__ dcache,
                 float* __restrict__ partial, const int32_t* __restrict__ cu, int nseq, int T_len, int C,
                 long long slots) {
-    constexpr int VEC = V16<T>::N;
+    constexpr int VEC = V4<T>::N;
     const int NV = C / VEC;
     const long long item = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (item >= slots * NV) return;
@@ -99,13 +116,37 @@ conv_bwd_kernel(const T* __restrict__ x, long long xs, const float* __restrict__
     for (int e = 0; e < VEC; ++e)
 #pragma unroll
         for (int j = 0; j < K; ++j) wv[e][j] = w[(size_t)(c0 + e) * K + j];
+    // the raw bytes of the x row (an input, a cached input before the sequence, or zero past its end) and
+    // of the dy row (zero outside this slot's tokens and halo, and past the sequence) of token tt
+    using Raw = typename V4<T>::Raw;
+    const auto fetch = [&](long long tt, Raw& rx, Raw& rd) {
+        rx = 0u;
+        rd = 0u;
+        if (tt < s1) {
+            if (tt >= s0)
+                rx = V4<T>::raw(x + tt * xs + c0);
+            else if (cache_in)
+                rx = V4<T>::raw(cache_in + ((size_t)seq * (K - 1) + (size_t)(tt - s0 + K - 1)) * C + c0);
+            if (tt >= t0) rd = V4<T>::raw(dy + tt * (long long)C + c0);
+        }
+    };
     float xw[K][VEC], dr[K][VEC];   // x rows t - K + 1 .. t (oldest first); du_{t - K + 1} .. du_t
 #pragma unroll
     for (int j = 0; j < K; ++j)
 #pragma unroll
         for (int e = 0; e < VEC; ++e) xw[j][e] = dr[j][e] = 0.f;
-    const long long t_end = t0 + n + K - 1;   // last du needed is that of token t0 + n + K - 2
-    for (long long t = t0 - (K - 1); t < t_end; ++t) {
+    const long long t_begin = t0 - (K - 1), t_end = t0 + n + K - 1;   // last du needed: token t0 + n + K - 2
+    Raw qx[kPrefetch], qd[kPrefetch];   // rows t .. t + kPrefetch - 1, loaded ahead
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i) fetch(t_begin + i < t_end ? t_begin + i : s1, qx[i], qd[i]);
+    for (long long t = t_begin; t < t_end; ++t) {
+        const Raw rx = qx[0], rd = qd[0];
+#pragma unroll
+        for (int i = 0; i + 1 < kPrefetch; ++i) {
+            qx[i] = qx[i + 1];
+            qd[i] = qd[i + 1];
+        }
+        fetch(t + kPrefetch < t_end ? t + kPrefetch : s1, qx[kPrefetch - 1], qd[kPrefetch - 1]);
 #pragma unroll
         for (int j = 0; j + 1 < K; ++j)
 #pragma unroll
@@ -113,23 +154,11 @@ conv_bwd_kernel(const T* __restrict__ x, long long xs, const float* __restrict__
                 xw[j][e] = xw[j + 1][e];
                 dr[j][e] = dr[j + 1][e];
             }
-        // the newest window row: x, a cached input before the sequence, or nothing past its end
-        float* xr = xw[K - 1];
-        if (t >= s1) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) xr[e] = 0.f;
-        } else if (t >= s0) {
-            V16<T>::load(x + t * xs + c0, xr);
-        } else if (cache_in) {
-            V16<T>::load(cache_in + ((size_t)seq * (K - 1) + (size_t)(t - s0 + K - 1)) * C + c0, xr);
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) xr[e] = 0.f;
-        }
+        V4<T>::unpack(rx, xw[K - 1]);
         float* d = dr[K - 1];
         if (t >= t0 && t < s1) {   // du_t = dy_t silu'(u_t); this slot's own tokens add to dw
             float g[VEC];
-            V16<T>::load(dy + t * (long long)C + c0, g);
+            V4<T>::unpack(rd, g);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 float u = 0.f;
@@ -156,14 +185,14 @@ conv_bwd_kernel(const T* __restrict__ x, long long xs, const float* __restrict__
             float gx[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                float a = 0.f;
+                float acc_x = 0.f;
 #pragma unroll
-                for (int j = 0; j < K; ++j) a = fmaf(wv[e][j], dr[K - 1 - j][e], a);
-                gx[e] = a;
+                for (int j = 0; j < K; ++j) acc_x = fmaf(wv[e][j], dr[K - 1 - j][e], acc_x);
+                gx[e] = acc_x;
             }
             if (dco && p >= s1 - (K - 1)) {   // the outgoing cache holds this input
                 float gc[VEC];
-                V16<T>::load(dco + ((size_t)seq * (K - 1) + (size_t)(p - (s1 - (K - 1)))) * C + c0, gc);
+                V4<T>::load(dco + ((size_t)seq * (K - 1) + (size_t)(p - (s1 - (K - 1)))) * C + c0, gc);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) gx[e] += gc[e];
             }
@@ -194,15 +223,6 @@ __global__ void conv_bwd_empty_kernel(const T* __restrict__ dco, float* __restri
     dcache[i] = dco ? to_f32(dco[i]) : 0.f;
 }
 
-// dw[c][j] = sum over slots (in order) of the slots' shares.
-__global__ void conv_dw_reduce_kernel(const float* __restrict__ partial, long long slots, int CK, float* __restrict__ dw) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= CK) return;
-    float t = 0.f;
-    for (long long s = 0; s < slots; ++s) t += partial[(size_t)s * CK + i];
-    dw[i] = t;
-}
-
 long long conv_slots(const ConvArgs& a) {
     const long long ttot = a.packed ? (long long)a.T : (long long)a.B * a.T;
     return (ttot + kSlot - 1) / kSlot + a.num_seqs;
@@ -211,7 +231,7 @@ long long conv_slots(const ConvArgs& a) {
 template <typename T, int K>
 cudaError_t launch_k(const ConvArgs& a, const void* dy, const void* dco, float* dx, float* dw, float* dcache,
                      float* partial) {
-    constexpr int VEC = V16<T>::N;
+    constexpr int VEC = V4<T>::N;
     const long long slots = conv_slots(a);
     const long long items = slots * (a.C / VEC);
     const int T_len = a.T;
@@ -227,7 +247,7 @@ cudaError_t launch_k(const ConvArgs& a, const void* dy, const void* dco, float* 
     }
     if (dw) {
         const int CK = a.C * K;
-        conv_dw_reduce_kernel<<<(CK + 255) / 256, 256, 0, a.stream>>>(partial, slots, CK, dw);
+        column_sum_kernel<<<(CK + 31) / 32, kColSumThreads, 0, a.stream>>>(partial, slots, CK, dw);
     }
     return cudaGetLastError();
 }

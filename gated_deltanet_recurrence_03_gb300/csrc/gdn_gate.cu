@@ -99,18 +99,53 @@ cudaError_t launch_typed(const void* in, void* out, const void* z, const float* 
 // With inv = (mean(o^2) + eps)^-1/2, o_hat = o inv, s = silu(z) and gy = dy w s, per row:
 //     do = inv (gy - o_hat mean(gy o_hat)),   dz = dy o_hat w silu'(z),
 // and dw = sum over the rows of dy o_hat s: each block sums its rows' terms per column (threads of a
-// column in a fixed order) into partial[block][dv]; a second kernel adds the blocks in order.
+// column in a fixed order) into partial[block][dv]; column_sum_kernel adds the blocks in a fixed order.
 constexpr int kBwdBlocksMax = 1024;
+
+// Four values per lane (8 bytes of bf16, 16 of fp32): a warp holds 32 / (DV / 4) rows per pass, the state
+// of a thread stays small, and the next pass's raw o, z, dy are loaded while this pass computes.
+template <typename T>
+struct Vec8;
+template <>
+struct Vec8<__nv_bfloat16> {
+    static constexpr int N = 4;
+    using Raw = uint2;
+    __device__ static void unpack(const Raw& u, float* f) {
+        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+        for (int e = 0; e < N; ++e) f[e] = __bfloat162float(h[e]);
+    }
+};
+template <>
+struct Vec8<float> {
+    static constexpr int N = 4;
+    using Raw = uint4;
+    __device__ static void unpack(const Raw& u, float* f) {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y); f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    }
+};
+
+template <int N>
+__device__ __forceinline__ void store_f32(float* p, const float (&f)[N]) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < N; e += 4) *reinterpret_cast<float4*>(p + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+    } else {
+        static_assert(N == 2, "two or a multiple of four values");
+        *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
+    }
+}
 
 template <int DV, typename T>
 __global__ void __launch_bounds__(32 * kWarps)
 output_gate_bwd_kernel(const T* __restrict__ o_in, const T* __restrict__ z, const float* __restrict__ w, float eps,
                        const T* __restrict__ dy_in, float* __restrict__ d_o, float* __restrict__ d_z,
                        float* __restrict__ partial, long long rows) {
-    constexpr int VEC = Vec16<T>::N;
+    constexpr int VEC = Vec8<T>::N;
     constexpr int LPR = DV / VEC;          // lanes per row
     constexpr int RPW = 32 / LPR;          // rows per warp and pass
     constexpr int THREADS = 32 * kWarps;
+    static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must split evenly over a warp");
     __shared__ float red[THREADS][VEC + 1];
     const int tid = threadIdx.x, lane = tid & 31, sub = lane % LPR;
     float wv[VEC], acc[VEC];
@@ -120,31 +155,37 @@ output_gate_bwd_kernel(const T* __restrict__ o_in, const T* __restrict__ z, cons
         acc[e] = 0.f;
     }
     const long long rows_per_pass = (long long)gridDim.x * kWarps * RPW;
-    for (long long row = ((long long)blockIdx.x * kWarps + (tid >> 5)) * RPW + lane / LPR; row - lane / LPR < rows;
-         row += rows_per_pass) {
+    long long row = ((long long)blockIdx.x * kWarps + (tid >> 5)) * RPW + lane / LPR;
+    using Raw = typename Vec8<T>::Raw;
+    const auto fetch = [&](long long r, Raw& ro, Raw& rz, Raw& rd) {
+        if (r < rows) {
+            const size_t off = (size_t)r * DV + sub * VEC;
+            ro = *reinterpret_cast<const Raw*>(o_in + off);
+            rz = *reinterpret_cast<const Raw*>(z + off);
+            rd = *reinterpret_cast<const Raw*>(dy_in + off);
+        }
+    };
+    Raw no{}, nz{}, nd{};
+    fetch(row, no, nz, nd);
+    for (; row - lane / LPR < rows; row += rows_per_pass) {   // warp-uniform: the warp's first row
         const bool ok = row < rows;
         float o[VEC], zz[VEC], dy[VEC];
+        Vec8<T>::unpack(no, o);
+        Vec8<T>::unpack(nz, zz);
+        Vec8<T>::unpack(nd, dy);
+        fetch(row + rows_per_pass, no, nz, nd);   // the next pass's rows, while this one computes
         float ss = 0.f;
-        if (ok) {
-            Vec16<T>::load(o_in + row * DV + sub * VEC, o);
-            Vec16<T>::load(z + row * DV + sub * VEC, zz);
-            Vec16<T>::load(dy_in + row * DV + sub * VEC, dy);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) ss = fmaf(o[e], o[e], ss);
-        }
+        for (int e = 0; e < VEC; ++e) ss = fmaf(o[e], o[e], ss);
 #pragma unroll
         for (int m = LPR / 2; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
         const float inv = rsqrtf(ss / (float)DV + eps);
-        float gy[VEC], oh[VEC], sg[VEC], dot = 0.f;
-        if (ok) {
+        float gy[VEC], dot = 0.f;
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float sig = 1.f / (1.f + __expf(-zz[e]));
-                sg[e] = sig;
-                oh[e] = o[e] * inv;
-                gy[e] = dy[e] * wv[e] * zz[e] * sig;
-                dot = fmaf(gy[e], oh[e], dot);
-            }
+        for (int e = 0; e < VEC; ++e) {
+            const float sig = 1.f / (1.f + __expf(-zz[e]));
+            gy[e] = dy[e] * wv[e] * zz[e] * sig;
+            dot = fmaf(gy[e], o[e] * inv, dot);
         }
 #pragma unroll
         for (int m = LPR / 2; m > 0; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
@@ -153,16 +194,13 @@ output_gate_bwd_kernel(const T* __restrict__ o_in, const T* __restrict__ z, cons
         float rdo[VEC], rdz[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-            const float sig = sg[e], sz = zz[e] * sig;
-            rdo[e] = inv * (gy[e] - oh[e] * mdot);
-            rdz[e] = dy[e] * oh[e] * wv[e] * sig * (1.f + zz[e] * (1.f - sig));
-            acc[e] = fmaf(dy[e] * oh[e], sz, acc[e]);
+            const float sig = 1.f / (1.f + __expf(-zz[e])), oh = o[e] * inv;
+            rdo[e] = inv * (gy[e] - oh * mdot);
+            rdz[e] = dy[e] * oh * wv[e] * sig * (1.f + zz[e] * (1.f - sig));
+            acc[e] = fmaf(dy[e] * oh, zz[e] * sig, acc[e]);
         }
-#pragma unroll
-        for (int e = 0; e < VEC; e += 4) {
-            *reinterpret_cast<float4*>(d_o + row * DV + sub * VEC + e) = make_float4(rdo[e], rdo[e + 1], rdo[e + 2], rdo[e + 3]);
-            *reinterpret_cast<float4*>(d_z + row * DV + sub * VEC + e) = make_float4(rdz[e], rdz[e + 1], rdz[e + 2], rdz[e + 3]);
-        }
+        store_f32(d_o + row * DV + sub * VEC, rdo);
+        store_f32(d_z + row * DV + sub * VEC, rdz);
     }
 #pragma unroll
     for (int e = 0; e < VEC; ++e) red[tid][e] = acc[e];
@@ -176,17 +214,9 @@ output_gate_bwd_kernel(const T* __restrict__ o_in, const T* __restrict__ z, cons
     }
 }
 
-__global__ void gate_dw_reduce_kernel(const float* __restrict__ partial, int blocks, int dv, float* __restrict__ dw) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= dv) return;
-    float t = 0.f;
-    for (int b = 0; b < blocks; ++b) t += partial[(size_t)b * dv + c];
-    dw[c] = t;
-}
-
 template <int DV, typename T>
 int bwd_blocks(long long rows) {
-    constexpr int RPW = 32 / (DV / Vec16<T>::N);
+    constexpr int RPW = 32 / (DV / Vec8<T>::N);
     const long long per_block = (long long)kWarps * RPW;
     return (int)std::min<long long>(std::max<long long>((rows + per_block - 1) / per_block, 1), kBwdBlocksMax);
 }
@@ -197,7 +227,7 @@ cudaError_t launch_bwd_dv(const void* o, const void* z, const float* w, float ep
     const int blocks = bwd_blocks<DV, T>(rows);
     output_gate_bwd_kernel<DV, T><<<blocks, 32 * kWarps, 0, stream>>>(
         static_cast<const T*>(o), static_cast<const T*>(z), w, eps, static_cast<const T*>(dy), d_o, d_z, partial, rows);
-    if (d_w) gate_dw_reduce_kernel<<<(DV + 127) / 128, 128, 0, stream>>>(partial, blocks, DV, d_w);
+    if (d_w) column_sum_kernel<<<(DV + 31) / 32, kColSumThreads, 0, stream>>>(partial, blocks, DV, d_w);
     return cudaGetLastError();
 }
 
@@ -224,6 +254,24 @@ cudaError_t launch_output_gate_to(const void* in, void* out, const void* z, cons
     if (rows <= 0) return cudaSuccess;
     return dtype == GDN_BF16 ? launch_typed<__nv_bfloat16>(in, out, z, w, eps, rows, dv, stream)
                              : launch_typed<float>(in, out, z, w, eps, rows, dv, stream);
+}
+
+__global__ void __launch_bounds__(kColSumThreads)
+column_sum_kernel(const float* __restrict__ in, long long rows, int cols, float* __restrict__ out) {
+    __shared__ float red[32][33];
+    const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5, c = blockIdx.x * 32 + lane;
+    float t = 0.f;
+    if (c < cols) {
+#pragma unroll 4
+        for (long long r = grp; r < rows; r += 32) t += in[(size_t)r * cols + c];
+    }
+    red[grp][lane] = t;
+    __syncthreads();
+    for (int w = 16; w > 0; w >>= 1) {
+        if (grp < w) red[grp][lane] += red[grp + w][lane];
+        __syncthreads();
+    }
+    if (grp == 0 && c < cols) out[c] = red[0][lane];
 }
 
 size_t output_gate_bwd_workspace_bytes(long long rows, int dv) {

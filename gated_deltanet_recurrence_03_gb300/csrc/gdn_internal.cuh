@@ -180,6 +180,12 @@ bool tc_prefill_eligible(int dtype, int dk, int dv, int Hqk, int Hv, int chunk, 
 size_t tc_prefill_workspace_bytes(int B, int T, int Hv, int num_seqs, bool packed);
 cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_events);
 
+// out[c] = sum over r < rows of in[r * cols + c], for c < cols, in a fixed order (deterministic): each block
+// takes 32 columns; its 32 x 32 threads sum every 32nd row (warp-coalesced) and a shared-memory tree adds
+// the 32 partial sums.  Launch: grid ceil(cols / 32), block kColSumThreads.
+constexpr int kColSumThreads = 1024;
+__global__ void column_sum_kernel(const float* __restrict__ in, long long rows, int cols, float* __restrict__ out);
+
 // Set the calling thread's gdn_last_error() message.
 void set_error_message(const char* msg);
 // GDN_OK when the current device is an sm_103 GPU this library runs on; otherwise the status (and
