@@ -7,11 +7,9 @@
 //     dxp[p] = sum_j w[c, j] du_{p - j}     (the input at p feeds the outputs p - j, j < K)
 //     dw[c, j] = sum_t du_t xp[t + j]
 // and the outgoing cache (the last K - 1 rows of xp) passes its gradient straight to those rows.
-// One thread per (64-token slot of a sequence, 4-byte vector of channels): it slides a K-row window of
-// x and a K-entry ring of du over its tokens plus K - 1 on each side, the raw rows loaded three ahead (the du of the next slot's first
-// tokens are recomputed, so slots are independent), writes dx of its own tokens (and of the cached
-// inputs in a sequence's first slot) and its share of dw; column_sum_kernel adds the slots' shares in a
-// fixed order.
+// Each 64-token slot of a sequence (chunk c of sequence i in slot floor(start_i / 64) + i + c) is
+// handled with its K - 1 tokens of halo on each side, so slots are independent; the slots' shares of dw
+// are added by column_sum_kernel in a fixed order.
 #include <algorithm>
 
 #include "gdn_internal.cuh"
@@ -47,166 +45,206 @@ __device__ bool conv_slot(const int32_t* cu, int nseq, int T_len, long long slot
     return true;
 }
 
-// 4-byte vectors of channels (2 bf16 or 1 fp32): a warp covers 128 contiguous bytes of a row, and the
-// per-thread state fits 64 registers, four blocks of 256 threads per SM (measured on the 8k layer's
-// projection: 16-byte vectors 926 us, 8-byte 749-769 us, 4-byte 641 us, 4-byte at four blocks per SM
-// 519-521 us; five or more blocks per SM spill and run slower).
-constexpr int kVecBytes = 4;
-constexpr int kMinBlocks = 4;
-constexpr int kPrefetch = 3;   // rows of x and dy loaded ahead of the row being used
+// One block of 256 threads per (64-token slot, block of channels of 256 bytes a row: 128 bf16 or 64 fp32):
+//  1. the slot's x rows (its tokens with K - 1 before and after; cached inputs before the sequence, zeros
+//     past it) and dy rows (its tokens and K - 1 after) are copied to shared memory with 16-byte loads,
+//     whole rows per half-warp;
+//  2. du = dy silu'(u) for the slot's tokens and the K - 1 after, each thread a channel pair and every
+//     NG-th token, into shared memory in fp32; the thread's own tokens add to its taps' sums;
+//  3. dx of the slot's tokens (and of the cached inputs in a sequence's first slot) from K neighbouring
+//     du rows, written as whole fp32 rows;
+//  4. the taps' sums of the token groups are added in a fixed order into the slot's share of dw.
+// Every phase is parallel over tokens and channels, and the loads of a block are all in flight at once.
+constexpr int kTileRowBytes = 256;
 
 template <typename T>
-struct V4 {
-    static constexpr int N = kVecBytes / (int)sizeof(T);
-    using Raw = uint32_t;
-    __device__ static Raw raw(const T* p) { return *reinterpret_cast<const Raw*>(p); }
-    __device__ static void unpack(const Raw& u, float* f) {
-        const T* h = reinterpret_cast<const T*>(&u);
-#pragma unroll
-        for (int e = 0; e < N; ++e) f[e] = to_f32(h[e]);
-    }
-    __device__ static void load(const T* p, float* f) { unpack(raw(p), f); }
-};
-
-template <int N>
-__device__ __forceinline__ void store_f32(float* p, const float (&f)[N]) {
-    if constexpr (N % 4 == 0) {
-#pragma unroll
-        for (int e = 0; e < N; e += 4) *reinterpret_cast<float4*>(p + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
-    } else if constexpr (N == 2) {
-        *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
-    } else {
-        static_assert(N == 1, "one, two or a multiple of four channels");
-        p[0] = f[0];
-    }
+__device__ __forceinline__ float2 ld2(const T* p);
+template <>
+__device__ __forceinline__ float2 ld2<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+template <>
+__device__ __forceinline__ float2 ld2<float>(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
-conv_bwd_kernel(const T* __restrict__ x, long long xs, const float* __restrict__ w, const T* __restrict__ cache_in,
-                const T* __restrict__ dy, const T* __restrict__ dco, float* __restrict__ dx, float* __restrict__ dcache,
-                float* __restrict__ partial, const int32_t* __restrict__ cu, int nseq, int T_len, int C,
-                long long slots) {
-    constexpr int VEC = V4<T>::N;
-    const int NV = C / VEC;
-    const long long item = (long long)blockIdx.x * kThreads + threadIdx.x;
-    if (item >= slots * NV) return;
-    const long long slot = item / NV;
-    const int c0 = (int)(item % NV) * VEC;
-    float acc[VEC][K];
-#pragma unroll
-    for (int e = 0; e < VEC; ++e)
-#pragma unroll
-        for (int j = 0; j < K; ++j) acc[e][j] = 0.f;
-    float* part = partial ? partial + ((size_t)slot * C + c0) * K : nullptr;
+__global__ void __launch_bounds__(kThreads)
+conv_bwd_tile_kernel(const T* __restrict__ x, long long xs, const float* __restrict__ w, const T* __restrict__ cache_in,
+                     const T* __restrict__ dy, const T* __restrict__ dco, float* __restrict__ dx,
+                     float* __restrict__ dcache, float* __restrict__ partial, const int32_t* __restrict__ cu, int nseq,
+                     int T_len, int C) {
+    constexpr int CB = kTileRowBytes / (int)sizeof(T);   // channels of the block
+    constexpr int V16N = 16 / (int)sizeof(T);           // channels in 16 bytes
+    constexpr int VPR = CB / V16N;                      // 16-byte vectors a row (16)
+    constexpr int RX = kSlot + 2 * (K - 1), RD = kSlot + K - 1;
+    constexpr int P = CB / 2, NG = kThreads / P;        // channel pairs; token groups
+    extern __shared__ __align__(16) uint8_t smem[];
+    T* sx = reinterpret_cast<T*>(smem);                                  // [RX][CB]
+    T* sdy = sx + RX * CB;                                               // [RD][CB]
+    float* sdu = reinterpret_cast<float*>(sdy + RD * CB);                // [RD][CB]
+    const int tid = threadIdx.x;
+    const int nblk = (C + CB - 1) / CB;
+    const long long slot = blockIdx.x / nblk;
+    const int cb0 = (int)(blockIdx.x % nblk) * CB;
+    const int pr = tid % P, grp = tid / P, c = cb0 + 2 * pr;
+    const bool cok = c < C;
+    float* part = partial ? partial + ((size_t)slot * C + c) * K : nullptr;
     int seq, n;
     long long t0;
     if (!conv_slot(cu, nseq, T_len, slot, seq, t0, n)) {   // an unused slot adds nothing
-        if (!part) return;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-#pragma unroll
-            for (int j = 0; j < K; ++j) part[e * K + j] = 0.f;
+        if (part && cok)
+            for (int i = 0; i < 2 * K; ++i) part[i] = 0.f;
         return;
     }
     long long s0, s1;
     seq_range(cu, seq, T_len, s0, s1);
-    float wv[VEC][K];
+    // 1. rows to shared memory: every load of the thread issued before the first store
+    // thread tid moves 16-byte piece q = tid % VPR of rows tid / VPR, + kThreads / VPR, ...
+    constexpr int RPP = kThreads / VPR, NLD = (RX + RD + RPP - 1) / RPP;
+    static_assert(kThreads % VPR == 0, "whole rows per pass");
+    const int q = tid % VPR, rb = tid / VPR, cc = cb0 + q * V16N;
+    const bool qok = cc < C;
+    const int xlo = (int)(s0 - (t0 - (K - 1))), xhi = (int)min((long long)RX, s1 - (t0 - (K - 1)));   // x rows [xlo, xhi) are inputs
+    const int dhi = (int)min((long long)RD, s1 - t0);                                                   // dy rows [0, dhi)
+    // element offsets of row 0 (formed into pointers only for rows that exist): x row r is token
+    // t0 - (K - 1) + r; before the sequence it is cache row r - xlo + K - 1 (only in a first slot, xlo > 0)
+    const long long xoff0 = (t0 - (K - 1)) * xs + cc;
+    const long long coff0 = ((long long)seq * (K - 1) + (K - 1) - xlo) * C + cc;
+    const long long doff0 = t0 * (long long)C + cc;
+    uint4 v[NLD];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e)
-#pragma unroll
-        for (int j = 0; j < K; ++j) wv[e][j] = w[(size_t)(c0 + e) * K + j];
-    // the raw bytes of the x row (an input, a cached input before the sequence, or zero past its end) and
-    // of the dy row (zero outside this slot's tokens and halo, and past the sequence) of token tt
-    using Raw = typename V4<T>::Raw;
-    const auto fetch = [&](long long tt, Raw& rx, Raw& rd) {
-        rx = 0u;
-        rd = 0u;
-        if (tt < s1) {
-            if (tt >= s0)
-                rx = V4<T>::raw(x + tt * xs + c0);
-            else if (cache_in)
-                rx = V4<T>::raw(cache_in + ((size_t)seq * (K - 1) + (size_t)(tt - s0 + K - 1)) * C + c0);
-            if (tt >= t0) rd = V4<T>::raw(dy + tt * (long long)C + c0);
-        }
-    };
-    float xw[K][VEC], dr[K][VEC];   // x rows t - K + 1 .. t (oldest first); du_{t - K + 1} .. du_t
-#pragma unroll
-    for (int j = 0; j < K; ++j)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) xw[j][e] = dr[j][e] = 0.f;
-    const long long t_begin = t0 - (K - 1), t_end = t0 + n + K - 1;   // last du needed: token t0 + n + K - 2
-    Raw qx[kPrefetch], qd[kPrefetch];   // rows t .. t + kPrefetch - 1, loaded ahead
-#pragma unroll
-    for (int i = 0; i < kPrefetch; ++i) fetch(t_begin + i < t_end ? t_begin + i : s1, qx[i], qd[i]);
-    for (long long t = t_begin; t < t_end; ++t) {
-        const Raw rx = qx[0], rd = qd[0];
-#pragma unroll
-        for (int i = 0; i + 1 < kPrefetch; ++i) {
-            qx[i] = qx[i + 1];
-            qd[i] = qd[i + 1];
-        }
-        fetch(t + kPrefetch < t_end ? t + kPrefetch : s1, qx[kPrefetch - 1], qd[kPrefetch - 1]);
-#pragma unroll
-        for (int j = 0; j + 1 < K; ++j)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                xw[j][e] = xw[j + 1][e];
-                dr[j][e] = dr[j + 1][e];
+    for (int k = 0; k < NLD; ++k) {
+        const int r = rb + k * RPP;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (qok && r < RX + RD) {
+            if (r < RX) {
+                if (r >= xlo && r < xhi)
+                    v[k] = *reinterpret_cast<const uint4*>(x + (xoff0 + (long long)r * xs));
+                else if (r < xlo && cache_in)
+                    v[k] = *reinterpret_cast<const uint4*>(cache_in + (coff0 + (long long)r * C));
+            } else if (r - RX < dhi) {
+                v[k] = *reinterpret_cast<const uint4*>(dy + (doff0 + (long long)(r - RX) * C));
             }
-        V4<T>::unpack(rx, xw[K - 1]);
-        float* d = dr[K - 1];
-        if (t >= t0 && t < s1) {   // du_t = dy_t silu'(u_t); this slot's own tokens add to dw
-            float g[VEC];
-            V4<T>::unpack(rd, g);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                float u = 0.f;
-#pragma unroll
-                for (int j = 0; j < K; ++j) u = fmaf(wv[e][j], xw[j][e], u);
-                const float sg = 1.f / (1.f + __expf(-u));
-                d[e] = g[e] * sg * (1.f + u * (1.f - sg));
-            }
-            if (t < t0 + n) {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e)
-#pragma unroll
-                    for (int j = 0; j < K; ++j) acc[e][j] = fmaf(d[e], xw[j][e], acc[e][j]);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) d[e] = 0.f;
-        }
-        // the input at p = t - (K - 1) feeds the outputs p .. t: its gradient is complete now
-        const long long p = t - (K - 1);
-        const bool own = p >= t0 && p < t0 + n;
-        const bool cached = K > 1 && dcache && t0 == s0 && p < s0 && p >= s0 - (K - 1);   // first slot: the cache
-        if (own || cached) {
-            float gx[VEC];
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                float acc_x = 0.f;
-#pragma unroll
-                for (int j = 0; j < K; ++j) acc_x = fmaf(wv[e][j], dr[K - 1 - j][e], acc_x);
-                gx[e] = acc_x;
-            }
-            if (dco && p >= s1 - (K - 1)) {   // the outgoing cache holds this input
-                float gc[VEC];
-                V4<T>::load(dco + ((size_t)seq * (K - 1) + (size_t)(p - (s1 - (K - 1)))) * C + c0, gc);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) gx[e] += gc[e];
-            }
-            if (own)
-                store_f32(dx + p * (long long)C + c0, gx);
-            else
-                store_f32(dcache + ((size_t)seq * (K - 1) + (size_t)(p - s0 + K - 1)) * C + c0, gx);
         }
     }
-    if (!part) return;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e)
+    for (int k = 0; k < NLD; ++k) {
+        const int r = rb + k * RPP;
+        if (r < RX + RD) *reinterpret_cast<uint4*>((r < RX ? sx + r * CB : sdy + (r - RX) * CB) + q * V16N) = v[k];
+    }
+    float wv[2][K], acc[2][K];
 #pragma unroll
-        for (int j = 0; j < K; ++j) part[e * K + j] = acc[e][j];
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            wv[e][j] = cok ? w[(size_t)(c + e) * K + j] : 0.f;
+            acc[e][j] = 0.f;
+        }
+    __syncthreads();
+    // 2. du of the slot's tokens and the K - 1 after (zero past the sequence): each thread a channel pair
+    //    and a run of consecutive tokens, the K x rows of a token sliding through registers
+    constexpr int LR = (RD + NG - 1) / NG;          // tokens of a run
+    const int nd = (int)min((long long)RD, s1 - t0);   // tokens with a du (the rest are past the sequence)
+    {
+        const int r0 = grp * LR;
+        float2 xw[K];
+#pragma unroll
+        for (int j = 0; j + 1 < K; ++j) xw[j + 1] = ld2<T>(sx + (r0 + j) * CB + 2 * pr);
+#pragma unroll
+        for (int i = 0; i < LR; ++i) {
+            const int r = r0 + i;
+            if (r >= RD) break;
+#pragma unroll
+            for (int j = 0; j + 1 < K; ++j) xw[j] = xw[j + 1];
+            xw[K - 1] = ld2<T>(sx + (r + K - 1) * CB + 2 * pr);
+            float2 d = make_float2(0.f, 0.f);
+            if (r < nd) {
+                const float2 g = ld2<T>(sdy + r * CB + 2 * pr);
+                float u0 = 0.f, u1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    u0 = fmaf(wv[0][j], xw[j].x, u0);
+                    u1 = fmaf(wv[1][j], xw[j].y, u1);
+                }
+                // sigmoid by the fast reciprocal; the clamp keeps 1 + e^-u finite and the result normal
+                const float g0 = __fdividef(1.f, 1.f + __expf(fminf(-u0, 80.f)));
+                const float g1 = __fdividef(1.f, 1.f + __expf(fminf(-u1, 80.f)));
+                d = make_float2(g.x * g0 * (1.f + u0 * (1.f - g0)), g.y * g1 * (1.f + u1 * (1.f - g1)));
+                if (r < n) {
+#pragma unroll
+                    for (int j = 0; j < K; ++j) {
+                        acc[0][j] = fmaf(d.x, xw[j].x, acc[0][j]);
+                        acc[1][j] = fmaf(d.y, xw[j].y, acc[1][j]);
+                    }
+                }
+            }
+            *reinterpret_cast<float2*>(sdu + r * CB + 2 * pr) = d;
+        }
+    }
+    __syncthreads();
+    // 3. dx of the slot's tokens, and of the cached inputs in a sequence's first slot: each thread a run of
+    //    consecutive positions, the K du rows sliding through registers
+    const int r_lo = (K > 1 && dcache && t0 == s0) ? -(K - 1) : 0;
+    constexpr int LP = (kSlot + K - 1 + NG - 1) / NG;   // positions of a run (at most 64 + K - 1)
+    // first position (relative to t0) that the outgoing cache holds; beyond any position of the slot if later
+    const int dco_from = (int)min(s1 - (K - 1) - t0, (long long)kSlot);
+    if (cok) {
+        const int q0 = r_lo + grp * LP;
+        float2 dw_[K];   // du rows q .. q + K - 1 (zero before the slot)
+#pragma unroll
+        for (int j = 0; j + 1 < K; ++j) {
+            const int rd = q0 + j;
+            dw_[j + 1] = rd >= 0 ? *reinterpret_cast<const float2*>(sdu + rd * CB + 2 * pr) : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < LP; ++i) {
+            const int r = q0 + i;
+            if (r >= n) break;
+#pragma unroll
+            for (int j = 0; j + 1 < K; ++j) dw_[j] = dw_[j + 1];
+            const int rd = r + K - 1;
+            dw_[K - 1] = rd >= 0 ? *reinterpret_cast<const float2*>(sdu + rd * CB + 2 * pr) : make_float2(0.f, 0.f);
+            float2 gx = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {   // du of token p + K - 1 - j is dw_[K - 1 - j]
+                gx.x = fmaf(wv[0][j], dw_[K - 1 - j].x, gx.x);
+                gx.y = fmaf(wv[1][j], dw_[K - 1 - j].y, gx.y);
+            }
+            const long long p = t0 + r;
+            if (dco && r >= dco_from) {   // the outgoing cache holds this input
+                const float2 gc = ld2<T>(dco + ((size_t)seq * (K - 1) + (size_t)(r - dco_from)) * C + c);
+                gx.x += gc.x;
+                gx.y += gc.y;
+            }
+            float* dst = r >= 0 ? dx + p * (long long)C + c
+                                : dcache + ((size_t)seq * (K - 1) + (size_t)(r + K - 1)) * C + c;
+            *reinterpret_cast<float2*>(dst) = gx;
+        }
+    }
+    // 4. the token groups' tap sums, added in group order
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(smem);   // [NG][P][2K] over the staged rows
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int j = 0; j < K; ++j) red[(grp * P + pr) * 2 * K + e * K + j] = acc[e][j];
+    __syncthreads();
+    if (part && grp == 0 && cok) {
+#pragma unroll
+        for (int i = 0; i < 2 * K; ++i) {
+            float t = 0.f;
+            for (int g = 0; g < NG; ++g) t += red[(g * P + pr) * 2 * K + i];
+            part[i] = t;   // channel c + i / K, tap i % K: [c][K] then [c + 1][K]
+        }
+    }
+}
+
+template <typename T, int K>
+constexpr size_t tile_smem_bytes() {
+    constexpr int CB = kTileRowBytes / (int)sizeof(T);
+    return (size_t)(kSlot + 2 * (K - 1)) * kTileRowBytes + (size_t)(kSlot + K - 1) * kTileRowBytes +
+           (size_t)(kSlot + K - 1) * CB * sizeof(float);
 }
 
 // Sequences without tokens: the outgoing cache is the incoming one, so its gradient passes through.
@@ -231,15 +269,19 @@ long long conv_slots(const ConvArgs& a) {
 template <typename T, int K>
 cudaError_t launch_k(const ConvArgs& a, const void* dy, const void* dco, float* dx, float* dw, float* dcache,
                      float* partial) {
-    constexpr int VEC = V4<T>::N;
     const long long slots = conv_slots(a);
-    const long long items = slots * (a.C / VEC);
     const int T_len = a.T;
     const int32_t* cu = a.packed ? a.cu_seqlens : nullptr;
-    if (items > 0)
-        conv_bwd_kernel<T, K><<<(unsigned)((items + kThreads - 1) / kThreads), kThreads, 0, a.stream>>>(
+    constexpr size_t smem = tile_smem_bytes<T, K>();
+    const long long blocks = slots * ((a.C + kTileRowBytes / (int)sizeof(T) - 1) / (kTileRowBytes / (int)sizeof(T)));
+    if (blocks > 0) {
+        cudaError_t e = cudaFuncSetAttribute(conv_bwd_tile_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        conv_bwd_tile_kernel<T, K><<<(unsigned)blocks, kThreads, smem, a.stream>>>(
             static_cast<const T*>(a.x), a.x_stride, a.w, static_cast<const T*>(a.cache_in), static_cast<const T*>(dy),
-            static_cast<const T*>(dco), dx, dcache, partial, cu, a.num_seqs, T_len, a.C, slots);
+            static_cast<const T*>(dco), dx, dcache, partial, cu, a.num_seqs, T_len, a.C);
+    }
     if (K > 1 && dcache) {
         const long long n = (long long)(K - 1) * a.C * a.num_seqs;
         conv_bwd_empty_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, a.stream>>>(static_cast<const T*>(dco), dcache, cu,

@@ -180,11 +180,12 @@ output_gate_bwd_kernel(const T* __restrict__ o_in, const T* __restrict__ z, cons
 #pragma unroll
         for (int m = LPR / 2; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
         const float inv = rsqrtf(ss / (float)DV + eps);
-        float gy[VEC], dot = 0.f;
+        float gy[VEC], sg[VEC], dot = 0.f;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-            const float sig = 1.f / (1.f + __expf(-zz[e]));
-            gy[e] = dy[e] * wv[e] * zz[e] * sig;
+            // sigmoid by the fast reciprocal; the clamp keeps 1 + e^-z finite and the result normal
+            sg[e] = __fdividef(1.f, 1.f + __expf(fminf(-zz[e], 80.f)));
+            gy[e] = dy[e] * wv[e] * zz[e] * sg[e];
             dot = fmaf(gy[e], o[e] * inv, dot);
         }
 #pragma unroll
@@ -194,7 +195,7 @@ output_gate_bwd_kernel(const T* __restrict__ o_in, const T* __restrict__ z, cons
         float rdo[VEC], rdz[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-            const float sig = 1.f / (1.f + __expf(-zz[e])), oh = o[e] * inv;
+            const float sig = sg[e], oh = o[e] * inv;
             rdo[e] = inv * (gy[e] - oh * mdot);
             rdz[e] = dy[e] * oh * wv[e] * sig * (1.f + zz[e] * (1.f - sig));
             acc[e] = fmaf(dy[e] * oh, zz[e] * sig, acc[e]);
