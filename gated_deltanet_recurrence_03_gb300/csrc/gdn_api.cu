@@ -462,8 +462,9 @@ size_t gdn_recurrent_bwd_workspace_size(int B, int T, int Hqk, int Hv, int dk, i
     const bool packed = o.cu_seqlens != nullptr;
     const int nseq = packed ? o.num_seqs : B;
     if (nseq <= 0) return 0;
-    size_t bytes = backward_layout(B, T, Hv, dk, dv, nseq, packed, true).total;
-    if (o.flags & (GDN_NORMALIZE_QK | GDN_RAW_GATES))
+    const bool front_end = (o.flags & (GDN_NORMALIZE_QK | GDN_RAW_GATES)) != 0;
+    size_t bytes = backward_layout(B, T, Hv, dk, dv, nseq, packed, true, front_end).total;
+    if (front_end)
         bytes = ((bytes + 255) & ~(size_t)255) + frontend_backward_bytes(B, T, Hqk, Hv, dk, dv, packed);
     return bytes;
 }
@@ -499,7 +500,7 @@ gdn_status_t gdn_recurrent_bwd(const void* q, const void* k, const void* v, cons
     for (const void* p : f_ptrs)
         if (p && !aligned_to(p, 4)) return fail(GDN_ERR_INVALID_ARG, "pointer %p not 4-byte aligned", p);
     if (nseq == 0) return GDN_OK;
-    const size_t core = backward_layout(B, T, Hv, dk, dv, nseq, packed, true).total;
+    const size_t core = backward_layout(B, T, Hv, dk, dv, nseq, packed, true, front_end).total;
     const size_t need =
         front_end ? ((core + 255) & ~(size_t)255) + frontend_backward_bytes(B, T, Hqk, Hv, dk, dv, packed) : core;
     if (!o.workspace || o.workspace_bytes < need)

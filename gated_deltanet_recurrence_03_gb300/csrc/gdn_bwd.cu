@@ -1296,6 +1296,8 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     ws.S = reinterpret_cast<float*>(base + Lw.S_off);
     ws.dS = reinterpret_cast<float*>(base + Lw.dS_off);
     ws.dU = reinterpret_cast<float*>(base + Lw.dU_off);
+    const bool front_end = (a.flags & (GDN_NORMALIZE_QK | GDN_RAW_GATES)) != 0;
+    ws.R = front_end ? reinterpret_cast<float*>(base + Lw.R_off) : nullptr;
     const TT* q = static_cast<const TT*>(a.q);
     const TT* k = static_cast<const TT*>(a.k);
     const TT* v = static_cast<const TT*>(a.v);
@@ -1321,18 +1323,22 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     if ((e = set_smem(bwd_state_adj_kernel<TT, DK, DV>, S2::BYTES)) != cudaSuccess) return e;
     if ((e = set_smem(bwd_local_kernel<TT, DK, DV>, S4::BYTES)) != cudaSuccess) return e;
 
+    // With the front end (only for bf16, dk = dv = 128: the caller checks), the WY kernel and the chains take
+    // the raw inputs with the l2 scalars and the gates inside; the chunk-local kernel runs in fp32 below.
+    const bool normalize = (a.flags & GDN_NORMALIZE_QK) != 0;
+    const float* A_log = (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr;
     bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
-        q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec, nullptr, nullptr, false);
+        q, k, v, g, beta, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec, A_log, a.dt_bias, normalize);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark(1);
     // the forward chain: on the tcgen05 tensor cores for bf16 inputs with dk = dv = 128 (16-byte aligned k)
     e = cudaErrorNotSupported;
     if constexpr (sizeof(TT) == 2 && DK == 128 && DV == 128)
-        e = launch_bwd_state_fwd_tc(a.k, a.S0, nullptr, ws.W, ws.U, ws.G, ws.S, nullptr, a.T, a.Hqk, a.Hv,
-                                    a.cu_seqlens, a.num_seqs, false, a.stream, a.status);
+        e = launch_bwd_state_fwd_tc(a.k, a.S0, nullptr, ws.W, ws.U, ws.G, ws.S, normalize ? ws.R : nullptr, a.T, a.Hqk,
+                                    a.Hv, a.cu_seqlens, a.num_seqs, normalize, a.stream, a.status);
     if (e == cudaErrorNotSupported)
         bwd_state_fwd_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
-            k, a.S0, nullptr, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, vec, false);
+            k, a.S0, nullptr, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, vec, normalize);
     else if (e != cudaSuccess)
         return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1341,7 +1347,9 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     e = cudaErrorNotSupported;
     if constexpr (sizeof(TT) == 2 && DK == 128 && DV == 128)
         e = launch_bwd_state_adj_tc(a.q, a.k, a.dout, a.dS_final, a.grad_S0, ws.W, ws.P, ws.G, ws.dS, ws.dU, a.T, a.Hqk,
-                                    a.Hv, a.cu_seqlens, a.num_seqs, a.scale, a.stream, a.status);
+                                    a.Hv, a.cu_seqlens, a.num_seqs, a.scale, a.stream, a.status,
+                                    normalize ? ws.R : nullptr, normalize);
+    if (e == cudaErrorNotSupported && front_end) return e;   // the general adjoint chain has no front end
     if (e == cudaErrorNotSupported)
         bwd_state_adj_kernel<TT, DK, DV><<<nst, kStThreads, S2::BYTES, a.stream>>>(
             q, k, dout, a.dS_final, a.grad_S0, ws, a.T, a.Hqk, a.Hv, a.cu_seqlens, a.num_seqs, a.scale, vec);
@@ -1349,9 +1357,17 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
         return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark(3);
-    bwd_local_kernel<TT, DK, DV><<<chunk_grid, kLoThreads, S4::BYTES, a.stream>>>(
-        q, k, v, beta, dout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk, a.Hv,
-        a.cu_seqlens, a.num_seqs, a.scale, vec);
+    if (front_end) {   // fp32 on the front end's outputs, with the workspace the front-end kernels above filled
+        using S4f = LoSmem<DK, DV>;
+        if ((e = set_smem(bwd_local_kernel<float, DK, DV>, S4f::BYTES)) != cudaSuccess) return e;
+        bwd_local_kernel<float, DK, DV><<<chunk_grid, kLoThreads, S4f::BYTES, a.stream>>>(
+            a.lq, a.lk, a.lv, a.lbeta, a.ldout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk,
+            a.Hv, a.cu_seqlens, a.num_seqs, a.scale, true);
+    } else {
+        bwd_local_kernel<TT, DK, DV><<<chunk_grid, kLoThreads, S4::BYTES, a.stream>>>(
+            q, k, v, beta, dout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk, a.Hv,
+            a.cu_seqlens, a.num_seqs, a.scale, vec);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark(4);
     return cudaSuccess;
@@ -1379,7 +1395,7 @@ cudaError_t launch_dtype(const BackwardArgs& a, const BwdLayout& L) {
 
 }  // namespace
 
-BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed, bool adjoint) {
+BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed, bool adjoint, bool with_r) {
     const long long ttot = packed ? (long long)T : (long long)B * T;
     BwdLayout L{};
     L.slots = (ttot + kC - 1) / kC + nseq;
@@ -1398,6 +1414,7 @@ BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool p
     if (adjoint) {
         take(L.dS_off, (size_t)dk * dv);
         take(L.dU_off, (size_t)kC * dv);
+        if (with_r) take(L.R_off, (size_t)2 * kC);   // the front end's per-row l2 scalars
     } else {
         take(L.R_off, (size_t)2 * kC);   // the prefill front end's per-row l2 scalars
     }
@@ -1415,7 +1432,8 @@ cudaError_t launch_chunked_prefill(const PrefillArgs& a) {
 }
 
 cudaError_t launch_backward(const BackwardArgs& a) {
-    const BwdLayout L = backward_layout(a.B, a.T, a.Hv, a.dk, a.dv, a.num_seqs, a.cu_seqlens != nullptr, true);
+    const bool front_end = (a.flags & (GDN_NORMALIZE_QK | GDN_RAW_GATES)) != 0;
+    const BwdLayout L = backward_layout(a.B, a.T, a.Hv, a.dk, a.dv, a.num_seqs, a.cu_seqlens != nullptr, true, front_end);
     return a.dtype == GDN_BF16 ? launch_dtype<__nv_bfloat16>(a, L) : launch_dtype<float>(a, L);
 }
 

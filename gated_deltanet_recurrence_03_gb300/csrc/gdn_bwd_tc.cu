@@ -467,7 +467,7 @@ bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
                         const __grid_constant__ CUtensorMap tm_ds, const float* __restrict__ ws_G,
                         const float* __restrict__ dS_final, float* __restrict__ grad_S0, float* __restrict__ ws_dS,
                         int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu, int nseq, float scale,
-                        unsigned* status) {
+                        unsigned* status, const float* __restrict__ ws_R, int normalize) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
@@ -534,12 +534,14 @@ bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
     auto load_st = [&](long long c) {   // Q tile, W, P, G of chunk c
         if (!waits_ok) return;
         const int tc0 = (int)(t0 + c * kC);
-        mbar_arrive_expect_tx(bar_st, 16384 + 32768 + 16384 + 256);
+        mbar_arrive_expect_tx(bar_st, 16384 + 32768 + 16384 + 256 + (normalize ? 512 : 0));
         tma_load_3d(sb + A_QT, &tm_q, 0, hk, tc0, bar_st);
         tma_load_3d(sb + A_QT + 8192, &tm_q, 64, hk, tc0, bar_st);
         for (int p = 0; p < 4; ++p) tma_load_2d(sb + A_WST + p * 8192, &tm_w, 32 * p, (int)(wi(c) * kC), bar_st);
         for (int p = 0; p < 2; ++p) tma_load_2d(sb + A_PST + p * 8192, &tm_p, 32 * p, (int)(wi(c) * kC), bar_st);
         bulk_g2s(sb + A_GST, ws_G + wi(c) * kC, 256, bar_st);
+        // with in-kernel l2 normalisation: the rows' scalars 1/|k| (64) and 1/|q| (64) after G
+        if (normalize) bulk_g2s(sb + A_GST + 256, ws_R + wi(c) * 2 * kC, 512, bar_st);
         issued[2] += 1;
     };
     const float* sG = reinterpret_cast<const float*>(sm + A_GST);
@@ -687,6 +689,7 @@ bwd_state_adj_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
                 put_a();
                 if (R < 64) b = __expf(sG[kC - 1] - sG[R]);
                 else b = (R - 64) < n ? scale * __expf(sG[R - 64]) : 0.f;
+                if (normalize) b *= sG[kC + R];   // K -> diag(1/|k|) K for rows R < 64, Q likewise for the rest
                 tmem_wait_st();
                 tc_fence_before();
                 nb_arrive(2, kThreads);
@@ -854,9 +857,11 @@ namespace gdn {
 cudaError_t launch_bwd_state_adj_tc(const void* q, const void* k, const void* dout, const float* dS_final,
                                     float* grad_S0, const float* ws_W, const float* ws_P, const float* ws_G,
                                     float* ws_dS, float* ws_dU, int T, int Hqk, int Hv, const int32_t* cu, int nseq,
-                                    float scale, cudaStream_t stream, unsigned* status) {
+                                    float scale, cudaStream_t stream, unsigned* status, const float* ws_R,
+                                    bool normalize) {
     const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (!al16(q) || !al16(k) || !al16(dout)) return cudaErrorNotSupported;
+    if (normalize && !ws_R) return cudaErrorInvalidValue;
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
     if (!encode) return cudaErrorNotSupported;
     const long long tokens = cu ? (long long)T : (long long)nseq * T;
@@ -893,7 +898,7 @@ cudaError_t launch_bwd_state_adj_tc(const void* q, const void* k, const void* do
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((long long)nseq * Hv * kSlices);
     bwd_state_adj_tc_kernel<<<grid, kThreads, A_SMEM, stream>>>(tk, tq, to, tw, tp, tdu, tds, ws_G, dS_final, grad_S0, ws_dS,
-                                                                T, Hqk, Hv, cu, nseq, scale, status);
+                                                                T, Hqk, Hv, cu, nseq, scale, status, ws_R, normalize ? 1 : 0);
     return cudaGetLastError();
 }
 

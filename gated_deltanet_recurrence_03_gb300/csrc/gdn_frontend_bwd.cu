@@ -6,9 +6,11 @@
 //     beta = sigmoid(b)                                       db = dbeta beta (1 - beta)
 //     dA_log = sum over tokens of dg g,  d dt_bias = sum over tokens of da   (per value head)
 // Around the recurrence's own backward: a pre-pass writes the front end's outputs (normalised q, k,
-// the gates, and v, dout) as fp32 into the workspace, the recurrence's backward runs on them in fp32
-// (so that it differentiates the same fp32 values the forward kernels form in registers), and a
-// post-pass maps the gradients back in place.
+// the gates, and v, dout) as fp32 into the workspace, the recurrence's backward differentiates the
+// same fp32 values the forward kernels form in registers, and a post-pass maps the gradients back in
+// place.  For bf16 inputs with dk = dv = 128 the WY kernel and the two tcgen05 chains run on the raw
+// inputs with the front end inside (per-row l2 scalars, gates formed in fp32) and only the
+// chunk-local kernel reads the fp32 copies; other shapes run every kernel in fp32 on the copies.
 #include <algorithm>
 
 #include "gdn_internal.cuh"
@@ -189,9 +191,22 @@ cudaError_t run_frontend_backward(const BackwardArgs& in, unsigned flags, const 
         if (e != cudaSuccess) return e;
     }
     BackwardArgs a = in;
-    a.q = q32; a.k = k32; a.v = v32; a.dout = do32; a.g = g32; a.beta = b32;
-    a.dtype = GDN_F32;
-    cudaError_t e = launch_backward(a);
+    const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    cudaError_t e;
+    if (sizeof(TT) == 2 && in.dk == 128 && in.dv == 128 && al16(in.q) && al16(in.k) && al16(in.dout)) {
+        // bf16 at the tensor-core shape: the WY kernel and the two tcgen05 chains on the raw inputs with the
+        // front end inside, the chunk-local kernel in fp32 on the copies above
+        a.flags = flags;
+        a.A_log = A_log;
+        a.dt_bias = dt_bias;
+        a.lq = q32; a.lk = k32; a.lv = v32; a.lbeta = b32; a.ldout = do32;
+        e = launch_backward(a);
+    } else {   // every kernel in fp32 on the copies
+        a.q = q32; a.k = k32; a.v = v32; a.dout = do32; a.g = g32; a.beta = b32;
+        a.dtype = GDN_F32;
+        a.flags = 0;
+        e = launch_backward(a);
+    }
     if (e != cudaSuccess) return e;
     if (norm && ttot > 0) {
         const unsigned blocks = (unsigned)((qrows + kRowThreads / 32 - 1) / (kRowThreads / 32));

@@ -110,6 +110,18 @@ struct BackwardArgs {
     unsigned* status;           // device status word (bounded waits)
     void** events;              // optional: events[i] recorded after kernel i (1..4)
     int num_events;
+    // The fused front end (GDN_NORMALIZE_QK, GDN_RAW_GATES; 0 = none): g and beta then hold the raw a, b.
+    // bf16 inputs with dk = dv = 128 then run the WY kernel and the tcgen05 chains on the raw inputs with
+    // the front end inside (per-row l2 scalars, gates formed in fp32) and the chunk-local kernel in fp32
+    // on lq, lk (normalised q, k), lv, lbeta (formed beta) and ldout, fp32 copies the caller provides.
+    unsigned flags;
+    const float* A_log;
+    const float* dt_bias;
+    const float* lq;
+    const float* lk;
+    const float* lv;
+    const float* lbeta;
+    const float* ldout;
 };
 
 // Workspace of the backward pass: per (chunk slot, value head) fp32 arrays T, P (C x C), W (C x dk),
@@ -119,7 +131,9 @@ struct BwdLayout {
     long long slots;
     size_t T_off, P_off, W_off, U_off, G_off, S_off, dS_off, dU_off, R_off, total;
 };
-BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed, bool adjoint);
+// with_r: also the per-row l2 scalars (R) of the front end, next to the adjoint arrays.
+BwdLayout backward_layout(int B, int T, int Hv, int dk, int dv, int nseq, bool packed, bool adjoint,
+                          bool with_r = false);
 cudaError_t launch_backward(const BackwardArgs& a);
 // The backward through the fused front end (GDN_NORMALIZE_QK, GDN_RAW_GATES): fp32 copies of the front
 // end's outputs after the first core_bytes of a.workspace (frontend_backward_bytes more), the backward
@@ -142,7 +156,8 @@ cudaError_t launch_bwd_state_fwd_tc(const void* k, const float* S0, float* S_fin
 cudaError_t launch_bwd_state_adj_tc(const void* q, const void* k, const void* dout, const float* dS_final,
                                     float* grad_S0, const float* ws_W, const float* ws_P, const float* ws_G,
                                     float* ws_dS, float* ws_dU, int T, int Hqk, int Hv, const int32_t* cu, int nseq,
-                                    float scale, cudaStream_t stream, unsigned* status);
+                                    float scale, cudaStream_t stream, unsigned* status, const float* ws_R = nullptr,
+                                    bool normalize = false);
 // Chunked prefill for shapes outside the tensor-core path (fp32 inputs, head dims 32 / 64, front end
 // included): the backward's WY kernel and forward chain plus an output kernel.
 size_t chunked_prefill_workspace_bytes(int B, int T, int Hv, int dk, int dv, int nseq, bool packed);
