@@ -252,6 +252,9 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + P_BAR + 20);
     int* sFactor = reinterpret_cast<int*>(sm + P_BAR + 24);   // [2]: decay ratios factorise safely
     const uint32_t bar_drain = sb + P_BAR + 32;
+    // Once every CTA of this grid has started, the chain grid that follows may take the SMs that free
+    // up and run its set-up; it waits for this grid's completion before it reads the workspace.
+    griddep_launch_dependents();
 
     const int slot = blockIdx.x, pair = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -710,11 +713,21 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         mbar_init(bar_mma2, 1);
         mbar_fence_init();
     }
+    const size_t srow = (((size_t)i * Hv + h) * kD + R) * kD + 64 * z + cb;   // 32 floats of state row R
+    // S0 is an input: its rows are read while the prep grid may still be running.  Everything that
+    // reads the prep's workspace (or writes memory) comes after griddep_wait below.
+    uint32_t s0v[32];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+        const float4 x = (S0 && epi) ? *reinterpret_cast<const float4*>(S0 + srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        s0v[e] = __float_as_uint(x.x); s0v[e + 1] = __float_as_uint(x.y);
+        s0v[e + 2] = __float_as_uint(x.z); s0v[e + 3] = __float_as_uint(x.w);
+    }
     __syncthreads();
     tc_fence_after();
+    griddep_wait();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
-    const size_t srow = (((size_t)i * Hv + h) * kD + R) * kD + 64 * z + cb;   // 32 floats of state row R
 
     auto wait_a = [&](long long c) {
         return mbar_wait_bounded(bar_a0 + 8 * (uint32_t)(c & 1), (uint32_t)((c >> 1) & 1), abort_flag, status,
@@ -807,10 +820,10 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 
     if (nch == 0) {   // empty sequence: the final state is the initial state
         if (S_final && epi) {
-            for (int e = 0; e < 32; e += 4) {
-                const float4 v = S0 ? *reinterpret_cast<const float4*>(S0 + srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4*>(S_final + srow + e) = v;
-            }
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(S_final + srow + e) =
+                    make_float4(__uint_as_float(s0v[e]), __uint_as_float(s0v[e + 1]), __uint_as_float(s0v[e + 2]),
+                                __uint_as_float(s0v[e + 3]));
         }
     } else {
         if (tid == kIssuer) {
@@ -821,13 +834,7 @@ tc_chain_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         if (epi) {
             wait_k(0);
             const float g0 = reinterpret_cast<const float*>(sm + C_VEC)[64];   // vector of chunk 0 (K stage 0)
-            uint32_t v[32];
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-                const float4 x = S0 ? *reinterpret_cast<const float4*>(S0 + srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-                v[e] = __float_as_uint(x.x); v[e + 1] = __float_as_uint(x.y);
-                v[e + 2] = __float_as_uint(x.z); v[e + 3] = __float_as_uint(x.w);
-            }
+            uint32_t (&v)[32] = s0v;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const float* f = reinterpret_cast<const float*>(v + 8 * c);
@@ -1080,10 +1087,24 @@ cudaError_t launch_tc_prefill(const PrefillArgs& a, void** events, int num_event
         a.Hqk, a.Hv, a.scale, ws_a1, ws_vec, a.status, (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr, a.dt_bias,
         (a.flags & GDN_NORMALIZE_QK) ? 1 : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // The chain follows the prep with programmatic stream serialisation: its CTAs take the SMs freed by the
+    // prep's last wave and run their set-up there.  Not when an event is recorded between the two.
+    const bool mid_event = events && num_events > 1 && events[1];
     record_event(events, num_events, 1, a.stream);
-    tc_chain_kernel<<<(unsigned)((long long)a.num_seqs * a.Hv * kSlices), kChainThreads, C_SMEM, a.stream>>>(
-        tk, tv, to, ws_a1, ws_vec, a.S0, static_cast<bf16*>(a.out), a.S_final, a.cu_seqlens, a.num_seqs, T_len, a.Hqk,
-        a.Hv, (int)slots, a.status);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((long long)a.num_seqs * a.Hv * kSlices));
+    cfg.blockDim = dim3(kChainThreads);
+    cfg.dynamicSmemBytes = C_SMEM;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = mid_event ? 0 : 1;
+    e = cudaLaunchKernelEx(&cfg, tc_chain_kernel, tk, tv, to, (const uint8_t*)ws_a1, (const float*)ws_vec, a.S0,
+                           static_cast<bf16*>(a.out), a.S_final, a.cu_seqlens, a.num_seqs, T_len, a.Hqk, a.Hv,
+                           (int)slots, a.status);
+    if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     record_event(events, num_events, 2, a.stream);
     return cudaSuccess;
