@@ -39,19 +39,19 @@ __device__ __forceinline__ void tile_zero(float (&acc)[RM][CN]) {
 }
 
 // ---------------------------------------------------------------- tensor-core products in fp32 accuracy
-// mma.sync m16n8k8 with tf32 operands; each fp32 operand is split as x = hi + lo (hi = x rounded to
-// tf32, lo = the remainder rounded to tf32) and a b ~ hi_a hi_b + hi_a lo_b + lo_a hi_b, whose
-// dropped lo_a lo_b term is about 2^-22 of the product.  Fragment coordinates (g = lane / 4,
-// t = lane % 4): A (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4); B (k = t, n = g), (k = t + 4, n = g);
-// accumulator (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// mma.sync m16n8k8 with tf32 operands; each fp32 operand is split as x = hi + lo and
+// a b ~ hi_a hi_b + hi_a lo_b + lo_a hi_b (the error-corrected tf32 product of Ootomo and Yokota,
+// 2022).  hi is x rounded to tf32's 10 fraction bits, to nearest with ties away from zero, on the
+// bit pattern: half a tf32 ulp (bit 12) is added and the 13 low bits cleared, integer operations
+// only (a conversion instruction per element throttled the kernels).  lo = x - hi is exact in fp32
+// and at most half a tf32 ulp of x; it is passed as it is, and the tensor core reads its 19 high bits
+// (a truncation of at most 2^-10 of lo), so the error of hi + lo is below 2^-21 |x| and the dropped
+// lo_a lo_b term about 2^-22 of the product.  Fragment coordinates (g = lane / 4, t = lane % 4):
+// A (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4); B (k = t, n = g), (k = t + 4, n = g); accumulator
+// (g, 2t), (g, 2t + 1), (g + 8, 2t), (g + 8, 2t + 1).
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-    hi = to_tf32(x);
-    lo = to_tf32(x - __uint_as_float(hi));
+    hi = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
 }
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "

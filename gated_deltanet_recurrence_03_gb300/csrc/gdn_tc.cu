@@ -102,11 +102,9 @@ static_assert(P_SMEM <= 113 * 1024, "two CTAs per SM");
 
 __device__ __forceinline__ int lblk(int I, int J) { return I * (I + 1) / 2 + J; }   // J <= I
 
-__device__ __forceinline__ uint32_t tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// x rounded to tf32 (10 fraction bits), to nearest with ties away from zero, by integer operations on
+// its bit pattern: half a tf32 ulp (bit 12) is added to the magnitude and the 13 low bits cleared.
+__device__ __forceinline__ uint32_t tf32_rna(float x) { return (__float_as_uint(x) + 0x1000u) & 0xffffe000u; }
 
 __device__ __forceinline__ void mma_tf32_m16n8k8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
