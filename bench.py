@@ -670,9 +670,9 @@ def run_gpu(args):
                                       "unit": "TFLOP/s", "frac": round(bwd_tf / alu_peak, 4),
                                       "peak_source": "fp32 FMA lanes x 2 x 2070 MHz (unit counts)"}},
         "layer_backward": {"workload": "prefill_gqa_8k backward through the layer's other pieces: the recurrence's "
-                                       "backward with the fused front end (l2 norm of q, k and gates from raw a, b: the WY "
-                                       "kernel and the tcgen05 chains on the raw bf16 rows with in-kernel l2 scalars, the "
-                                       "chunk-local kernel on fp32 copies, the chain rule back), the output gate's backward (bf16 in, fp32 gradients) and the causal conv's "
+                                       "backward with the fused front end (l2 norm of q, k and gates from raw a, b: every "
+                                       "kernel on the raw bf16 rows with in-kernel l2 scalars and gates, the chain rule "
+                                       "back), the output gate's backward (bf16 in, fp32 gradients) and the causal conv's "
                                        "backward over the packed 8192-channel q/k/v projection (K=4)",
                            "front_end_backward_ms": round(fe_ms, 4),
                            "front_end_backward_tokens_per_s": round(world * tokens / (fe_ms / 1e3), 1),

@@ -149,6 +149,23 @@ __device__ __forceinline__ void mma_prod(float (&acc)[NT][4], const float* A, in
         }
     }
 }
+// The same with column k of A scaled by as[k] (A diag(as) B: a diagonal between the factors), A fp32.
+template <int NT, int K, bool AT, bool EB = false>
+__device__ __forceinline__ void mma_prod_as(float (&acc)[NT][4], const float* A, int lda, const float* as,
+                                            const float* B, int ldb, int row0, int nb0, int g, int t) {
+#pragma unroll 2
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t ah[4], al[4];
+        if (AT) frag_at_scaled(A, lda, as, row0, k0, g, t, ah, al);
+        else frag_a_scaled(A, lda, as, row0, k0, g, t, ah, al);
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            uint32_t bh[2], bl[2];
+            frag_b<EB>(B, ldb, 8 * (nb0 + q), k0, g, t, bh, bl);
+            mma_split<false, EB>(acc[q], ah, al, bh, bl);
+        }
+    }
+}
 // sign * (N accumulator fragments of rows row0 .. row0 + 15, n-tiles nb0 .. nb0 + N - 1) to D.
 template <int N>
 __device__ __forceinline__ void store_frag(float* D, int ld, const float (&f)[N][4], int row0, int nb0, int g, int t,
@@ -749,9 +766,9 @@ struct LoSmem {
     static constexpr int dU_ = 0, U_ = kC * LD, dO_ = 2 * kC * LD, V_ = 3 * kC * LD, S_ = 4 * kC * LD,
                          Lam_ = S_ + DK * LD, PS = Lam_ + DK * LD, DVB_END = DVB_ + 2 * PS, DW_END = DVB_ + kC * LK;
     static constexpr int VEC_ = DVB_END > DW_END ? DVB_END : DW_END;
-    // G, beta, dG, dbeta, row scratch, h, reduction scratch [8][C], warp sums
+    // G, beta, dG, dbeta, row scratch, h, the l2 scalars of K and Q rows, reduction scratch [8][C], warp sums
     static constexpr int G_ = VEC_, Beta_ = G_ + kC, dG_ = Beta_ + kC, dB_ = dG_ + kC, Row_ = dB_ + kC,
-                         H_ = Row_ + kC, Scr_ = H_ + kC, Red_ = Scr_ + 8 * kC;
+                         H_ = Row_ + kC, RK_ = H_ + kC, RQ_ = RK_ + kC, Scr_ = RQ_ + kC, Red_ = Scr_ + 8 * kC;
     static constexpr int FLOATS = Red_ + kLoThreads / 32;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
     static_assert(Q_ % 4 == 0 && KK_ % 4 == 0 && T_ % 4 == 0 && X_ % 4 == 0 && DVB_ % 4 == 0, "aligned regions");
@@ -820,7 +837,8 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                  const TT* __restrict__ beta, const TT* __restrict__ dout, Ws ws, float* __restrict__ grad_q,
                  float* __restrict__ grad_k, float* __restrict__ grad_v, float* __restrict__ grad_g,
                  float* __restrict__ grad_beta, int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu, int nseq,
-                 float scale, bool vec) {
+                 float scale, bool vec, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
+                 bool normalize) {
     using L = LoSmem<DK, DV>;
     using D = WsDims<DK, DV>;
     constexpr int NTW = DK / 32;   // n-tiles of 8 per warp of a C x dk product
@@ -839,6 +857,8 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
     float* sdB = sm + L::dB_;
     float* sRow = sm + L::Row_;
     float* sH = sm + L::H_;
+    float* sRK = sm + L::RK_;   // 1 / |k_r|, 1 / |q_r| with in-kernel normalisation, else 1
+    float* sRQ = sm + L::RQ_;
     float* sScr = sm + L::Scr_;
     float* sRed = sm + L::Red_;
 
@@ -853,13 +873,31 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 
     ld_in<TT, kC, DK, kLoThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
     ld_in<TT, kC, DK, kLoThreads>(sQ, L::LK, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+    if (tid < kC) {   // the WY kernel's l2 scalars (the same for every value head of this query/key head)
+        const size_t w0 = (size_t)slot * Hv + (size_t)hk * G;
+        sRK[tid] = normalize ? ws.R[w0 * D::R + tid] : 1.f;
+        sRQ[tid] = normalize ? ws.R[w0 * D::R + kC + tid] : 1.f;
+    }
     __syncthreads();
-    {   // Gram matrices K K^T and Q K^T (shared by the value heads)
+    // K and Q stay as loaded (exact for bf16 inputs); the normalised rows diag(rk) K and diag(rq) Q enter
+    // through the scalars: on the Gram entries, on the A columns of the products with K or Q as B, and on
+    // the row sums and the products' columns below.
+    {   // Gram matrices K_n K_n^T and Q_n K_n^T (shared by the value heads)
         float kk[2][4], qk[2][4];
         tile_zero(kk);
         tile_zero(qk);
         mma_prod<2, DK, false, true, kEx, kEx>(kk, sK, L::LK, sK, L::LK, row0, pb0, g, t);
         mma_prod<2, DK, false, true, kEx, kEx>(qk, sQ, L::LK, sK, L::LK, row0, pb0, g, t);
+        if (normalize) {
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = frow(row0, g, e), c = fcol(pb0 + qq, t, e);
+                    kk[qq][e] *= sRK[r] * sRK[c];
+                    qk[qq][e] *= sRQ[r] * sRK[c];
+                }
+        }
         store_frag<2>(sKK, kLCC, kk, row0, pb0, g, t, 1.f);
         store_frag<2>(sQK, kLCC, qk, row0, pb0, g, t, 1.f);
     }
@@ -870,7 +908,12 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
         ld_ws<kC, kC, kLoThreads>(sT, kLCC, ws.T + wi * D::T, kC, tid);
         if (tid < kC) {
             sG[tid] = ws.G[wi * D::G + tid];
-            sBeta[tid] = tid < n ? to_f32(beta[(tok0 + tid) * Hv + h]) : 0.f;
+            float bt = tid < n ? to_f32(beta[(tok0 + tid) * Hv + h]) : 0.f;
+            if (A_log && tid < n) {   // beta from the raw projection b, as the WY kernel forms it
+                float gt;
+                gates_from_raw(0.f, bt, A_log[h], dt_bias[h], gt, bt);
+            }
+            sBeta[tid] = bt;
             sdG[tid] = 0.f;
             sdB[tid] = 0.f;
             sH[tid] = 0.f;
@@ -1012,8 +1055,8 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                     dQ[qq][e] = (e < 2 ? gra : grb) * fX[qq][e];
                     dK[qq][e] = (e < 2 ? kca : kcb) * fY[qq][e];
                 }
-            frag_rows_add(gra * xa, grb * xb, sScr, sdG, tid, row0, wg, g, t);
-            frag_rows_add(-kca * ya, -kcb * yb, sScr, sH, tid, row0, wg, g, t);   // sH = -h
+            frag_rows_add(gra * sRQ[ra] * xa, grb * sRQ[rb] * xb, sScr, sdG, tid, row0, wg, g, t);
+            frag_rows_add(-kca * sRK[ra] * ya, -kcb * sRK[rb] * yb, sScr, sH, tid, row0, wg, g, t);   // sH = -h
         }
         if (tid < 32) {
             float th = sH[tid] + sH[tid + 32], tl = tid < kLoThreads / 32 ? sRed[tid] : 0.f;
@@ -1039,8 +1082,8 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                 }
             frag_rows_minus_cols(F, sScr, sdG, tid, row0, wg, mt, g, t);   // its barriers publish sX and sDW
         }
-        mma_prod<NTW, kC, false, false, false, kEx>(dQ, sX, kLCC, sK, L::LK, row0, nb0, g, t);   // dQ += E K
-        mma_prod<NTW, kC, true, false, false, kEx>(dK, sX, kLCC, sQ, L::LK, row0, nb0, g, t);    // dK += E^T Q
+        mma_prod_as<NTW, kC, false, kEx>(dQ, sX, kLCC, sRK, sK, L::LK, row0, nb0, g, t);   // dQ += E diag(rk) K
+        mma_prod_as<NTW, kC, true, kEx>(dK, sX, kLCC, sRQ, sQ, L::LK, row0, nb0, g, t);    // dK += E^T diag(rq) Q
         {   // R = T^T dW;  dK += diag(beta gamma) R;  dbeta_s += gamma_s R_s.k_s;  dG_s += beta_s gamma_s R_s.k_s
             float R[NTW][4];
             tile_zero(R);
@@ -1057,6 +1100,8 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
                     if (e < 2) rka += x; else rkb += x;
                     dK[qq][e] = fmaf(e < 2 ? bga : bgb, R[qq][e], dK[qq][e]);
                 }
+            rka *= sRK[ra];
+            rkb *= sRK[rb];
             frag_rows_add(gma * rka, gmb * rkb, sScr, sdB, tid, row0, wg, g, t);   // also ends the reads of E
             frag_rows_add(bga * rka, bgb * rkb, sScr, sdG, tid, row0, wg, g, t);
         }
@@ -1069,7 +1114,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int r = frow(row0, g, e), s = fcol(pb0 + qq, t, e);
-                    sX[r * kLCC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]), Tk[qq][e], fTv[qq][e]) : 0.f;
+                    sX[r * kLCC + s] = s <= r ? sBeta[s] * fmaf(__expf(sG[s]) * sRK[s], Tk[qq][e], fTv[qq][e]) : 0.f;
                 }
         }
         __syncthreads();
@@ -1109,7 +1154,7 @@ bwd_local_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* _
             frag_rows_add(ba, bb, sScr, sdB, tid, row0, wg, g, t);
             frag_rows_minus_cols(F, sScr, sdG, tid, row0, wg, mt, g, t);
         }
-        mma_prod<NTW, kC, false, false, false, kEx>(dK, sX, kLCC, sK, L::LK, row0, nb0, g, t);   // dK += (H + H^T) K
+        mma_prod_as<NTW, kC, false, kEx>(dK, sX, kLCC, sRK, sK, L::LK, row0, nb0, g, t);   // dK += (H + H^T) diag(rk) K
         if (tid < 32) {   // dg = suffix sums of dG: lane l holds tokens 2l, 2l + 1
             const float a = sdG[2 * tid], b = sdG[2 * tid + 1];
             float x = a + b;
@@ -1323,8 +1368,8 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     if ((e = set_smem(bwd_state_adj_kernel<TT, DK, DV>, S2::BYTES)) != cudaSuccess) return e;
     if ((e = set_smem(bwd_local_kernel<TT, DK, DV>, S4::BYTES)) != cudaSuccess) return e;
 
-    // With the front end (only for bf16, dk = dv = 128: the caller checks), the WY kernel and the chains take
-    // the raw inputs with the l2 scalars and the gates inside; the chunk-local kernel runs in fp32 below.
+    // With the front end (only for bf16, dk = dv = 128: the caller checks), every kernel takes the raw inputs
+    // with the l2 scalars and the gates inside (the WY kernel forms them and keeps the scalars per chunk).
     const bool normalize = (a.flags & GDN_NORMALIZE_QK) != 0;
     const float* A_log = (a.flags & GDN_RAW_GATES) ? a.A_log : nullptr;
     bwd_wy_kernel<TT, DK, DV><<<chunk_grid, kWyThreads, S1::BYTES, a.stream>>>(
@@ -1357,17 +1402,10 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
         return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark(3);
-    if (front_end) {   // fp32 on the front end's outputs, with the workspace the front-end kernels above filled
-        using S4f = LoSmem<DK, DV>;
-        if ((e = set_smem(bwd_local_kernel<float, DK, DV>, S4f::BYTES)) != cudaSuccess) return e;
-        bwd_local_kernel<float, DK, DV><<<chunk_grid, kLoThreads, S4f::BYTES, a.stream>>>(
-            a.lq, a.lk, a.lv, a.lbeta, a.ldout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk,
-            a.Hv, a.cu_seqlens, a.num_seqs, a.scale, true);
-    } else {
-        bwd_local_kernel<TT, DK, DV><<<chunk_grid, kLoThreads, S4::BYTES, a.stream>>>(
-            q, k, v, beta, dout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk, a.Hv,
-            a.cu_seqlens, a.num_seqs, a.scale, vec);
-    }
+    // with the front end, on the raw rows as well: the WY kernel's l2 scalars, beta from the raw b
+    bwd_local_kernel<TT, DK, DV><<<chunk_grid, kLoThreads, S4::BYTES, a.stream>>>(
+        q, k, v, beta, dout, ws, a.grad_q, a.grad_k, a.grad_v, a.grad_g, a.grad_beta, a.T, a.Hqk, a.Hv,
+        a.cu_seqlens, a.num_seqs, a.scale, vec, A_log, a.dt_bias, normalize);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark(4);
     return cudaSuccess;

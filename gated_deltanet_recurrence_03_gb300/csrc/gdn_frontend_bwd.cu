@@ -5,12 +5,11 @@
 //     g = -exp(A_log) softplus(a + dt_bias)                   da = dg (-exp(A_log)) sigmoid(a + dt_bias)
 //     beta = sigmoid(b)                                       db = dbeta beta (1 - beta)
 //     dA_log = sum over tokens of dg g,  d dt_bias = sum over tokens of da   (per value head)
-// Around the recurrence's own backward: a pre-pass writes the front end's outputs (normalised q, k,
-// the gates, and v, dout) as fp32 into the workspace, the recurrence's backward differentiates the
-// same fp32 values the forward kernels form in registers, and a post-pass maps the gradients back in
-// place.  For bf16 inputs with dk = dv = 128 the WY kernel and the two tcgen05 chains run on the raw
-// inputs with the front end inside (per-row l2 scalars, gates formed in fp32) and only the
-// chunk-local kernel reads the fp32 copies; other shapes run every kernel in fp32 on the copies.
+// The recurrence's backward differentiates the fp32 values the forward kernels form in registers, and
+// a post-pass maps its gradients back to the raw inputs in place.  For bf16 inputs with dk = dv = 128
+// its kernels run on the raw inputs with the front end inside (per-row l2 scalars, gates formed in
+// fp32); for other shapes a pre-pass first writes the front end's outputs (normalised q, k, the gates,
+// and v, dout) as fp32 into the workspace and every kernel runs in fp32 on those copies.
 #include <algorithm>
 
 #include "gdn_internal.cuh"
@@ -173,7 +172,9 @@ cudaError_t run_frontend_backward(const BackwardArgs& in, unsigned flags, const 
     cudaStream_t s = in.stream;
     const TT* q = static_cast<const TT*>(in.q);
     const TT* k = static_cast<const TT*>(in.k);
-    if (ttot > 0) {
+    const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool inside = sizeof(TT) == 2 && in.dk == 128 && in.dv == 128 && al16(in.q) && al16(in.k) && al16(in.dout);
+    if (ttot > 0 && !inside) {
         if (norm) {
             const unsigned blocks = (unsigned)((qrows + kRowThreads / 32 - 1) / (kRowThreads / 32));
             fe_l2_fwd_kernel<TT><<<blocks, kRowThreads, 0, s>>>(q, q32, qrows, in.dk);
@@ -191,15 +192,11 @@ cudaError_t run_frontend_backward(const BackwardArgs& in, unsigned flags, const 
         if (e != cudaSuccess) return e;
     }
     BackwardArgs a = in;
-    const auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     cudaError_t e;
-    if (sizeof(TT) == 2 && in.dk == 128 && in.dv == 128 && al16(in.q) && al16(in.k) && al16(in.dout)) {
-        // bf16 at the tensor-core shape: the WY kernel and the two tcgen05 chains on the raw inputs with the
-        // front end inside, the chunk-local kernel in fp32 on the copies above
+    if (inside) {   // bf16 at the tensor-core shape: every kernel on the raw inputs with the front end inside
         a.flags = flags;
         a.A_log = A_log;
         a.dt_bias = dt_bias;
-        a.lq = q32; a.lk = k32; a.lv = v32; a.lbeta = b32; a.ldout = do32;
         e = launch_backward(a);
     } else {   // every kernel in fp32 on the copies
         a.q = q32; a.k = k32; a.v = v32; a.dout = do32; a.g = g32; a.beta = b32;

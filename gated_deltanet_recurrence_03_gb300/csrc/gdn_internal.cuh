@@ -111,17 +111,12 @@ struct BackwardArgs {
     void** events;              // optional: events[i] recorded after kernel i (1..4)
     int num_events;
     // The fused front end (GDN_NORMALIZE_QK, GDN_RAW_GATES; 0 = none): g and beta then hold the raw a, b.
-    // bf16 inputs with dk = dv = 128 then run the WY kernel and the tcgen05 chains on the raw inputs with
-    // the front end inside (per-row l2 scalars, gates formed in fp32) and the chunk-local kernel in fp32
-    // on lq, lk (normalised q, k), lv, lbeta (formed beta) and ldout, fp32 copies the caller provides.
+    // Only for bf16 inputs with dk = dv = 128: every kernel then runs on the raw inputs with the front
+    // end inside (per-row l2 scalars, which the WY kernel forms and keeps per chunk, and the gates formed
+    // in fp32).
     unsigned flags;
     const float* A_log;
     const float* dt_bias;
-    const float* lq;
-    const float* lk;
-    const float* lv;
-    const float* lbeta;
-    const float* ldout;
 };
 
 // Workspace of the backward pass: per (chunk slot, value head) fp32 arrays T, P (C x C), W (C x dk),

@@ -281,10 +281,10 @@ gdn_status_t gdn_causal_conv1d_bwd(const void* x, long long x_stride, const floa
  * a, b passed as g, beta (da = dg (-exp(A_log)) sigmoid(a + dt_bias), db = dbeta beta (1 - beta)) --
  * and, when opts->grad_A_log / grad_dt_bias are not NULL, [Hv] fp32 sums over all tokens of dg g and
  * of da (overwritten, deterministic order).  With either flag the inputs' front-end outputs are formed
- * in fp32 in the workspace (gdn_recurrent_bwd_workspace_size grows accordingly).  For bf16 inputs with
- * dk = dv = 128 the WY kernel and both chunk chains read the raw inputs and form the per-row l2 scalars
- * and the gates in-kernel in fp32, and only the chunk-local kernel reads the fp32 copies; otherwise the
- * whole backward runs on the copies in fp32 (the split-tf32 kernels).  It is computed through the chunked form
+ * in fp32: for bf16 inputs with dk = dv = 128 (16-byte aligned q, k, grad_out) inside the kernels,
+ * which read the raw inputs and form the per-row l2 scalars and the gates in fp32; otherwise as fp32
+ * copies in the workspace (gdn_recurrent_bwd_workspace_size grows accordingly), on which the whole
+ * backward runs in fp32 (the split-tf32 kernels).  It is computed through the chunked form
  * of the loop (64-token chunks): the workspace (256-byte aligned, gdn_recurrent_bwd_workspace_size
  * bytes) holds per (chunk, value head) the chunk's UT inverse, decay-masked Q K^T, W, U, decay
  * prefix sums, the state at the chunk start and its adjoint, and dU, all fp32; GDN_ERR_WORKSPACE if
