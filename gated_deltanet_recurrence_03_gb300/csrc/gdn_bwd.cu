@@ -239,21 +239,6 @@ __device__ __forceinline__ void ld_ws(float* __restrict__ dst, int ld, const flo
     ld_in<float, ROWS, WIDTH, NT>(dst, ld, src, stride, ROWS, tid, true);
 }
 
-// l2 normalisation of q and k kept as per-row scalars: r[i] = 1 / sqrt(|x_i|^2 + 1e-6) for the ROWS rows
-// of a [ROWS][WIDTH] tile in shared memory, one warp per row.  The tile itself stays as loaded (bf16
-// rows stay exact in tf32); each product applies the scalars to its other operand or its output.
-template <int ROWS, int WIDTH, int NWARPS>
-__device__ __forceinline__ void row_rnorm(const float* __restrict__ x, int ld, float* __restrict__ r, int warp,
-                                          int lane) {
-    for (int i = warp; i < ROWS; i += NWARPS) {
-        float s = 0.f;
-        for (int c = lane; c < WIDTH; c += 32) s = fmaf(x[i * ld + c], x[i * ld + c], s);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) r[i] = rsqrtf(s + 1e-6f);
-    }
-}
-
 // Workspace slot of chunk 0 of sequence i.
 __device__ __forceinline__ long long slot_base(const int32_t* cu, int i, int T) {
     long long t0, t1;
@@ -307,30 +292,48 @@ struct ChainTiles {
 // ---------------------------------------------------------------- kernel 1: WY factors per chunk
 constexpr int kWyThreads = 256;
 
+// Shared memory of the WY kernel: about 106 KB at dk = dv = 128, so that two CTAs fit on an SM.  Q and
+// V are staged half their columns at a time; Q K^T lives in the L buffer (P of every value head is
+// formed before the first L).
 template <int DK, int DV>
 struct WySmem {
-    static constexpr int LK = DK + 4, LQV = (DK > DV ? DK : DV) + 4;   // = 4 mod 32
-    static constexpr int K_ = 0, QV_ = K_ + kC * LK, KK_ = QV_ + kC * LQV, QK_ = KK_ + kC * kLCC,
-                         L_ = QK_ + kC * kLCC, T_ = L_ + kC * kLCC, Y_ = T_ + kC * kLCC, VEC_ = Y_ + 3 * 256;
+    static constexpr int DH = (DK > DV ? DK : DV) / 2;   // staged columns of Q or V
+    static constexpr int LK = DK + 4, LQV = DH + 4;
+    static constexpr int K_ = 0, QV_ = K_ + kC * LK, KK_ = QV_ + kC * LQV, L_ = KK_ + kC * kLCC,
+                         T_ = L_ + kC * kLCC, Y_ = T_ + kC * kLCC, VEC_ = Y_ + 3 * 256;
     static constexpr int FLOATS = VEC_ + 6 * kC;
     static constexpr size_t BYTES = (size_t)FLOATS * 4;
 };
 
+// sum over the WIDTH columns of x_i^2 added to r[i] (one warp per row).
+template <int ROWS, int WIDTH, int NWARPS>
+__device__ __forceinline__ void row_sumsq_add(const float* __restrict__ x, int ld, float* __restrict__ r, int warp,
+                                              int lane) {
+    for (int i = warp; i < ROWS; i += NWARPS) {
+        float s = 0.f;
+        for (int c = lane; c < WIDTH; c += 32) s = fmaf(x[i * ld + c], x[i * ld + c], s);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) r[i] += s;
+    }
+}
+
 // With A_log non-null, g and beta hold the raw projections a, b and the gates are formed on load;
 // with normalize, q and k are l2-normalised through per-row scalars (the prefill's front end).
 template <typename TT, int DK, int DV>
-__global__ void __launch_bounds__(kWyThreads)
+__global__ void __launch_bounds__(kWyThreads, 2)
 bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __restrict__ v, const TT* __restrict__ g,
               const TT* __restrict__ beta, Ws ws, int T_len, int Hqk, int Hv, const int32_t* __restrict__ cu,
               int nseq, float scale, bool vec, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
               bool normalize) {
     using L = WySmem<DK, DV>;
     using D = WsDims<DK, DV>;
+    constexpr int QH = DK / 2, VH = DV / 2;   // columns of Q and of V per staged half
     extern __shared__ __align__(16) float sm[];
     float* sK = sm + L::K_;
     float* sQV = sm + L::QV_;
     float* sKK = sm + L::KK_;
-    float* sQK = sm + L::QK_;
+    float* sQK = sm + L::L_;   // Q K^T until P of every value head is out, then L
     float* sL = sm + L::L_;
     float* sT = sm + L::T_;
     float* sY = sm + L::Y_;   // off-diagonal block sums of the solve: up to 3 blocks of 16 x 16
@@ -348,33 +351,43 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
     if (!slot_chunk(cu, nseq, T_len, slot, seq, tok0, n)) return;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, lg = lane / 4, lt = lane % 4;   // fragment (g, t)
     constexpr bool kEx = sizeof(TT) == 2;   // bf16 K, Q, V are exact in tf32
+    const TT* qrow = q + (tok0 * Hqk + hk) * DK;
 
     ld_in<TT, kC, DK, kWyThreads>(sK, L::LK, k + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
-    ld_in<TT, kC, DK, kWyThreads>(sQV, L::LQV, q + (tok0 * Hqk + hk) * DK, (size_t)Hqk * DK, n, tid, vec);
+    ld_in<TT, kC, QH, kWyThreads>(sQV, L::LQV, qrow, (size_t)Hqk * DK, n, tid, vec);
+    if (tid < kC) {
+        sRK[tid] = normalize ? 0.f : 1.f;
+        sRQ[tid] = normalize ? 0.f : 1.f;
+    }
     __syncthreads();
+    // Gram matrices K K^T and Q K^T on tensor cores (both operands exact in tf32 for bf16 inputs); Q K^T
+    // over the two column halves of Q in turn
+    using TG = ChainTiles<kC, kC>;
+    float kk[TG::NT][4], qk[TG::NT][4];
+    tile_zero(kk);
+    tile_zero(qk);
+    const int gm = 16 * (warp % TG::MT), gn = (warp / TG::MT) * TG::NT;
     if (normalize) {
-        row_rnorm<kC, DK, kWyThreads / 32>(sK, L::LK, sRK, warp, lane);
-        row_rnorm<kC, DK, kWyThreads / 32>(sQV, L::LQV, sRQ, warp, lane);
-    } else if (tid < kC) {
-        sRK[tid] = 1.f;
-        sRQ[tid] = 1.f;
+        row_sumsq_add<kC, DK, kWyThreads / 32>(sK, L::LK, sRK, warp, lane);
+        row_sumsq_add<kC, QH, kWyThreads / 32>(sQV, L::LQV, sRQ, warp, lane);
     }
-    {   // Gram matrices K K^T and Q K^T on tensor cores (both operands exact in tf32 for bf16 inputs)
-        using TG = ChainTiles<kC, kC>;
-        float kk[TG::NT][4], qk[TG::NT][4];
-        tile_zero(kk);
-        tile_zero(qk);
-        const int gm = 16 * (warp % TG::MT), gn = (warp / TG::MT) * TG::NT;
-        mma_prod<TG::NT, DK, false, true, kEx, kEx>(kk, sK, L::LK, sK, L::LK, gm, gn, lg, lt);
-        mma_prod<TG::NT, DK, false, true, kEx, kEx>(qk, sQV, L::LQV, sK, L::LK, gm, gn, lg, lt);
-        store_frag<TG::NT>(sKK, kLCC, kk, gm, gn, lg, lt, 1.f);
-        store_frag<TG::NT>(sQK, kLCC, qk, gm, gn, lg, lt, 1.f);
-    }
+    mma_prod<TG::NT, DK, false, true, kEx, kEx>(kk, sK, L::LK, sK, L::LK, gm, gn, lg, lt);
+    mma_prod<TG::NT, QH, false, true, kEx, kEx>(qk, sQV, L::LQV, sK, L::LK, gm, gn, lg, lt);
     __syncthreads();
+    ld_in<TT, kC, QH, kWyThreads>(sQV, L::LQV, qrow + QH, (size_t)Hqk * DK, n, tid, vec);
+    __syncthreads();
+    if (normalize) row_sumsq_add<kC, QH, kWyThreads / 32>(sQV, L::LQV, sRQ, warp, lane);
+    mma_prod<TG::NT, QH, false, true, kEx, kEx>(qk, sQV, L::LQV, sK + QH, L::LK, gm, gn, lg, lt);
+    store_frag<TG::NT>(sKK, kLCC, kk, gm, gn, lg, lt, 1.f);
+    store_frag<TG::NT>(sQK, kLCC, qk, gm, gn, lg, lt, 1.f);
+    __syncthreads();
+    if (normalize && tid < kC) {
+        sRK[tid] = rsqrtf(sRK[tid] + 1e-6f);
+        sRQ[tid] = rsqrtf(sRQ[tid] + 1e-6f);
+    }
 
-    for (int j = 0; j < G; ++j) {
-        const int h = hk * G + j;
-        const size_t wi = (size_t)slot * Hv + h;
+    // The gates of value head h and G = their inclusive prefix sum (lane l of warp 0: tokens 2l, 2l + 1).
+    const auto head_gates = [&](int h) {
         if (tid < kC) {
             const bool ok = tid < n;
             float gt = ok ? to_f32(g[(tok0 + tid) * Hv + h]) : 0.f;
@@ -383,10 +396,8 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
             sGraw[tid] = gt;
             sBeta[tid] = bt;
         }
-        // V of this value head (Q is no longer needed: its Gram is in sQK)
-        ld_in<TT, kC, DV, kWyThreads>(sQV, L::LQV, v + (tok0 * Hv + h) * DV, (size_t)Hv * DV, n, tid, vec);
         __syncthreads();
-        if (tid < 32) {   // G = inclusive prefix sum of g: lane l holds tokens 2l, 2l + 1
+        if (tid < 32) {
             const float a = sGraw[2 * tid], b = sGraw[2 * tid + 1];
             float x = a + b;
 #pragma unroll
@@ -398,20 +409,37 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
             sG[2 * tid + 1] = x;
         }
         __syncthreads();
+    };
+
+    // P = scale D o QK^T (s <= r) of every value head to the workspace, with G and the l2 scalars
+    for (int j = 0; j < G; ++j) {
+        const int h = hk * G + j;
+        const size_t wi = (size_t)slot * Hv + h;
+        head_gates(h);
         if (tid < kC) {
-            sBG[tid] = sBeta[tid] * __expf(sG[tid]) * sRK[tid];   // W = T diag(beta gamma) (diag(rk) K)
             ws.G[wi * D::G + tid] = sG[tid];
-            if (normalize) {   // for the chain and the output kernel
+            if (normalize) {   // for the chains, the output kernel and the chunk-local kernel
                 ws.R[wi * D::R + tid] = sRK[tid];
                 ws.R[wi * D::R + kC + tid] = sRQ[tid];
             }
         }
-        // P = scale D o QK^T (s <= r) to the workspace; L = diag(beta) (D o KK^T) strictly below the diagonal
         for (int idx = tid; idx < kC * kC; idx += kWyThreads) {
             const int r = idx / kC, s = idx % kC;
             const float d = s <= r ? __expf(sG[r] - sG[s]) : 0.f;
             ws.P[wi * D::P + idx] = scale * d * (sRQ[r] * sRK[s]) * sQK[r * kLCC + s];
-            sL[r * kLCC + s] = s < r ? sBeta[r] * d * (sRK[r] * sRK[s]) * sKK[r * kLCC + s] : 0.f;
+        }
+        __syncthreads();   // sG of the next head; after the last, the Q K^T buffer is free for L
+    }
+
+    for (int j = 0; j < G; ++j) {
+        const int h = hk * G + j;
+        const size_t wi = (size_t)slot * Hv + h;
+        head_gates(h);
+        if (tid < kC) sBG[tid] = sBeta[tid] * __expf(sG[tid]) * sRK[tid];   // W = T diag(beta gamma) (diag(rk) K)
+        // L = diag(beta) (D o KK^T) strictly below the diagonal
+        for (int idx = tid; idx < kC * kC; idx += kWyThreads) {
+            const int r = idx / kC, s = idx % kC;
+            sL[r * kLCC + s] = s < r ? sBeta[r] * __expf(sG[r] - sG[s]) * (sRK[r] * sRK[s]) * sKK[r * kLCC + s] : 0.f;
         }
         __syncthreads();
         {   // T = (I + L)^{-1} in 16 x 16 blocks: each diagonal block by forward substitution (one thread
@@ -424,7 +452,7 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
                 for (int r = 0; r < 16; ++r) {
                     float acc = r == c ? 1.f : 0.f;
 #pragma unroll
-                    for (int q = 0; q < r; ++q) acc = fmaf(-sL[(o + r) * kLCC + o + q], x[q], acc);
+                    for (int qq = 0; qq < r; ++qq) acc = fmaf(-sL[(o + r) * kLCC + o + qq], x[qq], acc);
                     x[r] = acc;
                     sT[(o + r) * kLCC + o + c] = acc;
                 }
@@ -443,8 +471,8 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
                     float acc = 0.f;
                     for (int bl = bj; bl < bi; ++bl)
 #pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            acc = fmaf(sL[(16 * bi + r) * kLCC + 16 * bl + q], sT[(16 * bl + q) * kLCC + 16 * bj + c], acc);
+                        for (int qq = 0; qq < 16; ++qq)
+                            acc = fmaf(sL[(16 * bi + r) * kLCC + 16 * bl + qq], sT[(16 * bl + qq) * kLCC + 16 * bj + c], acc);
                     sY[idx] = acc;
                 }
                 __syncthreads();
@@ -452,8 +480,8 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
                     const int bj = idx / 256, e = idx % 256, r = e / 16, c = e % 16, bi = bj + d;
                     float acc = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        acc = fmaf(sT[(16 * bi + r) * kLCC + 16 * bi + q], sY[bj * 256 + q * 16 + c], acc);
+                    for (int qq = 0; qq < 16; ++qq)
+                        acc = fmaf(sT[(16 * bi + r) * kLCC + 16 * bi + qq], sY[bj * 256 + qq * 16 + c], acc);
                     sT[(16 * bi + r) * kLCC + 16 * bj + c] = -acc;
                 }
                 __syncthreads();
@@ -482,8 +510,11 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
                 for (int e = 0; e < 4; ++e)
                     ws.W[wi * D::W + (size_t)frow(wm, lg, e) * DK + fcol(wn + qq, lt, e)] = acc[qq][e];
         }
-        {   // U~ = T diag(beta) V on tensor cores (V exact for bf16 inputs)
-            using TV = ChainTiles<kC, DV>;
+        // U~ = T diag(beta) V on tensor cores (V exact for bf16 inputs), over the two column halves of V
+        for (int half = 0; half < 2; ++half) {
+            ld_in<TT, kC, VH, kWyThreads>(sQV, L::LQV, v + (tok0 * Hv + h) * DV + half * VH, (size_t)Hv * DV, n, tid, vec);
+            __syncthreads();
+            using TV = ChainTiles<kC, VH>;
             float acc[TV::NT][4];
             tile_zero(acc);
             const int vm = 16 * (warp % TV::MT), vn = (warp / TV::MT) * TV::NT;
@@ -502,9 +533,9 @@ bwd_wy_kernel(const TT* __restrict__ q, const TT* __restrict__ k, const TT* __re
             for (int qq = 0; qq < TV::NT; ++qq)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    ws.U[wi * D::U + (size_t)frow(vm, lg, e) * DV + fcol(vn + qq, lt, e)] = acc[qq][e];
+                    ws.U[wi * D::U + (size_t)frow(vm, lg, e) * DV + half * VH + fcol(vn + qq, lt, e)] = acc[qq][e];
+            __syncthreads();   // sQV is refilled next (the other half of V, or the next head's V)
         }
-        __syncthreads();
     }
 }
 
@@ -1284,7 +1315,7 @@ cudaError_t launch_fwd_typed(const PrefillArgs& a, const BwdLayout& Lw) {
     using S2 = StSmem<DK, DV>;
     using S3 = OutSmem<DK, DV>;
     cudaError_t e;
-    if ((e = set_smem(bwd_wy_kernel<TT, DK, DV>, S1::BYTES)) != cudaSuccess) return e;
+    if ((e = set_smem2(bwd_wy_kernel<TT, DK, DV>, S1::BYTES)) != cudaSuccess) return e;
     if ((e = set_smem(bwd_state_fwd_kernel<TT, DK, DV>, S2::BYTES)) != cudaSuccess) return e;
     if ((e = set_smem(fwd_out_kernel<TT, DK, DV>, S3::BYTES)) != cudaSuccess) return e;
     const dim3 chunk_grid((unsigned)Lw.slots, (unsigned)a.Hqk);
@@ -1328,6 +1359,12 @@ template <typename F>
 cudaError_t set_smem(F* kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
+// The same, with the largest shared-memory carveout: for kernels that run two CTAs per SM.
+template <typename F>
+cudaError_t set_smem2(F* kernel, size_t bytes) {
+    const cudaError_t e = set_smem(kernel, bytes);
+    return e == cudaSuccess ? cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) : e;
+}
 
 template <typename TT, int DK, int DV>
 cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
@@ -1363,7 +1400,7 @@ cudaError_t launch_typed(const BackwardArgs& a, const BwdLayout& Lw) {
     using S4 = LoSmem<DK, DV>;
     const dim3 chunk_grid((unsigned)Lw.slots, (unsigned)a.Hqk);
     const unsigned nst = (unsigned)((long long)a.num_seqs * a.Hv * NSL);
-    if ((e = set_smem(bwd_wy_kernel<TT, DK, DV>, S1::BYTES)) != cudaSuccess) return e;
+    if ((e = set_smem2(bwd_wy_kernel<TT, DK, DV>, S1::BYTES)) != cudaSuccess) return e;
     if ((e = set_smem(bwd_state_fwd_kernel<TT, DK, DV>, S2::BYTES)) != cudaSuccess) return e;
     if ((e = set_smem(bwd_state_adj_kernel<TT, DK, DV>, S2::BYTES)) != cudaSuccess) return e;
     if ((e = set_smem(bwd_local_kernel<TT, DK, DV>, S4::BYTES)) != cudaSuccess) return e;
