@@ -128,6 +128,49 @@ fe_gates_bwd_kernel(const TT* __restrict__ a, const TT* __restrict__ b, const fl
     }
 }
 
+// The same over all value heads at once (Hv <= 256): thread (r, h) of a block of Hv x R threads takes
+// tokens b R + r, b R + r + NB R, ... of head h (coalesced rows of Hv gates), and each block writes its
+// per-head sums of dg g and da, added over its R threads in a fixed order, to pa[b][h], pd[b][h];
+// column_sum_kernel then adds the blocks in a fixed order.
+constexpr int kGateRows = 256;
+template <typename TT>
+__global__ void __launch_bounds__(kGateRows)
+fe_gates_bwd_rows_kernel(const TT* __restrict__ a, const TT* __restrict__ b, const float* __restrict__ A_log,
+                         const float* __restrict__ dt_bias, float* __restrict__ dg, float* __restrict__ dbeta,
+                         float* __restrict__ pa, float* __restrict__ pd, long long tokens, int Hv, int R) {
+    __shared__ float red[2][kGateRows];
+    const int tid = threadIdx.x, h = tid % Hv, r = tid / Hv;
+    const long long NB = gridDim.x;
+    float s_ag = 0.f, s_dt = 0.f;
+    if (r < R) {
+        const float al = A_log[h], dt = dt_bias[h], ea = __expf(al);
+        for (long long t = (long long)blockIdx.x * R + r; t < tokens; t += NB * R) {
+            const long long i = t * Hv + h;
+            const float av = to_f32(a[i]), bv = to_f32(b[i]);
+            float g, beta;
+            gates_from_raw(av, bv, al, dt, g, beta);
+            const float sig = 1.f / (1.f + __expf(-(av + dt)));
+            const float dgi = dg[i], dai = -dgi * ea * sig;
+            dg[i] = dai;
+            dbeta[i] = dbeta[i] * beta * (1.f - beta);
+            s_ag = fmaf(dgi, g, s_ag);
+            s_dt += dai;
+        }
+    }
+    red[0][tid] = s_ag;
+    red[1][tid] = s_dt;
+    __syncthreads();
+    if (tid < Hv) {
+        float x = 0.f, y = 0.f;
+        for (int q = 0; q < R; ++q) {
+            x += red[0][q * Hv + tid];
+            y += red[1][q * Hv + tid];
+        }
+        pa[(size_t)blockIdx.x * Hv + tid] = x;
+        pd[(size_t)blockIdx.x * Hv + tid] = y;
+    }
+}
+
 unsigned grid_for(long long n, int threads) {
     const long long b = (n + threads - 1) / threads;
     return (unsigned)std::min<long long>(std::max<long long>(b, 1), 1 << 20);
@@ -210,10 +253,23 @@ cudaError_t run_frontend_backward(const BackwardArgs& in, unsigned flags, const 
         fe_l2_bwd_kernel<TT><<<blocks, kRowThreads, 0, s>>>(q, in.grad_q, qrows, in.dk);
         fe_l2_bwd_kernel<TT><<<blocks, kRowThreads, 0, s>>>(k, in.grad_k, qrows, in.dk);
     }
-    if (raw)   // also for no tokens: the parameter gradients are then zero
+    if (raw && in.Hv <= kGateRows) {   // also for no tokens: the parameter gradients are then zero
+        // the per-block sums go to the gate copies' region (free once the recurrence's backward has run;
+        // each of its two arrays holds ttot x Hv floats, at least NB x Hv)
+        const int R = kGateRows / in.Hv;
+        const long long NB = std::min<long long>((ttot + R - 1) / R, 1184);
+        if (NB > 0)
+            fe_gates_bwd_rows_kernel<TT><<<(unsigned)NB, in.Hv * R, 0, s>>>(
+                static_cast<const TT*>(in.g), static_cast<const TT*>(in.beta), A_log, dt_bias, in.grad_g,
+                in.grad_beta, g32, b32, ttot, in.Hv, R);
+        const unsigned cb = (unsigned)((in.Hv + 31) / 32);
+        if (grad_A_log) column_sum_kernel<<<cb, kColSumThreads, 0, s>>>(g32, NB, in.Hv, grad_A_log);
+        if (grad_dt_bias) column_sum_kernel<<<cb, kColSumThreads, 0, s>>>(b32, NB, in.Hv, grad_dt_bias);
+    } else if (raw) {
         fe_gates_bwd_kernel<TT><<<in.Hv, kGateThreads, 0, s>>>(
             static_cast<const TT*>(in.g), static_cast<const TT*>(in.beta), A_log, dt_bias, in.grad_g, in.grad_beta,
             grad_A_log, grad_dt_bias, ttot, in.Hv);
+    }
     return cudaGetLastError();
 }
 
