@@ -450,10 +450,12 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             if (hg == 1) {   // own lane: [0 | P_1 row] (the zero half is written by group 0)
                 tmem_st32(tl + T_AP + 32, w);
-            } else {         // P_0 row r belongs to lane r: hand it over through shared memory
+            } else {         // P_0 row r belongs to lane r: hand it over through shared memory, 16-byte
+                             // chunk c of row r at chunk c ^ (r % 8) (eight consecutive rows: all banks)
                 uint4* dst = reinterpret_cast<uint4*>(sm + P_HANDOFF + r * 128);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                for (int c = 0; c < 8; ++c)
+                    dst[c ^ (r & 7)] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) w[e] = 0u;
                 tmem_st32(tl + T_AP, w);
@@ -467,7 +469,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint4* src = reinterpret_cast<const uint4*>(sm + P_HANDOFF + R * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const uint4 x = src[c];
+                const uint4 x = src[c ^ (R & 7)];
                 w[4 * c] = x.x; w[4 * c + 1] = x.y; w[4 * c + 2] = x.z; w[4 * c + 3] = x.w;
             }
         } else {
