@@ -65,6 +65,21 @@ def test_front_end_backward_packed_small_heads():
     run(w, True, True, seqlens=lens)
 
 
+def test_front_end_backward_packed_tensor_core_shape():
+    """Packed sequences (an empty one, a one-token one, one across three chunks) at dk = dv = 128 in bf16:
+    every kernel on the raw rows, the chunk-local kernel reading the per-slot l2 scalars back."""
+    lens = (70, 0, 1, 130)
+    w = gi.Workload("fe_bwd_packed128", "prefill", "bf16", B=1, T=sum(lens), Hqk=2, Hv=4, dk=128, dv=128,
+                    s0_std=0.1, seqlens=lens, seed=45)
+    run(w, True, True, seqlens=lens)
+
+
+def test_front_end_backward_many_value_heads():
+    """More than 256 value heads: the per-head parameter sums take the one-block-per-head path."""
+    w = gi.Workload("fe_bwd_wide", "prefill", "f32", B=1, T=24, Hqk=1, Hv=264, dk=32, dv=32, s0_std=0.1, seed=46)
+    run(w, False, True)
+
+
 def test_front_end_backward_of_unit_rows_matches_the_plain_backward():
     """Rows already of unit length: the l2 norm changes them by eps only, so the front-end path's q / k
     gradients (projected onto the tangent space) and the plain path's differ by the radial component,

@@ -109,6 +109,29 @@ def test_deterministic():
     np.testing.assert_array_equal(a[1], b[1])
 
 
+def test_chain_launch_order_does_not_change_the_bits():
+    """Without an event between them the chain kernel follows the prep by programmatic dependent launch
+    (its set-up overlapping the prep's last CTAs, its workspace reads after the prep grid completed);
+    with one it starts after the prep.  Both orders give the same bits, packed sequences included."""
+    lens = (300, 0, 1, 129, 64)
+    w = gi.scaled(gi.WORKLOADS["prefill_gqa_8k"], B=1, T=sum(lens), Hqk=2, Hv=4, seqlens=lens)
+    x = gi.make_prefill_inputs(w)
+    dt = torch.bfloat16
+    q, k, v, g, beta = (up(x[n], dt) for n in ("q", "k", "v", "g", "beta"))
+    S0 = up(x["S0"], torch.float32)
+    cu = torch.from_numpy(np.asarray(x["cu_seqlens"], dtype=np.int32)).cuda()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for e in ev:
+        e.record()
+    o1, s1 = gdn.gdn_chunk_fwd(q, k, v, g, beta, S0, cu_seqlens=cu)
+    o2, s2 = gdn.gdn_chunk_fwd(q, k, v, g, beta, S0, cu_seqlens=cu, events=[e.cuda_event for e in ev])
+    torch.cuda.synchronize()
+    gdn.check_device_status()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    assert rel_err(orc.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], S0=x["S0"],
+                               cu_seqlens=x["cu_seqlens"])[0], o1.float().cpu().numpy()) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("name,dtype,d", [("tc", "bf16", 128), ("split_tf32", "f32", 32)])
 def test_chunk_option_gives_the_same_result(name, dtype, d):
     """opts.chunk 16, 32 and 64 run the same 64-token blocking: bit-identical results, each within
