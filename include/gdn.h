@@ -117,7 +117,9 @@ void gdn_opts_init(gdn_opts_t* opts);
  * S_final (zeros when S0 is NULL).  Three kernel families, chosen in this order (opts->chunk does
  * not take part in the choice: the two chunked families block in 64-token chunks for every value):
  *   - bf16 inputs with dk = dv = 128: the tcgen05 tensor-core path; it needs the workspace
- *     (GDN_ERR_WORKSPACE if missing or too small);
+ *     (GDN_ERR_WORKSPACE if missing or too small).  Its two kernels run back to back, the second
+ *     launched with programmatic stream serialisation so that its set-up overlaps the first one's
+ *     last CTAs; an event in opts->events[1] (recorded between them) makes it a plain launch;
  *   - other inputs, when the workspace is at least gdn_chunk_fwd_workspace_size() bytes (256-byte
  *     aligned): the same chunk algebra on split-tf32 tensor-core MMAs in fp32 accuracy,
  *     GDN_NORMALIZE_QK and GDN_RAW_GATES included;
