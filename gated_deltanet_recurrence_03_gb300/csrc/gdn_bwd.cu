@@ -14,8 +14,9 @@
 // and the chunk-local gradients follow by the chain rule through T (dT -> -T^T dT T^T), the decay
 // ratios (d exp(G_r - G_s) adds to G_r and subtracts from G_s) and dg = reverse cumulative sum of dG.
 //
-// Four kernels, all in fp32 accuracy: the WY kernel on CUDA cores, the chains and the chunk-local
-// kernel on tf32 tensor cores with each fp32 operand split into two tf32 parts:
+// Four kernels, all in fp32 accuracy, their products on tf32 tensor cores with each fp32 operand split
+// into two tf32 parts (the WY kernel's triangular solve on CUDA cores; for bf16 inputs with
+// dk = dv = 128 the two chains run instead as the tcgen05 kernels of gdn_bwd_tc.cu):
 //   bwd_wy_kernel         per (chunk, query/key head): T, W, U~, P and G of each of its value heads
 //   bwd_state_fwd_kernel  per (sequence, value head, column slice): chunk-start states S, and U
 //   bwd_state_adj_kernel  per (sequence, value head, column slice), chunks in reverse: lam, dU, dS0
