@@ -2,6 +2,7 @@
 import math
 
 import numpy as np
+import pytest
 
 from oracle import gates
 
@@ -98,3 +99,23 @@ def test_gated_rmsnorm_backward_is_scale_free_in_o():
     inv = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True))
     slip = inv * dy * w * gates.silu(z)
     assert np.max(np.abs(np.sum(slip * o, axis=-1))) > 1e-3
+
+
+@pytest.mark.parametrize("slip", ["sigmoid_for_silu_grad", "no_inv_on_do", "dz_without_weight", "dw_without_gate"])
+def test_gated_rmsnorm_backward_pin_catches_planted_slips(slip):
+    """Each plausible slip in the gate's chain rule, written into a copy of its formulas, is caught by
+    the finite-difference pin above (some gradient off by far more than its tolerance)."""
+    rng = np.random.default_rng(5)
+    o, z, w, dy = rng.normal(size=(4, 8)), rng.normal(size=(4, 8)), rng.normal(1.0, 0.2, size=8), rng.normal(size=(4, 8))
+    eps = 1e-6
+    inv = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    oh, s = o * inv, gates.silu(z)
+    gy = dy * w * s
+    do = (1.0 if slip == "no_inv_on_do" else inv) * (gy - oh * np.mean(gy * oh, axis=-1, keepdims=True))
+    dz = dy * oh * (1.0 if slip == "dz_without_weight" else w) * (
+        gates.sigmoid(z) if slip == "sigmoid_for_silu_grad" else gates.silu_grad(z))
+    dw = np.sum(dy * oh * (1.0 if slip == "dw_without_gate" else s), axis=0)
+    loss = lambda oo=o, zz=z, ww=w: float(np.sum(gates.gated_rmsnorm(oo, zz, ww, eps) * dy))
+    worst = max(np.max(np.abs(do - _fd(lambda t: loss(oo=t), o))), np.max(np.abs(dz - _fd(lambda t: loss(zz=t), z))),
+                np.max(np.abs(dw - _fd(lambda t: loss(ww=t), w))))
+    assert worst > 1e-3, f"{slip} went unnoticed ({worst:.2e})"
